@@ -1,0 +1,310 @@
+"""Python face of the CPU oracle (``oracle.cpp``): ctypes marshalling only.
+
+TEST INFRASTRUCTURE ONLY.  The oracle is the plain double-precision statement of the DiT forward;
+only the tests, the package smoke check and the bench's CPU-baseline leg may import it.  It shares
+no code with the CUDA library and never imports it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib = None
+_lock = threading.Lock()
+
+_c_dp = ctypes.POINTER(ctypes.c_double)
+_c_fp = ctypes.POINTER(ctypes.c_float)
+
+
+class OrcConfig(ctypes.Structure):
+    _fields_ = [("n_blocks", ctypes.c_int), ("hidden", ctypes.c_int), ("n_heads", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("ffn_hidden", ctypes.c_int), ("norm", ctypes.c_int),
+                ("norm_eps", ctypes.c_double), ("adaln", ctypes.c_int), ("n_mod", ctypes.c_int),
+                ("t_dim", ctypes.c_int), ("rope_axes", ctypes.c_int), ("rope_dims", ctypes.c_int * 3),
+                ("rotary_dim", ctypes.c_int), ("rope_base", ctypes.c_double), ("io_channels", ctypes.c_int)]
+
+
+_BLOCK_NAMES = ["w_qkv", "b_qkv", "w_o", "b_o", "w_in", "b_in", "w_down", "b_down", "w_ada", "b_ada",
+                "ln1_g", "ln1_b", "ln2_g", "ln2_b"]
+_GLOB_NAMES = ["w_ada_final", "b_ada_final", "lnf_g", "lnf_b", "w_pre", "b_pre", "w_post", "b_post"]
+
+
+class OrcBlock(ctypes.Structure):
+    _fields_ = [(n, _c_fp) for n in _BLOCK_NAMES]
+
+
+class OrcWeights(ctypes.Structure):
+    _fields_ = [("blocks", ctypes.POINTER(OrcBlock))] + [(n, _c_fp) for n in _GLOB_NAMES]
+
+
+def build(force: bool = False) -> str:
+    """Compile ``liboracle.so`` beside its source (g++, OpenMP, no FMA contraction, no fast-math)."""
+    src = os.path.join(_HERE, "oracle.cpp")
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(src):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["g++", "-O2", "-std=c++17", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
+                               "-fPIC", "-shared", src, "-o", tmp])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = ctypes.CDLL(build())
+            _lib.orc_forward.restype = ctypes.c_int
+            _lib.orc_check_layout.restype = ctypes.c_int
+            _lib.orc_count_q_tiles.restype = ctypes.c_int
+            _lib.orc_get_threads.restype = ctypes.c_int
+    return _lib
+
+
+def set_threads(n: int) -> None:
+    lib().orc_set_threads(int(n))
+
+
+def _d(a):
+    return a.ctypes.data_as(_c_dp)
+
+
+def _p(a):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def _f(a):
+    return a.ctypes.data_as(_c_fp) if a is not None else None
+
+
+def _dbl(a):
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _flt(a):
+    return None if a is None else np.ascontiguousarray(a, dtype=np.float32)
+
+
+def config(m: dict) -> OrcConfig:
+    c = OrcConfig()
+    c.n_blocks, c.hidden, c.n_heads = m["n_blocks"], m["hidden"], m["n_heads"]
+    c.head_dim, c.ffn_hidden = m["head_dim"], m["ffn_hidden"]
+    c.norm = 0 if m["norm"] == "rms" else 1
+    c.norm_eps = m["norm_eps"]
+    c.adaln = 1 if m["adaln"] else 0
+    c.n_mod, c.t_dim, c.rope_axes = m["n_mod"], m["t_dim"], m["rope_axes"]
+    for i in range(3):
+        c.rope_dims[i] = m["rope_dims"][i]
+    c.rotary_dim, c.rope_base, c.io_channels = m["rotary_dim"], m["rope_base"], m["io_channels"]
+    return c
+
+
+class _Weights:
+    """Keeps the float32 arrays alive while the ctypes view of them is in use."""
+
+    def __init__(self, m: dict, weights: dict):
+        self.keep = []
+        self.blocks = (OrcBlock * m["n_blocks"])()
+        for l, bw in enumerate(weights["blocks"]):
+            for n in _BLOCK_NAMES:
+                a = _flt(bw.get(n))
+                self.keep.append(a)
+                setattr(self.blocks[l], n, _f(a))
+        self.w = OrcWeights()
+        self.w.blocks = ctypes.cast(self.blocks, ctypes.POINTER(OrcBlock))
+        for n in _GLOB_NAMES:
+            a = _flt(weights["glob"].get(n))
+            self.keep.append(a)
+            setattr(self.w, n, _f(a))
+
+
+# ------------------------------------------------------------------------------------------------
+# op-level entry points
+# ------------------------------------------------------------------------------------------------
+
+def linspace(start: float, stop: float, n: int) -> np.ndarray:
+    out = np.empty((n,), dtype=np.float64)
+    lib().orc_linspace(ctypes.c_double(start), ctypes.c_double(stop), ctypes.c_int(n), _d(out))
+    return out
+
+
+def check_layout(cu, doc_ids, tags, n_tokens: int, n_mod: int) -> int:
+    cu = np.ascontiguousarray(cu, dtype=np.int32)
+    doc_ids = np.ascontiguousarray(doc_ids, dtype=np.int32)
+    tags = np.ascontiguousarray(tags, dtype=np.uint8)
+    return int(lib().orc_check_layout(_p(cu), len(cu) - 1, _p(doc_ids), _p(tags),
+                                      int(n_tokens), int(n_mod)))
+
+
+def count_q_tiles(cu, tile: int = 128) -> int:
+    cu = np.ascontiguousarray(cu, dtype=np.int32)
+    return int(lib().orc_count_q_tiles(_p(cu), len(cu) - 1, int(tile)))
+
+
+def timestep_embedding(t: float, t_dim: int) -> np.ndarray:
+    out = np.empty((t_dim,), dtype=np.float64)
+    lib().orc_timestep_embedding(ctypes.c_double(t), ctypes.c_int(t_dim), _d(out))
+    return out
+
+
+def adaln(m: dict, weights: dict, t: float):
+    """Returns (mod [L, n_mod, 6, d], mod_final [n_mod, 2, d]) in float64."""
+    c = config(m)
+    w = _Weights(m, weights)
+    d, L, nm = m["hidden"], m["n_blocks"], m["n_mod"]
+    mod = np.empty((L, nm, 6, d), dtype=np.float64)
+    modf = np.empty((nm, 2, d), dtype=np.float64)
+    lib().orc_adaln(ctypes.byref(c), ctypes.byref(w.w), ctypes.c_double(t), _d(mod), _d(modf))
+    return mod, modf
+
+
+def rope_inv_freq(m: dict) -> np.ndarray:
+    c = config(m)
+    out = np.empty((m["rotary_dim"] // 2,), dtype=np.float32)
+    lib().orc_rope_inv_freq(ctypes.byref(c), _f(out))
+    return out
+
+
+def rope_cos_sin(m: dict, pos) -> tuple[np.ndarray, np.ndarray]:
+    c = config(m)
+    pos = _dbl(pos)
+    n = pos.shape[0]
+    half = m["rotary_dim"] // 2
+    cs = np.empty((n, half), dtype=np.float64)
+    sn = np.empty((n, half), dtype=np.float64)
+    lib().orc_rope_cos_sin(ctypes.byref(c), _d(pos), ctypes.c_int(n), _d(cs), _d(sn))
+    return cs, sn
+
+
+def rope_apply(x, n_heads: int, head_dim: int, rotary_dim: int, cs, sn) -> np.ndarray:
+    x = _dbl(x).copy()
+    n = x.shape[0]
+    lib().orc_rope_apply(_d(x), ctypes.c_int(n), ctypes.c_int(n_heads), ctypes.c_int(head_dim),
+                         ctypes.c_int(rotary_dim), _d(_dbl(cs)), _d(_dbl(sn)))
+    return x
+
+
+def rms_norm(x, eps: float) -> np.ndarray:
+    x = _dbl(x)
+    y = np.empty_like(x)
+    lib().orc_rms_norm(_d(x), ctypes.c_int(x.shape[0]), ctypes.c_int(x.shape[1]), ctypes.c_double(eps), _d(y))
+    return y
+
+
+def layer_norm(x, eps: float, g=None, b=None) -> np.ndarray:
+    x = _dbl(x)
+    y = np.empty_like(x)
+    g, b = _flt(g), _flt(b)
+    lib().orc_layer_norm(_d(x), ctypes.c_int(x.shape[0]), ctypes.c_int(x.shape[1]), ctypes.c_double(eps),
+                         _f(g), _f(b), _d(y))
+    return y
+
+
+def modulate(nrm, tags, shift, scale) -> np.ndarray:
+    """shift, scale: [n_mod, d]."""
+    nrm = _dbl(nrm)
+    tags = np.ascontiguousarray(tags, dtype=np.uint8)
+    shift, scale = _dbl(shift), _dbl(scale)
+    y = np.empty_like(nrm)
+    lib().orc_modulate(_d(nrm), ctypes.c_int(nrm.shape[0]), ctypes.c_int(nrm.shape[1]), _p(tags),
+                       _d(shift), _d(scale), ctypes.c_size_t(shift.shape[1]), _d(y))
+    return y
+
+
+def linear(x, W, b=None) -> np.ndarray:
+    x = _dbl(x)
+    W = _flt(W)
+    b = _flt(b)
+    m, k = x.shape
+    n_out = W.shape[0]
+    y = np.empty((m, n_out), dtype=np.float64)
+    lib().orc_linear(_d(x), ctypes.c_int(m), ctypes.c_int(k), _f(W), _f(b), ctypes.c_int(n_out), _d(y))
+    return y
+
+
+def conv1x1(x, W, b=None) -> np.ndarray:
+    """x: [ci, T] channel-major; W: [co, ci]."""
+    x = _dbl(x)
+    W = _flt(W)
+    b = _flt(b)
+    ci, T = x.shape
+    co = W.shape[0]
+    y = np.empty((co, T), dtype=np.float64)
+    lib().orc_conv1x1(_d(x), ctypes.c_int(ci), ctypes.c_int(T), _f(W), _f(b), ctypes.c_int(co), _d(y))
+    return y
+
+
+def attention(q, k, v, cu, n_heads: int, head_dim: int) -> np.ndarray:
+    """q, k, v: [N, H*Dh]; returns [N, H*Dh]."""
+    q, k, v = _dbl(q), _dbl(k), _dbl(v)
+    cu = np.ascontiguousarray(cu, dtype=np.int32)
+    o = np.empty_like(q)
+    lib().orc_attention(_d(q), _d(k), _d(v), ctypes.c_int(q.shape[0]), ctypes.c_int(n_heads),
+                        ctypes.c_int(head_dim), _p(cu), ctypes.c_int(len(cu) - 1), _d(o))
+    return o
+
+
+def attention_rows(q, k, v, cu, n_heads: int, head_dim: int, rows) -> np.ndarray:
+    q, k, v = _dbl(q), _dbl(k), _dbl(v)
+    cu = np.ascontiguousarray(cu, dtype=np.int32)
+    rows = np.ascontiguousarray(rows, dtype=np.int32)
+    o = np.empty((len(rows), q.shape[1]), dtype=np.float64)
+    lib().orc_attention_rows(_d(q), _d(k), _d(v), ctypes.c_int(q.shape[0]), ctypes.c_int(n_heads),
+                             ctypes.c_int(head_dim), _p(cu), ctypes.c_int(len(cu) - 1), _p(rows),
+                             ctypes.c_int(len(rows)), _d(o))
+    return o
+
+
+def swiglu(uv) -> np.ndarray:
+    uv = _dbl(uv)
+    n, f2 = uv.shape
+    h = np.empty((n, f2 // 2), dtype=np.float64)
+    lib().orc_swiglu(_d(uv), ctypes.c_int(n), ctypes.c_int(f2 // 2), _d(h))
+    return h
+
+
+def euler_step(x, v, sigma: float, sigma_next: float) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32).copy()
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    lib().orc_euler_step(_f(x), _f(v), ctypes.c_int64(x.size), ctypes.c_float(sigma), ctypes.c_float(sigma_next))
+    return x
+
+
+def block_forward(m: dict, weights: dict, l: int, mod_block, x, layout: dict, cs, sn) -> np.ndarray:
+    """One block in place on a float64 copy of x [N, d]; mod_block [n_mod, 6, d] or None."""
+    c = config(m)
+    w = _Weights(m, weights)
+    x = _dbl(x).copy()
+    mb = _dbl(mod_block) if mod_block is not None else None
+    lib().orc_block_forward(ctypes.byref(c), ctypes.byref(w.blocks[l]), _d(mb) if mb is not None else None,
+                            _d(x), ctypes.c_int(x.shape[0]),
+                            _p(np.ascontiguousarray(layout["cu_seqlens"], dtype=np.int32)),
+                            ctypes.c_int(layout["n_docs"]),
+                            _p(np.ascontiguousarray(layout["tags"], dtype=np.uint8)),
+                            _d(_dbl(cs)), _d(_dbl(sn)))
+    return x
+
+
+def forward(m: dict, weights: dict, x_in, layout: dict, t: float, dumps: bool = False):
+    """Whole forward.  Returns (out float64 shaped like x_in, block dumps [L, N, d] or None)."""
+    c = config(m)
+    w = _Weights(m, weights)
+    x_in = np.ascontiguousarray(x_in, dtype=np.float32)
+    n = layout["n_tokens"]
+    out = np.empty(x_in.shape, dtype=np.float64)
+    dm = np.empty((m["n_blocks"], n, m["hidden"]), dtype=np.float64) if dumps else None
+    cu = np.ascontiguousarray(layout["cu_seqlens"], dtype=np.int32)
+    ids = np.ascontiguousarray(layout["doc_ids"], dtype=np.int32)
+    tags = np.ascontiguousarray(layout["tags"], dtype=np.uint8)
+    pos = _dbl(layout["pos"])
+    rc = lib().orc_forward(ctypes.byref(c), ctypes.byref(w.w), _f(x_in), ctypes.c_int(n), _p(cu),
+                           ctypes.c_int(layout["n_docs"]), _p(ids), _p(tags), _d(pos),
+                           ctypes.c_double(t), _d(out), _d(dm) if dumps else None)
+    if rc:
+        raise ValueError(f"oracle: invalid packed layout (code {rc})")
+    return out, dm

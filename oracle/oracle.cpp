@@ -1,0 +1,513 @@
+// CPU oracle for the packed-varlen joint video+audio DiT forward and its Euler loop.
+//
+// TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, obviously-correct statement of what the
+// GPU library computes.  Only the test suite, the package smoke check and the bench's CPU-baseline
+// leg may load it; the library itself never does.  It shares no code, header, table or helper with
+// the CUDA path.  Every sum accumulates in double, every op is a naive loop in the order its
+// definition states, and inputs (bf16-valued or fp32 weights, fp32 tokens) are widened to double.
+// The Euler step alone is fp32, because the page fixes it as an exact, bit-reproducible step.
+//
+// Sources (page title, then the section):
+//   [H3]  "feat(minimax-h3): port the MiniMax-H3 omni-modal video+audio DiT"
+//   [M3]  "feat(MODEL-MUSIC-MUSIC3): the 2.4B fp32 DiT onto the device, staged once"
+//   [BF]  "feat(minimax-h3): stream the ORIGINAL bf16 DiT to the device, one tensor at a time"
+//
+// Readings where the pages are silent are marked READING and are listed in the design notes.
+// Functions whose values no page or closed form pins are marked "parity unpinned".
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <vector>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+extern "C" {
+
+typedef struct {
+  int n_blocks, hidden, n_heads, head_dim, ffn_hidden;
+  int norm;  // 0 = RMSNorm, 1 = LayerNorm
+  double norm_eps;
+  int adaln;  // 1 = modality-indexed AdaLN with gated residuals; 0 = plain residual adds
+  int n_mod, t_dim;
+  int rope_axes;
+  int rope_dims[3];  // per-axis rotary widths in dims (pairs = dims / 2)
+  int rotary_dim;    // sum of rope_dims, <= head_dim
+  double rope_base;
+  int io_channels;   // > 0: 1x1 pre/post convolutions io_channels <-> hidden
+} orc_config;
+
+typedef struct {
+  const float *w_qkv, *b_qkv, *w_o, *b_o, *w_in, *b_in, *w_down, *b_down;
+  const float *w_ada, *b_ada;
+  const float *ln1_g, *ln1_b, *ln2_g, *ln2_b;
+} orc_block;
+
+typedef struct {
+  const orc_block* blocks;
+  const float *w_ada_final, *b_ada_final;
+  const float *lnf_g, *lnf_b;
+  const float *w_pre, *b_pre, *w_post, *b_post;
+} orc_weights;
+
+static int g_threads = 1;
+
+void orc_set_threads(int n) { g_threads = n > 0 ? n : 1; }
+
+int orc_get_threads(void) { return g_threads; }
+
+// ---------------------------------------------------------------------------------------------
+// Packed layout.  [H3] "Correctness gates": the packed layout carries ids, tags, masks,
+// cu_seqlens and doc ids, gated exact.  Contract checked here: cu[0] = 0, strictly increasing,
+// cu[D] = N, doc_ids[i] = j exactly when cu[j] <= i < cu[j+1], every tag < n_mod.
+// Returns 0 when valid, else a positive code naming the first broken rule.
+// ---------------------------------------------------------------------------------------------
+int orc_check_layout(const int32_t* cu, int n_docs, const int32_t* doc_ids, const uint8_t* tags, int n_tokens,
+                     int n_mod) {
+  if (n_docs < 1) return 1;
+  if (cu[0] != 0) return 2;
+  for (int j = 0; j < n_docs; ++j)
+    if (cu[j + 1] <= cu[j]) return 3;
+  if (cu[n_docs] != n_tokens) return 4;
+  for (int j = 0; j < n_docs; ++j)
+    for (int i = cu[j]; i < cu[j + 1]; ++i)
+      if (doc_ids[i] != j) return 5;
+  for (int i = 0; i < n_tokens; ++i)
+    if ((int)tags[i] >= n_mod) return 6;
+  return 0;
+}
+
+// Number of 128-row query tiles the varlen attention visits: sum over documents of
+// ceil(len / 128).  Every (document, row) pair falls in exactly one tile.
+int orc_count_q_tiles(const int32_t* cu, int n_docs, int tile) {
+  int n = 0;
+  for (int j = 0; j < n_docs; ++j) n += (cu[j + 1] - cu[j] + tile - 1) / tile;
+  return n;
+}
+
+// ---------------------------------------------------------------------------------------------
+// fp64 position grid.  [H3] "Correctness gates": numpy.linspace(endpoint=False) evaluates
+// i*step + start, and that arithmetic order is what makes the grid bit-exact.
+// step = (stop - start) / n.
+// ---------------------------------------------------------------------------------------------
+void orc_linspace(double start, double stop, int n, double* out) {
+  double step = (stop - start) / (double)n;
+  for (int i = 0; i < n; ++i) out[i] = (double)i * step + start;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Timestep embedding.  READING (pages silent on the formula): the usual DiT sinusoid,
+// half = t_dim/2, f_k = exp(-ln(10000) * k / half), e = [cos(1000 t f_k) | sin(1000 t f_k)].
+// The ungated SiLU of [H3] "The device-resident forward (W2b)" is applied by the caller.
+// parity unpinned beyond the closed form at t = 0.
+// ---------------------------------------------------------------------------------------------
+void orc_timestep_embedding(double t, int t_dim, double* out) {
+  int half = t_dim / 2;
+  for (int k = 0; k < half; ++k) {
+    double f = exp(-log(10000.0) * (double)k / (double)half);
+    double a = 1000.0 * t * f;
+    out[k] = cos(a);
+    out[half + k] = sin(a);
+  }
+}
+
+static inline double silu(double v) { return v / (1.0 + exp(-v)); }
+
+// ---------------------------------------------------------------------------------------------
+// Modality-indexed AdaLN conditioning.  [H3] "The device-resident forward (W2b)": an ungated
+// SiLU on the conditioning path and two indexed AdaLN modulates.  Per block l and modality m:
+//   mod[l][m][:] = W_ada[l][m*6d : (m+1)*6d, :] . silu(e) + b_ada[...]
+// split into six d-wide chunks in the order shift1, scale1, gate1, shift2, scale2, gate2 (READING:
+// the DiT convention).  The final layer uses [n_mod][2d] = (shift_f, scale_f).
+// ---------------------------------------------------------------------------------------------
+void orc_adaln(const orc_config* c, const orc_weights* w, double t, double* mod, double* mod_final) {
+  int d = c->hidden, td = c->t_dim;
+  std::vector<double> e(td), se(td);
+  orc_timestep_embedding(t, td, e.data());
+  for (int k = 0; k < td; ++k) se[k] = silu(e[k]);
+  int rows = c->n_mod * 6 * d;
+  for (int l = 0; l < c->n_blocks; ++l) {
+    const orc_block* b = &w->blocks[l];
+    for (int r = 0; r < rows; ++r) {
+      double s = 0.0;
+      for (int k = 0; k < td; ++k) s += (double)b->w_ada[(size_t)r * td + k] * se[k];
+      if (b->b_ada) s += (double)b->b_ada[r];
+      mod[(size_t)l * rows + r] = s;
+    }
+  }
+  int rf = c->n_mod * 2 * d;
+  for (int r = 0; r < rf; ++r) {
+    double s = 0.0;
+    for (int k = 0; k < td; ++k) s += (double)w->w_ada_final[(size_t)r * td + k] * se[k];
+    if (w->b_ada_final) s += (double)w->b_ada_final[r];
+    mod_final[r] = s;
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// RoPE angles.  [H3] "The device-resident forward (W2b)": plain NeoX rotate_half whose angles come
+// from three axes of the fp64 position grid, fed through a per-row cos/sin cache.  [BF] "What this
+// enables": rope.inv_freq is a stored tensor (READING: fp32).
+//   inv_a[k] = base^(-2k / dim_a), k < dim_a/2, computed in double and rounded to fp32.
+//   The per-row angle vector concatenates the axis blocks (t, h, w); theta_j = pos[axis(j)] * inv[j]
+//   in double.  cos/sin are returned in double.
+// ---------------------------------------------------------------------------------------------
+void orc_rope_inv_freq(const orc_config* c, float* inv) {
+  int j = 0;
+  for (int a = 0; a < c->rope_axes; ++a) {
+    int da = c->rope_dims[a];
+    for (int k = 0; k < da / 2; ++k) inv[j++] = (float)pow(c->rope_base, -2.0 * (double)k / (double)da);
+  }
+}
+
+void orc_rope_cos_sin(const orc_config* c, const double* pos, int n_tokens, double* cos_out, double* sin_out) {
+  int half = c->rotary_dim / 2;
+  std::vector<float> inv(half);
+  std::vector<int> axis(half);
+  orc_rope_inv_freq(c, inv.data());
+  int j = 0;
+  for (int a = 0; a < c->rope_axes; ++a)
+    for (int k = 0; k < c->rope_dims[a] / 2; ++k) axis[j++] = a;
+  for (int r = 0; r < n_tokens; ++r)
+    for (int q = 0; q < half; ++q) {
+      double th = pos[(size_t)r * 3 + axis[q]] * (double)inv[q];
+      cos_out[(size_t)r * half + q] = cos(th);
+      sin_out[(size_t)r * half + q] = sin(th);
+    }
+}
+
+// NeoX rotate_half over the first R = rotary_dim dims of every head, in place; dims >= R pass
+// through ([M3] "What moved": ApplyPartialRotary).  For j < R/2 the pair is (x_j, x_{j+R/2}):
+//   x'_j       = x_j cos - x_{j+R/2} sin
+//   x'_{j+R/2} = x_{j+R/2} cos + x_j sin
+void orc_rope_apply(double* x, int n_tokens, int n_heads, int head_dim, int rotary_dim, const double* cs,
+                    const double* sn) {
+  int half = rotary_dim / 2;
+  for (int r = 0; r < n_tokens; ++r)
+    for (int h = 0; h < n_heads; ++h) {
+      double* v = x + ((size_t)r * n_heads + h) * head_dim;
+      for (int j = 0; j < half; ++j) {
+        double c0 = cs[(size_t)r * half + j], s0 = sn[(size_t)r * half + j];
+        double a = v[j], b = v[j + half];
+        v[j] = a * c0 - b * s0;
+        v[j + half] = b * c0 + a * s0;
+      }
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Norms.  [H3] "The device-resident forward (W2b)": RmsNorm (the CPU reference accumulates in
+// double).  READING: no affine weight (the "bare norm" of the AdaLN invariant).
+//   RMS(x) = x / sqrt(mean(x^2) + eps)
+// [M3] "What moved": LayerNorm for the music DiT: (x - mean) / sqrt(var + eps) * g + b,
+// var the biased (population) variance.
+// ---------------------------------------------------------------------------------------------
+void orc_rms_norm(const double* x, int n, int d, double eps, double* y) {
+#pragma omp parallel for num_threads(g_threads) schedule(static)
+  for (int r = 0; r < n; ++r) {
+    const double* xr = x + (size_t)r * d;
+    double ss = 0.0;
+    for (int i = 0; i < d; ++i) ss += xr[i] * xr[i];
+    double inv = 1.0 / sqrt(ss / (double)d + eps);
+    for (int i = 0; i < d; ++i) y[(size_t)r * d + i] = xr[i] * inv;
+  }
+}
+
+void orc_layer_norm(const double* x, int n, int d, double eps, const float* g, const float* b, double* y) {
+#pragma omp parallel for num_threads(g_threads) schedule(static)
+  for (int r = 0; r < n; ++r) {
+    const double* xr = x + (size_t)r * d;
+    double mu = 0.0;
+    for (int i = 0; i < d; ++i) mu += xr[i];
+    mu /= (double)d;
+    double var = 0.0;
+    for (int i = 0; i < d; ++i) var += (xr[i] - mu) * (xr[i] - mu);
+    var /= (double)d;
+    double inv = 1.0 / sqrt(var + eps);
+    for (int i = 0; i < d; ++i) {
+      double v = (xr[i] - mu) * inv;
+      if (g) v *= (double)g[i];
+      if (b) v += (double)b[i];
+      y[(size_t)r * d + i] = v;
+    }
+  }
+}
+
+// Indexed AdaLN modulate: token r takes the row of its modality tag.
+//   y = n * (1 + scale[tag]) + shift[tag]
+// shift / scale point at [n_mod] rows of d values, ``stride`` doubles apart.
+void orc_modulate(const double* nrm, int n, int d, const uint8_t* tags, const double* shift, const double* scale,
+                  size_t stride, double* y) {
+  for (int r = 0; r < n; ++r) {
+    const double* sh = shift + (size_t)tags[r] * stride;
+    const double* sc = scale + (size_t)tags[r] * stride;
+    for (int i = 0; i < d; ++i) y[(size_t)r * d + i] = nrm[(size_t)r * d + i] * (1.0 + sc[i]) + sh[i];
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Linear map, MatmulBT: y[i][o] = sum_k x[i][k] * W[o][k] + b[o], W row-major [n_out, k]
+// ([M3] "What moved": Linear -> vt::MatmulBT plus a rank-1 bias add).
+// ---------------------------------------------------------------------------------------------
+void orc_linear(const double* x, int m, int k, const float* W, const float* b, int n_out, double* y) {
+#pragma omp parallel for num_threads(g_threads) schedule(static)
+  for (int i = 0; i < m; ++i) {
+    const double* xi = x + (size_t)i * k;
+    for (int o = 0; o < n_out; ++o) {
+      const float* wo = W + (size_t)o * k;
+      double s = 0.0;
+      for (int q = 0; q < k; ++q) s += xi[q] * (double)wo[q];
+      if (b) s += (double)b[o];
+      y[(size_t)i * n_out + o] = s;
+    }
+  }
+}
+
+// 1x1 convolution written as the convolution itself, per document, channel-major:
+//   y[co][t] = sum_ci W[co][ci] * x[ci][t] + b[co]
+// [M3] "What moved" states that this equals MatmulBT on the frame-major transposed activation;
+// the tests check that identity against orc_linear.
+void orc_conv1x1(const double* x, int ci, int T, const float* W, const float* b, int co, double* y) {
+  for (int o = 0; o < co; ++o)
+    for (int t = 0; t < T; ++t) {
+      double s = 0.0;
+      for (int c = 0; c < ci; ++c) s += (double)W[(size_t)o * ci + c] * x[(size_t)c * T + t];
+      if (b) s += (double)b[o];
+      y[(size_t)o * T + t] = s;
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Varlen non-causal attention.  [H3] "Correctness gates": vt::DFlashBlockAttention(causal=false)
+// over the packed sequence; [M3] "What moved": non-causal attention with no bias.  For each
+// document [a, b) and head h, with q, k, v laid [N][H][Dh]:
+//   s_ij = q_i . k_j / sqrt(Dh)   for i, j in [a, b)     (READING: the usual 1/sqrt(Dh) scale)
+//   p_i  = softmax_j(s_i)         (max-subtracted, double)
+//   o_i  = sum_j p_ij v_j
+// No mask other than the document block.
+// ---------------------------------------------------------------------------------------------
+static void attend_row(const double* q, const double* k, const double* v, int H, int Dh, int a, int b, int i,
+                       int h, double* o, std::vector<double>& s) {
+  int hd = H * Dh;
+  double scale = 1.0 / sqrt((double)Dh);
+  const double* qi = q + (size_t)i * hd + (size_t)h * Dh;
+  double mx = -INFINITY;
+  for (int j = a; j < b; ++j) {
+    const double* kj = k + (size_t)j * hd + (size_t)h * Dh;
+    double acc = 0.0;
+    for (int e = 0; e < Dh; ++e) acc += qi[e] * kj[e];
+    s[j - a] = acc * scale;
+    if (s[j - a] > mx) mx = s[j - a];
+  }
+  double den = 0.0;
+  for (int j = a; j < b; ++j) {
+    s[j - a] = exp(s[j - a] - mx);
+    den += s[j - a];
+  }
+  for (int e = 0; e < Dh; ++e) {
+    double acc = 0.0;
+    for (int j = a; j < b; ++j) acc += s[j - a] * v[(size_t)j * hd + (size_t)h * Dh + e];
+    o[e] = acc / den;
+  }
+}
+
+void orc_attention(const double* q, const double* k, const double* v, int n_tokens, int H, int Dh,
+                   const int32_t* cu, int n_docs, double* o) {
+  (void)n_tokens;
+  for (int dj = 0; dj < n_docs; ++dj) {
+    int a = cu[dj], b = cu[dj + 1];
+#pragma omp parallel num_threads(g_threads)
+    {
+      std::vector<double> s(b - a);
+#pragma omp for schedule(dynamic, 4)
+      for (int idx = 0; idx < (b - a) * H; ++idx) {
+        int i = a + idx / H, h = idx % H;
+        attend_row(q, k, v, H, Dh, a, b, i, h, o + (size_t)i * H * Dh + (size_t)h * Dh, s);
+      }
+    }
+  }
+}
+
+// The same attention for a list of query rows only (out[r] for rows[r], all heads).
+void orc_attention_rows(const double* q, const double* k, const double* v, int n_tokens, int H, int Dh,
+                        const int32_t* cu, int n_docs, const int32_t* rows, int n_rows, double* o) {
+  (void)n_tokens;
+#pragma omp parallel num_threads(g_threads)
+  {
+    std::vector<double> s;
+#pragma omp for schedule(dynamic, 1)
+    for (int idx = 0; idx < n_rows * H; ++idx) {
+      int r = idx / H, h = idx % H, i = rows[r];
+      int dj = 0;
+      while (!(cu[dj] <= i && i < cu[dj + 1])) ++dj;
+      s.resize(cu[dj + 1] - cu[dj]);
+      attend_row(q, k, v, H, Dh, cu[dj], cu[dj + 1], i, h, o + (size_t)r * H * Dh + (size_t)h * Dh, s);
+    }
+  }
+  (void)n_docs;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Gated FFN.  [M3] "What moved" and "Correctness": the FFN computes value * silu(gate) with the
+// value in the first half of the merged up projection and the gate in the second half.
+//   uv = [u | g] (2F wide);  h = u * silu(g)
+// ---------------------------------------------------------------------------------------------
+void orc_swiglu(const double* uv, int n, int F, double* hout) {
+  for (int r = 0; r < n; ++r)
+    for (int i = 0; i < F; ++i) {
+      double u = uv[(size_t)r * 2 * F + i], g = uv[(size_t)r * 2 * F + F + i];
+      hout[(size_t)r * F + i] = u * silu(g);
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// One Euler-ancestral (eta = 0) step of the rectified flow, in fp32 and in exactly this order
+// ([H3] "Correctness gates": the euler-ancestral eta0 scheduler and rf_v_to_x0, gated exact):
+//   x0 = x - sigma * v
+//   x  <- x0 + sigma_next * (x - x0) / sigma      (left to right: (sigma_next * (x - x0)) / sigma)
+// Built with -ffp-contract=off so that no product is fused into an add.
+// ---------------------------------------------------------------------------------------------
+void orc_euler_step(float* x, const float* v, int64_t n, float sigma, float sigma_next) {
+  for (int64_t i = 0; i < n; ++i) {
+    float sv = sigma * v[i];
+    float x0 = x[i] - sv;
+    float dx = x[i] - x0;
+    float num = sigma_next * dx;
+    float q = num / sigma;
+    x[i] = x0 + q;
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// One transformer block, in place on the fp64 residual x [N][d].  [H3] "The device-resident
+// forward (W2b)" lists the ops; with AdaLN on:
+//   y  = RMS(x) * (1 + scale1[tag]) + shift1[tag]
+//   [q | k | v] = y W_qkv^T + b_qkv          (fused order [q_all | k_all | v_all], heads contiguous)
+//   q, k <- NeoX rotate_half with the per-row cos/sin
+//   o  = varlen attention(q, k, v)
+//   x += gate1[tag] * (o W_o^T + b_o)
+//   y2 = RMS(x) * (1 + scale2[tag]) + shift2[tag]
+//   h  = u * silu(g),  [u | g] = y2 W_in^T + b_in
+//   x += gate2[tag] * (h W_down^T + b_down)
+// With AdaLN off (the music DiT, [M3] "What moved"): LayerNorm with (g, b) in place of the
+// modulated RMSNorm and plain residual adds in place of the gated ones.
+// mod points at this block's [n_mod][6d] row block (NULL when AdaLN is off).
+// ---------------------------------------------------------------------------------------------
+void orc_block_forward(const orc_config* c, const orc_block* w, const double* mod, double* x, int n,
+                       const int32_t* cu, int n_docs, const uint8_t* tags, const double* cs, const double* sn) {
+  int d = c->hidden, F = c->ffn_hidden, H = c->n_heads, Dh = c->head_dim;
+  size_t md = (size_t)6 * d;
+  std::vector<double> nrm((size_t)n * d), y((size_t)n * d), qkv((size_t)n * 3 * d);
+  std::vector<double> q((size_t)n * d), k((size_t)n * d), v((size_t)n * d), o((size_t)n * d), t((size_t)n * d);
+  if (c->norm == 0) {
+    orc_rms_norm(x, n, d, c->norm_eps, nrm.data());
+  } else {
+    orc_layer_norm(x, n, d, c->norm_eps, w->ln1_g, w->ln1_b, nrm.data());
+  }
+  if (c->adaln)
+    orc_modulate(nrm.data(), n, d, tags, mod + 0 * d, mod + 1 * d, md, y.data());
+  else
+    y = nrm;
+  orc_linear(y.data(), n, d, w->w_qkv, w->b_qkv, 3 * d, qkv.data());
+  for (int r = 0; r < n; ++r)
+    for (int i = 0; i < d; ++i) {
+      q[(size_t)r * d + i] = qkv[(size_t)r * 3 * d + i];
+      k[(size_t)r * d + i] = qkv[(size_t)r * 3 * d + d + i];
+      v[(size_t)r * d + i] = qkv[(size_t)r * 3 * d + 2 * d + i];
+    }
+  orc_rope_apply(q.data(), n, H, Dh, c->rotary_dim, cs, sn);
+  orc_rope_apply(k.data(), n, H, Dh, c->rotary_dim, cs, sn);
+  orc_attention(q.data(), k.data(), v.data(), n, H, Dh, cu, n_docs, o.data());
+  orc_linear(o.data(), n, d, w->w_o, w->b_o, d, t.data());
+  for (int r = 0; r < n; ++r) {
+    const double* g1 = c->adaln ? mod + (size_t)tags[r] * md + 2 * d : nullptr;
+    for (int i = 0; i < d; ++i) x[(size_t)r * d + i] += (g1 ? g1[i] : 1.0) * t[(size_t)r * d + i];
+  }
+  if (c->norm == 0) {
+    orc_rms_norm(x, n, d, c->norm_eps, nrm.data());
+  } else {
+    orc_layer_norm(x, n, d, c->norm_eps, w->ln2_g, w->ln2_b, nrm.data());
+  }
+  if (c->adaln)
+    orc_modulate(nrm.data(), n, d, tags, mod + 3 * d, mod + 4 * d, md, y.data());
+  else
+    y = nrm;
+  std::vector<double> uv((size_t)n * 2 * F), hh((size_t)n * F);
+  orc_linear(y.data(), n, d, w->w_in, w->b_in, 2 * F, uv.data());
+  orc_swiglu(uv.data(), n, F, hh.data());
+  orc_linear(hh.data(), n, F, w->w_down, w->b_down, d, t.data());
+  for (int r = 0; r < n; ++r) {
+    const double* g2 = c->adaln ? mod + (size_t)tags[r] * md + 5 * d : nullptr;
+    for (int i = 0; i < d; ++i) x[(size_t)r * d + i] += (g2 ? g2[i] : 1.0) * t[(size_t)r * d + i];
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Whole forward.  x_in: token-major [N][d] fp32, or, when io_channels > 0, channel-major per
+// document ([io][len_j] blocks back to back).  out has the same layout and size as x_in.
+// Final layer (READING: the configs give no latent widths, so the patch embedding and output heads
+// are not part of this forward): with AdaLN, out = RMS(x) * (1 + scale_f[tag]) + shift_f[tag];
+// without it, out = LN_f(x), then the 1x1 post-convolution back to io channels.
+// dumps (may be NULL) receives the residual after each block, [L][N][d].
+// Returns the layout check's code (0 when valid).
+// ---------------------------------------------------------------------------------------------
+int orc_forward(const orc_config* c, const orc_weights* w, const float* x_in, int n, const int32_t* cu, int n_docs,
+                const int32_t* doc_ids, const uint8_t* tags, const double* pos, double t, double* out,
+                double* dumps) {
+  int rc = orc_check_layout(cu, n_docs, doc_ids, tags, n, c->adaln ? c->n_mod : 1);
+  if (rc) return rc;
+  int d = c->hidden, half = c->rotary_dim / 2;
+  std::vector<double> x((size_t)n * d);
+  if (c->io_channels > 0) {
+    int ci = c->io_channels;
+    for (int j = 0; j < n_docs; ++j) {
+      int a = cu[j], len = cu[j + 1] - cu[j];
+      std::vector<double> xin((size_t)ci * len), yd((size_t)d * len);
+      for (size_t e = 0; e < xin.size(); ++e) xin[e] = (double)x_in[(size_t)ci * a + e];
+      orc_conv1x1(xin.data(), ci, len, w->w_pre, w->b_pre, d, yd.data());
+      for (int s = 0; s < len; ++s)
+        for (int o = 0; o < d; ++o) x[(size_t)(a + s) * d + o] = yd[(size_t)o * len + s];
+    }
+  } else {
+    for (size_t e = 0; e < x.size(); ++e) x[e] = (double)x_in[e];
+  }
+  std::vector<double> cs((size_t)n * half), sn((size_t)n * half);
+  orc_rope_cos_sin(c, pos, n, cs.data(), sn.data());
+  std::vector<double> mod, modf;
+  if (c->adaln) {
+    mod.resize((size_t)c->n_blocks * c->n_mod * 6 * d);
+    modf.resize((size_t)c->n_mod * 2 * d);
+    orc_adaln(c, w, t, mod.data(), modf.data());
+  }
+  for (int l = 0; l < c->n_blocks; ++l) {
+    const double* ml = c->adaln ? mod.data() + (size_t)l * c->n_mod * 6 * d : nullptr;
+    orc_block_forward(c, &w->blocks[l], ml, x.data(), n, cu, n_docs, tags, cs.data(), sn.data());
+    if (dumps) memcpy(dumps + (size_t)l * n * d, x.data(), sizeof(double) * (size_t)n * d);
+  }
+  std::vector<double> nrm((size_t)n * d);
+  if (c->adaln) {
+    orc_rms_norm(x.data(), n, d, c->norm_eps, nrm.data());
+    orc_modulate(nrm.data(), n, d, tags, modf.data(), modf.data() + d, (size_t)2 * d, out);
+  } else {
+    orc_layer_norm(x.data(), n, d, c->norm_eps, w->lnf_g, w->lnf_b, nrm.data());
+    if (c->io_channels > 0) {
+      int co = c->io_channels;
+      for (int j = 0; j < n_docs; ++j) {
+        int a = cu[j], len = cu[j + 1] - cu[j];
+        std::vector<double> xd((size_t)d * len), yd((size_t)co * len);
+        for (int s = 0; s < len; ++s)
+          for (int o = 0; o < d; ++o) xd[(size_t)o * len + s] = nrm[(size_t)(a + s) * d + o];
+        orc_conv1x1(xd.data(), d, len, w->w_post, w->b_post, co, yd.data());
+        memcpy(out + (size_t)co * a, yd.data(), sizeof(double) * yd.size());
+      }
+    } else {
+      memcpy(out, nrm.data(), sizeof(double) * nrm.size());
+    }
+  }
+  return 0;
+}
+
+}  // extern "C"

@@ -1,0 +1,406 @@
+"""Pins for the CPU oracle, independent of the oracle itself.
+
+Each test checks the oracle against something it does not compute: numpy.linspace, closed forms,
+invariants of the mathematics, textbook special cases, library routines (numpy matmul / einsum),
+and brute force by an independent numpy forward on 8-token inputs.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests import numpy_dit
+
+# ---------------------------------------------------------------------------------------------
+# small models used by brute force
+# ---------------------------------------------------------------------------------------------
+
+TINY_RMS = dict(n_blocks=2, hidden=16, n_heads=2, head_dim=8, ffn_hidden=24, norm="rms", norm_eps=1e-6,
+                adaln=True, n_mod=2, t_dim=16, rope_axes=3, rope_dims=(2, 2, 4), rotary_dim=8,
+                rope_base=10000.0, io_channels=0, dtype="fp32")
+TINY_LN = dict(n_blocks=2, hidden=16, n_heads=2, head_dim=8, ffn_hidden=24, norm="ln", norm_eps=1e-5,
+               adaln=False, n_mod=1, t_dim=16, rope_axes=1, rope_dims=(4, 0, 0), rotary_dim=4,
+               rope_base=10000.0, io_channels=6, dtype="fp32")
+DOCS8 = [dict(video=(1, 2, 2), audio=1), dict(video=(1, 1, 2), audio=1)]
+
+
+def _workload(m, seed, docs, w_std=0.3, bias_std=0.2):
+    return dict(model=m, seed=seed, docs=docs, t=0.3, w_std=w_std, bias_std=bias_std, x_std=1.0)
+
+
+def _ln_params_random(W, seed):
+    """Give LayerNorm gains/shifts non-trivial values so the affine path is exercised."""
+    for l, b in enumerate(W["blocks"]):
+        for n in ("ln1_g", "ln2_g"):
+            b[n] = 1.0 + synth.normal(seed, f"{l}{n}", b[n].shape, 0.2)
+        for n in ("ln1_b", "ln2_b"):
+            b[n] = synth.normal(seed, f"{l}{n}", b[n].shape, 0.2)
+    W["glob"]["lnf_g"] = 1.0 + synth.normal(seed, "lnf_g", W["glob"]["lnf_g"].shape, 0.2)
+    W["glob"]["lnf_b"] = synth.normal(seed, "lnf_b", W["glob"]["lnf_b"].shape, 0.2)
+
+
+# ---------------------------------------------------------------------------------------------
+# fp64 grid: bit-exact against numpy.linspace(endpoint=False)
+# ---------------------------------------------------------------------------------------------
+
+PROBES = [(0.0, 3.0, 7), (0.1, 5.3, 17), (0.0, 8.0, 512), (0.0, 16.0, 1024), (0.0, 2.0, 32), (-1.7, 2.9, 33),
+          (0.0, 1.0, 16), (3.3, 3.4, 100), (0.0, 86.0, 86), (1e-3, 7.0, 1000)]
+
+
+@pytest.mark.parametrize("start,stop,n", PROBES)
+def test_linspace_bit_exact_vs_numpy(start, stop, n):
+    ref = np.linspace(start, stop, n, endpoint=False)
+    assert np.array_equal(oracle.linspace(start, stop, n).view(np.uint64), ref.view(np.uint64))
+    assert np.array_equal(synth.grid_axis(start, stop, n).view(np.uint64), ref.view(np.uint64))
+
+
+def test_linspace_order_matters():
+    """The pin discriminates: a different arithmetic order misses numpy on some probe."""
+    miss = 0
+    for start, stop, n in PROBES:
+        alt = np.array([i * (stop - start) / n + start for i in range(n)])
+        miss += int(not np.array_equal(alt, np.linspace(start, stop, n, endpoint=False)))
+    assert miss > 0
+
+
+def test_layout_sizes_and_grid():
+    expect = {"tiny": [96, 160], "video_audio_bf16": [8704, 8704], "long_doc_bf16": [33792],
+              "denoise_loop": [17408, 9216], "music_fp32": [86, 86]}
+    for name, sizes in expect.items():
+        lay = synth.build_layout(synth.WORKLOADS[name]["docs"])
+        assert list(np.diff(lay["cu_seqlens"])) == sizes
+        assert lay["n_tokens"] == sum(sizes)
+        assert oracle.check_layout(lay["cu_seqlens"], lay["doc_ids"], lay["tags"], lay["n_tokens"], 2) == 0
+    lay = synth.build_layout(synth.WORKLOADS["tiny"]["docs"])
+    # doc A: 96 video tokens on T2,H6,W8, w fastest; doc B: 128 video then 32 audio
+    assert np.array_equal(lay["pos"][:96], np.array([(t, h, w) for t in range(2) for h in range(6)
+                                                      for w in range(8)], dtype=np.float64))
+    assert (lay["tags"][96:224] == 0).all() and (lay["tags"][224:] == 1).all()
+    assert np.array_equal(lay["pos"][224:, 0], np.linspace(0, 2, 32, endpoint=False))
+    assert (lay["pos"][224:, 1:] == 0).all()
+
+
+def test_layout_check_rejects():
+    lay = synth.build_layout(synth.WORKLOADS["tiny"]["docs"])
+    cu, ids, tags, n = lay["cu_seqlens"], lay["doc_ids"], lay["tags"], lay["n_tokens"]
+    assert oracle.check_layout(cu, ids, tags, n, 2) == 0
+    bad = cu.copy(); bad[0] = 1
+    assert oracle.check_layout(bad, ids, tags, n, 2) == 2
+    bad = cu.copy(); bad[1] = 0
+    assert oracle.check_layout(bad, ids, tags, n, 2) == 3
+    assert oracle.check_layout(cu, ids, tags, n + 1, 2) == 4
+    bad = ids.copy(); bad[95] = 1
+    assert oracle.check_layout(cu, bad, tags, n, 2) == 5
+    bad = tags.copy(); bad[3] = 2
+    assert oracle.check_layout(cu, ids, bad, n, 2) == 6
+    assert oracle.count_q_tiles(np.array([0, 96, 256])) == 1 + 2
+    assert oracle.count_q_tiles(np.array([0, 8704, 17408])) == 2 * 68
+
+
+# ---------------------------------------------------------------------------------------------
+# timestep embedding, AdaLN, norms
+# ---------------------------------------------------------------------------------------------
+
+def test_timestep_embedding_closed_form_at_zero():
+    e = oracle.timestep_embedding(0.0, 256)
+    assert (e[:128] == 1.0).all() and (e[128:] == 0.0).all()
+
+
+def test_adaln_is_matvec_of_silu_embedding():
+    w = _workload(TINY_RMS, 5, DOCS8)
+    W = synth.make_weights(w)
+    mod, modf = oracle.adaln(TINY_RMS, W, 0.3)
+    e = oracle.timestep_embedding(0.3, 16)
+    se = e / (1 + np.exp(-e))
+    for l in range(2):
+        ref = W["blocks"][l]["w_ada"].astype(np.float64) @ se + W["blocks"][l]["b_ada"]
+        assert np.allclose(mod[l].reshape(-1), ref, rtol=0, atol=1e-14)
+    ref = W["glob"]["w_ada_final"].astype(np.float64) @ se + W["glob"]["b_ada_final"]
+    assert np.allclose(modf.reshape(-1), ref, rtol=0, atol=1e-14)
+
+
+def test_rms_norm_closed_form():
+    x = synth.normal(7, "rms", (5, 64), 3.0).astype(np.float64)
+    y = oracle.rms_norm(x, 1e-6)
+    m = (x * x).mean(axis=1)
+    assert np.allclose((y * y).mean(axis=1), m / (m + 1e-6), rtol=1e-14, atol=0)
+    c = np.full((1, 32), 0.25)
+    assert np.allclose(oracle.rms_norm(c, 1e-6), 0.25 / np.sqrt(0.0625 + 1e-6), rtol=1e-15)
+    # direction is preserved
+    assert np.allclose(y / np.linalg.norm(y, axis=1, keepdims=True), x / np.linalg.norm(x, axis=1, keepdims=True))
+
+
+def test_layer_norm_closed_form():
+    x = synth.normal(7, "ln", (5, 64), 3.0).astype(np.float64) + 4.0
+    y = oracle.layer_norm(x, 1e-5)
+    v = x.var(axis=1)
+    assert np.allclose(y.mean(axis=1), 0.0, atol=1e-14)
+    assert np.allclose((y * y).mean(axis=1), v / (v + 1e-5), rtol=1e-13)
+    g = np.full(64, 2.0, dtype=np.float32)
+    b = np.full(64, 3.0, dtype=np.float32)
+    y2 = oracle.layer_norm(x, 1e-5, g, b)
+    assert np.allclose(y2, 2 * y + 3, rtol=1e-15, atol=1e-15)
+
+
+def test_modulate_zero_is_bare_norm_bit_exact():
+    x = synth.normal(8, "m", (6, 32), 1.0)
+    nrm = oracle.rms_norm(x, 1e-6)
+    tags = np.array([0, 1, 1, 0, 1, 0], dtype=np.uint8)
+    z = np.zeros((2, 32))
+    assert np.array_equal(oracle.modulate(nrm, tags, z, z), nrm)
+    sh = np.stack([np.full(32, 1.0), np.full(32, -2.0)])
+    sc = np.stack([np.full(32, 0.5), np.full(32, 1.0)])
+    y = oracle.modulate(nrm, tags, sh, sc)
+    assert np.allclose(y[0], nrm[0] * 1.5 + 1.0) and np.allclose(y[1], nrm[1] * 2.0 - 2.0)
+
+
+# ---------------------------------------------------------------------------------------------
+# RoPE
+# ---------------------------------------------------------------------------------------------
+
+M3AX = dict(TINY_RMS, rope_dims=(2, 2, 4), rotary_dim=8, head_dim=8)
+
+
+def test_rope_identity_at_origin_bit_exact():
+    pos = np.zeros((3, 3))
+    cs, sn = oracle.rope_cos_sin(M3AX, pos)
+    x = synth.normal(9, "x", (3, 16), 1.0)
+    assert np.array_equal(oracle.rope_apply(x, 2, 8, 8, cs, sn), x.astype(np.float64))
+
+
+def test_rope_norm_preserving_and_rotation_matrix():
+    lay = synth.build_layout([dict(video=(3, 4, 5), audio=7)])
+    cs, sn = oracle.rope_cos_sin(M3AX, lay["pos"])
+    x = synth.normal(9, "y", (lay["n_tokens"], 16), 1.0).astype(np.float64)
+    y = oracle.rope_apply(x, 2, 8, 8, cs, sn)
+    for h in range(2):
+        a, b = np.linalg.norm(x[:, 8 * h:8 * h + 8], axis=1), np.linalg.norm(y[:, 8 * h:8 * h + 8], axis=1)
+        assert np.allclose(a, b, rtol=1e-14)
+    # one pair = a 2-D rotation by +theta (textbook [[c, -s], [s, c]])
+    th = 0.7
+    R = np.array([[np.cos(th), -np.sin(th)], [np.sin(th), np.cos(th)]])
+    v = np.array([[0.3, -1.1]])
+    out = oracle.rope_apply(v, 1, 2, 2, np.array([[np.cos(th)]]), np.array([[np.sin(th)]]))
+    assert np.allclose(out[0], R @ v[0], rtol=0, atol=1e-15)
+
+
+def test_rope_pairs_are_rotate_half():
+    """A unit vector in dim j moves only within the pair (j, j + R/2)."""
+    pos = np.array([[1.0, 2.0, 3.0]])
+    cs, sn = oracle.rope_cos_sin(M3AX, pos)
+    for j in range(8):
+        e = np.zeros((1, 8)); e[0, j] = 1.0
+        y = oracle.rope_apply(e, 1, 8, 8, cs, sn)
+        partner = j + 4 if j < 4 else j - 4
+        nz = set(np.nonzero(np.abs(y[0]) > 1e-15)[0].tolist())
+        assert nz <= {j, partner} and partner in nz
+
+
+def test_rope_axis_blocks_concatenate_t_h_w():
+    """Position (p,0,0) turns only the t block; (0,p,0) only h; (0,0,p) only w.  Pair 0 of each block
+    has inverse frequency exactly 1, so its angle is the position itself."""
+    m = dict(TINY_RMS, rope_dims=(4, 6, 6), rotary_dim=16, head_dim=16)
+    blocks = [(0, 2), (2, 5), (5, 8)]
+    for a, (lo, hi) in enumerate(blocks):
+        pos = np.zeros((1, 3)); pos[0, a] = 2.5
+        cs, sn = oracle.rope_cos_sin(m, pos)
+        moved = np.nonzero(cs[0] != 1.0)[0]
+        assert lo in moved and all(lo <= j < hi for j in moved)
+        assert cs[0, lo] == np.cos(2.5) and sn[0, lo] == np.sin(2.5)
+
+
+def test_rope_relative_position_invariance():
+    """Shifting every position of a document by an integer leaves its attention output unchanged."""
+    m = TINY_RMS
+    lay = synth.build_layout([dict(video=(2, 2, 3), audio=3)])
+    n = lay["n_tokens"]
+    q, k, v = (synth.normal(10, nm, (n, 16), 1.0).astype(np.float64) for nm in "qkv")
+    outs = []
+    for shift in (0.0, 5.0):
+        pos = lay["pos"] + shift
+        cs, sn = oracle.rope_cos_sin(m, pos)
+        qr, kr = oracle.rope_apply(q, 2, 8, 8, cs, sn), oracle.rope_apply(k, 2, 8, 8, cs, sn)
+        outs.append(oracle.attention(qr, kr, v, lay["cu_seqlens"], 2, 8))
+    assert np.allclose(outs[0], outs[1], rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------------------------
+# linear map, 1x1 conv, gated FFN
+# ---------------------------------------------------------------------------------------------
+
+def test_linear_matches_numpy_matmul():
+    x = synth.normal(11, "x", (7, 33), 1.0).astype(np.float64)
+    W = synth.normal(11, "W", (19, 33), 0.5)
+    b = synth.normal(11, "b", (19,), 0.5)
+    assert np.allclose(oracle.linear(x, W, b), x @ W.astype(np.float64).T + b, rtol=1e-13, atol=1e-13)
+
+
+def test_conv1x1_equals_matmulbt_on_transposed_activation():
+    x = synth.normal(12, "x", (6, 9), 1.0).astype(np.float64)  # [ci, T]
+    W = synth.normal(12, "W", (5, 6), 0.5)
+    b = synth.normal(12, "b", (5,), 0.5)
+    direct = oracle.conv1x1(x, W, b)
+    via_gemm = oracle.linear(x.T, W, b).T
+    assert np.allclose(direct, via_gemm, rtol=1e-14, atol=1e-14)
+
+
+def test_swiglu_value_first_gate_second():
+    uv = np.array([[1.0, 2.0]])
+    assert np.isclose(oracle.swiglu(uv)[0, 0], 1.0 * 2.0 / (1.0 + np.exp(-2.0)), rtol=1e-15)
+    uv = np.array([[3.0, 0.0]])
+    assert oracle.swiglu(uv)[0, 0] == 0.0
+
+
+# ---------------------------------------------------------------------------------------------
+# attention
+# ---------------------------------------------------------------------------------------------
+
+def test_attention_identical_keys_give_mean_of_v():
+    lay = synth.build_layout([dict(video=(1, 3, 4)), dict(video=(1, 1, 5))])
+    n = lay["n_tokens"]
+    q = synth.normal(13, "q", (n, 16), 1.0)
+    k = np.tile(synth.normal(13, "k", (1, 16), 1.0), (n, 1))
+    v = synth.normal(13, "v", (n, 16), 1.0).astype(np.float64)
+    o = oracle.attention(q, k, v, lay["cu_seqlens"], 2, 8)
+    cu = lay["cu_seqlens"]
+    for j in range(2):
+        assert np.allclose(o[cu[j]:cu[j + 1]], v[cu[j]:cu[j + 1]].mean(axis=0), rtol=0, atol=1e-14)
+
+
+def test_attention_block_diagonal_equals_docs_alone_and_one_token_doc():
+    lay = synth.build_layout([dict(video=(1, 3, 4), audio=2), dict(video=(1, 1, 1)), dict(video=(1, 2, 3))])
+    n, cu = lay["n_tokens"], lay["cu_seqlens"]
+    q, k, v = (synth.normal(14, nm, (n, 16), 1.0).astype(np.float64) for nm in "qkv")
+    o = oracle.attention(q, k, v, cu, 2, 8)
+    for j in range(3):
+        a, b = cu[j], cu[j + 1]
+        alone = oracle.attention(q[a:b], k[a:b], v[a:b], np.array([0, b - a]), 2, 8)
+        assert np.array_equal(o[a:b], alone)
+    assert np.allclose(o[cu[1]], v[cu[1]], rtol=0, atol=1e-15)  # a 1-token document returns its v
+
+
+def test_attention_matches_numpy_softmax_and_rows():
+    lay = synth.build_layout([dict(video=(1, 3, 4), audio=2), dict(video=(1, 2, 3))])
+    n, cu = lay["n_tokens"], lay["cu_seqlens"]
+    q, k, v = (synth.normal(15, nm, (n, 16), 1.0).astype(np.float64) for nm in "qkv")
+    o = oracle.attention(q, k, v, cu, 2, 8)
+    assert np.allclose(o, numpy_dit.attention(q, k, v, cu, 2, 8), rtol=0, atol=1e-13)
+    rows = np.array([0, 5, 13, n - 1])
+    assert np.array_equal(oracle.attention_rows(q, k, v, cu, 2, 8, rows), o[rows])
+
+
+def test_attention_permutation_equivariance():
+    lay = synth.build_layout([dict(video=(1, 3, 4))])
+    n, cu = lay["n_tokens"], lay["cu_seqlens"]
+    q, k, v = (synth.normal(16, nm, (n, 16), 1.0).astype(np.float64) for nm in "qkv")
+    perm = np.random.default_rng(0).permutation(n)
+    o = oracle.attention(q, k, v, cu, 2, 8)
+    op = oracle.attention(q[perm], k[perm], v[perm], cu, 2, 8)
+    assert np.allclose(op, o[perm], rtol=0, atol=1e-14)
+
+
+# ---------------------------------------------------------------------------------------------
+# Euler step (fp32, exact order)
+# ---------------------------------------------------------------------------------------------
+
+def _numpy_euler(x, v, s, sn):
+    s, sn = np.float32(s), np.float32(sn)
+    x0 = x - s * v
+    return x0 + (sn * (x - x0)) / s
+
+
+def test_euler_bit_exact_vs_numpy_float32():
+    x = synth.normal(17, "x", (4099,), 1.0)
+    v = synth.normal(17, "v", (4099,), 1.0)
+    sig = synth.sigmas(50)
+    for i in (0, 1, 17, 48, 49):
+        got = oracle.euler_step(x, v, sig[i], sig[i + 1])
+        ref = _numpy_euler(x, v, sig[i], sig[i + 1])
+        assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)), i
+
+
+def test_euler_last_step_lands_on_x0_and_constant_velocity_telescopes():
+    x = synth.normal(18, "x", (1000,), 1.0)
+    v = synth.normal(18, "v", (1000,), 1.0)
+    got = oracle.euler_step(x, v, np.float32(0.02), np.float32(0.0))
+    assert np.array_equal(got, x - np.float32(0.02) * v)
+    sig = synth.sigmas(50)
+    assert sig[0] == 1.0 and sig[50] == 0.0 and sig[25] == np.float32(0.5)
+    z = x.copy()
+    for i in range(50):
+        z = oracle.euler_step(z, v, sig[i], sig[i + 1])
+    assert np.allclose(z, x - v, rtol=0, atol=2e-5)
+
+
+# ---------------------------------------------------------------------------------------------
+# whole forward: brute force on 8 tokens, invariants
+# ---------------------------------------------------------------------------------------------
+
+def test_forward_brute_force_rms_adaln():
+    w = _workload(TINY_RMS, 21, DOCS8)
+    lay = synth.build_layout(DOCS8)
+    assert lay["n_tokens"] == 8 and lay["tags"].tolist().count(1) == 2
+    W = synth.make_weights(w, bf16=False)
+    x = synth.make_tokens(w, lay)
+    out, _ = oracle.forward(TINY_RMS, W, x, lay, 0.3)
+    ref = numpy_dit.forward(TINY_RMS, W, x, lay, 0.3)
+    assert np.abs(out - ref).max() <= 1e-12 * np.abs(ref).max()
+
+
+def test_forward_brute_force_layernorm_partial_rotary_conv():
+    w = _workload(TINY_LN, 22, [dict(frames=5), dict(frames=3)])
+    lay = synth.build_layout(w["docs"])
+    W = synth.make_weights(w, bf16=False)
+    _ln_params_random(W, 22)
+    x = synth.make_tokens(w, lay)
+    out, _ = oracle.forward(TINY_LN, W, x, lay, 0.0)
+    ref = numpy_dit.forward(TINY_LN, W, x, lay, 0.0)
+    assert out.shape == (6 * 8,)
+    assert np.abs(out - ref).max() <= 1e-12 * np.abs(ref).max()
+
+
+def test_forward_gate_zero_block_is_identity_bit_exact():
+    w = _workload(TINY_RMS, 23, DOCS8)
+    lay = synth.build_layout(DOCS8)
+    W = synth.make_weights(w, bf16=False)
+    d = TINY_RMS["hidden"]
+    for b in W["blocks"]:
+        wa = b["w_ada"].reshape(2, 6, d, -1)
+        wa[:, 2] = 0.0; wa[:, 5] = 0.0
+        ba = b["b_ada"].reshape(2, 6, d)
+        ba[:, 2] = 0.0; ba[:, 5] = 0.0
+    x = synth.make_tokens(w, lay)
+    _, dumps = oracle.forward(TINY_RMS, W, x, lay, 0.3, dumps=True)
+    assert np.array_equal(dumps[0], x.astype(np.float64)) and np.array_equal(dumps[1], x.astype(np.float64))
+
+
+def test_forward_modality_swap_symmetry():
+    """Swapping every tag together with the two modalities' AdaLN rows gives the same result."""
+    w = _workload(TINY_RMS, 24, DOCS8)
+    lay = synth.build_layout(DOCS8)
+    W = synth.make_weights(w, bf16=False)
+    x = synth.make_tokens(w, lay)
+    out, _ = oracle.forward(TINY_RMS, W, x, lay, 0.3)
+    d = TINY_RMS["hidden"]
+    for b in W["blocks"]:
+        b["w_ada"] = b["w_ada"].reshape(2, -1)[::-1].reshape(b["w_ada"].shape).copy()
+        b["b_ada"] = b["b_ada"].reshape(2, -1)[::-1].reshape(-1).copy()
+    W["glob"]["w_ada_final"] = W["glob"]["w_ada_final"].reshape(2, -1)[::-1].reshape(2 * 2 * d, -1).copy()
+    W["glob"]["b_ada_final"] = W["glob"]["b_ada_final"].reshape(2, -1)[::-1].reshape(-1).copy()
+    lay2 = dict(lay, tags=(1 - lay["tags"]).astype(np.uint8))
+    out2, _ = oracle.forward(TINY_RMS, W, x, lay2, 0.3)
+    assert np.array_equal(out, out2)
+
+
+def test_forward_thread_count_does_not_change_bits():
+    w = synth.WORKLOADS["ragged"]
+    w = dict(w, model=dict(w["model"], n_blocks=1))
+    lay = synth.build_layout(w["docs"][:2])
+    W = synth.make_weights(w)
+    x = synth.make_tokens(w, lay)
+    oracle.set_threads(1)
+    a, _ = oracle.forward(w["model"], W, x, lay, 0.37)
+    oracle.set_threads(4)
+    b, _ = oracle.forward(w["model"], W, x, lay, 0.37)
+    oracle.set_threads(1)
+    assert np.array_equal(a, b)
