@@ -1,0 +1,281 @@
+/*
+ * dit.h -- C ABI of libdit.so: the forward pass of a non-causal joint video+audio diffusion
+ * transformer (DiT) over a packed variable-length token sequence, and the rectified-flow Euler
+ * step of the denoise loop around it, on one NVIDIA GB300 (sm_103a).
+ *
+ * Sources, cited as page title then section:
+ *   [H3] "feat(minimax-h3): port the MiniMax-H3 omni-modal video+audio DiT"
+ *   [M3] "feat(MODEL-MUSIC-MUSIC3): the 2.4B fp32 DiT onto the device, staged once"
+ *   [BF] "feat(minimax-h3): stream the ORIGINAL bf16 DiT to the device, one tensor at a time"
+ *
+ * Conventions shared by every call:
+ *   - Array arguments are DEVICE pointers owned by the caller unless the name ends in _host.
+ *     Nothing here frees or retains a caller pointer beyond the call, except bound weights
+ *     (dit_bind_weights), which must outlive the handle.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  All device
+ *     work is enqueued on it; no call synchronises the device unless it says so.
+ *   - Errors are return codes only: no exception, abort or exit crosses this boundary.  Host-side
+ *     validation happens before any launch, so a call that returns an error launched nothing.
+ *     Device-side failures (an invalid packed layout, a bounded wait that ran out) are recorded in
+ *     a device status word and are read back by dit_get_stats / dit_sync_status.
+ *   - Row-major everywhere.  A linear map's weight is [out, in] (the "MatmulBT" convention of
+ *     [M3] "What moved": Y = X W^T).
+ */
+#ifndef DIT_H_
+#define DIT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DIT_API __attribute__((visibility("default")))
+#else
+#define DIT_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DIT_OK = 0,
+  DIT_ERR_INVALID_ARG = 1,    /* null / misaligned pointer, negative size, bad enum */
+  DIT_ERR_CONFIG = 2,         /* a dit_config field out of the supported range */
+  DIT_ERR_UNBOUND = 3,        /* dit_forward before dit_bind_weights */
+  DIT_ERR_MISSING_WEIGHT = 4, /* a required weight pointer is NULL; dit_last_error names it */
+  DIT_ERR_LAYOUT = 5,         /* packed layout rejected (host checks, or the device validator) */
+  DIT_ERR_CAPACITY = 6,       /* n_tokens > max_tokens, n_docs > max_docs, workspace too small */
+  DIT_ERR_CUDA = 7,           /* a CUDA runtime call failed; dit_last_error has its message */
+  DIT_ERR_DEVICE_TIMEOUT = 8, /* a kernel's bounded wait ran out; the kernel exited cleanly */
+  DIT_ERR_UNSUPPORTED = 9     /* shape outside what the kernels tile (see dit_create) */
+} dit_status;
+
+enum { DIT_RMSNORM = 0, DIT_LAYERNORM = 1 };
+enum { DIT_BF16 = 0, DIT_FP32 = 1 };
+
+/* Model configuration.  [H3] "The device-resident forward (W2b)" for the modality-indexed AdaLN
+ * DiT (adaln = 1, RMSNorm); [M3] "What moved" for the music DiT (adaln = 0, LayerNorm, partial
+ * rotary, 1x1 pre/post convolutions). */
+typedef struct {
+  int n_blocks;       /* L */
+  int hidden;         /* d */
+  int n_heads;        /* H */
+  int head_dim;       /* Dh, H * Dh == d */
+  int ffn_hidden;     /* F: the FFN computes value * silu(gate) over an up projection 2F wide */
+  int norm;           /* DIT_RMSNORM (no affine) | DIT_LAYERNORM (gain + shift) */
+  float norm_eps;
+  int adaln;          /* 1: modality-indexed AdaLN modulate + gated residuals; 0: plain residuals */
+  int n_modalities;   /* tags index [0, n_modalities): 0 = video, 1 = audio */
+  int t_embed_dim;    /* width of the sinusoidal timestep embedding (even) */
+  int rope_axes;      /* 3 (t, h, w) or 1 (t) */
+  int rope_dims[3];   /* rotary width per axis, in dims (even); their sum is rotary_dim */
+  int rotary_dim;     /* R <= head_dim: NeoX rotate_half on the first R dims of each head */
+  double rope_base;   /* inverse frequency base (10000) */
+  int io_channels;    /* 0, or the channel count of 1x1 pre/post convolutions around the stack */
+  int dtype;          /* DIT_BF16 (bf16 weights and GEMM operands, fp32 residual) | DIT_FP32 */
+  int max_tokens;     /* capacity: largest n_tokens a forward may pass */
+  int max_docs;       /* capacity: largest n_docs a forward may pass */
+} dit_config;
+
+/* One block's weights (device pointers, dtype = cfg.dtype; biases may be NULL = zero).
+ *   w_qkv  [3d, d]   fused rows in the order [q_all | k_all | v_all], heads contiguous
+ *                    ([H3] "Update: video-VAE decoder block ported": the DiT's fused qkv order)
+ *   w_o    [d, d]
+ *   w_in   [2F, d]   rows 0..F-1 the value, rows F..2F-1 the gate ([M3] "Correctness")
+ *   w_down [d, F]
+ *   w_ada  [n_mod * 6d, t_embed_dim]  per modality six d-wide chunks:
+ *          shift1, scale1, gate1, shift2, scale2, gate2           (adaln = 1 only)
+ *   ln1_g/ln1_b/ln2_g/ln2_b [d]                                     (LayerNorm only) */
+typedef struct {
+  const void *w_qkv, *b_qkv, *w_o, *b_o, *w_in, *b_in, *w_down, *b_down;
+  const void *w_ada, *b_ada;
+  const void *ln1_g, *ln1_b, *ln2_g, *ln2_b;
+} dit_block_weights;
+
+/* All weights.  `blocks` is a HOST array of n_blocks entries (read during the call only).
+ *   w_ada_final [n_mod * 2d, t_embed_dim]: shift_f, scale_f        (adaln = 1)
+ *   lnf_g, lnf_b [d]                                                 (LayerNorm)
+ *   w_pre [d, io], w_post [io, d] with biases b_pre [d], b_post [io] (io_channels > 0) */
+typedef struct {
+  int n_blocks;
+  const dit_block_weights* blocks;
+  const void *w_ada_final, *b_ada_final;
+  const void *lnf_g, *lnf_b;
+  const void *w_pre, *b_pre, *w_post, *b_post;
+} dit_weights;
+
+typedef struct {
+  int64_t forwards;             /* dit_forward calls that launched work */
+  int64_t kernels_launched;     /* every kernel this handle launched */
+  int64_t gemm_launches, attention_launches, norm_launches, other_launches;
+  int64_t attention_tiles;      /* (q-tile, head) work items of the last forward (device count) */
+  int64_t bound_bytes;          /* bytes of library-owned repacked weight copies */
+  int32_t device_status;        /* last status word read back (0 = ok) */
+  int32_t last_layout_error;    /* device validator's code for the last forward (0 = ok) */
+} dit_stats;
+
+typedef struct dit_handle dit_handle;
+
+/* ---------------------------------------------------------------------------------------------
+ * Model-level calls
+ * ------------------------------------------------------------------------------------------- */
+
+/* Validate `cfg` and create a handle.  No device memory is allocated here.
+ * What the kernels tile: dtype DIT_BF16 with adaln = 1 and RMSNorm; hidden a multiple of 256 with
+ * hidden / 128 in {1..6, 8, 10, 12, 16, 20, 24, 32, 40, 48, 64}; head_dim 64 or 128; ffn_hidden a
+ * multiple of 128; rotary_dim / 2 and head_dim - rotary_dim multiples of 16; t_embed_dim a
+ * multiple of 8 (of 256 above 256); io_channels 0.  Anything else returns DIT_ERR_CONFIG (not a
+ * valid model) or DIT_ERR_UNSUPPORTED (valid, not tiled), dit_last_error(NULL) naming the field. */
+DIT_API dit_status dit_create(const dit_config* cfg, dit_handle** out);
+
+/* Release the handle and its repacked weight copies (synchronises the device first). */
+DIT_API dit_status dit_destroy(dit_handle* h);
+
+/* Message for the last error on this handle (h may be NULL for dit_create's error). */
+DIT_API const char* dit_last_error(const dit_handle* h);
+
+/* Bytes of caller-provided device workspace a forward of n_tokens tokens in n_docs documents needs
+ * (activations, cos/sin cache, tile schedule, status word).  0 when cfg is invalid. */
+DIT_API size_t dit_workspace_bytes(const dit_config* cfg, int n_tokens, int n_docs);
+
+/* Bind the weights once ([M3] "Speed": staged once, never per forward).  Non-owning: the caller's
+ * tensors must stay alive and unchanged while the handle is used.  The library makes these
+ * repacked copies on the device (enqueued on `stream`, owned by the handle): fp32 biases, the
+ * FFN up projection with value/gate rows interleaved per 128 features (the stage-time half swap of
+ * [M3] "What moved"), and every block's AdaLN matrix concatenated into one.  The first NULL
+ * required pointer returns DIT_ERR_MISSING_WEIGHT and dit_last_error names it ([H3] "Update:
+ * quantized arms land": missing tensors are reported by name). */
+DIT_API dit_status dit_bind_weights(dit_handle* h, const dit_weights* w, void* stream);
+
+/* One DiT forward.  [H3] "The device-resident forward (W2b)": every activation stays on the
+ * device; the block stack never round-trips through the host.
+ *   x_tokens      fp32 [n_tokens, d] token-major (io_channels > 0: channel-major per document,
+ *                 [io, len_j] blocks back to back)
+ *   cu_seqlens    int32 [n_docs + 1], cu[0] = 0, strictly increasing, cu[n_docs] = n_tokens
+ *   doc_ids       int32 [n_tokens], doc_ids[i] = j for cu[j] <= i < cu[j+1]
+ *   modality_tags uint8 [n_tokens], < n_modalities
+ *   pos_thw       fp64 [n_tokens, 3] (t, h, w) position grid ([H3] "Correctness gates")
+ *   timestep      the flow time t = sigma in [0, 1]
+ *   out           fp32, same layout and size as x_tokens (may not alias x_tokens)
+ *   workspace     device buffer of at least dit_workspace_bytes(cfg, n_tokens, n_docs) bytes,
+ *                 256-byte aligned; its contents on entry are ignored.
+ * Attention is block-diagonal over cu_seqlens and non-causal ([H3] "Correctness gates":
+ * DFlashBlockAttention(causal=false)); no mask tensor exists.  Asynchronous on `stream`.  The
+ * device validator checks doc_ids/tags against cu_seqlens; if it rejects the layout every later
+ * kernel of the forward returns early and the status word reads DIT_ERR_LAYOUT. */
+DIT_API dit_status dit_forward(dit_handle* h, const float* x_tokens, const int32_t* cu_seqlens, int n_docs,
+                       const int32_t* doc_ids, const uint8_t* modality_tags, const double* pos_thw, int n_tokens,
+                       float timestep, float* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* The same forward from HOST buffers: copies the inputs in (cudaMemcpyAsync, one per array),
+ * runs dit_forward and copies `out_host` back, all on `stream`, then synchronises the stream.
+ * Use pinned host memory for full copy speed.  workspace must hold
+ * dit_workspace_bytes_host(cfg, n_tokens, n_docs) bytes (forward workspace + staging). */
+DIT_API size_t dit_workspace_bytes_host(const dit_config* cfg, int n_tokens, int n_docs);
+DIT_API dit_status dit_forward_host(dit_handle* h, const float* x_host, const int32_t* cu_host, int n_docs,
+                            const int32_t* doc_ids_host, const uint8_t* tags_host, const double* pos_host,
+                            int n_tokens, float timestep, float* out_host, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/* One Euler-ancestral (eta = 0) step of the rectified flow, in place on x, fp32, in this exact
+ * order with no fused multiply-add ([H3] "Correctness gates": euler-ancestral eta0 scheduler +
+ * rf_v_to_x0, gated exact):
+ *   x0 = x - sigma * v;   x <- x0 + (sigma_next * (x - x0)) / sigma
+ * x, v: fp32 [n] device.  sigma must be > 0.  Bit-identical to the same IEEE fp32 sequence on a
+ * CPU.  Stateless: resuming a loop at step k with the saved x gives the uninterrupted result. */
+DIT_API dit_status dit_euler_step(float* x, const float* v, int64_t n, float sigma, float sigma_next, void* stream);
+
+/* Counters (asserted by the tests) and the device status word.  dit_sync_status synchronises
+ * `stream`, reads the status word of `workspace` (the one the last forward used) and returns it
+ * as a dit_status. */
+DIT_API dit_status dit_get_stats(const dit_handle* h, dit_stats* out);
+DIT_API dit_status dit_sync_status(dit_handle* h, const void* workspace, void* stream);
+
+/* Per-block dumps for parity tests: when `dump` is non-NULL each later forward copies the fp32
+ * residual after block l into dump + l * n_tokens * d (device, caller-owned, L * N * d floats). */
+DIT_API dit_status dit_set_dump(dit_handle* h, float* dump);
+
+/* Per-kernel-kind timing with CUDA events recorded on the forward's stream around every launch.
+ * enable = 1 starts collecting (events are created lazily); dit_get_kernel_times synchronises and
+ * returns, per kind, the summed milliseconds and launch count since the last reset.
+ * Kinds: 0 gemm_qkv, 1 attention, 2 gemm_out, 3 gemm_ffn_up, 4 gemm_ffn_down, 5 norm_modulate,
+ *        6 other (schedule, cos/sin cache, AdaLN, copies). */
+#define DIT_KERNEL_KINDS 7
+DIT_API dit_status dit_set_kernel_timing(dit_handle* h, int enable);
+DIT_API dit_status dit_get_kernel_times(dit_handle* h, double* ms_out, int64_t* launches_out);
+
+/* ---------------------------------------------------------------------------------------------
+ * Op-level calls: each runs one kernel of the forward on caller buffers, for parity testing and
+ * for composing the forward differently.  Shapes and layouts are those the forward uses.
+ * ------------------------------------------------------------------------------------------- */
+
+/* Norm + indexed AdaLN modulate ([H3] "The device-resident forward (W2b)"):
+ *   y[r] = N(x[r]) * (1 + scale[tag[r]]) + shift[tag[r]]
+ * N = RMSNorm x / sqrt(mean(x^2) + eps) (norm = DIT_RMSNORM) or LayerNorm with gain/shift ln_g,
+ * ln_b (DIT_LAYERNORM).  x fp32 [n, d]; shift/scale fp32 rows of d values, row m at
+ * shift + m * mod_stride (NULL shift and scale = no modulation); tags uint8 [n] (may be NULL
+ * when shift is NULL).  Output bf16 bits [n, d] (out_kind 0) or fp32 [n, d] (out_kind 1).
+ * Requires d % 128 == 0 and d <= 8192. */
+DIT_API dit_status dit_op_norm_modulate(const float* x, int n, int d, int norm, float eps, const float* ln_g,
+                                const float* ln_b, const uint8_t* tags, const float* shift, const float* scale,
+                                int64_t mod_stride, void* y, int out_kind, void* stream);
+
+/* Per-row RoPE cos/sin cache from the fp64 grid ([BF] "What this enables": BuildRopeCosSin;
+ * [H3] "The device-resident forward (W2b)": a per-row cos/sin cache fed from three axes of the
+ * fp64 position grid).  inv[k] of axis a = (float) base^(-2k/dims[a]); theta = pos[r][axis] * inv
+ * in fp64; cos/sin in fp64, stored fp32 [n, rotary_dim/2] with the axis blocks concatenated. */
+DIT_API dit_status dit_op_rope_cache(const double* pos, int n, int n_axes, const int* dims_host, double base,
+                             float* cos_out, float* sin_out, void* stream);
+
+/* AdaLN conditioning: e = [cos(1000 t f_k) | sin(1000 t f_k)], f_k = exp(-ln(1e4) k / (t_dim/2));
+ * mod[r] = W[r] . silu(e) + b[r] for r < rows.  W bf16 bits [rows, t_dim], b fp32 [rows] or NULL,
+ * mod fp32 [rows].  t_dim % 256 == 0 or t_dim in {64, 128}. */
+DIT_API dit_status dit_op_adaln(const void* w, const float* b, int rows, int t_dim, float t, float* mod, void* stream);
+
+/* GEMM D = A B^T on the tcgen05 tensor cores, bf16 operands, fp32 accumulation in TMEM.
+ * A bf16 [M, K] row-major, B bf16 [N, K] row-major (the weight), bias fp32 [N] or NULL.
+ * M >= 1 any; N % 256 == 0; K % 64 == 0; A, B 16-byte aligned.  Epilogues:
+ *   dit_op_gemm            out = A B^T + bias, stored bf16 bits (out_kind 0) or fp32 (1), [M, N]
+ *   dit_op_gemm_qkv_rope   N = 3d: q, k get bias + NeoX rotate_half with cos/sin [M, R/2] on the
+ *                          first R dims of each Dh-wide head and are stored bf16 [M, d]; v is
+ *                          stored TRANSPOSED, vt bf16 [d, n_pad] (vt[c * n_pad + row]),
+ *                          n_pad >= M, n_pad % 8 == 0.
+ *   dit_op_gemm_gated_residual  x[M, N] (fp32, in place) += gate[tag[r]] * (A B^T + bias);
+ *                          gate rows at gate + m * gate_stride (NULL gate = plain residual add).
+ *   dit_op_gemm_swiglu     B, bias in the interleaved layout of dit_op_pack_ffn_in (2F rows);
+ *                          h bf16 [M, F] = (u + b_u) * silu(g + b_g). */
+DIT_API dit_status dit_op_gemm(const void* a, const void* b, const float* bias, int M, int N, int K, void* out, int out_kind,
+                       void* stream);
+DIT_API dit_status dit_op_gemm_qkv_rope(const void* a, const void* b, const float* bias, int M, int d, int K, int n_heads,
+                                int head_dim, int rotary_dim, const float* cos_cache, const float* sin_cache,
+                                void* q, void* k, void* vt, int n_pad, void* stream);
+DIT_API dit_status dit_op_gemm_gated_residual(const void* a, const void* b, const float* bias, int M, int N, int K,
+                                      float* x, const float* gate, int64_t gate_stride, const uint8_t* tags,
+                                      void* stream);
+DIT_API dit_status dit_op_gemm_swiglu(const void* a, const void* b_packed, const float* bias_packed, int M, int F, int K,
+                              void* h, void* stream);
+
+/* Interleave an FFN up projection [2F, d] (value rows then gate rows) into 128-feature groups:
+ * packed rows [256 g, 256 g + 128) = value rows [128 g, +128), the next 128 = the gate rows
+ * [F + 128 g, +128).  bias (fp32 [2F] or NULL) is interleaved the same way into bias_packed
+ * (fp32 [2F]; zeros when bias is NULL).  F % 128 == 0. */
+DIT_API dit_status dit_op_pack_ffn_in(const void* w_in, const float* b_in, int F, int d, void* w_packed, float* b_packed,
+                              void* stream);
+
+/* Varlen non-causal flash attention on the tcgen05 tensor cores ([H3] "Correctness gates":
+ * DFlashBlockAttention(causal=false) over the packed sequence; [M3] "What moved": non-causal,
+ * no bias).  Per document [cu[j], cu[j+1]) and head h:  o_i = softmax_j(q_i . k_j / sqrt(Dh)) v_j.
+ *   q, k  bf16 [n_tokens, H * Dh];  vt bf16 [H * Dh, n_pad] (n_pad % 8 == 0, n_pad >= n_tokens)
+ *   o     bf16 [n_tokens, H * Dh]
+ * head_dim is 64 or 128.  The (document, 128-row q-tile) list is built on the device from cu_seqlens
+ * into `workspace` (dit_attention_workspace_bytes(n_docs, n_tokens) bytes). */
+DIT_API size_t dit_attention_workspace_bytes(int n_docs, int n_tokens);
+DIT_API dit_status dit_op_attention(const void* q, const void* k, const void* vt, int n_pad, const int32_t* cu_seqlens,
+                            int n_docs, int n_tokens, int n_heads, int head_dim, void* o, void* workspace,
+                            void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DIT_H_ */

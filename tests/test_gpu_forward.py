@@ -1,0 +1,234 @@
+"""Whole-forward parity through the C ABI, against the oracle on the same seeded inputs, plus the
+forward's invariants and its error paths."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+# Gate from the bf16 stream's tolerance: every block output within 3e-3 of its RMS.
+GATE = 3e-3
+# Stricter gate on each block's update x_out - x_in, which the residual otherwise dwarfs: the bf16
+# GEMM operands put ~2^-9 relative noise on every product, so the update may differ by a few
+# percent of its own magnitude, never by its size.
+DELTA_MAX = 0.08
+DELTA_RMS = 0.02
+
+
+def _gu():
+    from tests import gpu_util
+    return gpu_util
+
+
+def _dit():
+    from video_audio_gen_gb300 import dit
+    return dit
+
+
+def check_against_oracle(w, run, ref_out, ref_dumps):
+    x_in = run["x"].astype(np.float64)
+    prev_g, prev_o = x_in, x_in
+    for l in range(w["model"]["n_blocks"]):
+        g, o = run["dumps"][l], ref_dumps[l]
+        rms = np.sqrt((o ** 2).mean())
+        assert np.abs(g - o).max() <= GATE * rms, (l, np.abs(g - o).max() / rms)
+        dg, do = g - prev_g, o - prev_o
+        err = dg - do
+        assert np.abs(err).max() <= DELTA_MAX * np.abs(do).max(), (l, np.abs(err).max() / np.abs(do).max())
+        assert np.sqrt((err ** 2).mean()) <= DELTA_RMS * np.sqrt((do ** 2).mean())
+        prev_g, prev_o = g, o
+    rms = np.sqrt((ref_out ** 2).mean())
+    assert np.isfinite(run["out"]).all()
+    assert np.abs(run["out"] - ref_out).max() <= GATE * rms
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged"])
+def test_forward_matches_oracle(name):
+    gu = _gu()
+    w = synth.WORKLOADS[name]
+    run = gu.run_forward(w, dumps=True)
+    assert run["status"] == 0
+    oracle.set_threads(8)
+    ref, dumps = oracle.forward(w["model"], run["weights"], run["x"], run["layout"], run["t"], dumps=True)
+    oracle.set_threads(1)
+    check_against_oracle(w, run, ref, dumps)
+
+
+def test_forward_counters_and_tiles():
+    """The CUDA path ran: launch counters and the device tile count are asserted, not printed."""
+    gu = _gu()
+    w = synth.WORKLOADS["ragged"]
+    run = gu.run_forward(w)
+    st = run["stats"]
+    L = w["model"]["n_blocks"]
+    assert st["forwards"] == 1
+    assert st["gemm_launches"] == 4 * L and st["attention_launches"] == L and st["norm_launches"] == 2 * L + 1
+    assert st["attention_tiles"] == oracle.count_q_tiles(run["layout"]["cu_seqlens"]) * w["model"]["n_heads"]
+    assert st["device_status"] == 0 and st["last_layout_error"] == 0
+
+
+def test_segmentation_bit_identity():
+    """Perturbing one document's tokens leaves every output row of the other documents bit-identical."""
+    gu = _gu()
+    w = synth.WORKLOADS["ragged"]
+    lay = synth.build_layout(w["docs"])
+    W = synth.make_weights(w)
+    x = synth.make_tokens(w, lay)
+    r1 = gu.run_forward(w, layout=lay, weights=W, x=x)
+    cu = lay["cu_seqlens"]
+    x2 = x.copy()
+    x2[cu[1]:cu[2]] += synth.normal(5, "perturb", (cu[2] - cu[1], x.shape[1]), 0.5)
+    r2 = gu.run_forward(w, layout=lay, weights=W, x=x2, handle=r1["handle"])
+    other = np.ones(lay["n_tokens"], dtype=bool)
+    other[cu[1]:cu[2]] = False
+    assert np.array_equal(r1["out"][other], r2["out"][other])
+    assert not np.array_equal(r1["out"][~other], r2["out"][~other])
+
+
+def test_forward_host_equals_device_forward():
+    gu = _gu()
+    w = synth.WORKLOADS["tiny"]
+    run = gu.run_forward(w)
+    h, lay = run["handle"], run["layout"]
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    out = torch.empty(run["x"].shape, dtype=torch.float32).pin_memory()
+    ws = gu.workspace(h, lay["n_tokens"], lay["n_docs"], host=True)
+    h.forward_host(pin(run["x"]), pin(lay["cu_seqlens"].astype(np.int32)), pin(lay["doc_ids"].astype(np.int32)),
+                   pin(lay["tags"]), pin(lay["pos"]), run["t"], out, ws)
+    assert np.array_equal(out.double().numpy(), run["out"])
+
+
+def test_device_validator_rejects_bad_layout():
+    """A doc id that disagrees with cu_seqlens: the forward's kernels skip their work and the status
+    word reads DIT_ERR_LAYOUT with the same code the oracle's layout check gives."""
+    dit, gu = _dit(), _gu()
+    w = synth.WORKLOADS["tiny"]
+    lay = synth.build_layout(w["docs"])
+    W = synth.make_weights(w)
+    h = gu.make_handle(w["model"], lay, W)
+    bad = dict(lay)
+    bad["doc_ids"] = lay["doc_ids"].copy()
+    bad["doc_ids"][100] = 0
+    code = oracle.check_layout(bad["cu_seqlens"], bad["doc_ids"], bad["tags"], lay["n_tokens"], 2)
+    assert code == 5
+    dl = gu.dev_layout(bad)
+    x = gu.dev_f32(synth.make_tokens(w, lay))
+    out = torch.full_like(x, 7.0)
+    ws = gu.workspace(h, lay["n_tokens"], lay["n_docs"])
+    h.forward(x, dl["cu"], dl["ids"], dl["tags"], dl["pos"], 0.5, out, ws)
+    assert h.sync_status(ws) == dit.DIT_ERR_LAYOUT
+    assert h.stats()["last_layout_error"] == code
+    assert (out == 7.0).all()  # nothing was written
+    bad_tags = dict(lay)
+    bad_tags["tags"] = lay["tags"].copy()
+    bad_tags["tags"][5] = 9
+    dl = gu.dev_layout(bad_tags)
+    h.forward(x, dl["cu"], dl["ids"], dl["tags"], dl["pos"], 0.5, out, ws)
+    assert h.sync_status(ws) == dit.DIT_ERR_LAYOUT and h.stats()["last_layout_error"] == 6
+    # and a good layout afterwards runs normally on the same handle and workspace
+    dl = gu.dev_layout(lay)
+    h.forward(x, dl["cu"], dl["ids"], dl["tags"], dl["pos"], 0.5, out, ws)
+    assert h.sync_status(ws) == dit.DIT_OK
+
+
+def test_host_validation_errors_launch_nothing():
+    dit, gu = _dit(), _gu()
+    w = synth.WORKLOADS["tiny"]
+    lay = synth.build_layout(w["docs"])
+    W = synth.make_weights(w)
+    h = gu.make_handle(w["model"], lay, W)
+    dl = gu.dev_layout(lay)
+    x = gu.dev_f32(synth.make_tokens(w, lay))
+    out = torch.empty_like(x)
+    ws = gu.workspace(h, lay["n_tokens"], lay["n_docs"])
+    before = h.stats()["kernels_launched"]
+    with pytest.raises(dit.DitError) as e:
+        h.forward(x, dl["cu"], dl["ids"], dl["tags"], dl["pos"], 0.5, out, ws[:1024])
+    assert e.value.status == dit.DIT_ERR_CAPACITY
+    with pytest.raises(dit.DitError) as e:
+        h.forward(x, dl["cu"], dl["ids"], dl["tags"], dl["pos"], 0.5, x, ws)
+    assert e.value.status == dit.DIT_ERR_INVALID_ARG
+    assert h.stats()["kernels_launched"] == before
+
+
+def test_missing_weight_is_named():
+    dit, gu = _dit(), _gu()
+    w = synth.WORKLOADS["tiny"]
+    W = synth.make_weights(w)
+    blocks, glob = gu.upload_weights(W, True)
+    blocks[1]["w_down"] = None
+    h = dit.Dit(w["model"], 256, 2)
+    with pytest.raises(dit.DitError) as e:
+        h.bind_weights(blocks, glob)
+    assert e.value.status == dit.DIT_ERR_MISSING_WEIGHT and "blocks[1].w_down" in str(e.value)
+    x = torch.zeros((256, 256), device="cuda")
+    with pytest.raises(dit.DitError) as e:
+        h.forward(x, torch.zeros(3, dtype=torch.int32, device="cuda"), torch.zeros(256, dtype=torch.int32, device="cuda"),
+                  torch.zeros(256, dtype=torch.uint8, device="cuda"), torch.zeros((256, 3), dtype=torch.float64,
+                                                                                device="cuda"),
+                  0.5, torch.empty_like(x), torch.empty(1 << 20, dtype=torch.uint8, device="cuda"))
+    assert e.value.status == dit.DIT_ERR_UNBOUND
+
+
+# ------------------------------------------------------------------------------------------------
+# the denoise loop
+# ------------------------------------------------------------------------------------------------
+
+LOOP_SMALL = dict(model=dict(synth.WORKLOADS["ragged"]["model"], hidden=256, n_heads=2, ffn_hidden=1024),
+                  seed=44, docs=[dict(video=(2, 8, 16), audio=64), dict(video=(1, 8, 16), audio=64)],
+                  t="schedule", steps=50, w_std=0.02, bias_std=0.0, x_std=1.0)
+
+
+def _gpu_loop(h, lay, x0, sig, start=0, stop=None, x_from=None):
+    dit, gu = _dit(), _gu()
+    dl = gu.dev_layout(lay)
+    x = gu.dev_f32(x0 if x_from is None else x_from)
+    v = torch.empty_like(x)
+    ws = gu.workspace(h, lay["n_tokens"], lay["n_docs"])
+    stop = len(sig) - 1 if stop is None else stop
+    for i in range(start, stop):
+        h.forward(x, dl["cu"], dl["ids"], dl["tags"], dl["pos"], float(sig[i]), v, ws)
+        dit.euler_step(x, v, float(sig[i]), float(sig[i + 1]))
+    assert h.sync_status(ws) == 0
+    return x.cpu().numpy()
+
+
+@pytest.mark.slow
+def test_denoise_loop_matches_oracle_reduced():
+    """50 Euler steps on a reduced copy of the two-request loop, every forward and step on the GPU,
+    against the same 50 steps in the oracle."""
+    gu = _gu()
+    w = LOOP_SMALL
+    lay = synth.build_layout(w["docs"])
+    W = synth.make_weights(w)
+    x0 = synth.make_tokens(w, lay)
+    sig = synth.sigmas(50)
+    h = gu.make_handle(w["model"], lay, W)
+    xg = _gpu_loop(h, lay, x0, sig)
+    oracle.set_threads(8)
+    xo = x0.copy()
+    for i in range(50):
+        v, _ = oracle.forward(w["model"], W, xo, lay, float(sig[i]))
+        xo = oracle.euler_step(xo, v.astype(np.float32), sig[i], sig[i + 1])
+    oracle.set_threads(1)
+    rms = np.sqrt((xo.astype(np.float64) ** 2).mean())
+    assert np.abs(xg.astype(np.float64) - xo).max() <= GATE * rms
+
+
+def test_denoise_loop_resume_is_bit_identical():
+    """The loop state is x alone: stopping after step k and resuming from the saved x reproduces the
+    uninterrupted run bit for bit."""
+    gu = _gu()
+    w = LOOP_SMALL
+    lay = synth.build_layout(w["docs"])
+    W = synth.make_weights(w)
+    x0 = synth.make_tokens(w, lay)
+    sig = synth.sigmas(50)
+    h = gu.make_handle(w["model"], lay, W)
+    full = _gpu_loop(h, lay, x0, sig, 0, 6)
+    part = _gpu_loop(h, lay, x0, sig, 0, 3)
+    resumed = _gpu_loop(h, lay, x0, sig, 3, 6, x_from=part)
+    assert np.array_equal(full.view(np.uint32), resumed.view(np.uint32))

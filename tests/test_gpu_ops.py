@@ -1,0 +1,349 @@
+"""Kernel-level parity: each CUDA op of the forward, called through the C ABI, against the oracle
+on the same seeded inputs.  Sizes span several tiles with ragged tails; bounds are derived from the
+arithmetic (fp32 accumulation, one bf16 rounding of the stored result)."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+BF16_REL = 2.0 ** -8   # one bf16 rounding (2^-9) with a factor 2 of headroom
+
+
+def _dit():
+    from video_audio_gen_gb300 import dit
+    return dit
+
+
+def _gu():
+    from tests import gpu_util
+    return gpu_util
+
+
+def bf16_to_f64(t):
+    return t.float().double().cpu().numpy()
+
+
+def fp32_sum_bound(a, b):
+    """Elementwise bound on the error of an fp32-accumulated dot product: K * 2^-23 * sum|a||b|."""
+    K = a.shape[1]
+    return K * 2.0 ** -23 * (np.abs(a) @ np.abs(b).T)
+
+
+# ------------------------------------------------------------------------------------------------
+# norm + modulate
+# ------------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n,d", [(1, 256), (333, 512), (130, 3072), (77, 5120)])
+def test_rms_norm_modulate_matches_oracle(n, d):
+    dit, gu = _dit(), _gu()
+    x = synth.normal(31, "x", (n, d), 2.0)
+    tags = (synth.uniform(31, "tags", n) < 0.3).astype(np.uint8)
+    shift = synth.normal(31, "sh", (2, d), 0.2)
+    scale = synth.normal(31, "sc", (2, d), 0.2)
+    ref = oracle.modulate(oracle.rms_norm(x, 1e-6), tags, shift, scale)
+    xd = gu.dev_f32(x)
+    y = torch.empty((n, d), dtype=torch.bfloat16, device="cuda")
+    dit.norm_modulate(xd, dit.DIT_RMSNORM, 1e-6, y, 0, tags=torch.from_numpy(tags).cuda(),
+                      shift=gu.dev_f32(shift), scale=gu.dev_f32(scale), mod_stride=d)
+    got = bf16_to_f64(y)
+    assert np.all(np.abs(got - ref) <= BF16_REL * np.abs(ref) + 1e-5)
+    yf = torch.empty((n, d), dtype=torch.float32, device="cuda")
+    dit.norm_modulate(xd, dit.DIT_RMSNORM, 1e-6, yf, 1, tags=torch.from_numpy(tags).cuda(),
+                      shift=gu.dev_f32(shift), scale=gu.dev_f32(scale), mod_stride=d)
+    gotf = yf.double().cpu().numpy()
+    assert np.abs(gotf - ref).max() <= 1e-5 * np.abs(ref).max()
+
+
+def test_norm_without_modulation_is_bare_rms():
+    dit, gu = _dit(), _gu()
+    x = synth.normal(32, "x", (200, 768), 1.5)
+    yf = torch.empty((200, 768), dtype=torch.float32, device="cuda")
+    dit.norm_modulate(gu.dev_f32(x), dit.DIT_RMSNORM, 1e-6, yf, 1)
+    ref = oracle.rms_norm(x, 1e-6)
+    assert np.abs(yf.double().cpu().numpy() - ref).max() <= 1e-5 * np.abs(ref).max()
+
+
+def test_layer_norm_affine_matches_oracle():
+    dit, gu = _dit(), _gu()
+    x = synth.normal(33, "x", (150, 2048), 1.0) + 0.5
+    g = 1.0 + synth.normal(33, "g", (2048,), 0.1)
+    b = synth.normal(33, "b", (2048,), 0.1)
+    yf = torch.empty((150, 2048), dtype=torch.float32, device="cuda")
+    dit.norm_modulate(gu.dev_f32(x), dit.DIT_LAYERNORM, 1e-5, yf, 1, ln_g=gu.dev_f32(g), ln_b=gu.dev_f32(b))
+    ref = oracle.layer_norm(x, 1e-5, g, b)
+    assert np.abs(yf.double().cpu().numpy() - ref).max() <= 2e-5 * np.abs(ref).max()
+
+
+# ------------------------------------------------------------------------------------------------
+# cos/sin cache, AdaLN conditioning
+# ------------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["tiny", "video_audio_bf16", "ragged"])
+def test_rope_cache_matches_oracle(name):
+    dit, gu = _dit(), _gu()
+    w = synth.WORKLOADS[name]
+    m = w["model"]
+    lay = synth.build_layout(w["docs"])
+    half = m["rotary_dim"] // 2
+    cs = torch.empty((lay["n_tokens"], half), dtype=torch.float32, device="cuda")
+    sn = torch.empty_like(cs)
+    dit.rope_cache(gu.dev_layout(lay)["pos"], m["rope_axes"], m["rope_dims"], m["rope_base"], cs, sn)
+    rc, rs = oracle.rope_cos_sin(m, lay["pos"])
+    gc, gs = cs.cpu().numpy(), sn.cpu().numpy()
+    # fp64 cos/sin rounded once to fp32: equal to the oracle's rounding, up to one fp32 ulp where the
+    # two fp64 libraries round the last bit differently
+    ulp = np.spacing(np.float32(1.0))
+    assert np.abs(gc - rc).max() <= ulp and np.abs(gs - rs).max() <= ulp
+    assert (gc == rc.astype(np.float32)).mean() > 0.999 and (gs == rs.astype(np.float32)).mean() > 0.999
+
+
+def test_adaln_matches_oracle():
+    dit, gu = _dit(), _gu()
+    w = synth.WORKLOADS["tiny"]
+    m = w["model"]
+    W = synth.make_weights(w)
+    # give the projection non-zero biases so the bias path is exercised
+    for l, b in enumerate(W["blocks"]):
+        b["b_ada"] = synth.normal(34, f"b{l}", b["b_ada"].shape, 0.05)
+    W["glob"]["b_ada_final"] = synth.normal(34, "bf", W["glob"]["b_ada_final"].shape, 0.05)
+    for t in (0.0, 0.5, 0.9731):
+        mod, modf = oracle.adaln(m, W, float(np.float32(t)))
+        wall = np.concatenate([b["w_ada"] for b in W["bits"]["blocks"]] + [W["bits"]["glob"]["w_ada_final"]])
+        ball = np.concatenate([b["b_ada"] for b in W["blocks"]] + [W["glob"]["b_ada_final"]])
+        out = torch.empty((wall.shape[0],), dtype=torch.float32, device="cuda")
+        dit.adaln(gu.dev_bf16(wall), gu.dev_f32(ball), t, out)
+        ref = np.concatenate([mod.reshape(-1), modf.reshape(-1)])
+        assert np.abs(out.double().cpu().numpy() - ref).max() <= 2e-5, t
+
+
+# ------------------------------------------------------------------------------------------------
+# GEMM engine and its epilogues
+# ------------------------------------------------------------------------------------------------
+
+def _ab(M, N, K, seed, std_b=0.05):
+    a, abits = synth.normal(seed, "A", (M, K), 1.0, bf16=True)
+    b, bbits = synth.normal(seed, "B", (N, K), std_b, bf16=True)
+    bias = synth.normal(seed, "bias", (N,), 0.1)
+    return a, abits, b, bbits, bias
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 256, 64), (333, 512, 512), (128, 768, 256), (1000, 1024, 1536)])
+def test_gemm_store_matches_oracle(M, N, K):
+    dit, gu = _dit(), _gu()
+    a, abits, b, bbits, bias = _ab(M, N, K, 40 + M)
+    ref = oracle.linear(a, b, bias)
+    bound = fp32_sum_bound(a.astype(np.float64), b.astype(np.float64))
+    out = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    dit.gemm(gu.dev_bf16(abits), gu.dev_bf16(bbits), gu.dev_f32(bias), out, 1)
+    got = out.double().cpu().numpy()
+    assert np.all(np.abs(got - ref) <= bound + 1e-6)
+    outb = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    dit.gemm(gu.dev_bf16(abits), gu.dev_bf16(bbits), None, outb, 0)
+    refb = oracle.linear(a, b, None)
+    assert np.all(np.abs(bf16_to_f64(outb) - refb) <= BF16_REL * np.abs(refb) + bound + 1e-6)
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged"])
+def test_gemm_qkv_rope_matches_oracle(name):
+    dit, gu = _dit(), _gu()
+    w = synth.WORKLOADS[name]
+    m = w["model"]
+    lay = synth.build_layout(w["docs"])
+    M, d, H, Dh, R = lay["n_tokens"], m["hidden"], m["n_heads"], m["head_dim"], m["rotary_dim"]
+    a, abits, b, bbits, bias = _ab(M, 3 * d, d, 50)
+    cs, sn = oracle.rope_cos_sin(m, lay["pos"])
+    qkv = oracle.linear(a, b, bias)
+    qr = oracle.rope_apply(qkv[:, :d], H, Dh, R, cs, sn)
+    kr = oracle.rope_apply(qkv[:, d:2 * d], H, Dh, R, cs, sn)
+    vr = qkv[:, 2 * d:]
+    n_pad = (M + 7) // 8 * 8
+    q = torch.empty((M, d), dtype=torch.bfloat16, device="cuda")
+    k = torch.empty_like(q)
+    vt = torch.zeros((d, n_pad), dtype=torch.bfloat16, device="cuda")
+    gcs = torch.empty((M, R // 2), dtype=torch.float32, device="cuda")
+    gsn = torch.empty_like(gcs)
+    dit.rope_cache(gu.dev_layout(lay)["pos"], m["rope_axes"], m["rope_dims"], m["rope_base"], gcs, gsn)
+    dit.gemm_qkv_rope(gu.dev_bf16(abits), gu.dev_bf16(bbits), gu.dev_f32(bias), H, Dh, R, gcs, gsn, q, k, vt, n_pad)
+    bound = fp32_sum_bound(a.astype(np.float64), b.astype(np.float64))
+    # rotation mixes two accumulators: bound both, plus fp32 cos/sin (2^-24) and the bf16 store
+    bq = bound[:, :d] + np.roll(bound[:, :d], 1, axis=1)  # generous pair bound
+    for got, ref, bb in ((bf16_to_f64(q), qr, bq), (bf16_to_f64(k), kr, bq)):
+        err = np.abs(got - ref)
+        assert np.all(err <= BF16_REL * np.abs(ref) + 2 * bb.max() + 1e-5), err.max()
+    gv = bf16_to_f64(vt)[:, :M].T
+    assert np.all(np.abs(gv - vr) <= BF16_REL * np.abs(vr) + bound[:, 2 * d:] + 1e-6)
+
+
+def test_gemm_gated_residual_matches_oracle():
+    dit, gu = _dit(), _gu()
+    M, N, K = 555, 512, 1024
+    a, abits, b, bbits, bias = _ab(M, N, K, 60)
+    x = synth.normal(60, "x", (M, N), 1.0)
+    gate = synth.normal(60, "gate", (2, N), 0.3)
+    tags = (synth.uniform(60, "tags", M) < 0.5).astype(np.uint8)
+    ref = x.astype(np.float64) + gate[tags].astype(np.float64) * oracle.linear(a, b, bias)
+    xd = gu.dev_f32(x)
+    dit.gemm_gated_residual(gu.dev_bf16(abits), gu.dev_bf16(bbits), gu.dev_f32(bias), xd, gate=gu.dev_f32(gate),
+                            gate_stride=N, tags=torch.from_numpy(tags).cuda())
+    bound = fp32_sum_bound(a.astype(np.float64), b.astype(np.float64)) * np.abs(gate[tags]) + 2 ** -23 * 4
+    assert np.all(np.abs(xd.double().cpu().numpy() - ref) <= bound + 1e-6)
+    # gate = NULL: plain residual add
+    xd2 = gu.dev_f32(x)
+    dit.gemm_gated_residual(gu.dev_bf16(abits), gu.dev_bf16(bbits), None, xd2)
+    ref2 = x.astype(np.float64) + oracle.linear(a, b, None)
+    assert np.abs(xd2.double().cpu().numpy() - ref2).max() <= 1e-4
+
+
+def test_gemm_swiglu_matches_oracle():
+    dit, gu = _dit(), _gu()
+    M, F, d = 300, 768, 512
+    a, abits, _, _, _ = _ab(M, 256, d, 70)
+    win, wbits = synth.normal(70, "win", (2 * F, d), 0.05, bf16=True)
+    bin_ = synth.normal(70, "bin", (2 * F,), 0.1)
+    ref = oracle.swiglu(oracle.linear(a, win, bin_))
+    wp = torch.empty((2 * F, d), dtype=torch.bfloat16, device="cuda")
+    bp = torch.empty((2 * F,), dtype=torch.float32, device="cuda")
+    dit.pack_ffn_in(gu.dev_bf16(wbits), gu.dev_f32(bin_), wp, bp)
+    h = torch.empty((M, F), dtype=torch.bfloat16, device="cuda")
+    dit.gemm_swiglu(gu.dev_bf16(abits), wp, bp, h)
+    got = bf16_to_f64(h)
+    uv_bound = fp32_sum_bound(a.astype(np.float64), win.astype(np.float64))
+    # |d(u silu g)| <= |silu g| du + |u| |silu'| dg with |silu'| <= 1.1
+    uv = oracle.linear(a, win, bin_)
+    u, g = uv[:, :F], uv[:, F:]
+    prop = np.abs(g) * uv_bound[:, :F] + 1.1 * np.abs(u) * uv_bound[:, F:]
+    assert np.all(np.abs(got - ref) <= BF16_REL * np.abs(ref) + prop + 1e-5 * np.abs(u) + 1e-6)
+
+
+# ------------------------------------------------------------------------------------------------
+# attention
+# ------------------------------------------------------------------------------------------------
+
+def _attn_inputs(lay, H, Dh, seed, same_keys=False):
+    n = lay["n_tokens"]
+    q, qb = synth.normal(seed, "q", (n, H * Dh), 1.0, bf16=True)
+    k, kb = synth.normal(seed, "k", (n, H * Dh), 1.0, bf16=True)
+    if same_keys:
+        k = np.tile(k[:1], (n, 1))
+        kb = np.tile(kb[:1], (n, 1))
+    v, vb = synth.normal(seed, "v", (n, H * Dh), 1.0, bf16=True)
+    return q, qb, k, kb, v, vb
+
+
+def _run_attention(lay, H, Dh, qb, kb, vb):
+    dit, gu = _dit(), _gu()
+    n = lay["n_tokens"]
+    n_pad = (n + 7) // 8 * 8
+    vt = np.zeros((H * Dh, n_pad), dtype=np.uint16)
+    vt[:, :n] = vb.T
+    o = torch.empty((n, H * Dh), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(dit.attention_workspace_bytes(lay["n_docs"], n), dtype=torch.uint8, device="cuda")
+    dit.attention(gu.dev_bf16(qb), gu.dev_bf16(kb), gu.dev_bf16(vt), n_pad, gu.dev_layout(lay)["cu"], H, Dh, o, ws)
+    torch.cuda.synchronize()
+    return bf16_to_f64(o)
+
+
+def attn_tol(ref, v):
+    """P is rounded to bf16 before P.V (relative 2^-9 per weight) and O is stored bf16."""
+    return BF16_REL * np.abs(ref) + 2.0 ** -8 * np.abs(v).max()
+
+
+DOCSETS = {
+    "tiny": synth.WORKLOADS["tiny"]["docs"],
+    "ragged": synth.WORKLOADS["ragged"]["docs"],
+    "edges": [dict(video=(1, 1, 1)), dict(video=(1, 1, 127)), dict(video=(1, 1, 128)), dict(video=(1, 1, 129)),
+              dict(video=(1, 5, 51)), dict(video=(1, 1, 1), audio=1)],
+}
+
+
+@pytest.mark.parametrize("docs", list(DOCSETS))
+@pytest.mark.parametrize("Dh", [64, 128])
+def test_attention_matches_oracle(docs, Dh):
+    lay = synth.build_layout(DOCSETS[docs])
+    H = 2
+    q, qb, k, kb, v, vb = _attn_inputs(lay, H, Dh, 80 + Dh)
+    ref = oracle.attention(q, k, v, lay["cu_seqlens"], H, Dh)
+    got = _run_attention(lay, H, Dh, qb, kb, vb)
+    assert np.all(np.abs(got - ref) <= attn_tol(ref, v))
+
+
+def test_attention_identical_keys_gives_mean_of_v():
+    lay = synth.build_layout(DOCSETS["ragged"])
+    H, Dh = 2, 128
+    q, qb, k, kb, v, vb = _attn_inputs(lay, H, Dh, 90, same_keys=True)
+    got = _run_attention(lay, H, Dh, qb, kb, vb)
+    cu = lay["cu_seqlens"]
+    for j in range(lay["n_docs"]):
+        mean = v[cu[j]:cu[j + 1]].astype(np.float64).mean(axis=0)
+        assert np.all(np.abs(got[cu[j]:cu[j + 1]] - mean) <= BF16_REL * np.abs(mean) + 2 ** -8 * np.abs(v).max())
+
+
+def test_attention_one_token_doc_returns_v_and_docs_do_not_mix():
+    lay = synth.build_layout(DOCSETS["edges"])
+    H, Dh = 2, 128
+    q, qb, k, kb, v, vb = _attn_inputs(lay, H, Dh, 91)
+    got = _run_attention(lay, H, Dh, qb, kb, vb)
+    assert np.array_equal(got[0], v[0].astype(np.float64))  # the 1-token document: softmax weight exactly 1
+    # perturb document 3: every other document's rows stay bit-identical
+    cu = lay["cu_seqlens"]
+    qb2, kb2, vb2 = qb.copy(), kb.copy(), vb.copy()
+    a, b = cu[3], cu[4]
+    qb2[a:b] ^= 0x0040
+    kb2[a:b] ^= 0x0040
+    vb2[a:b] ^= 0x0040
+    got2 = _run_attention(lay, H, Dh, qb2, kb2, vb2)
+    mask = np.ones(lay["n_tokens"], dtype=bool)
+    mask[a:b] = False
+    assert np.array_equal(got[mask], got2[mask])
+    assert not np.array_equal(got[~mask], got2[~mask])
+
+
+@pytest.mark.slow
+def test_attention_full_size_sampled_rows():
+    """The 17,408-token, 24-head launch the forward uses, checked on sampled query rows."""
+    w = synth.WORKLOADS["video_audio_bf16"]
+    m = w["model"]
+    lay = synth.build_layout(w["docs"])
+    H, Dh = m["n_heads"], m["head_dim"]
+    q, qb, k, kb, v, vb = _attn_inputs(lay, H, Dh, 92)
+    got = _run_attention(lay, H, Dh, qb, kb, vb)
+    n = lay["n_tokens"]
+    rows = np.unique(np.concatenate([[0, 127, 128, 8703, 8704, n - 1],
+                                     (synth.uniform(92, "rows", 26) * n).astype(np.int64)]))
+    oracle.set_threads(8)
+    ref = oracle.attention_rows(q, k, v, lay["cu_seqlens"], H, Dh, rows)
+    oracle.set_threads(1)
+    assert np.all(np.abs(got[rows] - ref) <= attn_tol(ref, v))
+
+
+# ------------------------------------------------------------------------------------------------
+# Euler step: bit-exact
+# ------------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n", [1, 7, 4096, 1_000_003])
+def test_euler_step_bit_exact(n):
+    dit, gu = _dit(), _gu()
+    x = synth.normal(100, "x", (n,), 1.0)
+    v = synth.normal(100, "v", (n,), 1.0)
+    sig = synth.sigmas(50)
+    for i in (0, 13, 49):
+        xd = gu.dev_f32(x)
+        dit.euler_step(xd, gu.dev_f32(v), float(sig[i]), float(sig[i + 1]))
+        ref = oracle.euler_step(x, v, sig[i], sig[i + 1])
+        assert np.array_equal(xd.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
+def test_euler_unaligned_view_bit_exact():
+    dit, gu = _dit(), _gu()
+    x = synth.normal(101, "x", (1001,), 1.0)
+    v = synth.normal(101, "v", (1001,), 1.0)
+    xd = gu.dev_f32(x)
+    vd = gu.dev_f32(v)
+    dit.euler_step(xd[1:], vd[1:], 0.5, 0.48)
+    ref = oracle.euler_step(x[1:], v[1:], np.float32(0.5), np.float32(0.48))
+    got = xd.cpu().numpy()
+    assert got[0] == x[0] and np.array_equal(got[1:].view(np.uint32), ref.view(np.uint32))

@@ -1,0 +1,721 @@
+// C ABI of libdit.so (declared in include/dit.h): handle, validation, bind-time weight repacks,
+// workspace layout and the orchestration of one DiT forward on a caller stream.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <string>
+#include <vector>
+
+#include "../../include/dit.h"
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace dit;
+
+namespace {
+
+thread_local std::string g_create_error;
+
+constexpr size_t kAlign = 256;
+
+inline size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+
+struct BlockDev {
+  const void* w_qkv = nullptr;
+  const void* w_o = nullptr;
+  const void* w_down = nullptr;
+  void* w_in_packed = nullptr;
+  float* b_qkv = nullptr;
+  float* b_o = nullptr;
+  float* b_in_packed = nullptr;
+  float* b_down = nullptr;
+};
+
+// Workspace layout of one forward (offsets in bytes from the workspace base).
+struct WsLayout {
+  size_t status, items, mod, cosc, sinc, resid, y, q, k, vt, o, h, total;
+  int n_pad, max_items, half, mod_rows;
+};
+
+struct TimedLaunch {
+  int kind;
+  cudaEvent_t a, b;
+};
+
+}  // namespace
+
+struct dit_handle {
+  dit_config cfg;
+  bool bound = false;
+  std::string err;
+  std::vector<void*> allocs;
+  std::vector<BlockDev> blocks;
+  void* w_ada_all = nullptr;   // bf16 [ada_rows, t_dim]: L blocks x [n_mod * 6d], then final [n_mod * 2d]
+  float* b_ada_all = nullptr;  // fp32 [ada_rows]
+  int ada_rows = 0;
+  float* dump = nullptr;
+  dit_stats stats;
+  bool timing = false;
+  std::vector<cudaEvent_t> ev_pool;
+  size_t ev_next = 0;
+  std::vector<TimedLaunch> timed;
+  double ms_acc[DIT_KERNEL_KINDS];
+  int64_t n_acc[DIT_KERNEL_KINDS];
+};
+
+namespace {
+
+dit_status set_err(dit_handle* h, dit_status st, const char* fmt, ...) __attribute__((format(printf, 3, 4)));
+dit_status set_err(dit_handle* h, dit_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  if (h)
+    h->err = buf;
+  else
+    g_create_error = buf;
+  return st;
+}
+
+dit_status cuda_err(dit_handle* h, cudaError_t e, const char* what) {
+  return set_err(h, DIT_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define DIT_CK(h, call, what)                            \
+  do {                                                   \
+    cudaError_t e_ = (call);                             \
+    if (e_ != cudaSuccess) return cuda_err((h), e_, (what)); \
+  } while (0)
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+dit_status validate_config(const dit_config* c) {
+  if (!c) return set_err(nullptr, DIT_ERR_INVALID_ARG, "config is NULL");
+  if (c->n_blocks < 1) return set_err(nullptr, DIT_ERR_CONFIG, "n_blocks must be >= 1");
+  if (c->hidden < 1 || c->n_heads < 1 || c->head_dim < 1 || c->n_heads * c->head_dim != c->hidden)
+    return set_err(nullptr, DIT_ERR_CONFIG, "hidden must equal n_heads * head_dim");
+  if (c->ffn_hidden < 1) return set_err(nullptr, DIT_ERR_CONFIG, "ffn_hidden must be >= 1");
+  if (c->norm != DIT_RMSNORM && c->norm != DIT_LAYERNORM) return set_err(nullptr, DIT_ERR_CONFIG, "bad norm");
+  if (!(c->norm_eps > 0.f)) return set_err(nullptr, DIT_ERR_CONFIG, "norm_eps must be > 0");
+  if (c->adaln != 0 && c->adaln != 1) return set_err(nullptr, DIT_ERR_CONFIG, "adaln must be 0 or 1");
+  if (c->adaln && (c->n_modalities < 1 || c->n_modalities > 255))
+    return set_err(nullptr, DIT_ERR_CONFIG, "n_modalities must be in [1, 255]");
+  if (c->adaln && (c->t_embed_dim < 8 || c->t_embed_dim % 8 || (c->t_embed_dim > 256 && c->t_embed_dim % 256)))
+    return set_err(nullptr, DIT_ERR_CONFIG, "t_embed_dim must be a multiple of 8 (and of 256 above 256)");
+  if (c->rope_axes != 1 && c->rope_axes != 3) return set_err(nullptr, DIT_ERR_CONFIG, "rope_axes must be 1 or 3");
+  int rsum = 0;
+  for (int a = 0; a < c->rope_axes; ++a) {
+    if (c->rope_dims[a] < 0 || c->rope_dims[a] % 2) return set_err(nullptr, DIT_ERR_CONFIG, "rope_dims must be even");
+    rsum += c->rope_dims[a];
+  }
+  if (rsum != c->rotary_dim || c->rotary_dim > c->head_dim || c->rotary_dim < 0)
+    return set_err(nullptr, DIT_ERR_CONFIG, "rotary_dim must equal sum(rope_dims) and be <= head_dim");
+  if (!(c->rope_base > 1.0)) return set_err(nullptr, DIT_ERR_CONFIG, "rope_base must be > 1");
+  if (c->io_channels < 0) return set_err(nullptr, DIT_ERR_CONFIG, "io_channels must be >= 0");
+  if (c->max_tokens < 1 || c->max_docs < 1) return set_err(nullptr, DIT_ERR_CONFIG, "max_tokens/max_docs must be >= 1");
+  if (c->dtype != DIT_BF16 && c->dtype != DIT_FP32) return set_err(nullptr, DIT_ERR_CONFIG, "bad dtype");
+  // What the sm_103a kernels tile.
+  if (c->dtype == DIT_FP32) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "the fp32 forward is not built in this library");
+  if (c->hidden % 256) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "hidden must be a multiple of 256");
+  if (c->head_dim != 128 && c->head_dim != 64)
+    return set_err(nullptr, DIT_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+  if ((c->rotary_dim / 2) % 16 || (c->head_dim - c->rotary_dim) % 16)
+    return set_err(nullptr, DIT_ERR_UNSUPPORTED, "rotary_dim/2 and head_dim-rotary_dim must be multiples of 16");
+  if (c->ffn_hidden % 128) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "ffn_hidden must be a multiple of 128");
+  if (!norm_width_supported(c->hidden)) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "hidden width not tiled by the norm kernel");
+  if (c->io_channels) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "pre/post convolutions need the fp32 forward");
+  if (c->norm == DIT_LAYERNORM) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "LayerNorm blocks need the fp32 forward");
+  if (!c->adaln) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "the bf16 forward needs adaln = 1");
+  return DIT_OK;
+}
+
+WsLayout ws_layout(const dit_config* c, int n, int n_docs) {
+  WsLayout w;
+  const int d = c->hidden, F = c->ffn_hidden;
+  w.n_pad = (n + 7) & ~7;
+  w.max_items = attention_max_items(n_docs, n);
+  w.half = c->rotary_dim / 2;
+  w.mod_rows = c->adaln ? c->n_blocks * c->n_modalities * 6 * d + c->n_modalities * 2 * d : 0;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes);
+    return o;
+  };
+  w.status = take(64);
+  w.items = take((size_t)w.max_items * sizeof(int2));
+  w.mod = take((size_t)w.mod_rows * 4);
+  w.cosc = take((size_t)n * w.half * 4);
+  w.sinc = take((size_t)n * w.half * 4);
+  w.resid = take((size_t)n * d * 4);
+  w.y = take((size_t)n * d * 2);
+  w.q = take((size_t)n * d * 2);
+  w.k = take((size_t)n * d * 2);
+  w.vt = take((size_t)d * w.n_pad * 2);
+  w.o = take((size_t)n * d * 2);
+  w.h = take((size_t)n * F * 2);
+  w.total = off;
+  return w;
+}
+
+// status word layout at ws + status: [0] device status bits, [1] layout code, [2] attention item count
+struct StatusWords {
+  int bits, layout_code, count, pad;
+};
+
+template <typename T>
+T* at(void* base, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(base) + off);
+}
+
+void* dev_alloc(dit_handle* h, size_t bytes, cudaError_t* e) {
+  void* p = nullptr;
+  *e = cudaMalloc(&p, bytes ? bytes : 16);
+  if (*e == cudaSuccess) {
+    h->allocs.push_back(p);
+    h->stats.bound_bytes += (int64_t)bytes;
+  }
+  return p;
+}
+
+cudaEvent_t next_event(dit_handle* h) {
+  if (h->ev_next >= h->ev_pool.size()) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    h->ev_pool.push_back(e);
+  }
+  return h->ev_pool[h->ev_next++];
+}
+
+// Record-around helper: kind < 0 means untimed.
+struct Launch {
+  dit_handle* h;
+  cudaStream_t s;
+  int kind;
+  cudaEvent_t a = nullptr;
+  Launch(dit_handle* h_, cudaStream_t s_, int k) : h(h_), s(s_), kind(k) {
+    if (h && h->timing) {
+      a = next_event(h);
+      if (a) cudaEventRecord(a, s);
+    }
+  }
+  void done() {
+    if (h && h->timing && a) {
+      cudaEvent_t b = next_event(h);
+      if (b) {
+        cudaEventRecord(b, s);
+        h->timed.push_back({kind, a, b});
+      }
+    }
+    if (h) {
+      h->stats.kernels_launched++;
+      if (kind == 0 || kind == 2 || kind == 3 || kind == 4) h->stats.gemm_launches++;
+      else if (kind == 1) h->stats.attention_launches++;
+      else if (kind == 5) h->stats.norm_launches++;
+      else h->stats.other_launches++;
+    }
+  }
+};
+
+}  // namespace
+
+extern "C" {
+
+const char* dit_last_error(const dit_handle* h) { return h ? h->err.c_str() : g_create_error.c_str(); }
+
+dit_status dit_create(const dit_config* cfg, dit_handle** out) {
+  if (!out) return set_err(nullptr, DIT_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  dit_status st = validate_config(cfg);
+  if (st != DIT_OK) return st;
+  dit_handle* h = new dit_handle();
+  h->cfg = *cfg;
+  memset(&h->stats, 0, sizeof h->stats);
+  memset(h->ms_acc, 0, sizeof h->ms_acc);
+  memset(h->n_acc, 0, sizeof h->n_acc);
+  *out = h;
+  g_create_error.clear();
+  return DIT_OK;
+}
+
+dit_status dit_destroy(dit_handle* h) {
+  if (!h) return DIT_ERR_INVALID_ARG;
+  cudaDeviceSynchronize();
+  for (void* p : h->allocs) cudaFree(p);
+  for (cudaEvent_t e : h->ev_pool) cudaEventDestroy(e);
+  delete h;
+  return DIT_OK;
+}
+
+size_t dit_workspace_bytes(const dit_config* cfg, int n_tokens, int n_docs) {
+  if (validate_config(cfg) != DIT_OK || n_tokens < 1 || n_docs < 1) return 0;
+  return ws_layout(cfg, n_tokens, n_docs).total;
+}
+
+dit_status dit_bind_weights(dit_handle* h, const dit_weights* w, void* stream) {
+  if (!h) return DIT_ERR_INVALID_ARG;
+  if (!w || !w->blocks) return set_err(h, DIT_ERR_INVALID_ARG, "weights or weights->blocks is NULL");
+  const dit_config& c = h->cfg;
+  if (w->n_blocks != c.n_blocks)
+    return set_err(h, DIT_ERR_INVALID_ARG, "weights.n_blocks %d != config n_blocks %d", w->n_blocks, c.n_blocks);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int d = c.hidden, F = c.ffn_hidden, nm = c.n_modalities, td = c.t_embed_dim;
+  // Missing tensors are reported by name before anything is allocated.
+  for (int l = 0; l < c.n_blocks; ++l) {
+    const dit_block_weights& b = w->blocks[l];
+    const struct {
+      const void* p;
+      const char* name;
+    } req[] = {{b.w_qkv, "w_qkv"}, {b.w_o, "w_o"}, {b.w_in, "w_in"}, {b.w_down, "w_down"}, {b.w_ada, "w_ada"}};
+    for (const auto& r : req) {
+      if (!r.p) return set_err(h, DIT_ERR_MISSING_WEIGHT, "missing weight: blocks[%d].%s", l, r.name);
+      if (!aligned16(r.p)) return set_err(h, DIT_ERR_INVALID_ARG, "blocks[%d].%s is not 16-byte aligned", l, r.name);
+    }
+  }
+  if (!w->w_ada_final) return set_err(h, DIT_ERR_MISSING_WEIGHT, "missing weight: w_ada_final");
+
+  // Free a previous binding.
+  cudaStreamSynchronize(s);
+  for (void* p : h->allocs) cudaFree(p);
+  h->allocs.clear();
+  h->blocks.assign(c.n_blocks, BlockDev());
+  h->stats.bound_bytes = 0;
+  h->bound = false;
+
+  cudaError_t e;
+  const int is_bf16 = c.dtype == DIT_BF16;
+  auto bias_f32 = [&](const void* src, long long n) -> float* {
+    float* dst = static_cast<float*>(dev_alloc(h, n * 4, &e));
+    if (e != cudaSuccess) return nullptr;
+    if (src)
+      e = to_f32_launch(src, is_bf16, n, dst, s);
+    else
+      e = cudaMemsetAsync(dst, 0, n * 4, s);
+    return e == cudaSuccess ? dst : nullptr;
+  };
+  for (int l = 0; l < c.n_blocks; ++l) {
+    const dit_block_weights& b = w->blocks[l];
+    BlockDev& bd = h->blocks[l];
+    bd.w_qkv = b.w_qkv;
+    bd.w_o = b.w_o;
+    bd.w_down = b.w_down;
+    if (!(bd.b_qkv = bias_f32(b.b_qkv, 3ll * d))) return cuda_err(h, e, "bind b_qkv");
+    if (!(bd.b_o = bias_f32(b.b_o, d))) return cuda_err(h, e, "bind b_o");
+    if (!(bd.b_down = bias_f32(b.b_down, d))) return cuda_err(h, e, "bind b_down");
+    float* b_in = nullptr;
+    if (b.b_in && !(b_in = bias_f32(b.b_in, 2ll * F))) return cuda_err(h, e, "bind b_in");
+    bd.w_in_packed = dev_alloc(h, (size_t)2 * F * d * 2, &e);
+    if (e != cudaSuccess) return cuda_err(h, e, "alloc w_in");
+    bd.b_in_packed = static_cast<float*>(dev_alloc(h, (size_t)2 * F * 4, &e));
+    if (e != cudaSuccess) return cuda_err(h, e, "alloc b_in");
+    DIT_CK(h, pack_ffn_in_launch(b.w_in, b_in, F, d, bd.w_in_packed, bd.b_in_packed, s), "pack w_in");
+  }
+  // AdaLN matrices of every block, then the final layer's, in one [rows, t_dim] matrix.
+  const size_t blk_rows = (size_t)nm * 6 * d, fin_rows = (size_t)nm * 2 * d;
+  h->ada_rows = (int)(c.n_blocks * blk_rows + fin_rows);
+  h->w_ada_all = dev_alloc(h, (size_t)h->ada_rows * td * 2, &e);
+  if (e != cudaSuccess) return cuda_err(h, e, "alloc w_ada");
+  h->b_ada_all = static_cast<float*>(dev_alloc(h, (size_t)h->ada_rows * 4, &e));
+  if (e != cudaSuccess) return cuda_err(h, e, "alloc b_ada");
+  for (int l = 0; l < c.n_blocks; ++l) {
+    DIT_CK(h, cudaMemcpyAsync(static_cast<char*>(h->w_ada_all) + (size_t)l * blk_rows * td * 2, w->blocks[l].w_ada,
+                              blk_rows * td * 2, cudaMemcpyDeviceToDevice, s), "copy w_ada");
+    if (w->blocks[l].b_ada)
+      DIT_CK(h, to_f32_launch(w->blocks[l].b_ada, is_bf16, (long long)blk_rows, h->b_ada_all + l * blk_rows, s), "b_ada");
+    else
+      DIT_CK(h, cudaMemsetAsync(h->b_ada_all + l * blk_rows, 0, blk_rows * 4, s), "b_ada");
+  }
+  DIT_CK(h, cudaMemcpyAsync(static_cast<char*>(h->w_ada_all) + (size_t)c.n_blocks * blk_rows * td * 2, w->w_ada_final,
+                            fin_rows * td * 2, cudaMemcpyDeviceToDevice, s), "copy w_ada_final");
+  if (w->b_ada_final)
+    DIT_CK(h, to_f32_launch(w->b_ada_final, is_bf16, (long long)fin_rows, h->b_ada_all + c.n_blocks * blk_rows, s),
+           "b_ada_final");
+  else
+    DIT_CK(h, cudaMemsetAsync(h->b_ada_all + c.n_blocks * blk_rows, 0, fin_rows * 4, s), "b_ada_final");
+  DIT_CK(h, cudaStreamSynchronize(s), "bind sync");
+  h->bound = true;
+  return DIT_OK;
+}
+
+dit_status dit_forward(dit_handle* h, const float* x_tokens, const int32_t* cu_seqlens, int n_docs,
+                       const int32_t* doc_ids, const uint8_t* modality_tags, const double* pos_thw, int n_tokens,
+                       float timestep, float* out, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!h) return DIT_ERR_INVALID_ARG;
+  if (!h->bound) return set_err(h, DIT_ERR_UNBOUND, "dit_forward before dit_bind_weights");
+  const dit_config& c = h->cfg;
+  if (!x_tokens || !cu_seqlens || !doc_ids || !modality_tags || !pos_thw || !out || !workspace)
+    return set_err(h, DIT_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (n_tokens < 1 || n_docs < 1) return set_err(h, DIT_ERR_LAYOUT, "n_tokens and n_docs must be >= 1");
+  if (n_tokens > c.max_tokens || n_docs > c.max_docs)
+    return set_err(h, DIT_ERR_CAPACITY, "n_tokens %d / n_docs %d exceed max_tokens %d / max_docs %d", n_tokens,
+                   n_docs, c.max_tokens, c.max_docs);
+  if (!aligned16(x_tokens) || !aligned16(out) || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
+    return set_err(h, DIT_ERR_INVALID_ARG, "x/out must be 16-byte and workspace 256-byte aligned");
+  if (static_cast<const void*>(x_tokens) == static_cast<const void*>(out))
+    return set_err(h, DIT_ERR_INVALID_ARG, "out may not alias x_tokens");
+  const WsLayout L = ws_layout(&c, n_tokens, n_docs);
+  if (workspace_bytes < L.total)
+    return set_err(h, DIT_ERR_CAPACITY, "workspace %zu bytes < required %zu", workspace_bytes, L.total);
+  if (!(timestep >= 0.f && timestep <= 1.f)) return set_err(h, DIT_ERR_INVALID_ARG, "timestep must be in [0, 1]");
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int d = c.hidden, F = c.ffn_hidden, H = c.n_heads, nm = c.n_modalities;
+  const int N = n_tokens;
+  StatusWords* sw = at<StatusWords>(workspace, L.status);
+  int* status = &sw->bits;
+  int2* items = at<int2>(workspace, L.items);
+  float* mod = at<float>(workspace, L.mod);
+  float* cosc = at<float>(workspace, L.cosc);
+  float* sinc = at<float>(workspace, L.sinc);
+  float* resid = at<float>(workspace, L.resid);
+  void* y = at<void>(workspace, L.y);
+  void* q = at<void>(workspace, L.q);
+  void* k = at<void>(workspace, L.k);
+  void* vt = at<void>(workspace, L.vt);
+  void* o = at<void>(workspace, L.o);
+  void* hbuf = at<void>(workspace, L.h);
+
+  {
+    Launch ln(h, s, 6);
+    DIT_CK(h, cudaMemsetAsync(sw, 0, sizeof(StatusWords), s), "status reset");
+    DIT_CK(h, attention_schedule_launch(cu_seqlens, n_docs, N, doc_ids, modality_tags, nm, items, &sw->count,
+                                        L.max_items, &sw->layout_code, status, s), "schedule");
+    ln.done();
+  }
+  {
+    Launch ln(h, s, 6);
+    DIT_CK(h, rope_cache_launch(pos_thw, N, c.rope_axes, c.rope_dims, c.rope_base, cosc, sinc, status, s), "rope cache");
+    ln.done();
+  }
+  {
+    Launch ln(h, s, 6);
+    DIT_CK(h, adaln_launch(h->w_ada_all, h->b_ada_all, h->ada_rows, c.t_embed_dim, timestep, mod, status, s), "adaln");
+    ln.done();
+  }
+  DIT_CK(h, cudaMemcpyAsync(resid, x_tokens, (size_t)N * d * 4, cudaMemcpyDeviceToDevice, s), "copy x");
+
+  const long long mstride = 6ll * d;  // between modality rows of one block's [n_mod][6][d]
+  AttnArgs aa;
+  aa.n_tokens = N;
+  aa.n_heads = H;
+  aa.head_dim = c.head_dim;
+  aa.n_pad = L.n_pad;
+  aa.n_docs = n_docs;
+  aa.cu = cu_seqlens;
+  aa.items = items;
+  aa.count = &sw->count;
+  aa.max_items = L.max_items;
+  aa.scale_log2 = (float)(1.4426950408889634 / sqrt((double)c.head_dim));
+  aa.status = status;
+
+  for (int l = 0; l < c.n_blocks; ++l) {
+    const BlockDev& B = h->blocks[l];
+    const float* ml = mod + (size_t)l * nm * 6 * d;
+    {
+      Launch ln(h, s, 5);
+      DIT_CK(h, norm_modulate_launch(resid, N, d, c.norm, c.norm_eps, nullptr, nullptr, modality_tags, ml + 0 * d,
+                                     ml + 1 * d, mstride, y, 0, status, s), "norm1");
+      ln.done();
+    }
+    {
+      Launch ln(h, s, 0);
+      GemmArgs g{};
+      g.M = N; g.N = 3 * d; g.K = d; g.bias = B.b_qkv;
+      g.d = d; g.head_dim = c.head_dim; g.rot_half = c.rotary_dim / 2;
+      g.cos_cache = cosc; g.sin_cache = sinc; g.q = q; g.k = k; g.vt = vt; g.n_pad = L.n_pad;
+      g.status = status;
+      DIT_CK(h, gemm_launch(kEpiQkvRope, y, B.w_qkv, g, s), "gemm qkv");
+      ln.done();
+    }
+    {
+      Launch ln(h, s, 1);
+      DIT_CK(h, attention_launch(q, k, vt, o, aa, s), "attention");
+      ln.done();
+    }
+    {
+      Launch ln(h, s, 2);
+      GemmArgs g{};
+      g.M = N; g.N = d; g.K = d; g.bias = B.b_o;
+      g.x = resid; g.gate = ml + 2 * d; g.gate_stride = mstride; g.tags = modality_tags; g.status = status;
+      DIT_CK(h, gemm_launch(kEpiGatedResid, o, B.w_o, g, s), "gemm out");
+      ln.done();
+    }
+    {
+      Launch ln(h, s, 5);
+      DIT_CK(h, norm_modulate_launch(resid, N, d, c.norm, c.norm_eps, nullptr, nullptr, modality_tags, ml + 3 * d,
+                                     ml + 4 * d, mstride, y, 0, status, s), "norm2");
+      ln.done();
+    }
+    {
+      Launch ln(h, s, 3);
+      GemmArgs g{};
+      g.M = N; g.N = 2 * F; g.K = d; g.bias = B.b_in_packed; g.out = hbuf; g.status = status;
+      DIT_CK(h, gemm_launch(kEpiSwiglu, y, B.w_in_packed, g, s), "gemm ffn up");
+      ln.done();
+    }
+    {
+      Launch ln(h, s, 4);
+      GemmArgs g{};
+      g.M = N; g.N = d; g.K = F; g.bias = B.b_down;
+      g.x = resid; g.gate = ml + 5 * d; g.gate_stride = mstride; g.tags = modality_tags; g.status = status;
+      DIT_CK(h, gemm_launch(kEpiGatedResid, hbuf, B.w_down, g, s), "gemm ffn down");
+      ln.done();
+    }
+    if (h->dump)
+      DIT_CK(h, cudaMemcpyAsync(h->dump + (size_t)l * N * d, resid, (size_t)N * d * 4, cudaMemcpyDeviceToDevice, s),
+             "dump");
+  }
+  {
+    const float* mf = mod + (size_t)c.n_blocks * nm * 6 * d;
+    Launch ln(h, s, 5);
+    DIT_CK(h, norm_modulate_launch(resid, N, d, c.norm, c.norm_eps, nullptr, nullptr, modality_tags, mf, mf + d,
+                                   2ll * d, out, 1, status, s), "final norm");
+    ln.done();
+  }
+  h->stats.forwards++;
+  return DIT_OK;
+}
+
+size_t dit_workspace_bytes_host(const dit_config* cfg, int n_tokens, int n_docs) {
+  size_t base = dit_workspace_bytes(cfg, n_tokens, n_docs);
+  if (!base) return 0;
+  const size_t width = cfg->io_channels ? cfg->io_channels : cfg->hidden;
+  size_t extra = align_up((size_t)n_tokens * width * 4) * 2 + align_up((size_t)(n_docs + 1) * 4) +
+                 align_up((size_t)n_tokens * 4) + align_up((size_t)n_tokens) + align_up((size_t)n_tokens * 24);
+  return align_up(base) + extra;
+}
+
+dit_status dit_forward_host(dit_handle* h, const float* x_host, const int32_t* cu_host, int n_docs,
+                            const int32_t* doc_ids_host, const uint8_t* tags_host, const double* pos_host,
+                            int n_tokens, float timestep, float* out_host, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  if (!h) return DIT_ERR_INVALID_ARG;
+  if (!x_host || !cu_host || !doc_ids_host || !tags_host || !pos_host || !out_host || !workspace)
+    return set_err(h, DIT_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (n_tokens < 1 || n_docs < 1) return set_err(h, DIT_ERR_LAYOUT, "n_tokens and n_docs must be >= 1");
+  const size_t need = dit_workspace_bytes_host(&h->cfg, n_tokens, n_docs);
+  if (!need || workspace_bytes < need) return set_err(h, DIT_ERR_CAPACITY, "workspace too small for the host forward");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t base = align_up(dit_workspace_bytes(&h->cfg, n_tokens, n_docs));
+  const size_t width = h->cfg.io_channels ? h->cfg.io_channels : h->cfg.hidden;
+  const size_t xb = (size_t)n_tokens * width * 4;
+  char* p = static_cast<char*>(workspace) + base;
+  float* x_d = reinterpret_cast<float*>(p); p += align_up(xb);
+  float* out_d = reinterpret_cast<float*>(p); p += align_up(xb);
+  int32_t* cu_d = reinterpret_cast<int32_t*>(p); p += align_up((size_t)(n_docs + 1) * 4);
+  int32_t* ids_d = reinterpret_cast<int32_t*>(p); p += align_up((size_t)n_tokens * 4);
+  uint8_t* tags_d = reinterpret_cast<uint8_t*>(p); p += align_up((size_t)n_tokens);
+  double* pos_d = reinterpret_cast<double*>(p);
+  DIT_CK(h, cudaMemcpyAsync(x_d, x_host, xb, cudaMemcpyHostToDevice, s), "h2d x");
+  DIT_CK(h, cudaMemcpyAsync(cu_d, cu_host, (size_t)(n_docs + 1) * 4, cudaMemcpyHostToDevice, s), "h2d cu");
+  DIT_CK(h, cudaMemcpyAsync(ids_d, doc_ids_host, (size_t)n_tokens * 4, cudaMemcpyHostToDevice, s), "h2d doc_ids");
+  DIT_CK(h, cudaMemcpyAsync(tags_d, tags_host, (size_t)n_tokens, cudaMemcpyHostToDevice, s), "h2d tags");
+  DIT_CK(h, cudaMemcpyAsync(pos_d, pos_host, (size_t)n_tokens * 24, cudaMemcpyHostToDevice, s), "h2d pos");
+  dit_status st = dit_forward(h, x_d, cu_d, n_docs, ids_d, tags_d, pos_d, n_tokens, timestep, out_d, workspace,
+                              base, stream);
+  if (st != DIT_OK) return st;
+  DIT_CK(h, cudaMemcpyAsync(out_host, out_d, xb, cudaMemcpyDeviceToHost, s), "d2h out");
+  DIT_CK(h, cudaStreamSynchronize(s), "host forward sync");
+  return DIT_OK;
+}
+
+dit_status dit_euler_step(float* x, const float* v, int64_t n, float sigma, float sigma_next, void* stream) {
+  if (n < 0 || (n > 0 && (!x || !v))) return set_err(nullptr, DIT_ERR_INVALID_ARG, "bad euler arguments");
+  if (!(sigma > 0.f)) return set_err(nullptr, DIT_ERR_INVALID_ARG, "sigma must be > 0");
+  cudaError_t e = euler_launch(x, v, n, sigma, sigma_next, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DIT_OK : cuda_err(nullptr, e, "euler");
+}
+
+dit_status dit_get_stats(const dit_handle* h, dit_stats* out) {
+  if (!h || !out) return DIT_ERR_INVALID_ARG;
+  *out = h->stats;
+  return DIT_OK;
+}
+
+dit_status dit_sync_status(dit_handle* h, const void* workspace, void* stream) {
+  if (!h || !workspace) return DIT_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  StatusWords sw;
+  DIT_CK(h, cudaStreamSynchronize(s), "sync");
+  DIT_CK(h, cudaMemcpy(&sw, workspace, sizeof sw, cudaMemcpyDeviceToHost), "read status");
+  h->stats.device_status = sw.bits;
+  h->stats.last_layout_error = sw.layout_code;
+  h->stats.attention_tiles = (int64_t)sw.count * h->cfg.n_heads;
+  if (sw.bits & kDevLayout) return set_err(h, DIT_ERR_LAYOUT, "device validator rejected the layout (code %d)", sw.layout_code);
+  if (sw.bits & kDevTimeout) return set_err(h, DIT_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait ran out");
+  if (sw.bits & kDevCapacity) return set_err(h, DIT_ERR_CAPACITY, "tile schedule overflow");
+  return DIT_OK;
+}
+
+dit_status dit_set_dump(dit_handle* h, float* dump) {
+  if (!h) return DIT_ERR_INVALID_ARG;
+  h->dump = dump;
+  return DIT_OK;
+}
+
+dit_status dit_set_kernel_timing(dit_handle* h, int enable) {
+  if (!h) return DIT_ERR_INVALID_ARG;
+  h->timing = enable != 0;
+  h->timed.clear();
+  h->ev_next = 0;
+  memset(h->ms_acc, 0, sizeof h->ms_acc);
+  memset(h->n_acc, 0, sizeof h->n_acc);
+  return DIT_OK;
+}
+
+dit_status dit_get_kernel_times(dit_handle* h, double* ms_out, int64_t* launches_out) {
+  if (!h || !ms_out || !launches_out) return DIT_ERR_INVALID_ARG;
+  DIT_CK(h, cudaDeviceSynchronize(), "timing sync");
+  for (const TimedLaunch& t : h->timed) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, t.a, t.b) == cudaSuccess) {
+      h->ms_acc[t.kind] += ms;
+      h->n_acc[t.kind] += 1;
+    }
+  }
+  h->timed.clear();
+  h->ev_next = 0;
+  for (int i = 0; i < DIT_KERNEL_KINDS; ++i) {
+    ms_out[i] = h->ms_acc[i];
+    launches_out[i] = h->n_acc[i];
+  }
+  return DIT_OK;
+}
+
+// ------------------------------------------------------------------------------------------------
+// op-level entry points
+// ------------------------------------------------------------------------------------------------
+
+dit_status dit_op_norm_modulate(const float* x, int n, int d, int norm, float eps, const float* ln_g, const float* ln_b,
+                                const uint8_t* tags, const float* shift, const float* scale, int64_t mod_stride,
+                                void* y, int out_kind, void* stream) {
+  if (n < 0 || !x || !y || (shift && (!scale || !tags)) || (out_kind != 0 && out_kind != 1) ||
+      (norm != DIT_RMSNORM && norm != DIT_LAYERNORM))
+    return set_err(nullptr, DIT_ERR_INVALID_ARG, "bad norm_modulate arguments");
+  if (!norm_width_supported(d)) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "width %d not tiled by the norm kernel", d);
+  if (!aligned16(x) || !aligned16(y) || (shift && (!aligned16(shift) || !aligned16(scale) || mod_stride % 4)))
+    return set_err(nullptr, DIT_ERR_INVALID_ARG, "norm_modulate pointers must be 16-byte aligned");
+  cudaError_t e = norm_modulate_launch(x, n, d, norm, eps, ln_g, ln_b, tags, shift, scale, mod_stride, y, out_kind,
+                                       nullptr, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DIT_OK : cuda_err(nullptr, e, "norm_modulate");
+}
+
+dit_status dit_op_rope_cache(const double* pos, int n, int n_axes, const int* dims_host, double base, float* cos_out,
+                             float* sin_out, void* stream) {
+  if (n < 0 || !pos || !cos_out || !sin_out || !dims_host || (n_axes != 1 && n_axes != 3))
+    return set_err(nullptr, DIT_ERR_INVALID_ARG, "bad rope_cache arguments");
+  cudaError_t e = rope_cache_launch(pos, n, n_axes, dims_host, base, cos_out, sin_out, nullptr,
+                                    static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DIT_OK : cuda_err(nullptr, e, "rope_cache");
+}
+
+dit_status dit_op_adaln(const void* w, const float* b, int rows, int t_dim, float t, float* mod, void* stream) {
+  if (rows < 0 || !w || !mod || t_dim < 8 || t_dim % 8 || (t_dim > 256 && t_dim % 256) || !aligned16(w))
+    return set_err(nullptr, DIT_ERR_INVALID_ARG, "bad adaln arguments");
+  cudaError_t e = adaln_launch(w, b, rows, t_dim, t, mod, nullptr, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DIT_OK : cuda_err(nullptr, e, "adaln");
+}
+
+static dit_status check_gemm(const void* a, const void* b, int M, int N, int K) {
+  if (!a || !b || M < 0 || N <= 0 || K <= 0) return set_err(nullptr, DIT_ERR_INVALID_ARG, "bad GEMM arguments");
+  if (N % 256 || K % 64) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "GEMM needs N %% 256 == 0 and K %% 64 == 0");
+  if (!aligned16(a) || !aligned16(b)) return set_err(nullptr, DIT_ERR_INVALID_ARG, "GEMM operands must be 16-byte aligned");
+  return DIT_OK;
+}
+
+dit_status dit_op_gemm(const void* a, const void* b, const float* bias, int M, int N, int K, void* out, int out_kind,
+                       void* stream) {
+  dit_status st = check_gemm(a, b, M, N, K);
+  if (st != DIT_OK) return st;
+  if (!out || (out_kind != 0 && out_kind != 1)) return set_err(nullptr, DIT_ERR_INVALID_ARG, "bad GEMM output");
+  GemmArgs g{};
+  g.M = M; g.N = N; g.K = K; g.bias = bias; g.out = out; g.out_kind = out_kind;
+  cudaError_t e = gemm_launch(kEpiStore, a, b, g, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DIT_OK : cuda_err(nullptr, e, "gemm");
+}
+
+dit_status dit_op_gemm_qkv_rope(const void* a, const void* b, const float* bias, int M, int d, int K, int n_heads,
+                                int head_dim, int rotary_dim, const float* cos_cache, const float* sin_cache, void* q,
+                                void* k, void* vt, int n_pad, void* stream) {
+  dit_status st = check_gemm(a, b, M, 3 * d, K);
+  if (st != DIT_OK) return st;
+  if (d % 256 || n_heads * head_dim != d || 256 % head_dim || rotary_dim > head_dim || (rotary_dim / 2) % 16 ||
+      (head_dim - rotary_dim) % 16 || !q || !k || !vt || n_pad < M || n_pad % 8 ||
+      (rotary_dim > 0 && (!cos_cache || !sin_cache)))
+    return set_err(nullptr, DIT_ERR_INVALID_ARG, "bad qkv_rope arguments");
+  GemmArgs g{};
+  g.M = M; g.N = 3 * d; g.K = K; g.bias = bias; g.d = d; g.head_dim = head_dim; g.rot_half = rotary_dim / 2;
+  g.cos_cache = cos_cache; g.sin_cache = sin_cache; g.q = q; g.k = k; g.vt = vt; g.n_pad = n_pad;
+  cudaError_t e = gemm_launch(kEpiQkvRope, a, b, g, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DIT_OK : cuda_err(nullptr, e, "gemm qkv");
+}
+
+dit_status dit_op_gemm_gated_residual(const void* a, const void* b, const float* bias, int M, int N, int K, float* x,
+                                      const float* gate, int64_t gate_stride, const uint8_t* tags, void* stream) {
+  dit_status st = check_gemm(a, b, M, N, K);
+  if (st != DIT_OK) return st;
+  if (!x || (gate && (!tags || gate_stride % 4 || !aligned16(gate))) || !aligned16(x))
+    return set_err(nullptr, DIT_ERR_INVALID_ARG, "bad gated_residual arguments");
+  GemmArgs g{};
+  g.M = M; g.N = N; g.K = K; g.bias = bias; g.x = x; g.gate = gate; g.gate_stride = gate_stride; g.tags = tags;
+  cudaError_t e = gemm_launch(kEpiGatedResid, a, b, g, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DIT_OK : cuda_err(nullptr, e, "gemm gated residual");
+}
+
+dit_status dit_op_gemm_swiglu(const void* a, const void* b_packed, const float* bias_packed, int M, int F, int K,
+                              void* hout, void* stream) {
+  dit_status st = check_gemm(a, b_packed, M, 2 * F, K);
+  if (st != DIT_OK) return st;
+  if (!hout || F % 128) return set_err(nullptr, DIT_ERR_INVALID_ARG, "bad swiglu arguments");
+  GemmArgs g{};
+  g.M = M; g.N = 2 * F; g.K = K; g.bias = bias_packed; g.out = hout;
+  cudaError_t e = gemm_launch(kEpiSwiglu, a, b_packed, g, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DIT_OK : cuda_err(nullptr, e, "gemm swiglu");
+}
+
+dit_status dit_op_pack_ffn_in(const void* w_in, const float* b_in, int F, int d, void* w_packed, float* b_packed,
+                              void* stream) {
+  if (!w_in || !w_packed || !b_packed || F <= 0 || F % 128 || d <= 0 || d % 8 || !aligned16(w_in) || !aligned16(w_packed))
+    return set_err(nullptr, DIT_ERR_INVALID_ARG, "bad pack_ffn_in arguments");
+  cudaError_t e = pack_ffn_in_launch(w_in, b_in, F, d, w_packed, b_packed, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DIT_OK : cuda_err(nullptr, e, "pack_ffn_in");
+}
+
+size_t dit_attention_workspace_bytes(int n_docs, int n_tokens) {
+  if (n_docs < 1 || n_tokens < 1) return 0;
+  return align_up(sizeof(StatusWords)) + align_up((size_t)attention_max_items(n_docs, n_tokens) * sizeof(int2));
+}
+
+dit_status dit_op_attention(const void* q, const void* k, const void* vt, int n_pad, const int32_t* cu_seqlens,
+                            int n_docs, int n_tokens, int n_heads, int head_dim, void* o, void* workspace,
+                            void* stream) {
+  if (!q || !k || !vt || !o || !cu_seqlens || !workspace || n_docs < 1 || n_tokens < 1 || n_heads < 1 ||
+      n_pad < n_tokens || n_pad % 8 || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
+    return set_err(nullptr, DIT_ERR_INVALID_ARG, "bad attention arguments");
+  if (head_dim != 128 && head_dim != 64) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "attention needs head_dim 64 or 128");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(vt) || !aligned16(o))
+    return set_err(nullptr, DIT_ERR_INVALID_ARG, "attention operands must be 16-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  StatusWords* sw = static_cast<StatusWords*>(workspace);
+  int2* items = at<int2>(workspace, align_up(sizeof(StatusWords)));
+  const int max_items = attention_max_items(n_docs, n_tokens);
+  cudaError_t e = cudaMemsetAsync(sw, 0, sizeof(StatusWords), s);
+  if (e == cudaSuccess)
+    e = attention_schedule_launch(cu_seqlens, n_docs, n_tokens, nullptr, nullptr, 0, items, &sw->count, max_items,
+                                  &sw->layout_code, &sw->bits, s);
+  if (e != cudaSuccess) return cuda_err(nullptr, e, "attention schedule");
+  AttnArgs aa;
+  aa.n_tokens = n_tokens; aa.n_heads = n_heads; aa.head_dim = head_dim; aa.n_pad = n_pad; aa.n_docs = n_docs;
+  aa.cu = cu_seqlens; aa.items = items; aa.count = &sw->count; aa.max_items = max_items;
+  aa.scale_log2 = (float)(1.4426950408889634 / sqrt((double)head_dim));
+  aa.status = &sw->bits;
+  e = attention_launch(q, k, vt, o, aa, s);
+  return e == cudaSuccess ? DIT_OK : cuda_err(nullptr, e, "attention");
+}
+
+}  // extern "C"

@@ -1,0 +1,397 @@
+// Varlen, bidirectional (non-causal) flash attention over a packed sequence on the tcgen05 tensor
+// cores.  [H3] "Correctness gates": attention reuses DFlashBlockAttention(causal=false) for packed
+// varlen; [M3] "What moved": non-causal attention with no bias.  For document [a, b) and head h:
+//     o_i = sum_j softmax_j(q_i . k_j / sqrt(Dh)) v_j,   i, j in [a, b)
+// The block-diagonal structure comes from cu_seqlens alone: no mask tensor exists.
+//
+// One CTA = one (document, 128-row q-tile, head).  Key/value tiles are 128 tokens wide and start
+// at multiples of 128 in the packed sequence (so the TMA x coordinate of the transposed V is
+// 16-byte aligned); columns outside the document are masked to -inf.
+//   warp 0     TMA producer: Q once, then (K tile, V^T tile) pairs through a 2-stage ring
+//   warp 1     TMEM allocator + UMMA issuer: S(j) = Q K(j)^T into TMEM, O(j) = P(j) V(j) into TMEM
+//   warps 2-5  softmax: thread <-> query row; reads S(j) from TMEM, keeps the running max/sum,
+//              writes P(j) (bf16) into shared memory as the next MMA's A operand, and folds the
+//              partial O(j) from TMEM into its fp32 register accumulator (rescaled by exp2(dm)).
+// TMEM: S double buffer (2 x 128 columns) + O partial double buffer (2 x 128 columns) = 512.
+#include "common.cuh"
+#include "kernels.h"
+#include "tmap.h"
+
+namespace dit {
+
+namespace {
+
+constexpr int TQ = 128, TK = 128;
+constexpr int ATOM = 128 * 64 * 2;         // 128 rows x 64 bf16 columns, 128-byte swizzled (16 KB)
+constexpr int P_BYTES = 2 * ATOM;          // P tile: 128 q rows x 128 kv columns
+constexpr int KV_STAGES = 2;
+constexpr int ATT_THREADS = 192;
+
+// Shared-memory plan for head dim HD (64 or 128):
+//   Q  [128 q, HD]   HD/64 atoms of 16 KB          K  [128 kv, HD]  HD/64 atoms of 16 KB
+//   Vt [HD, 128 kv]  2 atoms (kv halves) of HD * 128 bytes each
+//   P  [128 q, 128 kv] x 2 buffers
+template <int HD>
+struct AttPlan {
+  static constexpr int Q_BYTES = 128 * HD * 2;
+  static constexpr int K_BYTES = 128 * HD * 2;
+  static constexpr int V_ATOM = HD * 128;
+  static constexpr int V_BYTES = 2 * V_ATOM;
+  static constexpr int SMEM = Q_BYTES + KV_STAGES * (K_BYTES + V_BYTES) + 2 * P_BYTES + 1024 + 256;
+  static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, TK);
+  static constexpr uint32_t IDESC_O = idesc_bf16_f32(128, HD);
+};
+
+__device__ __forceinline__ bool wait_noabort(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait(a, parity)) return true;
+    if ((i & 255u) == 255u && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+template <int HD>
+__global__ void __launch_bounds__(ATT_THREADS, 1)
+    attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O, const AttnArgs args) {
+  if (args.status && (*reinterpret_cast<volatile int*>(args.status) & kDevLayout)) return;
+  const int count = *args.count;
+  const int head = blockIdx.x / args.max_items;
+  const int item_idx = blockIdx.x - head * args.max_items;
+  if (item_idx >= count || head >= args.n_heads) return;
+  const int2 item = args.items[item_idx];
+  const int doc = item.x, q0 = item.y;
+  const int ds = args.cu[doc], de = args.cu[doc + 1];
+  const int kv_base = (ds / TK) * TK;
+  const int n_kv = (de - kv_base + TK - 1) / TK;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  using Plan = AttPlan<HD>;
+  uint8_t* sQ = smem;
+  uint8_t* sK = sQ + Plan::Q_BYTES;                    // [stage]
+  uint8_t* sV = sK + KV_STAGES * Plan::K_BYTES;        // [stage]
+  uint8_t* sP = sV + KV_STAGES * Plan::V_BYTES;        // [2]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * P_BYTES);
+  uint64_t* q_full = bars;
+  uint64_t* kv_full = bars + 1;                        // [2]
+  uint64_t* kv_empty = bars + 3;                       // [2]
+  uint64_t* s_full = bars + 5;                         // [2]
+  uint64_t* p_full = bars + 7;                         // [2]
+  uint64_t* o_full = bars + 9;                         // [2]
+  uint64_t* mma_done = bars + 11;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+      mbar_init(&s_full[s], 1);
+      mbar_init(&p_full[s], 4);
+      mbar_init(&o_full[s], 1);
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t t_s = tmem;            // S buffers at columns 0, 128
+  const uint32_t t_o = tmem + 256;      // O partial buffers at columns 256, 256 + HD
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const int hx = head * HD;
+      mbar_arrive_expect_tx(q_full, Plan::Q_BYTES);
+#pragma unroll
+      for (int a = 0; a < HD / 64; ++a) tma_load_2d(sQ + a * ATOM, &tmQ, q_full, hx + 64 * a, q0);
+      int issued = 0;
+      for (int j = 0; j < n_kv; ++j) {
+        const int st = j & 1;
+        const uint32_t ph = (j >> 1) & 1;
+        if (!mbar_wait(&kv_empty[st], ph ^ 1, abort_flag, args.status)) break;
+        const int kv0 = kv_base + j * TK;
+        mbar_arrive_expect_tx(&kv_full[st], Plan::K_BYTES + Plan::V_BYTES);
+#pragma unroll
+        for (int a = 0; a < HD / 64; ++a)
+          tma_load_2d(sK + st * Plan::K_BYTES + a * ATOM, &tmK, &kv_full[st], hx + 64 * a, kv0);
+        tma_load_2d(sV + st * Plan::V_BYTES, &tmV, &kv_full[st], kv0, hx);
+        tma_load_2d(sV + st * Plan::V_BYTES + Plan::V_ATOM, &tmV, &kv_full[st], kv0 + 64, hx);
+        ++issued;
+      }
+      // Every copy this CTA issued must land before the CTA may exit.
+      wait_noabort(q_full, 0);
+      for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j) wait_noabort(&kv_full[j & 1], (j >> 1) & 1);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      bool ok = mbar_wait(q_full, 0, abort_flag, args.status);
+      tc_fence_after();
+      const uint32_t q_addr = smem_u32(sQ);
+      auto issue_s = [&](int j) -> bool {
+        const int st = j & 1;
+        if (!mbar_wait(&kv_full[st], (j >> 1) & 1, abort_flag, args.status)) return false;
+        tc_fence_after();
+        const uint32_t k_addr = smem_u32(sK + st * Plan::K_BYTES);
+#pragma unroll
+        for (int ks = 0; ks < HD / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * ATOM + (ks & 3) * 32;
+          umma_bf16(t_s + st * TK, sdesc_sw128(q_addr + off), sdesc_sw128(k_addr + off), Plan::IDESC_S, ks != 0);
+        }
+        umma_commit(&s_full[st]);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int j = 0; ok && j < n_kv; ++j) {
+        if (j + 1 < n_kv && !issue_s(j + 1)) break;
+        const int pb = j & 1;
+        if (!mbar_wait(&p_full[pb], (j >> 1) & 1, abort_flag, args.status)) break;
+        tc_fence_after();
+        const uint32_t p_addr = smem_u32(sP + pb * P_BYTES);
+        const uint32_t v_addr = smem_u32(sV + (j & 1) * Plan::V_BYTES);
+#pragma unroll
+        for (int ks = 0; ks < TK / 16; ++ks) {
+          const uint32_t p_off = (ks >> 2) * ATOM + (ks & 3) * 32;
+          const uint32_t v_off = (ks >> 2) * Plan::V_ATOM + (ks & 3) * 32;
+          umma_bf16(t_o + pb * HD, sdesc_sw128(p_addr + p_off), sdesc_sw128(v_addr + v_off), Plan::IDESC_O, ks != 0);
+        }
+        umma_commit(&o_full[pb]);
+        umma_commit(&kv_empty[j & 1]);
+      }
+      // No MMA may still read shared memory or write TMEM when the CTA tears down.
+      umma_commit(mma_done);
+      wait_noabort(mma_done, 0);
+    }
+  } else {
+    // ---------------- softmax warps ----------------
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;          // tile row owned by this thread
+    const int row = q0 + r;                     // packed-sequence row
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const float sc = args.scale_log2;
+    float acc[HD];
+#pragma unroll
+    for (int i = 0; i < HD; ++i) acc[i] = 0.f;
+    float m = -INFINITY, l = 0.f, alpha_prev = 1.f;
+    bool ok = true;
+
+    auto fold_o = [&](int jj, float alpha) -> bool {
+      const int pb = jj & 1;
+      if (!mbar_wait(&o_full[pb], (jj >> 1) & 1, abort_flag, args.status)) return false;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < HD; c += 32) {
+        uint32_t v[32];
+        tmem_ld32(t_o + pb * HD + lane_off + c, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[c + i] = fmaf(acc[c + i], alpha, __uint_as_float(v[i]));
+      }
+      return true;
+    };
+
+    for (int j = 0; j < n_kv; ++j) {
+      const int sb = j & 1;
+      if (!mbar_wait(&s_full[sb], (j >> 1) & 1, abort_flag, args.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int c0 = kv_base + j * TK;
+      const int lo = ds > c0 ? ds - c0 : 0;
+      const int hi = de - c0 < TK ? de - c0 : TK;
+      const uint32_t ts = t_s + sb * TK + lane_off;
+      // pass 1: row max of the scaled scores
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < TK; c += 32) {
+        uint32_t v[32];
+        tmem_ld32(ts + c, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int cc = c + i;
+          if (cc >= lo && cc < hi) mx = fmaxf(mx, __uint_as_float(v[i]));
+        }
+      }
+      const float m_new = fmaxf(m, mx * sc);
+      const float alpha = (m == -INFINITY) ? 0.f : fast_exp2(m - m_new);
+      // pass 2: p = exp2(s * sc - m_new), bf16 into shared memory (swizzled K-major A operand)
+      const uint32_t p_base = smem_u32(sP + sb * P_BYTES) + r * 128;
+      float rs = 0.f;
+#pragma unroll
+      for (int c = 0; c < TK; c += 32) {
+        uint32_t v[32];
+        tmem_ld32(ts + c, v);
+        tmem_ld_wait();
+        float p[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int cc = c + i;
+          p[i] = (cc >= lo && cc < hi) ? fast_exp2(fmaf(__uint_as_float(v[i]), sc, -m_new)) : 0.f;
+          rs += p[i];
+        }
+        const uint32_t atom = (c >> 6) * ATOM;
+#pragma unroll
+        for (int k8 = 0; k8 < 4; ++k8) {
+          const int chunk = ((c & 63) >> 3) + k8;  // 16-byte chunk within the 128-byte row
+          const uint32_t addr = p_base + atom + ((chunk ^ (r & 7)) << 4);
+          st_shared_v4(addr, pack_bf16x2(p[8 * k8 + 0], p[8 * k8 + 1]), pack_bf16x2(p[8 * k8 + 2], p[8 * k8 + 3]),
+                       pack_bf16x2(p[8 * k8 + 4], p[8 * k8 + 5]), pack_bf16x2(p[8 * k8 + 6], p[8 * k8 + 7]));
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[sb]);
+      l = l * alpha + rs;
+      m = m_new;
+      // fold the previous tile's partial O (computed relative to the previous max)
+      if (j > 0 && !fold_o(j - 1, alpha_prev)) {
+        ok = false;
+        break;
+      }
+      alpha_prev = alpha;
+    }
+    if (ok && n_kv > 0) ok = fold_o(n_kv - 1, alpha_prev);
+    if (ok && row < de) {
+      const float inv = 1.f / l;
+      __nv_bfloat16* orow = O + (size_t)row * (args.n_heads * HD) + head * HD;
+#pragma unroll
+      for (int c = 0; c < HD; c += 8)
+        st_global_v4(orow + c, pack_bf16x2(acc[c] * inv, acc[c + 1] * inv), pack_bf16x2(acc[c + 2] * inv, acc[c + 3] * inv),
+                     pack_bf16x2(acc[c + 4] * inv, acc[c + 5] * inv), pack_bf16x2(acc[c + 6] * inv, acc[c + 7] * inv));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// Validate the packed layout and emit the (document, q-tile) list, longest documents first.
+// Codes follow the layout contract: 1 no documents, 2 cu[0] != 0, 3 not strictly increasing,
+// 4 cu[D] != N, 5 a doc id disagrees with cu_seqlens, 6 a tag >= n_mod, 7 list overflow.
+__global__ void schedule_kernel(const int32_t* cu, int n_docs, int n_tokens, const int32_t* doc_ids,
+                                const uint8_t* tags, int n_mod, int2* items, int* count, int max_items,
+                                int* layout_code, int* status) {
+  __shared__ int code;
+  if (threadIdx.x == 0) {
+    code = 0;
+    if (n_docs < 1) code = 1;
+    else if (cu[0] != 0) code = 2;
+    else {
+      for (int j = 0; j < n_docs && !code; ++j)
+        if (cu[j + 1] <= cu[j]) code = 3;
+      if (!code && cu[n_docs] != n_tokens) code = 4;
+    }
+  }
+  __syncthreads();
+  if (code == 0 && doc_ids) {
+    for (int i = threadIdx.x; i < n_tokens; i += blockDim.x) {
+      const int j = doc_ids[i];
+      if (j < 0 || j >= n_docs || i < cu[j] || i >= cu[j + 1]) atomicCAS(&code, 0, 5);
+    }
+  }
+  __syncthreads();
+  if (code == 0 && tags) {
+    for (int i = threadIdx.x; i < n_tokens; i += blockDim.x)
+      if ((int)tags[i] >= n_mod) atomicCAS(&code, 0, 6);
+  }
+  __syncthreads();
+  if (threadIdx.x != 0) return;
+  int n = 0;
+  if (code == 0) {
+    // selection by length, longest first (n_docs is small; ties keep packing order)
+    int prev_len = 0x7fffffff, prev_idx = -1;
+    for (int k = 0; k < n_docs && !code; ++k) {
+      int best = -1, best_len = -1;
+      for (int j = 0; j < n_docs; ++j) {
+        const int len = cu[j + 1] - cu[j];
+        const bool after_prev = len < prev_len || (len == prev_len && j > prev_idx);
+        if (after_prev && len > best_len) {
+          best = j;
+          best_len = len;
+        }
+      }
+      prev_len = best_len;
+      prev_idx = best;
+      for (int q = cu[best]; q < cu[best + 1]; q += TQ) {
+        if (n >= max_items) {
+          code = 7;
+          break;
+        }
+        items[n++] = make_int2(best, q);
+      }
+    }
+  }
+  if (code) {
+    n = 0;
+    atomicOr(status, code == 7 ? kDevCapacity : kDevLayout);
+  }
+  *count = n;
+  if (layout_code) *layout_code = code;
+}
+
+int attention_max_items_impl(int n_docs, int n_tokens) { return (n_tokens + TQ - 1) / TQ + n_docs; }
+
+template <int HD>
+cudaError_t attention_launch_t(const void* q, const void* k, const void* vt, void* o, const AttnArgs& args,
+                               cudaStream_t stream);
+
+}  // namespace
+
+int attention_max_items(int n_docs, int n_tokens) { return attention_max_items_impl(n_docs, n_tokens); }
+
+cudaError_t attention_schedule_launch(const int32_t* cu, int n_docs, int n_tokens, const int32_t* doc_ids,
+                                      const uint8_t* tags, int n_mod, int2* items, int* count, int max_items,
+                                      int* layout_code, int* status, cudaStream_t stream) {
+  schedule_kernel<<<1, 256, 0, stream>>>(cu, n_docs, n_tokens, doc_ids, tags, n_mod, items, count, max_items,
+                                         layout_code, status);
+  return cudaGetLastError();
+}
+
+namespace {
+
+template <int HD>
+cudaError_t attention_launch_t(const void* q, const void* k, const void* vt, void* o, const AttnArgs& args,
+                               cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(attention_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         AttPlan<HD>::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int d = args.n_heads * HD;
+  CUtensorMap tq, tk, tv;
+  if (!make_tmap_bf16_2d(&tq, q, d, args.n_tokens, (uint64_t)d * 2, 64, TQ)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16_2d(&tk, k, d, args.n_tokens, (uint64_t)d * 2, 64, TK)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16_2d(&tv, vt, args.n_pad, d, (uint64_t)args.n_pad * 2, 64, HD)) return cudaErrorInvalidValue;
+  const int grid = args.max_items * args.n_heads;
+  if (grid <= 0) return cudaSuccess;
+  attention_kernel<HD><<<grid, ATT_THREADS, AttPlan<HD>::SMEM, stream>>>(tq, tk, tv, static_cast<__nv_bfloat16*>(o),
+                                                                          args);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t attention_launch(const void* q, const void* k, const void* vt, void* o, const AttnArgs& args,
+                             cudaStream_t stream) {
+  if (args.head_dim == 128) return attention_launch_t<128>(q, k, vt, o, args, stream);
+  if (args.head_dim == 64) return attention_launch_t<64>(q, k, vt, o, args, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace dit

@@ -1,0 +1,318 @@
+// Bandwidth-bound kernels of the forward: fused norm + indexed AdaLN modulate, the per-row RoPE
+// cos/sin cache, the AdaLN conditioning GEMV, the Euler step, and bind-time repacks.
+#include "common.cuh"
+#include "kernels.h"
+
+#include <math.h>
+
+namespace dit {
+
+namespace {
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Norm + indexed AdaLN modulate.  [H3] "The device-resident forward (W2b)": RmsNorm followed by
+// an indexed AdaLN modulate (shift/scale chosen per token by its modality tag).  One warp per row;
+// the row stays in registers between the statistics pass and the output pass; fp32 statistics.
+//   RMS:   n = x / sqrt(mean(x^2) + eps)
+//   LN:    n = (x - mean) / sqrt(mean((x - mean)^2) + eps) * g + b
+//   out    y = n * (1 + scale[tag]) + shift[tag]       (no modulation when shift == nullptr)
+// ---------------------------------------------------------------------------------------------
+template <int NV>
+__global__ void __launch_bounds__(256) norm_mod_kernel(const float* __restrict__ x, int n, int d, int norm, float eps,
+                                                       const float* __restrict__ g, const float* __restrict__ b,
+                                                       const uint8_t* __restrict__ tags,
+                                                       const float* __restrict__ shift,
+                                                       const float* __restrict__ scale, long long stride, void* y,
+                                                       int out_kind, const int* status) {
+  if (status && (*reinterpret_cast<const volatile int*>(status) & kDevLayout)) return;
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= n) return;
+  const float* xr = x + (size_t)row * d;
+  float4 v[NV];
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    v[i] = *reinterpret_cast<const float4*>(xr + (i * 32 + lane) * 4);
+    s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+  }
+  float mean = 0.f, inv;
+  if (norm == 0) {
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+    ss = warp_sum(ss);
+    inv = 1.0f / sqrtf(ss / (float)d + eps);
+  } else {
+    mean = warp_sum(s) / (float)d;
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const float a0 = v[i].x - mean, a1 = v[i].y - mean, a2 = v[i].z - mean, a3 = v[i].w - mean;
+      ss += a0 * a0 + a1 * a1 + a2 * a2 + a3 * a3;
+    }
+    ss = warp_sum(ss);
+    inv = 1.0f / sqrtf(ss / (float)d + eps);
+  }
+  const float* sh = shift ? shift + (size_t)tags[row] * stride : nullptr;
+  const float* sc = scale ? scale + (size_t)tags[row] * stride : nullptr;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int c = (i * 32 + lane) * 4;
+    float o[4] = {(v[i].x - mean) * inv, (v[i].y - mean) * inv, (v[i].z - mean) * inv, (v[i].w - mean) * inv};
+    if (norm == 1) {
+      if (g) {
+        const float4 gg = *reinterpret_cast<const float4*>(g + c);
+        o[0] *= gg.x; o[1] *= gg.y; o[2] *= gg.z; o[3] *= gg.w;
+      }
+      if (b) {
+        const float4 bb = *reinterpret_cast<const float4*>(b + c);
+        o[0] += bb.x; o[1] += bb.y; o[2] += bb.z; o[3] += bb.w;
+      }
+    }
+    if (sh) {
+      const float4 a = *reinterpret_cast<const float4*>(sh + c);
+      const float4 m = *reinterpret_cast<const float4*>(sc + c);
+      o[0] = o[0] * (1.f + m.x) + a.x;
+      o[1] = o[1] * (1.f + m.y) + a.y;
+      o[2] = o[2] * (1.f + m.z) + a.z;
+      o[3] = o[3] * (1.f + m.w) + a.w;
+    }
+    if (out_kind == 0) {
+      uint2 pk = make_uint2(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]));
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(y) + (size_t)row * d + c) = pk;
+    } else {
+      *reinterpret_cast<float4*>(static_cast<float*>(y) + (size_t)row * d + c) = make_float4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// RoPE cos/sin cache.  [BF] "What this enables": BuildRopeCosSin runs before any kernel with a
+// stored inv_freq; [H3] "The device-resident forward (W2b)": a per-row cos/sin cache whose angles
+// come from three axes of the fp64 position grid.  theta = pos[row][axis(j)] * (double)inv[j]
+// in fp64; cos and sin in fp64, rounded to fp32.
+// ---------------------------------------------------------------------------------------------
+struct RopeTable {
+  float inv[128];
+  unsigned char axis[128];
+};
+
+__global__ void rope_cache_kernel(const double* __restrict__ pos, int n, int half, const RopeTable tab,
+                                  float* __restrict__ cs, float* __restrict__ sn, const int* status) {
+  if (status && (*reinterpret_cast<const volatile int*>(status) & kDevLayout)) return;
+  const long long total = (long long)n * half;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total; i += (long long)gridDim.x * blockDim.x) {
+    const int row = (int)(i / half), j = (int)(i - (long long)row * half);
+    const double th = pos[(size_t)row * 3 + tab.axis[j]] * (double)tab.inv[j];
+    double s, c;
+    sincos(th, &s, &c);
+    cs[i] = (float)c;
+    sn[i] = (float)s;
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// AdaLN conditioning.  e = [cos(1000 t f_k) | sin(1000 t f_k)], f_k = exp(-ln(1e4) k / half)
+// (fp64), silu(e) in fp64 -> fp32 ([H3] "The device-resident forward (W2b)": the ungated SiLU;
+// the time embedder is an fp32 island per [H3] "Update: quantized arms land").  Then
+// mod[r] = W[r] . silu(e) + b[r], one warp per row, fp32 accumulation.
+// ---------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) adaln_kernel(const __nv_bfloat16* __restrict__ w, const float* __restrict__ b,
+                                                    int rows, int t_dim, float t, float* __restrict__ mod,
+                                                    const int* status) {
+  if (status && (*reinterpret_cast<const volatile int*>(status) & kDevLayout)) return;
+  extern __shared__ float se[];
+  const int half = t_dim / 2;
+  for (int k = threadIdx.x; k < half; k += blockDim.x) {
+    const double f = exp(-log(10000.0) * (double)k / (double)half);
+    const double a = 1000.0 * (double)t * f;
+    const double ec = cos(a), es = sin(a);
+    se[k] = (float)(ec / (1.0 + exp(-ec)));
+    se[half + k] = (float)(es / (1.0 + exp(-es)));
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += warps) {
+    const __nv_bfloat16* wr = w + (size_t)r * t_dim;
+    float acc = 0.f;
+    for (int k0 = lane * 8; k0 < t_dim; k0 += 256) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(wr + k0);
+      const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 f = __bfloat1622float2(p[q]);
+        acc = fmaf(f.x, se[k0 + 2 * q], acc);
+        acc = fmaf(f.y, se[k0 + 2 * q + 1], acc);
+      }
+    }
+    acc = warp_sum(acc);
+    if (lane == 0) mod[r] = acc + (b ? b[r] : 0.f);
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Euler-ancestral (eta = 0) step of the rectified flow, fp32, exactly this sequence of IEEE
+// round-to-nearest operations with no contraction ([H3] "Correctness gates": euler-ancestral
+// eta0 scheduler + rf_v_to_x0, gated exact):
+//   x0 = x - sigma * v;  x <- x0 + (sigma_next * (x - x0)) / sigma
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ float euler_one(float x, float v, float s, float sn) {
+  const float x0 = __fsub_rn(x, __fmul_rn(s, v));
+  const float q = __fdiv_rn(__fmul_rn(sn, __fsub_rn(x, x0)), s);
+  return __fadd_rn(x0, q);
+}
+
+__global__ void euler_kernel(float* __restrict__ x, const float* __restrict__ v, long long n, float s, float sn) {
+  const long long n4 = n / 4;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4; i += stride) {
+    float4 a = reinterpret_cast<float4*>(x)[i];
+    const float4 b = reinterpret_cast<const float4*>(v)[i];
+    a.x = euler_one(a.x, b.x, s, sn);
+    a.y = euler_one(a.y, b.y, s, sn);
+    a.z = euler_one(a.z, b.z, s, sn);
+    a.w = euler_one(a.w, b.w, s, sn);
+    reinterpret_cast<float4*>(x)[i] = a;
+  }
+  for (long long i = n4 * 4 + blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += stride)
+    x[i] = euler_one(x[i], v[i], s, sn);
+}
+
+__global__ void euler_kernel_scalar(float* __restrict__ x, const float* __restrict__ v, long long n, float s, float sn) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += stride)
+    x[i] = euler_one(x[i], v[i], s, sn);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Bind-time repacks
+// ---------------------------------------------------------------------------------------------
+// Packed row p of the FFN up projection: group g = p / 256, w = p % 256; value rows first.
+__global__ void pack_ffn_in_kernel(const __nv_bfloat16* __restrict__ src, const float* __restrict__ b_src, int F, int d,
+                                   __nv_bfloat16* __restrict__ dst, float* __restrict__ b_dst) {
+  const int p = blockIdx.x;
+  const int g = p >> 8, w = p & 255;
+  const int s = w < 128 ? 128 * g + w : F + 128 * g + (w - 128);
+  const uint4* in = reinterpret_cast<const uint4*>(src + (size_t)s * d);
+  uint4* out = reinterpret_cast<uint4*>(dst + (size_t)p * d);
+  for (int i = threadIdx.x; i < d / 8; i += blockDim.x) out[i] = in[i];
+  if (threadIdx.x == 0) b_dst[p] = b_src ? b_src[s] : 0.f;
+}
+
+__global__ void to_f32_kernel(const void* __restrict__ src, int is_bf16, long long n, float* __restrict__ dst) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+    dst[i] = is_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(src)[i]) : static_cast<const float*>(src)[i];
+}
+
+template <int NV>
+cudaError_t norm_launch_t(const float* x, int n, int d, int norm, float eps, const float* g, const float* b,
+                          const uint8_t* tags, const float* shift, const float* scale, long long stride, void* y,
+                          int out_kind, const int* status, cudaStream_t s) {
+  const int rows_per_block = 8;
+  norm_mod_kernel<NV><<<(n + rows_per_block - 1) / rows_per_block, 32 * rows_per_block, 0, s>>>(
+      x, n, d, norm, eps, g, b, tags, shift, scale, stride, y, out_kind, status);
+  return cudaGetLastError();
+}
+
+int grid_for(long long work, int threads) {
+  long long g = (work + threads - 1) / threads;
+  const long long cap = (long long)num_sms() * 8;
+  if (g > cap) g = cap;
+  return g < 1 ? 1 : (int)g;
+}
+
+}  // namespace
+
+int num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+
+cudaError_t norm_modulate_launch(const float* x, int n, int d, int norm, float eps, const float* ln_g,
+                                 const float* ln_b, const uint8_t* tags, const float* shift, const float* scale,
+                                 long long mod_stride, void* y, int out_kind, const int* status, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  switch (d / 128) {
+#define DIT_NV(k) \
+  case k: return norm_launch_t<k>(x, n, d, norm, eps, ln_g, ln_b, tags, shift, scale, mod_stride, y, out_kind, status, s);
+    DIT_NV(1) DIT_NV(2) DIT_NV(3) DIT_NV(4) DIT_NV(5) DIT_NV(6) DIT_NV(8) DIT_NV(10) DIT_NV(12) DIT_NV(16)
+    DIT_NV(20) DIT_NV(24) DIT_NV(32) DIT_NV(40) DIT_NV(48) DIT_NV(64)
+#undef DIT_NV
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+bool norm_width_supported(int d) {
+  if (d <= 0 || d % 128) return false;
+  switch (d / 128) {
+    case 1: case 2: case 3: case 4: case 5: case 6: case 8: case 10: case 12: case 16: case 20: case 24:
+    case 32: case 40: case 48: case 64: return true;
+    default: return false;
+  }
+}
+
+cudaError_t rope_cache_launch(const double* pos, int n, int n_axes, const int* dims, double base, float* cos_out,
+                              float* sin_out, const int* status, cudaStream_t s) {
+  RopeTable tab;
+  int half = 0;
+  for (int a = 0; a < n_axes; ++a)
+    for (int k = 0; k < dims[a] / 2; ++k) {
+      if (half >= 128) return cudaErrorInvalidValue;
+      tab.inv[half] = (float)pow(base, -2.0 * (double)k / (double)dims[a]);
+      tab.axis[half] = (unsigned char)a;
+      ++half;
+    }
+  if (n <= 0 || half == 0) return cudaSuccess;
+  rope_cache_kernel<<<grid_for((long long)n * half, 256), 256, 0, s>>>(pos, n, half, tab, cos_out, sin_out, status);
+  return cudaGetLastError();
+}
+
+cudaError_t adaln_launch(const void* w, const float* b, int rows, int t_dim, float t, float* mod, const int* status,
+                         cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  const int warps_per_block = 8;
+  int blocks = (rows + warps_per_block - 1) / warps_per_block;
+  if (blocks > num_sms() * 8) blocks = num_sms() * 8;
+  adaln_kernel<<<blocks, 32 * warps_per_block, t_dim * sizeof(float), s>>>(
+      static_cast<const __nv_bfloat16*>(w), b, rows, t_dim, t, mod, status);
+  return cudaGetLastError();
+}
+
+cudaError_t euler_launch(float* x, const float* v, long long n, float sigma, float sigma_next, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  const bool aligned = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(v)) & 15) == 0;
+  if (aligned)
+    euler_kernel<<<grid_for(n / 4 + 1, 256), 256, 0, s>>>(x, v, n, sigma, sigma_next);
+  else
+    euler_kernel_scalar<<<grid_for(n, 256), 256, 0, s>>>(x, v, n, sigma, sigma_next);
+  return cudaGetLastError();
+}
+
+cudaError_t pack_ffn_in_launch(const void* w_in, const float* b_in, int F, int d, void* w_packed, float* b_packed,
+                               cudaStream_t s) {
+  pack_ffn_in_kernel<<<2 * F, 128, 0, s>>>(static_cast<const __nv_bfloat16*>(w_in), b_in, F, d,
+                                           static_cast<__nv_bfloat16*>(w_packed), b_packed);
+  return cudaGetLastError();
+}
+
+cudaError_t to_f32_launch(const void* src, int src_is_bf16, long long n, float* dst, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  to_f32_kernel<<<grid_for(n, 256), 256, 0, s>>>(src, src_is_bf16, n, dst);
+  return cudaGetLastError();
+}
+
+}  // namespace dit

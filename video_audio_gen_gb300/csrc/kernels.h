@@ -1,0 +1,82 @@
+// Internal launcher interface between the C ABI (api.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace dit {
+
+// Epilogue kinds of the tcgen05 GEMM engine.
+enum GemmEpilogue : int {
+  kEpiStore = 0,        // out = acc + bias (bf16 or fp32)
+  kEpiQkvRope = 1,      // q, k: + bias, NeoX RoPE, bf16 [M, d]; v: + bias, bf16 transposed [d, n_pad]
+  kEpiGatedResid = 2,   // x += gate[tag] * (acc + bias), fp32 in place
+  kEpiSwiglu = 3,       // h = (u + b_u) * silu(g + b_g), interleaved 128-feature groups, bf16 [M, F]
+};
+
+struct GemmArgs {
+  int M, N, K;
+  const float* bias;       // [N] or nullptr
+  // kEpiStore
+  void* out;
+  int out_kind;            // 0 bf16, 1 fp32
+  // kEpiQkvRope
+  int d, head_dim, rot_half;
+  const float* cos_cache;  // [M, rot_half]
+  const float* sin_cache;
+  void* q;
+  void* k;
+  void* vt;
+  int n_pad;
+  // kEpiGatedResid
+  float* x;
+  const float* gate;
+  long long gate_stride;
+  const uint8_t* tags;
+  // common
+  int* status;             // device status word (may be null)
+  int group_n;             // N-blocks per raster group (L2 reuse of B)
+};
+
+// Launch D = A B^T with the given epilogue.  A bf16 [M, K], B bf16 [N, K].  Returns a CUDA error.
+cudaError_t gemm_launch(int epilogue, const void* A, const void* B, const GemmArgs& args, cudaStream_t stream);
+
+// Attention: q, k bf16 [N, H*Dh], vt bf16 [H*Dh, n_pad], o bf16 [N, H*Dh].  `items` is the
+// device tile list built by attention_schedule_launch (int2 {doc, q_start}), `count` its length.
+struct AttnArgs {
+  int n_tokens, n_heads, head_dim, n_pad, n_docs;
+  const int32_t* cu;
+  const int2* items;
+  const int* count;
+  int max_items;
+  float scale_log2;   // log2(e) / sqrt(Dh)
+  int* status;
+};
+cudaError_t attention_launch(const void* q, const void* k, const void* vt, void* o, const AttnArgs& args,
+                             cudaStream_t stream);
+
+// Validates cu_seqlens (and doc_ids / tags when given) and writes the (doc, q_start) tile list,
+// longest documents first.  On a bad layout sets kDevLayout in *status and writes count = 0.
+cudaError_t attention_schedule_launch(const int32_t* cu, int n_docs, int n_tokens, const int32_t* doc_ids,
+                                      const uint8_t* tags, int n_mod, int2* items, int* count, int max_items,
+                                      int* layout_code, int* status, cudaStream_t stream);
+int attention_max_items(int n_docs, int n_tokens);
+
+// Elementwise / reduction kernels.
+cudaError_t norm_modulate_launch(const float* x, int n, int d, int norm, float eps, const float* ln_g,
+                                 const float* ln_b, const uint8_t* tags, const float* shift, const float* scale,
+                                 long long mod_stride, void* y, int out_kind, const int* status, cudaStream_t s);
+cudaError_t rope_cache_launch(const double* pos, int n, int n_axes, const int* dims, double base, float* cos_out,
+                              float* sin_out, const int* status, cudaStream_t s);
+cudaError_t adaln_launch(const void* w, const float* b, int rows, int t_dim, float t, float* mod, const int* status,
+                         cudaStream_t s);
+cudaError_t euler_launch(float* x, const float* v, long long n, float sigma, float sigma_next, cudaStream_t s);
+cudaError_t pack_ffn_in_launch(const void* w_in, const float* b_in, int F, int d, void* w_packed, float* b_packed,
+                               cudaStream_t s);
+cudaError_t to_f32_launch(const void* src, int src_is_bf16, long long n, float* dst, cudaStream_t s);
+
+int num_sms();
+bool norm_width_supported(int d);
+
+}  // namespace dit
