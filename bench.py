@@ -1,0 +1,428 @@
+"""Benchmark: DiT forward tokens/s and ms/forward on GB300, with the roofline of the dominant kernel.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+One step = one DiT forward (every block: norm+modulate, QKV GEMM with RoPE, varlen attention,
+out-projection with gated residual, FFN up with SiLU gate, FFN down with gated residual, final
+norm) over the packed sequence of the workload, inputs already resident in HBM.  The denoise_loop
+workload's step is one denoise step (forward + Euler step).  Prints ONE JSON line on rank 0.
+
+--impl reference times the CPU oracle (the plain double-precision statement of the same forward)
+on the host cores on a bounded sample of the workload, scaled to the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "DiT forward tokens/s & ms/forward on 1 GB300; % of bf16 tensor-pipe peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KINDS = ["gemm_qkv", "attention", "gemm_out", "gemm_ffn_up", "gemm_ffn_down", "norm_modulate", "other"]
+
+# DRAM traffic per launch from ncu captures (dram__bytes_read.sum + dram__bytes_write.sum), keyed by
+# kernel kind and workload, with the sha256 of the kernel source the capture was taken on; the
+# figure is reported only while the source is unchanged.  See profiles/.
+TRAFFIC = {}
+
+
+# ------------------------------------------------------------------------------------------------
+# host logic shared with the multi-process tests
+# ------------------------------------------------------------------------------------------------
+
+def rank_documents(docs: list, rank: int, world: int) -> list:
+    """Weak scaling: every rank runs its own copy of the workload's documents (independent requests,
+    no data-path exchange).  Returns this rank's document list."""
+    assert 0 <= rank < world
+    return [dict(d) for d in docs]
+
+
+def rank_seed(seed: int, rank: int) -> int:
+    return seed + 1000 * rank
+
+
+def reduce_max_ms(ms: float, dist=None) -> float:
+    """Max of a per-rank time over the process group (identity without one)."""
+    if dist is None or not dist.is_initialized():
+        return ms
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def step_flops(m: dict, cu) -> dict:
+    """Algorithmic FLOPs of one forward, per kernel kind (per launch x L)."""
+    N = int(cu[-1])
+    d, F, L = m["hidden"], m["ffn_hidden"], m["n_blocks"]
+    s2 = sum(int(cu[j + 1] - cu[j]) ** 2 for j in range(len(cu) - 1))
+    per = {"gemm_qkv": 2.0 * N * 3 * d * d, "attention": 4.0 * s2 * d, "gemm_out": 2.0 * N * d * d,
+           "gemm_ffn_up": 2.0 * N * 2 * F * d, "gemm_ffn_down": 2.0 * N * d * F}
+    return {"per_launch": per, "total": L * sum(per.values())}
+
+
+def norm_bytes(m: dict, N: int) -> float:
+    """Algorithmic HBM bytes of one norm+modulate launch: fp32 row in, bf16 row out, one tag byte."""
+    return N * m["hidden"] * (4 + 2) + N
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def source_hash(name: str) -> str:
+    with open(os.path.join(ROOT, "video_audio_gen_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU baseline: the oracle on a bounded sample of the workload
+# ------------------------------------------------------------------------------------------------
+
+def oracle_sample(w: dict, lay: dict, budget_rows: int | None = None):
+    """Time the oracle computing one block for a sample of R query rows of the workload: norm and
+    modulate, the QKV projection and RoPE of those rows, attention of those rows over the full
+    document (keys/values of the document are seeded inputs), the output projection with gated
+    residual and the gated FFN.  Scaled to tokens/s of the whole forward: R rows x 1 block per
+    sample; the forward is N rows x L blocks.  Returns (tokens_per_s, seconds, rows, threads)."""
+    import oracle
+    import synth
+    m = w["model"]
+    d, F, H, Dh = m["hidden"], m["ffn_hidden"], m["n_heads"], m["head_dim"]
+    threads = len(os.sched_getaffinity(0))
+    oracle.set_threads(threads)
+    R = budget_rows or 2 * threads
+    cu = lay["cu_seqlens"]
+    # the sample's rows: spread over the longest document
+    j = int(np.argmax(np.diff(cu)))
+    a, b = int(cu[j]), int(cu[j + 1])
+    rows = np.linspace(a, b - 1, R).astype(np.int64)
+    seed = w["seed"]
+    x = synth.normal(seed, "sample.x", (R, d), 1.0)
+    wq, _ = synth.normal(seed, "block0.w_qkv", (3 * d, d), w["w_std"], bf16=True)
+    wo, _ = synth.normal(seed, "block0.w_o", (d, d), w["w_std"], bf16=True)
+    wi, _ = synth.normal(seed, "block0.w_in", (2 * F, d), w["w_std"], bf16=True)
+    wd, _ = synth.normal(seed, "block0.w_down", (d, F), w["w_std"], bf16=True)
+    S = b - a
+    kdoc = synth.normal(seed, "sample.k", (S, d), 1.0)
+    vdoc = synth.normal(seed, "sample.v", (S, d), 1.0)
+    shift = synth.normal(seed, "sample.mod", (6, d), 0.1)
+    tags = np.zeros(R, dtype=np.uint8)
+    sub = dict(m, n_blocks=1)
+    t0 = time.perf_counter()
+    y = oracle.modulate(oracle.rms_norm(x, m["norm_eps"]), tags, shift[0:1], shift[1:2])
+    qkv = oracle.linear(y, wq, None)
+    cs, sn = oracle.rope_cos_sin(sub, lay["pos"][rows])
+    q = oracle.rope_apply(qkv[:, :d], H, Dh, m["rotary_dim"], cs, sn)
+    # attention of the sampled rows over the whole document: the rows are placed first in a local
+    # sequence whose keys/values are the document's
+    qfull = np.zeros((S, d))
+    qfull[:R] = q
+    o = oracle.attention_rows(qfull, kdoc, vdoc, np.array([0, S], dtype=np.int32), H, Dh, np.arange(R))
+    xo = x + shift[2] * oracle.linear(o, wo, None)
+    y2 = oracle.modulate(oracle.rms_norm(xo, m["norm_eps"]), tags, shift[3:4], shift[4:5])
+    hh = oracle.swiglu(oracle.linear(y2, wi, None))
+    _ = xo + shift[5] * oracle.linear(hh, wd, None)
+    dt = time.perf_counter() - t0
+    oracle.set_threads(1)
+    per_token_block = dt / R
+    tokens_per_s = 1.0 / (per_token_block * m["n_blocks"])
+    return tokens_per_s, dt, R, threads
+
+
+# ------------------------------------------------------------------------------------------------
+# GPU arm
+# ------------------------------------------------------------------------------------------------
+
+def run_gpu(args, w, dist, rank, world):
+    import torch
+
+    import synth
+    from tests import gpu_util
+    from video_audio_gen_gb300 import dit
+
+    dev = torch.cuda.current_device()
+    m = w["model"]
+    docs = rank_documents(w["docs"], rank, world)
+    lay = synth.build_layout(docs)
+    wr = dict(w, seed=rank_seed(w["seed"], rank))
+    W = synth.make_weights(wr)
+    h = gpu_util.make_handle(m, lay, W)
+    del W
+    N, D = lay["n_tokens"], lay["n_docs"]
+    dl = gpu_util.dev_layout(lay)
+    x_host = synth.make_tokens(wr, lay)
+    x = gpu_util.dev_f32(x_host)
+    out = torch.empty_like(x)
+    ws = gpu_util.workspace(h, N, D)
+    t_step = synth.timestep(w) if w["t"] != "schedule" else 1.0
+    loop = w["t"] == "schedule"
+    sig = synth.sigmas(w.get("steps", 50))
+    stream = torch.cuda.current_stream()
+
+    def one_step(i):
+        if loop:
+            k = i % (len(sig) - 1)
+            h.forward(x, dl["cu"], dl["ids"], dl["tags"], dl["pos"], float(sig[k]), out, ws)
+            dit.euler_step(x, out, float(sig[k]), float(sig[k + 1]))
+        else:
+            h.forward(x, dl["cu"], dl["ids"], dl["tags"], dl["pos"], t_step, out, ws)
+
+    for i in range(args.warmup):
+        one_step(i)
+    assert h.sync_status(ws) == 0, "device status after warm-up"
+    torch.cuda.synchronize()
+    launches0 = h.stats()["kernels_launched"]
+    h.set_kernel_timing(True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev) as clk:
+        e0.record(stream)
+        for i in range(args.steps):
+            one_step(args.warmup + i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    ms_total = e0.elapsed_time(e1)
+    kt = h.kernel_times()
+    h.set_kernel_timing(False)
+    launches = h.stats()["kernels_launched"] - launches0
+    assert h.sync_status(ws) == 0, "device status after the timed region"
+    ms_total = reduce_max_ms(ms_total, dist)
+    ms_step = ms_total / args.steps
+
+    # roofline of the dominant kernel kind (largest summed time), from its CUDA-event durations
+    fl = step_flops(m, lay["cu_seqlens"])
+    peaks, peak_src = load_peaks()
+    kernels = {}
+    for k in KINDS:
+        ms, n = kt[k]
+        if n == 0:
+            continue
+        avg = ms / n
+        entry = {"launches": n, "avg_ms": round(avg, 4), "share": None}
+        if k in fl["per_launch"]:
+            tf = fl["per_launch"][k] / (avg * 1e-3) / 1e12
+            entry.update(bound="tensor", achieved_tflops=round(tf, 1),
+                         frac=round(tf / peaks["bf16_tflops_sustained"], 3))
+        elif k == "norm_modulate":
+            gbs = norm_bytes(m, N) / (avg * 1e-3) / 1e9
+            entry.update(bound="hbm", achieved_gbs=round(gbs, 1), frac=round(gbs / peaks["hbm_gbs"], 3))
+        kernels[k] = entry
+    tot = sum(kt[k][0] for k in KINDS)
+    for k in kernels:
+        kernels[k]["share"] = round(kt[k][0] / tot, 3) if tot else None
+    top = max((k for k in kernels if k in fl["per_launch"]), key=lambda k: kt[k][0])
+    src = "attention.cu" if top == "attention" else "gemm.cu"
+    tr = TRAFFIC.get((top, args.workload))
+    traffic = tr["bytes"] if tr and tr["src_sha"] == source_hash(src) else None
+    roofline = {"bound": "tensor", "kernel": top, "achieved": kernels[top]["achieved_tflops"],
+                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s", "frac": kernels[top]["frac"],
+                "traffic": traffic, "peak_source": f"bf16_tflops_sustained of {peak_src}",
+                "algorithmic_flops_per_launch": fl["per_launch"][top]}
+
+    if args.no_e2e:
+        return dict(ms_step=ms_step, tokens=N, world=world, kernels=kernels, roofline=roofline, clocks=clk.summary(),
+                    launches=launches, e2e_ms=float("nan"), h2d=0, d2h=0, flops=fl["total"], docs=D, lay=lay)
+    # end to end through the C ABI from pinned host buffers (copies inside the timed region)
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    hx, hcu = pin(x_host), pin(lay["cu_seqlens"].astype(np.int32))
+    hids, htags, hpos = pin(lay["doc_ids"].astype(np.int32)), pin(lay["tags"]), pin(lay["pos"])
+    hout = torch.empty(x_host.shape, dtype=torch.float32).pin_memory()
+    wsh = gpu_util.workspace(h, N, D, host=True)
+    for _ in range(2):
+        h.forward_host(hx, hcu, hids, htags, hpos, t_step, hout, wsh)
+    e2e_steps = max(3, min(args.steps, 10))
+    if dist is not None:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        h.forward_host(hx, hcu, hids, htags, hpos, t_step, hout, wsh)
+    e2e_ms = reduce_max_ms((time.perf_counter() - t0) * 1e3 / e2e_steps, dist)
+    h2d = hx.numel() * 4 + hcu.numel() * 4 + hids.numel() * 4 + htags.numel() + hpos.numel() * 8
+    d2h = hout.numel() * 4
+    return dict(ms_step=ms_step, tokens=N, world=world, kernels=kernels, roofline=roofline, clocks=clk.summary(),
+                launches=launches, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, flops=fl["total"], docs=D, lay=lay)
+
+
+def workload_config(name, w, lay, extra=None):
+    m = w["model"]
+    docs = ", ".join(f"{synth_doc(d)}" for d in w["docs"])
+    c = {"workload": f"{name}: {m['n_blocks']} blocks, d={m['hidden']}, {m['n_heads']}x{m['head_dim']} heads, "
+                     f"FFN {m['ffn_hidden']} (value*silu(gate)), {m['norm']}norm + modality AdaLN; "
+                     f"{lay['n_tokens']} packed tokens in {lay['n_docs']} documents ({docs})",
+         "tokens": int(lay["n_tokens"]), "documents": int(lay["n_docs"]),
+         "cu_seqlens": [int(v) for v in lay["cu_seqlens"]],
+         "l2": "inputs larger than L2 (bf16 weights and fp32 activations of several GB stream every step)"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+def synth_doc(d):
+    if "frames" in d:
+        return f"{d['frames']} frames"
+    t, hh, ww = d.get("video", (0, 0, 0))
+    return f"video {t}x{hh}x{ww}" + (f" + {d['audio']} audio" if d.get("audio") else "")
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="video_audio_bf16",
+                    choices=["video_audio_bf16", "long_doc_bf16", "denoise_loop", "video_audio_bf16_l1", "tiny",
+                             "ragged"])
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    import synth
+    w = synth.WORKLOADS[args.workload]
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    is_loop = w["t"] == "schedule"
+    metric = METRIC if not is_loop else "DiT denoise step ms/step (forward + Euler) and tokens/s on 1 GB300"
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        lay = synth.build_layout(w["docs"])
+        vals, secs = [], []
+        for _ in range(args.steps):
+            tps, dt, R, threads = oracle_sample(w, lay)
+            vals.append(tps)
+            secs.append(dt)
+        tps = statistics.median(vals)
+        ms_step = lay["n_tokens"] / tps * 1e3
+        sample = (f"{R} query rows x 1 block of the workload per step ({args.steps} steps, median), "
+                  f"scaled by N={lay['n_tokens']} rows x L={w['model']['n_blocks']} blocks")
+        line = {"impl": "reference", "metric": metric, "value": round(tps, 4), "unit": "tokens/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 1),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": workload_config(args.workload, w, lay),
+                "cpu_baseline": {"value": round(tps, 4), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                                 "sample": sample},
+                "e2e": {"value": round(tps, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        local = int(os.environ.get("LOCAL_RANK", "0"))
+        torch.cuda.set_device(local)
+        tdist.init_process_group("nccl")
+        dist = tdist
+    r = run_gpu(args, w, dist, rank, world)
+    if rank == 0:
+        tokens_total = r["tokens"] * world
+        value = tokens_total / (r["ms_step"] * 1e-3)
+        tflops = r["flops"] / (r["ms_step"] * 1e-3) / 1e12
+        peaks, peak_src = load_peaks()
+        line = {"metric": metric, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(r["ms_step"], 3),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic (seeded N(0, 0.02) bf16 weights, N(0, 1) fp32 tokens)",
+                "config": workload_config(args.workload, w, r["lay"], {
+                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                    "forward_tflop": round(r["flops"] / 1e12, 3),
+                    "step_tflops": round(tflops, 1),
+                    "step_frac_of_bf16_peak": round(tflops / peaks["bf16_tflops_sustained"], 3)}),
+                "roofline": r["roofline"], "kernels": r["kernels"],
+                "e2e": {"value": round(tokens_total / (r["e2e_ms"] * 1e-3), 1), "unit": "tokens/s",
+                        "ms_per_step": round(r["e2e_ms"], 3), "h2d_bytes_per_step": int(r["h2d"]),
+                        "d2h_bytes_per_step": int(r["d2h"])},
+                "gpu_launches": int(r["launches"]), "clocks": r["clocks"]}
+        if not args.no_cpu_baseline:
+            tps, dt, R, threads = oracle_sample(w, r["lay"])
+            line["cpu_baseline"] = {"value": round(tps, 4), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                                    "sample": f"{R} query rows x 1 block ({dt:.1f} s on {threads} threads), "
+                                              f"scaled by N={r['tokens']} rows x L={w['model']['n_blocks']} blocks"}
+        print(json.dumps(line))
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

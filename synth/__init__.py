@@ -171,6 +171,11 @@ WORKLOADS = {
     "denoise_loop": dict(model=C2_MODEL, seed=4,
                          docs=[dict(video=(8, 32, 64), audio=1024), dict(video=(4, 32, 64), audio=1024)],
                          t="schedule", steps=50, w_std=0.02, bias_std=0.0, x_std=1.0),
+    # One block of the video+audio model on its full 17,408-token sequence: every kernel launch has
+    # exactly the full workload's shape, with a few GB on the device (profiling captures).
+    "video_audio_bf16_l1": dict(model=dict(C2_MODEL, n_blocks=1), seed=2,
+                                docs=[dict(video=(8, 32, 32), audio=512), dict(video=(8, 32, 32), audio=512)],
+                                t="uniform", w_std=0.02, bias_std=0.0, x_std=1.0),
     # Parity cases that span several 128-row tiles with ragged document ends, a 1-token document and
     # non-zero biases (the oracle finishes them in seconds).
     "ragged": dict(model=_model(n_blocks=2, hidden=512, n_heads=4, head_dim=128, ffn_hidden=1536,

@@ -28,6 +28,7 @@ constexpr int B_BYTES = BN * BK * 2;   // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int GEMM_THREADS = 192;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int SMEM_BYTES_RESID = SMEM_BYTES + BM * 64 * 4;  // + the residual epilogue's staging tile
 constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
 
 struct TileCoord {
@@ -183,32 +184,77 @@ __device__ __forceinline__ void epi_qkv(const GemmArgs& a, uint32_t t, int row, 
 }
 
 // x[row, n0 + c] += gate[tag[row]][n0 + c] * (acc + bias)     (gate == nullptr: plain add)
-__device__ __forceinline__ void epi_resid(const GemmArgs& a, uint32_t t, int row, int n0) {
-  const bool live = row < a.M;
-  const float* g = nullptr;
-  float* xr = nullptr;
-  if (live) {
-    if (a.gate) g = a.gate + (size_t)a.tags[row] * a.gate_stride + n0;
-    xr = a.x + (size_t)row * a.N + n0;
-  }
+//
+// The residual stream is fp32 in HBM, so this epilogue is a read-modify-write of a 128 x 256 fp32
+// tile.  TMEM hands each thread one row, which would make every global access a 32-row scatter;
+// instead the tile goes through shared memory 64 columns at a time:
+//   phase A  each thread moves its row's 64 accumulator columns TMEM -> registers -> shared memory
+//            (16-byte chunks XOR-swizzled by row so a warp's stores spread over all banks)
+//   phase B  each warp walks 32 rows; per row its 32 lanes own 2 adjacent columns, so the loads and
+//            stores of x (and of the gate and bias) are 256 contiguous bytes per row.
+constexpr int RES_COLS = 64;
+constexpr int RES_STAGE_BYTES = BM * RES_COLS * 4;  // 32 KB
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ void epi_resid(const GemmArgs& a, uint32_t t, int tile_row0, int quarter, int ew, int n0,
+                                          float* stage, uint64_t* tempty_bar) {
+  const int lane = threadIdx.x & 31;
+  const int r_own = quarter * 32 + lane;  // the tile row whose TMEM lane this thread reads
+  const uint32_t st_row = smem_u32(stage) + r_own * (RES_COLS * 4);
 #pragma unroll 1
-  for (int c = 0; c < BN; c += 32) {
-    uint32_t r[32];
-    tmem_ld32(t + c, r);
-    tmem_ld_wait();
-    if (!live) continue;
+  for (int c0 = 0; c0 < BN; c0 += RES_COLS) {
+    // phase A: TMEM -> shared memory (swizzled)
 #pragma unroll
-    for (int i = 0; i < 32; i += 4) {
-      float b[4];
-      load_bias4(a.bias, n0 + c + i, b);
-      float4 xv = *reinterpret_cast<float4*>(xr + c + i);
-      float4 gv = g ? *reinterpret_cast<const float4*>(g + c + i) : make_float4(1.f, 1.f, 1.f, 1.f);
-      xv.x += gv.x * (__uint_as_float(r[i + 0]) + b[0]);
-      xv.y += gv.y * (__uint_as_float(r[i + 1]) + b[1]);
-      xv.z += gv.z * (__uint_as_float(r[i + 2]) + b[2]);
-      xv.w += gv.w * (__uint_as_float(r[i + 3]) + b[3]);
-      *reinterpret_cast<float4*>(xr + c + i) = xv;
+    for (int h = 0; h < RES_COLS; h += 32) {
+      uint32_t r[32];
+      tmem_ld32(t + c0 + h, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int chunk = (h >> 2) + q;  // 16-byte chunk index within the 256-byte row
+        st_shared_v4(st_row + ((chunk ^ (r_own & 7)) << 4), r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
+      }
     }
+    if (c0 + RES_COLS == BN) {
+      // every accumulator column of this tile is out of TMEM: hand the buffer back to the MMA warp
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar);
+    }
+    epi_bar();
+    // phase B: coalesced read-modify-write of 32 rows x 64 columns per warp
+    const int col = n0 + c0 + 2 * lane;
+    float2 bb = make_float2(0.f, 0.f);
+    if (a.bias) bb = *reinterpret_cast<const float2*>(a.bias + col);
+    const int chunk = lane >> 1, half8 = (lane & 1) * 8;
+#pragma unroll 1
+    for (int rr0 = 0; rr0 < 32; rr0 += 8) {
+      float2 acc[8], xv[8], gv[8];
+      int rows[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int rt = ew * 32 + rr0 + u;
+        rows[u] = tile_row0 + rt;
+        const uint32_t sa = smem_u32(stage) + rt * (RES_COLS * 4) + ((chunk ^ (rt & 7)) << 4) + half8;
+        asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(acc[u].x), "=f"(acc[u].y) : "r"(sa));
+        if (rows[u] < a.M) {
+          xv[u] = *reinterpret_cast<const float2*>(a.x + (size_t)rows[u] * a.N + col);
+          gv[u] = a.gate ? *reinterpret_cast<const float2*>(a.gate + (size_t)a.tags[rows[u]] * a.gate_stride + col)
+                         : make_float2(1.f, 1.f);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (rows[u] < a.M) {
+          float2 o;
+          o.x = xv[u].x + gv[u].x * (acc[u].x + bb.x);
+          o.y = xv[u].y + gv[u].y * (acc[u].y + bb.y);
+          *reinterpret_cast<float2*>(a.x + (size_t)rows[u] * a.N + col) = o;
+        }
+      }
+    }
+    epi_bar();  // the staging buffer is reused by the next column block
   }
 }
 
@@ -256,6 +302,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* res_stage = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES + 256);  // residual epilogue only
 
   if (args.status && (*reinterpret_cast<volatile int*>(args.status) & kDevLayout)) return;
 
@@ -359,13 +406,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const int row = tc.mb * BM + quarter * 32 + lane;
       const uint32_t t = tmem + acc * BN + (static_cast<uint32_t>(quarter * 32) << 16);
       const int n0 = tc.nb * BN;
-      if (EPI == kEpiStore) epi_store(args, t, row, n0);
-      if (EPI == kEpiQkvRope) epi_qkv(args, t, row, n0);
-      if (EPI == kEpiGatedResid) epi_resid(args, t, row, n0);
-      if (EPI == kEpiSwiglu) epi_swiglu(args, t, row, n0);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (EPI == kEpiGatedResid) {
+        epi_resid(args, t, tc.mb * BM, quarter, warp - 2, n0, res_stage, &tempty[acc]);
+      } else {
+        if (EPI == kEpiStore) epi_store(args, t, row, n0);
+        if (EPI == kEpiQkvRope) epi_qkv(args, t, row, n0);
+        if (EPI == kEpiSwiglu) epi_swiglu(args, t, row, n0);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
@@ -381,9 +431,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
 template <int EPI>
 cudaError_t launch_t(const void* A, const void* B, const GemmArgs& args, cudaStream_t stream) {
+  constexpr int smem = EPI == kEpiGatedResid ? SMEM_BYTES_RESID : SMEM_BYTES;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -392,7 +443,7 @@ cudaError_t launch_t(const void* A, const void* B, const GemmArgs& args, cudaStr
   if (!make_tmap_bf16_2d(&tb, B, args.K, args.N, (uint64_t)args.K * 2, BK, BN)) return cudaErrorInvalidValue;
   const int tiles = ((args.M + BM - 1) / BM) * (args.N / BN);
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  gemm_kernel<EPI><<<grid, GEMM_THREADS, SMEM_BYTES, stream>>>(ta, tb, args);
+  gemm_kernel<EPI><<<grid, GEMM_THREADS, smem, stream>>>(ta, tb, args);
   return cudaGetLastError();
 }
 
