@@ -239,7 +239,8 @@ DIT_API dit_status dit_op_adaln(const void* w, const float* b, int rows, int t_d
  *   dit_op_gemm_qkv_rope   N = 3d: q, k get bias + NeoX rotate_half with cos/sin [M, R/2] on the
  *                          first R dims of each Dh-wide head and are stored bf16 [M, d]; v is
  *                          stored TRANSPOSED, vt bf16 [d, n_pad] (vt[c * n_pad + row]),
- *                          n_pad >= M, n_pad % 8 == 0.
+ *                          n_pad >= M, n_pad % 8 == 0; the padding columns [M, n_pad) are
+ *                          written as zeros.
  *   dit_op_gemm_gated_residual  x[M, N] (fp32, in place) += gate[tag[r]] * (A B^T + bias);
  *                          gate rows at gate + m * gate_stride (NULL gate = plain residual add).
  *   dit_op_gemm_swiglu     B, bias in the interleaved layout of dit_op_pack_ffn_in (2F rows);
@@ -265,7 +266,12 @@ DIT_API dit_status dit_op_pack_ffn_in(const void* w_in, const float* b_in, int F
 /* Varlen non-causal flash attention on the tcgen05 tensor cores ([H3] "Correctness gates":
  * DFlashBlockAttention(causal=false) over the packed sequence; [M3] "What moved": non-causal,
  * no bias).  Per document [cu[j], cu[j+1]) and head h:  o_i = softmax_j(q_i . k_j / sqrt(Dh)) v_j.
- *   q, k  bf16 [n_tokens, H * Dh];  vt bf16 [H * Dh, n_pad] (n_pad % 8 == 0, n_pad >= n_tokens)
+ *   q, k  bf16 [n_tokens, H * Dh];  vt bf16 [H * Dh, n_pad] (n_pad % 8 == 0, n_pad >= n_tokens;
+ *         its padding columns must hold finite values, e.g. the zeros dit_op_gemm_qkv_rope writes)
+ * Key/value tiles are 128 tokens wide and 128-aligned, so a document's boundary tiles also load
+ * its neighbours' keys and values; their softmax weights are exactly 0, which keeps every document's
+ * output bit-independent of the others' (finite) values.  A non-finite value in one document's V
+ * can still reach a neighbour sharing a boundary tile (0 * NaN = NaN).
  *   o     bf16 [n_tokens, H * Dh]
  * head_dim is 64 or 128.  The (document, 128-row q-tile) list is built on the device from cu_seqlens
  * into `workspace` (dit_attention_workspace_bytes(n_docs, n_tokens) bytes). */

@@ -46,10 +46,15 @@ def make_handle(model: dict, lay: dict, W: dict, max_tokens=None, max_docs=None)
     return h
 
 
-def workspace(h: dit.Dit, n_tokens: int, n_docs: int, host: bool = False) -> torch.Tensor:
+def workspace(h: dit.Dit, n_tokens: int, n_docs: int, host: bool = False, poison: bool = True) -> torch.Tensor:
+    """Device workspace for a forward.  Poisoned with 0xFF bytes (NaN in every float format) by
+    default: the forward must not depend on what the workspace held on entry."""
     nbytes = h.workspace_bytes(n_tokens, n_docs, host=host)
     assert nbytes > 0
-    return torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    if poison:
+        ws.fill_(255)
+    return ws
 
 
 def run_forward(w: dict, dumps: bool = False, layout=None, weights=None, x=None, t=None, handle=None):

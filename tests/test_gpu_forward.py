@@ -70,6 +70,16 @@ def test_forward_counters_and_tiles():
     assert st["device_status"] == 0 and st["last_layout_error"] == 0
 
 
+def test_forward_is_deterministic():
+    """Two forwards of the same inputs give the same bits (no race, no order-dependent reduction)."""
+    gu = _gu()
+    w = synth.WORKLOADS["ragged"]
+    r1 = gu.run_forward(w)
+    r2 = gu.run_forward(w, layout=r1["layout"], weights=r1["weights"], x=r1["x"], handle=r1["handle"])
+    diff = np.nonzero((r1["out"] != r2["out"]).any(axis=1))[0]
+    assert diff.size == 0, f"rows differing between identical forwards: {diff[:20].tolist()} ({diff.size})"
+
+
 def test_segmentation_bit_identity():
     """Perturbing one document's tokens leaves every output row of the other documents bit-identical."""
     gu = _gu()
@@ -84,7 +94,8 @@ def test_segmentation_bit_identity():
     r2 = gu.run_forward(w, layout=lay, weights=W, x=x2, handle=r1["handle"])
     other = np.ones(lay["n_tokens"], dtype=bool)
     other[cu[1]:cu[2]] = False
-    assert np.array_equal(r1["out"][other], r2["out"][other])
+    bad = np.nonzero(other & (r1["out"] != r2["out"]).any(axis=1))[0]
+    assert bad.size == 0, f"rows of unperturbed documents changed: {bad[:20].tolist()} ({bad.size})"
     assert not np.array_equal(r1["out"][~other], r2["out"][~other])
 
 
@@ -214,8 +225,11 @@ def test_denoise_loop_matches_oracle_reduced():
         v, _ = oracle.forward(w["model"], W, xo, lay, float(sig[i]))
         xo = oracle.euler_step(xo, v.astype(np.float32), sig[i], sig[i + 1])
     oracle.set_threads(1)
-    rms = np.sqrt((xo.astype(np.float64) ** 2).mean())
-    assert np.abs(xg.astype(np.float64) - xo).max() <= GATE * rms
+    # Each step moves x by (sigma_next - sigma) * v, and the steps' sigma decrements sum to 1, so the
+    # loop inherits the per-forward bound on v's scale (the initial noise's RMS); the final x itself
+    # nearly cancels (x0 - sum dsigma v) and is no scale to measure against.
+    rms_v = np.sqrt((x0.astype(np.float64) ** 2).mean())
+    assert np.abs(xg.astype(np.float64) - xo).max() <= GATE * rms_v
 
 
 def test_denoise_loop_resume_is_bit_identical():

@@ -163,7 +163,7 @@ def test_gemm_qkv_rope_matches_oracle(name):
     n_pad = (M + 7) // 8 * 8
     q = torch.empty((M, d), dtype=torch.bfloat16, device="cuda")
     k = torch.empty_like(q)
-    vt = torch.zeros((d, n_pad), dtype=torch.bfloat16, device="cuda")
+    vt = torch.full((d, n_pad), float("nan"), dtype=torch.bfloat16, device="cuda")  # garbage on entry
     gcs = torch.empty((M, R // 2), dtype=torch.float32, device="cuda")
     gsn = torch.empty_like(gcs)
     dit.rope_cache(gu.dev_layout(lay)["pos"], m["rope_axes"], m["rope_dims"], m["rope_base"], gcs, gsn)
@@ -176,6 +176,7 @@ def test_gemm_qkv_rope_matches_oracle(name):
         assert np.all(err <= BF16_REL * np.abs(ref) + 2 * bb.max() + 1e-5), err.max()
     gv = bf16_to_f64(vt)[:, :M].T
     assert np.all(np.abs(gv - vr) <= BF16_REL * np.abs(vr) + bound[:, 2 * d:] + 1e-6)
+    assert (bf16_to_f64(vt)[:, M:] == 0).all()  # padding columns are written as zeros
 
 
 def test_gemm_gated_residual_matches_oracle():

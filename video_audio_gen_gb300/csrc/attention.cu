@@ -75,24 +75,28 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   uint8_t* sP = sV + KV_STAGES * Plan::V_BYTES;        // [2]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * P_BYTES);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;                        // [2]
-  uint64_t* kv_empty = bars + 3;                       // [2]
-  uint64_t* s_full = bars + 5;                         // [2]
-  uint64_t* p_full = bars + 7;                         // [2]
-  uint64_t* o_full = bars + 9;                         // [2]
-  uint64_t* mma_done = bars + 11;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  uint64_t* k_full = bars + 1;                         // [2]  K tile landed
+  uint64_t* k_empty = bars + 3;                        // [2]  S MMA done with the K tile
+  uint64_t* v_full = bars + 5;                         // [2]  V^T tile landed
+  uint64_t* v_empty = bars + 7;                        // [2]  PV MMA done with the V^T tile
+  uint64_t* s_full = bars + 9;                         // [2]
+  uint64_t* p_full = bars + 11;                        // [2]
+  uint64_t* o_done = bars + 13;                        // [2]
+  uint64_t* mma_done = bars + 15;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
       mbar_init(&s_full[s], 1);
       mbar_init(&p_full[s], 4);
-      mbar_init(&o_full[s], 1);
+      mbar_init(&o_done[s], 1);
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -104,7 +108,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t t_s = tmem;            // S buffers at columns 0, 128
-  const uint32_t t_o = tmem + 256;      // O partial buffers at columns 256, 256 + HD
+  const uint32_t t_o = tmem + 256;      // O accumulator at columns [256, 256 + HD)
 
   if (warp == 0) {
     if (lane == 0) {
@@ -112,32 +116,55 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       mbar_arrive_expect_tx(q_full, Plan::Q_BYTES);
 #pragma unroll
       for (int a = 0; a < HD / 64; ++a) tma_load_2d(sQ + a * ATOM, &tmQ, q_full, hx + 64 * a, q0);
-      int issued = 0;
-      for (int j = 0; j < n_kv; ++j) {
+      // K tiles run two ahead of the V tiles: K(j) only waits for S(j-2), V(j) for P(j-2) V(j-2).
+      auto load_k = [&](int j) -> bool {
         const int st = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        if (!mbar_wait(&kv_empty[st], ph ^ 1, abort_flag, args.status)) break;
+        if (!mbar_wait(&k_empty[st], ((j >> 1) & 1) ^ 1, abort_flag, args.status)) return false;
         const int kv0 = kv_base + j * TK;
-        mbar_arrive_expect_tx(&kv_full[st], Plan::K_BYTES + Plan::V_BYTES);
+        mbar_arrive_expect_tx(&k_full[st], Plan::K_BYTES);
 #pragma unroll
         for (int a = 0; a < HD / 64; ++a)
-          tma_load_2d(sK + st * Plan::K_BYTES + a * ATOM, &tmK, &kv_full[st], hx + 64 * a, kv0);
-        tma_load_2d(sV + st * Plan::V_BYTES, &tmV, &kv_full[st], kv0, hx);
-        tma_load_2d(sV + st * Plan::V_BYTES + Plan::V_ATOM, &tmV, &kv_full[st], kv0 + 64, hx);
-        ++issued;
+          tma_load_2d(sK + st * Plan::K_BYTES + a * ATOM, &tmK, &k_full[st], hx + 64 * a, kv0);
+        return true;
+      };
+      auto load_v = [&](int j) -> bool {
+        const int st = j & 1;
+        if (!mbar_wait(&v_empty[st], ((j >> 1) & 1) ^ 1, abort_flag, args.status)) return false;
+        const int kv0 = kv_base + j * TK;
+        mbar_arrive_expect_tx(&v_full[st], Plan::V_BYTES);
+        tma_load_2d(sV + st * Plan::V_BYTES, &tmV, &v_full[st], kv0, hx);
+        tma_load_2d(sV + st * Plan::V_BYTES + Plan::V_ATOM, &tmV, &v_full[st], kv0 + 64, hx);
+        return true;
+      };
+      int nk = 0, nv = 0;
+      bool ok = true;
+      for (; ok && nk < n_kv && nk < 2; ++nk) ok = load_k(nk);
+      while (ok && nv < n_kv) {
+        ok = load_v(nv);
+        if (!ok) break;
+        ++nv;
+        if (nk < n_kv) {
+          ok = load_k(nk);
+          if (ok) ++nk;
+        }
       }
       // Every copy this CTA issued must land before the CTA may exit.
       wait_noabort(q_full, 0);
-      for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j) wait_noabort(&kv_full[j & 1], (j >> 1) & 1);
+      for (int j = nk - 2 < 0 ? 0 : nk - 2; j < nk; ++j) wait_noabort(&k_full[j & 1], (j >> 1) & 1);
+      for (int j = nv - 2 < 0 ? 0 : nv - 2; j < nv; ++j) wait_noabort(&v_full[j & 1], (j >> 1) & 1);
     }
   } else if (warp == 1) {
     if (lane == 0) {
+      // MMA issue order: S(0), S(1), then for each j: [P(j) ready] O += P(j) V(j), S(j+2).
+      // S(j+2) reuses S buffer j%2, which the softmax released when it published P(j); the commit
+      // after S(j) also covers every earlier MMA (tcgen05 ops of one thread complete in order), so
+      // when the softmax sees S(j) it knows O += P(j-2) V(j-2) is done and P buffer j%2 is free.
       bool ok = mbar_wait(q_full, 0, abort_flag, args.status);
       tc_fence_after();
       const uint32_t q_addr = smem_u32(sQ);
       auto issue_s = [&](int j) -> bool {
         const int st = j & 1;
-        if (!mbar_wait(&kv_full[st], (j >> 1) & 1, abort_flag, args.status)) return false;
+        if (!mbar_wait(&k_full[st], (j >> 1) & 1, abort_flag, args.status)) return false;
         tc_fence_after();
         const uint32_t k_addr = smem_u32(sK + st * Plan::K_BYTES);
 #pragma unroll
@@ -146,13 +173,15 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
           umma_bf16(t_s + st * TK, sdesc_sw128(q_addr + off), sdesc_sw128(k_addr + off), Plan::IDESC_S, ks != 0);
         }
         umma_commit(&s_full[st]);
+        umma_commit(&k_empty[st]);
         return true;
       };
       if (ok) ok = issue_s(0);
+      if (ok && n_kv > 1) ok = issue_s(1);
       for (int j = 0; ok && j < n_kv; ++j) {
-        if (j + 1 < n_kv && !issue_s(j + 1)) break;
         const int pb = j & 1;
         if (!mbar_wait(&p_full[pb], (j >> 1) & 1, abort_flag, args.status)) break;
+        if (!mbar_wait(&v_full[pb], (j >> 1) & 1, abort_flag, args.status)) break;
         tc_fence_after();
         const uint32_t p_addr = smem_u32(sP + pb * P_BYTES);
         const uint32_t v_addr = smem_u32(sV + (j & 1) * Plan::V_BYTES);
@@ -160,10 +189,11 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         for (int ks = 0; ks < TK / 16; ++ks) {
           const uint32_t p_off = (ks >> 2) * ATOM + (ks & 3) * 32;
           const uint32_t v_off = (ks >> 2) * Plan::V_ATOM + (ks & 3) * 32;
-          umma_bf16(t_o + pb * HD, sdesc_sw128(p_addr + p_off), sdesc_sw128(v_addr + v_off), Plan::IDESC_O, ks != 0);
+          umma_bf16(t_o, sdesc_sw128(p_addr + p_off), sdesc_sw128(v_addr + v_off), Plan::IDESC_O, (j | ks) != 0);
         }
-        umma_commit(&o_full[pb]);
-        umma_commit(&kv_empty[j & 1]);
+        umma_commit(&o_done[pb]);
+        umma_commit(&v_empty[pb]);
+        if (j + 2 < n_kv && !issue_s(j + 2)) break;
       }
       // No MMA may still read shared memory or write TMEM when the CTA tears down.
       umma_commit(mma_done);
@@ -171,31 +201,17 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     }
   } else {
     // ---------------- softmax warps ----------------
+    // Thread <-> query row.  O accumulates in TMEM through the MMA; the running max m is only raised
+    // (and O, l rescaled by exp2(m_old - m_new)) when a row's max grows by more than 2^8, so most
+    // tiles never touch O.  Between raises p = exp2(s * scale - m) stays below 2^8.
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;          // tile row owned by this thread
     const int row = q0 + r;                     // packed-sequence row
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const float sc = args.scale_log2;
-    float acc[HD];
-#pragma unroll
-    for (int i = 0; i < HD; ++i) acc[i] = 0.f;
-    float m = -INFINITY, l = 0.f, alpha_prev = 1.f;
+    constexpr float kRescaleThreshold = 8.0f;   // log2 units
+    float m = -INFINITY, l = 0.f;
     bool ok = true;
-
-    auto fold_o = [&](int jj, float alpha) -> bool {
-      const int pb = jj & 1;
-      if (!mbar_wait(&o_full[pb], (jj >> 1) & 1, abort_flag, args.status)) return false;
-      tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < HD; c += 32) {
-        uint32_t v[32];
-        tmem_ld32(t_o + pb * HD + lane_off + c, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) acc[c + i] = fmaf(acc[c + i], alpha, __uint_as_float(v[i]));
-      }
-      return true;
-    };
 
     for (int j = 0; j < n_kv; ++j) {
       const int sb = j & 1;
@@ -207,67 +223,92 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       const int c0 = kv_base + j * TK;
       const int lo = ds > c0 ? ds - c0 : 0;
       const int hi = de - c0 < TK ? de - c0 : TK;
+      const bool interior = (lo == 0) && (hi == TK);
       const uint32_t ts = t_s + sb * TK + lane_off;
-      // pass 1: row max of the scaled scores
+      uint32_t sv[TK];
+#pragma unroll
+      for (int c = 0; c < TK; c += 32) tmem_ld32(ts + c, *reinterpret_cast<uint32_t(*)[32]>(&sv[c]));
+#pragma unroll
+      for (int c = 0; c < TK; c += 32) tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&sv[c]));
       float mx = -INFINITY;
+      if (interior) {
 #pragma unroll
-      for (int c = 0; c < TK; c += 32) {
-        uint32_t v[32];
-        tmem_ld32(ts + c, v);
-        tmem_ld_wait();
+        for (int i = 0; i < TK; ++i) mx = fmaxf(mx, __uint_as_float(sv[i]));
+      } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int cc = c + i;
-          if (cc >= lo && cc < hi) mx = fmaxf(mx, __uint_as_float(v[i]));
+        for (int i = 0; i < TK; ++i) {
+          const bool in = i >= lo && i < hi;
+          if (!in) sv[i] = __float_as_uint(-INFINITY);
+          mx = fmaxf(mx, __uint_as_float(sv[i]));
         }
       }
-      const float m_new = fmaxf(m, mx * sc);
-      const float alpha = (m == -INFINITY) ? 0.f : fast_exp2(m - m_new);
-      // pass 2: p = exp2(s * sc - m_new), bf16 into shared memory (swizzled K-major A operand)
+      const float m_cand = mx * sc;
+      const bool raise = m_cand > m + kRescaleThreshold;  // always true on the first tile (m = -inf)
+      if (__any_sync(0xffffffffu, raise)) {
+        const float m_new = raise ? m_cand : m;
+        const float alpha = raise ? fast_exp2(m - m_new) : 1.f;  // exp2(-inf) = 0 on the first tile
+        if (j > 0) {
+          // O holds sum_{i<j} P(i) V(i) relative to m: wait for the last PV, rescale in place
+          if (!mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, args.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < HD; c += 32) {
+            uint32_t ov[32];
+            tmem_ld32_sync(t_o + lane_off + c, ov);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+            tmem_st32(t_o + lane_off + c, ov);
+            tmem_st_wait();
+          }
+        }
+        l *= alpha;
+        m = m_new;
+      }
+      // p = exp2(s * scale - m) -> bf16 into shared memory (swizzled K-major A operand of P V)
       const uint32_t p_base = smem_u32(sP + sb * P_BYTES) + r * 128;
       float rs = 0.f;
 #pragma unroll
-      for (int c = 0; c < TK; c += 32) {
-        uint32_t v[32];
-        tmem_ld32(ts + c, v);
-        tmem_ld_wait();
-        float p[32];
+      for (int c = 0; c < TK; c += 8) {
+        float p[8];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int cc = c + i;
-          p[i] = (cc >= lo && cc < hi) ? fast_exp2(fmaf(__uint_as_float(v[i]), sc, -m_new)) : 0.f;
+        for (int i = 0; i < 8; ++i) {
+          p[i] = fast_exp2(fmaf(__uint_as_float(sv[c + i]), sc, -m));
           rs += p[i];
         }
-        const uint32_t atom = (c >> 6) * ATOM;
-#pragma unroll
-        for (int k8 = 0; k8 < 4; ++k8) {
-          const int chunk = ((c & 63) >> 3) + k8;  // 16-byte chunk within the 128-byte row
-          const uint32_t addr = p_base + atom + ((chunk ^ (r & 7)) << 4);
-          st_shared_v4(addr, pack_bf16x2(p[8 * k8 + 0], p[8 * k8 + 1]), pack_bf16x2(p[8 * k8 + 2], p[8 * k8 + 3]),
-                       pack_bf16x2(p[8 * k8 + 4], p[8 * k8 + 5]), pack_bf16x2(p[8 * k8 + 6], p[8 * k8 + 7]));
-        }
+        const int chunk = (c & 63) >> 3;  // 16-byte chunk within the 128-byte row of atom c / 64
+        st_shared_v4(p_base + (c >> 6) * ATOM + ((chunk ^ (r & 7)) << 4), pack_bf16x2(p[0], p[1]),
+                     pack_bf16x2(p[2], p[3]), pack_bf16x2(p[4], p[5]), pack_bf16x2(p[6], p[7]));
       }
+      l += rs;
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[sb]);
-      l = l * alpha + rs;
-      m = m_new;
-      // fold the previous tile's partial O (computed relative to the previous max)
-      if (j > 0 && !fold_o(j - 1, alpha_prev)) {
-        ok = false;
-        break;
-      }
-      alpha_prev = alpha;
     }
-    if (ok && n_kv > 0) ok = fold_o(n_kv - 1, alpha_prev);
-    if (ok && row < de) {
+    if (ok && n_kv > 0) {
+      const int jl = n_kv - 1;
+      ok = mbar_wait(&o_done[jl & 1], (jl >> 1) & 1, abort_flag, args.status);
+      tc_fence_after();
+    }
+    if (ok) {
       const float inv = 1.f / l;
       __nv_bfloat16* orow = O + (size_t)row * (args.n_heads * HD) + head * HD;
 #pragma unroll
-      for (int c = 0; c < HD; c += 8)
-        st_global_v4(orow + c, pack_bf16x2(acc[c] * inv, acc[c + 1] * inv), pack_bf16x2(acc[c + 2] * inv, acc[c + 3] * inv),
-                     pack_bf16x2(acc[c + 4] * inv, acc[c + 5] * inv), pack_bf16x2(acc[c + 6] * inv, acc[c + 7] * inv));
+      for (int c = 0; c < HD; c += 32) {
+        uint32_t ov[32];
+        tmem_ld32_sync(t_o + lane_off + c, ov);
+        if (row < de) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 8)
+            st_global_v4(orow + c + i, pack_bf16x2(__uint_as_float(ov[i]) * inv, __uint_as_float(ov[i + 1]) * inv),
+                         pack_bf16x2(__uint_as_float(ov[i + 2]) * inv, __uint_as_float(ov[i + 3]) * inv),
+                         pack_bf16x2(__uint_as_float(ov[i + 4]) * inv, __uint_as_float(ov[i + 5]) * inv),
+                         pack_bf16x2(__uint_as_float(ov[i + 6]) * inv, __uint_as_float(ov[i + 7]) * inv));
+        }
+      }
     }
   }
 

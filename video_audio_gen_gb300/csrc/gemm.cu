@@ -72,8 +72,7 @@ __device__ __forceinline__ void epi_store(const GemmArgs& a, uint32_t t, int row
 #pragma unroll 1
   for (int c = 0; c < BN; c += 32) {
     uint32_t r[32];
-    tmem_ld32(t + c, r);
-    tmem_ld_wait();
+    tmem_ld32_sync(t + c, r);
     if (!live) continue;
     float v[32];
 #pragma unroll
@@ -113,20 +112,23 @@ __device__ __forceinline__ void epi_qkv(const GemmArgs& a, uint32_t t, int row, 
   const int seg = n0 / a.d;
   const int col0 = n0 - seg * a.d;
   if (seg == 2) {
+    // v is stored transposed; its padding columns [M, n_pad) are written as zeros so that the
+    // attention's masked key/value tiles never multiply uninitialised memory (0 * NaN = NaN).
     __nv_bfloat16* vt = static_cast<__nv_bfloat16*>(a.vt);
+    const bool pad = !live && row < a.n_pad;
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
       uint32_t r[32];
-      tmem_ld32(t + c, r);
-      tmem_ld_wait();
-      if (!live) continue;
+      tmem_ld32_sync(t + c, r);
+      if (!live && !pad) continue;
 #pragma unroll
       for (int i = 0; i < 32; i += 4) {
         float b[4];
         load_bias4(a.bias, n0 + c + i, b);
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          vt[(size_t)(col0 + c + i + j) * a.n_pad + row] = __float2bfloat16_rn(__uint_as_float(r[i + j]) + b[j]);
+          vt[(size_t)(col0 + c + i + j) * a.n_pad + row] =
+              __float2bfloat16_rn(live ? __uint_as_float(r[i + j]) + b[j] : 0.f);
       }
     }
     return;
@@ -142,7 +144,8 @@ __device__ __forceinline__ void epi_qkv(const GemmArgs& a, uint32_t t, int row, 
       uint32_t r1[16], r2[16];
       tmem_ld16(t + hb + c, r1);
       tmem_ld16(t + hb + half + c, r2);
-      tmem_ld_wait();
+      tmem_ld_wait_regs(r1);
+      tmem_ld_wait_regs(r2);
       if (!live) continue;
       float o1[16], o2[16];
 #pragma unroll
@@ -168,7 +171,7 @@ __device__ __forceinline__ void epi_qkv(const GemmArgs& a, uint32_t t, int row, 
     for (int c = 2 * half; c < Dh; c += 16) {  // partial rotary: dims >= R pass through
       uint32_t r1[16];
       tmem_ld16(t + hb + c, r1);
-      tmem_ld_wait();
+      tmem_ld_wait_regs(r1);
       if (!live) continue;
       float o1[16];
 #pragma unroll
@@ -208,8 +211,7 @@ __device__ __forceinline__ void epi_resid(const GemmArgs& a, uint32_t t, int til
 #pragma unroll
     for (int h = 0; h < RES_COLS; h += 32) {
       uint32_t r[32];
-      tmem_ld32(t + c0 + h, r);
-      tmem_ld_wait();
+      tmem_ld32_sync(t + c0 + h, r);
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         const int chunk = (h >> 2) + q;  // 16-byte chunk index within the 256-byte row
@@ -270,7 +272,8 @@ __device__ __forceinline__ void epi_swiglu(const GemmArgs& a, uint32_t t, int ro
     uint32_t ru[16], rg[16];
     tmem_ld16(t + c, ru);
     tmem_ld16(t + BN / 2 + c, rg);
-    tmem_ld_wait();
+    tmem_ld_wait_regs(ru);
+    tmem_ld_wait_regs(rg);
     if (!live) continue;
     float h[16];
 #pragma unroll
