@@ -280,6 +280,26 @@ DIT_API dit_status dit_op_attention(const void* q, const void* k, const void* vt
                             int n_docs, int n_tokens, int n_heads, int head_dim, void* o, void* workspace,
                             void* stream);
 
+/* The same attention with no caller-provided scratch, for callers that cannot allocate device
+ * memory: e.g. a plugin running inside another framework's executor that is handed no allocator, or
+ * a latency-critical serving thread that cannot afford cudaMalloc's implicit device synchronisation.
+ * The pages have no counterpart of this call; it exists for such callers only.
+ *   Arguments, layouts and results are those of dit_op_attention, without `workspace`.
+ *   Scratch: a fixed array inside libdit.so's device memory (256 bytes of status words plus
+ *   DIT_ATTENTION_NOALLOC_MAX_TILES (document, q-tile) entries of 8 bytes, about 64 KB), held by
+ *   every GPU that loads the library until the process exits.  Nothing is allocated or freed.
+ *   Capacity: ceil(n_tokens / 128) + n_docs <= DIT_ATTENTION_NOALLOC_MAX_TILES, else
+ *   DIT_ERR_CAPACITY with dit_last_error(NULL) saying so, before any work is enqueued.
+ *   Set-up: the first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) and caches it; make that first call before any stream capture.
+ *   Sharing: all calls use the same array, which keeps the last call's contents (the status words
+ *   are cleared at the start of each call).  Calls whose device work overlaps (other streams, other
+ *   host threads on the same device) race on it: serialise them. */
+#define DIT_ATTENTION_NOALLOC_MAX_TILES 8192
+DIT_API dit_status dit_op_attention_noalloc(const void* q, const void* k, const void* vt, int n_pad,
+                                            const int32_t* cu_seqlens, int n_docs, int n_tokens, int n_heads,
+                                            int head_dim, void* o, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,63 @@
+"""dit_op_attention_noalloc against dit_op_attention, through the C ABI.
+
+The no-allocation variant exists for callers that cannot call cudaMalloc (a plugin inside another
+framework's executor with no allocator handed to it, a latency-critical serving thread that cannot
+take cudaMalloc's implicit device synchronisation): its scratch lives in a fixed array inside the
+library.  Two calls in a row with different layouts check that the shared array is reset between
+calls.  This file is collected last so a failure here cannot hide any other test's result; it also
+passes on its own in a fresh process.
+"""
+import numpy as np
+import pytest
+
+import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+BF16_REL = 2.0 ** -8
+
+
+def _attention_inputs(docs, H, Dh, seed):
+    from tests import gpu_util as gu
+    lay = synth.build_layout(docs)
+    n = lay["n_tokens"]
+    n_pad = (n + 7) // 8 * 8
+    _, qb = synth.normal(seed, "q", (n, H * Dh), 1.0, bf16=True)
+    _, kb = synth.normal(seed, "k", (n, H * Dh), 1.0, bf16=True)
+    v, vb = synth.normal(seed, "v", (n, H * Dh), 1.0, bf16=True)
+    vt = np.zeros((H * Dh, n_pad), dtype=np.uint16)
+    vt[:, :n] = vb.T
+    return lay, n_pad, gu.dev_bf16(qb), gu.dev_bf16(kb), gu.dev_bf16(vt), gu.dev_layout(lay)["cu"], v
+
+
+def test_attention_noalloc_matches_workspace_entry_point():
+    from video_audio_gen_gb300 import build, dit
+    build.build()
+    cases = [(synth.WORKLOADS["ragged"]["docs"], 2, 128, 201),   # 4 documents, ragged ends
+             (synth.WORKLOADS["tiny"]["docs"], 4, 64, 202)]      # then 2 documents, head dim 64
+    for docs, H, Dh, seed in cases:                              # two calls in a row
+        lay, n_pad, q, k, vt, cu, v = _attention_inputs(docs, H, Dh, seed)
+        n = lay["n_tokens"]
+        ws = torch.empty(dit.attention_workspace_bytes(lay["n_docs"], n), dtype=torch.uint8, device="cuda")
+        ref = torch.empty((n, H * Dh), dtype=torch.bfloat16, device="cuda")
+        dit.attention(q, k, vt, n_pad, cu, H, Dh, ref, ws)
+        got = torch.full((n, H * Dh), float("nan"), dtype=torch.bfloat16, device="cuda")
+        dit.attention_noalloc(q, k, vt, n_pad, cu, H, Dh, got)
+        torch.cuda.synchronize()
+        r = ref.float().double().cpu().numpy()
+        g = got.float().double().cpu().numpy()
+        assert np.isfinite(g).all()
+        assert np.all(np.abs(g - r) <= BF16_REL * np.abs(r) + 2.0 ** -8 * np.abs(v).max())
+
+
+def test_attention_noalloc_rejects_sizes_beyond_its_scratch():
+    from video_audio_gen_gb300 import build, dit
+    build.build()
+    n = 128 * 8192 + 1  # ceil(n / 128) + 1 document = 8194 tiles > 8192
+    dummy = torch.empty(16, dtype=torch.bfloat16, device="cuda")
+    cu = torch.tensor([0, n], dtype=torch.int32, device="cuda")
+    st = dit.lib().dit_op_attention_noalloc(dummy.data_ptr(), dummy.data_ptr(), dummy.data_ptr(), (n + 7) & ~7,
+                                            cu.data_ptr(), 1, n, 1, 128, dummy.data_ptr(), None)
+    assert st == dit.DIT_ERR_CAPACITY
+    assert b"fixed scratch" in dit.lib().dit_last_error(None)

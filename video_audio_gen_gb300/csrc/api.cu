@@ -6,6 +6,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -719,3 +720,82 @@ dit_status dit_op_attention(const void* q, const void* k, const void* vt, int n_
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------------------------------
+// Attention without caller-provided scratch
+//
+// Some callers cannot call cudaMalloc: a plugin that runs inside another framework's executor and is
+// handed no allocator, or a latency-critical serving thread for which cudaMalloc's implicit device
+// synchronisation is not acceptable.  dit_op_attention needs a small scratch buffer (three status
+// words and the (document, q-tile) list); this variant keeps that scratch in a fixed array in the
+// library's own device memory instead, so it allocates nothing.  Every GPU that loads the library
+// holds the array until the process exits.
+// ------------------------------------------------------------------------------------------------
+namespace {
+
+constexpr int kNoAllocMaxItems = 8192;       // (document, 128-row q-tile) pairs
+constexpr size_t kNoAllocStatusBytes = 256;  // StatusWords, padded to the array's alignment
+constexpr int kNoAllocMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_attention_scratch[kNoAllocStatusBytes + kNoAllocMaxItems * 8];
+
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of g_attention_scratch on the current device.  The host-side symbol is only a
+// stand-in for the array, so its device address is looked up once per device (the first call on
+// that device) and cached.
+cudaError_t noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress((void**)&p, g_attention_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" dit_status dit_op_attention_noalloc(const void* q, const void* k, const void* vt, int n_pad,
+                                               const int32_t* cu_seqlens, int n_docs, int n_tokens, int n_heads,
+                                               int head_dim, void* o, void* stream) {
+  if (!q || !k || !vt || !o || !cu_seqlens || n_docs < 1 || n_tokens < 1 || n_heads < 1 || n_pad < n_tokens ||
+      n_pad % 8)
+    return set_err(nullptr, DIT_ERR_INVALID_ARG, "bad attention arguments");
+  if (head_dim != 128 && head_dim != 64) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "attention needs head_dim 64 or 128");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(vt) || !aligned16(o))
+    return set_err(nullptr, DIT_ERR_INVALID_ARG, "attention operands must be 16-byte aligned");
+  const int max_items = attention_max_items(n_docs, n_tokens);
+  if (max_items > kNoAllocMaxItems)
+    return set_err(nullptr, DIT_ERR_CAPACITY,
+                   "dit_op_attention_noalloc: ceil(n_tokens / 128) + n_docs = %d exceeds its fixed scratch of %d "
+                   "tiles; use dit_op_attention with a workspace",
+                   max_items, kNoAllocMaxItems);
+  void* scratch = nullptr;
+  cudaError_t e = noalloc_scratch(&scratch);
+  if (e != cudaSuccess) return cuda_err(nullptr, e, "cudaGetSymbolAddress(attention scratch)");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  StatusWords* sw = static_cast<StatusWords*>(scratch);
+  int2* items = reinterpret_cast<int2*>(static_cast<char*>(scratch) + kNoAllocStatusBytes);
+  // The array keeps the previous call's contents: the status bits are OR-ed into, so they start at
+  // zero; the count, the layout code and the tile list are rewritten by the schedule kernel.
+  e = cudaMemsetAsync(sw, 0, sizeof(StatusWords), s);
+  if (e == cudaSuccess)
+    e = attention_schedule_launch(cu_seqlens, n_docs, n_tokens, nullptr, nullptr, 0, items, &sw->count, max_items,
+                                  &sw->layout_code, &sw->bits, s);
+  if (e != cudaSuccess) return cuda_err(nullptr, e, "attention schedule");
+  AttnArgs aa;
+  aa.n_tokens = n_tokens; aa.n_heads = n_heads; aa.head_dim = head_dim; aa.n_pad = n_pad; aa.n_docs = n_docs;
+  aa.cu = cu_seqlens; aa.items = items; aa.count = &sw->count; aa.max_items = max_items;
+  aa.scale_log2 = (float)(1.4426950408889634 / sqrt((double)head_dim));
+  aa.status = &sw->bits;
+  e = attention_launch(q, k, vt, o, aa, s);
+  return e == cudaSuccess ? DIT_OK : cuda_err(nullptr, e, "attention");
+}

@@ -25,7 +25,8 @@ EXPORTS = ["dit_create", "dit_destroy", "dit_last_error", "dit_workspace_bytes",
            "dit_workspace_bytes_host", "dit_forward_host", "dit_euler_step", "dit_get_stats", "dit_sync_status",
            "dit_set_dump", "dit_set_kernel_timing", "dit_get_kernel_times", "dit_op_norm_modulate",
            "dit_op_rope_cache", "dit_op_adaln", "dit_op_gemm", "dit_op_gemm_qkv_rope", "dit_op_gemm_gated_residual",
-           "dit_op_gemm_swiglu", "dit_op_pack_ffn_in", "dit_attention_workspace_bytes", "dit_op_attention"]
+           "dit_op_gemm_swiglu", "dit_op_pack_ffn_in", "dit_attention_workspace_bytes", "dit_op_attention",
+           "dit_op_attention_noalloc"]
 
 
 class DitError(RuntimeError):
@@ -105,6 +106,7 @@ def lib():
             "dit_op_pack_ffn_in": (i32, [vp, vp, i32, i32, vp, vp, vp]),
             "dit_attention_workspace_bytes": (sz, [i32, i32]),
             "dit_op_attention": (i32, [vp, vp, vp, i32, vp, i32, i32, i32, i32, vp, vp, vp]),
+            "dit_op_attention_noalloc": (i32, [vp, vp, vp, i32, vp, i32, i32, i32, i32, vp, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -292,3 +294,12 @@ def attention(q, k, vt, n_pad, cu_seqlens, n_heads, head_dim, o, workspace, stre
     n_tokens = q.shape[0]
     _check(lib().dit_op_attention(_ptr(q), _ptr(k), _ptr(vt), n_pad, _ptr(cu_seqlens), cu_seqlens.numel() - 1,
                                   n_tokens, n_heads, head_dim, _ptr(o), _ptr(workspace), _stream(stream)))
+
+
+def attention_noalloc(q, k, vt, n_pad, cu_seqlens, n_heads, head_dim, o, stream=None):
+    """dit_op_attention_noalloc: the attention with its scratch in the library's fixed device array
+    (for callers that cannot allocate); calls whose device work overlaps must be serialised."""
+    n_tokens = q.shape[0]
+    _check(lib().dit_op_attention_noalloc(_ptr(q), _ptr(k), _ptr(vt), n_pad, _ptr(cu_seqlens),
+                                          cu_seqlens.numel() - 1, n_tokens, n_heads, head_dim, _ptr(o),
+                                          _stream(stream)))
