@@ -35,7 +35,14 @@ KINDS = ["gemm_qkv", "attention", "gemm_out", "gemm_ffn_up", "gemm_ffn_down", "n
 # DRAM traffic per launch from ncu captures (dram__bytes_read.sum + dram__bytes_write.sum), keyed by
 # kernel kind and workload, with the sha256 of the kernel source the capture was taken on; the
 # figure is reported only while the source is unchanged.  See profiles/.
-TRAFFIC = {}
+TRAFFIC = {
+    ("attention", "video_audio_bf16"): {"bytes": 410065408, "src_sha": "7d4af3d2bac76750",
+                                        "profile": "profiles/attention_video_audio_bf16.md"},
+    ("gemm_ffn_up", "video_audio_bf16"): {"bytes": 807116800, "src_sha": "14a32effdb9cf011",
+                                          "profile": "profiles/gemm_video_audio_bf16.md"},
+    ("gemm_qkv", "video_audio_bf16"): {"bytes": 802932736, "src_sha": "14a32effdb9cf011",
+                                       "profile": "profiles/gemm_video_audio_bf16.md"},
+}
 
 
 # ------------------------------------------------------------------------------------------------
@@ -283,6 +290,10 @@ def run_gpu(args, w, dist, rank, world):
         elif k == "norm_modulate":
             gbs = norm_bytes(m, N) / (avg * 1e-3) / 1e9
             entry.update(bound="hbm", achieved_gbs=round(gbs, 1), frac=round(gbs / peaks["hbm_gbs"], 3))
+        tr = TRAFFIC.get((k, args.workload))
+        if tr:
+            src = "attention.cu" if k == "attention" else ("gemm.cu" if k.startswith("gemm") else "elementwise.cu")
+            entry["traffic"] = tr["bytes"] if tr["src_sha"] == source_hash(src) else None
         kernels[k] = entry
     tot = sum(kt[k][0] for k in KINDS)
     for k in kernels:

@@ -1,0 +1,136 @@
+"""The gates discriminate: each plausible mistake, planted in the oracle's inputs on the CPU, fails the
+gate the GPU path is held to, while the unmutated oracle and bf16-level noise pass.
+
+Whole-forward gates (tests/parity.py) catch mistakes in the block structure.  They cannot catch RoPE
+mistakes at these weight scales: with N(0, 0.02) weights the attention logits are ~0.1, the softmax is
+nearly uniform and any rotation leaves the forward almost unchanged.  RoPE is therefore held to the
+op-level gate of the QKV + RoPE kernel test (one bf16 rounding of q and k), where its mistakes fail."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests.parity import forward_gates
+
+W0 = synth.WORKLOADS["tiny"]
+
+
+@pytest.fixture(scope="module")
+def base():
+    lay = synth.build_layout(W0["docs"])
+    W = synth.make_weights(W0)
+    x = synth.make_tokens(W0, lay)
+    oracle.set_threads(4)
+    out, dumps = oracle.forward(W0["model"], W, x, lay, 0.5, dumps=True)
+    return lay, W, x, out, dumps
+
+
+def _copy(W):
+    return dict(blocks=[{k: (v.copy() if v is not None else None) for k, v in b.items()} for b in W["blocks"]],
+                glob={k: (v.copy() if v is not None else None) for k, v in W["glob"].items()})
+
+
+def _run(W, x, lay, m=None):
+    return oracle.forward(m or W0["model"], W, x, lay, 0.5, dumps=True)
+
+
+def test_gates_pass_for_the_oracle_itself_and_for_bf16_level_noise(base):
+    lay, W, x, out, dumps = base
+    assert forward_gates(x, dumps, dumps, out, out) == []
+    # perturb every block output by one bf16 rounding of its update: must still pass
+    rng = np.random.default_rng(0)
+    noisy = dumps.copy()
+    prev = x.astype(np.float64)
+    for l in range(len(dumps)):
+        upd = dumps[l] - prev
+        noisy[l] = prev + upd * (1 + rng.uniform(-2 ** -9, 2 ** -9, upd.shape))
+        prev = dumps[l]
+    assert forward_gates(x, noisy, dumps, out, out) == []
+
+
+def _mutations():
+    m = W0["model"]
+    d, F, H, Dh = m["hidden"], m["ffn_hidden"], m["n_heads"], m["head_dim"]
+
+    def swap_value_gate(W, lay):
+        for b in W["blocks"]:
+            b["w_in"] = np.concatenate([b["w_in"][F:], b["w_in"][:F]])
+            b["b_in"] = np.concatenate([b["b_in"][F:], b["b_in"][:F]])
+        return W, lay
+
+    def swap_q_k(W, lay):
+        for b in W["blocks"]:
+            b["w_qkv"] = np.concatenate([b["w_qkv"][d:2 * d], b["w_qkv"][:d], b["w_qkv"][2 * d:]])
+        return W, lay
+
+    def drop_document_boundary(W, lay):
+        lay = dict(lay, cu_seqlens=np.array([0, lay["n_tokens"]], dtype=np.int32),
+                   doc_ids=np.zeros(lay["n_tokens"], dtype=np.int32), n_docs=1)
+        return W, lay
+
+    def wrong_modality_row(W, lay):
+        return W, dict(lay, tags=(1 - lay["tags"]).astype(np.uint8))
+
+    def ungated_residual(W, lay):
+        for b in W["blocks"]:
+            wa = b["w_ada"].reshape(2, 6, d, -1)
+            ba = b["b_ada"].reshape(2, 6, d)
+            for c in (2, 5):
+                wa[:, c] = 0.0
+                ba[:, c] = 1.0
+        return W, lay
+
+    return [swap_value_gate, swap_q_k, drop_document_boundary, wrong_modality_row, ungated_residual]
+
+
+@pytest.mark.parametrize("mutate", _mutations(), ids=lambda f: f.__name__)
+def test_planted_mistake_fails_the_gates(base, mutate):
+    lay, W, x, out, dumps = base
+    W2, lay2 = mutate(_copy(W), dict(lay))
+    out2, dumps2 = _run(W2, x, lay2)
+    assert forward_gates(x, dumps2, dumps, out2, out) != []
+
+
+# ------------------------------------------------------------------------------------------------
+# RoPE mistakes against the op-level gate of the QKV + RoPE kernel
+# ------------------------------------------------------------------------------------------------
+
+BF16_REL = 2.0 ** -8
+
+
+def _qk_after_rope(m, lay, qk, pos=None, perm=None):
+    cs, sn = oracle.rope_cos_sin(m, lay["pos"] if pos is None else pos)
+    H, Dh = m["n_heads"], m["head_dim"]
+    if perm is not None:  # rotate pairs (perm[j], perm[j + Dh/2]) instead of (j, j + Dh/2)
+        idx = np.concatenate([h * Dh + perm for h in range(H)])
+        inv = np.argsort(idx)
+        return oracle.rope_apply(qk[:, idx], H, Dh, m["rotary_dim"], cs, sn)[:, inv]
+    return oracle.rope_apply(qk, H, Dh, m["rotary_dim"], cs, sn)
+
+
+def _rope_mutations():
+    Dh = W0["model"]["head_dim"]
+    inter = np.empty(Dh, dtype=np.int64)
+    inter[:Dh // 2] = np.arange(0, Dh, 2)
+    inter[Dh // 2:] = np.arange(1, Dh, 2)
+    return {
+        "interleaved_pairs": lambda m, lay, qk: _qk_after_rope(m, lay, qk, perm=inter),
+        "wrong_direction": lambda m, lay, qk: _qk_after_rope(m, lay, qk, pos=-lay["pos"]),
+        "audio_after_video": lambda m, lay, qk: _qk_after_rope(
+            m, lay, qk, pos=lay["pos"] + np.outer(lay["tags"] == 1, [2.0, 0.0, 0.0])),
+        "axes_swapped": lambda m, lay, qk: _qk_after_rope(m, lay, qk, pos=lay["pos"][:, [1, 0, 2]]),
+    }
+
+
+@pytest.mark.parametrize("name", list(_rope_mutations()))
+def test_planted_rope_mistake_fails_the_qkv_op_gate(base, name):
+    lay, W, x, out, dumps = base
+    m = W0["model"]
+    y = oracle.rms_norm(x, m["norm_eps"])
+    qk = oracle.linear(y, W["blocks"][0]["w_qkv"][:m["hidden"]], None)
+    ref = _qk_after_rope(m, lay, qk)
+    mut = _rope_mutations()[name](m, lay, qk)
+    tol = BF16_REL * np.abs(ref) + 1e-5
+    assert np.any(np.abs(mut - ref) > tol)
+    # and the unmutated rotation passes the same gate under one bf16 rounding
+    assert np.all(np.abs(ref * (1 + 2 ** -9) - ref) <= tol)
