@@ -108,7 +108,7 @@ typedef struct {
   int64_t forwards;             /* dit_forward calls that launched work */
   int64_t kernels_launched;     /* every kernel this handle launched */
   int64_t gemm_launches, attention_launches, norm_launches, other_launches;
-  int64_t attention_tiles;      /* (q-tile, head) work items of the last forward (device count) */
+  int64_t attention_tiles;      /* (128-row q-tile, head) work items of the last forward (device count) */
   int64_t bound_bytes;          /* bytes of library-owned repacked weight copies */
   int32_t device_status;        /* last status word read back (0 = ok) */
   int32_t last_layout_error;    /* device validator's code for the last forward (0 = ok) */
@@ -273,8 +273,8 @@ DIT_API dit_status dit_op_pack_ffn_in(const void* w_in, const float* b_in, int F
  * output bit-independent of the others' (finite) values.  A non-finite value in one document's V
  * can still reach a neighbour sharing a boundary tile (0 * NaN = NaN).
  *   o     bf16 [n_tokens, H * Dh]
- * head_dim is 64 or 128.  The (document, 128-row q-tile) list is built on the device from cu_seqlens
- * into `workspace` (dit_attention_workspace_bytes(n_docs, n_tokens) bytes). */
+ * head_dim is 64 or 128.  The (document, 128-row q-tile) work list is built on the device from
+ * cu_seqlens into `workspace` (dit_attention_workspace_bytes(n_docs, n_tokens) bytes). */
 DIT_API size_t dit_attention_workspace_bytes(int n_docs, int n_tokens);
 DIT_API dit_status dit_op_attention(const void* q, const void* k, const void* vt, int n_pad, const int32_t* cu_seqlens,
                             int n_docs, int n_tokens, int n_heads, int head_dim, void* o, void* workspace,
@@ -286,8 +286,8 @@ DIT_API dit_status dit_op_attention(const void* q, const void* k, const void* vt
  * The pages have no counterpart of this call; it exists for such callers only.
  *   Arguments, layouts and results are those of dit_op_attention, without `workspace`.
  *   Scratch: a fixed array inside libdit.so's device memory (256 bytes of status words plus
- *   DIT_ATTENTION_NOALLOC_MAX_TILES (document, q-tile) entries of 8 bytes, about 64 KB), held by
- *   every GPU that loads the library until the process exits.  Nothing is allocated or freed.
+ *   DIT_ATTENTION_NOALLOC_MAX_TILES (document, 128-row q-tile) entries of 8 bytes, about 64 KB),
+ *   held by every GPU that loads the library until the process exits.  Nothing is allocated or freed.
  *   Capacity: ceil(n_tokens / 128) + n_docs <= DIT_ATTENTION_NOALLOC_MAX_TILES, else
  *   DIT_ERR_CAPACITY with dit_last_error(NULL) saying so, before any work is enqueued.
  *   Set-up: the first call on each device looks up the array's device address

@@ -236,12 +236,13 @@ def make_weights(w: dict, bf16: bool | None = None):
     seed = w["seed"]
 
     def gen(name, shp):
-        if name.startswith("ln") and name.endswith("_g"):
+        base = name.split(".")[-1]  # "block3.b_qkv" -> "b_qkv"
+        if base.startswith("ln") and base.endswith("_g"):
             v = np.ones(shp, dtype=np.float32)
             return v, (np.full(shp, 0x3F80, dtype=np.uint16) if bf16 else None)
-        if name.startswith("ln") and name.endswith("_b"):
+        if base.startswith("ln") and base.endswith("_b"):
             return np.zeros(shp, dtype=np.float32), (np.zeros(shp, dtype=np.uint16) if bf16 else None)
-        std = w["bias_std"] if name.startswith("b_") else w["w_std"]
+        std = w["bias_std"] if base.startswith("b_") else w["w_std"]
         if std == 0.0:
             return np.zeros(shp, dtype=np.float32), (np.zeros(shp, dtype=np.uint16) if bf16 else None)
         if bf16:

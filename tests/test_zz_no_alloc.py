@@ -52,12 +52,19 @@ def test_attention_noalloc_matches_workspace_entry_point():
 
 
 def test_attention_noalloc_rejects_sizes_beyond_its_scratch():
+    """More work items than the fixed array holds: rejected before any work is enqueued.  The inputs
+    are real, correctly sized buffers, so nothing could be out of bounds even if it were not."""
     from video_audio_gen_gb300 import build, dit
     build.build()
-    n = 128 * 8192 + 1  # ceil(n / 128) + 1 document = 8194 tiles > 8192
-    dummy = torch.empty(16, dtype=torch.bfloat16, device="cuda")
-    cu = torch.tensor([0, n], dtype=torch.int32, device="cuda")
-    st = dit.lib().dit_op_attention_noalloc(dummy.data_ptr(), dummy.data_ptr(), dummy.data_ptr(), (n + 7) & ~7,
-                                            cu.data_ptr(), 1, n, 1, 128, dummy.data_ptr(), None)
+    n_docs = 9000  # one token each: at least 9000 (document, q block) items > 8192
+    n = n_docs
+    n_pad = (n + 7) // 8 * 8
+    q = torch.zeros((n, 128), dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros_like(q)
+    vt = torch.zeros((128, n_pad), dtype=torch.bfloat16, device="cuda")
+    o = torch.empty_like(q)
+    cu = torch.arange(n + 1, dtype=torch.int32, device="cuda")
+    st = dit.lib().dit_op_attention_noalloc(q.data_ptr(), k.data_ptr(), vt.data_ptr(), n_pad, cu.data_ptr(), n_docs,
+                                            n, 1, 128, o.data_ptr(), None)
     assert st == dit.DIT_ERR_CAPACITY
     assert b"fixed scratch" in dit.lib().dit_last_error(None)

@@ -733,7 +733,7 @@ dit_status dit_op_attention(const void* q, const void* k, const void* vt, int n_
 // ------------------------------------------------------------------------------------------------
 namespace {
 
-constexpr int kNoAllocMaxItems = 8192;       // (document, 128-row q-tile) pairs
+constexpr int kNoAllocMaxItems = 8192;       // (document, 128-row q-tile) work items
 constexpr size_t kNoAllocStatusBytes = 256;  // StatusWords, padded to the array's alignment
 constexpr int kNoAllocMaxDevices = 64;
 
@@ -775,8 +775,8 @@ extern "C" dit_status dit_op_attention_noalloc(const void* q, const void* k, con
   const int max_items = attention_max_items(n_docs, n_tokens);
   if (max_items > kNoAllocMaxItems)
     return set_err(nullptr, DIT_ERR_CAPACITY,
-                   "dit_op_attention_noalloc: ceil(n_tokens / 128) + n_docs = %d exceeds its fixed scratch of %d "
-                   "tiles; use dit_op_attention with a workspace",
+                   "dit_op_attention_noalloc: ceil(n_tokens / 128) + n_docs = %d work items exceeds its fixed "
+                   "scratch of %d; use dit_op_attention with a workspace",
                    max_items, kNoAllocMaxItems);
   void* scratch = nullptr;
   cudaError_t e = noalloc_scratch(&scratch);

@@ -93,6 +93,92 @@ __global__ void __launch_bounds__(256) norm_mod_kernel(const float* __restrict__
   }
 }
 
+// The same norm + modulate for widths d = 1024 * VPT: a persistent grid of 256-thread blocks, each
+// thread owning VPT float4 of a row, walks the rows with a stride of gridDim.x and prefetches the
+// next row into registers before reducing the current one, so every block keeps a row's loads in
+// flight while it computes (the kernel is HBM-bound: 4 bytes in, 2 or 4 out per element).
+template <int VPT>
+__global__ void __launch_bounds__(256) norm_mod_persistent_kernel(
+    const float* __restrict__ x, int n, int d, int norm, float eps, const float* __restrict__ g,
+    const float* __restrict__ b, const uint8_t* __restrict__ tags, const float* __restrict__ shift,
+    const float* __restrict__ scale, long long stride, void* y, int out_kind, const int* status) {
+  if (status && (*reinterpret_cast<const volatile int*>(status) & kDevLayout)) return;
+  __shared__ float red[2][8];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int row = blockIdx.x;
+  float4 cur[VPT], nxt[VPT];
+  auto load = [&](int r, float4 (&v)[VPT]) {
+#pragma unroll
+    for (int i = 0; i < VPT; ++i)
+      v[i] = *reinterpret_cast<const float4*>(x + (size_t)r * d + (i * 256 + threadIdx.x) * 4);
+  };
+  if (row < n) load(row, cur);
+  int parity = 0;
+  // block sum through one of two shared slots (alternating, so one barrier per reduction suffices)
+  auto block_sum = [&](float s) -> float {
+    s = warp_sum(s);
+    if (lane == 0) red[parity][warp] = s;
+    __syncthreads();
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) t += red[parity][w];
+    parity ^= 1;
+    return t;
+  };
+  for (; row < n; row += gridDim.x) {
+    const int nrow = row + gridDim.x;
+    if (nrow < n) load(nrow, nxt);
+    float mean = 0.f;
+    if (norm == 1) {
+      float s = 0.f;
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) s += (cur[i].x + cur[i].y) + (cur[i].z + cur[i].w);
+      mean = block_sum(s) / (float)d;
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const float a0 = cur[i].x - mean, a1 = cur[i].y - mean, a2 = cur[i].z - mean, a3 = cur[i].w - mean;
+      ss += a0 * a0 + a1 * a1 + a2 * a2 + a3 * a3;
+    }
+    const float inv = 1.0f / sqrtf(block_sum(ss) / (float)d + eps);
+    const float* sh = shift ? shift + (size_t)tags[row] * stride : nullptr;
+    const float* sc = scale ? scale + (size_t)tags[row] * stride : nullptr;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int c = (i * 256 + threadIdx.x) * 4;
+      float o[4] = {(cur[i].x - mean) * inv, (cur[i].y - mean) * inv, (cur[i].z - mean) * inv,
+                    (cur[i].w - mean) * inv};
+      if (norm == 1) {
+        if (g) {
+          const float4 gg = *reinterpret_cast<const float4*>(g + c);
+          o[0] *= gg.x; o[1] *= gg.y; o[2] *= gg.z; o[3] *= gg.w;
+        }
+        if (b) {
+          const float4 bb = *reinterpret_cast<const float4*>(b + c);
+          o[0] += bb.x; o[1] += bb.y; o[2] += bb.z; o[3] += bb.w;
+        }
+      }
+      if (sh) {
+        const float4 a = *reinterpret_cast<const float4*>(sh + c);
+        const float4 m = *reinterpret_cast<const float4*>(sc + c);
+        o[0] = o[0] * (1.f + m.x) + a.x;
+        o[1] = o[1] * (1.f + m.y) + a.y;
+        o[2] = o[2] * (1.f + m.z) + a.z;
+        o[3] = o[3] * (1.f + m.w) + a.w;
+      }
+      if (out_kind == 0) {
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(y) + (size_t)row * d + c) =
+            make_uint2(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]));
+      } else {
+        *reinterpret_cast<float4*>(static_cast<float*>(y) + (size_t)row * d + c) = make_float4(o[0], o[1], o[2], o[3]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) cur[i] = nxt[i];
+  }
+}
+
 // ---------------------------------------------------------------------------------------------
 // RoPE cos/sin cache.  [BF] "What this enables": BuildRopeCosSin runs before any kernel with a
 // stored inv_freq; [H3] "The device-resident forward (W2b)": a per-row cos/sin cache whose angles
@@ -246,6 +332,26 @@ cudaError_t norm_modulate_launch(const float* x, int n, int d, int norm, float e
                                  const float* ln_b, const uint8_t* tags, const float* shift, const float* scale,
                                  long long mod_stride, void* y, int out_kind, const int* status, cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
+  if (d % 1024 == 0 && d <= 8192) {
+    switch (d / 1024) {
+#define DIT_VPT(k)                                                                                              \
+  case k: {                                                                                                     \
+    static int per_sm = 0;                                                                                      \
+    if (!per_sm &&                                                                                              \
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, norm_mod_persistent_kernel<k>, 256, 0) !=        \
+            cudaSuccess)                                                                                        \
+      per_sm = 4;                                                                                               \
+    int blocks = num_sms() * (per_sm > 0 ? per_sm : 1);                                                         \
+    if (blocks > n) blocks = n;                                                                                 \
+    norm_mod_persistent_kernel<k><<<blocks, 256, 0, s>>>(x, n, d, norm, eps, ln_g, ln_b, tags, shift, scale,     \
+                                                         mod_stride, y, out_kind, status);                      \
+    return cudaGetLastError();                                                                                  \
+  }
+      DIT_VPT(1) DIT_VPT(2) DIT_VPT(3) DIT_VPT(4) DIT_VPT(5) DIT_VPT(6) DIT_VPT(7) DIT_VPT(8)
+#undef DIT_VPT
+      default: break;
+    }
+  }
   switch (d / 128) {
 #define DIT_NV(k) \
   case k: return norm_launch_t<k>(x, n, d, norm, eps, ln_g, ln_b, tags, shift, scale, mod_stride, y, out_kind, status, s);
