@@ -86,6 +86,11 @@ def norm_bytes(m: dict, N: int) -> float:
     return N * m["hidden"] * (4 + 2) + N
 
 
+def fp32_alu_peak_tflops(peaks: dict, n_sms: int) -> float:
+    """FP32 FMA peak derived from unit counts: SMs x 128 FP32 lanes x 2 FLOP x the maximum SM clock."""
+    return n_sms * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -170,6 +175,17 @@ def oracle_sample(w: dict, lay: dict, budget_rows: int | None = None):
     d, F, H, Dh = m["hidden"], m["ffn_hidden"], m["n_heads"], m["head_dim"]
     threads = len(os.sched_getaffinity(0))
     oracle.set_threads(threads)
+    if not m["adaln"]:
+        # small token counts (the music DiT): one whole block over every token, scaled by L
+        sub = dict(m, n_blocks=1)
+        W = synth.make_weights(dict(w, model=sub))
+        x = synth.normal(w["seed"], "sample.x", (lay["n_tokens"], d), 1.0)
+        cs, sn = oracle.rope_cos_sin(sub, lay["pos"])
+        t0 = time.perf_counter()
+        oracle.block_forward(sub, W, 0, None, x, lay, cs, sn)
+        dt = time.perf_counter() - t0
+        oracle.set_threads(1)
+        return lay["n_tokens"] / (dt * m["n_blocks"]), dt, lay["n_tokens"], threads
     R = budget_rows or 2 * threads
     cu = lay["cu_seqlens"]
     # the sample's rows: spread over the longest document
@@ -276,6 +292,7 @@ def run_gpu(args, w, dist, rank, world):
     # roofline of the dominant kernel kind (largest summed time), from its CUDA-event durations
     fl = step_flops(m, lay["cu_seqlens"])
     peaks, peak_src = load_peaks()
+    alu_peak = fp32_alu_peak_tflops(peaks, torch.cuda.get_device_properties(dev).multi_processor_count)
     kernels = {}
     for k in KINDS:
         ms, n = kt[k]
@@ -285,8 +302,11 @@ def run_gpu(args, w, dist, rank, world):
         entry = {"launches": n, "avg_ms": round(avg, 4), "share": None}
         if k in fl["per_launch"]:
             tf = fl["per_launch"][k] / (avg * 1e-3) / 1e12
-            entry.update(bound="tensor", achieved_tflops=round(tf, 1),
-                         frac=round(tf / peaks["bf16_tflops_sustained"], 3))
+            if m["dtype"] == "fp32":
+                entry.update(bound="alu", achieved_tflops=round(tf, 1), frac=round(tf / alu_peak, 3))
+            else:
+                entry.update(bound="tensor", achieved_tflops=round(tf, 1),
+                             frac=round(tf / peaks["bf16_tflops_sustained"], 3))
         elif k == "norm_modulate":
             gbs = norm_bytes(m, N) / (avg * 1e-3) / 1e9
             entry.update(bound="hbm", achieved_gbs=round(gbs, 1), frac=round(gbs / peaks["hbm_gbs"], 3))
@@ -302,10 +322,17 @@ def run_gpu(args, w, dist, rank, world):
     src = "attention.cu" if top == "attention" else "gemm.cu"
     tr = TRAFFIC.get((top, args.workload))
     traffic = tr["bytes"] if tr and tr["src_sha"] == source_hash(src) else None
-    roofline = {"bound": "tensor", "kernel": top, "achieved": kernels[top]["achieved_tflops"],
-                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s", "frac": kernels[top]["frac"],
-                "traffic": traffic, "peak_source": f"bf16_tflops_sustained of {peak_src}",
-                "algorithmic_flops_per_launch": fl["per_launch"][top]}
+    if m["dtype"] == "fp32":
+        roofline = {"bound": "alu", "kernel": top, "achieved": kernels[top]["achieved_tflops"],
+                    "peak": round(alu_peak, 1), "unit": "TFLOP/s", "frac": kernels[top]["frac"], "traffic": traffic,
+                    "peak_source": "derived: SMs x 128 FP32 lanes x 2 FLOP x sm_max_mhz (FFMA; TF32 would not meet "
+                                   "the 1e-5 tolerance)",
+                    "algorithmic_flops_per_launch": fl["per_launch"][top]}
+    else:
+        roofline = {"bound": "tensor", "kernel": top, "achieved": kernels[top]["achieved_tflops"],
+                    "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s", "frac": kernels[top]["frac"],
+                    "traffic": traffic, "peak_source": f"bf16_tflops_sustained of {peak_src}",
+                    "algorithmic_flops_per_launch": fl["per_launch"][top]}
 
     if args.no_e2e:
         return dict(ms_step=ms_step, tokens=N, world=world, kernels=kernels, roofline=roofline, clocks=clk.summary(),
@@ -339,7 +366,7 @@ def workload_config(name, w, lay, extra=None):
                      f"{lay['n_tokens']} packed tokens in {lay['n_docs']} documents ({docs})",
          "tokens": int(lay["n_tokens"]), "documents": int(lay["n_docs"]),
          "cu_seqlens": [int(v) for v in lay["cu_seqlens"]],
-         "l2": "inputs larger than L2 (bf16 weights and fp32 activations of several GB stream every step)"}
+         "l2": "inputs larger than L2 (the weights, several GB, and the activations stream every step)"}
     if extra:
         c.update(extra)
     return c
@@ -358,8 +385,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="video_audio_bf16",
-                    choices=["video_audio_bf16", "long_doc_bf16", "denoise_loop", "video_audio_bf16_l1", "tiny",
-                             "ragged"])
+                    choices=["video_audio_bf16", "long_doc_bf16", "denoise_loop", "music_fp32", "video_audio_bf16_l1",
+                             "tiny", "ragged", "music_small"])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
@@ -386,6 +413,9 @@ def main():
         ms_step = lay["n_tokens"] / tps * 1e3
         sample = (f"{R} query rows x 1 block of the workload per step ({args.steps} steps, median), "
                   f"scaled by N={lay['n_tokens']} rows x L={w['model']['n_blocks']} blocks")
+        if not w["model"]["adaln"]:
+            sample = (f"1 whole block over all {R} tokens per step ({args.steps} steps, median), "
+                      f"scaled by L={w['model']['n_blocks']} blocks")
         line = {"impl": "reference", "metric": metric, "value": round(tps, 4), "unit": "tokens/s",
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 1),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -405,6 +435,7 @@ def main():
         tdist.init_process_group("nccl")
         dist = tdist
     r = run_gpu(args, w, dist, rank, world)
+    m_dtype = "f32" if w["model"]["dtype"] == "fp32" else "bf16"
     if rank == 0:
         tokens_total = r["tokens"] * world
         value = tokens_total / (r["ms_step"] * 1e-3)
@@ -412,7 +443,7 @@ def main():
         peaks, peak_src = load_peaks()
         line = {"metric": metric, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(r["ms_step"], 3),
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": m_dtype,
                 "data": "synthetic (seeded N(0, 0.02) bf16 weights, N(0, 1) fp32 tokens)",
                 "config": workload_config(args.workload, w, r["lay"], {
                     "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
@@ -426,8 +457,9 @@ def main():
                 "gpu_launches": int(r["launches"]), "clocks": r["clocks"]}
         if not args.no_cpu_baseline:
             tps, dt, R, threads = oracle_sample(w, r["lay"])
+            what = (f"1 whole block over all {R} tokens" if not w["model"]["adaln"] else f"{R} query rows x 1 block")
             line["cpu_baseline"] = {"value": round(tps, 4), "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                                    "sample": f"{R} query rows x 1 block ({dt:.1f} s on {threads} threads), "
+                                    "sample": f"{what} ({dt:.1f} s on {threads} threads), "
                                               f"scaled by N={r['tokens']} rows x L={w['model']['n_blocks']} blocks"}
         print(json.dumps(line))
     if dist is not None:

@@ -185,7 +185,7 @@ WORKLOADS = {
                    t=0.37, w_std=0.02, bias_std=0.02, x_std=1.0),
     "music_small": dict(model=_model(n_blocks=2, hidden=256, n_heads=2, head_dim=128, ffn_hidden=1024,
                                      norm="ln", norm_eps=1e-5, adaln=False, n_mod=1, rope_axes=1,
-                                     rope_dims=(64, 0, 0), rotary_dim=64, io_channels=32, dtype="fp32"),
+                                     rope_dims=(64, 0, 0), rotary_dim=64, io_channels=128, dtype="fp32"),
                         seed=12, docs=[dict(frames=37), dict(frames=37)], t=0.0, w_std=0.02,
                         bias_std=0.02, x_std=1.0),
 }

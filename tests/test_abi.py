@@ -50,6 +50,7 @@ def test_create_validates_config():
     h.h = None  # nothing was allocated; skip dit_destroy's device synchronisation here
     bad = [(dict(n_heads=23), dit.DIT_ERR_CONFIG), (dict(rope_dims=(32, 48, 40)), dit.DIT_ERR_CONFIG),
            (dict(hidden=3200, n_heads=25), dit.DIT_ERR_UNSUPPORTED), (dict(dtype="fp32"), dit.DIT_ERR_UNSUPPORTED),
+           (dict(dtype="fp32", adaln=False, io_channels=96), dit.DIT_ERR_UNSUPPORTED),
            (dict(head_dim=96, n_heads=32, rope_dims=(32, 32, 32), rotary_dim=96), dit.DIT_ERR_UNSUPPORTED), (dict(n_blocks=0), dit.DIT_ERR_CONFIG)]
     for kw, st in bad:
         with pytest.raises(dit.DitError) as e:

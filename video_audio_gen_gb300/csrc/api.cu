@@ -28,6 +28,11 @@ struct BlockDev {
   const void* w_qkv = nullptr;
   const void* w_o = nullptr;
   const void* w_down = nullptr;
+  const void* w_in = nullptr;      // fp32 path: value rows then gate rows, used as bound
+  float* ln1_g = nullptr;          // fp32 path, LayerNorm gains / shifts (NULL = none)
+  float* ln1_b = nullptr;
+  float* ln2_g = nullptr;
+  float* ln2_b = nullptr;
   void* w_in_packed = nullptr;
   float* b_qkv = nullptr;
   float* b_o = nullptr;
@@ -37,7 +42,7 @@ struct BlockDev {
 
 // Workspace layout of one forward (offsets in bytes from the workspace base).
 struct WsLayout {
-  size_t status, items, mod, cosc, sinc, resid, y, q, k, vt, o, h, total;
+  size_t status, items, mod, cosc, sinc, resid, y, q, k, vt, o, h, part = 0, resid_lo = 0, total;
   int n_pad, max_items, half, mod_rows;
 };
 
@@ -57,6 +62,9 @@ struct dit_handle {
   void* w_ada_all = nullptr;   // bf16 [ada_rows, t_dim]: L blocks x [n_mod * 6d], then final [n_mod * 2d]
   float* b_ada_all = nullptr;  // fp32 [ada_rows]
   int ada_rows = 0;
+  // fp32 path: final LayerNorm and the 1x1 pre/post convolutions
+  float *lnf_g = nullptr, *lnf_b = nullptr, *b_pre = nullptr, *b_post = nullptr;
+  const float *w_pre = nullptr, *w_post = nullptr;
   float* dump = nullptr;
   dit_stats stats;
   bool timing = false;
@@ -121,21 +129,30 @@ dit_status validate_config(const dit_config* c) {
   if (c->max_tokens < 1 || c->max_docs < 1) return set_err(nullptr, DIT_ERR_CONFIG, "max_tokens/max_docs must be >= 1");
   if (c->dtype != DIT_BF16 && c->dtype != DIT_FP32) return set_err(nullptr, DIT_ERR_CONFIG, "bad dtype");
   // What the sm_103a kernels tile.
-  if (c->dtype == DIT_FP32) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "the fp32 forward is not built in this library");
-  if (c->hidden % 256) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "hidden must be a multiple of 256");
   if (c->head_dim != 128 && c->head_dim != 64)
     return set_err(nullptr, DIT_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+  if (!norm_width_supported(c->hidden)) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "hidden width not tiled by the norm kernel");
+  if (c->dtype == DIT_FP32) {
+    if (c->adaln) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "the fp32 forward has no AdaLN (adaln must be 0)");
+    if (c->hidden % 128) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "fp32: hidden must be a multiple of 128");
+    if (c->ffn_hidden % 64) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "fp32: ffn_hidden must be a multiple of 64");
+    if (c->io_channels % 128) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "fp32: io_channels must be 0 or a multiple of 128");
+    return DIT_OK;
+  }
+  if (c->hidden % 256) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "hidden must be a multiple of 256");
   if ((c->rotary_dim / 2) % 16 || (c->head_dim - c->rotary_dim) % 16)
     return set_err(nullptr, DIT_ERR_UNSUPPORTED, "rotary_dim/2 and head_dim-rotary_dim must be multiples of 16");
   if (c->ffn_hidden % 128) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "ffn_hidden must be a multiple of 128");
-  if (!norm_width_supported(c->hidden)) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "hidden width not tiled by the norm kernel");
   if (c->io_channels) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "pre/post convolutions need the fp32 forward");
   if (c->norm == DIT_LAYERNORM) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "LayerNorm blocks need the fp32 forward");
   if (!c->adaln) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "the bf16 forward needs adaln = 1");
   return DIT_OK;
 }
 
+WsLayout ws_layout_fp32(const dit_config* c, int n, int n_docs);
+
 WsLayout ws_layout(const dit_config* c, int n, int n_docs) {
+  if (c->dtype == DIT_FP32) return ws_layout_fp32(c, n, n_docs);
   WsLayout w;
   const int d = c->hidden, F = c->ffn_hidden;
   w.n_pad = (n + 7) & ~7;
@@ -160,6 +177,42 @@ WsLayout ws_layout(const dit_config* c, int n, int n_docs) {
   w.vt = take((size_t)d * w.n_pad * 2);
   w.o = take((size_t)n * d * 2);
   w.h = take((size_t)n * F * 2);
+  w.total = off;
+  return w;
+}
+
+// fp32 forward: fp32 activations, split-K partial sums, frame-major staging for the 1x1 convolutions.
+// Reuses WsLayout's fields: q/k hold fp32 q, k; vt holds fp32 v [N, d]; h fp32 [N, F]; mod the
+// frame-major staging [N, io]; items the split-K partial buffer.
+WsLayout ws_layout_fp32(const dit_config* c, int n, int n_docs) {
+  WsLayout w;
+  const int d = c->hidden, F = c->ffn_hidden, io = c->io_channels;
+  w.n_pad = (n + 7) & ~7;
+  w.max_items = attention_max_items(n_docs, n);
+  w.half = c->rotary_dim / 2;
+  w.mod_rows = 0;
+  size_t widest = (size_t)3 * d;
+  if ((size_t)2 * F > widest) widest = (size_t)2 * F;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes);
+    return o;
+  };
+  w.status = take(64);
+  w.items = take((size_t)w.max_items * sizeof(int2));
+  w.cosc = take((size_t)n * w.half * 4);
+  w.sinc = take((size_t)n * w.half * 4);
+  w.resid = take((size_t)n * d * 4);
+  w.y = take((size_t)n * d * 4);
+  w.q = take((size_t)n * d * 4);
+  w.k = take((size_t)n * d * 4);
+  w.vt = take((size_t)n * d * 4);
+  w.o = take((size_t)n * d * 4);
+  w.h = take((size_t)n * F * 4);
+  w.mod = take((size_t)n * (io ? io : 1) * 4);
+  w.part = take((size_t)kSgemmMaxSplits * n * widest * 4);
+  w.resid_lo = take((size_t)n * d * 4);
   w.total = off;
   return w;
 }
@@ -223,6 +276,196 @@ struct Launch {
   }
 };
 
+
+// ------------------------------------------------------------------------------------------------
+// fp32 path (the music DiT shape): bind and forward
+// ------------------------------------------------------------------------------------------------
+dit_status bind_fp32(dit_handle* h, const dit_weights* w, cudaStream_t s) {
+  const dit_config& c = h->cfg;
+  const int d = c.hidden, F = c.ffn_hidden, io = c.io_channels;
+  for (int l = 0; l < c.n_blocks; ++l) {
+    const dit_block_weights& b = w->blocks[l];
+    const struct {
+      const void* p;
+      const char* name;
+    } req[] = {{b.w_qkv, "w_qkv"}, {b.w_o, "w_o"}, {b.w_in, "w_in"}, {b.w_down, "w_down"}};
+    for (const auto& r : req) {
+      if (!r.p) return set_err(h, DIT_ERR_MISSING_WEIGHT, "missing weight: blocks[%d].%s", l, r.name);
+      if (!aligned16(r.p)) return set_err(h, DIT_ERR_INVALID_ARG, "blocks[%d].%s is not 16-byte aligned", l, r.name);
+    }
+  }
+  if (io && !w->w_pre) return set_err(h, DIT_ERR_MISSING_WEIGHT, "missing weight: w_pre");
+  if (io && !w->w_post) return set_err(h, DIT_ERR_MISSING_WEIGHT, "missing weight: w_post");
+  cudaStreamSynchronize(s);
+  for (void* p : h->allocs) cudaFree(p);
+  h->allocs.clear();
+  h->blocks.assign(c.n_blocks, BlockDev());
+  h->stats.bound_bytes = 0;
+  h->bound = false;
+  cudaError_t e = cudaSuccess;
+  // fp32 copies of the small vectors (NULL stays NULL for LayerNorm parameters: no affine)
+  auto vec = [&](const void* src, long long n, bool zero_if_null) -> float* {
+    if (!src && !zero_if_null) return nullptr;
+    float* dst = static_cast<float*>(dev_alloc(h, n * 4, &e));
+    if (e != cudaSuccess) return nullptr;
+    e = src ? to_f32_launch(src, 0, n, dst, s) : cudaMemsetAsync(dst, 0, n * 4, s);
+    return e == cudaSuccess ? dst : nullptr;
+  };
+  for (int l = 0; l < c.n_blocks; ++l) {
+    const dit_block_weights& b = w->blocks[l];
+    BlockDev& bd = h->blocks[l];
+    bd.w_qkv = b.w_qkv;
+    bd.w_o = b.w_o;
+    bd.w_in = b.w_in;
+    bd.w_down = b.w_down;
+    if (!(bd.b_qkv = vec(b.b_qkv, 3ll * d, true))) return cuda_err(h, e, "bind b_qkv");
+    if (!(bd.b_o = vec(b.b_o, d, true))) return cuda_err(h, e, "bind b_o");
+    if (!(bd.b_in_packed = vec(b.b_in, 2ll * F, true))) return cuda_err(h, e, "bind b_in");
+    if (!(bd.b_down = vec(b.b_down, d, true))) return cuda_err(h, e, "bind b_down");
+    bd.ln1_g = vec(b.ln1_g, d, false);
+    bd.ln1_b = vec(b.ln1_b, d, false);
+    bd.ln2_g = vec(b.ln2_g, d, false);
+    bd.ln2_b = vec(b.ln2_b, d, false);
+    if (e != cudaSuccess) return cuda_err(h, e, "bind layer norm");
+  }
+  h->lnf_g = vec(w->lnf_g, d, false);
+  h->lnf_b = vec(w->lnf_b, d, false);
+  if (io) {
+    h->w_pre = static_cast<const float*>(w->w_pre);
+    h->w_post = static_cast<const float*>(w->w_post);
+    h->b_pre = vec(w->b_pre, d, true);
+    h->b_post = vec(w->b_post, io, true);
+  }
+  if (e != cudaSuccess) return cuda_err(h, e, "bind final / io weights");
+  DIT_CK(h, cudaStreamSynchronize(s), "bind sync");
+  h->bound = true;
+  return DIT_OK;
+}
+
+// One fp32 GEMM of the forward: partial sums, then the reduction that applies the epilogue.
+struct Sgemm {
+  dit_handle* h;
+  cudaStream_t s;
+  float* part;
+  const int* status;
+  int S;  // effective splits of the last partial launch
+  cudaError_t run(const float* A, const float* B, int M, int N, int K) {
+    const int want = sgemm_splits(M, N, K);
+    S = sgemm_effective_splits(K, want);
+    return sgemm_partial_launch(A, B, M, N, K, want, part, status, s);
+  }
+};
+
+dit_status forward_fp32(dit_handle* h, const float* x_tokens, const int32_t* cu_seqlens, int n_docs,
+                        const int32_t* doc_ids, const uint8_t* modality_tags, const double* pos_thw, int N,
+                        float* out, void* workspace, const WsLayout& L, cudaStream_t s) {
+  const dit_config& c = h->cfg;
+  const int d = c.hidden, F = c.ffn_hidden, H = c.n_heads, io = c.io_channels;
+  StatusWords* sw = at<StatusWords>(workspace, L.status);
+  int* status = &sw->bits;
+  int2* items = at<int2>(workspace, L.items);
+  float* cosc = at<float>(workspace, L.cosc);
+  float* sinc = at<float>(workspace, L.sinc);
+  float* resid = at<float>(workspace, L.resid);
+  float* resid_lo = at<float>(workspace, L.resid_lo);
+  float* y = at<float>(workspace, L.y);
+  float* q = at<float>(workspace, L.q);
+  float* k = at<float>(workspace, L.k);
+  float* v = at<float>(workspace, L.vt);
+  float* o = at<float>(workspace, L.o);
+  float* hb = at<float>(workspace, L.h);
+  float* xt = at<float>(workspace, L.mod);
+  Sgemm g{h, s, at<float>(workspace, L.part), status, 1};
+  {
+    Launch ln(h, s, 6);
+    DIT_CK(h, cudaMemsetAsync(sw, 0, sizeof(StatusWords), s), "status reset");
+    DIT_CK(h, attention_schedule_launch(cu_seqlens, n_docs, N, doc_ids, modality_tags, 1, items, &sw->count,
+                                        L.max_items, &sw->layout_code, status, s), "layout check");
+    ln.done();
+  }
+  if (L.half > 0) {
+    Launch ln(h, s, 6);
+    DIT_CK(h, rope_cache_launch(pos_thw, N, c.rope_axes, c.rope_dims, c.rope_base, cosc, sinc, status, s), "rope cache");
+    ln.done();
+  }
+  if (io) {
+    // 1x1 pre-convolution as MatmulBT on the frame-major activation ([M3] "What moved")
+    Launch ln(h, s, 6);
+    DIT_CK(h, io_transpose_launch(x_tokens, xt, cu_seqlens, doc_ids, N, io, 1, status, s), "to frames");
+    DIT_CK(h, g.run(xt, h->w_pre, N, d, io), "pre-conv");
+    DIT_CK(h, sgemm_reduce_store_launch(g.part, g.S, N, d, h->b_pre, resid, 0, resid_lo, status, s),
+           "pre-conv reduce");
+    ln.done();
+  } else {
+    DIT_CK(h, cudaMemcpyAsync(resid, x_tokens, (size_t)N * d * 4, cudaMemcpyDeviceToDevice, s), "copy x");
+    DIT_CK(h, cudaMemsetAsync(resid_lo, 0, (size_t)N * d * 4, s), "clear residual low part");
+  }
+  for (int l = 0; l < c.n_blocks; ++l) {
+    const BlockDev& B = h->blocks[l];
+    {
+      Launch ln(h, s, 5);
+      DIT_CK(h, norm_modulate_launch(resid, resid_lo, N, d, c.norm, c.norm_eps, B.ln1_g, B.ln1_b, nullptr, nullptr, nullptr, 0, y,
+                                     1, status, s), "norm1");
+      ln.done();
+    }
+    {
+      Launch ln(h, s, 0);
+      DIT_CK(h, g.run(y, static_cast<const float*>(B.w_qkv), N, 3 * d, d), "qkv");
+      DIT_CK(h, sgemm_reduce_qkv_launch(g.part, g.S, N, d, c.head_dim, L.half, B.b_qkv, cosc, sinc, q, k, v, status, s),
+             "qkv reduce");
+      ln.done();
+    }
+    {
+      Launch ln(h, s, 1);
+      DIT_CK(h, attention_f32_launch(q, k, v, cu_seqlens, doc_ids, N, H, c.head_dim, o, status, s), "attention");
+      ln.done();
+    }
+    {
+      Launch ln(h, s, 2);
+      DIT_CK(h, g.run(o, static_cast<const float*>(B.w_o), N, d, d), "out-proj");
+      DIT_CK(h, sgemm_reduce_store_launch(g.part, g.S, N, d, B.b_o, resid, 1, resid_lo, status, s), "out-proj reduce");
+      ln.done();
+    }
+    {
+      Launch ln(h, s, 5);
+      DIT_CK(h, norm_modulate_launch(resid, resid_lo, N, d, c.norm, c.norm_eps, B.ln2_g, B.ln2_b, nullptr, nullptr, nullptr, 0, y,
+                                     1, status, s), "norm2");
+      ln.done();
+    }
+    {
+      Launch ln(h, s, 3);
+      DIT_CK(h, g.run(y, static_cast<const float*>(B.w_in), N, 2 * F, d), "ffn up");
+      DIT_CK(h, sgemm_reduce_swiglu_launch(g.part, g.S, N, F, B.b_in_packed, hb, status, s), "ffn up reduce");
+      ln.done();
+    }
+    {
+      Launch ln(h, s, 4);
+      DIT_CK(h, g.run(hb, static_cast<const float*>(B.w_down), N, d, F), "ffn down");
+      DIT_CK(h, sgemm_reduce_store_launch(g.part, g.S, N, d, B.b_down, resid, 1, resid_lo, status, s),
+             "ffn down reduce");
+      ln.done();
+    }
+    if (h->dump)
+      DIT_CK(h, cudaMemcpyAsync(h->dump + (size_t)l * N * d, resid, (size_t)N * d * 4, cudaMemcpyDeviceToDevice, s),
+             "dump");
+  }
+  {
+    Launch ln(h, s, 5);
+    DIT_CK(h, norm_modulate_launch(resid, resid_lo, N, d, c.norm, c.norm_eps, h->lnf_g, h->lnf_b, nullptr, nullptr, nullptr, 0,
+                                   io ? y : out, 1, status, s), "final norm");
+    ln.done();
+  }
+  if (io) {
+    Launch ln(h, s, 6);
+    DIT_CK(h, g.run(y, h->w_post, N, io, d), "post-conv");
+    DIT_CK(h, sgemm_reduce_store_launch(g.part, g.S, N, io, h->b_post, xt, 0, nullptr, status, s), "post-conv reduce");
+    DIT_CK(h, io_transpose_launch(xt, out, cu_seqlens, doc_ids, N, io, 0, status, s), "to channels");
+    ln.done();
+  }
+  h->stats.forwards++;
+  return DIT_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -265,6 +508,7 @@ dit_status dit_bind_weights(dit_handle* h, const dit_weights* w, void* stream) {
   if (w->n_blocks != c.n_blocks)
     return set_err(h, DIT_ERR_INVALID_ARG, "weights.n_blocks %d != config n_blocks %d", w->n_blocks, c.n_blocks);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (c.dtype == DIT_FP32) return bind_fp32(h, w, s);
   const int d = c.hidden, F = c.ffn_hidden, nm = c.n_modalities, td = c.t_embed_dim;
   // Missing tensors are reported by name before anything is allocated.
   for (int l = 0; l < c.n_blocks; ++l) {
@@ -365,6 +609,9 @@ dit_status dit_forward(dit_handle* h, const float* x_tokens, const int32_t* cu_s
   if (!(timestep >= 0.f && timestep <= 1.f)) return set_err(h, DIT_ERR_INVALID_ARG, "timestep must be in [0, 1]");
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (c.dtype == DIT_FP32)
+    return forward_fp32(h, x_tokens, cu_seqlens, n_docs, doc_ids, modality_tags, pos_thw, n_tokens, out, workspace, L,
+                        s);
   const int d = c.hidden, F = c.ffn_hidden, H = c.n_heads, nm = c.n_modalities;
   const int N = n_tokens;
   StatusWords* sw = at<StatusWords>(workspace, L.status);
@@ -374,6 +621,7 @@ dit_status dit_forward(dit_handle* h, const float* x_tokens, const int32_t* cu_s
   float* cosc = at<float>(workspace, L.cosc);
   float* sinc = at<float>(workspace, L.sinc);
   float* resid = at<float>(workspace, L.resid);
+  const float* resid_lo = nullptr;  // the bf16 forward keeps a plain fp32 residual
   void* y = at<void>(workspace, L.y);
   void* q = at<void>(workspace, L.q);
   void* k = at<void>(workspace, L.k);
@@ -419,7 +667,7 @@ dit_status dit_forward(dit_handle* h, const float* x_tokens, const int32_t* cu_s
     const float* ml = mod + (size_t)l * nm * 6 * d;
     {
       Launch ln(h, s, 5);
-      DIT_CK(h, norm_modulate_launch(resid, N, d, c.norm, c.norm_eps, nullptr, nullptr, modality_tags, ml + 0 * d,
+      DIT_CK(h, norm_modulate_launch(resid, resid_lo, N, d, c.norm, c.norm_eps, nullptr, nullptr, modality_tags, ml + 0 * d,
                                      ml + 1 * d, mstride, y, 0, status, s), "norm1");
       ln.done();
     }
@@ -448,7 +696,7 @@ dit_status dit_forward(dit_handle* h, const float* x_tokens, const int32_t* cu_s
     }
     {
       Launch ln(h, s, 5);
-      DIT_CK(h, norm_modulate_launch(resid, N, d, c.norm, c.norm_eps, nullptr, nullptr, modality_tags, ml + 3 * d,
+      DIT_CK(h, norm_modulate_launch(resid, resid_lo, N, d, c.norm, c.norm_eps, nullptr, nullptr, modality_tags, ml + 3 * d,
                                      ml + 4 * d, mstride, y, 0, status, s), "norm2");
       ln.done();
     }
@@ -474,7 +722,7 @@ dit_status dit_forward(dit_handle* h, const float* x_tokens, const int32_t* cu_s
   {
     const float* mf = mod + (size_t)c.n_blocks * nm * 6 * d;
     Launch ln(h, s, 5);
-    DIT_CK(h, norm_modulate_launch(resid, N, d, c.norm, c.norm_eps, nullptr, nullptr, modality_tags, mf, mf + d,
+    DIT_CK(h, norm_modulate_launch(resid, resid_lo, N, d, c.norm, c.norm_eps, nullptr, nullptr, modality_tags, mf, mf + d,
                                    2ll * d, out, 1, status, s), "final norm");
     ln.done();
   }
@@ -601,7 +849,7 @@ dit_status dit_op_norm_modulate(const float* x, int n, int d, int norm, float ep
   if (!norm_width_supported(d)) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "width %d not tiled by the norm kernel", d);
   if (!aligned16(x) || !aligned16(y) || (shift && (!aligned16(shift) || !aligned16(scale) || mod_stride % 4)))
     return set_err(nullptr, DIT_ERR_INVALID_ARG, "norm_modulate pointers must be 16-byte aligned");
-  cudaError_t e = norm_modulate_launch(x, n, d, norm, eps, ln_g, ln_b, tags, shift, scale, mod_stride, y, out_kind,
+  cudaError_t e = norm_modulate_launch(x, nullptr, n, d, norm, eps, ln_g, ln_b, tags, shift, scale, mod_stride, y, out_kind,
                                        nullptr, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? DIT_OK : cuda_err(nullptr, e, "norm_modulate");
 }

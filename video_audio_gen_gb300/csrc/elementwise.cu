@@ -24,7 +24,8 @@ __device__ __forceinline__ float warp_sum(float v) {
 //   out    y = n * (1 + scale[tag]) + shift[tag]       (no modulation when shift == nullptr)
 // ---------------------------------------------------------------------------------------------
 template <int NV>
-__global__ void __launch_bounds__(256) norm_mod_kernel(const float* __restrict__ x, int n, int d, int norm, float eps,
+__global__ void __launch_bounds__(256) norm_mod_kernel(const float* __restrict__ x, const float* __restrict__ x_lo,
+                                                       int n, int d, int norm, float eps,
                                                        const float* __restrict__ g, const float* __restrict__ b,
                                                        const uint8_t* __restrict__ tags,
                                                        const float* __restrict__ shift,
@@ -40,6 +41,10 @@ __global__ void __launch_bounds__(256) norm_mod_kernel(const float* __restrict__
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
     v[i] = *reinterpret_cast<const float4*>(xr + (i * 32 + lane) * 4);
+    if (x_lo) {
+      const float4 e = *reinterpret_cast<const float4*>(x_lo + (size_t)row * d + (i * 32 + lane) * 4);
+      v[i].x += e.x; v[i].y += e.y; v[i].z += e.z; v[i].w += e.w;
+    }
     s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
   }
   float mean = 0.f, inv;
@@ -99,7 +104,7 @@ __global__ void __launch_bounds__(256) norm_mod_kernel(const float* __restrict__
 // flight while it computes (the kernel is HBM-bound: 4 bytes in, 2 or 4 out per element).
 template <int VPT>
 __global__ void __launch_bounds__(256) norm_mod_persistent_kernel(
-    const float* __restrict__ x, int n, int d, int norm, float eps, const float* __restrict__ g,
+    const float* __restrict__ x, const float* __restrict__ x_lo, int n, int d, int norm, float eps, const float* __restrict__ g,
     const float* __restrict__ b, const uint8_t* __restrict__ tags, const float* __restrict__ shift,
     const float* __restrict__ scale, long long stride, void* y, int out_kind, const int* status) {
   if (status && (*reinterpret_cast<const volatile int*>(status) & kDevLayout)) return;
@@ -109,8 +114,13 @@ __global__ void __launch_bounds__(256) norm_mod_persistent_kernel(
   float4 cur[VPT], nxt[VPT];
   auto load = [&](int r, float4 (&v)[VPT]) {
 #pragma unroll
-    for (int i = 0; i < VPT; ++i)
+    for (int i = 0; i < VPT; ++i) {
       v[i] = *reinterpret_cast<const float4*>(x + (size_t)r * d + (i * 256 + threadIdx.x) * 4);
+      if (x_lo) {  // compensated residual: high + low part
+        const float4 e = *reinterpret_cast<const float4*>(x_lo + (size_t)r * d + (i * 256 + threadIdx.x) * 4);
+        v[i].x += e.x; v[i].y += e.y; v[i].z += e.z; v[i].w += e.w;
+      }
+    }
   };
   if (row < n) load(row, cur);
   int parity = 0;
@@ -299,12 +309,13 @@ __global__ void to_f32_kernel(const void* __restrict__ src, int is_bf16, long lo
 }
 
 template <int NV>
-cudaError_t norm_launch_t(const float* x, int n, int d, int norm, float eps, const float* g, const float* b,
+cudaError_t norm_launch_t(const float* x, const float* x_lo, int n, int d, int norm, float eps, const float* g,
+                          const float* b,
                           const uint8_t* tags, const float* shift, const float* scale, long long stride, void* y,
                           int out_kind, const int* status, cudaStream_t s) {
   const int rows_per_block = 8;
   norm_mod_kernel<NV><<<(n + rows_per_block - 1) / rows_per_block, 32 * rows_per_block, 0, s>>>(
-      x, n, d, norm, eps, g, b, tags, shift, scale, stride, y, out_kind, status);
+      x, x_lo, n, d, norm, eps, g, b, tags, shift, scale, stride, y, out_kind, status);
   return cudaGetLastError();
 }
 
@@ -328,7 +339,7 @@ int num_sms() {
   return n;
 }
 
-cudaError_t norm_modulate_launch(const float* x, int n, int d, int norm, float eps, const float* ln_g,
+cudaError_t norm_modulate_launch(const float* x, const float* x_lo, int n, int d, int norm, float eps, const float* ln_g,
                                  const float* ln_b, const uint8_t* tags, const float* shift, const float* scale,
                                  long long mod_stride, void* y, int out_kind, const int* status, cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
@@ -343,7 +354,7 @@ cudaError_t norm_modulate_launch(const float* x, int n, int d, int norm, float e
       per_sm = 4;                                                                                               \
     int blocks = num_sms() * (per_sm > 0 ? per_sm : 1);                                                         \
     if (blocks > n) blocks = n;                                                                                 \
-    norm_mod_persistent_kernel<k><<<blocks, 256, 0, s>>>(x, n, d, norm, eps, ln_g, ln_b, tags, shift, scale,     \
+    norm_mod_persistent_kernel<k><<<blocks, 256, 0, s>>>(x, x_lo, n, d, norm, eps, ln_g, ln_b, tags, shift, scale, \
                                                          mod_stride, y, out_kind, status);                      \
     return cudaGetLastError();                                                                                  \
   }
@@ -354,7 +365,7 @@ cudaError_t norm_modulate_launch(const float* x, int n, int d, int norm, float e
   }
   switch (d / 128) {
 #define DIT_NV(k) \
-  case k: return norm_launch_t<k>(x, n, d, norm, eps, ln_g, ln_b, tags, shift, scale, mod_stride, y, out_kind, status, s);
+  case k: return norm_launch_t<k>(x, x_lo, n, d, norm, eps, ln_g, ln_b, tags, shift, scale, mod_stride, y, out_kind, status, s);
     DIT_NV(1) DIT_NV(2) DIT_NV(3) DIT_NV(4) DIT_NV(5) DIT_NV(6) DIT_NV(8) DIT_NV(10) DIT_NV(12) DIT_NV(16)
     DIT_NV(20) DIT_NV(24) DIT_NV(32) DIT_NV(40) DIT_NV(48) DIT_NV(64)
 #undef DIT_NV

@@ -64,7 +64,7 @@ cudaError_t attention_schedule_launch(const int32_t* cu, int n_docs, int n_token
 int attention_max_items(int n_docs, int n_tokens);
 
 // Elementwise / reduction kernels.
-cudaError_t norm_modulate_launch(const float* x, int n, int d, int norm, float eps, const float* ln_g,
+cudaError_t norm_modulate_launch(const float* x, const float* x_lo, int n, int d, int norm, float eps, const float* ln_g,
                                  const float* ln_b, const uint8_t* tags, const float* shift, const float* scale,
                                  long long mod_stride, void* y, int out_kind, const int* status, cudaStream_t s);
 cudaError_t rope_cache_launch(const double* pos, int n, int n_axes, const int* dims, double base, float* cos_out,
@@ -78,5 +78,25 @@ cudaError_t to_f32_launch(const void* src, int src_is_bf16, long long n, float* 
 
 int num_sms();
 bool norm_width_supported(int d);
+
+// fp32 path (csrc/fp32.cu): split-K FFMA GEMM D = A B^T (A [M, K], B [N, K], fp32, N % 128 == 0,
+// K % 16 == 0) into partials [S][M][N], then fixed-order reductions with the epilogues.
+constexpr int kSgemmMaxSplits = 16;
+int sgemm_splits(int M, int N, int K);
+int sgemm_effective_splits(int K, int S);
+cudaError_t sgemm_partial_launch(const float* A, const float* B, int M, int N, int K, int S, float* part,
+                                 const int* status, cudaStream_t s);
+cudaError_t sgemm_reduce_store_launch(const float* part, int S, int M, int N, const float* bias, float* out, int add,
+                                      float* lo, const int* status, cudaStream_t s);
+cudaError_t sgemm_reduce_qkv_launch(const float* part, int S, int M, int d, int Dh, int half, const float* bias,
+                                    const float* cs, const float* sn, float* q, float* k, float* v, const int* status,
+                                    cudaStream_t s);
+cudaError_t sgemm_reduce_swiglu_launch(const float* part, int S, int M, int F, const float* bias, float* h,
+                                       const int* status, cudaStream_t s);
+cudaError_t attention_f32_launch(const float* q, const float* k, const float* v, const int32_t* cu,
+                                 const int32_t* doc_ids, int n, int H, int Dh, float* o, const int* status,
+                                 cudaStream_t s);
+cudaError_t io_transpose_launch(const float* src, float* dst, const int32_t* cu, const int32_t* doc_ids, int n, int io,
+                                int to_frames, const int* status, cudaStream_t s);
 
 }  // namespace dit
