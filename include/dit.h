@@ -191,6 +191,14 @@ DIT_API dit_status dit_euler_step(float* x, const float* v, int64_t n, float sig
 DIT_API dit_status dit_get_stats(const dit_handle* h, dit_stats* out);
 DIT_API dit_status dit_sync_status(dit_handle* h, const void* workspace, void* stream);
 
+/* Failure-path self-test of the bounded waits.  Launches one kernel that waits on an mbarrier
+ * nothing ever arrives at, through the same bounded wait the GEMM and attention pipelines use, with
+ * a limit of limit_ns (0 < limit_ns <= 1e9).  The wait runs out, the kernel records the timeout in
+ * *status_word (a caller-owned device int) and returns; the call synchronises `stream` and returns
+ * DIT_ERR_DEVICE_TIMEOUT when that happened (DIT_OK would mean the wait ended some other way).  No
+ * trap, no fault: the context stays usable for the next call. */
+DIT_API dit_status dit_selftest_wait_timeout(uint64_t limit_ns, int* status_word, void* stream);
+
 /* Per-block dumps for parity tests: when `dump` is non-NULL each later forward copies the fp32
  * residual after block l into dump + l * n_tokens * d (device, caller-owned, L * N * d floats). */
 DIT_API dit_status dit_set_dump(dit_handle* h, float* dump);

@@ -270,3 +270,21 @@ def test_fp32_forward_matches_oracle(name):
     oracle.set_threads(1)
     worst = _fp32_check(w, run, ref, dumps, per_element=(name == "music_small"))
     print(f"{name}: worst max|g - r| / RMS over the layer outputs = {worst:.3e}")
+
+
+# ------------------------------------------------------------------------------------------------
+# failure detection without a GPU fault
+# ------------------------------------------------------------------------------------------------
+
+def test_bounded_wait_runs_out_reports_and_leaves_context_usable():
+    """A wait on an mbarrier that nothing arrives at (the flag nobody sets) ends after its limit with
+    the timeout recorded in the status word; the next forward on the same context runs normally."""
+    dit, gu = _dit(), _gu()
+    word = torch.zeros(1, dtype=torch.int32, device="cuda")
+    import time
+    t0 = time.perf_counter()
+    assert dit.selftest_wait_timeout(1_000_000, word) == dit.DIT_ERR_DEVICE_TIMEOUT  # 1 ms limit
+    assert time.perf_counter() - t0 < 5.0
+    assert int(word.item()) & 1  # kDevTimeout
+    run = gu.run_forward(synth.WORKLOADS["tiny"])
+    assert run["status"] == 0 and np.isfinite(run["out"]).all()

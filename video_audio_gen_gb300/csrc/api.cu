@@ -801,6 +801,19 @@ dit_status dit_sync_status(dit_handle* h, const void* workspace, void* stream) {
   return DIT_OK;
 }
 
+dit_status dit_selftest_wait_timeout(uint64_t limit_ns, int* status_word, void* stream) {
+  if (!status_word || limit_ns == 0 || limit_ns > 1000000000ull)
+    return set_err(nullptr, DIT_ERR_INVALID_ARG, "status_word must be a device int; 0 < limit_ns <= 1e9");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int bits = 0;
+  cudaError_t e = cudaMemsetAsync(status_word, 0, sizeof(int), s);
+  if (e == cudaSuccess) e = wait_timeout_selftest_launch(status_word, limit_ns, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&bits, status_word, sizeof(int), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_err(nullptr, e, "wait self-test");
+  return (bits & kDevTimeout) ? DIT_ERR_DEVICE_TIMEOUT : DIT_OK;
+}
+
 dit_status dit_set_dump(dit_handle* h, float* dump) {
   if (!h) return DIT_ERR_INVALID_ARG;
   h->dump = dump;

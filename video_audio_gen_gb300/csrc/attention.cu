@@ -320,299 +320,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   }
 }
 
-// ---------------------------------------------------------------------------------------------
-// Two q-tiles per CTA.  One CTA = one (document, 256-row q block, head): tiles A = rows [q0, q0+128)
-// and B = [q0+128, q0+256) share every K / V^T tile, and two softmax warpgroups work on them in turn
-// so that one tile's softmax overlaps the other tile's MMAs.
-//   warp 0      TMA producer: Q_A, Q_B once; K(j) and V^T(j) through 2-stage rings
-//   warp 1      TMEM allocator + MMA issuer, in the order
-//                 S_A(0) S_B(0) | PV_A(0) S_A(1) PV_B(0) S_B(1) | PV_A(1) S_A(2) PV_B(1) S_B(2) | ...
-//   warps 2-5   softmax of tile A, warps 6-9 softmax of tile B (thread <-> query row)
-// TMEM: S_A [0,128) S_B [128,256) O_A [256,256+HD) O_B [256+HD,256+2HD).  The softmax writes P as
-// packed bf16 over the first 64 columns of its S region and the P V MMA reads its A operand from
-// there, so P never touches shared memory.  Because S_t(j+1) is issued after PV_t(j) and the MMAs of
-// one thread execute in order, S_t(j+1) overwrites P_t(j) only after PV_t(j) has read it, and when a
-// softmax warpgroup sees S_t(j) complete, O_t already holds every P_t(i) V(i), i < j: the lazy
-// rescale of O_t needs no extra wait.
-// ---------------------------------------------------------------------------------------------
-template <int HD>
-struct PairPlan {
-  static constexpr int Q_BYTES = 128 * HD * 2;   // one q-tile
-  static constexpr int K_BYTES = 128 * HD * 2;
-  static constexpr int V_ATOM = HD * 128;
-  static constexpr int V_BYTES = 2 * V_ATOM;
-  static constexpr int SMEM = 2 * Q_BYTES + KV_STAGES * (K_BYTES + V_BYTES) + 1024 + 512;
-  static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, TK);
-  static constexpr uint32_t IDESC_O = idesc_bf16_f32(128, HD);
-};
-constexpr int PAIR_THREADS = 320;
-constexpr int PAIR_ROWS = 256;
-constexpr int ITEM_ROWS = TQ;  // query rows per scheduled work item of the kernel in use
-
-template <int HD>
-__global__ void __launch_bounds__(PAIR_THREADS, 1)
-    attention_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                          const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O, const AttnArgs args) {
-  if (args.status && (*reinterpret_cast<volatile int*>(args.status) & kDevLayout)) return;
-  const int count = *args.count;
-  const int head = blockIdx.x / args.max_items;
-  const int item_idx = blockIdx.x - head * args.max_items;
-  if (item_idx >= count || head >= args.n_heads) return;
-  const int2 item = args.items[item_idx];
-  const int doc = item.x, q0 = item.y;
-  const int ds = args.cu[doc], de = args.cu[doc + 1];
-  const bool has_b = q0 + 128 < de;
-  const int kv_base = (ds / TK) * TK;
-  const int n_kv = (de - kv_base + TK - 1) / TK;
-
-  using Plan = PairPlan<HD>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem;                                   // [2] tiles
-  uint8_t* sK = sQ + 2 * Plan::Q_BYTES;                 // [stage]
-  uint8_t* sV = sK + KV_STAGES * Plan::K_BYTES;         // [stage]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + KV_STAGES * Plan::V_BYTES);
-  uint64_t* q_full = bars;
-  uint64_t* k_full = bars + 1;    // [2]
-  uint64_t* k_empty = bars + 3;   // [2]
-  uint64_t* v_full = bars + 5;    // [2]
-  uint64_t* v_empty = bars + 7;   // [2]
-  uint64_t* s_full = bars + 9;    // [2] per tile
-  uint64_t* p_full = bars + 11;   // [2] per tile
-  uint64_t* o_done = bars + 13;   // [2] per tile
-  uint64_t* mma_done = bars + 15;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&k_full[s], 1);
-      mbar_init(&k_empty[s], 1);
-      mbar_init(&v_full[s], 1);
-      mbar_init(&v_empty[s], 1);
-      mbar_init(&s_full[s], 1);
-      mbar_init(&p_full[s], 4);
-      mbar_init(&o_done[s], 1);
-    }
-    mbar_init(mma_done, 1);
-    *abort_flag = 0;
-    mbar_fence_init();
-  }
-  if (warp == 1) tmem_alloc(tmem_slot, 512);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      const int hx = head * HD;
-      mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * Plan::Q_BYTES);
-#pragma unroll
-      for (int a = 0; a < HD / 64; ++a) tma_load_2d(sQ + a * ATOM, &tmQ, q_full, hx + 64 * a, q0);
-      if (has_b) {
-#pragma unroll
-        for (int a = 0; a < HD / 64; ++a)
-          tma_load_2d(sQ + Plan::Q_BYTES + a * ATOM, &tmQ, q_full, hx + 64 * a, q0 + 128);
-      }
-      int nk = 0, nv = 0;
-      bool ok = true;
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int st = j & 1;
-        const int kv0 = kv_base + j * TK;
-        if (!mbar_wait(&k_empty[st], ((j >> 1) & 1) ^ 1, abort_flag, args.status)) break;
-        mbar_arrive_expect_tx(&k_full[st], Plan::K_BYTES);
-#pragma unroll
-        for (int a = 0; a < HD / 64; ++a)
-          tma_load_2d(sK + st * Plan::K_BYTES + a * ATOM, &tmK, &k_full[st], hx + 64 * a, kv0);
-        ++nk;
-        if (!mbar_wait(&v_empty[st], ((j >> 1) & 1) ^ 1, abort_flag, args.status)) break;
-        mbar_arrive_expect_tx(&v_full[st], Plan::V_BYTES);
-        tma_load_2d(sV + st * Plan::V_BYTES, &tmV, &v_full[st], kv0, hx);
-        tma_load_2d(sV + st * Plan::V_BYTES + Plan::V_ATOM, &tmV, &v_full[st], kv0 + 64, hx);
-        ++nv;
-      }
-      wait_noabort(q_full, 0);
-      for (int j = nk - 2 < 0 ? 0 : nk - 2; j < nk; ++j) wait_noabort(&k_full[j & 1], (j >> 1) & 1);
-      for (int j = nv - 2 < 0 ? 0 : nv - 2; j < nv; ++j) wait_noabort(&v_full[j & 1], (j >> 1) & 1);
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      bool ok = mbar_wait(q_full, 0, abort_flag, args.status);
-      tc_fence_after();
-      const uint32_t q_addr = smem_u32(sQ);
-      auto issue_s = [&](int t, int j) {
-        const uint32_t k_addr = smem_u32(sK + (j & 1) * Plan::K_BYTES);
-        const uint32_t qa = q_addr + t * Plan::Q_BYTES;
-#pragma unroll
-        for (int ks = 0; ks < HD / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * ATOM + (ks & 3) * 32;
-          umma_bf16(tmem + t * TK, sdesc_sw128(qa + off), sdesc_sw128(k_addr + off), Plan::IDESC_S, ks != 0);
-        }
-        umma_commit(&s_full[t]);
-      };
-      auto issue_pv = [&](int t, int j) {
-        const uint32_t v_addr = smem_u32(sV + (j & 1) * Plan::V_BYTES);
-#pragma unroll
-        for (int ks = 0; ks < TK / 16; ++ks) {
-          const uint32_t v_off = (ks >> 2) * Plan::V_ATOM + (ks & 3) * 32;
-          umma_bf16_ts(tmem + 256 + t * HD, tmem + t * TK + ks * 8, sdesc_sw128(v_addr + v_off), Plan::IDESC_O,
-                       (j | ks) != 0);
-        }
-      };
-      if (ok) ok = mbar_wait(&k_full[0], 0, abort_flag, args.status);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0, 0);
-        if (has_b) issue_s(1, 0);
-        umma_commit(&k_empty[0]);
-      }
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const bool more = j + 1 < n_kv;
-        if (!mbar_wait(&v_full[j & 1], (j >> 1) & 1, abort_flag, args.status)) break;
-        if (more && !mbar_wait(&k_full[(j + 1) & 1], ((j + 1) >> 1) & 1, abort_flag, args.status)) break;
-        for (int t = 0; t < (has_b ? 2 : 1); ++t) {
-          if (!mbar_wait(&p_full[t], j & 1, abort_flag, args.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          issue_pv(t, j);
-          if (more) issue_s(t, j + 1);
-        }
-        if (!ok) break;
-        umma_commit(&v_empty[j & 1]);
-        if (more) umma_commit(&k_empty[(j + 1) & 1]);
-      }
-      umma_commit(&o_done[0]);
-      umma_commit(&o_done[1]);
-      umma_commit(mma_done);
-      wait_noabort(mma_done, 0);
-    }
-  } else {
-    const int t = (warp - 2) >> 2;               // 0: tile A (warps 2-5), 1: tile B (warps 6-9)
-    if (t == 0 || has_b) {
-      const int quarter = warp & 3;
-      const int r = quarter * 32 + lane;
-      const int row = q0 + t * 128 + r;
-      const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-      const uint32_t ts = tmem + t * TK + lane_off;
-      const uint32_t to = tmem + 256 + t * HD + lane_off;
-      const float sc = args.scale_log2;
-      float m = -INFINITY, l = 0.f;
-      bool ok = true;
-      for (int j = 0; j < n_kv; ++j) {
-        if (!mbar_wait(&s_full[t], j & 1, abort_flag, args.status)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const int c0 = kv_base + j * TK;
-        const int lo = ds > c0 ? ds - c0 : 0;
-        const int hi = de - c0 < TK ? de - c0 : TK;
-        const bool interior = lo == 0 && hi == TK;
-        // The running max m is an attained score, so p = exp2(s * scale - m) never loses the largest
-        // weights; it is raised only when a tile's scores would overflow the exponent (row sum past
-        // 2^64) and on the first tile (m = -inf).  Most tiles skip the max entirely.  S stays in
-        // TMEM until P is written, so the rare raise pass reads it again.
-        // sv holds the 128 scores; p is packed in place: pair i (columns 2i, 2i+1) goes to sv[i],
-        // which is at or below both sources, so nothing unread is overwritten.
-        uint32_t sv[TK];
-        float rs = 0.f, alpha = 1.f;
-        bool need_max = (j == 0);
-#pragma unroll 1
-        for (int pass = 0; pass < 2; ++pass) {
-#pragma unroll
-          for (int c = 0; c < TK; c += 32) tmem_ld32(ts + c, *reinterpret_cast<uint32_t(*)[32]>(&sv[c]));
-#pragma unroll
-          for (int c = 0; c < TK; c += 32) tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&sv[c]));
-          if (need_max) {
-            float mx = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < TK; i += 2) {
-              const float a = (i >= lo && i < hi) ? __uint_as_float(sv[i]) : -INFINITY;
-              const float b = (i + 1 >= lo && i + 1 < hi) ? __uint_as_float(sv[i + 1]) : -INFINITY;
-              mx = fmax3(mx, a, b);
-            }
-            const float m_new = fmaxf(m, mx * sc);
-            alpha = fast_exp2(m - m_new);  // 0 on the first tile (m = -inf)
-            l *= alpha;
-            m = m_new;
-          }
-          float2 rs2 = make_float2(0.f, 0.f);
-          const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-m, -m);
-#pragma unroll
-          for (int i = 0; i < 64; ++i) {
-            const float2 x =
-                ffma2(make_float2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])), sc2, nm2);
-            float2 p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-            if (!interior) {
-              if (!(2 * i >= lo && 2 * i < hi)) p.x = 0.f;
-              if (!(2 * i + 1 >= lo && 2 * i + 1 < hi)) p.y = 0.f;
-            }
-            rs2 = fadd2(rs2, p);
-            sv[i] = pack_bf16x2(p.x, p.y);
-          }
-          rs = rs2.x + rs2.y;
-          const bool over = !(rs <= 18446744073709551616.0f);  // > 2^64, inf or NaN
-          if (!__any_sync(0xffffffffu, over)) break;
-          need_max = true;
-        }
-        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {  // warp-uniform: tcgen05.ld/st are .aligned
-          // the max was raised: O_t holds P_t(i) V(i) for all i < j (see the ordering note above)
-          // and is rescaled in place before P_t(j) is published
-#pragma unroll
-          for (int c = 0; c < HD; c += 32) {
-            uint32_t ov[32];
-            tmem_ld32_sync(to + c, ov);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-            tmem_st32(to + c, ov);
-            tmem_st_wait();
-          }
-        }
-        // P over the first 64 columns of this tile's S region (all of S has been read)
-        tmem_st32(ts, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-        tmem_st32(ts + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-        tmem_st_wait();
-        l += rs;
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[t]);
-      }
-      if (ok) {
-        ok = mbar_wait(&o_done[t], 0, abort_flag, args.status);
-        tc_fence_after();
-      }
-      if (ok) {
-        const float inv = 1.f / l;
-        __nv_bfloat16* orow = O + (size_t)row * (args.n_heads * HD) + head * HD;
-#pragma unroll
-        for (int c = 0; c < HD; c += 32) {
-          uint32_t ov[32];
-          tmem_ld32_sync(to + c, ov);
-          if (row < de) {
-#pragma unroll
-            for (int i = 0; i < 32; i += 8)
-              st_global_v4(orow + c + i, pack_bf16x2(__uint_as_float(ov[i]) * inv, __uint_as_float(ov[i + 1]) * inv),
-                           pack_bf16x2(__uint_as_float(ov[i + 2]) * inv, __uint_as_float(ov[i + 3]) * inv),
-                           pack_bf16x2(__uint_as_float(ov[i + 4]) * inv, __uint_as_float(ov[i + 5]) * inv),
-                           pack_bf16x2(__uint_as_float(ov[i + 6]) * inv, __uint_as_float(ov[i + 7]) * inv));
-          }
-        }
-      }
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
-}
+constexpr int ITEM_ROWS = TQ;  // query rows per scheduled work item
 
 // Validate the packed layout and emit the (document, q-tile) list, longest documents first.
 // Codes follow the layout contract: 1 no documents, 2 cu[0] != 0, 3 not strictly increasing,
@@ -661,7 +369,7 @@ __global__ void schedule_kernel(const int32_t* cu, int n_docs, int n_tokens, con
       }
       prev_len = best_len;
       prev_idx = best;
-      for (int q = cu[best]; q < cu[best + 1]; q += TQ) {
+      for (int q = cu[best]; q < cu[best + 1]; q += ITEM_ROWS) {
         if (n >= max_items) {
           code = 7;
           break;
@@ -678,7 +386,7 @@ __global__ void schedule_kernel(const int32_t* cu, int n_docs, int n_tokens, con
   if (layout_code) *layout_code = code;
 }
 
-int attention_max_items_impl(int n_docs, int n_tokens) { return (n_tokens + TQ - 1) / TQ + n_docs; }
+int attention_max_items_impl(int n_docs, int n_tokens) { return (n_tokens + ITEM_ROWS - 1) / ITEM_ROWS + n_docs; }
 
 template <int HD>
 cudaError_t attention_launch_t(const void* q, const void* k, const void* vt, void* o, const AttnArgs& args,

@@ -308,6 +308,19 @@ __global__ void to_f32_kernel(const void* __restrict__ src, int is_bf16, long lo
     dst[i] = is_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(src)[i]) : static_cast<const float*>(src)[i];
 }
 
+// Failure-path self-test: wait on an mbarrier that nothing ever arrives at, through the same bounded
+// wait every pipelined kernel uses, with a short limit.  The wait must run out, record kDevTimeout
+// in the status word and return, leaving the context usable.
+__global__ void wait_timeout_selftest_kernel(int* status, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  abort_flag = 0;
+  mbar_fence_init();
+  mbar_wait(&bar, 0, &abort_flag, status, limit_ns);
+}
+
 template <int NV>
 cudaError_t norm_launch_t(const float* x, const float* x_lo, int n, int d, int norm, float eps, const float* g,
                           const float* b,
@@ -429,6 +442,11 @@ cudaError_t pack_ffn_in_launch(const void* w_in, const float* b_in, int F, int d
 cudaError_t to_f32_launch(const void* src, int src_is_bf16, long long n, float* dst, cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
   to_f32_kernel<<<grid_for(n, 256), 256, 0, s>>>(src, src_is_bf16, n, dst);
+  return cudaGetLastError();
+}
+
+cudaError_t wait_timeout_selftest_launch(int* status, unsigned long long limit_ns, cudaStream_t s) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, s>>>(status, limit_ns);
   return cudaGetLastError();
 }
 

@@ -196,7 +196,6 @@ __device__ __forceinline__ void epi_qkv(const GemmArgs& a, uint32_t t, int row, 
 //   phase B  each warp walks 32 rows; per row its 32 lanes own 2 adjacent columns, so the loads and
 //            stores of x (and of the gate and bias) are 256 contiguous bytes per row.
 constexpr int RES_COLS = 64;
-constexpr int RES_STAGE_BYTES = BM * RES_COLS * 4;  // 32 KB
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 

@@ -78,6 +78,7 @@ cudaError_t to_f32_launch(const void* src, int src_is_bf16, long long n, float* 
 
 int num_sms();
 bool norm_width_supported(int d);
+cudaError_t wait_timeout_selftest_launch(int* status, unsigned long long limit_ns, cudaStream_t s);
 
 // fp32 path (csrc/fp32.cu): split-K FFMA GEMM D = A B^T (A [M, K], B [N, K], fp32, N % 128 == 0,
 // K % 16 == 0) into partials [S][M][N], then fixed-order reductions with the epilogues.

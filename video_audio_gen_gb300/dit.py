@@ -26,7 +26,7 @@ EXPORTS = ["dit_create", "dit_destroy", "dit_last_error", "dit_workspace_bytes",
            "dit_set_dump", "dit_set_kernel_timing", "dit_get_kernel_times", "dit_op_norm_modulate",
            "dit_op_rope_cache", "dit_op_adaln", "dit_op_gemm", "dit_op_gemm_qkv_rope", "dit_op_gemm_gated_residual",
            "dit_op_gemm_swiglu", "dit_op_pack_ffn_in", "dit_attention_workspace_bytes", "dit_op_attention",
-           "dit_op_attention_noalloc"]
+           "dit_op_attention_noalloc", "dit_selftest_wait_timeout"]
 
 
 class DitError(RuntimeError):
@@ -107,6 +107,7 @@ def lib():
             "dit_attention_workspace_bytes": (sz, [i32, i32]),
             "dit_op_attention": (i32, [vp, vp, vp, i32, vp, i32, i32, i32, i32, vp, vp, vp]),
             "dit_op_attention_noalloc": (i32, [vp, vp, vp, i32, vp, i32, i32, i32, i32, vp, vp]),
+            "dit_selftest_wait_timeout": (i32, [ctypes.c_uint64, vp, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -231,6 +232,12 @@ class Dit:
 # ------------------------------------------------------------------------------------------------
 # op-level calls
 # ------------------------------------------------------------------------------------------------
+
+def selftest_wait_timeout(limit_ns: int, status_word, stream=None) -> int:
+    """Run the bounded-wait self-test; returns the dit_status (DIT_ERR_DEVICE_TIMEOUT when the wait ran
+    out and was reported, as it should)."""
+    return int(lib().dit_selftest_wait_timeout(int(limit_ns), _ptr(status_word), _stream(stream)))
+
 
 def euler_step(x, v, sigma: float, sigma_next: float, stream=None):
     _check(lib().dit_euler_step(_ptr(x), _ptr(v), x.numel(), float(sigma), float(sigma_next), _stream(stream)))
