@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(256) norm_mod_kernel(const float* __restrict__
 // thread owning VPT float4 of a row, walks the rows with a stride of gridDim.x and prefetches the
 // next row into registers before reducing the current one, so every block keeps a row's loads in
 // flight while it computes (the kernel is HBM-bound: 4 bytes in, 2 or 4 out per element).
-template <int VPT>
+template <int VPT, bool LO>
 __global__ void __launch_bounds__(256) norm_mod_persistent_kernel(
     const float* __restrict__ x, const float* __restrict__ x_lo, int n, int d, int norm, float eps, const float* __restrict__ g,
     const float* __restrict__ b, const uint8_t* __restrict__ tags, const float* __restrict__ shift,
@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(256) norm_mod_persistent_kernel(
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
       v[i] = *reinterpret_cast<const float4*>(x + (size_t)r * d + (i * 256 + threadIdx.x) * 4);
-      if (x_lo) {  // compensated residual: high + low part
+      if (LO) {  // compensated residual: high + low part
         const float4 e = *reinterpret_cast<const float4*>(x_lo + (size_t)r * d + (i * 256 + threadIdx.x) * 4);
         v[i].x += e.x; v[i].y += e.y; v[i].z += e.z; v[i].w += e.w;
       }
@@ -362,13 +362,17 @@ cudaError_t norm_modulate_launch(const float* x, const float* x_lo, int n, int d
   case k: {                                                                                                     \
     static int per_sm = 0;                                                                                      \
     if (!per_sm &&                                                                                              \
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, norm_mod_persistent_kernel<k>, 256, 0) !=        \
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, norm_mod_persistent_kernel<k, false>, 256, 0) != \
             cudaSuccess)                                                                                        \
       per_sm = 4;                                                                                               \
     int blocks = num_sms() * (per_sm > 0 ? per_sm : 1);                                                         \
     if (blocks > n) blocks = n;                                                                                 \
-    norm_mod_persistent_kernel<k><<<blocks, 256, 0, s>>>(x, x_lo, n, d, norm, eps, ln_g, ln_b, tags, shift, scale, \
-                                                         mod_stride, y, out_kind, status);                      \
+    if (x_lo)                                                                                                   \
+      norm_mod_persistent_kernel<k, true><<<blocks, 256, 0, s>>>(x, x_lo, n, d, norm, eps, ln_g, ln_b, tags,     \
+                                                                 shift, scale, mod_stride, y, out_kind, status); \
+    else                                                                                                        \
+      norm_mod_persistent_kernel<k, false><<<blocks, 256, 0, s>>>(x, x_lo, n, d, norm, eps, ln_g, ln_b, tags,    \
+                                                                  shift, scale, mod_stride, y, out_kind, status); \
     return cudaGetLastError();                                                                                  \
   }
       DIT_VPT(1) DIT_VPT(2) DIT_VPT(3) DIT_VPT(4) DIT_VPT(5) DIT_VPT(6) DIT_VPT(7) DIT_VPT(8)

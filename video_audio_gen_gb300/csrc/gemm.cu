@@ -196,6 +196,7 @@ __device__ __forceinline__ void epi_qkv(const GemmArgs& a, uint32_t t, int row, 
 //   phase B  each warp walks 32 rows; per row its 32 lanes own 2 adjacent columns, so the loads and
 //            stores of x (and of the gate and bias) are 256 contiguous bytes per row.
 constexpr int RES_COLS = 64;
+constexpr int RES_BATCH = 32;  // rows whose loads a warp has in flight at once
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -230,11 +231,11 @@ __device__ __forceinline__ void epi_resid(const GemmArgs& a, uint32_t t, int til
     if (a.bias) bb = *reinterpret_cast<const float2*>(a.bias + col);
     const int chunk = lane >> 1, half8 = (lane & 1) * 8;
 #pragma unroll 1
-    for (int rr0 = 0; rr0 < 32; rr0 += 8) {
-      float2 acc[8], xv[8], gv[8];
-      int rows[8];
+    for (int rr0 = 0; rr0 < 32; rr0 += RES_BATCH) {
+      float2 acc[RES_BATCH], xv[RES_BATCH], gv[RES_BATCH];
+      int rows[RES_BATCH];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < RES_BATCH; ++u) {
         const int rt = ew * 32 + rr0 + u;
         rows[u] = tile_row0 + rt;
         const uint32_t sa = smem_u32(stage) + rt * (RES_COLS * 4) + ((chunk ^ (rt & 7)) << 4) + half8;
@@ -246,7 +247,7 @@ __device__ __forceinline__ void epi_resid(const GemmArgs& a, uint32_t t, int til
         }
       }
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < RES_BATCH; ++u) {
         if (rows[u] < a.M) {
           float2 o;
           o.x = xv[u].x + gv[u].x * (acc[u].x + bb.x);
