@@ -7,12 +7,15 @@
 // One CTA = one (document, 128-row q-tile, head).  Key/value tiles are 128 tokens wide and start
 // at multiples of 128 in the packed sequence (so the TMA x coordinate of the transposed V is
 // 16-byte aligned); columns outside the document are masked to -inf.
-//   warp 0     TMA producer: Q once, then (K tile, V^T tile) pairs through a 2-stage ring
-//   warp 1     TMEM allocator + UMMA issuer: S(j) = Q K(j)^T into TMEM, O(j) = P(j) V(j) into TMEM
-//   warps 2-5  softmax: thread <-> query row; reads S(j) from TMEM, keeps the running max/sum,
-//              writes P(j) (bf16) into shared memory as the next MMA's A operand, and folds the
-//              partial O(j) from TMEM into its fp32 register accumulator (rescaled by exp2(dm)).
-// TMEM: S double buffer (2 x 128 columns) + O partial double buffer (2 x 128 columns) = 512.
+//   warp 0     TMA producer: Q once, then K and V^T tiles through two 2-stage rings
+//   warp 1     TMEM allocator + UMMA issuer: S(j) = Q K(j)^T into TMEM; P(j) V(j) into TMEM, its
+//              first 64 key columns accumulated into O_0 and the last 64 into O_1
+//   warps 2-9  softmax, two warps per query row: warp half h owns key columns [64h, 64h + 64) of
+//              every tile and keeps its own running max m_h, sum l_h and accumulator O_h, exactly as
+//              two independent passes over disjoint key subsets would; the halves exchange nothing
+//              per tile and are merged once at the end:
+//                  o = (2^(m_0-m) O_0 + 2^(m_1-m) O_1) / (2^(m_0-m) l_0 + 2^(m_1-m) l_1),  m = max(m_0, m_1)
+// TMEM: S double buffer (2 x 128 columns) + O_0, O_1 (2 x HD columns) <= 512.
 #include "common.cuh"
 #include "kernels.h"
 #include "tmap.h"
@@ -25,7 +28,8 @@ constexpr int TQ = 128, TK = 128;
 constexpr int ATOM = 128 * 64 * 2;         // 128 rows x 64 bf16 columns, 128-byte swizzled (16 KB)
 constexpr int P_BYTES = 2 * ATOM;          // P tile: 128 q rows x 128 kv columns
 constexpr int KV_STAGES = 2;
-constexpr int ATT_THREADS = 192;
+constexpr int ATT_THREADS = 320;
+constexpr int SOFTMAX_THREADS = 256;
 
 // Shared-memory plan for head dim HD (64 or 128):
 //   Q  [128 q, HD]   HD/64 atoms of 16 KB          K  [128 kv, HD]  HD/64 atoms of 16 KB
@@ -95,7 +99,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
       mbar_init(&s_full[s], 1);
-      mbar_init(&p_full[s], 4);
+      mbar_init(&p_full[s], SOFTMAX_THREADS / 32);
       mbar_init(&o_done[s], 1);
     }
     mbar_init(mma_done, 1);
@@ -108,7 +112,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t t_s = tmem;            // S buffers at columns 0, 128
-  const uint32_t t_o = tmem + 256;      // O accumulator at columns [256, 256 + HD)
+  const uint32_t t_o = tmem + 256;      // O_0 at columns [256, 256 + HD), O_1 at [256 + HD, 256 + 2 HD)
 
   if (warp == 0) {
     if (lane == 0) {
@@ -187,9 +191,11 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         const uint32_t v_addr = smem_u32(sV + (j & 1) * Plan::V_BYTES);
 #pragma unroll
         for (int ks = 0; ks < TK / 16; ++ks) {
+          // key columns [0, 64) (P atom 0, V^T atom 0) -> O_0; [64, 128) (atom 1) -> O_1
           const uint32_t p_off = (ks >> 2) * ATOM + (ks & 3) * 32;
           const uint32_t v_off = (ks >> 2) * Plan::V_ATOM + (ks & 3) * 32;
-          umma_bf16(t_o, sdesc_sw128(p_addr + p_off), sdesc_sw128(v_addr + v_off), Plan::IDESC_O, (j | ks) != 0);
+          umma_bf16(t_o + (ks >> 2) * HD, sdesc_sw128(p_addr + p_off), sdesc_sw128(v_addr + v_off), Plan::IDESC_O,
+                    (j | (ks & 3)) != 0);
         }
         umma_commit(&o_done[pb]);
         umma_commit(&v_empty[pb]);
@@ -201,15 +207,19 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     }
   } else {
     // ---------------- softmax warps ----------------
-    // Thread <-> query row.  O accumulates in TMEM through the MMA; the running max m is only raised
-    // (and O, l rescaled by exp2(m_old - m_new)) when a row's max grows by more than 2^8, so most
-    // tiles never touch O.  Between raises p = exp2(s * scale - m) stays below 2^8.
+    // Two warps per row: TMEM lane quarter = warp % 4 (the rows a warp may access), key-column half
+    // = (warp - 2) / 4.  O_h accumulates in TMEM through the MMA; the running max m_h is only raised
+    // (and O_h, l_h rescaled by exp2(m_old - m_new)) when the half-row max grows by more than 2^8,
+    // so most tiles never touch O_h.  Between raises p = exp2(s * scale - m_h) stays below 2^8.
+    constexpr int HC = TK / 2;                   // key columns per half
     const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;          // tile row owned by this thread
-    const int row = q0 + r;                     // packed-sequence row
+    const int half = (warp - 2) >> 2;
+    const int r = quarter * 32 + lane;           // tile row owned by this thread
+    const int row = q0 + r;                      // packed-sequence row
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t t_oh = t_o + half * HD + lane_off;
     const float sc = args.scale_log2;
-    constexpr float kRescaleThreshold = 8.0f;   // log2 units
+    constexpr float kRescaleThreshold = 8.0f;    // log2 units
     float m = -INFINITY, l = 0.f;
     bool ok = true;
 
@@ -220,35 +230,38 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         break;
       }
       tc_fence_after();
-      const int c0 = kv_base + j * TK;
+      const int c0 = kv_base + j * TK + half * HC;
       const int lo = ds > c0 ? ds - c0 : 0;
-      const int hi = de - c0 < TK ? de - c0 : TK;
-      const bool interior = (lo == 0) && (hi == TK);
-      const uint32_t ts = t_s + sb * TK + lane_off;
-      uint32_t sv[TK];
+      const int hi = de - c0 < HC ? de - c0 : HC;
+      const bool interior = (lo == 0) && (hi == HC);
+      const uint32_t ts = t_s + sb * TK + half * HC + lane_off;
+      uint32_t sv[HC];
 #pragma unroll
-      for (int c = 0; c < TK; c += 32) tmem_ld32(ts + c, *reinterpret_cast<uint32_t(*)[32]>(&sv[c]));
+      for (int c = 0; c < HC; c += 32) tmem_ld32(ts + c, *reinterpret_cast<uint32_t(*)[32]>(&sv[c]));
 #pragma unroll
-      for (int c = 0; c < TK; c += 32) tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&sv[c]));
-      float mx = -INFINITY;
-      if (interior) {
+      for (int c = 0; c < HC; c += 32) tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&sv[c]));
+      if (!interior) {
 #pragma unroll
-        for (int i = 0; i < TK; ++i) mx = fmaxf(mx, __uint_as_float(sv[i]));
-      } else {
-#pragma unroll
-        for (int i = 0; i < TK; ++i) {
-          const bool in = i >= lo && i < hi;
-          if (!in) sv[i] = __float_as_uint(-INFINITY);
-          mx = fmaxf(mx, __uint_as_float(sv[i]));
-        }
+        for (int i = 0; i < HC; ++i)
+          if (i < lo || i >= hi) sv[i] = __float_as_uint(-INFINITY);
       }
-      const float m_cand = mx * sc;
-      const bool raise = m_cand > m + kRescaleThreshold;  // always true on the first tile (m = -inf)
+      // half-row max: four independent chains of three-input max
+      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < HC; i += 8) {
+        mx0 = fmax3(mx0, __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]));
+        mx1 = fmax3(mx1, __uint_as_float(sv[i + 2]), __uint_as_float(sv[i + 3]));
+        mx2 = fmax3(mx2, __uint_as_float(sv[i + 4]), __uint_as_float(sv[i + 5]));
+        mx3 = fmax3(mx3, __uint_as_float(sv[i + 6]), __uint_as_float(sv[i + 7]));
+      }
+      const float m_cand = fmaxf(fmax3(mx0, mx1, mx2), mx3) * sc;
+      // true on the first tile with a key of the document in this half (m = -inf until then)
+      const bool raise = m_cand > m + kRescaleThreshold;
       if (__any_sync(0xffffffffu, raise)) {
         const float m_new = raise ? m_cand : m;
-        const float alpha = raise ? fast_exp2(m - m_new) : 1.f;  // exp2(-inf) = 0 on the first tile
+        const float alpha = raise ? fast_exp2(m - m_new) : 1.f;  // exp2(-inf) = 0 before the first key
         if (j > 0) {
-          // O holds sum_{i<j} P(i) V(i) relative to m: wait for the last PV, rescale in place
+          // O_h holds this half's sum over tiles < j relative to m: wait for the last PV, rescale
           if (!mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, args.status)) {
             ok = false;
             break;
@@ -257,32 +270,37 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
 #pragma unroll
           for (int c = 0; c < HD; c += 32) {
             uint32_t ov[32];
-            tmem_ld32_sync(t_o + lane_off + c, ov);
+            tmem_ld32_sync(t_oh + c, ov);
 #pragma unroll
             for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-            tmem_st32(t_o + lane_off + c, ov);
+            tmem_st32(t_oh + c, ov);
             tmem_st_wait();
           }
         }
         l *= alpha;
         m = m_new;
       }
-      // p = exp2(s * scale - m) -> bf16 into shared memory (swizzled K-major A operand of P V)
-      const uint32_t p_base = smem_u32(sP + sb * P_BYTES) + r * 128;
-      float rs = 0.f;
+      // A half that has seen no key of the document yet has m = -inf and only masked scores:
+      // p = exp2(-inf - 0) = 0 keeps O_h and l_h at zero.
+      const float mu = m == -INFINITY ? 0.f : m;
+      // p = exp2(s * scale - m) -> bf16 into shared memory (swizzled K-major A operand of P V):
+      // this half's 64 columns are exactly P atom `half`, one 128-byte swizzled row per query row
+      const uint32_t p_row = smem_u32(sP + sb * P_BYTES + half * ATOM) + r * 128;
+      float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
 #pragma unroll
-      for (int c = 0; c < TK; c += 8) {
+      for (int c = 0; c < HC; c += 8) {
         float p[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          p[i] = fast_exp2(fmaf(__uint_as_float(sv[c + i]), sc, -m));
-          rs += p[i];
-        }
-        const int chunk = (c & 63) >> 3;  // 16-byte chunk within the 128-byte row of atom c / 64
-        st_shared_v4(p_base + (c >> 6) * ATOM + ((chunk ^ (r & 7)) << 4), pack_bf16x2(p[0], p[1]),
-                     pack_bf16x2(p[2], p[3]), pack_bf16x2(p[4], p[5]), pack_bf16x2(p[6], p[7]));
+        for (int i = 0; i < 8; ++i) p[i] = fast_exp2(fmaf(__uint_as_float(sv[c + i]), sc, -mu));
+        rs0 += p[0] + p[1];
+        rs1 += p[2] + p[3];
+        rs2 += p[4] + p[5];
+        rs3 += p[6] + p[7];
+        const int chunk = c >> 3;
+        st_shared_v4(p_row + ((chunk ^ (r & 7)) << 4), pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]),
+                     pack_bf16x2(p[4], p[5]), pack_bf16x2(p[6], p[7]));
       }
-      l += rs;
+      l += (rs0 + rs1) + (rs2 + rs3);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
@@ -293,20 +311,37 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       ok = mbar_wait(&o_done[jl & 1], (jl >> 1) & 1, abort_flag, args.status);
       tc_fence_after();
     }
+    // Merge the halves.  Once the last PV is done no MMA reads P, so P buffer 0 holds the exchange
+    // of (m_h, l_h).  Every softmax warp reaches the barrier (all waits above are bounded).
+    float* xch = reinterpret_cast<float*>(sP);   // [2 halves][m | l][128 rows]
+    xch[half * 256 + r] = m;
+    xch[half * 256 + 128 + r] = l;
+    asm volatile("bar.sync 1, %0;" ::"n"(SOFTMAX_THREADS) : "memory");
     if (ok) {
-      const float inv = 1.f / l;
-      __nv_bfloat16* orow = O + (size_t)row * (args.n_heads * HD) + head * HD;
+      const float m0 = xch[r], l0 = xch[128 + r], m1 = xch[256 + r], l1 = xch[384 + r];
+      const float mm = fmaxf(m0, m1);
+      const float a0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - mm);
+      const float a1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - mm);
+      const float inv = 1.f / (a0 * l0 + a1 * l1);
+      const float w0 = a0 * inv, w1 = a1 * inv;
+      // this warp writes output columns [half * HD / 2, half * HD / 2 + HD / 2)
+      __nv_bfloat16* orow = O + (size_t)row * (args.n_heads * HD) + head * HD + half * (HD / 2);
 #pragma unroll
-      for (int c = 0; c < HD; c += 32) {
-        uint32_t ov[32];
-        tmem_ld32_sync(t_o + lane_off + c, ov);
+      for (int c = 0; c < HD / 2; c += 32) {
+        uint32_t o0[32], o1[32];
+        tmem_ld32(t_o + lane_off + half * (HD / 2) + c, o0);
+        tmem_ld32(t_o + HD + lane_off + half * (HD / 2) + c, o1);
+        tmem_ld_wait_regs(o0);
+        tmem_ld_wait_regs(o1);
         if (row < de) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 8)
-            st_global_v4(orow + c + i, pack_bf16x2(__uint_as_float(ov[i]) * inv, __uint_as_float(ov[i + 1]) * inv),
-                         pack_bf16x2(__uint_as_float(ov[i + 2]) * inv, __uint_as_float(ov[i + 3]) * inv),
-                         pack_bf16x2(__uint_as_float(ov[i + 4]) * inv, __uint_as_float(ov[i + 5]) * inv),
-                         pack_bf16x2(__uint_as_float(ov[i + 6]) * inv, __uint_as_float(ov[i + 7]) * inv));
+          for (int i = 0; i < 32; i += 8) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = __uint_as_float(o0[i + u]) * w0 + __uint_as_float(o1[i + u]) * w1;
+            st_global_v4(orow + c + i, pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                         pack_bf16x2(v[6], v[7]));
+          }
         }
       }
     }
