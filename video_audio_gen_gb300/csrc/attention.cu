@@ -8,14 +8,20 @@
 // at multiples of 128 in the packed sequence (so the TMA x coordinate of the transposed V is
 // 16-byte aligned); columns outside the document are masked to -inf.
 //   warp 0     TMA producer: Q once, then K and V^T tiles through two 2-stage rings
-//   warp 1     TMEM allocator + UMMA issuer: S(j) = Q K(j)^T into TMEM; P(j) V(j) into TMEM, its
-//              first 64 key columns accumulated into O_0 and the last 64 into O_1
+//   warp 1     TMEM allocator + S issuer: S(j) = Q K(j)^T into TMEM buffer j % 2, issued as soon as
+//              the softmax has loaded S(j - 2) from that buffer
+//   warp 10    PV issuer: O_h += P(j) V(j) once P(j) is in shared memory; key columns [0, 64)
+//              accumulate into O_0, [64, 128) into O_1
 //   warps 2-9  softmax, two warps per query row: warp half h owns key columns [64h, 64h + 64) of
 //              every tile and keeps its own running max m_h, sum l_h and accumulator O_h, exactly as
 //              two independent passes over disjoint key subsets would; the halves exchange nothing
 //              per tile and are merged once at the end:
 //                  o = (2^(m_0-m) O_0 + 2^(m_1-m) O_1) / (2^(m_0-m) l_0 + 2^(m_1-m) l_1),  m = max(m_0, m_1)
-// TMEM: S double buffer (2 x 128 columns) + O_0, O_1 (2 x HD columns) <= 512.
+// Two issuing threads, because one thread's tcgen05.mma issue runs nearly in step with the tensor
+// pipe: whatever else that thread waits on leaves the pipe idle.  With S and PV on separate
+// threads, S(j + 2) runs while the softmax works on tile j, and PV(j) while it works on j + 1.
+// TMEM: S double buffer (2 x 128 columns) + O_0, O_1 (2 x HD columns) <= 512.  P(j) (bf16) goes to
+// shared memory buffer j % 2 in the swizzled K-major layout the PV MMA reads.
 #include "common.cuh"
 #include "kernels.h"
 #include "tmap.h"
@@ -28,8 +34,9 @@ constexpr int TQ = 128, TK = 128;
 constexpr int ATOM = 128 * 64 * 2;         // 128 rows x 64 bf16 columns, 128-byte swizzled (16 KB)
 constexpr int P_BYTES = 2 * ATOM;          // P tile: 128 q rows x 128 kv columns
 constexpr int KV_STAGES = 2;
-constexpr int ATT_THREADS = 320;
+constexpr int ATT_THREADS = 352;           // producer, S issuer, 8 softmax warps, PV issuer
 constexpr int SOFTMAX_THREADS = 256;
+constexpr int PV_WARP = 10;
 
 // Shared-memory plan for head dim HD (64 or 128):
 //   Q  [128 q, HD]   HD/64 atoms of 16 KB          K  [128 kv, HD]  HD/64 atoms of 16 KB
@@ -79,30 +86,36 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   uint8_t* sP = sV + KV_STAGES * Plan::V_BYTES;        // [2]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * P_BYTES);
   uint64_t* q_full = bars;
-  uint64_t* k_full = bars + 1;                         // [2]  K tile landed
-  uint64_t* k_empty = bars + 3;                        // [2]  S MMA done with the K tile
-  uint64_t* v_full = bars + 5;                         // [2]  V^T tile landed
-  uint64_t* v_empty = bars + 7;                        // [2]  PV MMA done with the V^T tile
-  uint64_t* s_full = bars + 9;                         // [2]
-  uint64_t* p_full = bars + 11;                        // [2]
-  uint64_t* o_done = bars + 13;                        // [2]
-  uint64_t* mma_done = bars + 15;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  uint64_t* k_full = bars + 1;                         // [stage]  K tile landed
+  uint64_t* k_empty = k_full + KV_STAGES;              // [stage]  S MMA done with the K tile
+  uint64_t* v_full = k_empty + KV_STAGES;              // [stage]  V^T tile landed
+  uint64_t* v_empty = v_full + KV_STAGES;              // [stage]  PV MMA done with the V^T tile
+  uint64_t* s_full = v_empty + KV_STAGES;              // [2]  S(j) in TMEM buffer j % 2
+  uint64_t* s_free = s_full + 2;                       // [2]  softmax has loaded S(j) from its buffer
+  uint64_t* p_full = s_free + 2;                       // [2]  P(j) in shared memory buffer j % 2
+  uint64_t* o_done = p_full + 2;                       // [2]  O += P(j) V(j) complete
+  uint64_t* s_drain = o_done + 2;                      // every S MMA complete
+  uint64_t* o_drain = s_drain + 1;                     // every PV MMA complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < KV_STAGES; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(&s_full[s], 1);
+      mbar_init(&s_free[s], SOFTMAX_THREADS / 32);
       mbar_init(&p_full[s], SOFTMAX_THREADS / 32);
       mbar_init(&o_done[s], 1);
     }
-    mbar_init(mma_done, 1);
+    mbar_init(s_drain, 1);
+    mbar_init(o_drain, 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -120,10 +133,11 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       mbar_arrive_expect_tx(q_full, Plan::Q_BYTES);
 #pragma unroll
       for (int a = 0; a < HD / 64; ++a) tma_load_2d(sQ + a * ATOM, &tmQ, q_full, hx + 64 * a, q0);
-      // K tiles run two ahead of the V tiles: K(j) only waits for S(j-2), V(j) for P(j-2) V(j-2).
+      // K tiles run two ahead of the V tiles: K(j) waits for S(j - KV_STAGES), V(j) for
+      // P(j - KV_STAGES) V(j - KV_STAGES).
       auto load_k = [&](int j) -> bool {
-        const int st = j & 1;
-        if (!mbar_wait(&k_empty[st], ((j >> 1) & 1) ^ 1, abort_flag, args.status)) return false;
+        const int st = j % KV_STAGES;
+        if (!mbar_wait(&k_empty[st], ((j / KV_STAGES) & 1) ^ 1, abort_flag, args.status)) return false;
         const int kv0 = kv_base + j * TK;
         mbar_arrive_expect_tx(&k_full[st], Plan::K_BYTES);
 #pragma unroll
@@ -132,8 +146,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         return true;
       };
       auto load_v = [&](int j) -> bool {
-        const int st = j & 1;
-        if (!mbar_wait(&v_empty[st], ((j >> 1) & 1) ^ 1, abort_flag, args.status)) return false;
+        const int st = j % KV_STAGES;
+        if (!mbar_wait(&v_empty[st], ((j / KV_STAGES) & 1) ^ 1, abort_flag, args.status)) return false;
         const int kv0 = kv_base + j * TK;
         mbar_arrive_expect_tx(&v_full[st], Plan::V_BYTES);
         tma_load_2d(sV + st * Plan::V_BYTES, &tmV, &v_full[st], kv0, hx);
@@ -154,41 +168,44 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       }
       // Every copy this CTA issued must land before the CTA may exit.
       wait_noabort(q_full, 0);
-      for (int j = nk - 2 < 0 ? 0 : nk - 2; j < nk; ++j) wait_noabort(&k_full[j & 1], (j >> 1) & 1);
-      for (int j = nv - 2 < 0 ? 0 : nv - 2; j < nv; ++j) wait_noabort(&v_full[j & 1], (j >> 1) & 1);
+      for (int j = nk - KV_STAGES < 0 ? 0 : nk - KV_STAGES; j < nk; ++j)
+        wait_noabort(&k_full[j % KV_STAGES], (j / KV_STAGES) & 1);
+      for (int j = nv - KV_STAGES < 0 ? 0 : nv - KV_STAGES; j < nv; ++j)
+        wait_noabort(&v_full[j % KV_STAGES], (j / KV_STAGES) & 1);
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // MMA issue order: S(0), S(1), then for each j: [P(j) ready] O += P(j) V(j), S(j+2).
-      // S(j+2) reuses S buffer j%2, which the softmax released when it published P(j); the commit
-      // after S(j) also covers every earlier MMA (tcgen05 ops of one thread complete in order), so
-      // when the softmax sees S(j) it knows O += P(j-2) V(j-2) is done and P buffer j%2 is free.
+      // S(j) into buffer j % 2 once K(j) has landed and the softmax has loaded S(j - 2) from it.
       bool ok = mbar_wait(q_full, 0, abort_flag, args.status);
       tc_fence_after();
       const uint32_t q_addr = smem_u32(sQ);
-      auto issue_s = [&](int j) -> bool {
-        const int st = j & 1;
-        if (!mbar_wait(&k_full[st], (j >> 1) & 1, abort_flag, args.status)) return false;
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int st = j % KV_STAGES, sb = j & 1;
+        if (j >= 2 && !mbar_wait(&s_free[sb], ((j - 2) >> 1) & 1, abort_flag, args.status)) break;
+        if (!mbar_wait(&k_full[st], (j / KV_STAGES) & 1, abort_flag, args.status)) break;
         tc_fence_after();
         const uint32_t k_addr = smem_u32(sK + st * Plan::K_BYTES);
 #pragma unroll
         for (int ks = 0; ks < HD / 16; ++ks) {
           const uint32_t off = (ks >> 2) * ATOM + (ks & 3) * 32;
-          umma_bf16(t_s + st * TK, sdesc_sw128(q_addr + off), sdesc_sw128(k_addr + off), Plan::IDESC_S, ks != 0);
+          umma_bf16(t_s + sb * TK, sdesc_sw128(q_addr + off), sdesc_sw128(k_addr + off), Plan::IDESC_S, ks != 0);
         }
-        umma_commit(&s_full[st]);
+        umma_commit(&s_full[sb]);
         umma_commit(&k_empty[st]);
-        return true;
-      };
-      if (ok) ok = issue_s(0);
-      if (ok && n_kv > 1) ok = issue_s(1);
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int pb = j & 1;
+      }
+      // No MMA may still read shared memory or write TMEM when the CTA tears down.
+      umma_commit(s_drain);
+      wait_noabort(s_drain, 0);
+    }
+  } else if (warp == PV_WARP) {
+    if (lane == 0) {
+      for (int j = 0; j < n_kv; ++j) {
+        const int pb = j & 1, st = j % KV_STAGES;
         if (!mbar_wait(&p_full[pb], (j >> 1) & 1, abort_flag, args.status)) break;
-        if (!mbar_wait(&v_full[pb], (j >> 1) & 1, abort_flag, args.status)) break;
+        if (!mbar_wait(&v_full[st], (j / KV_STAGES) & 1, abort_flag, args.status)) break;
         tc_fence_after();
         const uint32_t p_addr = smem_u32(sP + pb * P_BYTES);
-        const uint32_t v_addr = smem_u32(sV + (j & 1) * Plan::V_BYTES);
+        const uint32_t v_addr = smem_u32(sV + st * Plan::V_BYTES);
 #pragma unroll
         for (int ks = 0; ks < TK / 16; ++ks) {
           // key columns [0, 64) (P atom 0, V^T atom 0) -> O_0; [64, 128) (atom 1) -> O_1
@@ -198,12 +215,10 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                     (j | (ks & 3)) != 0);
         }
         umma_commit(&o_done[pb]);
-        umma_commit(&v_empty[pb]);
-        if (j + 2 < n_kv && !issue_s(j + 2)) break;
+        umma_commit(&v_empty[st]);
       }
-      // No MMA may still read shared memory or write TMEM when the CTA tears down.
-      umma_commit(mma_done);
-      wait_noabort(mma_done, 0);
+      umma_commit(o_drain);
+      wait_noabort(o_drain, 0);
     }
   } else {
     // ---------------- softmax warps ----------------
@@ -240,6 +255,10 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       for (int c = 0; c < HC; c += 32) tmem_ld32(ts + c, *reinterpret_cast<uint32_t(*)[32]>(&sv[c]));
 #pragma unroll
       for (int c = 0; c < HC; c += 32) tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&sv[c]));
+      // the scores are in registers: the S issuer may overwrite this buffer with S(j + 2)
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[sb]);
       if (!interior) {
 #pragma unroll
         for (int i = 0; i < HC; ++i)
@@ -283,9 +302,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       // A half that has seen no key of the document yet has m = -inf and only masked scores:
       // p = exp2(-inf - 0) = 0 keeps O_h and l_h at zero.
       const float mu = m == -INFINITY ? 0.f : m;
-      // p = exp2(s * scale - m) -> bf16 into shared memory (swizzled K-major A operand of P V):
-      // this half's 64 columns are exactly P atom `half`, one 128-byte swizzled row per query row
-      const uint32_t p_row = smem_u32(sP + sb * P_BYTES + half * ATOM) + r * 128;
+      // p = exp2(s * scale - m) -> bf16 pairs; this half's 64 columns are exactly P atom `half` of
+      // shared-memory buffer j % 2, one 128-byte swizzled row per query row
+      uint32_t pk[HC / 2];
       float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
 #pragma unroll
       for (int c = 0; c < HC; c += 8) {
@@ -296,11 +315,21 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         rs1 += p[2] + p[3];
         rs2 += p[4] + p[5];
         rs3 += p[6] + p[7];
-        const int chunk = c >> 3;
-        st_shared_v4(p_row + ((chunk ^ (r & 7)) << 4), pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]),
-                     pack_bf16x2(p[4], p[5]), pack_bf16x2(p[6], p[7]));
+        pk[c / 2] = pack_bf16x2(p[0], p[1]);
+        pk[c / 2 + 1] = pack_bf16x2(p[2], p[3]);
+        pk[c / 2 + 2] = pack_bf16x2(p[4], p[5]);
+        pk[c / 2 + 3] = pack_bf16x2(p[6], p[7]);
       }
       l += (rs0 + rs1) + (rs2 + rs3);
+      // P buffer j % 2 is free once O += P(j - 2) V(j - 2) has completed
+      if (j >= 2 && !mbar_wait(&o_done[sb], ((j - 2) >> 1) & 1, abort_flag, args.status)) {
+        ok = false;
+        break;
+      }
+      const uint32_t p_row = smem_u32(sP + sb * P_BYTES + half * ATOM) + r * 128;
+#pragma unroll
+      for (int c = 0; c < HC / 8; ++c)
+        st_shared_v4(p_row + ((c ^ (r & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
@@ -311,9 +340,10 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       ok = mbar_wait(&o_done[jl & 1], (jl >> 1) & 1, abort_flag, args.status);
       tc_fence_after();
     }
-    // Merge the halves.  Once the last PV is done no MMA reads P, so P buffer 0 holds the exchange
-    // of (m_h, l_h).  Every softmax warp reaches the barrier (all waits above are bounded).
-    float* xch = reinterpret_cast<float*>(sP);   // [2 halves][m | l][128 rows]
+    // Merge the halves.  Once the last PV is done no MMA reads shared memory and every K tile has
+    // landed, so K stage 0 holds the exchange of (m_h, l_h).  Every softmax warp reaches the barrier
+    // (all waits above are bounded).
+    float* xch = reinterpret_cast<float*>(sK);   // [2 halves][m | l][128 rows]
     xch[half * 256 + r] = m;
     xch[half * 256 + 128 + r] = l;
     asm volatile("bar.sync 1, %0;" ::"n"(SOFTMAX_THREADS) : "memory");
