@@ -305,22 +305,20 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       // p = exp2(s * scale - m) -> bf16 pairs; this half's 64 columns are exactly P atom `half` of
       // shared-memory buffer j % 2, one 128-byte swizzled row per query row
       uint32_t pk[HC / 2];
-      float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
+      // paired fp32 arithmetic (one f32x2 FMA / add per two scores); four partial row sums
+      const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-mu, -mu);
+      float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
       for (int c = 0; c < HC; c += 8) {
-        float p[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) p[i] = fast_exp2(fmaf(__uint_as_float(sv[c + i]), sc, -mu));
-        rs0 += p[0] + p[1];
-        rs1 += p[2] + p[3];
-        rs2 += p[4] + p[5];
-        rs3 += p[6] + p[7];
-        pk[c / 2] = pack_bf16x2(p[0], p[1]);
-        pk[c / 2 + 1] = pack_bf16x2(p[2], p[3]);
-        pk[c / 2 + 2] = pack_bf16x2(p[4], p[5]);
-        pk[c / 2 + 3] = pack_bf16x2(p[6], p[7]);
+        for (int u = 0; u < 4; ++u) {
+          const float2 x = ffma2(make_float2(__uint_as_float(sv[c + 2 * u]), __uint_as_float(sv[c + 2 * u + 1])), sc2, nm2);
+          const float2 e = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+          rs[u] = fadd2(rs[u], e);
+          pk[c / 2 + u] = pack_bf16x2(e.x, e.y);
+        }
       }
-      l += (rs0 + rs1) + (rs2 + rs3);
+      l += (rs[0].x + rs[0].y + rs[1].x + rs[1].y) + (rs[2].x + rs[2].y + rs[3].x + rs[3].y);
       // P buffer j % 2 is free once O += P(j - 2) V(j - 2) has completed
       if (j >= 2 && !mbar_wait(&o_done[sb], ((j - 2) >> 1) & 1, abort_flag, args.status)) {
         ok = false;
