@@ -10,8 +10,8 @@
 //   warp 0     TMA producer: Q once, then K and V^T tiles through two 2-stage rings
 //   warp 1     TMEM allocator + S issuer: S(j) = Q K(j)^T into TMEM buffer j % 2, issued as soon as
 //              the softmax has loaded S(j - 2) from that buffer
-//   warp 10    PV issuer: O_h += P(j) V(j) once P(j) is in shared memory; key columns [0, 64)
-//              accumulate into O_0, [64, 128) into O_1
+//   warp 10    PV issuer: O_h += P(j) V(j) once P(j) is in shared memory and V(j) has landed (one
+//              barrier counts both); key columns [0, 64) accumulate into O_0, [64, 128) into O_1
 //   warps 2-9  softmax, two warps per query row: warp half h owns key columns [64h, 64h + 64) of
 //              every tile and keeps its own running max m_h, sum l_h and accumulator O_h, exactly as
 //              two independent passes over disjoint key subsets would; the halves exchange nothing
@@ -20,6 +20,8 @@
 // Two issuing threads, because one thread's tcgen05.mma issue runs nearly in step with the tensor
 // pipe: whatever else that thread waits on leaves the pipe idle.  With S and PV on separate
 // threads, S(j + 2) runs while the softmax works on tile j, and PV(j) while it works on j + 1.
+// The softmax waits on one barrier per tile: "S(j) ready" completes only when S(j) is in TMEM and
+// O += P(j - 2) V(j - 2) is done, so it also says that P buffer j % 2 is free.
 // TMEM: S double buffer (2 x 128 columns) + O_0, O_1 (2 x HD columns) <= 512.  P(j) (bf16) goes to
 // shared memory buffer j % 2 in the swizzled K-major layout the PV MMA reads.
 #include "common.cuh"
@@ -37,6 +39,7 @@ constexpr int KV_STAGES = 2;
 constexpr int ATT_THREADS = 352;           // producer, S issuer, 8 softmax warps, PV issuer
 constexpr int SOFTMAX_THREADS = 256;
 constexpr int PV_WARP = 10;
+static_assert(KV_STAGES == 2, "V(j) lands on the barrier of P buffer j % 2");
 
 // Shared-memory plan for head dim HD (64 or 128):
 //   Q  [128 q, HD]   HD/64 atoms of 16 KB          K  [128 kv, HD]  HD/64 atoms of 16 KB
@@ -88,11 +91,10 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   uint64_t* q_full = bars;
   uint64_t* k_full = bars + 1;                         // [stage]  K tile landed
   uint64_t* k_empty = k_full + KV_STAGES;              // [stage]  S MMA done with the K tile
-  uint64_t* v_full = k_empty + KV_STAGES;              // [stage]  V^T tile landed
-  uint64_t* v_empty = v_full + KV_STAGES;              // [stage]  PV MMA done with the V^T tile
-  uint64_t* s_full = v_empty + KV_STAGES;              // [2]  S(j) in TMEM buffer j % 2
+  uint64_t* v_empty = k_empty + KV_STAGES;             // [stage]  PV MMA done with the V^T tile
+  uint64_t* s_full = v_empty + KV_STAGES;              // [2]  S(j) in TMEM and P(j - 2) V(j - 2) done
   uint64_t* s_free = s_full + 2;                       // [2]  softmax has loaded S(j) from its buffer
-  uint64_t* p_full = s_free + 2;                       // [2]  P(j) in shared memory buffer j % 2
+  uint64_t* p_full = s_free + 2;                       // [2]  P(j) in shared memory and V(j) landed
   uint64_t* o_done = p_full + 2;                       // [2]  O += P(j) V(j) complete
   uint64_t* s_drain = o_done + 2;                      // every S MMA complete
   uint64_t* o_drain = s_drain + 1;                     // every PV MMA complete
@@ -105,13 +107,12 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     for (int s = 0; s < KV_STAGES; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
-      mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&s_full[s], 1);
+      mbar_init(&s_full[s], 2);                          // S commit + PV commit of tile j - 2
       mbar_init(&s_free[s], SOFTMAX_THREADS / 32);
-      mbar_init(&p_full[s], SOFTMAX_THREADS / 32);
+      mbar_init(&p_full[s], SOFTMAX_THREADS / 32 + 1);   // softmax warps + the V^T load
       mbar_init(&o_done[s], 1);
     }
     mbar_init(s_drain, 1);
@@ -149,9 +150,10 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         const int st = j % KV_STAGES;
         if (!mbar_wait(&v_empty[st], ((j / KV_STAGES) & 1) ^ 1, abort_flag, args.status)) return false;
         const int kv0 = kv_base + j * TK;
-        mbar_arrive_expect_tx(&v_full[st], Plan::V_BYTES);
-        tma_load_2d(sV + st * Plan::V_BYTES, &tmV, &v_full[st], kv0, hx);
-        tma_load_2d(sV + st * Plan::V_BYTES + Plan::V_ATOM, &tmV, &v_full[st], kv0 + 64, hx);
+        // V(j) completes on the barrier that also counts the softmax warps' P(j) (stage = j % 2)
+        mbar_arrive_expect_tx(&p_full[st], Plan::V_BYTES);
+        tma_load_2d(sV + st * Plan::V_BYTES, &tmV, &p_full[st], kv0, hx);
+        tma_load_2d(sV + st * Plan::V_BYTES + Plan::V_ATOM, &tmV, &p_full[st], kv0 + 64, hx);
         return true;
       };
       int nk = 0, nv = 0;
@@ -171,7 +173,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       for (int j = nk - KV_STAGES < 0 ? 0 : nk - KV_STAGES; j < nk; ++j)
         wait_noabort(&k_full[j % KV_STAGES], (j / KV_STAGES) & 1);
       for (int j = nv - KV_STAGES < 0 ? 0 : nv - KV_STAGES; j < nv; ++j)
-        wait_noabort(&v_full[j % KV_STAGES], (j / KV_STAGES) & 1);
+        wait_noabort(&p_full[j % KV_STAGES], (j / KV_STAGES) & 1);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -199,10 +201,12 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     }
   } else if (warp == PV_WARP) {
     if (lane == 0) {
+      // tiles 0 and 1 have no PV two tiles back: their "S ready" phases get that arrival now
+      mbar_arrive(&s_full[0]);
+      mbar_arrive(&s_full[1]);
       for (int j = 0; j < n_kv; ++j) {
         const int pb = j & 1, st = j % KV_STAGES;
         if (!mbar_wait(&p_full[pb], (j >> 1) & 1, abort_flag, args.status)) break;
-        if (!mbar_wait(&v_full[st], (j / KV_STAGES) & 1, abort_flag, args.status)) break;
         tc_fence_after();
         const uint32_t p_addr = smem_u32(sP + pb * P_BYTES);
         const uint32_t v_addr = smem_u32(sV + st * Plan::V_BYTES);
@@ -216,6 +220,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         }
         umma_commit(&o_done[pb]);
         umma_commit(&v_empty[st]);
+        umma_commit(&s_full[pb]);                          // the second arrival of "S(j + 2) ready"
       }
       umma_commit(o_drain);
       wait_noabort(o_drain, 0);
@@ -319,11 +324,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         }
       }
       l += (rs[0].x + rs[0].y + rs[1].x + rs[1].y) + (rs[2].x + rs[2].y + rs[3].x + rs[3].y);
-      // P buffer j % 2 is free once O += P(j - 2) V(j - 2) has completed
-      if (j >= 2 && !mbar_wait(&o_done[sb], ((j - 2) >> 1) & 1, abort_flag, args.status)) {
-        ok = false;
-        break;
-      }
+      // P buffer j % 2 is free: "S(j) ready" included O += P(j - 2) V(j - 2) being done
       const uint32_t p_row = smem_u32(sP + sb * P_BYTES + half * ATOM) + r * 128;
 #pragma unroll
       for (int c = 0; c < HC / 8; ++c)
