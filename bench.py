@@ -30,13 +30,14 @@ import numpy as np  # noqa: E402
 
 METRIC = "DiT forward tokens/s & ms/forward on 1 GB300; % of bf16 tensor-pipe peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+SAMPLE_SECONDS = 10.0   # target CPU work of the oracle baseline sample
 KINDS = ["gemm_qkv", "attention", "gemm_out", "gemm_ffn_up", "gemm_ffn_down", "norm_modulate", "other"]
 
 # DRAM traffic per launch from ncu captures (dram__bytes_read.sum + dram__bytes_write.sum), keyed by
 # kernel kind and workload, with the sha256 of the kernel source the capture was taken on; the
 # figure is reported only while the source is unchanged.  See profiles/.
 TRAFFIC = {
-    ("attention", "video_audio_bf16"): {"bytes": 409653248, "src_sha": "f6c8628799f523b9",
+    ("attention", "video_audio_bf16"): {"bytes": 410346240, "src_sha": "cd92e0423d13c9de",
                                         "profile": "profiles/attention_video_audio_bf16.md"},
     ("gemm_qkv", "video_audio_bf16"): {"bytes": 793978592, "src_sha": "41de12cade82e5ed",
                                        "profile": "profiles/gemm_video_audio_bf16.md"},
@@ -169,7 +170,14 @@ class ClockSampler:
 # CPU baseline: the oracle on a bounded sample of the workload
 # ------------------------------------------------------------------------------------------------
 
-def oracle_sample(w: dict, lay: dict, budget_rows: int | None = None):
+def sample_rows(w: dict, lay: dict, seconds: float) -> int:
+    """Rows of the oracle sample that take about `seconds` of CPU work (calibrated on a few rows)."""
+    threads = len(os.sched_getaffinity(0))
+    _, dt0, r0, _ = oracle_sample(w, lay, budget_rows=2 * threads)
+    return int(min(4096, max(r0, r0 * seconds / max(dt0, 1e-3))))
+
+
+def oracle_sample(w: dict, lay: dict, budget_rows: int | None = None, seconds: float = SAMPLE_SECONDS):
     """Time the oracle computing one block for a sample of R query rows of the workload: norm and
     modulate, the QKV projection and RoPE of those rows, attention of those rows over the full
     document (keys/values of the document are seeded inputs), the output projection with gated
@@ -182,21 +190,30 @@ def oracle_sample(w: dict, lay: dict, budget_rows: int | None = None):
     threads = len(os.sched_getaffinity(0))
     oracle.set_threads(threads)
     if not m["adaln"]:
-        # small token counts (the music DiT): one whole block over every token, scaled by L
+        # small token counts (the music DiT): whole blocks over every token, repeated until about
+        # `seconds` of CPU work, scaled by L
         sub = dict(m, n_blocks=1)
         W = synth.make_weights(dict(w, model=sub))
         x = synth.normal(w["seed"], "sample.x", (lay["n_tokens"], d), 1.0)
         cs, sn = oracle.rope_cos_sin(sub, lay["pos"])
+        reps, dt = 0, 0.0
         t0 = time.perf_counter()
-        oracle.block_forward(sub, W, 0, None, x, lay, cs, sn)
-        dt = time.perf_counter() - t0
+        while reps == 0 or dt < seconds:
+            oracle.block_forward(sub, W, 0, None, x, lay, cs, sn)
+            reps += 1
+            dt = time.perf_counter() - t0
         oracle.set_threads(1)
-        return lay["n_tokens"] / (dt * m["n_blocks"]), dt, lay["n_tokens"], threads
-    R = budget_rows or 2 * threads
+        return lay["n_tokens"] * reps / (dt * m["n_blocks"]), dt, lay["n_tokens"] * reps, threads
+    if budget_rows is None:
+        R = sample_rows(w, lay, seconds)
+        oracle.set_threads(threads)
+    else:
+        R = budget_rows
     cu = lay["cu_seqlens"]
     # the sample's rows: spread over the longest document
     j = int(np.argmax(np.diff(cu)))
     a, b = int(cu[j]), int(cu[j + 1])
+    R = min(R, b - a)
     rows = np.linspace(a, b - 1, R).astype(np.int64)
     seed = w["seed"]
     x = synth.normal(seed, "sample.x", (R, d), 1.0)
@@ -364,6 +381,22 @@ def run_gpu(args, w, dist, rank, world):
                 launches=launches, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, flops=fl["total"], docs=D, lay=lay)
 
 
+L2_BYTES = 129 * 1024 * 1024
+
+
+def l2_note(m: dict, lay: dict) -> str:
+    """How the timed steps relate to the 129 MB L2: the bytes one forward streams (weights once,
+    the fp32 residual and the bf16 activations of every block) against the cache size."""
+    d, F, L, N = m["hidden"], m["ffn_hidden"], m["n_blocks"], lay["n_tokens"]
+    wb = 4 if m["dtype"] == "fp32" else 2
+    weights = L * (4 * d * d + 3 * d * F) * wb
+    acts = L * N * (4 * d * 4 + 2 * F * 2)
+    total = weights + acts
+    if total > L2_BYTES:
+        return f"inputs larger than L2: about {total / 1e9:.2f} GB of weights and activations stream each step"
+    return f"working set about {total / 1e6:.0f} MB, within L2 (no flush): a parity-size case, not a bench workload"
+
+
 def workload_config(name, w, lay, extra=None):
     m = w["model"]
     docs = ", ".join(f"{synth_doc(d)}" for d in w["docs"])
@@ -374,7 +407,7 @@ def workload_config(name, w, lay, extra=None):
                      f"{lay['n_tokens']} packed tokens in {lay['n_docs']} documents ({docs})",
          "tokens": int(lay["n_tokens"]), "documents": int(lay["n_docs"]),
          "cu_seqlens": [int(v) for v in lay["cu_seqlens"]],
-         "l2": "inputs larger than L2 (the weights, several GB, and the activations stream every step)"}
+         "l2": l2_note(m, lay)}
     if extra:
         c.update(extra)
     return c
@@ -413,8 +446,11 @@ def main():
             return
         lay = synth.build_layout(w["docs"])
         vals, secs = [], []
+        # each step a bounded sample: the whole run stays within a couple of minutes
+        per_step = max(1.0, min(SAMPLE_SECONDS, 120.0 / max(1, args.steps)))
+        rows = sample_rows(w, lay, per_step) if w["model"]["adaln"] else None
         for _ in range(args.steps):
-            tps, dt, R, threads = oracle_sample(w, lay)
+            tps, dt, R, threads = oracle_sample(w, lay, budget_rows=rows, seconds=per_step)
             vals.append(tps)
             secs.append(dt)
         tps = statistics.median(vals)
@@ -422,7 +458,7 @@ def main():
         sample = (f"{R} query rows x 1 block of the workload per step ({args.steps} steps, median), "
                   f"scaled by N={lay['n_tokens']} rows x L={w['model']['n_blocks']} blocks")
         if not w["model"]["adaln"]:
-            sample = (f"1 whole block over all {R} tokens per step ({args.steps} steps, median), "
+            sample = (f"whole blocks over {R} tokens per step ({args.steps} steps, median), "
                       f"scaled by L={w['model']['n_blocks']} blocks")
         line = {"impl": "reference", "metric": metric, "value": round(tps, 4), "unit": "tokens/s",
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 1),
@@ -467,7 +503,7 @@ def main():
                 "gpu_launches": int(r["launches"]), "clocks": r["clocks"]}
         if not args.no_cpu_baseline:
             tps, dt, R, threads = oracle_sample(w, r["lay"])
-            what = (f"1 whole block over all {R} tokens" if not w["model"]["adaln"] else f"{R} query rows x 1 block")
+            what = (f"whole blocks over {R} tokens in all" if not w["model"]["adaln"] else f"{R} query rows x 1 block")
             line["cpu_baseline"] = {"value": round(tps, 4), "unit": "tokens/s", "cores": threads, "kind": "oracle",
                                     "sample": f"{what} ({dt:.1f} s on {threads} threads), "
                                               f"scaled by N={r['tokens']} rows x L={w['model']['n_blocks']} blocks"}
