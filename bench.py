@@ -98,6 +98,15 @@ def fp32_alu_peak_tflops(peaks: dict, n_sms: int) -> float:
     return n_sms * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
 
 
+TF32_PER_BF16 = 1.1 / 2.25   # nominal dense tf32 / bf16 tensor rates
+
+
+def fp32_3xtf32_peak_tflops(peaks: dict) -> float:
+    """fp32-equivalent peak of the 3xTF32 GEMM: the tf32 rate (measured sustained bf16 figure x the
+    nominal tf32/bf16 ratio) over the three tf32 products it spends per fp32 product."""
+    return peaks["bf16_tflops_sustained"] * TF32_PER_BF16 / 3.0
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -316,6 +325,7 @@ def run_gpu(args, w, dist, rank, world):
     fl = step_flops(m, lay["cu_seqlens"])
     peaks, peak_src = load_peaks()
     alu_peak = fp32_alu_peak_tflops(peaks, torch.cuda.get_device_properties(dev).multi_processor_count)
+    tf32x3_peak = fp32_3xtf32_peak_tflops(peaks)
     kernels = {}
     for k in KINDS:
         ms, n = kt[k]
@@ -325,8 +335,10 @@ def run_gpu(args, w, dist, rank, world):
         entry = {"launches": n, "avg_ms": round(avg, 4), "share": None}
         if k in fl["per_launch"]:
             tf = fl["per_launch"][k] / (avg * 1e-3) / 1e12
-            if m["dtype"] == "fp32":
+            if m["dtype"] == "fp32" and k == "attention":
                 entry.update(bound="alu", achieved_tflops=round(tf, 1), frac=round(tf / alu_peak, 3))
+            elif m["dtype"] == "fp32":
+                entry.update(bound="tensor", achieved_tflops=round(tf, 1), frac=round(tf / tf32x3_peak, 3))
             else:
                 entry.update(bound="tensor", achieved_tflops=round(tf, 1),
                              frac=round(tf / peaks["bf16_tflops_sustained"], 3))
@@ -345,11 +357,16 @@ def run_gpu(args, w, dist, rank, world):
     src = "attention.cu" if top == "attention" else "gemm.cu"
     tr = TRAFFIC.get((top, args.workload))
     traffic = tr["bytes"] if tr and tr["src_sha"] == source_hash(src) else None
-    if m["dtype"] == "fp32":
+    if m["dtype"] == "fp32" and top == "attention":
         roofline = {"bound": "alu", "kernel": top, "achieved": kernels[top]["achieved_tflops"],
                     "peak": round(alu_peak, 1), "unit": "TFLOP/s", "frac": kernels[top]["frac"], "traffic": traffic,
-                    "peak_source": "derived: SMs x 128 FP32 lanes x 2 FLOP x sm_max_mhz (FFMA; TF32 would not meet "
-                                   "the 1e-5 tolerance)",
+                    "peak_source": "derived: SMs x 128 FP32 lanes x 2 FLOP x sm_max_mhz (FFMA)",
+                    "algorithmic_flops_per_launch": fl["per_launch"][top]}
+    elif m["dtype"] == "fp32":
+        roofline = {"bound": "tensor", "kernel": top, "achieved": kernels[top]["achieved_tflops"],
+                    "peak": round(tf32x3_peak, 1), "unit": "TFLOP/s", "frac": kernels[top]["frac"], "traffic": traffic,
+                    "peak_source": f"3xTF32: bf16_tflops_sustained of {peak_src} x nominal tf32/bf16 (1.1/2.25) / 3 "
+                                   "tf32 products per fp32 product",
                     "algorithmic_flops_per_launch": fl["per_launch"][top]}
     else:
         roofline = {"bound": "tensor", "kernel": top, "achieved": kernels[top]["achieved_tflops"],

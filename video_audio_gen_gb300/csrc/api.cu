@@ -24,7 +24,14 @@ constexpr size_t kAlign = 256;
 
 inline size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 
+// An fp32 weight as the 3xTF32 GEMM reads it: tf32(w) and tf32(w - tf32(w)), library-owned.
+struct SplitW {
+  float* hi = nullptr;
+  float* lo = nullptr;
+};
+
 struct BlockDev {
+  SplitW s_qkv, s_o, s_in, s_down;  // fp32 path
   const void* w_qkv = nullptr;
   const void* w_o = nullptr;
   const void* w_down = nullptr;
@@ -42,7 +49,8 @@ struct BlockDev {
 
 // Workspace layout of one forward (offsets in bytes from the workspace base).
 struct WsLayout {
-  size_t status, items, mod, cosc, sinc, resid, y, q, k, vt, o, h, part = 0, resid_lo = 0, total;
+  size_t status, items, mod, cosc, sinc, resid, y, q, k, vt, o, h, part = 0, resid_lo = 0, xs_hi = 0, xs_lo = 0,
+      total;
   int n_pad, max_items, half, mod_rows;
 };
 
@@ -65,6 +73,7 @@ struct dit_handle {
   // fp32 path: final LayerNorm and the 1x1 pre/post convolutions
   float *lnf_g = nullptr, *lnf_b = nullptr, *b_pre = nullptr, *b_post = nullptr;
   const float *w_pre = nullptr, *w_post = nullptr;
+  SplitW s_pre, s_post;  // fp32 path: the 1x1 convolutions' weights split for the 3xTF32 GEMM
   float* dump = nullptr;
   dit_stats stats;
   bool timing = false;
@@ -213,6 +222,11 @@ WsLayout ws_layout_fp32(const dit_config* c, int n, int n_docs) {
   w.mod = take((size_t)n * (io ? io : 1) * 4);
   w.part = take((size_t)kSgemmMaxSplits * n * widest * 4);
   w.resid_lo = take((size_t)n * d * 4);
+  size_t widest_in = (size_t)d;  // the GEMM inputs: io (pre-conv), d, F (FFN down)
+  if ((size_t)F > widest_in) widest_in = (size_t)F;
+  if ((size_t)io > widest_in) widest_in = (size_t)io;
+  w.xs_hi = take((size_t)n * widest_in * 4);
+  w.xs_lo = take((size_t)n * widest_in * 4);
   w.total = off;
   return w;
 }
@@ -311,9 +325,21 @@ dit_status bind_fp32(dit_handle* h, const dit_weights* w, cudaStream_t s) {
     e = src ? to_f32_launch(src, 0, n, dst, s) : cudaMemsetAsync(dst, 0, n * 4, s);
     return e == cudaSuccess ? dst : nullptr;
   };
+  // tf32 (hi, lo) copies of every fp32 linear weight, read by the 3xTF32 GEMM
+  auto split = [&](const void* src, long long n, SplitW* out) -> bool {
+    out->hi = static_cast<float*>(dev_alloc(h, n * 4, &e));
+    if (e != cudaSuccess) return false;
+    out->lo = static_cast<float*>(dev_alloc(h, n * 4, &e));
+    if (e != cudaSuccess) return false;
+    e = tf32_split_launch(static_cast<const float*>(src), (size_t)n, out->hi, out->lo, s);
+    return e == cudaSuccess;
+  };
   for (int l = 0; l < c.n_blocks; ++l) {
     const dit_block_weights& b = w->blocks[l];
     BlockDev& bd = h->blocks[l];
+    if (!split(b.w_qkv, 3ll * d * d, &bd.s_qkv) || !split(b.w_o, (long long)d * d, &bd.s_o) ||
+        !split(b.w_in, 2ll * F * d, &bd.s_in) || !split(b.w_down, (long long)d * F, &bd.s_down))
+      return cuda_err(h, e, "bind: split fp32 weights");
     bd.w_qkv = b.w_qkv;
     bd.w_o = b.w_o;
     bd.w_in = b.w_in;
@@ -333,6 +359,8 @@ dit_status bind_fp32(dit_handle* h, const dit_weights* w, cudaStream_t s) {
   if (io) {
     h->w_pre = static_cast<const float*>(w->w_pre);
     h->w_post = static_cast<const float*>(w->w_post);
+    if (!split(w->w_pre, (long long)d * io, &h->s_pre) || !split(w->w_post, (long long)io * d, &h->s_post))
+      return cuda_err(h, e, "bind: split conv weights");
     h->b_pre = vec(w->b_pre, d, true);
     h->b_post = vec(w->b_post, io, true);
   }
@@ -342,17 +370,22 @@ dit_status bind_fp32(dit_handle* h, const dit_weights* w, cudaStream_t s) {
   return DIT_OK;
 }
 
-// One fp32 GEMM of the forward: partial sums, then the reduction that applies the epilogue.
+// One fp32 GEMM of the forward: the input split into tf32 (hi, lo), the 3xTF32 partial sums, then
+// (by the caller) the fixed-order reduction that applies the epilogue.
 struct Sgemm {
   dit_handle* h;
   cudaStream_t s;
   float* part;
+  float* x_hi;
+  float* x_lo;
   const int* status;
   int S;  // effective splits of the last partial launch
-  cudaError_t run(const float* A, const float* B, int M, int N, int K) {
-    const int want = sgemm_splits(M, N, K);
-    S = sgemm_effective_splits(K, want);
-    return sgemm_partial_launch(A, B, M, N, K, want, part, status, s);
+  cudaError_t run(const float* X, const SplitW& W, int M, int N, int K) {
+    cudaError_t e = tf32_split_launch(X, (size_t)M * K, x_hi, x_lo, s);
+    if (e != cudaSuccess) return e;
+    const int want = tf32x3_splits(M, N, K);
+    S = tf32x3_effective_splits(K, want);
+    return tf32x3_partial_launch(x_hi, x_lo, W.hi, W.lo, M, N, K, want, part, status, s);
   }
 };
 
@@ -375,7 +408,7 @@ dit_status forward_fp32(dit_handle* h, const float* x_tokens, const int32_t* cu_
   float* o = at<float>(workspace, L.o);
   float* hb = at<float>(workspace, L.h);
   float* xt = at<float>(workspace, L.mod);
-  Sgemm g{h, s, at<float>(workspace, L.part), status, 1};
+  Sgemm g{h, s, at<float>(workspace, L.part), at<float>(workspace, L.xs_hi), at<float>(workspace, L.xs_lo), status, 1};
   {
     Launch ln(h, s, 6);
     DIT_CK(h, cudaMemsetAsync(sw, 0, sizeof(StatusWords), s), "status reset");
@@ -392,7 +425,7 @@ dit_status forward_fp32(dit_handle* h, const float* x_tokens, const int32_t* cu_
     // 1x1 pre-convolution as MatmulBT on the frame-major activation ([M3] "What moved")
     Launch ln(h, s, 6);
     DIT_CK(h, io_transpose_launch(x_tokens, xt, cu_seqlens, doc_ids, N, io, 1, status, s), "to frames");
-    DIT_CK(h, g.run(xt, h->w_pre, N, d, io), "pre-conv");
+    DIT_CK(h, g.run(xt, h->s_pre, N, d, io), "pre-conv");
     DIT_CK(h, sgemm_reduce_store_launch(g.part, g.S, N, d, h->b_pre, resid, 0, resid_lo, status, s),
            "pre-conv reduce");
     ln.done();
@@ -410,7 +443,7 @@ dit_status forward_fp32(dit_handle* h, const float* x_tokens, const int32_t* cu_
     }
     {
       Launch ln(h, s, 0);
-      DIT_CK(h, g.run(y, static_cast<const float*>(B.w_qkv), N, 3 * d, d), "qkv");
+      DIT_CK(h, g.run(y, B.s_qkv, N, 3 * d, d), "qkv");
       DIT_CK(h, sgemm_reduce_qkv_launch(g.part, g.S, N, d, c.head_dim, L.half, B.b_qkv, cosc, sinc, q, k, v, status, s),
              "qkv reduce");
       ln.done();
@@ -422,7 +455,7 @@ dit_status forward_fp32(dit_handle* h, const float* x_tokens, const int32_t* cu_
     }
     {
       Launch ln(h, s, 2);
-      DIT_CK(h, g.run(o, static_cast<const float*>(B.w_o), N, d, d), "out-proj");
+      DIT_CK(h, g.run(o, B.s_o, N, d, d), "out-proj");
       DIT_CK(h, sgemm_reduce_store_launch(g.part, g.S, N, d, B.b_o, resid, 1, resid_lo, status, s), "out-proj reduce");
       ln.done();
     }
@@ -434,13 +467,13 @@ dit_status forward_fp32(dit_handle* h, const float* x_tokens, const int32_t* cu_
     }
     {
       Launch ln(h, s, 3);
-      DIT_CK(h, g.run(y, static_cast<const float*>(B.w_in), N, 2 * F, d), "ffn up");
+      DIT_CK(h, g.run(y, B.s_in, N, 2 * F, d), "ffn up");
       DIT_CK(h, sgemm_reduce_swiglu_launch(g.part, g.S, N, F, B.b_in_packed, hb, status, s), "ffn up reduce");
       ln.done();
     }
     {
       Launch ln(h, s, 4);
-      DIT_CK(h, g.run(hb, static_cast<const float*>(B.w_down), N, d, F), "ffn down");
+      DIT_CK(h, g.run(hb, B.s_down, N, d, F), "ffn down");
       DIT_CK(h, sgemm_reduce_store_launch(g.part, g.S, N, d, B.b_down, resid, 1, resid_lo, status, s),
              "ffn down reduce");
       ln.done();
@@ -457,7 +490,7 @@ dit_status forward_fp32(dit_handle* h, const float* x_tokens, const int32_t* cu_
   }
   if (io) {
     Launch ln(h, s, 6);
-    DIT_CK(h, g.run(y, h->w_post, N, io, d), "post-conv");
+    DIT_CK(h, g.run(y, h->s_post, N, io, d), "post-conv");
     DIT_CK(h, sgemm_reduce_store_launch(g.part, g.S, N, io, h->b_post, xt, 0, nullptr, status, s), "post-conv reduce");
     DIT_CK(h, io_transpose_launch(xt, out, cu_seqlens, doc_ids, N, io, 0, status, s), "to channels");
     ln.done();

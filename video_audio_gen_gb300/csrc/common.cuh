@@ -162,6 +162,24 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Instruction descriptor for tcgen05.mma kind::tf32: A and B tf32 (fp32 containers, the low 13
+// mantissa bits ignored), D fp32, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_tf32_f32(int M, int N) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// D(tmem) (+)= A(smem desc) * B(smem desc)^T, kind::tf32, K = 8 per instruction.
+__device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Shared-memory matrix descriptor for a K-major operand stored as 128-byte-swizzled atoms of
 // 8 rows x 128 bytes (what a TMA load with CU_TENSOR_MAP_SWIZZLE_128B writes for a box whose inner
 // extent is 64 bf16).  Rows follow each other every 128 bytes, so 8-row groups are 1024 bytes

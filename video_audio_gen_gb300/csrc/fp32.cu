@@ -1,89 +1,24 @@
 // The fp32 forward path: the music DiT shape of [M3] "What moved" (fp32 stays fp32: every weight and
 // activation is fp32; LayerNorm, partial rotary, non-causal attention with no bias,
 // value * silu(gate), 1x1 pre/post convolutions as MatmulBT on the frame-major activation).
-// TF32 tensor cores would round operands to 10 mantissa bits, far above the 1e-5 tolerance, so the
-// contractions run on the fp32 FMA pipes:
-//   sgemm_partial_kernel   register-blocked 64x128x16 tiles, split-K; each split writes its partial
-//                          sums (accumulated in 64-deep chunks) to a [S][M][N] buffer
-//   sgemm_reduce_*         sums the S partials in a fixed order and applies the epilogue (bias,
-//                          residual add, NeoX RoPE + q/k/v split, value * silu(gate))
-//   attention_f32_kernel   one warp per (query row, head), exact fp32 online softmax with expf
-//   io_transpose_kernel    channel-major [io, len] per document <-> frame-major [N, io]
+// A single TF32 product would round operands to 10 mantissa bits, far above the 1e-5 tolerance;
+// three of them on split operands (3xTF32) keep fp32-level accuracy on the tensor cores:
+//   tf32_split_kernel       x -> tf32(x), tf32(x - tf32(x)) (weights once at bind, activations per GEMM)
+//   tf32x3_partial_kernel   tcgen05 kind::tf32, 32-deep accumulation chunks summed in fp32; split-K,
+//                           each split writes its partial sums to a [S][M][N] buffer
+//   sgemm_reduce_*          sums the S partials in a fixed order and applies the epilogue (bias,
+//                           residual add, NeoX RoPE + q/k/v split, value * silu(gate))
+//   attention_f32_kernel    one warp per (query row, head), exact fp32 online softmax with expf
+//   io_transpose_kernel     channel-major [io, len] per document <-> frame-major [N, io]
 #include "common.cuh"
 #include "kernels.h"
+#include "tmap.h"
 
 #include <math.h>
 
 namespace dit {
 
 namespace {
-
-constexpr int SBM = 64, SBN = 128, SBK = 16;
-constexpr int SCHUNK = 64;  // k-depth of one partial-sum chunk
-
-__global__ void __launch_bounds__(256) sgemm_partial_kernel(const float* __restrict__ A, const float* __restrict__ B,
-                                                            int M, int N, int K, int k_split,
-                                                            float* __restrict__ part, const int* status) {
-  if (status && (*reinterpret_cast<const volatile int*>(status) & kDevLayout)) return;
-  __shared__ __align__(16) float As[SBK][SBM + 4];
-  __shared__ __align__(16) float Bs[SBK][SBN + 4];
-  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-  const int n0 = blockIdx.x * SBN, m0 = blockIdx.y * SBM, s = blockIdx.z;
-  const int kb = s * k_split, ke = min(K, kb + k_split);
-  float acc[4][8], chk[4][8];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc[i][j] = chk[i][j] = 0.f;
-  // load mapping: A row (tid / 4), k quad (tid % 4); B rows (tid / 4) and (tid / 4 + 64)
-  const int lr = tid >> 2, lq = (tid & 3) * 4;
-  const int am = m0 + lr;
-  float4 ra, rb0, rb1;
-  auto gload = [&](int k0) {
-    ra = am < M ? *reinterpret_cast<const float4*>(A + (size_t)am * K + k0 + lq) : make_float4(0.f, 0.f, 0.f, 0.f);
-    rb0 = *reinterpret_cast<const float4*>(B + (size_t)(n0 + lr) * K + k0 + lq);
-    rb1 = *reinterpret_cast<const float4*>(B + (size_t)(n0 + lr + 64) * K + k0 + lq);
-  };
-  if (kb < ke) gload(kb);
-  for (int k0 = kb; k0 < ke; k0 += SBK) {
-    __syncthreads();
-    As[lq + 0][lr] = ra.x; As[lq + 1][lr] = ra.y; As[lq + 2][lr] = ra.z; As[lq + 3][lr] = ra.w;
-    Bs[lq + 0][lr] = rb0.x; Bs[lq + 1][lr] = rb0.y; Bs[lq + 2][lr] = rb0.z; Bs[lq + 3][lr] = rb0.w;
-    Bs[lq + 0][lr + 64] = rb1.x; Bs[lq + 1][lr + 64] = rb1.y; Bs[lq + 2][lr + 64] = rb1.z; Bs[lq + 3][lr + 64] = rb1.w;
-    __syncthreads();
-    if (k0 + SBK < ke) gload(k0 + SBK);  // prefetch the next tile while this one is consumed
-#pragma unroll
-    for (int kk = 0; kk < SBK; ++kk) {
-      const float4 a = *reinterpret_cast<const float4*>(&As[kk][ty * 4]);
-      const float4 b0 = *reinterpret_cast<const float4*>(&Bs[kk][tx * 4]);
-      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[kk][64 + tx * 4]);
-      const float av[4] = {a.x, a.y, a.z, a.w};
-      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) chk[i][j] = fmaf(av[i], bv[j], chk[i][j]);
-    }
-    if (((k0 - kb + SBK) % SCHUNK) == 0 || k0 + SBK >= ke) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          acc[i][j] += chk[i][j];
-          chk[i][j] = 0.f;
-        }
-    }
-  }
-  float* out = part + (size_t)s * M * N;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int m = m0 + ty * 4 + i;
-    if (m >= M) continue;
-    *reinterpret_cast<float4*>(out + (size_t)m * N + n0 + tx * 4) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-    *reinterpret_cast<float4*>(out + (size_t)m * N + n0 + 64 + tx * 4) =
-        make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
-  }
-}
 
 __device__ __forceinline__ float sum_parts(const float* __restrict__ part, int S, size_t MN, size_t idx) {
   float v = 0.f;
@@ -223,6 +158,197 @@ __global__ void io_transpose_kernel(const float* __restrict__ src, float* __rest
   }
 }
 
+// ------------------------------------------------------------------------------------------
+// 3xTF32 partial GEMM on the tcgen05 tensor cores.  Every fp32 operand x is split once into
+// x_hi = tf32(x) and x_lo = tf32(x - x_hi) (round to nearest), and
+//     a . b  ~=  a_hi b_hi + a_hi b_lo + a_lo b_hi
+// drops only a_lo b_lo and the tf32 rounding of the low parts, about 2^-21 of |a b| per product.
+// The tensor core's fp32 accumulation of these products is biased (measured on GB300: the error
+// of a TMEM accumulation grows linearly with its depth, about 2e-5 relative at K = 2048), so the
+// MMAs accumulate only 32-deep chunks, alternately into two TMEM accumulators, and the epilogue
+// adds each chunk into fp32 running sums in registers (round to nearest), much as the FFMA path's
+// 64-deep chunks did.  The roles are transposed so that the small token count sits on the MMA's
+// N side: one CTA owns 128 output features (M = 128 rows of W) x NT tokens (N = NT <= 256, all
+// the tokens of a music forward in one tile) x one K split, and writes part[split][token][feature]
+// for the same fixed-order reductions as before.
+//   warp 0     TMA producer: W_hi, W_lo [128 x 32] and X_hi, X_lo [NT x 32] per 32-deep stage
+//   warp 1     TMEM allocator + MMA issuer: 4 K-steps x 3 products per stage, one stage per chunk
+//   warps 2-9  epilogue: TMEM lane = feature, column = token; two warps per lane quarter split the
+//              token columns; running sums in registers, coalesced stores along features
+constexpr int T3_BK = 32;                 // K per stage: one 128-byte swizzled row of fp32
+constexpr int T3_ROWS = 128;              // output features per CTA (MMA M)
+constexpr int T3_STAGES = 2;
+constexpr int T3_CHUNK = 1;               // stages per accumulation chunk (32-deep)
+constexpr int T3_W_BYTES = T3_ROWS * T3_BK * 4;  // 16 KB
+constexpr int T3_THREADS = 320;
+constexpr int T3_MAX_UNITS = 8;           // 16-column units per epilogue warp (NT <= 256)
+
+struct T3Args {
+  int M, N, K, k_split, nt;
+  float* part;
+  int* status;
+};
+
+__global__ void __launch_bounds__(T3_THREADS, 1)
+    tf32x3_partial_kernel(const __grid_constant__ CUtensorMap tmWhi, const __grid_constant__ CUtensorMap tmWlo,
+                          const __grid_constant__ CUtensorMap tmXhi, const __grid_constant__ CUtensorMap tmXlo,
+                          const T3Args a) {
+  if (a.status && (*reinterpret_cast<const volatile int*>(a.status) & kDevLayout)) return;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int nt = a.nt;
+  const int x_bytes = nt * T3_BK * 4;
+  const int stage_bytes = 2 * T3_W_BYTES + 2 * x_bytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + T3_STAGES * stage_bytes);
+  uint64_t* empty = full + T3_STAGES;
+  uint64_t* chunk_full = empty + T3_STAGES;   // [2] an accumulator holds a finished chunk
+  uint64_t* chunk_empty = chunk_full + 2;     // [2] the epilogue has added it to its running sums
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(chunk_empty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * T3_ROWS, m0 = blockIdx.y * nt, split = blockIdx.z;
+  const int kb = split * a.k_split;
+  const int ke = min(a.K, kb + a.k_split);
+  const int n_kb = ke > kb ? (ke - kb) / T3_BK : 0;
+  const int n_chunks = (n_kb + T3_CHUNK - 1) / T3_CHUNK;
+
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < T3_STAGES; ++st) {
+      mbar_init(&full[st], 1);
+      mbar_init(&empty[st], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&chunk_full[b], 1);
+      mbar_init(&chunk_empty[b], 8);
+    }
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int i = 0;
+      for (; i < n_kb; ++i) {
+        const int st = i % T3_STAGES;
+        if (!mbar_wait(&empty[st], ((i / T3_STAGES) & 1) ^ 1, abort_flag, a.status)) break;
+        uint8_t* base = smem + st * stage_bytes;
+        const int k0 = kb + i * T3_BK;
+        mbar_arrive_expect_tx(&full[st], stage_bytes);
+        tma_load_2d(base, &tmWhi, &full[st], k0, n0);
+        tma_load_2d(base + T3_W_BYTES, &tmWlo, &full[st], k0, n0);
+        tma_load_2d(base + 2 * T3_W_BYTES, &tmXhi, &full[st], k0, m0);
+        tma_load_2d(base + 2 * T3_W_BYTES + x_bytes, &tmXlo, &full[st], k0, m0);
+      }
+      // Every copy issued must land before the CTA exits: wait for the stages still in flight.
+      for (int j = i - T3_STAGES < 0 ? 0 : i - T3_STAGES; j < i; ++j)
+        mbar_wait(&full[j % T3_STAGES], (j / T3_STAGES) & 1, abort_flag, nullptr);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_tf32_f32(T3_ROWS, nt);
+      for (int i = 0; i < n_kb; ++i) {
+        const int st = i % T3_STAGES;
+        const int c = i / T3_CHUNK, cb = c & 1;
+        const bool chunk_start = (i % T3_CHUNK) == 0;
+        const bool chunk_end = (i % T3_CHUNK) == T3_CHUNK - 1 || i == n_kb - 1;
+        if (chunk_start && !mbar_wait(&chunk_empty[cb], ((c >> 1) & 1) ^ 1, abort_flag, a.status)) break;
+        if (!mbar_wait(&full[st], (i / T3_STAGES) & 1, abort_flag, a.status)) break;
+        tc_fence_after();
+        const uint32_t acc = tmem + cb * nt;
+        const uint32_t whi = smem_u32(smem + st * stage_bytes);
+        const uint32_t wlo = whi + T3_W_BYTES;
+        const uint32_t xhi = whi + 2 * T3_W_BYTES;
+        const uint32_t xlo = xhi + x_bytes;
+        // The small cross terms go first, while the accumulator is still about 2^-11 of its final
+        // size (their rounding is then negligible); the four hi x hi products come last.
+#pragma unroll
+        for (int ks = 0; ks < T3_BK / 8; ++ks) {
+          const uint32_t off = ks * 32;  // K = 8 fp32 per instruction
+          umma_tf32(acc, sdesc_sw128(whi + off), sdesc_sw128(xlo + off), idesc, !(chunk_start && ks == 0));
+          umma_tf32(acc, sdesc_sw128(wlo + off), sdesc_sw128(xhi + off), idesc, 1);
+        }
+#pragma unroll
+        for (int ks = 0; ks < T3_BK / 8; ++ks) {
+          const uint32_t off = ks * 32;
+          umma_tf32(acc, sdesc_sw128(whi + off), sdesc_sw128(xhi + off), idesc, 1);
+        }
+        umma_commit(&empty[st]);
+        if (chunk_end) umma_commit(&chunk_full[cb]);
+      }
+    }
+  } else {
+    // epilogue: lane quarter = warp % 4 (TMEM access rule), column half = (warp - 2) / 4
+    const int quarter = warp & 3;
+    const int units = nt / 16;
+    const int u0 = (warp - 2) >> 2 ? (units + 1) / 2 : 0;
+    const int u1 = (warp - 2) >> 2 ? units : (units + 1) / 2;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    float run[T3_MAX_UNITS * 16];
+#pragma unroll
+    for (int i = 0; i < T3_MAX_UNITS * 16; ++i) run[i] = 0.f;
+    bool ok = true;
+    for (int c = 0; c < n_chunks; ++c) {
+      const int cb = c & 1;
+      if (!mbar_wait(&chunk_full[cb], (c >> 1) & 1, abort_flag, a.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int u = 0; u < T3_MAX_UNITS; ++u) {
+        if (u0 + u < u1) {
+          uint32_t v[16];
+          tmem_ld16(tmem + lane_off + cb * nt + (u0 + u) * 16, v);
+          tmem_ld_wait_regs(v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) run[u * 16 + j] = __fadd_rn(run[u * 16 + j], __uint_as_float(v[j]));
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&chunk_empty[cb]);
+    }
+    if (ok) {
+      float* dst = a.part + (size_t)split * a.M * a.N + n0 + quarter * 32 + lane;
+#pragma unroll
+      for (int u = 0; u < T3_MAX_UNITS; ++u) {
+        if (u0 + u < u1) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int m = m0 + (u0 + u) * 16 + j;
+            if (m < a.M) dst[(size_t)m * a.N] = run[u * 16 + j];
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// x -> (tf32(x), tf32(x - tf32(x))), round to nearest (ties away from zero)
+__global__ void tf32_split_kernel(const float* __restrict__ x, size_t n, float* __restrict__ hi, float* __restrict__ lo) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const float v = x[i];
+    uint32_t h, l;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(h) : "f"(v));
+    const float r = __fsub_rn(v, __uint_as_float(h));
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(l) : "f"(r));
+    hi[i] = __uint_as_float(h);
+    lo[i] = __uint_as_float(l);
+  }
+}
+
 int ew_grid(size_t work) {
   size_t g = (work + 255) / 256;
   const size_t cap = (size_t)num_sms() * 16;
@@ -231,31 +357,57 @@ int ew_grid(size_t work) {
 
 }  // namespace
 
-int sgemm_splits(int M, int N, int K) {
-  const int tiles = (N / SBN) * ((M + SBM - 1) / SBM);
-  const int target = 4 * num_sms();  // about two resident CTAs per SM, twice over
-  int S = (target + tiles - 1) / tiles;
-  const int max_s = K / SCHUNK > 0 ? K / SCHUNK : 1;
+int tf32x3_token_tile(int M) {
+  const int m16 = (M + 15) / 16 * 16;
+  return m16 < 256 ? (m16 < 32 ? 32 : m16) : 256;
+}
+
+int tf32x3_splits(int M, int N, int K) {
+  const int tiles = (N / T3_ROWS) * ((M + tf32x3_token_tile(M) - 1) / tf32x3_token_tile(M));
+  int S = (2 * num_sms() + tiles - 1) / tiles;  // about two waves of one CTA per SM
+  const int max_s = K / T3_BK > 0 ? K / T3_BK : 1;
   if (S > max_s) S = max_s;
   if (S > kSgemmMaxSplits) S = kSgemmMaxSplits;
   return S < 1 ? 1 : S;
 }
 
-cudaError_t sgemm_partial_launch(const float* A, const float* B, int M, int N, int K, int S, float* part,
-                                 const int* status, cudaStream_t s) {
-  if (M <= 0) return cudaSuccess;
+int tf32x3_effective_splits(int K, int S) {
   int ks = (K + S - 1) / S;
-  ks = (ks + SCHUNK - 1) / SCHUNK * SCHUNK;  // split boundaries on chunk boundaries
+  ks = (ks + T3_BK - 1) / T3_BK * T3_BK;
+  return (K + ks - 1) / ks;
+}
+
+cudaError_t tf32x3_partial_launch(const float* x_hi, const float* x_lo, const float* w_hi, const float* w_lo, int M,
+                                  int N, int K, int S, float* part, const int* status, cudaStream_t s) {
+  if (M <= 0) return cudaSuccess;
+  if (N % T3_ROWS || K % T3_BK) return cudaErrorInvalidValue;
+  const int nt = tf32x3_token_tile(M);
+  int ks = (K + S - 1) / S;
+  ks = (ks + T3_BK - 1) / T3_BK * T3_BK;
   const int S_eff = (K + ks - 1) / ks;
-  dim3 grid(N / SBN, (M + SBM - 1) / SBM, S_eff);
-  sgemm_partial_kernel<<<grid, 256, 0, s>>>(A, B, M, N, K, ks, part, status);
+  CUtensorMap whi, wlo, xhi, xlo;
+  if (!make_tmap_f32_2d(&whi, w_hi, K, N, (uint64_t)K * 4, T3_ROWS) ||
+      !make_tmap_f32_2d(&wlo, w_lo, K, N, (uint64_t)K * 4, T3_ROWS) ||
+      !make_tmap_f32_2d(&xhi, x_hi, K, M, (uint64_t)K * 4, nt) ||
+      !make_tmap_f32_2d(&xlo, x_lo, K, M, (uint64_t)K * 4, nt))
+    return cudaErrorInvalidValue;
+  const int smem = T3_STAGES * (2 * T3_W_BYTES + 2 * nt * T3_BK * 4) + 1024 + 256;
+  static int attr_smem = 0;
+  if (smem > attr_smem) {
+    cudaError_t e = cudaFuncSetAttribute(tf32x3_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_smem = smem;
+  }
+  T3Args a{M, N, K, ks, nt, part, const_cast<int*>(status)};
+  dim3 grid(N / T3_ROWS, (M + nt - 1) / nt, S_eff);
+  tf32x3_partial_kernel<<<grid, T3_THREADS, smem, s>>>(whi, wlo, xhi, xlo, a);
   return cudaGetLastError();
 }
 
-int sgemm_effective_splits(int K, int S) {
-  int ks = (K + S - 1) / S;
-  ks = (ks + SCHUNK - 1) / SCHUNK * SCHUNK;
-  return (K + ks - 1) / ks;
+cudaError_t tf32_split_launch(const float* x, size_t n, float* hi, float* lo, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  tf32_split_kernel<<<ew_grid(n), 256, 0, s>>>(x, n, hi, lo);
+  return cudaGetLastError();
 }
 
 cudaError_t sgemm_reduce_store_launch(const float* part, int S, int M, int N, const float* bias, float* out, int add,

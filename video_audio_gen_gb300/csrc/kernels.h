@@ -80,13 +80,15 @@ int num_sms();
 bool norm_width_supported(int d);
 cudaError_t wait_timeout_selftest_launch(int* status, unsigned long long limit_ns, cudaStream_t s);
 
-// fp32 path (csrc/fp32.cu): split-K FFMA GEMM D = A B^T (A [M, K], B [N, K], fp32, N % 128 == 0,
-// K % 16 == 0) into partials [S][M][N], then fixed-order reductions with the epilogues.
+// fp32 path (csrc/fp32.cu): split-K 3xTF32 tensor-core GEMM D = X W^T (X [M, K], W [N, K], fp32 given
+// as tf32 (hi, lo) pairs, N % 128 == 0, K % 32 == 0) into partials [S][M][N], then fixed-order
+// reductions that apply the epilogues.
 constexpr int kSgemmMaxSplits = 16;
-int sgemm_splits(int M, int N, int K);
-int sgemm_effective_splits(int K, int S);
-cudaError_t sgemm_partial_launch(const float* A, const float* B, int M, int N, int K, int S, float* part,
-                                 const int* status, cudaStream_t s);
+int tf32x3_splits(int M, int N, int K);
+int tf32x3_effective_splits(int K, int S);
+cudaError_t tf32x3_partial_launch(const float* x_hi, const float* x_lo, const float* w_hi, const float* w_lo, int M,
+                                  int N, int K, int S, float* part, const int* status, cudaStream_t s);
+cudaError_t tf32_split_launch(const float* x, size_t n, float* hi, float* lo, cudaStream_t s);
 cudaError_t sgemm_reduce_store_launch(const float* part, int S, int M, int N, const float* bias, float* out, int add,
                                       float* lo, const int* status, cudaStream_t s);
 cudaError_t sgemm_reduce_qkv_launch(const float* part, int S, int M, int d, int Dh, int half, const float* bias,
