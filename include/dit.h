@@ -264,6 +264,20 @@ DIT_API dit_status dit_op_gemm_gated_residual(const void* a, const void* b, cons
 DIT_API dit_status dit_op_gemm_swiglu(const void* a, const void* b_packed, const float* bias_packed, int M, int F, int K,
                               void* h, void* stream);
 
+/* fp32 GEMM y = x w^T + bias exactly as the fp32 forward computes its linear maps ([M3] "What
+ * moved": every Linear is a MatmulBT with a rank-1 bias add; fp32 stays fp32): 3xTF32 on the
+ * tcgen05 tensor cores (each operand split into tf32 hi + lo parts, three tf32 products per fp32
+ * product, 32-deep accumulation chunks summed in fp32), split-K partial sums reduced in a fixed order.
+ *   x fp32 [M, K] row-major, w fp32 [N, K] row-major, bias fp32 [N] or NULL, y fp32 [M, N] (written).
+ *   M >= 1; N % 128 == 0; K % 32 == 0; x, w, y 16-byte aligned.
+ *   workspace: device scratch of dit_gemm_f32_workspace_bytes(M, N, K) bytes, caller-owned (the hi/lo
+ *   splits of x and w and the partial sums); not retained after the call's device work.
+ *   Results are deterministic; calls on one stream are ordered.  Errors: DIT_ERR_INVALID_ARG for bad
+ *   shapes or pointers (nothing launched), DIT_ERR_CUDA when a launch fails. */
+DIT_API size_t dit_gemm_f32_workspace_bytes(int M, int N, int K);
+DIT_API dit_status dit_op_gemm_f32(const float* x, const float* w, const float* bias, int M, int N, int K, float* y,
+                           void* workspace, void* stream);
+
 /* Interleave an FFN up projection [2F, d] (value rows then gate rows) into 128-feature groups:
  * packed rows [256 g, 256 g + 128) = value rows [128 g, +128), the next 128 = the gate rows
  * [F + 128 g, +128).  bias (fp32 [2F] or NULL) is interleaved the same way into bias_packed

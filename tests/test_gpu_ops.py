@@ -199,6 +199,52 @@ def test_gemm_gated_residual_matches_oracle():
     assert np.abs(xd2.double().cpu().numpy() - ref2).max() <= 1e-4
 
 
+def tf32x3_bound(x, w, ref):
+    """Elementwise bound for the 3xTF32 fp32 GEMM, from its arithmetic: the split drops about
+    3 x 2^-22 of |x w| per product; each 32-deep TMEM chunk (12 accumulating MMAs) adds at most
+    4e-6 of its sum of |x w| (the accumulation is biased, so this is linear, not a random walk);
+    the chunk sums and the K-split reduction are fp32 round-to-nearest adds (one 2^-24 of the sum of
+    |x w| each); the store rounds once."""
+    K = x.shape[1]
+    P = np.abs(x) @ np.abs(w).T
+    return (5e-6 + (K / 32 + 16) * 2.0 ** -24) * P + 2.0 ** -23 * np.abs(ref)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 128, 32), (17, 128, 4096), (74, 256, 1024), (300, 384, 96),
+                                   (172, 2048, 8192)])
+def test_gemm_f32_matches_oracle(M, N, K):
+    """The fp32 forward's linear map (3xTF32 on the tensor cores): token counts below, at and above
+    one 256-wide token tile, ragged M, the music DiT's deepest K; against the oracle's fp64 linear."""
+    dit, gu = _dit(), _gu()
+    x = synth.normal(140, "x", (M, K), 1.0)
+    w = synth.normal(140, "w", (N, K), 0.02)
+    b = synth.normal(140, "b", (N,), 0.02)
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    ws = torch.empty(dit.gemm_f32_workspace_bytes(M, N, K), dtype=torch.uint8, device="cuda")
+    ws.fill_(0xFF)  # stale NaN bytes: nothing may read scratch it did not write
+    dit.gemm_f32(gu.dev_f32(x), gu.dev_f32(w), gu.dev_f32(b), y, ws)
+    torch.cuda.synchronize()
+    oracle.set_threads(16)
+    ref = oracle.linear(x.astype(np.float64), w, b)
+    oracle.set_threads(1)
+    got = y.double().cpu().numpy()
+    bound = tf32x3_bound(x.astype(np.float64), w.astype(np.float64), ref)
+    assert np.all(np.abs(got - ref) <= bound), float((np.abs(got - ref) / bound).max())
+    # a single tf32 product would miss by ~1e-3 relative: the bound is far tighter than that
+    P = np.abs(x).astype(np.float64) @ np.abs(w).astype(np.float64).T
+    assert np.abs(got - ref).max() <= 2e-5 * P.max()
+
+
+def test_gemm_f32_rejects_bad_shapes():
+    dit, gu = _dit(), _gu()
+    x = gu.dev_f32(np.zeros((4, 48), np.float32))
+    w = gu.dev_f32(np.zeros((128, 48), np.float32))
+    y = torch.empty((4, 128), dtype=torch.float32, device="cuda")
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    with pytest.raises(dit.DitError):
+        dit.gemm_f32(x, w, None, y, ws)  # K = 48 is not a multiple of 32
+
+
 def test_gemm_swiglu_matches_oracle():
     dit, gu = _dit(), _gu()
     M, F, d = 300, 768, 512

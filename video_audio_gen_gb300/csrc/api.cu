@@ -981,6 +981,54 @@ dit_status dit_op_pack_ffn_in(const void* w_in, const float* b_in, int F, int d,
   return e == cudaSuccess ? DIT_OK : cuda_err(nullptr, e, "pack_ffn_in");
 }
 
+namespace {
+struct GemmF32Ws {
+  size_t x_hi, x_lo, w_hi, w_lo, part, total;
+};
+GemmF32Ws gemm_f32_ws(int M, int N, int K) {
+  GemmF32Ws w{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes);
+    return o;
+  };
+  w.x_hi = take((size_t)M * K * 4);
+  w.x_lo = take((size_t)M * K * 4);
+  w.w_hi = take((size_t)N * K * 4);
+  w.w_lo = take((size_t)N * K * 4);
+  w.part = take((size_t)kSgemmMaxSplits * M * N * 4);
+  w.total = off;
+  return w;
+}
+}  // namespace
+
+size_t dit_gemm_f32_workspace_bytes(int M, int N, int K) {
+  if (M < 1 || N < 1 || K < 1) return 0;
+  return gemm_f32_ws(M, N, K).total;
+}
+
+dit_status dit_op_gemm_f32(const float* x, const float* w, const float* bias, int M, int N, int K, float* y,
+                           void* workspace, void* stream) {
+  if (!x || !w || !y || !workspace || M < 1 || N < 128 || N % 128 || K < 32 || K % 32 || !aligned16(x) ||
+      !aligned16(w) || !aligned16(y))
+    return set_err(nullptr, DIT_ERR_INVALID_ARG, "fp32 GEMM needs M >= 1, N %% 128 == 0, K %% 32 == 0, aligned pointers");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const GemmF32Ws L = gemm_f32_ws(M, N, K);
+  float* x_hi = at<float>(workspace, L.x_hi);
+  float* x_lo = at<float>(workspace, L.x_lo);
+  float* w_hi = at<float>(workspace, L.w_hi);
+  float* w_lo = at<float>(workspace, L.w_lo);
+  float* part = at<float>(workspace, L.part);
+  cudaError_t e = tf32_split_launch(x, (size_t)M * K, x_hi, x_lo, s);
+  if (e == cudaSuccess) e = tf32_split_launch(w, (size_t)N * K, w_hi, w_lo, s);
+  const int want = tf32x3_splits(M, N, K);
+  if (e == cudaSuccess) e = tf32x3_partial_launch(x_hi, x_lo, w_hi, w_lo, M, N, K, want, part, nullptr, s);
+  if (e == cudaSuccess)
+    e = sgemm_reduce_store_launch(part, tf32x3_effective_splits(K, want), M, N, bias, y, 0, nullptr, nullptr, s);
+  return e == cudaSuccess ? DIT_OK : cuda_err(nullptr, e, "fp32 gemm");
+}
+
 size_t dit_attention_workspace_bytes(int n_docs, int n_tokens) {
   if (n_docs < 1 || n_tokens < 1) return 0;
   return align_up(sizeof(StatusWords)) + align_up((size_t)attention_max_items(n_docs, n_tokens) * sizeof(int2));

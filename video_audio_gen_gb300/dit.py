@@ -25,7 +25,7 @@ EXPORTS = ["dit_create", "dit_destroy", "dit_last_error", "dit_workspace_bytes",
            "dit_workspace_bytes_host", "dit_forward_host", "dit_euler_step", "dit_get_stats", "dit_sync_status",
            "dit_set_dump", "dit_set_kernel_timing", "dit_get_kernel_times", "dit_op_norm_modulate",
            "dit_op_rope_cache", "dit_op_adaln", "dit_op_gemm", "dit_op_gemm_qkv_rope", "dit_op_gemm_gated_residual",
-           "dit_op_gemm_swiglu", "dit_op_pack_ffn_in", "dit_attention_workspace_bytes", "dit_op_attention",
+           "dit_op_gemm_swiglu", "dit_gemm_f32_workspace_bytes", "dit_op_gemm_f32", "dit_op_pack_ffn_in", "dit_attention_workspace_bytes", "dit_op_attention",
            "dit_op_attention_noalloc", "dit_selftest_wait_timeout"]
 
 
@@ -105,6 +105,8 @@ def lib():
             "dit_op_gemm_swiglu": (i32, [vp, vp, vp, i32, i32, i32, vp, vp]),
             "dit_op_pack_ffn_in": (i32, [vp, vp, i32, i32, vp, vp, vp]),
             "dit_attention_workspace_bytes": (sz, [i32, i32]),
+            "dit_gemm_f32_workspace_bytes": (sz, [i32, i32, i32]),
+            "dit_op_gemm_f32": (i32, [vp, vp, vp, i32, i32, i32, vp, vp, vp]),
             "dit_op_attention": (i32, [vp, vp, vp, i32, vp, i32, i32, i32, i32, vp, vp, vp]),
             "dit_op_attention_noalloc": (i32, [vp, vp, vp, i32, vp, i32, i32, i32, i32, vp, vp]),
             "dit_selftest_wait_timeout": (i32, [ctypes.c_uint64, vp, vp]),
@@ -265,6 +267,17 @@ def gemm(a, b, bias, out, out_kind: int, stream=None):
     M, K = a.shape
     N = b.shape[0]
     _check(lib().dit_op_gemm(_ptr(a), _ptr(b), _ptr(bias), M, N, K, _ptr(out), out_kind, _stream(stream)))
+
+
+def gemm_f32_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(lib().dit_gemm_f32_workspace_bytes(M, N, K))
+
+
+def gemm_f32(x, w, bias, y, workspace, stream=None):
+    """dit_op_gemm_f32: y = x w^T + bias in fp32 (3xTF32 on the tensor cores)."""
+    M, K = x.shape
+    N = w.shape[0]
+    _check(lib().dit_op_gemm_f32(_ptr(x), _ptr(w), _ptr(bias), M, N, K, _ptr(y), _ptr(workspace), _stream(stream)))
 
 
 def gemm_qkv_rope(a, b, bias, n_heads, head_dim, rotary_dim, cos_c, sin_c, q, k, vt, n_pad, stream=None):
