@@ -183,6 +183,16 @@ WORKLOADS = {
                    seed=11, docs=[dict(video=(2, 5, 7), audio=13), dict(video=(3, 8, 9), audio=41),
                                   dict(video=(1, 1, 1)), dict(video=(4, 12, 10), audio=37)],
                    t=0.37, w_std=0.02, bias_std=0.02, x_std=1.0),
+    # Parity case for the tile schedule and the key masking: 13 documents whose lengths sit on and
+    # around the 128-token tile (1, 2, 127, 128, 129, 255, 256, 257, 300, ...), none starting on a
+    # tile boundary after the first, head_dim 64, non-zero biases.
+    "many_docs": dict(model=_model(), seed=13,
+                      docs=[dict(video=(1, 1, 1)), dict(video=(2, 8, 8)), dict(video=(2, 8, 8), audio=1),
+                            dict(video=(4, 8, 8)), dict(video=(1, 9, 14), audio=1), dict(video=(1, 1, 2)),
+                            dict(video=(3, 5, 17)), dict(video=(1, 8, 8)), dict(video=(2, 10, 15)),
+                            dict(video=(1, 1, 1), audio=5), dict(video=(5, 5, 5), audio=3),
+                            dict(video=(1, 3, 3)), dict(video=(2, 16, 8), audio=1)],
+                      t=0.61, w_std=0.02, bias_std=0.02, x_std=1.0),
     "music_small": dict(model=_model(n_blocks=2, hidden=256, n_heads=2, head_dim=128, ffn_hidden=1024,
                                      norm="ln", norm_eps=1e-5, adaln=False, n_mod=1, rope_axes=1,
                                      rope_dims=(64, 0, 0), rotary_dim=64, io_channels=128, dtype="fp32"),

@@ -27,7 +27,7 @@ def check_against_oracle(w, run, ref_out, ref_dumps):
     assert not fails, fails
 
 
-@pytest.mark.parametrize("name", ["tiny", "ragged"])
+@pytest.mark.parametrize("name", ["tiny", "ragged", "many_docs"])
 def test_forward_matches_oracle(name):
     gu = _gu()
     w = synth.WORKLOADS[name]
