@@ -473,13 +473,9 @@ namespace {
 template <int HD>
 cudaError_t attention_launch_t(const void* q, const void* k, const void* vt, void* o, const AttnArgs& args,
                                cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attention_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         AttPlan<HD>::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static unsigned long long smem_set = 0;
+  cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(attention_kernel<HD>), AttPlan<HD>::SMEM, &smem_set);
+  if (e != cudaSuccess) return e;
   const int d = args.n_heads * HD;
   CUtensorMap tq, tk, tv;
   if (!make_tmap_bf16_2d(&tq, q, d, args.n_tokens, (uint64_t)d * 2, 64, TQ)) return cudaErrorInvalidValue;

@@ -392,12 +392,10 @@ cudaError_t tf32x3_partial_launch(const float* x_hi, const float* x_lo, const fl
       !make_tmap_f32_2d(&xlo, x_lo, K, M, (uint64_t)K * 4, nt))
     return cudaErrorInvalidValue;
   const int smem = T3_STAGES * (2 * T3_W_BYTES + 2 * nt * T3_BK * 4) + 1024 + 256;
-  static int attr_smem = 0;
-  if (smem > attr_smem) {
-    cudaError_t e = cudaFuncSetAttribute(tf32x3_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_smem = smem;
-  }
+  static unsigned long long smem_set = 0;  // opted in to the largest plan (NT = 256) once per device
+  cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(tf32x3_partial_kernel),
+                              2 * (2 * T3_W_BYTES + 2 * 256 * T3_BK * 4) + 1024 + 256, &smem_set);
+  if (e != cudaSuccess) return e;
   T3Args a{M, N, K, ks, nt, part, const_cast<int*>(status)};
   dim3 grid(N / T3_ROWS, (M + nt - 1) / nt, S_eff);
   tf32x3_partial_kernel<<<grid, T3_THREADS, smem, s>>>(whi, wlo, xhi, xlo, a);

@@ -435,12 +435,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 template <int EPI>
 cudaError_t launch_t(const void* A, const void* B, const GemmArgs& args, cudaStream_t stream) {
   constexpr int smem = EPI == kEpiGatedResid ? SMEM_BYTES_RESID : SMEM_BYTES;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static unsigned long long smem_set = 0;
+  cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(gemm_kernel<EPI>), smem, &smem_set);
+  if (e != cudaSuccess) return e;
   CUtensorMap ta, tb;
   if (!make_tmap_bf16_2d(&ta, A, args.K, args.M, (uint64_t)args.K * 2, BK, BM)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16_2d(&tb, B, args.K, args.N, (uint64_t)args.K * 2, BK, BN)) return cudaErrorInvalidValue;

@@ -7,6 +7,19 @@
 
 namespace dit {
 
+// Opt `func` into `bytes` of dynamic shared memory on the current device.  The attribute is per
+// device, so the cache is a bitmask of the devices (0-63) already set, one mask per kernel.
+inline cudaError_t opt_in_smem(const void* func, int bytes, unsigned long long* done_mask) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev >= 0 && dev < 64 ? 1ull << dev : 0ull;
+  if (bit && (__atomic_load_n(done_mask, __ATOMIC_ACQUIRE) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) __atomic_fetch_or(done_mask, bit, __ATOMIC_RELEASE);
+  return e;
+}
+
 // Epilogue kinds of the tcgen05 GEMM engine.
 enum GemmEpilogue : int {
   kEpiStore = 0,        // out = acc + bias (bf16 or fp32)
