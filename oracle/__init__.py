@@ -60,6 +60,8 @@ def lib():
         if _lib is None:
             _lib = ctypes.CDLL(build())
             _lib.orc_forward.restype = ctypes.c_int
+            _lib.orc_forward_mod.restype = ctypes.c_int
+            _lib.orc_time_shift.restype = ctypes.c_double
             _lib.orc_check_layout.restype = ctypes.c_int
             _lib.orc_count_q_tiles.restype = ctypes.c_int
             _lib.orc_get_threads.restype = ctypes.c_int
@@ -152,15 +154,31 @@ def timestep_embedding(t: float, t_dim: int) -> np.ndarray:
     return out
 
 
-def adaln(m: dict, weights: dict, t: float):
-    """Returns (mod [L, n_mod, 6, d], mod_final [n_mod, 2, d]) in float64."""
+def adaln(m: dict, weights: dict, t):
+    """Returns (mod [L, n_mod, 6, d], mod_final [n_mod, 2, d]) in float64.  t is one timestep, or
+    one per modality (the per-modality sigma schedules)."""
     c = config(m)
     w = _Weights(m, weights)
     d, L, nm = m["hidden"], m["n_blocks"], m["n_mod"]
     mod = np.empty((L, nm, 6, d), dtype=np.float64)
     modf = np.empty((nm, 2, d), dtype=np.float64)
-    lib().orc_adaln(ctypes.byref(c), ctypes.byref(w.w), ctypes.c_double(t), _d(mod), _d(modf))
+    if np.ndim(t) == 0:
+        lib().orc_adaln(ctypes.byref(c), ctypes.byref(w.w), ctypes.c_double(t), _d(mod), _d(modf))
+    else:
+        tm = np.ascontiguousarray(t, dtype=np.float64)
+        assert tm.shape == (nm,)
+        lib().orc_adaln_mod(ctypes.byref(c), ctypes.byref(w.w), _d(tm), _d(mod), _d(modf))
     return mod, modf
+
+
+def time_shift(sigma: float, shift: float) -> float:
+    """The rectified-flow time shift of one sigma, in double (the oracle's formula)."""
+    return float(lib().orc_time_shift(ctypes.c_double(sigma), ctypes.c_double(shift)))
+
+
+def sigmas_shifted(base, shift: float) -> np.ndarray:
+    """fp32 shifted schedule: each fp32 base sigma shifted in double, then rounded to fp32."""
+    return np.array([time_shift(float(s), shift) for s in np.asarray(base, dtype=np.float32)], dtype=np.float32)
 
 
 def rope_inv_freq(m: dict) -> np.ndarray:
@@ -275,6 +293,18 @@ def euler_step(x, v, sigma: float, sigma_next: float) -> np.ndarray:
     return x
 
 
+def euler_step_tagged(x, v, tags, sigma, sigma_next) -> np.ndarray:
+    """Euler step of x [N, d] with each row's modality sigma pair (sigma[tags[r]], sigma_next[tags[r]])."""
+    x = np.ascontiguousarray(x, dtype=np.float32).copy()
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    tags = np.ascontiguousarray(tags, dtype=np.uint8)
+    st = np.ascontiguousarray(sigma, dtype=np.float32)
+    sn = np.ascontiguousarray(sigma_next, dtype=np.float32)
+    lib().orc_euler_step_tagged(_f(x), _f(v), ctypes.c_int(x.shape[0]), ctypes.c_int(x.shape[1]),
+                                _p(tags), _f(st), _f(sn))
+    return x
+
+
 def block_forward(m: dict, weights: dict, l: int, mod_block, x, layout: dict, cs, sn) -> np.ndarray:
     """One block in place on a float64 copy of x [N, d]; mod_block [n_mod, 6, d] or None."""
     c = config(m)
@@ -290,8 +320,9 @@ def block_forward(m: dict, weights: dict, l: int, mod_block, x, layout: dict, cs
     return x
 
 
-def forward(m: dict, weights: dict, x_in, layout: dict, t: float, dumps: bool = False):
-    """Whole forward.  Returns (out float64 shaped like x_in, block dumps [L, N, d] or None)."""
+def forward(m: dict, weights: dict, x_in, layout: dict, t, dumps: bool = False):
+    """Whole forward.  Returns (out float64 shaped like x_in, block dumps [L, N, d] or None).
+    t is one timestep, or one per modality."""
     c = config(m)
     w = _Weights(m, weights)
     x_in = np.ascontiguousarray(x_in, dtype=np.float32)
@@ -302,9 +333,15 @@ def forward(m: dict, weights: dict, x_in, layout: dict, t: float, dumps: bool = 
     ids = np.ascontiguousarray(layout["doc_ids"], dtype=np.int32)
     tags = np.ascontiguousarray(layout["tags"], dtype=np.uint8)
     pos = _dbl(layout["pos"])
-    rc = lib().orc_forward(ctypes.byref(c), ctypes.byref(w.w), _f(x_in), ctypes.c_int(n), _p(cu),
-                           ctypes.c_int(layout["n_docs"]), _p(ids), _p(tags), _d(pos),
-                           ctypes.c_double(t), _d(out), _d(dm) if dumps else None)
+    if np.ndim(t) == 0:
+        rc = lib().orc_forward(ctypes.byref(c), ctypes.byref(w.w), _f(x_in), ctypes.c_int(n), _p(cu),
+                               ctypes.c_int(layout["n_docs"]), _p(ids), _p(tags), _d(pos),
+                               ctypes.c_double(t), _d(out), _d(dm) if dumps else None)
+    else:
+        tm = np.ascontiguousarray(t, dtype=np.float64)
+        rc = lib().orc_forward_mod(ctypes.byref(c), ctypes.byref(w.w), _f(x_in), ctypes.c_int(n), _p(cu),
+                                   ctypes.c_int(layout["n_docs"]), _p(ids), _p(tags), _d(pos),
+                                   _d(tm), _d(out), _d(dm) if dumps else None)
     if rc:
         raise ValueError(f"oracle: invalid packed layout (code {rc})")
     return out, dm

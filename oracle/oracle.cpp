@@ -123,29 +123,51 @@ static inline double silu(double v) { return v / (1.0 + exp(-v)); }
 // split into six d-wide chunks in the order shift1, scale1, gate1, shift2, scale2, gate2 (READING:
 // the DiT convention).  The final layer uses [n_mod][2d] = (shift_f, scale_f).
 // ---------------------------------------------------------------------------------------------
-void orc_adaln(const orc_config* c, const orc_weights* w, double t, double* mod, double* mod_final) {
+// With one timestep per modality (the per-modality sigma schedules of [H3] "Milestone: the whole
+// t2va path composes end to end": video shift 12, audio 3), the rows of modality m are computed
+// from the embedding of t_mod[m].
+void orc_adaln_mod(const orc_config* c, const orc_weights* w, const double* t_mod, double* mod, double* mod_final) {
   int d = c->hidden, td = c->t_dim;
-  std::vector<double> e(td), se(td);
-  orc_timestep_embedding(t, td, e.data());
-  for (int k = 0; k < td; ++k) se[k] = silu(e[k]);
+  std::vector<double> se((size_t)c->n_mod * td);
+  for (int m = 0; m < c->n_mod; ++m) {
+    std::vector<double> e(td);
+    orc_timestep_embedding(t_mod[m], td, e.data());
+    for (int k = 0; k < td; ++k) se[(size_t)m * td + k] = silu(e[k]);
+  }
   int rows = c->n_mod * 6 * d;
   for (int l = 0; l < c->n_blocks; ++l) {
     const orc_block* b = &w->blocks[l];
     for (int r = 0; r < rows; ++r) {
+      const double* sm = &se[(size_t)(r / (6 * d)) * td];
       double s = 0.0;
-      for (int k = 0; k < td; ++k) s += (double)b->w_ada[(size_t)r * td + k] * se[k];
+      for (int k = 0; k < td; ++k) s += (double)b->w_ada[(size_t)r * td + k] * sm[k];
       if (b->b_ada) s += (double)b->b_ada[r];
       mod[(size_t)l * rows + r] = s;
     }
   }
   int rf = c->n_mod * 2 * d;
   for (int r = 0; r < rf; ++r) {
+    const double* sm = &se[(size_t)(r / (2 * d)) * td];
     double s = 0.0;
-    for (int k = 0; k < td; ++k) s += (double)w->w_ada_final[(size_t)r * td + k] * se[k];
+    for (int k = 0; k < td; ++k) s += (double)w->w_ada_final[(size_t)r * td + k] * sm[k];
     if (w->b_ada_final) s += (double)w->b_ada_final[r];
     mod_final[r] = s;
   }
 }
+
+void orc_adaln(const orc_config* c, const orc_weights* w, double t, double* mod, double* mod_final) {
+  std::vector<double> tm((size_t)c->n_mod, t);
+  orc_adaln_mod(c, w, tm.data(), mod, mod_final);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Rectified-flow time shift.  [H3] "Milestone: the whole t2va path composes end to end": sigma
+// schedules with video shift 12 and audio 3.  READING (the pages name the shift, not its formula):
+// the usual rectified-flow shift of a sigma in [0, 1],
+//   shift(sigma, s) = s * sigma / (1 + (s - 1) * sigma),
+// evaluated in double on the fp32 base sigma and rounded to fp32 by the caller.
+// ---------------------------------------------------------------------------------------------
+double orc_time_shift(double sigma, double s) { return s * sigma / (1.0 + (s - 1.0) * sigma); }
 
 // ---------------------------------------------------------------------------------------------
 // RoPE angles.  [H3] "The device-resident forward (W2b)": plain NeoX rotate_half whose angles come
@@ -381,6 +403,14 @@ void orc_euler_step(float* x, const float* v, int64_t n, float sigma, float sigm
   }
 }
 
+// The same step with the sigma pair of each token's modality: row r of x [n_tokens][d] uses
+// (sigma[tags[r]], sigma_next[tags[r]]).
+void orc_euler_step_tagged(float* x, const float* v, int n_tokens, int d, const uint8_t* tags, const float* sigma,
+                           const float* sigma_next) {
+  for (int r = 0; r < n_tokens; ++r)
+    orc_euler_step(x + (size_t)r * d, v + (size_t)r * d, d, sigma[tags[r]], sigma_next[tags[r]]);
+}
+
 // ---------------------------------------------------------------------------------------------
 // One transformer block, in place on the fp64 residual x [N][d].  [H3] "The device-resident
 // forward (W2b)" lists the ops; with AdaLN on:
@@ -454,9 +484,9 @@ void orc_block_forward(const orc_config* c, const orc_block* w, const double* mo
 // dumps (may be NULL) receives the residual after each block, [L][N][d].
 // Returns the layout check's code (0 when valid).
 // ---------------------------------------------------------------------------------------------
-int orc_forward(const orc_config* c, const orc_weights* w, const float* x_in, int n, const int32_t* cu, int n_docs,
-                const int32_t* doc_ids, const uint8_t* tags, const double* pos, double t, double* out,
-                double* dumps) {
+int orc_forward_mod(const orc_config* c, const orc_weights* w, const float* x_in, int n, const int32_t* cu,
+                    int n_docs, const int32_t* doc_ids, const uint8_t* tags, const double* pos, const double* t_mod,
+                    double* out, double* dumps) {
   int rc = orc_check_layout(cu, n_docs, doc_ids, tags, n, c->adaln ? c->n_mod : 1);
   if (rc) return rc;
   int d = c->hidden, half = c->rotary_dim / 2;
@@ -480,7 +510,7 @@ int orc_forward(const orc_config* c, const orc_weights* w, const float* x_in, in
   if (c->adaln) {
     mod.resize((size_t)c->n_blocks * c->n_mod * 6 * d);
     modf.resize((size_t)c->n_mod * 2 * d);
-    orc_adaln(c, w, t, mod.data(), modf.data());
+    orc_adaln_mod(c, w, t_mod, mod.data(), modf.data());
   }
   for (int l = 0; l < c->n_blocks; ++l) {
     const double* ml = c->adaln ? mod.data() + (size_t)l * c->n_mod * 6 * d : nullptr;
@@ -508,6 +538,13 @@ int orc_forward(const orc_config* c, const orc_weights* w, const float* x_in, in
     }
   }
   return 0;
+}
+
+int orc_forward(const orc_config* c, const orc_weights* w, const float* x_in, int n, const int32_t* cu, int n_docs,
+                const int32_t* doc_ids, const uint8_t* tags, const double* pos, double t, double* out,
+                double* dumps) {
+  std::vector<double> tm((size_t)(c->n_mod > 0 ? c->n_mod : 1), t);
+  return orc_forward_mod(c, w, x_in, n, cu, n_docs, doc_ids, tags, pos, tm.data(), out, dumps);
 }
 
 }  // extern "C"

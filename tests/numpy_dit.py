@@ -78,12 +78,17 @@ def forward(m, W, x_in, lay, t):
     else:
         x = np.asarray(x_in, dtype=np.float64).copy()
     ang = rope_angles(m, lay["pos"])
+    nm = m["n_mod"]
     if m["adaln"]:
-        se = silu(t_embed(t, m["t_dim"]))
+        # one timestep, or one per modality: the rows of modality i come from the embedding of t[i]
+        ts = [t] * nm if np.ndim(t) == 0 else list(t)
+        se = [silu(t_embed(ti, m["t_dim"])) for ti in ts]
     for l, bw in enumerate(W["blocks"]):
         B = {k: f64(v) for k, v in bw.items()}
         if m["adaln"]:
-            mod = (B["w_ada"] @ se + B["b_ada"]).reshape(m["n_mod"], 6, d)[tags]  # [N, 6, d]
+            wa = B["w_ada"].reshape(nm, 6 * d, -1)
+            ba = B["b_ada"].reshape(nm, 6 * d)
+            mod = np.stack([wa[i] @ se[i] + ba[i] for i in range(nm)]).reshape(nm, 6, d)[tags]  # [N, 6, d]
             y = norm(x, m) * (1 + mod[:, 1]) + mod[:, 0]
         else:
             y = norm(x, m, B.get("ln1_g"), B.get("ln1_b"))
@@ -103,7 +108,9 @@ def forward(m, W, x_in, lay, t):
         x = x + (mod[:, 5] * upd if m["adaln"] else upd)
     if m["adaln"]:
         G = {k: f64(v) for k, v in W["glob"].items()}
-        mf = (G["w_ada_final"] @ se + G["b_ada_final"]).reshape(m["n_mod"], 2, d)[tags]
+        wf = G["w_ada_final"].reshape(nm, 2 * d, -1)
+        bf = G["b_ada_final"].reshape(nm, 2 * d)
+        mf = np.stack([wf[i] @ se[i] + bf[i] for i in range(nm)]).reshape(nm, 2, d)[tags]
         return norm(x, m) * (1 + mf[:, 1]) + mf[:, 0]
     G = {k: f64(v) for k, v in W["glob"].items()}
     y = norm(x, m, G.get("lnf_g"), G.get("lnf_b"))

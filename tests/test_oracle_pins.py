@@ -404,3 +404,69 @@ def test_forward_thread_count_does_not_change_bits():
     b, _ = oracle.forward(w["model"], W, x, lay, 0.37)
     oracle.set_threads(1)
     assert np.array_equal(a, b)
+
+
+# ---------------------------------------------------------------------------------------------
+# per-modality sigma schedules ([H3] "Milestone: the whole t2va path composes end to end": video
+# shift 12, audio 3): the time shift, per-modality AdaLN timesteps, the tagged Euler step
+# ---------------------------------------------------------------------------------------------
+
+def test_time_shift_closed_forms_and_group_law():
+    sig = np.linspace(0.0, 1.0, 41)
+    for s in (1.0, 3.0, 12.0):
+        assert oracle.time_shift(0.0, s) == 0.0 and oracle.time_shift(1.0, s) == 1.0
+    assert all(oracle.time_shift(float(x), 1.0) == float(x) for x in sig)  # shift 1 is the identity
+    assert oracle.time_shift(0.5, 3.0) == 0.75
+    assert abs(oracle.time_shift(0.5, 12.0) - 12.0 / 13.0) <= 1e-16
+    for s in (3.0, 12.0):  # increasing in sigma, and above the identity for s > 1
+        v = [oracle.time_shift(float(x), s) for x in sig]
+        assert all(b > a for a, b in zip(v, v[1:]))
+        assert all(vi >= float(x) for vi, x in zip(v, sig))
+    # the shifts form a group under composition: shift(shift(sigma, a), b) = shift(sigma, a b)
+    for x in sig:
+        assert abs(oracle.time_shift(oracle.time_shift(float(x), 3.0), 4.0) - oracle.time_shift(float(x), 12.0)) <= 1e-15
+
+
+def test_shifted_schedule_is_the_base_schedule_rounded_once():
+    base = synth.sigmas(50)
+    sv = oracle.sigmas_shifted(base, 12.0)
+    assert sv.dtype == np.float32 and sv[0] == 1.0 and sv[-1] == 0.0
+    assert np.array_equal(sv, np.float32([12.0 * float(b) / (1.0 + 11.0 * float(b)) for b in base]))
+
+
+def test_adaln_per_modality_rows_come_from_their_own_timestep():
+    w = _workload(TINY_RMS, 23, DOCS8)
+    W = synth.make_weights(w, bf16=False)
+    mod2, modf2 = oracle.adaln(TINY_RMS, W, [0.3, 0.8])
+    modv, modfv = oracle.adaln(TINY_RMS, W, 0.3)
+    moda, modfa = oracle.adaln(TINY_RMS, W, 0.8)
+    assert np.array_equal(mod2[:, 0], modv[:, 0]) and np.array_equal(mod2[:, 1], moda[:, 1])
+    assert np.array_equal(modf2[0], modfv[0]) and np.array_equal(modf2[1], modfa[1])
+    eq, eqf = oracle.adaln(TINY_RMS, W, [0.3, 0.3])
+    assert np.array_equal(eq, modv) and np.array_equal(eqf, modfv)
+
+
+def test_euler_tagged_is_the_scalar_step_row_by_row():
+    x = synth.normal(24, "x", (9, 16), 1.0)
+    v = synth.normal(24, "v", (9, 16), 1.0)
+    tags = np.array([0, 1, 1, 0, 0, 1, 0, 1, 0], dtype=np.uint8)
+    st, sn = np.float32([0.9, 0.7]), np.float32([0.85, 0.6])
+    got = oracle.euler_step_tagged(x, v, tags, st, sn)
+    for r in range(9):
+        assert np.array_equal(got[r], oracle.euler_step(x[r], v[r], st[tags[r]], sn[tags[r]]))
+    same = oracle.euler_step_tagged(x, v, tags, np.float32([0.9, 0.9]), np.float32([0.85, 0.85]))
+    assert np.array_equal(same, oracle.euler_step(x, v, 0.9, 0.85))
+
+
+def test_forward_per_modality_timesteps_brute_force():
+    w = _workload(TINY_RMS, 25, DOCS8)
+    lay = synth.build_layout(DOCS8)
+    W = synth.make_weights(w, bf16=False)
+    x = synth.make_tokens(w, lay)
+    out, _ = oracle.forward(TINY_RMS, W, x, lay, [0.3, 0.8])
+    ref = numpy_dit.forward(TINY_RMS, W, x, lay, [0.3, 0.8])
+    assert np.abs(out - ref).max() <= 1e-12 * np.abs(ref).max()
+    one, _ = oracle.forward(TINY_RMS, W, x, lay, 0.3)
+    same, _ = oracle.forward(TINY_RMS, W, x, lay, [0.3, 0.3])
+    assert np.array_equal(one, same)
+    assert np.abs(out - one).max() > 1e-3 * np.abs(one).max()  # the audio rows really changed
