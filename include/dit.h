@@ -167,6 +167,21 @@ DIT_API dit_status dit_forward(dit_handle* h, const float* x_tokens, const int32
                        const int32_t* doc_ids, const uint8_t* modality_tags, const double* pos_thw, int n_tokens,
                        float timestep, float* out, void* workspace, size_t workspace_bytes, void* stream);
 
+/* dit_forward with one timestep per modality.  [H3] "Milestone: the whole t2va path composes end
+ * to end": the joint loop runs separate sigma schedules for video (shift 12) and audio (shift 3),
+ * so at one Euler step the two modalities sit at different flow times.  Every AdaLN row of
+ * modality m (the per-block [m][6][d] rows and the final [m][2][d] rows) is computed from the
+ * timestep embedding of timesteps[m].
+ *   timesteps  host fp32 [n_modalities], each in [0, 1]; read before the call returns.
+ * Every other argument, layout and error is that of dit_forward; with all timesteps equal the
+ * result is bit-identical to dit_forward at that timestep.  n_modalities above 8 returns
+ * DIT_ERR_UNSUPPORTED.  A handle built without AdaLN (the fp32 forward) has no timestep input:
+ * timesteps[0] is range-checked and otherwise unused. */
+DIT_API dit_status dit_forward_modal(dit_handle* h, const float* x_tokens, const int32_t* cu_seqlens, int n_docs,
+                             const int32_t* doc_ids, const uint8_t* modality_tags, const double* pos_thw,
+                             int n_tokens, const float* timesteps, float* out, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
 /* The same forward from HOST buffers: copies the inputs in (cudaMemcpyAsync, one per array),
  * runs dit_forward and copies `out_host` back, all on `stream`, then synchronises the stream.
  * Use pinned host memory for full copy speed.  workspace must hold
@@ -184,6 +199,23 @@ DIT_API dit_status dit_forward_host(dit_handle* h, const float* x_host, const in
  * x, v: fp32 [n] device.  sigma must be > 0.  Bit-identical to the same IEEE fp32 sequence on a
  * CPU.  Stateless: resuming a loop at step k with the saved x gives the uninterrupted result. */
 DIT_API dit_status dit_euler_step(float* x, const float* v, int64_t n, float sigma, float sigma_next, void* stream);
+
+/* dit_euler_step with each token's own modality schedule: row r of x [n_tokens][d] takes the
+ * pair (sigma[tags[r]], sigma_next[tags[r]]) and the same fp32 operation order, so every row is
+ * bit-identical to dit_euler_step on that row with that pair.  [H3] "Milestone: the whole t2va
+ * path composes end to end" (separate video and audio schedules in one packed sequence).
+ *   x, v        fp32 [n_tokens][d] device; x updated in place
+ *   tags        uint8 [n_tokens] device; a row whose tag is >= n_modalities is left unchanged
+ *   sigma, sigma_next  HOST fp32 [n_modalities]; every sigma must be > 0
+ *   n_modalities in [1, 8].  Returns DIT_ERR_INVALID_ARG on a bad argument, before any launch. */
+DIT_API dit_status dit_euler_step_modal(float* x, const float* v, int n_tokens, int d, const uint8_t* tags,
+                                const float* sigma, const float* sigma_next, int n_modalities, void* stream);
+
+/* The rectified-flow time shift of one sigma, s * sigma / (1 + (s - 1) * sigma), evaluated in
+ * double and rounded to fp32.  [H3] "Milestone: the whole t2va path composes end to end" names
+ * the shifts (video 12, audio 3); the pages give no formula, and this is the usual one for
+ * sigma in [0, 1] (shift 1 is the identity; sigma 0 and 1 are fixed points).  Host only. */
+DIT_API float dit_time_shift(float sigma, float shift);
 
 /* Counters (asserted by the tests) and the device status word.  dit_sync_status synchronises
  * `stream`, reads the status word of `workspace` (the one the last forward used) and returns it

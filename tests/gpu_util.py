@@ -17,6 +17,10 @@ def dev_f32(a: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
 
 
+def dev_u8(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint8)).cuda()
+
+
 def dev_layout(lay: dict) -> dict:
     return dict(cu=torch.from_numpy(lay["cu_seqlens"].astype(np.int32)).cuda(),
                 ids=torch.from_numpy(lay["doc_ids"].astype(np.int32)).cuda(),
@@ -58,7 +62,8 @@ def workspace(h: dit.Dit, n_tokens: int, n_docs: int, host: bool = False, poison
 
 
 def run_forward(w: dict, dumps: bool = False, layout=None, weights=None, x=None, t=None, handle=None):
-    """One forward of workload ``w`` (seeded inputs unless given).  Returns numpy results."""
+    """One forward of workload ``w`` (seeded inputs unless given).  ``t`` may be one flow time or a
+    sequence with one per modality (the per-modality forward).  Returns numpy results."""
     lay = layout or synth.build_layout(w["docs"])
     W = weights or synth.make_weights(w)
     xin = synth.make_tokens(w, lay) if x is None else x
@@ -73,7 +78,10 @@ def run_forward(w: dict, dumps: bool = False, layout=None, weights=None, x=None,
     if dumps:
         dump = torch.empty((m["n_blocks"], lay["n_tokens"], m["hidden"]), dtype=torch.float32, device="cuda")
         h.set_dump(dump)
-    h.forward(xd, dl["cu"], dl["ids"], dl["tags"], dl["pos"], tt, out, ws)
+    if np.ndim(tt) == 0:
+        h.forward(xd, dl["cu"], dl["ids"], dl["tags"], dl["pos"], tt, out, ws)
+    else:  # one flow time per modality
+        h.forward_modal(xd, dl["cu"], dl["ids"], dl["tags"], dl["pos"], list(tt), out, ws)
     st = h.sync_status(ws)
     torch.cuda.synchronize()
     if dumps:

@@ -39,6 +39,64 @@ def test_forward_matches_oracle(name):
     check_against_oracle(w, run, ref, dumps)
 
 
+def _modal_t(seed):
+    """Two different fp32 flow times (video, audio) drawn from the workload's seed."""
+    u = synth.uniform(seed, "modal timesteps", 2)
+    return [float(np.float32(u[0])), float(np.float32(0.5 * u[1]))]
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged"])
+def test_forward_modal_matches_oracle(name):
+    """Video and audio at different flow times: every AdaLN row takes its own modality's timestep."""
+    gu = _gu()
+    w = synth.WORKLOADS[name]
+    t = _modal_t(w["seed"] + 7)
+    assert t[0] != t[1]
+    run = gu.run_forward(w, dumps=True, t=t)
+    assert run["status"] == 0
+    oracle.set_threads(8)
+    ref, dumps = oracle.forward(w["model"], run["weights"], run["x"], run["layout"], t, dumps=True)
+    oracle.set_threads(1)
+    check_against_oracle(w, run, ref, dumps)
+    # Against the single-t forward at the video time: documents without audio never read an audio
+    # AdaLN row and stay bit-identical; the audio rows differ.
+    lay = run["layout"]
+    one = gu.run_forward(w, layout=lay, weights=run["weights"], x=run["x"], t=t[0], handle=run["handle"])
+    audio = lay["tags"] == 1
+    has_audio = np.bincount(lay["doc_ids"][audio], minlength=lay["n_docs"]) > 0
+    video_only = ~has_audio[lay["doc_ids"]]
+    assert video_only.any() and audio.any()
+    assert np.array_equal(one["out"][video_only].view(np.uint64), run["out"][video_only].view(np.uint64))
+    assert not np.array_equal(one["out"][audio], run["out"][audio])
+
+
+def test_forward_modal_equal_timesteps_is_forward():
+    """All modalities at one t: bit-identical to dit_forward at that t."""
+    gu = _gu()
+    w = synth.WORKLOADS["ragged"]
+    t = synth.timestep(w)
+    r1 = gu.run_forward(w)
+    r2 = gu.run_forward(w, layout=r1["layout"], weights=r1["weights"], x=r1["x"], t=[t, t], handle=r1["handle"])
+    assert np.array_equal(r1["out"].view(np.uint64), r2["out"].view(np.uint64))
+
+
+def test_forward_modal_rejects_bad_timesteps():
+    dit, gu = _dit(), _gu()
+    w = synth.WORKLOADS["tiny"]
+    run = gu.run_forward(w)
+    h, lay = run["handle"], run["layout"]
+    dl = gu.dev_layout(lay)
+    x = gu.dev_f32(run["x"])
+    out = torch.full_like(x, 3.0)
+    ws = gu.workspace(h, lay["n_tokens"], lay["n_docs"])
+    for bad in ([0.5, 1.5], [-0.1, 0.5], [float("nan"), 0.5]):
+        with pytest.raises(dit.DitError) as e:
+            h.forward_modal(x, dl["cu"], dl["ids"], dl["tags"], dl["pos"], bad, out, ws)
+        assert e.value.status == dit.DIT_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert (out == 3.0).all()
+
+
 def test_forward_counters_and_tiles():
     """The CUDA path ran: launch counters and the device tile count are asserted, not printed."""
     gu = _gu()
@@ -210,6 +268,47 @@ def test_denoise_loop_matches_oracle_reduced():
     # Each step moves x by (sigma_next - sigma) * v, and the steps' sigma decrements sum to 1, so the
     # loop inherits the per-forward bound on v's scale (the initial noise's RMS); the final x itself
     # nearly cancels (x0 - sum dsigma v) and is no scale to measure against.
+    rms_v = np.sqrt((x0.astype(np.float64) ** 2).mean())
+    assert np.abs(xg.astype(np.float64) - xo).max() <= GATE * rms_v
+
+
+def _gpu_loop_modal(h, lay, x0, sig_v, sig_a):
+    dit, gu = _dit(), _gu()
+    dl = gu.dev_layout(lay)
+    x = gu.dev_f32(x0)
+    v = torch.empty_like(x)
+    ws = gu.workspace(h, lay["n_tokens"], lay["n_docs"])
+    for i in range(len(sig_v) - 1):
+        h.forward_modal(x, dl["cu"], dl["ids"], dl["tags"], dl["pos"], [sig_v[i], sig_a[i]], v, ws)
+        dit.euler_step_modal(x, v, dl["tags"], [sig_v[i], sig_a[i]], [sig_v[i + 1], sig_a[i + 1]])
+    assert h.sync_status(ws) == 0
+    return x.cpu().numpy()
+
+
+@pytest.mark.slow
+def test_denoise_loop_shifted_modal_schedules_match_oracle():
+    """The joint loop with separate schedules: video sigmas shifted by 12, audio by 3 (tag 0 = video,
+    1 = audio), each forward at the pair (sigma_v, sigma_a) and each token stepped on its own
+    modality's pair; 50 steps on the GPU against the same 50 in the oracle."""
+    dit, gu = _dit(), _gu()
+    w = LOOP_SMALL
+    lay = synth.build_layout(w["docs"])
+    W = synth.make_weights(w)
+    x0 = synth.make_tokens(w, lay)
+    base = synth.sigmas(50)
+    sv = np.array([dit.time_shift(float(s), 12.0) for s in base], dtype=np.float32)
+    sa = np.array([dit.time_shift(float(s), 3.0) for s in base], dtype=np.float32)
+    assert np.array_equal(sv.view(np.uint32), oracle.sigmas_shifted(base, 12.0).view(np.uint32))
+    assert np.array_equal(sa.view(np.uint32), oracle.sigmas_shifted(base, 3.0).view(np.uint32))
+    h = gu.make_handle(w["model"], lay, W)
+    xg = _gpu_loop_modal(h, lay, x0, [float(a) for a in sv], [float(a) for a in sa])
+    oracle.set_threads(8)
+    xo = x0.copy()
+    for i in range(50):
+        v, _ = oracle.forward(w["model"], W, xo, lay, [float(sv[i]), float(sa[i])])
+        xo = oracle.euler_step_tagged(xo, v.astype(np.float32), lay["tags"], [sv[i], sa[i]], [sv[i + 1], sa[i + 1]])
+    oracle.set_threads(1)
+    # the same bound as the single-schedule loop: each modality's decrements still sum to 1
     rms_v = np.sqrt((x0.astype(np.float64) ** 2).mean())
     assert np.abs(xg.astype(np.float64) - xo).max() <= GATE * rms_v
 

@@ -384,6 +384,47 @@ def test_euler_step_bit_exact(n):
         assert np.array_equal(xd.cpu().numpy().view(np.uint32), ref.view(np.uint32))
 
 
+@pytest.mark.parametrize("n_tokens,d,n_mod", [(1, 1, 1), (1001, 7, 3), (4096, 256, 2), (17, 3072, 8)])
+def test_euler_step_modal_bit_exact(n_tokens, d, n_mod):
+    """Each row stepped with its own modality's sigma pair, bit for bit the oracle's fp32 sequence;
+    rows whose tag is out of range are left as they were."""
+    dit, gu = _dit(), _gu()
+    x = synth.normal(102, "x", (n_tokens, d), 1.0)
+    v = synth.normal(102, "v", (n_tokens, d), 1.0)
+    tags = (synth.uniform(102, "tags", n_tokens) * (n_mod + 1)).astype(np.uint8)  # includes tag n_mod
+    base = synth.sigmas(50)
+    shifts = [1.0, 12.0, 3.0, 0.5, 2.0, 7.0, 1.5, 4.0][:n_mod]
+    for i in (0, 31, 49):
+        sg = [float(oracle.sigmas_shifted(base[i:i + 2], s)[0]) for s in shifts]
+        sn = [float(oracle.sigmas_shifted(base[i:i + 2], s)[1]) for s in shifts]
+        xd = gu.dev_f32(x)
+        dit.euler_step_modal(xd, gu.dev_f32(v), gu.dev_u8(tags), sg, sn)
+        got = xd.cpu().numpy()
+        ok = tags < n_mod
+        ref = oracle.euler_step_tagged(x[ok], v[ok], tags[ok], sg, sn)
+        assert np.array_equal(got[ok].view(np.uint32), ref.view(np.uint32))
+        assert np.array_equal(got[~ok].view(np.uint32), x[~ok].view(np.uint32))
+
+
+def test_euler_step_modal_rejects_bad_arguments():
+    dit, gu = _dit(), _gu()
+    xd = gu.dev_f32(np.ones((4, 8), dtype=np.float32))
+    tags = gu.dev_u8(np.zeros(4, dtype=np.uint8))
+    for sg, sn in (([0.0], [0.0]), ([0.5] * 9, [0.4] * 9), ([], [])):
+        with pytest.raises(dit.DitError):
+            dit.euler_step_modal(xd, xd, tags, sg, sn)
+    assert (xd == 1.0).all()
+
+
+def test_time_shift_matches_oracle():
+    """dit_time_shift on the fp32 base schedule gives the oracle's shifted schedule bit for bit."""
+    dit = _dit()
+    base = synth.sigmas(50)
+    for shift in (1.0, 3.0, 12.0, 0.25, 5.5):
+        got = np.array([dit.time_shift(float(s), shift) for s in base], dtype=np.float32)
+        assert np.array_equal(got.view(np.uint32), oracle.sigmas_shifted(base, shift).view(np.uint32)), shift
+
+
 def test_euler_unaligned_view_bit_exact():
     dit, gu = _dit(), _gu()
     x = synth.normal(101, "x", (1001,), 1.0)

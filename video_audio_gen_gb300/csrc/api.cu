@@ -620,9 +620,11 @@ dit_status dit_bind_weights(dit_handle* h, const dit_weights* w, void* stream) {
   return DIT_OK;
 }
 
-dit_status dit_forward(dit_handle* h, const float* x_tokens, const int32_t* cu_seqlens, int n_docs,
-                       const int32_t* doc_ids, const uint8_t* modality_tags, const double* pos_thw, int n_tokens,
-                       float timestep, float* out, void* workspace, size_t workspace_bytes, void* stream) {
+// The forward with its AdaLN timesteps: n_t = 1 (every modality at t[0]) or n_t = n_modalities.
+static dit_status forward_impl(dit_handle* h, const float* x_tokens, const int32_t* cu_seqlens, int n_docs,
+                               const int32_t* doc_ids, const uint8_t* modality_tags, const double* pos_thw,
+                               int n_tokens, const float* t_in, int n_t, float* out, void* workspace,
+                               size_t workspace_bytes, void* stream) {
   if (!h) return DIT_ERR_INVALID_ARG;
   if (!h->bound) return set_err(h, DIT_ERR_UNBOUND, "dit_forward before dit_bind_weights");
   const dit_config& c = h->cfg;
@@ -639,7 +641,8 @@ dit_status dit_forward(dit_handle* h, const float* x_tokens, const int32_t* cu_s
   const WsLayout L = ws_layout(&c, n_tokens, n_docs);
   if (workspace_bytes < L.total)
     return set_err(h, DIT_ERR_CAPACITY, "workspace %zu bytes < required %zu", workspace_bytes, L.total);
-  if (!(timestep >= 0.f && timestep <= 1.f)) return set_err(h, DIT_ERR_INVALID_ARG, "timestep must be in [0, 1]");
+  for (int i = 0; i < n_t; ++i)
+    if (!(t_in[i] >= 0.f && t_in[i] <= 1.f)) return set_err(h, DIT_ERR_INVALID_ARG, "timestep must be in [0, 1]");
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (c.dtype == DIT_FP32)
@@ -676,7 +679,14 @@ dit_status dit_forward(dit_handle* h, const float* x_tokens, const int32_t* cu_s
   }
   {
     Launch ln(h, s, 6);
-    DIT_CK(h, adaln_launch(h->w_ada_all, h->b_ada_all, h->ada_rows, c.t_embed_dim, timestep, mod, status, s), "adaln");
+    AdaTimesteps ts{};
+    ts.n_t = n_t;
+    for (int i = 0; i < n_t; ++i) ts.t[i] = t_in[i];
+    ts.six_d = 6 * d;
+    ts.two_d = 2 * d;
+    ts.mod_block = nm * 6 * d;
+    ts.block_rows = c.n_blocks * nm * 6 * d;
+    DIT_CK(h, adaln_launch(h->w_ada_all, h->b_ada_all, h->ada_rows, c.t_embed_dim, ts, mod, status, s), "adaln");
     ln.done();
   }
   DIT_CK(h, cudaMemcpyAsync(resid, x_tokens, (size_t)N * d * 4, cudaMemcpyDeviceToDevice, s), "copy x");
@@ -763,6 +773,26 @@ dit_status dit_forward(dit_handle* h, const float* x_tokens, const int32_t* cu_s
   return DIT_OK;
 }
 
+dit_status dit_forward(dit_handle* h, const float* x_tokens, const int32_t* cu_seqlens, int n_docs,
+                       const int32_t* doc_ids, const uint8_t* modality_tags, const double* pos_thw, int n_tokens,
+                       float timestep, float* out, void* workspace, size_t workspace_bytes, void* stream) {
+  return forward_impl(h, x_tokens, cu_seqlens, n_docs, doc_ids, modality_tags, pos_thw, n_tokens, &timestep, 1, out,
+                      workspace, workspace_bytes, stream);
+}
+
+dit_status dit_forward_modal(dit_handle* h, const float* x_tokens, const int32_t* cu_seqlens, int n_docs,
+                             const int32_t* doc_ids, const uint8_t* modality_tags, const double* pos_thw, int n_tokens,
+                             const float* timesteps, float* out, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  if (!h) return DIT_ERR_INVALID_ARG;
+  if (!timesteps) return set_err(h, DIT_ERR_INVALID_ARG, "timesteps is NULL");
+  const int nm = h->cfg.adaln ? h->cfg.n_modalities : 1;
+  if (nm > kMaxModalTimesteps)
+    return set_err(h, DIT_ERR_UNSUPPORTED, "per-modality timesteps support up to %d modalities", kMaxModalTimesteps);
+  return forward_impl(h, x_tokens, cu_seqlens, n_docs, doc_ids, modality_tags, pos_thw, n_tokens, timesteps, nm, out,
+                      workspace, workspace_bytes, stream);
+}
+
 size_t dit_workspace_bytes_host(const dit_config* cfg, int n_tokens, int n_docs) {
   size_t base = dit_workspace_bytes(cfg, n_tokens, n_docs);
   if (!base) return 0;
@@ -811,6 +841,27 @@ dit_status dit_euler_step(float* x, const float* v, int64_t n, float sigma, floa
   if (!(sigma > 0.f)) return set_err(nullptr, DIT_ERR_INVALID_ARG, "sigma must be > 0");
   cudaError_t e = euler_launch(x, v, n, sigma, sigma_next, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? DIT_OK : cuda_err(nullptr, e, "euler");
+}
+
+dit_status dit_euler_step_modal(float* x, const float* v, int n_tokens, int d, const uint8_t* tags,
+                                const float* sigma, const float* sigma_next, int n_modalities, void* stream) {
+  if (n_tokens < 0 || d < 1 || (n_tokens > 0 && (!x || !v || !tags)) || !sigma || !sigma_next || n_modalities < 1 ||
+      n_modalities > kMaxModalTimesteps)
+    return set_err(nullptr, DIT_ERR_INVALID_ARG, "bad tagged euler arguments");
+  ModalSigmas sg{};
+  sg.n = n_modalities;
+  for (int m = 0; m < n_modalities; ++m) {
+    if (!(sigma[m] > 0.f)) return set_err(nullptr, DIT_ERR_INVALID_ARG, "sigma must be > 0");
+    sg.sigma[m] = sigma[m];
+    sg.sigma_next[m] = sigma_next[m];
+  }
+  cudaError_t e = euler_tagged_launch(x, v, n_tokens, d, tags, sg, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DIT_OK : cuda_err(nullptr, e, "euler tagged");
+}
+
+float dit_time_shift(float sigma, float shift) {
+  const double s = (double)shift, x = (double)sigma;
+  return (float)(s * x / (1.0 + (s - 1.0) * x));
 }
 
 dit_status dit_get_stats(const dit_handle* h, dit_stats* out) {
@@ -912,7 +963,10 @@ dit_status dit_op_rope_cache(const double* pos, int n, int n_axes, const int* di
 dit_status dit_op_adaln(const void* w, const float* b, int rows, int t_dim, float t, float* mod, void* stream) {
   if (rows < 0 || !w || !mod || t_dim < 8 || t_dim % 8 || (t_dim > 256 && t_dim % 256) || !aligned16(w))
     return set_err(nullptr, DIT_ERR_INVALID_ARG, "bad adaln arguments");
-  cudaError_t e = adaln_launch(w, b, rows, t_dim, t, mod, nullptr, static_cast<cudaStream_t>(stream));
+  AdaTimesteps ts{};
+  ts.n_t = 1;
+  ts.t[0] = t;
+  cudaError_t e = adaln_launch(w, b, rows, t_dim, ts, mod, nullptr, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? DIT_OK : cuda_err(nullptr, e, "adaln");
 }
 

@@ -221,23 +221,31 @@ __global__ void rope_cache_kernel(const double* __restrict__ pos, int n, int hal
 // mod[r] = W[r] . silu(e) + b[r], one warp per row, fp32 accumulation.
 // ---------------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) adaln_kernel(const __nv_bfloat16* __restrict__ w, const float* __restrict__ b,
-                                                    int rows, int t_dim, float t, float* __restrict__ mod,
+                                                    int rows, int t_dim, const AdaTimesteps ts, float* __restrict__ mod,
                                                     const int* status) {
   if (status && (*reinterpret_cast<const volatile int*>(status) & kDevLayout)) return;
-  extern __shared__ float se[];
+  extern __shared__ float se[];  // [n_t][t_dim]: silu(embedding) of each timestep
   const int half = t_dim / 2;
-  for (int k = threadIdx.x; k < half; k += blockDim.x) {
+  for (int e = threadIdx.x; e < ts.n_t * half; e += blockDim.x) {
+    const int m = e / half, k = e - m * half;
     const double f = exp(-log(10000.0) * (double)k / (double)half);
-    const double a = 1000.0 * (double)t * f;
+    const double a = 1000.0 * (double)ts.t[m] * f;
     const double ec = cos(a), es = sin(a);
-    se[k] = (float)(ec / (1.0 + exp(-ec)));
-    se[half + k] = (float)(es / (1.0 + exp(-es)));
+    se[m * t_dim + k] = (float)(ec / (1.0 + exp(-ec)));
+    se[m * t_dim + half + k] = (float)(es / (1.0 + exp(-es)));
   }
   __syncthreads();
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += warps) {
     const __nv_bfloat16* wr = w + (size_t)r * t_dim;
+    // the modality of row r: blocks' rows are [n_mod][6d] per block, the final rows [n_mod][2d]
+    int m = 0;
+    if (ts.n_t > 1) {
+      m = r < ts.block_rows ? (r % ts.mod_block) / ts.six_d : (r - ts.block_rows) / ts.two_d;
+      m = m < ts.n_t ? m : ts.n_t - 1;
+    }
+    const float* sm = se + m * t_dim;
     float acc = 0.f;
     for (int k0 = lane * 8; k0 < t_dim; k0 += 256) {
       const uint4 raw = *reinterpret_cast<const uint4*>(wr + k0);
@@ -245,8 +253,8 @@ __global__ void __launch_bounds__(256) adaln_kernel(const __nv_bfloat16* __restr
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const float2 f = __bfloat1622float2(p[q]);
-        acc = fmaf(f.x, se[k0 + 2 * q], acc);
-        acc = fmaf(f.y, se[k0 + 2 * q + 1], acc);
+        acc = fmaf(f.x, sm[k0 + 2 * q], acc);
+        acc = fmaf(f.y, sm[k0 + 2 * q + 1], acc);
       }
     }
     acc = warp_sum(acc);
@@ -286,6 +294,18 @@ __global__ void euler_kernel_scalar(float* __restrict__ x, const float* __restri
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += stride)
     x[i] = euler_one(x[i], v[i], s, sn);
+}
+
+// Euler step with each row's modality sigma pair: row r of x [n_tokens, d] uses
+// (sigma[tags[r]], sigma_next[tags[r]]); the same fp32 operations as euler_one.
+__global__ void euler_tagged_kernel(float* __restrict__ x, const float* __restrict__ v, int n_tokens, int d,
+                                    const uint8_t* __restrict__ tags, const ModalSigmas sg) {
+  const long long n = (long long)n_tokens * d;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += stride) {
+    const int m = tags[i / d];
+    if (m < sg.n) x[i] = euler_one(x[i], v[i], sg.sigma[m], sg.sigma_next[m]);
+  }
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -415,14 +435,16 @@ cudaError_t rope_cache_launch(const double* pos, int n, int n_axes, const int* d
   return cudaGetLastError();
 }
 
-cudaError_t adaln_launch(const void* w, const float* b, int rows, int t_dim, float t, float* mod, const int* status,
-                         cudaStream_t s) {
+cudaError_t adaln_launch(const void* w, const float* b, int rows, int t_dim, const AdaTimesteps& ts, float* mod,
+                         const int* status, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
+  if (ts.n_t < 1 || ts.n_t > kMaxModalTimesteps) return cudaErrorInvalidValue;
+  if ((size_t)ts.n_t * t_dim * sizeof(float) > 48 * 1024) return cudaErrorInvalidValue;  // static smem budget
   const int warps_per_block = 8;
   int blocks = (rows + warps_per_block - 1) / warps_per_block;
   if (blocks > num_sms() * 8) blocks = num_sms() * 8;
-  adaln_kernel<<<blocks, 32 * warps_per_block, t_dim * sizeof(float), s>>>(
-      static_cast<const __nv_bfloat16*>(w), b, rows, t_dim, t, mod, status);
+  adaln_kernel<<<blocks, 32 * warps_per_block, ts.n_t * t_dim * sizeof(float), s>>>(
+      static_cast<const __nv_bfloat16*>(w), b, rows, t_dim, ts, mod, status);
   return cudaGetLastError();
 }
 
@@ -433,6 +455,14 @@ cudaError_t euler_launch(float* x, const float* v, long long n, float sigma, flo
     euler_kernel<<<grid_for(n / 4 + 1, 256), 256, 0, s>>>(x, v, n, sigma, sigma_next);
   else
     euler_kernel_scalar<<<grid_for(n, 256), 256, 0, s>>>(x, v, n, sigma, sigma_next);
+  return cudaGetLastError();
+}
+
+cudaError_t euler_tagged_launch(float* x, const float* v, int n_tokens, int d, const uint8_t* tags,
+                                const ModalSigmas& sg, cudaStream_t s) {
+  const long long n = (long long)n_tokens * d;
+  if (n <= 0) return cudaSuccess;
+  euler_tagged_kernel<<<grid_for(n, 256), 256, 0, s>>>(x, v, n_tokens, d, tags, sg);
   return cudaGetLastError();
 }
 

@@ -82,8 +82,25 @@ cudaError_t norm_modulate_launch(const float* x, const float* x_lo, int n, int d
                                  long long mod_stride, void* y, int out_kind, const int* status, cudaStream_t s);
 cudaError_t rope_cache_launch(const double* pos, int n, int n_axes, const int* dims, double base, float* cos_out,
                               float* sin_out, const int* status, cudaStream_t s);
-cudaError_t adaln_launch(const void* w, const float* b, int rows, int t_dim, float t, float* mod, const int* status,
-                         cudaStream_t s);
+// Timesteps of the AdaLN conditioning: one for every row (n_t = 1), or one per modality (n_t =
+// n_mod <= kMaxModalTimesteps), the row's modality following the concatenated layout: L blocks of
+// [n_mod][6d] rows (mod_block = n_mod * 6d rows each, block_rows = L * mod_block in all), then the
+// final [n_mod][2d].
+constexpr int kMaxModalTimesteps = 8;
+struct AdaTimesteps {
+  float t[kMaxModalTimesteps];
+  int n_t, six_d, two_d, mod_block, block_rows;
+};
+cudaError_t adaln_launch(const void* w, const float* b, int rows, int t_dim, const AdaTimesteps& ts, float* mod,
+                         const int* status, cudaStream_t s);
+// Per-modality sigma pairs of the tagged Euler step (n_mod <= kMaxModalTimesteps).
+struct ModalSigmas {
+  float sigma[kMaxModalTimesteps];
+  float sigma_next[kMaxModalTimesteps];
+  int n;  // pairs in use; a row whose tag is >= n is left unchanged
+};
+cudaError_t euler_tagged_launch(float* x, const float* v, int n_tokens, int d, const uint8_t* tags,
+                                const ModalSigmas& sg, cudaStream_t s);
 cudaError_t euler_launch(float* x, const float* v, long long n, float sigma, float sigma_next, cudaStream_t s);
 cudaError_t pack_ffn_in_launch(const void* w_in, const float* b_in, int F, int d, void* w_packed, float* b_packed,
                                cudaStream_t s);

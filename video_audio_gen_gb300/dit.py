@@ -22,7 +22,8 @@ DIT_BF16, DIT_FP32 = 0, 1
 KERNEL_KINDS = ["gemm_qkv", "attention", "gemm_out", "gemm_ffn_up", "gemm_ffn_down", "norm_modulate", "other"]
 
 EXPORTS = ["dit_create", "dit_destroy", "dit_last_error", "dit_workspace_bytes", "dit_bind_weights", "dit_forward",
-           "dit_workspace_bytes_host", "dit_forward_host", "dit_euler_step", "dit_get_stats", "dit_sync_status",
+           "dit_forward_modal", "dit_workspace_bytes_host", "dit_forward_host", "dit_euler_step",
+           "dit_euler_step_modal", "dit_time_shift", "dit_get_stats", "dit_sync_status",
            "dit_set_dump", "dit_set_kernel_timing", "dit_get_kernel_times", "dit_op_norm_modulate",
            "dit_op_rope_cache", "dit_op_adaln", "dit_op_gemm", "dit_op_gemm_qkv_rope", "dit_op_gemm_gated_residual",
            "dit_op_gemm_swiglu", "dit_gemm_f32_workspace_bytes", "dit_op_gemm_f32", "dit_op_pack_ffn_in", "dit_attention_workspace_bytes", "dit_op_attention",
@@ -90,7 +91,12 @@ def lib():
             "dit_bind_weights": (i32, [vp, ctypes.POINTER(DitWeights), vp]),
             "dit_forward": (i32, [vp, vp, vp, i32, vp, vp, vp, i32, f32, vp, vp, sz, vp]),
             "dit_forward_host": (i32, [vp, vp, vp, i32, vp, vp, vp, i32, f32, vp, vp, sz, vp]),
+            "dit_forward_modal": (i32, [vp, vp, vp, i32, vp, vp, vp, i32, ctypes.POINTER(ctypes.c_float), vp, vp,
+                                        sz, vp]),
             "dit_euler_step": (i32, [vp, vp, i64, f32, f32, vp]),
+            "dit_euler_step_modal": (i32, [vp, vp, i32, i32, vp, ctypes.POINTER(ctypes.c_float),
+                                           ctypes.POINTER(ctypes.c_float), i32, vp]),
+            "dit_time_shift": (f32, [f32, f32]),
             "dit_get_stats": (i32, [vp, ctypes.POINTER(DitStats)]),
             "dit_sync_status": (i32, [vp, vp, vp]),
             "dit_set_dump": (i32, [vp, vp]),
@@ -202,6 +208,15 @@ class Dit:
                                  n_tokens, float(t), _ptr(out), _ptr(workspace), workspace.numel(),
                                  _stream(stream)), self.h)
 
+    def forward_modal(self, x, cu_seqlens, doc_ids, tags, pos, ts, out, workspace, stream=None):
+        """dit_forward_modal: `ts` holds one flow time per modality (tag order)."""
+        n_docs = cu_seqlens.numel() - 1
+        n_tokens = doc_ids.numel()
+        arr = (ctypes.c_float * len(ts))(*[float(t) for t in ts])
+        _check(lib().dit_forward_modal(self.h, _ptr(x), _ptr(cu_seqlens), n_docs, _ptr(doc_ids), _ptr(tags),
+                                       _ptr(pos), n_tokens, arr, _ptr(out), _ptr(workspace), workspace.numel(),
+                                       _stream(stream)), self.h)
+
     def forward_host(self, x, cu_seqlens, doc_ids, tags, pos, t: float, out, workspace, stream=None):
         """Host (preferably pinned) CPU tensors in and out; device workspace."""
         n_docs = cu_seqlens.numel() - 1
@@ -243,6 +258,21 @@ def selftest_wait_timeout(limit_ns: int, status_word, stream=None) -> int:
 
 def euler_step(x, v, sigma: float, sigma_next: float, stream=None):
     _check(lib().dit_euler_step(_ptr(x), _ptr(v), x.numel(), float(sigma), float(sigma_next), _stream(stream)))
+
+
+def euler_step_modal(x, v, tags, sigma, sigma_next, stream=None):
+    """dit_euler_step_modal: row r of x [N, d] steps with (sigma[tags[r]], sigma_next[tags[r]])."""
+    n, d = x.shape
+    if len(sigma) != len(sigma_next):
+        raise ValueError("sigma and sigma_next differ in length")
+    st = (ctypes.c_float * len(sigma))(*[float(a) for a in sigma])
+    sn = (ctypes.c_float * len(sigma_next))(*[float(a) for a in sigma_next])
+    _check(lib().dit_euler_step_modal(_ptr(x), _ptr(v), n, d, _ptr(tags), st, sn, len(sigma), _stream(stream)))
+
+
+def time_shift(sigma: float, shift: float) -> float:
+    """dit_time_shift: shift * sigma / (1 + (shift - 1) * sigma) in double, rounded to fp32."""
+    return float(lib().dit_time_shift(float(sigma), float(shift)))
 
 
 def norm_modulate(x, norm: int, eps: float, y, out_kind: int, tags=None, shift=None, scale=None, mod_stride=0,
