@@ -61,6 +61,7 @@ def lib():
             _lib = ctypes.CDLL(build())
             _lib.orc_forward.restype = ctypes.c_int
             _lib.orc_forward_mod.restype = ctypes.c_int
+            _lib.orc_forward_latent.restype = ctypes.c_int
             _lib.orc_time_shift.restype = ctypes.c_double
             _lib.orc_check_layout.restype = ctypes.c_int
             _lib.orc_count_q_tiles.restype = ctypes.c_int
@@ -291,6 +292,72 @@ def euler_step(x, v, sigma: float, sigma_next: float) -> np.ndarray:
     v = np.ascontiguousarray(v, dtype=np.float32)
     lib().orc_euler_step(_f(x), _f(v), ctypes.c_int64(x.size), ctypes.c_float(sigma), ctypes.c_float(sigma_next))
     return x
+
+
+def patchify(lat, pt: int, ph: int, pw: int) -> np.ndarray:
+    """Latent [C, T*pt, H*ph, W*pw] -> tokens [T*H*W, C*pt*ph*pw] (exact)."""
+    lat = np.ascontiguousarray(lat, dtype=np.float32)
+    C, Tf, Hf, Wf = lat.shape
+    T, H, W = Tf // pt, Hf // ph, Wf // pw
+    assert T * pt == Tf and H * ph == Hf and W * pw == Wf
+    tok = np.empty((T * H * W, C * pt * ph * pw), dtype=np.float32)
+    lib().orc_patchify(_f(lat), C, T, H, W, pt, ph, pw, _f(tok))
+    return tok
+
+
+def unpatchify(tok, C: int, T: int, H: int, W: int, pt: int, ph: int, pw: int) -> np.ndarray:
+    """Tokens [T*H*W, C*pt*ph*pw] -> latent [C, T*pt, H*ph, W*pw] (exact)."""
+    tok = np.ascontiguousarray(tok, dtype=np.float32)
+    assert tok.shape == (T * H * W, C * pt * ph * pw)
+    lat = np.empty((C, T * pt, H * ph, W * pw), dtype=np.float32)
+    lib().orc_unpatchify(_f(tok), C, T, H, W, pt, ph, pw, _f(lat))
+    return lat
+
+
+def audio_pack(lat) -> np.ndarray:
+    """Audio latent [C, T] -> tokens [T, C]: patchify of a [C, T, 1, 1] latent with a 1x1x1 patch."""
+    lat = np.ascontiguousarray(lat, dtype=np.float32)
+    return patchify(lat.reshape(lat.shape[0], lat.shape[1], 1, 1), 1, 1, 1)
+
+
+def audio_unpack(tok) -> np.ndarray:
+    tok = np.ascontiguousarray(tok, dtype=np.float32)
+    T, C = tok.shape
+    return unpatchify(tok, C, T, 1, 1, 1, 1, 1).reshape(C, T)
+
+
+def forward_latent(m: dict, weights: dict, io: dict, z, layout: dict, t, dumps: bool = False):
+    """The forward between latent tokens: per-modality patch projection into the packed rows of that
+    modality, the forward, per-modality output heads.  io = dict(w_patch, b_patch, w_head, b_head), one
+    entry per modality; z[m] [rows_m, width_m] fp32.  Returns ([v_m float64], dumps or None)."""
+    c = config(m)
+    w = _Weights(m, weights)
+    n_mod = len(z)
+    n = layout["n_tokens"]
+    zs = [np.ascontiguousarray(a, dtype=np.float32) for a in z]
+    wp = [np.ascontiguousarray(a, dtype=np.float32) for a in io["w_patch"]]
+    wh = [np.ascontiguousarray(a, dtype=np.float32) for a in io["w_head"]]
+    bp = [None if a is None else np.ascontiguousarray(a, dtype=np.float32) for a in io["b_patch"]]
+    bh = [None if a is None else np.ascontiguousarray(a, dtype=np.float32) for a in io["b_head"]]
+    widths = [a.shape[1] for a in zs]
+    vs = [np.empty((a.shape[0], widths[i]), dtype=np.float64) for i, a in enumerate(zs)]
+    FP = _c_fp * n_mod
+    DP = _c_dp * n_mod
+    IA = ctypes.c_int * n_mod
+    opt = lambda a: _f(a) if a is not None else None
+    tm = np.ascontiguousarray([t] * n_mod if np.ndim(t) == 0 else t, dtype=np.float64)
+    dm = np.empty((m["n_blocks"], n, m["hidden"]), dtype=np.float64) if dumps else None
+    rc = lib().orc_forward_latent(
+        ctypes.byref(c), ctypes.byref(w.w), ctypes.c_int(n_mod), FP(*[_f(a) for a in zs]),
+        IA(*[a.shape[0] for a in zs]), IA(*widths), FP(*[_f(a) for a in wp]), FP(*[opt(a) for a in bp]),
+        FP(*[_f(a) for a in wh]), FP(*[opt(a) for a in bh]), ctypes.c_int(n),
+        _p(np.ascontiguousarray(layout["cu_seqlens"], dtype=np.int32)), ctypes.c_int(layout["n_docs"]),
+        _p(np.ascontiguousarray(layout["doc_ids"], dtype=np.int32)),
+        _p(np.ascontiguousarray(layout["tags"], dtype=np.uint8)), _d(_dbl(layout["pos"])), _d(tm),
+        DP(*[_d(a) for a in vs]), _d(dm) if dumps else None)
+    if rc:
+        raise ValueError(f"oracle: invalid packed layout (code {rc})")
+    return vs, dm
 
 
 def euler_step_tagged(x, v, tags, sigma, sigma_next) -> np.ndarray:

@@ -412,6 +412,51 @@ void orc_euler_step_tagged(float* x, const float* v, int n_tokens, int d, const 
 }
 
 // ---------------------------------------------------------------------------------------------
+// Latent <-> token packing.  [H3] "Correctness gates": patchify / unpatchify / audio pack / unpack
+// are gated exact with a round-trip identity; [H3] "Milestone: the whole t2va path composes end to
+// end": unpatchify and audio unpack follow the denoise loop.  [H3] "Encoder complete": a patch
+// embedding whose Conv3d has kernel == stride is a plain linear over the flattened patch.
+// READING (the pages give neither the order nor the patch): a latent [C][T*pt][H*ph][W*pw] becomes
+// T*H*W tokens in (t, h, w) order, w fastest (the packed layout's order); token features are the
+// patch flattened as a Conv3d weight [d][C][pt][ph][pw] flattens, (c, a, b, e) with e fastest.
+// Audio pack is the same map on a [C][T] latent with H = W = 1 and a 1x1x1 patch: [T][C].
+// Pure index permutations; values are copied, never computed.
+// ---------------------------------------------------------------------------------------------
+void orc_patchify(const float* lat, int C, int T, int H, int W, int pt, int ph, int pw, float* tok) {
+  const int P = C * pt * ph * pw;
+  const size_t Tf = (size_t)T * pt, Hf = (size_t)H * ph, Wf = (size_t)W * pw;
+  for (int t = 0; t < T; ++t)
+    for (int h = 0; h < H; ++h)
+      for (int w = 0; w < W; ++w) {
+        float* row = tok + ((size_t)(t * H + h) * W + w) * P;
+        int f = 0;
+        for (int c = 0; c < C; ++c)
+          for (int a = 0; a < pt; ++a)
+            for (int b = 0; b < ph; ++b)
+              for (int e = 0; e < pw; ++e)
+                row[f++] = lat[(((size_t)c * Tf + (size_t)t * pt + a) * Hf + (size_t)h * ph + b) * Wf +
+                               (size_t)w * pw + e];
+      }
+}
+
+void orc_unpatchify(const float* tok, int C, int T, int H, int W, int pt, int ph, int pw, float* lat) {
+  const int P = C * pt * ph * pw;
+  const size_t Tf = (size_t)T * pt, Hf = (size_t)H * ph, Wf = (size_t)W * pw;
+  for (int t = 0; t < T; ++t)
+    for (int h = 0; h < H; ++h)
+      for (int w = 0; w < W; ++w) {
+        const float* row = tok + ((size_t)(t * H + h) * W + w) * P;
+        int f = 0;
+        for (int c = 0; c < C; ++c)
+          for (int a = 0; a < pt; ++a)
+            for (int b = 0; b < ph; ++b)
+              for (int e = 0; e < pw; ++e)
+                lat[(((size_t)c * Tf + (size_t)t * pt + a) * Hf + (size_t)h * ph + b) * Wf + (size_t)w * pw + e] =
+                    row[f++];
+      }
+}
+
+// ---------------------------------------------------------------------------------------------
 // One transformer block, in place on the fp64 residual x [N][d].  [H3] "The device-resident
 // forward (W2b)" lists the ops; with AdaLN on:
 //   y  = RMS(x) * (1 + scale1[tag]) + shift1[tag]
@@ -484,12 +529,16 @@ void orc_block_forward(const orc_config* c, const orc_block* w, const double* mo
 // dumps (may be NULL) receives the residual after each block, [L][N][d].
 // Returns the layout check's code (0 when valid).
 // ---------------------------------------------------------------------------------------------
+static void forward_core(const orc_config* c, const orc_weights* w, std::vector<double>& x, int n, const int32_t* cu,
+                         int n_docs, const uint8_t* tags, const double* pos, const double* t_mod, double* out,
+                         double* dumps);
+
 int orc_forward_mod(const orc_config* c, const orc_weights* w, const float* x_in, int n, const int32_t* cu,
                     int n_docs, const int32_t* doc_ids, const uint8_t* tags, const double* pos, const double* t_mod,
                     double* out, double* dumps) {
   int rc = orc_check_layout(cu, n_docs, doc_ids, tags, n, c->adaln ? c->n_mod : 1);
   if (rc) return rc;
-  int d = c->hidden, half = c->rotary_dim / 2;
+  int d = c->hidden;
   std::vector<double> x((size_t)n * d);
   if (c->io_channels > 0) {
     int ci = c->io_channels;
@@ -504,6 +553,15 @@ int orc_forward_mod(const orc_config* c, const orc_weights* w, const float* x_in
   } else {
     for (size_t e = 0; e < x.size(); ++e) x[e] = (double)x_in[e];
   }
+  forward_core(c, w, x, n, cu, n_docs, tags, pos, t_mod, out, dumps);
+  return 0;
+}
+
+// The forward from the residual x [N][d] (already embedded) to the final layer's output.
+static void forward_core(const orc_config* c, const orc_weights* w, std::vector<double>& x, int n, const int32_t* cu,
+                         int n_docs, const uint8_t* tags, const double* pos, const double* t_mod, double* out,
+                         double* dumps) {
+  int d = c->hidden, half = c->rotary_dim / 2;
   std::vector<double> cs((size_t)n * half), sn((size_t)n * half);
   orc_rope_cos_sin(c, pos, n, cs.data(), sn.data());
   std::vector<double> mod, modf;
@@ -537,7 +595,6 @@ int orc_forward_mod(const orc_config* c, const orc_weights* w, const float* x_in
       memcpy(out, nrm.data(), sizeof(double) * nrm.size());
     }
   }
-  return 0;
 }
 
 int orc_forward(const orc_config* c, const orc_weights* w, const float* x_in, int n, const int32_t* cu, int n_docs,
@@ -545,6 +602,48 @@ int orc_forward(const orc_config* c, const orc_weights* w, const float* x_in, in
                 double* dumps) {
   std::vector<double> tm((size_t)(c->n_mod > 0 ? c->n_mod : 1), t);
   return orc_forward_mod(c, w, x_in, n, cu, n_docs, doc_ids, tags, pos, tm.data(), out, dumps);
+}
+
+// ---------------------------------------------------------------------------------------------
+// The forward between latent tokens.  [H3] "What this push adds": both patch projections and both
+// output heads stay fp32 islands around the bf16 block stream.  For each modality m the rows of
+// the packed sequence with tag m, in increasing order, are the rows of z[m] [rows_m][width[m]]:
+//   x[row]  = z[m][r] W_patch[m]^T + b_patch[m]          (W_patch[m] [d][width[m]])
+//   out     = the forward of x (blocks and the final layer)
+//   v[m][r] = out[row] W_head[m]^T + b_head[m]           (W_head[m] [width[m]][d])
+// everything in double.  n_rows[m] must equal the number of tokens tagged m (else code 8).
+// ---------------------------------------------------------------------------------------------
+int orc_forward_latent(const orc_config* c, const orc_weights* w, int n_mod, const float* const* z,
+                       const int* n_rows, const int* width, const float* const* w_patch, const float* const* b_patch,
+                       const float* const* w_head, const float* const* b_head, int n, const int32_t* cu, int n_docs,
+                       const int32_t* doc_ids, const uint8_t* tags, const double* pos, const double* t_mod,
+                       double* const* v_out, double* dumps) {
+  int rc = orc_check_layout(cu, n_docs, doc_ids, tags, n, n_mod);
+  if (rc) return rc;
+  const int d = c->hidden;
+  std::vector<std::vector<int>> rows((size_t)n_mod);
+  for (int i = 0; i < n; ++i) rows[tags[i]].push_back(i);
+  for (int m = 0; m < n_mod; ++m)
+    if ((int)rows[m].size() != n_rows[m]) return 8;
+  std::vector<double> x((size_t)n * d);
+  for (int m = 0; m < n_mod; ++m) {
+    const int M = n_rows[m], K = width[m];
+    if (M == 0) continue;
+    std::vector<double> zm((size_t)M * K), xm((size_t)M * d);
+    for (size_t e = 0; e < zm.size(); ++e) zm[e] = (double)z[m][e];
+    orc_linear(zm.data(), M, K, w_patch[m], b_patch[m], d, xm.data());
+    for (int r = 0; r < M; ++r) memcpy(&x[(size_t)rows[m][r] * d], &xm[(size_t)r * d], sizeof(double) * d);
+  }
+  std::vector<double> out((size_t)n * d);
+  forward_core(c, w, x, n, cu, n_docs, tags, pos, t_mod, out.data(), dumps);
+  for (int m = 0; m < n_mod; ++m) {
+    const int M = n_rows[m];
+    if (M == 0) continue;
+    std::vector<double> om((size_t)M * d);
+    for (int r = 0; r < M; ++r) memcpy(&om[(size_t)r * d], &out[(size_t)rows[m][r] * d], sizeof(double) * d);
+    orc_linear(om.data(), M, d, w_head[m], b_head[m], width[m], v_out[m]);
+  }
+  return 0;
 }
 
 }  // extern "C"

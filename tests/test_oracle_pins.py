@@ -470,3 +470,119 @@ def test_forward_per_modality_timesteps_brute_force():
     same, _ = oracle.forward(TINY_RMS, W, x, lay, [0.3, 0.3])
     assert np.array_equal(one, same)
     assert np.abs(out - one).max() > 1e-3 * np.abs(one).max()  # the audio rows really changed
+
+
+# ---------------------------------------------------------------------------------------------
+# latent <-> token packing and the fp32 islands around the block stack
+# ---------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("C,T,H,W,pt,ph,pw", [(3, 2, 3, 2, 2, 2, 2), (5, 3, 2, 4, 1, 2, 3), (2, 1, 1, 1, 1, 1, 1),
+                                              (4, 2, 5, 3, 1, 1, 1)])
+def test_patchify_is_the_reshape_transpose(C, T, H, W, pt, ph, pw):
+    """numpy's view of the same map: split each axis into (grid, patch), move the grid axes out front,
+    flatten the patch in (c, a, b, e) order."""
+    lat = synth.normal(30, "lat", (C, T * pt, H * ph, W * pw), 1.0)
+    want = lat.reshape(C, T, pt, H, ph, W, pw).transpose(1, 3, 5, 0, 2, 4, 6).reshape(T * H * W, C * pt * ph * pw)
+    got = oracle.patchify(lat, pt, ph, pw)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+def test_unpatchify_inverts_patchify_and_both_are_permutations():
+    C, T, H, W, pt, ph, pw = 3, 2, 4, 3, 1, 2, 2
+    n = C * T * pt * H * ph * W * pw
+    lat = np.arange(n, dtype=np.float32).reshape(C, T * pt, H * ph, W * pw)
+    tok = oracle.patchify(lat, pt, ph, pw)
+    assert np.array_equal(np.sort(tok.reshape(-1)), np.arange(n, dtype=np.float32))
+    assert np.array_equal(oracle.unpatchify(tok, C, T, H, W, pt, ph, pw), lat)
+    tok2 = synth.normal(31, "tok", tok.shape, 1.0)
+    back = oracle.patchify(oracle.unpatchify(tok2, C, T, H, W, pt, ph, pw), pt, ph, pw)
+    assert np.array_equal(back.view(np.uint32), tok2.view(np.uint32))
+    # token (t, h, w) holds the patch whose corner is (t*pt, h*ph, w*pw)
+    t, h, w = 1, 2, 1
+    r = (t * H + h) * W + w
+    assert tok[r, 0] == lat[0, t * pt, h * ph, w * pw]
+
+
+def test_audio_pack_is_the_transpose():
+    lat = synth.normal(32, "alat", (32, 37), 1.0)
+    tok = oracle.audio_pack(lat)
+    assert np.array_equal(tok, lat.T)
+    assert np.array_equal(oracle.audio_unpack(tok), lat)
+
+
+def test_patch_projection_is_a_strided_conv3d():
+    """Kernel == stride: a direct Conv3d loop equals the linear map on the patchified latent with the
+    conv weight flattened as [d, C*pt*ph*pw]."""
+    C, T, H, W, pt, ph, pw, d = 3, 2, 2, 3, 1, 2, 2, 5
+    lat = synth.normal(33, "lat", (C, T * pt, H * ph, W * pw), 1.0)
+    Wc = synth.normal(33, "w", (d, C, pt, ph, pw), 0.5)
+    b = synth.normal(33, "b", (d,), 0.5)
+    conv = np.zeros((d, T, H, W))
+    for o in range(d):
+        for t in range(T):
+            for h in range(H):
+                for w in range(W):
+                    acc = float(b[o])
+                    for c in range(C):
+                        for a in range(pt):
+                            for bb in range(ph):
+                                for e in range(pw):
+                                    acc += float(Wc[o, c, a, bb, e]) * float(lat[c, t * pt + a, h * ph + bb, w * pw + e])
+                    conv[o, t, h, w] = acc
+    got = oracle.linear(oracle.patchify(lat, pt, ph, pw), Wc.reshape(d, -1), b)
+    assert np.abs(got - conv.reshape(d, -1).T).max() <= 1e-13
+
+
+def _latent_io(seed, d, widths, std=0.3):
+    return dict(w_patch=[synth.normal(seed, f"wp{m}", (d, k), std) for m, k in enumerate(widths)],
+                b_patch=[synth.normal(seed, f"bp{m}", (d,), std) for m in range(len(widths))],
+                w_head=[synth.normal(seed, f"wh{m}", (k, d), std) for m, k in enumerate(widths)],
+                b_head=[synth.normal(seed, f"bh{m}", (k,), std) for m, k in enumerate(widths)])
+
+
+def test_forward_latent_brute_force():
+    """Per-modality patch projection into that modality's packed rows, the forward, per-modality
+    heads: against numpy matmuls around the independent numpy forward on 8 tokens."""
+    w = _workload(TINY_RMS, 34, DOCS8)
+    lay = synth.build_layout(DOCS8)
+    W = synth.make_weights(w, bf16=False)
+    widths = [12, 5]
+    io = _latent_io(34, TINY_RMS["hidden"], widths)
+    rows = [np.nonzero(lay["tags"] == m)[0] for m in range(2)]
+    z = [synth.normal(34, f"z{m}", (len(rows[m]), widths[m]), 1.0) for m in range(2)]
+    vs, _ = oracle.forward_latent(TINY_RMS, W, io, z, lay, [0.7, 0.2])
+    f64 = lambda a: np.asarray(a, dtype=np.float64)
+    x = np.zeros((lay["n_tokens"], TINY_RMS["hidden"]))
+    for m in range(2):
+        x[rows[m]] = f64(z[m]) @ f64(io["w_patch"][m]).T + f64(io["b_patch"][m])
+    out = numpy_dit.forward(TINY_RMS, W, x, lay, [0.7, 0.2])
+    for m in range(2):
+        ref = out[rows[m]] @ f64(io["w_head"][m]).T + f64(io["b_head"][m])
+        assert vs[m].shape == (len(rows[m]), widths[m])
+        assert np.abs(vs[m] - ref).max() <= 1e-12 * np.abs(ref).max()
+
+
+def test_forward_latent_with_identity_islands_is_the_forward():
+    """Width d, identity projections, zero biases: the latent forward is the plain forward row by row."""
+    w = _workload(TINY_RMS, 35, DOCS8)
+    lay = synth.build_layout(DOCS8)
+    W = synth.make_weights(w, bf16=False)
+    d = TINY_RMS["hidden"]
+    x = synth.make_tokens(w, lay)
+    eye = np.eye(d, dtype=np.float32)
+    io = dict(w_patch=[eye, eye], b_patch=[None, None], w_head=[eye, eye], b_head=[None, None])
+    rows = [np.nonzero(lay["tags"] == m)[0] for m in range(2)]
+    vs, _ = oracle.forward_latent(TINY_RMS, W, io, [x[rows[0]], x[rows[1]]], lay, [0.4, 0.9])
+    out, _ = oracle.forward(TINY_RMS, W, x, lay, [0.4, 0.9])
+    for m in range(2):
+        assert np.array_equal(vs[m], out[rows[m]])
+
+
+def test_forward_latent_rejects_row_counts_that_disagree_with_tags():
+    w = _workload(TINY_RMS, 36, DOCS8)
+    lay = synth.build_layout(DOCS8)
+    W = synth.make_weights(w, bf16=False)
+    io = _latent_io(36, TINY_RMS["hidden"], [4, 4])
+    z = [synth.normal(36, "z0", (5, 4), 1.0), synth.normal(36, "z1", (3, 4), 1.0)]  # tags say 6 and 2
+    with pytest.raises(ValueError, match="code 8"):
+        oracle.forward_latent(TINY_RMS, W, io, z, lay, 0.5)
