@@ -182,6 +182,75 @@ DIT_API dit_status dit_forward_modal(dit_handle* h, const float* x_tokens, const
                              int n_tokens, const float* timesteps, float* out, void* workspace,
                              size_t workspace_bytes, void* stream);
 
+/* ---------------------------------------------------------------------------------------------
+ * Latent I/O: the steps either side of the block stack.  [H3] "What this push adds": both patch
+ * projections and both output heads stay fp32 islands around the bf16 block stream.
+ * ------------------------------------------------------------------------------------------- */
+
+#define DIT_MAX_LATENT_MODALITIES 8
+
+/* Per-modality patch projection (token features -> d) and output head (d -> token features).
+ * Device pointers, fp32, row-major [out][in]; biases may be NULL (zero).
+ *   width[m]    token feature width of modality m: C*pt*ph*pw for a patchified video latent,
+ *               C for a packed audio latent (any width >= 1, at most 65536)
+ *   w_patch[m]  [d][width[m]]     b_patch[m] [d]
+ *   w_head[m]   [width[m]][d]     b_head[m]  [width[m]]
+ * dit_bind_latent_io copies the weights into the library's split (tf32 hi, lo) form, padded to
+ * the GEMM's tiles, and keeps its own copies of the biases: the caller's buffers may be freed
+ * once the call returns.  Needs a DIT_BF16 handle with adaln = 1 and n_modalities equal to the
+ * handle's (at most 8); otherwise DIT_ERR_UNSUPPORTED / DIT_ERR_INVALID_ARG.  Synchronises
+ * `stream`.  Binding again replaces the previous set. */
+typedef struct {
+  int n_modalities;
+  int width[DIT_MAX_LATENT_MODALITIES];
+  const float* w_patch[DIT_MAX_LATENT_MODALITIES];
+  const float* b_patch[DIT_MAX_LATENT_MODALITIES];
+  const float* w_head[DIT_MAX_LATENT_MODALITIES];
+  const float* b_head[DIT_MAX_LATENT_MODALITIES];
+} dit_latent_io;
+DIT_API dit_status dit_bind_latent_io(dit_handle* h, const dit_latent_io* io, void* stream);
+
+/* Workspace of dit_forward_latent (the forward's, plus the final hidden state, the row maps and
+ * the islands' GEMM scratch); 0 when no latent I/O is bound. */
+DIT_API size_t dit_workspace_bytes_latent(const dit_handle* h, int n_tokens, int n_docs);
+
+/* The forward between latent tokens, for one flow time per modality:
+ *   x[row] = z[m][r] W_patch[m]^T + b_patch[m]   for the r-th token tagged m (packed order)
+ *   out    = the forward of x (dit_forward_modal: blocks, final norm + modulate)
+ *   v[m][r] = out[row] W_head[m]^T + b_head[m]
+ * The projections and heads are fp32 GEMMs (3xTF32 on the tensor cores); the patch projection
+ * writes straight into the fp32 residual stream, the heads read the final layer's fp32 output.
+ *   z, v        HOST arrays of n_modalities DEVICE pointers: z[m] fp32 [n_rows[m]][width[m]],
+ *               v[m] fp32 [n_rows[m]][width[m]] (written); either may be NULL where n_rows[m] = 0
+ *   n_rows      HOST int [n_modalities]: the number of tokens tagged m; they must add up to
+ *               n_tokens (else DIT_ERR_INVALID_ARG).  The device checks them against the tags:
+ *               a mismatch sets the status word to DIT_ERR_LAYOUT (layout code 8) and no later
+ *               kernel of the call does work.
+ *   timesteps   HOST fp32 [n_modalities], each in [0, 1]
+ *   workspace   at least dit_workspace_bytes_latent(h, n_tokens, n_docs) bytes, 256-byte aligned
+ * The layout arguments are dit_forward's.  Asynchronous on `stream`. */
+DIT_API dit_status dit_forward_latent(dit_handle* h, const float* const* z, const int* n_rows,
+                              const int32_t* cu_seqlens, int n_docs, const int32_t* doc_ids,
+                              const uint8_t* modality_tags, const double* pos_thw, int n_tokens,
+                              const float* timesteps, float* const* v, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/* Latent <-> token packing, exact (values are moved, never computed).  [H3] "Correctness gates"
+ * (patchify / unpatchify / audio pack / unpack, exact with a round-trip identity).
+ *   latent  fp32 [C][T*pt][H*ph][W*pw] (T, H, W count patches, not latent frames or pixels)
+ *   tokens  fp32 [T*H*W][C*pt*ph*pw], token (t, h, w) at row (t*H + h)*W + w; its features are
+ *           the patch in (c, a, b, e) order, e fastest: the flattening of a Conv3d weight
+ *           [d][C][pt][ph][pw], so the patch projection with kernel == stride is a plain linear
+ *           ([H3] "Encoder complete").
+ * All sizes >= 1 and C*pt*ph*pw <= 12287; device buffers that do not overlap.  The audio forms
+ * move a [C][T] latent to [T][C] tokens and back (a 1x1x1 patch on an H = W = 1 latent). */
+DIT_API dit_status dit_patchify(const float* latent, int C, int T, int H, int W, int pt, int ph, int pw,
+                        float* tokens, void* stream);
+DIT_API dit_status dit_unpatchify(const float* tokens, int C, int T, int H, int W, int pt, int ph, int pw,
+                          float* latent, void* stream);
+DIT_API dit_status dit_audio_pack(const float* latent, int C, int T, float* tokens, void* stream);
+DIT_API dit_status dit_audio_unpack(const float* tokens, int C, int T, float* latent, void* stream);
+
 /* The same forward from HOST buffers: copies the inputs in (cudaMemcpyAsync, one per array),
  * runs dit_forward and copies `out_host` back, all on `stream`, then synchronises the stream.
  * Use pinned host memory for full copy speed.  workspace must hold
@@ -239,8 +308,9 @@ DIT_API dit_status dit_set_dump(dit_handle* h, float* dump);
  * enable = 1 starts collecting (events are created lazily); dit_get_kernel_times synchronises and
  * returns, per kind, the summed milliseconds and launch count since the last reset.
  * Kinds: 0 gemm_qkv, 1 attention, 2 gemm_out, 3 gemm_ffn_up, 4 gemm_ffn_down, 5 norm_modulate,
- *        6 other (schedule, cos/sin cache, AdaLN, copies). */
-#define DIT_KERNEL_KINDS 7
+ *        6 other (schedule, cos/sin cache, AdaLN, copies),
+ *        7 latent_io (row maps, patch projections and output heads of dit_forward_latent). */
+#define DIT_KERNEL_KINDS 8
 DIT_API dit_status dit_set_kernel_timing(dit_handle* h, int enable);
 DIT_API dit_status dit_get_kernel_times(dit_handle* h, double* ms_out, int64_t* launches_out);
 

@@ -279,3 +279,33 @@ def make_tokens(w: dict, layout: dict, name: str = "x") -> np.ndarray:
     n = layout["n_tokens"]
     width = m["io_channels"] if m["io_channels"] else m["hidden"]
     return normal(w["seed"], name, (n, width) if not m["io_channels"] else (width * n,), w["x_std"])
+
+
+# ---------------------------------------------------------------------------------------------
+# Latent I/O recipe.  The audio latent is 32 channels wide (the DiT emits a 32-wide audio latent,
+# [H3] "Milestone: the whole t2va path composes end to end"); the pages give no video latent
+# width or patch, so the stand-in is 48 channels with a (1, 2, 2) patch: 192 features per token.
+# Tokens of each modality are rows [rows_m, width_m] in packed order; projections N(0, 1/fan_in)
+# so activations keep unit scale, biases N(0, bias_std).
+# ---------------------------------------------------------------------------------------------
+
+VIDEO_LATENT = dict(channels=48, patch=(1, 2, 2))
+AUDIO_LATENT = dict(channels=32)
+
+
+def latent_widths() -> list[int]:
+    pt, ph, pw = VIDEO_LATENT["patch"]
+    return [VIDEO_LATENT["channels"] * pt * ph * pw, AUDIO_LATENT["channels"]]
+
+
+def make_latent_io(seed: int, d: int, widths, bias_std: float = 0.02) -> dict:
+    """Per-modality fp32 patch projections [d, width] and output heads [width, d] with biases."""
+    return dict(w_patch=[normal(seed, f"w_patch{m}", (d, k), 1.0 / np.sqrt(k)) for m, k in enumerate(widths)],
+                b_patch=[normal(seed, f"b_patch{m}", (d,), bias_std) for m in range(len(widths))],
+                w_head=[normal(seed, f"w_head{m}", (k, d), 1.0 / np.sqrt(d)) for m, k in enumerate(widths)],
+                b_head=[normal(seed, f"b_head{m}", (k,), bias_std) for m, k in enumerate(widths)])
+
+
+def make_latents(seed: int, layout: dict, widths, name: str = "z") -> list:
+    """Initial noise in token form: one N(0, 1) array [rows_m, width_m] per modality."""
+    return [normal(seed, f"{name}{m}", (int((layout["tags"] == m).sum()), k), 1.0) for m, k in enumerate(widths)]

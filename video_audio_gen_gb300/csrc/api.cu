@@ -6,6 +6,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -74,6 +75,13 @@ struct dit_handle {
   float *lnf_g = nullptr, *lnf_b = nullptr, *b_pre = nullptr, *b_post = nullptr;
   const float *w_pre = nullptr, *w_post = nullptr;
   SplitW s_pre, s_post;  // fp32 path: the 1x1 convolutions' weights split for the 3xTF32 GEMM
+  // latent I/O (dit_bind_latent_io): per modality the patch projection [d][kp] and the output head
+  // [np][d] split for the 3xTF32 GEMM, zero-padded to the GEMM's K chunk and N tile
+  int lat_n = 0;
+  int lat_width[kMaxModalTimesteps] = {}, lat_kp[kMaxModalTimesteps] = {}, lat_np[kMaxModalTimesteps] = {};
+  SplitW lat_patch[kMaxModalTimesteps], lat_head[kMaxModalTimesteps];
+  float* lat_b_patch[kMaxModalTimesteps] = {};
+  float* lat_b_head[kMaxModalTimesteps] = {};
   float* dump = nullptr;
   dit_stats stats;
   bool timing = false;
@@ -620,21 +628,65 @@ dit_status dit_bind_weights(dit_handle* h, const dit_weights* w, void* stream) {
   return DIT_OK;
 }
 
+// The latent forward's inputs and scratch, resolved on the host.
+struct LatentArgs {
+  const float* const* z;  // host array of device pointers, z[m] [count[m]][width[m]]
+  ModalRows mr;           // row counts (the caller's) and their offsets into `rows`
+  int* rows;              // device [N]: the rows of modality m at rows + off[m]
+  float *xs_hi, *xs_lo, *part;
+};
+
+// Splits of an island GEMM: the 3xTF32 plan's, capped so that splits x M stays within the N rows
+// the partial buffer holds.
+static int island_splits(int M, int Nn, int K, int n_tokens) {
+  int S = tf32x3_splits(M, Nn, K);
+  const int cap = n_tokens / M > 1 ? n_tokens / M : 1;
+  return S < cap ? S : cap;
+}
+
+// The patch projections: the row maps from the tags, then per modality x[rows_m] = z_m W_patch^T + b
+// written straight into the fp32 residual.
+static dit_status latent_embed(dit_handle* h, const LatentArgs& a, const uint8_t* tags, int N, float* resid,
+                               int* layout_code, int* status, cudaStream_t s) {
+  const int d = h->cfg.hidden;
+  {
+    Launch ln(h, s, 7);
+    DIT_CK(h, row_map_launch(tags, N, a.mr, a.rows, layout_code, status, s), "row maps");
+    ln.done();
+  }
+  for (int m = 0; m < a.mr.n; ++m) {
+    const int M = a.mr.count[m];
+    if (M == 0) continue;
+    const int Kp = h->lat_kp[m];
+    Launch ln(h, s, 7);
+    DIT_CK(h, tf32_split_rows_launch(a.z[m], h->lat_width[m], h->lat_width[m], nullptr, M, Kp, a.xs_hi, a.xs_lo,
+                                     status, s), "patch split");
+    const int want = island_splits(M, d, Kp, N);
+    DIT_CK(h, tf32x3_partial_launch(a.xs_hi, a.xs_lo, h->lat_patch[m].hi, h->lat_patch[m].lo, M, d, Kp, want, a.part,
+                                    status, s), "patch projection");
+    DIT_CK(h, sgemm_reduce_rows_launch(a.part, tf32x3_effective_splits(Kp, want), M, d, d, h->lat_b_patch[m],
+                                       a.rows + a.mr.off[m], resid, d, status, s), "patch projection store");
+    ln.done();
+  }
+  return DIT_OK;
+}
+
 // The forward with its AdaLN timesteps: n_t = 1 (every modality at t[0]) or n_t = n_modalities.
+// With `lat` the residual is filled by the patch projections instead of copied from x_tokens.
 static dit_status forward_impl(dit_handle* h, const float* x_tokens, const int32_t* cu_seqlens, int n_docs,
                                const int32_t* doc_ids, const uint8_t* modality_tags, const double* pos_thw,
                                int n_tokens, const float* t_in, int n_t, float* out, void* workspace,
-                               size_t workspace_bytes, void* stream) {
+                               size_t workspace_bytes, void* stream, const LatentArgs* lat = nullptr) {
   if (!h) return DIT_ERR_INVALID_ARG;
   if (!h->bound) return set_err(h, DIT_ERR_UNBOUND, "dit_forward before dit_bind_weights");
   const dit_config& c = h->cfg;
-  if (!x_tokens || !cu_seqlens || !doc_ids || !modality_tags || !pos_thw || !out || !workspace)
+  if ((!x_tokens && !lat) || !cu_seqlens || !doc_ids || !modality_tags || !pos_thw || !out || !workspace)
     return set_err(h, DIT_ERR_INVALID_ARG, "a required pointer is NULL");
   if (n_tokens < 1 || n_docs < 1) return set_err(h, DIT_ERR_LAYOUT, "n_tokens and n_docs must be >= 1");
   if (n_tokens > c.max_tokens || n_docs > c.max_docs)
     return set_err(h, DIT_ERR_CAPACITY, "n_tokens %d / n_docs %d exceed max_tokens %d / max_docs %d", n_tokens,
                    n_docs, c.max_tokens, c.max_docs);
-  if (!aligned16(x_tokens) || !aligned16(out) || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
+  if ((!lat && !aligned16(x_tokens)) || !aligned16(out) || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
     return set_err(h, DIT_ERR_INVALID_ARG, "x/out must be 16-byte and workspace 256-byte aligned");
   if (static_cast<const void*>(x_tokens) == static_cast<const void*>(out))
     return set_err(h, DIT_ERR_INVALID_ARG, "out may not alias x_tokens");
@@ -689,7 +741,12 @@ static dit_status forward_impl(dit_handle* h, const float* x_tokens, const int32
     DIT_CK(h, adaln_launch(h->w_ada_all, h->b_ada_all, h->ada_rows, c.t_embed_dim, ts, mod, status, s), "adaln");
     ln.done();
   }
-  DIT_CK(h, cudaMemcpyAsync(resid, x_tokens, (size_t)N * d * 4, cudaMemcpyDeviceToDevice, s), "copy x");
+  if (lat) {
+    const dit_status st = latent_embed(h, *lat, modality_tags, N, resid, &sw->layout_code, status, s);
+    if (st != DIT_OK) return st;
+  } else {
+    DIT_CK(h, cudaMemcpyAsync(resid, x_tokens, (size_t)N * d * 4, cudaMemcpyDeviceToDevice, s), "copy x");
+  }
 
   const long long mstride = 6ll * d;  // between modality rows of one block's [n_mod][6][d]
   AttnArgs aa;
@@ -791,6 +848,204 @@ dit_status dit_forward_modal(dit_handle* h, const float* x_tokens, const int32_t
     return set_err(h, DIT_ERR_UNSUPPORTED, "per-modality timesteps support up to %d modalities", kMaxModalTimesteps);
   return forward_impl(h, x_tokens, cu_seqlens, n_docs, doc_ids, modality_tags, pos_thw, n_tokens, timesteps, nm, out,
                       workspace, workspace_bytes, stream);
+}
+
+// ------------------------------------------------------------------------------------------------
+// Latent I/O
+// ------------------------------------------------------------------------------------------------
+
+namespace {
+
+// dit_forward_latent's workspace: the forward's, then the final hidden state [N][d], the row maps
+// [N], and the islands' split operands [N][kmax] x 2 and partial sums [N][nmax] (island_splits
+// keeps splits x M <= N).
+struct LatLayout {
+  size_t out_h, rows, xs_hi, xs_lo, part, total;
+};
+
+LatLayout lat_layout(const dit_handle* h, int N, int n_docs) {
+  LatLayout L{};
+  const int d = h->cfg.hidden;
+  size_t kmax = (size_t)d, nmax = (size_t)d;
+  for (int m = 0; m < h->lat_n; ++m) {
+    kmax = std::max(kmax, (size_t)h->lat_kp[m]);
+    nmax = std::max(nmax, (size_t)h->lat_np[m]);
+  }
+  size_t off = align_up(ws_layout(&h->cfg, N, n_docs).total);
+  L.out_h = off;
+  off = align_up(off + (size_t)N * d * 4);
+  L.rows = off;
+  off = align_up(off + (size_t)N * 4);
+  L.xs_hi = off;
+  off = align_up(off + (size_t)N * kmax * 4);
+  L.xs_lo = off;
+  off = align_up(off + (size_t)N * kmax * 4);
+  L.part = off;
+  off = align_up(off + (size_t)N * nmax * 4);
+  L.total = off;
+  return L;
+}
+
+}  // namespace
+
+dit_status dit_bind_latent_io(dit_handle* h, const dit_latent_io* io, void* stream) {
+  if (!h || !io) return DIT_ERR_INVALID_ARG;
+  const dit_config& c = h->cfg;
+  if (c.dtype != DIT_BF16 || !c.adaln)
+    return set_err(h, DIT_ERR_UNSUPPORTED, "latent I/O needs the bf16 model with AdaLN");
+  const int nm = io->n_modalities;
+  if (nm != c.n_modalities || nm < 1 || nm > kMaxModalTimesteps)
+    return set_err(h, DIT_ERR_INVALID_ARG, "n_modalities %d must equal the model's (%d) and be at most %d", nm,
+                   c.n_modalities, kMaxModalTimesteps);
+  for (int m = 0; m < nm; ++m) {
+    if (io->width[m] < 1 || io->width[m] > 65536)
+      return set_err(h, DIT_ERR_INVALID_ARG, "width[%d] = %d outside [1, 65536]", m, io->width[m]);
+    if (!io->w_patch[m] || !io->w_head[m]) return set_err(h, DIT_ERR_MISSING_WEIGHT, "w_patch/w_head[%d] is NULL", m);
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  const int d = c.hidden;
+  int kp[kMaxModalTimesteps], np[kMaxModalTimesteps];
+  SplitW patch[kMaxModalTimesteps], head[kMaxModalTimesteps];
+  float* bp[kMaxModalTimesteps] = {};
+  float* bh[kMaxModalTimesteps] = {};
+  auto alloc = [&](size_t floats) -> float* { return static_cast<float*>(dev_alloc(h, floats * 4, &e)); };
+  auto copy_bias = [&](const float* src, int n) -> float* {
+    if (!src) return nullptr;
+    float* dst = alloc((size_t)n);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dst, src, (size_t)n * 4, cudaMemcpyDeviceToDevice, s);
+    return dst;
+  };
+  for (int m = 0; m < nm; ++m) {
+    const int w = io->width[m];
+    kp[m] = (w + kTf32x3K - 1) / kTf32x3K * kTf32x3K;
+    np[m] = (w + kTf32x3N - 1) / kTf32x3N * kTf32x3N;
+    // patch projection [d][width] -> [d][kp], columns past width zero
+    patch[m].hi = alloc((size_t)d * kp[m]);
+    if (e == cudaSuccess) patch[m].lo = alloc((size_t)d * kp[m]);
+    if (e == cudaSuccess)
+      e = tf32_split_rows_launch(io->w_patch[m], w, w, nullptr, d, kp[m], patch[m].hi, patch[m].lo, nullptr, s);
+    // output head [width][d] -> [np][d], rows past width zero
+    if (e == cudaSuccess) head[m].hi = alloc((size_t)np[m] * d);
+    if (e == cudaSuccess) head[m].lo = alloc((size_t)np[m] * d);
+    if (e == cudaSuccess) e = cudaMemsetAsync(head[m].hi, 0, (size_t)np[m] * d * 4, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(head[m].lo, 0, (size_t)np[m] * d * 4, s);
+    if (e == cudaSuccess)
+      e = tf32_split_rows_launch(io->w_head[m], d, d, nullptr, w, d, head[m].hi, head[m].lo, nullptr, s);
+    if (e == cudaSuccess) bp[m] = copy_bias(io->b_patch[m], d);
+    if (e == cudaSuccess) bh[m] = copy_bias(io->b_head[m], w);
+    if (e != cudaSuccess) return cuda_err(h, e, "bind latent io");
+  }
+  DIT_CK(h, cudaStreamSynchronize(s), "bind latent io sync");
+  h->lat_n = nm;
+  for (int m = 0; m < nm; ++m) {
+    h->lat_width[m] = io->width[m];
+    h->lat_kp[m] = kp[m];
+    h->lat_np[m] = np[m];
+    h->lat_patch[m] = patch[m];
+    h->lat_head[m] = head[m];
+    h->lat_b_patch[m] = bp[m];
+    h->lat_b_head[m] = bh[m];
+  }
+  return DIT_OK;
+}
+
+size_t dit_workspace_bytes_latent(const dit_handle* h, int n_tokens, int n_docs) {
+  if (!h || h->lat_n == 0 || n_tokens < 1 || n_docs < 1) return 0;
+  return lat_layout(h, n_tokens, n_docs).total;
+}
+
+dit_status dit_forward_latent(dit_handle* h, const float* const* z, const int* n_rows, const int32_t* cu_seqlens,
+                              int n_docs, const int32_t* doc_ids, const uint8_t* modality_tags, const double* pos_thw,
+                              int n_tokens, const float* timesteps, float* const* v, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  if (!h) return DIT_ERR_INVALID_ARG;
+  if (!h->bound) return set_err(h, DIT_ERR_UNBOUND, "dit_forward_latent before dit_bind_weights");
+  if (h->lat_n == 0) return set_err(h, DIT_ERR_UNBOUND, "dit_forward_latent before dit_bind_latent_io");
+  if (!z || !n_rows || !v || !timesteps || !workspace)
+    return set_err(h, DIT_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (n_tokens < 1 || n_docs < 1) return set_err(h, DIT_ERR_LAYOUT, "n_tokens and n_docs must be >= 1");
+  if (n_tokens > h->cfg.max_tokens || n_docs > h->cfg.max_docs)
+    return set_err(h, DIT_ERR_CAPACITY, "n_tokens %d / n_docs %d exceed the handle's capacity", n_tokens, n_docs);
+  LatentArgs a{};
+  a.z = z;
+  a.mr.n = h->lat_n;
+  long long sum = 0;
+  for (int m = 0; m < h->lat_n; ++m) {
+    if (n_rows[m] < 0) return set_err(h, DIT_ERR_INVALID_ARG, "n_rows[%d] < 0", m);
+    if (n_rows[m] > 0 && (!z[m] || !v[m])) return set_err(h, DIT_ERR_INVALID_ARG, "z[%d] or v[%d] is NULL", m, m);
+    a.mr.count[m] = n_rows[m];
+    a.mr.off[m] = (int)sum;
+    sum += n_rows[m];
+  }
+  if (sum != n_tokens)
+    return set_err(h, DIT_ERR_INVALID_ARG, "n_rows add up to %lld, not n_tokens = %d", sum, n_tokens);
+  if (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1))
+    return set_err(h, DIT_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  const LatLayout LL = lat_layout(h, n_tokens, n_docs);
+  if (workspace_bytes < LL.total)
+    return set_err(h, DIT_ERR_CAPACITY, "workspace %zu bytes < required %zu", workspace_bytes, LL.total);
+  a.rows = at<int>(workspace, LL.rows);
+  a.xs_hi = at<float>(workspace, LL.xs_hi);
+  a.xs_lo = at<float>(workspace, LL.xs_lo);
+  a.part = at<float>(workspace, LL.part);
+  float* out_h = at<float>(workspace, LL.out_h);
+  dit_status st = forward_impl(h, nullptr, cu_seqlens, n_docs, doc_ids, modality_tags, pos_thw, n_tokens, timesteps,
+                               h->lat_n, out_h, workspace, workspace_bytes, stream, &a);
+  if (st != DIT_OK) return st;
+  // the output heads: v_m = out[rows_m] W_head^T + b_head
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* status = &at<StatusWords>(workspace, ws_layout(&h->cfg, n_tokens, n_docs).status)->bits;
+  const int d = h->cfg.hidden;
+  for (int m = 0; m < h->lat_n; ++m) {
+    const int M = n_rows[m];
+    if (M == 0) continue;
+    const int Np = h->lat_np[m];
+    Launch ln(h, s, 7);
+    DIT_CK(h, tf32_split_rows_launch(out_h, d, d, a.rows + a.mr.off[m], M, d, a.xs_hi, a.xs_lo, status, s),
+           "head split");
+    const int want = island_splits(M, Np, d, n_tokens);
+    DIT_CK(h, tf32x3_partial_launch(a.xs_hi, a.xs_lo, h->lat_head[m].hi, h->lat_head[m].lo, M, Np, d, want, a.part,
+                                    status, s), "output head");
+    DIT_CK(h, sgemm_reduce_rows_launch(a.part, tf32x3_effective_splits(d, want), M, Np, h->lat_width[m],
+                                       h->lat_b_head[m], nullptr, v[m], h->lat_width[m], status, s),
+           "output head store");
+    ln.done();
+  }
+  return DIT_OK;
+}
+
+static dit_status patch_call(const float* src, float* dst, int C, int T, int H, int W, int pt, int ph, int pw,
+                             int inverse, void* stream) {
+  if (!src || !dst) return set_err(nullptr, DIT_ERR_INVALID_ARG, "NULL latent or token buffer");
+  if (C < 1 || T < 1 || H < 1 || W < 1 || pt < 1 || ph < 1 || pw < 1)
+    return set_err(nullptr, DIT_ERR_INVALID_ARG, "every size must be >= 1");
+  const long long P = (long long)C * pt * ph * pw;
+  if (P > 12287) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "C*pt*ph*pw = %lld above 12287", P);
+  const long long n = P * T * H * W;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(src), b0 = reinterpret_cast<uintptr_t>(dst);
+  if (a0 < b0 + (uintptr_t)n * 4 && b0 < a0 + (uintptr_t)n * 4)
+    return set_err(nullptr, DIT_ERR_INVALID_ARG, "latent and token buffers overlap");
+  const cudaError_t e = patch_launch(src, dst, C, T, H, W, pt, ph, pw, inverse, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DIT_OK : cuda_err(nullptr, e, inverse ? "unpatchify" : "patchify");
+}
+
+dit_status dit_patchify(const float* latent, int C, int T, int H, int W, int pt, int ph, int pw, float* tokens,
+                        void* stream) {
+  return patch_call(latent, tokens, C, T, H, W, pt, ph, pw, 0, stream);
+}
+
+dit_status dit_unpatchify(const float* tokens, int C, int T, int H, int W, int pt, int ph, int pw, float* latent,
+                          void* stream) {
+  return patch_call(tokens, latent, C, T, H, W, pt, ph, pw, 1, stream);
+}
+
+dit_status dit_audio_pack(const float* latent, int C, int T, float* tokens, void* stream) {
+  return patch_call(latent, tokens, C, T, 1, 1, 1, 1, 1, 0, stream);
+}
+
+dit_status dit_audio_unpack(const float* tokens, int C, int T, float* latent, void* stream) {
+  return patch_call(tokens, latent, C, T, 1, 1, 1, 1, 1, 1, stream);
 }
 
 size_t dit_workspace_bytes_host(const dit_config* cfg, int n_tokens, int n_docs) {

@@ -175,8 +175,8 @@ __global__ void io_transpose_kernel(const float* __restrict__ src, float* __rest
 //   warp 1     TMEM allocator + MMA issuer: 4 K-steps x 3 products per stage, one stage per chunk
 //   warps 2-9  epilogue: TMEM lane = feature, column = token; two warps per lane quarter split the
 //              token columns; running sums in registers, coalesced stores along features
-constexpr int T3_BK = 32;                 // K per stage: one 128-byte swizzled row of fp32
-constexpr int T3_ROWS = 128;              // output features per CTA (MMA M)
+constexpr int T3_BK = kTf32x3K;           // K per stage: one 128-byte swizzled row of fp32
+constexpr int T3_ROWS = kTf32x3N;         // output features per CTA (MMA M)
 constexpr int T3_STAGES = 2;
 constexpr int T3_CHUNK = 1;               // stages per accumulation chunk (32-deep)
 constexpr int T3_W_BYTES = T3_ROWS * T3_BK * 4;  // 16 KB
@@ -349,6 +349,41 @@ __global__ void tf32_split_kernel(const float* __restrict__ x, size_t n, float* 
   }
 }
 
+// Row-gathered, column-padded split: row r of the [M][Kp] outputs is x row (rows ? rows[r] : r)
+// of stride ldx, columns K..Kp-1 zero (the GEMM's K is a multiple of its 32-deep chunk).
+__global__ void tf32_split_rows_kernel(const float* __restrict__ x, long long ldx, int K, const int* __restrict__ rows,
+                                       int M, int Kp, float* __restrict__ hi, float* __restrict__ lo,
+                                       const int* status) {
+  if (status && (*reinterpret_cast<const volatile int*>(status) & kDevLayout)) return;
+  const size_t n = (size_t)M * Kp;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const int r = (int)(i / Kp), k = (int)(i - (size_t)r * Kp);
+    float v = 0.f;
+    if (k < K) v = x[(size_t)(rows ? rows[r] : r) * ldx + k];
+    uint32_t h, l;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(h) : "f"(v));
+    const float rr = __fsub_rn(v, __uint_as_float(h));
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(l) : "f"(rr));
+    hi[i] = __uint_as_float(h);
+    lo[i] = __uint_as_float(l);
+  }
+}
+
+// out[(rows ? rows[r] : r) * ld_out + n] = sum over S partials [S][M][Np] + bias[n], n < n_out:
+// the row-scattered, column-trimmed store of a GEMM whose N was padded to Np.
+__global__ void sgemm_reduce_rows_kernel(const float* __restrict__ part, int S, int M, int Np, int n_out,
+                                         const float* __restrict__ bias, const int* __restrict__ rows,
+                                         float* __restrict__ out, long long ld_out, const int* status) {
+  if (status && (*reinterpret_cast<const volatile int*>(status) & kDevLayout)) return;
+  const size_t MNp = (size_t)M * Np;
+  const size_t n = (size_t)M * n_out;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const int r = (int)(i / n_out), c = (int)(i - (size_t)r * n_out);
+    const float v = sum_parts(part, S, MNp, (size_t)r * Np + c) + (bias ? bias[c] : 0.f);
+    out[(size_t)(rows ? rows[r] : r) * ld_out + c] = v;
+  }
+}
+
 int ew_grid(size_t work) {
   size_t g = (work + 255) / 256;
   const size_t cap = (size_t)num_sms() * 16;
@@ -405,6 +440,24 @@ cudaError_t tf32x3_partial_launch(const float* x_hi, const float* x_lo, const fl
 cudaError_t tf32_split_launch(const float* x, size_t n, float* hi, float* lo, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
   tf32_split_kernel<<<ew_grid(n), 256, 0, s>>>(x, n, hi, lo);
+  return cudaGetLastError();
+}
+
+cudaError_t tf32_split_rows_launch(const float* x, long long ldx, int K, const int* rows, int M, int Kp, float* hi,
+                                   float* lo, const int* status, cudaStream_t s) {
+  if (M <= 0) return cudaSuccess;
+  if (K < 1 || Kp < K || ldx < K) return cudaErrorInvalidValue;
+  tf32_split_rows_kernel<<<ew_grid((size_t)M * Kp), 256, 0, s>>>(x, ldx, K, rows, M, Kp, hi, lo, status);
+  return cudaGetLastError();
+}
+
+cudaError_t sgemm_reduce_rows_launch(const float* part, int S, int M, int Np, int n_out, const float* bias,
+                                     const int* rows, float* out, long long ld_out, const int* status,
+                                     cudaStream_t s) {
+  if (M <= 0) return cudaSuccess;
+  if (n_out < 1 || n_out > Np || ld_out < n_out) return cudaErrorInvalidValue;
+  sgemm_reduce_rows_kernel<<<ew_grid((size_t)M * n_out), 256, 0, s>>>(part, S, M, Np, n_out, bias, rows, out, ld_out,
+                                                                      status);
   return cudaGetLastError();
 }
 

@@ -102,6 +102,17 @@ struct ModalSigmas {
 cudaError_t euler_tagged_launch(float* x, const float* v, int n_tokens, int d, const uint8_t* tags,
                                 const ModalSigmas& sg, cudaStream_t s);
 cudaError_t euler_launch(float* x, const float* v, long long n, float sigma, float sigma_next, cudaStream_t s);
+// Latent <-> token packing (inverse = 0: latent [C][T*pt][H*ph][W*pw] -> tokens [T*H*W][C*pt*ph*pw]).
+cudaError_t patch_launch(const float* src, float* dst, int C, int T, int H, int W, int pt, int ph, int pw,
+                         int inverse, cudaStream_t s);
+// Per-modality row lists from the tags: rows[off[m] + k] = the k-th token tagged m, k < count[m].
+struct ModalRows {
+  int n;
+  int count[kMaxModalTimesteps];
+  int off[kMaxModalTimesteps];
+};
+cudaError_t row_map_launch(const uint8_t* tags, int n, const ModalRows& mr, int* rows, int* layout_code, int* status,
+                           cudaStream_t s);
 cudaError_t pack_ffn_in_launch(const void* w_in, const float* b_in, int F, int d, void* w_packed, float* b_packed,
                                cudaStream_t s);
 cudaError_t to_f32_launch(const void* src, int src_is_bf16, long long n, float* dst, cudaStream_t s);
@@ -119,6 +130,16 @@ int tf32x3_effective_splits(int K, int S);
 cudaError_t tf32x3_partial_launch(const float* x_hi, const float* x_lo, const float* w_hi, const float* w_lo, int M,
                                   int N, int K, int S, float* part, const int* status, cudaStream_t s);
 cudaError_t tf32_split_launch(const float* x, size_t n, float* hi, float* lo, cudaStream_t s);
+// The 3xTF32 GEMM's tiling: K a multiple of kTf32x3K, N (output features) a multiple of kTf32x3N.
+constexpr int kTf32x3K = 32;
+constexpr int kTf32x3N = 128;
+// Split of rows (rows ? rows[r] : r) of x (stride ldx, K columns) into [M][Kp] hi/lo, zero-padded.
+cudaError_t tf32_split_rows_launch(const float* x, long long ldx, int K, const int* rows, int M, int Kp, float* hi,
+                                   float* lo, const int* status, cudaStream_t s);
+// out[(rows ? rows[r] : r) * ld_out + n] = sum of the S partials [S][M][Np] + bias[n], for n < n_out.
+cudaError_t sgemm_reduce_rows_launch(const float* part, int S, int M, int Np, int n_out, const float* bias,
+                                     const int* rows, float* out, long long ld_out, const int* status,
+                                     cudaStream_t s);
 cudaError_t sgemm_reduce_store_launch(const float* part, int S, int M, int N, const float* bias, float* out, int add,
                                       float* lo, const int* status, cudaStream_t s);
 cudaError_t sgemm_reduce_qkv_launch(const float* part, int S, int M, int d, int Dh, int half, const float* bias,

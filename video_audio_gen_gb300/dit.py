@@ -19,15 +19,23 @@ STATUS_NAMES = {0: "DIT_OK", 1: "DIT_ERR_INVALID_ARG", 2: "DIT_ERR_CONFIG", 3: "
                 8: "DIT_ERR_DEVICE_TIMEOUT", 9: "DIT_ERR_UNSUPPORTED"}
 DIT_RMSNORM, DIT_LAYERNORM = 0, 1
 DIT_BF16, DIT_FP32 = 0, 1
-KERNEL_KINDS = ["gemm_qkv", "attention", "gemm_out", "gemm_ffn_up", "gemm_ffn_down", "norm_modulate", "other"]
+KERNEL_KINDS = ["gemm_qkv", "attention", "gemm_out", "gemm_ffn_up", "gemm_ffn_down", "norm_modulate", "other",
+                "latent_io"]
+MAX_LATENT_MODALITIES = 8
 
 EXPORTS = ["dit_create", "dit_destroy", "dit_last_error", "dit_workspace_bytes", "dit_bind_weights", "dit_forward",
            "dit_forward_modal", "dit_workspace_bytes_host", "dit_forward_host", "dit_euler_step",
-           "dit_euler_step_modal", "dit_time_shift", "dit_get_stats", "dit_sync_status",
+           "dit_euler_step_modal", "dit_time_shift", "dit_bind_latent_io", "dit_workspace_bytes_latent",
+           "dit_forward_latent", "dit_patchify", "dit_unpatchify", "dit_audio_pack", "dit_audio_unpack", "dit_get_stats", "dit_sync_status",
            "dit_set_dump", "dit_set_kernel_timing", "dit_get_kernel_times", "dit_op_norm_modulate",
            "dit_op_rope_cache", "dit_op_adaln", "dit_op_gemm", "dit_op_gemm_qkv_rope", "dit_op_gemm_gated_residual",
            "dit_op_gemm_swiglu", "dit_gemm_f32_workspace_bytes", "dit_op_gemm_f32", "dit_op_pack_ffn_in", "dit_attention_workspace_bytes", "dit_op_attention",
            "dit_op_attention_noalloc", "dit_selftest_wait_timeout"]
+
+
+class DitLatentIO(ctypes.Structure):
+    _fields_ = [("n_modalities", ctypes.c_int), ("width", ctypes.c_int * MAX_LATENT_MODALITIES)] + \
+               [(n, ctypes.c_void_p * MAX_LATENT_MODALITIES) for n in ("w_patch", "b_patch", "w_head", "b_head")]
 
 
 class DitError(RuntimeError):
@@ -97,6 +105,15 @@ def lib():
             "dit_euler_step_modal": (i32, [vp, vp, i32, i32, vp, ctypes.POINTER(ctypes.c_float),
                                            ctypes.POINTER(ctypes.c_float), i32, vp]),
             "dit_time_shift": (f32, [f32, f32]),
+            "dit_bind_latent_io": (i32, [vp, ctypes.POINTER(DitLatentIO), vp]),
+            "dit_workspace_bytes_latent": (sz, [vp, i32, i32]),
+            "dit_forward_latent": (i32, [vp, ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_int), vp, i32, vp,
+                                         vp, vp, i32, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_void_p),
+                                         vp, sz, vp]),
+            "dit_patchify": (i32, [vp, i32, i32, i32, i32, i32, i32, i32, vp, vp]),
+            "dit_unpatchify": (i32, [vp, i32, i32, i32, i32, i32, i32, i32, vp, vp]),
+            "dit_audio_pack": (i32, [vp, i32, i32, vp, vp]),
+            "dit_audio_unpack": (i32, [vp, i32, i32, vp, vp]),
             "dit_get_stats": (i32, [vp, ctypes.POINTER(DitStats)]),
             "dit_sync_status": (i32, [vp, vp, vp]),
             "dit_set_dump": (i32, [vp, vp]),
@@ -217,6 +234,33 @@ class Dit:
                                        _ptr(pos), n_tokens, arr, _ptr(out), _ptr(workspace), workspace.numel(),
                                        _stream(stream)), self.h)
 
+    def bind_latent_io(self, io: dict, stream=None):
+        """io: dict of per-modality lists of fp32 device tensors w_patch [d, width], b_patch [d] (or None),
+        w_head [width, d], b_head [width] (or None).  The library keeps its own copies."""
+        n = len(io["w_patch"])
+        s = DitLatentIO()
+        s.n_modalities = n
+        for m in range(n):
+            s.width[m] = io["w_patch"][m].shape[1]
+            for name in ("w_patch", "b_patch", "w_head", "b_head"):
+                t = io[name][m]
+                getattr(s, name)[m] = t.data_ptr() if t is not None else None
+        _check(lib().dit_bind_latent_io(self.h, ctypes.byref(s), _stream(stream)), self.h)
+
+    def workspace_bytes_latent(self, n_tokens: int, n_docs: int) -> int:
+        return int(lib().dit_workspace_bytes_latent(self.h, n_tokens, n_docs))
+
+    def forward_latent(self, z, cu_seqlens, doc_ids, tags, pos, ts, v, workspace, stream=None):
+        """z, v: per-modality lists of device tensors [rows_m, width_m]; ts one flow time per modality."""
+        n = len(z)
+        zp = (ctypes.c_void_p * n)(*[a.data_ptr() if a is not None and a.numel() else None for a in z])
+        vp_ = (ctypes.c_void_p * n)(*[a.data_ptr() if a is not None and a.numel() else None for a in v])
+        rows = (ctypes.c_int * n)(*[0 if a is None else int(a.shape[0]) for a in z])
+        tt = (ctypes.c_float * n)(*[float(t) for t in ts])
+        _check(lib().dit_forward_latent(self.h, zp, rows, _ptr(cu_seqlens), cu_seqlens.numel() - 1, _ptr(doc_ids),
+                                        _ptr(tags), _ptr(pos), doc_ids.numel(), tt, vp_, _ptr(workspace),
+                                        workspace.numel(), _stream(stream)), self.h)
+
     def forward_host(self, x, cu_seqlens, doc_ids, tags, pos, t: float, out, workspace, stream=None):
         """Host (preferably pinned) CPU tensors in and out; device workspace."""
         n_docs = cu_seqlens.numel() - 1
@@ -240,8 +284,8 @@ class Dit:
         _check(lib().dit_set_kernel_timing(self.h, 1 if enable else 0), self.h)
 
     def kernel_times(self) -> dict:
-        ms = (ctypes.c_double * 7)()
-        n = (ctypes.c_int64 * 7)()
+        ms = (ctypes.c_double * len(KERNEL_KINDS))()
+        n = (ctypes.c_int64 * len(KERNEL_KINDS))()
         _check(lib().dit_get_kernel_times(self.h, ms, n), self.h)
         return {k: (ms[i], n[i]) for i, k in enumerate(KERNEL_KINDS)}
 
@@ -273,6 +317,28 @@ def euler_step_modal(x, v, tags, sigma, sigma_next, stream=None):
 def time_shift(sigma: float, shift: float) -> float:
     """dit_time_shift: shift * sigma / (1 + (shift - 1) * sigma) in double, rounded to fp32."""
     return float(lib().dit_time_shift(float(sigma), float(shift)))
+
+
+def patchify(latent, pt: int, ph: int, pw: int, tokens, stream=None):
+    """dit_patchify: latent [C, T*pt, H*ph, W*pw] -> tokens [T*H*W, C*pt*ph*pw] (device fp32)."""
+    C, Tf, Hf, Wf = latent.shape
+    _check(lib().dit_patchify(_ptr(latent), C, Tf // pt, Hf // ph, Wf // pw, pt, ph, pw, _ptr(tokens),
+                              _stream(stream)))
+
+
+def unpatchify(tokens, C: int, T: int, H: int, W: int, pt: int, ph: int, pw: int, latent, stream=None):
+    _check(lib().dit_unpatchify(_ptr(tokens), C, T, H, W, pt, ph, pw, _ptr(latent), _stream(stream)))
+
+
+def audio_pack(latent, tokens, stream=None):
+    """dit_audio_pack: [C, T] -> [T, C]."""
+    C, T = latent.shape
+    _check(lib().dit_audio_pack(_ptr(latent), C, T, _ptr(tokens), _stream(stream)))
+
+
+def audio_unpack(tokens, latent, stream=None):
+    T, C = tokens.shape
+    _check(lib().dit_audio_unpack(_ptr(tokens), C, T, _ptr(latent), _stream(stream)))
 
 
 def norm_modulate(x, norm: int, eps: float, y, out_kind: int, tags=None, shift=None, scale=None, mod_stride=0,
