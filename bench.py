@@ -31,7 +31,7 @@ import numpy as np  # noqa: E402
 METRIC = "DiT forward tokens/s & ms/forward on 1 GB300; % of bf16 tensor-pipe peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 SAMPLE_SECONDS = 10.0   # target CPU work of the oracle baseline sample
-KINDS = ["gemm_qkv", "attention", "gemm_out", "gemm_ffn_up", "gemm_ffn_down", "norm_modulate", "other"]
+KINDS = ["gemm_qkv", "attention", "gemm_out", "gemm_ffn_up", "gemm_ffn_down", "norm_modulate", "other", "latent_io"]
 
 # DRAM traffic per launch from ncu captures (dram__bytes_read.sum + dram__bytes_write.sum), keyed by
 # kernel kind and workload, with the sha256 of the kernel source the capture was taken on; the
@@ -286,9 +286,26 @@ def run_gpu(args, w, dist, rank, world):
     loop = w["t"] == "schedule"
     sig = synth.sigmas(w.get("steps", 50))
     stream = torch.cuda.current_stream()
+    latent = w.get("latent", False)
+    if latent:
+        # the loop state is each modality's latent tokens; per-modality shifted schedules
+        widths = synth.latent_widths()
+        io = synth.make_latent_io(rank_seed(w["seed"], rank) + 50, m["hidden"], widths)
+        h.bind_latent_io({k: [None if a is None else gpu_util.dev_f32(a) for a in v] for k, v in io.items()})
+        del io
+        z_host = synth.make_latents(rank_seed(w["seed"], rank) + 50, lay, widths)
+        zd = [gpu_util.dev_f32(a) for a in z_host]
+        vd = [torch.empty_like(a) for a in zd]
+        ws = torch.empty(h.workspace_bytes_latent(N, D), dtype=torch.uint8, device="cuda")
+        sv, sa = ([dit.time_shift(float(a), sh) for a in sig] for sh in w["shifts"])
 
     def one_step(i):
-        if loop:
+        if latent:
+            k = i % (len(sig) - 1)
+            h.forward_latent(zd, dl["cu"], dl["ids"], dl["tags"], dl["pos"], [sv[k], sa[k]], vd, ws)
+            dit.euler_step(zd[0], vd[0], sv[k], sv[k + 1])
+            dit.euler_step(zd[1], vd[1], sa[k], sa[k + 1])
+        elif loop:
             k = i % (len(sig) - 1)
             h.forward(x, dl["cu"], dl["ids"], dl["tags"], dl["pos"], float(sig[k]), out, ws)
             dit.euler_step(x, out, float(sig[k]), float(sig[k + 1]))
@@ -383,8 +400,39 @@ def run_gpu(args, w, dist, rank, world):
     if args.no_e2e:
         return dict(ms_step=ms_step, tokens=N, world=world, kernels=kernels, roofline=roofline, clocks=clk.summary(),
                     launches=launches, e2e_ms=None, h2d=0, d2h=0, flops=fl["total"], docs=D, lay=lay)
-    # end to end through the C ABI from pinned host buffers (copies inside the timed region)
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    if latent:
+        # end to end: each step copies the latent tokens and the layout in from pinned host memory,
+        # runs the latent forward and both Euler steps, and reads the new latent tokens back
+        hz = [pin(a) for a in z_host]
+        hcu, hids = pin(lay["cu_seqlens"].astype(np.int32)), pin(lay["doc_ids"].astype(np.int32))
+        htags, hpos = pin(lay["tags"]), pin(lay["pos"])
+        hback = [torch.empty_like(a) for a in hz]
+
+        def e2e_step(i):
+            for dst, src in zip(zd, hz):
+                dst.copy_(src, non_blocking=True)
+            for key, src in (("cu", hcu), ("ids", hids), ("tags", htags), ("pos", hpos)):
+                dl[key].copy_(src, non_blocking=True)
+            one_step(i)
+            for dst, src in zip(hback, zd):
+                dst.copy_(src, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+
+        for i in range(2):
+            e2e_step(i)
+        e2e_steps = max(3, min(args.steps, 10))
+        if dist is not None:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for i in range(e2e_steps):
+            e2e_step(i)
+        e2e_ms = reduce_max_ms((time.perf_counter() - t0) * 1e3 / e2e_steps, dist)
+        h2d = sum(a.numel() * 4 for a in hz) + hcu.numel() * 4 + hids.numel() * 4 + htags.numel() + hpos.numel() * 8
+        d2h = sum(a.numel() * 4 for a in hback)
+        return dict(ms_step=ms_step, tokens=N, world=world, kernels=kernels, roofline=roofline, clocks=clk.summary(),
+                    launches=launches, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, flops=fl["total"], docs=D, lay=lay)
+    # end to end through the C ABI from pinned host buffers (copies inside the timed region)
     hx, hcu = pin(x_host), pin(lay["cu_seqlens"].astype(np.int32))
     hids, htags, hpos = pin(lay["doc_ids"].astype(np.int32)), pin(lay["tags"]), pin(lay["pos"])
     hout = torch.empty(x_host.shape, dtype=torch.float32).pin_memory()
@@ -431,6 +479,12 @@ def workload_config(name, w, lay, extra=None):
          "tokens": int(lay["n_tokens"]), "documents": int(lay["n_docs"]),
          "cu_seqlens": [int(v) for v in lay["cu_seqlens"]],
          "l2": l2_note(m, lay)}
+    if w.get("latent"):
+        import synth
+        widths = synth.latent_widths()
+        c["latent_io"] = (f"fp32 patch projections and output heads per modality: video {widths[0]} features "
+                          f"({synth.VIDEO_LATENT['channels']} channels, patch {synth.VIDEO_LATENT['patch']}), "
+                          f"audio {widths[1]}; sigma shifts video {w['shifts'][0]:g}, audio {w['shifts'][1]:g}")
     if extra:
         c.update(extra)
     return c
@@ -449,8 +503,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="video_audio_bf16",
-                    choices=["video_audio_bf16", "long_doc_bf16", "denoise_loop", "music_fp32", "video_audio_bf16_l1",
-                             "tiny", "ragged", "music_small"])
+                    choices=["video_audio_bf16", "long_doc_bf16", "denoise_loop", "t2va_loop", "music_fp32",
+                             "video_audio_bf16_l1", "tiny", "ragged", "music_small"])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
@@ -463,6 +517,9 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     is_loop = w["t"] == "schedule"
     metric = METRIC if not is_loop else "DiT denoise step ms/step (forward + Euler) and tokens/s on 1 GB300"
+    if w.get("latent"):
+        metric = ("DiT t2va denoise step ms/step (latent forward: patch projections, blocks, heads; Euler per "
+                  "modality) and tokens/s on 1 GB300")
 
     if args.impl == "reference":
         if rank != 0:

@@ -171,6 +171,12 @@ WORKLOADS = {
     "denoise_loop": dict(model=C2_MODEL, seed=4,
                          docs=[dict(video=(8, 32, 64), audio=1024), dict(video=(4, 32, 64), audio=1024)],
                          t="schedule", steps=50, w_std=0.02, bias_std=0.0, x_std=1.0),
+    # The same two requests as the joint loop in latent token space: per-modality fp32 patch
+    # projections and output heads around the block stack, video sigmas shifted by 12 and audio by 3.
+    "t2va_loop": dict(model=C2_MODEL, seed=4,
+                      docs=[dict(video=(8, 32, 64), audio=1024), dict(video=(4, 32, 64), audio=1024)],
+                      t="schedule", steps=50, latent=True, shifts=(12.0, 3.0), w_std=0.02, bias_std=0.0,
+                      x_std=1.0),
     # One block of the video+audio model on its full 17,408-token sequence: every kernel launch has
     # exactly the full workload's shape, with a few GB on the device (profiling captures).
     "video_audio_bf16_l1": dict(model=dict(C2_MODEL, n_blocks=1), seed=2,

@@ -118,7 +118,7 @@ def test_forward_latent_matches_oracle(name):
     w = synth.WORKLOADS[name]
     m = w["model"]
     lay, W, widths, io, z, h = _latent_setup(w)
-    ts = [0.83, 0.31]
+    ts = [float(np.float32(0.83)), float(np.float32(0.31))]
     dump = torch.empty((m["n_blocks"], lay["n_tokens"], m["hidden"]), dtype=torch.float32, device="cuda")
     vs, st = _run_latent(h, lay, z, ts, widths, dump)
     assert st == 0
