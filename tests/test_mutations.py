@@ -134,3 +134,31 @@ def test_planted_rope_mistake_fails_the_qkv_op_gate(base, name):
     assert np.any(np.abs(mut - ref) > tol)
     # and the unmutated rotation passes the same gate under one bf16 rounding
     assert np.all(np.abs(ref * (1 + 2 ** -9) - ref) <= tol)
+
+
+# ------------------------------------------------------------------------------------------------
+# per-modality timesteps and the latent I/O, against the gates they are held to
+# ------------------------------------------------------------------------------------------------
+
+def test_swapped_modality_timesteps_fail_the_forward_gates(base):
+    lay, W, x, _, _ = base
+    ref, rd = oracle.forward(W0["model"], W, x, lay, [0.8, 0.3], dumps=True)
+    mut, md = oracle.forward(W0["model"], W, x, lay, [0.3, 0.8], dumps=True)
+    assert forward_gates(x, md, rd, mut, ref) != []
+
+
+def test_latent_rows_in_the_wrong_packed_places_fail_the_head_gate(base):
+    """A row map that sends the r-th video token to another video row: the per-modality v gate
+    (3e-3 of RMS) fails."""
+    from tests.parity import GATE
+    lay, W, _, _, _ = base
+    widths = synth.latent_widths()
+    io = synth.make_latent_io(5, W0["model"]["hidden"], widths)
+    z = synth.make_latents(5, lay, widths)
+    ref, _ = oracle.forward_latent(W0["model"], W, io, z, lay, [0.6, 0.2])
+    perm = np.roll(np.arange(z[0].shape[0]), 7)
+    mut, _ = oracle.forward_latent(W0["model"], W, io, [z[0][perm], z[1]], lay, [0.6, 0.2])
+    mut_back = np.empty_like(mut[0])
+    mut_back[perm] = mut[0]  # undo the permutation on the output rows: only the packed places differ
+    rms = np.sqrt((ref[0] ** 2).mean())
+    assert np.abs(mut_back - ref[0]).max() > GATE * rms
