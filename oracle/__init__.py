@@ -63,6 +63,8 @@ def lib():
             _lib.orc_forward_mod.restype = ctypes.c_int
             _lib.orc_forward_latent.restype = ctypes.c_int
             _lib.orc_time_shift.restype = ctypes.c_double
+            _lib.orc_e2m1_decode.restype = ctypes.c_double
+            _lib.orc_e4m3_decode.restype = ctypes.c_double
             _lib.orc_check_layout.restype = ctypes.c_int
             _lib.orc_count_q_tiles.restype = ctypes.c_int
             _lib.orc_get_threads.restype = ctypes.c_int
@@ -292,6 +294,31 @@ def euler_step(x, v, sigma: float, sigma_next: float) -> np.ndarray:
     v = np.ascontiguousarray(v, dtype=np.float32)
     lib().orc_euler_step(_f(x), _f(v), ctypes.c_int64(x.size), ctypes.c_float(sigma), ctypes.c_float(sigma_next))
     return x
+
+
+def e2m1_decode(codes) -> np.ndarray:
+    c = np.ascontiguousarray(codes, dtype=np.uint8).reshape(-1)
+    return np.array([lib().orc_e2m1_decode(ctypes.c_uint8(int(v))) for v in c], dtype=np.float64)
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    c = np.ascontiguousarray(codes, dtype=np.uint8).reshape(-1)
+    return np.array([lib().orc_e4m3_decode(ctypes.c_uint8(int(v))) for v in c], dtype=np.float64)
+
+
+def nvfp4_linear(x, q, scales, g: float, b=None) -> np.ndarray:
+    """y = x W^T + b with the NVFP4 weight W = fp4(q) * e4m3(scales) * g; q [N, K/2] u8 (even k in the
+    low nibble), scales [N, K/16] u8 (E4M3 codes), g the fp32 global scale.  Double precision."""
+    x = _dbl(x)
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    sc = np.ascontiguousarray(scales, dtype=np.uint8)
+    M, K = x.shape
+    N = q.shape[0]
+    assert q.shape == (N, K // 2) and sc.shape == (N, K // 16)
+    y = np.empty((M, N), dtype=np.float64)
+    lib().orc_nvfp4_linear(_d(x), ctypes.c_int(M), ctypes.c_int(K), _p(q), _p(sc), ctypes.c_float(g), _f(_flt(b)),
+                           ctypes.c_int(N), _d(y))
+    return y
 
 
 def patchify(lat, pt: int, ph: int, pw: int) -> np.ndarray:

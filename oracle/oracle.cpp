@@ -457,6 +457,48 @@ void orc_unpatchify(const float* tok, int C, int T, int H, int W, int pt, int ph
 }
 
 // ---------------------------------------------------------------------------------------------
+// NVFP4 weights.  [H3] "What this push adds" (the NVFP4 checkpoint): each quantized projection
+// carries a U8 weight packing two FP4 values per byte (logical [N][K] stored [N][K/2]), an
+// F8_E4M3 scale per group of 16 along K ([N][K/16]) and an F32 global scale.
+// READINGS: the logical weight is fp4 * e4m3 scale * global (the global scale multiplies); the
+// element with the even K index sits in the low nibble.  FP4 is E2M1 (1 sign, 2 exponent bits
+// with bias 1, 1 mantissa bit; exponent 0 is subnormal, no inf/NaN); E4M3 is the "fn" form (bias
+// 7, exponent 0 subnormal, S.1111.111 NaN, no inf).  Both decoded from those definitions.
+// ---------------------------------------------------------------------------------------------
+double orc_e2m1_decode(uint8_t code) {
+  const int s = (code >> 3) & 1, e = (code >> 1) & 3, m = code & 1;
+  const double mag = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+  return s ? -mag : mag;
+}
+
+double orc_e4m3_decode(uint8_t code) {
+  const int s = (code >> 7) & 1, e = (code >> 3) & 15, m = code & 7;
+  if (e == 15 && m == 7) return NAN;
+  const double mag = e == 0 ? ldexp(m / 8.0, -6) : ldexp(1.0 + m / 8.0, e - 7);
+  return s ? -mag : mag;
+}
+
+// y [M][N] = x [M][K] W^T + b with W[n][k] = e2m1(q[n][k/2] nibble) * e4m3(s[n][k/16]) * g, in double.
+void orc_nvfp4_linear(const double* x, int M, int K, const uint8_t* q, const uint8_t* sc, float g, const float* b,
+                      int N, double* y) {
+  std::vector<double> W((size_t)N * K);
+  for (int n = 0; n < N; ++n)
+    for (int k = 0; k < K; ++k) {
+      const uint8_t byte = q[(size_t)n * (K / 2) + k / 2];
+      const uint8_t code = (k & 1) ? (byte >> 4) : (byte & 15);
+      W[(size_t)n * K + k] = orc_e2m1_decode(code) * orc_e4m3_decode(sc[(size_t)n * (K / 16) + k / 16]) * (double)g;
+    }
+#pragma omp parallel for num_threads(g_threads) schedule(static)
+  for (int i = 0; i < M; ++i)
+    for (int n = 0; n < N; ++n) {
+      double acc = 0.0;
+      for (int k = 0; k < K; ++k) acc += x[(size_t)i * K + k] * W[(size_t)n * K + k];
+      if (b) acc += (double)b[n];
+      y[(size_t)i * N + n] = acc;
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
 // One transformer block, in place on the fp64 residual x [N][d].  [H3] "The device-resident
 // forward (W2b)" lists the ops; with AdaLN on:
 //   y  = RMS(x) * (1 + scale1[tag]) + shift1[tag]

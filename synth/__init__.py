@@ -315,3 +315,22 @@ def make_latent_io(seed: int, d: int, widths, bias_std: float = 0.02) -> dict:
 def make_latents(seed: int, layout: dict, widths, name: str = "z") -> list:
     """Initial noise in token form: one N(0, 1) array [rows_m, width_m] per modality."""
     return [normal(seed, f"{name}{m}", (int((layout["tags"] == m).sum()), k), 1.0) for m, k in enumerate(widths)]
+
+
+# ---------------------------------------------------------------------------------------------
+# NVFP4 weights: random valid codes, no quantisation arithmetic.  Two FP4 (E2M1) codes per byte,
+# uniform over all 16; one E4M3 scale per 16 along K with exponent field 4..6 (2^-3 .. 2^-1) and a
+# random mantissa; the fp32 global scale 0.015, so the dequantised weight has RMS near 0.02.
+# ---------------------------------------------------------------------------------------------
+
+NVFP4_GLOBAL = 0.015
+
+
+def make_nvfp4(seed: int, name: str, N: int, K: int):
+    """(q [N, K/2] u8, scales [N, K/16] u8 E4M3 codes, global scale) for an [N, K] weight."""
+    assert K % 16 == 0
+    q = np.minimum(uniform(seed, name + ".q", N * K // 2) * 256, 255).astype(np.uint8).reshape(N, K // 2)
+    e = 4 + np.minimum(uniform(seed, name + ".se", N * K // 16) * 3, 2).astype(np.uint8)
+    m = np.minimum(uniform(seed, name + ".sm", N * K // 16) * 8, 7).astype(np.uint8)
+    s = ((e << 3) | m).astype(np.uint8).reshape(N, K // 16)
+    return q, s, NVFP4_GLOBAL

@@ -586,3 +586,65 @@ def test_forward_latent_rejects_row_counts_that_disagree_with_tags():
     z = [synth.normal(36, "z0", (5, 4), 1.0), synth.normal(36, "z1", (3, 4), 1.0)]  # tags say 6 and 2
     with pytest.raises(ValueError, match="code 8"):
         oracle.forward_latent(TINY_RMS, W, io, z, lay, 0.5)
+
+
+# ---------------------------------------------------------------------------------------------
+# NVFP4 weights
+# ---------------------------------------------------------------------------------------------
+
+def test_e2m1_decodes_to_the_fp4_grid():
+    """E2M1: 1 sign, 2 exponent bits (bias 1), 1 mantissa bit; exponent 0 subnormal.  The eight
+    magnitudes are 0, 0.5, 1, 1.5, 2, 3, 4, 6 and the high bit is the sign."""
+    v = oracle.e2m1_decode(np.arange(16))
+    assert list(v[:8]) == [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    assert np.array_equal(v[8:], -v[:8]) and np.signbit(v[8])
+
+
+def test_e4m3_decodes_like_torch_float8_e4m3fn():
+    torch = pytest.importorskip("torch")
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    got = oracle.e4m3_decode(np.arange(256))
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan) and nan.sum() == 2
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert got[0x7E] == 448.0 and got[0x08] == 2.0 ** -6 and got[0x01] == 2.0 ** -9 and got[0x38] == 1.0
+
+
+def test_nvfp4_linear_against_numpy_dequantisation():
+    torch = pytest.importorskip("torch")
+    M, N, K = 5, 7, 64
+    q, s, g = synth.make_nvfp4(60, "w", N, K)
+    x = synth.normal(60, "x", (M, K), 1.0)
+    b = synth.normal(60, "b", (N,), 0.1)
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    codes = np.empty((N, K), dtype=np.int64)
+    codes[:, 0::2] = q & 15
+    codes[:, 1::2] = q >> 4
+    fp4 = np.where(codes >= 8, -1.0, 1.0) * grid[codes & 7]
+    sc = torch.from_numpy(s.copy()).view(torch.float8_e4m3fn).double().numpy()
+    W = fp4 * np.repeat(sc, 16, axis=1) * np.float64(np.float32(g))
+    ref = x.astype(np.float64) @ W.T + b
+    got = oracle.nvfp4_linear(x, q, s, g, b)
+    assert np.abs(got - ref).max() <= 1e-13 * np.abs(ref).max()
+
+
+def test_nvfp4_even_k_sits_in_the_low_nibble():
+    """A weight whose only nonzero code is the high nibble of byte 0 reads x[:, 1]."""
+    K = 32
+    q = np.zeros((1, K // 2), dtype=np.uint8)
+    q[0, 0] = 0x20  # code 2 (= 1.0) at k = 1, code 0 at k = 0
+    s = np.full((1, K // 16), 0x38, dtype=np.uint8)  # scale 1.0
+    x = synth.normal(61, "x", (3, K), 1.0)
+    y = oracle.nvfp4_linear(x, q, s, 1.0)
+    assert np.array_equal(y[:, 0], x[:, 1].astype(np.float64))
+
+
+def test_synthetic_nvfp4_weights_have_the_intended_scale():
+    q, s, g = synth.make_nvfp4(62, "w", 256, 1024)
+    e = (s >> 3) & 15
+    assert e.min() == 4 and e.max() == 6 and (s >> 7).max() == 0
+    vals = oracle.e2m1_decode(np.arange(16))
+    codes = np.concatenate([q & 15, q >> 4], axis=1).reshape(-1)
+    assert np.bincount(codes, minlength=16).min() > 0.8 * codes.size / 16  # all 16 codes, near uniform
+    rms = np.sqrt((vals[codes] ** 2).mean()) * np.sqrt((oracle.e4m3_decode(s) ** 2).mean()) * g
+    assert 0.01 < rms < 0.04
