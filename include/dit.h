@@ -366,6 +366,21 @@ DIT_API dit_status dit_op_gemm_gated_residual(const void* a, const void* b, cons
 DIT_API dit_status dit_op_gemm_swiglu(const void* a, const void* b_packed, const float* bias_packed, int M, int F, int K,
                               void* h, void* stream);
 
+/* GEMM with NVFP4 weights.  [H3] "What this push adds": the NVFP4 checkpoint's projections carry
+ * a U8 weight with two FP4 (E2M1) codes per byte ([N][K/2]), an F8_E4M3 scale per group of 16
+ * along K ([N][K/16]) and an F32 global scale; the logical weight is code * scale * global (even
+ * k in the low nibble).  dit_op_pack_nvfp4 repacks q and s once into the tile-contiguous layout
+ * the kernel streams (dit_nvfp4_packed_bytes(N, K) = N*K*9/16 bytes, 16-byte aligned).
+ * dit_op_gemm_nvfp4 computes out = A W^T + bias with A f16 [M, K] (every code * scale product
+ * is exact in f16, so the tensor cores run f16 x f16 with fp32 accumulation; the global scale
+ * multiplies the accumulator).  out_kind 0 bf16, 1 fp32, 2 f16, [M, N].  N % 256 == 0,
+ * K % 64 == 0, A 16-byte aligned; else DIT_ERR_INVALID_ARG before any launch. */
+DIT_API size_t dit_nvfp4_packed_bytes(int N, int K);
+DIT_API dit_status dit_op_pack_nvfp4(const uint8_t* q, const uint8_t* scales, int N, int K, void* packed,
+                             void* stream);
+DIT_API dit_status dit_op_gemm_nvfp4(const void* a_f16, const void* packed, float w_scale, const float* bias, int M,
+                             int N, int K, void* out, int out_kind, void* stream);
+
 /* fp32 GEMM y = x w^T + bias exactly as the fp32 forward computes its linear maps ([M3] "What
  * moved": every Linear is a MatmulBT with a rank-1 bias add; fp32 stays fp32): 3xTF32 on the
  * tcgen05 tensor cores (each operand split into tf32 hi + lo parts, three tf32 products per fp32

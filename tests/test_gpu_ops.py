@@ -435,3 +435,66 @@ def test_euler_unaligned_view_bit_exact():
     ref = oracle.euler_step(x[1:], v[1:], np.float32(0.5), np.float32(0.48))
     got = xd.cpu().numpy()
     assert got[0] == x[0] and np.array_equal(got[1:].view(np.uint32), ref.view(np.uint32))
+
+
+# ------------------------------------------------------------------------------------------------
+# NVFP4 weights
+# ------------------------------------------------------------------------------------------------
+
+def _nvfp4_tiles(q, s, N, K):
+    """The tile-contiguous layout, built independently on the host: per (256-row block, 64-column
+    block) the 256 rows' 32 code bytes, then their 4 scale bytes."""
+    out = []
+    for nb in range(N // 256):
+        for kb in range(K // 64):
+            out.append(q[nb * 256:(nb + 1) * 256, kb * 32:(kb + 1) * 32].reshape(-1))
+            out.append(s[nb * 256:(nb + 1) * 256, kb * 4:(kb + 1) * 4].reshape(-1))
+    return np.concatenate(out)
+
+
+def test_pack_nvfp4_layout_is_exact():
+    dit, gu = _dit(), _gu()
+    N, K = 512, 192
+    q, s, g = synth.make_nvfp4(70, "w", N, K)
+    packed = torch.zeros(dit.nvfp4_packed_bytes(N, K), dtype=torch.uint8, device="cuda")
+    dit.pack_nvfp4(torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda(), packed)
+    assert np.array_equal(packed.cpu().numpy(), _nvfp4_tiles(q, s, N, K))
+
+
+@pytest.mark.parametrize("M,N,K,out_kind", [(1, 256, 64, 1), (200, 512, 1024, 1), (300, 768, 3072, 0),
+                                            (1000, 256, 128, 2), (129, 9216, 3072, 1)])
+def test_gemm_nvfp4_matches_oracle(M, N, K, out_kind):
+    """out = A W^T + bias with W = E2M1 code * E4M3 scale * global: the products are exact in f16,
+    so the only error is fp32 accumulation, bounded by (K + 2) 2^-23 sum|a||w|, plus the output
+    rounding (bf16 2^-8, f16 2^-11 relative)."""
+    dit, gu = _dit(), _gu()
+    q, s, g = synth.make_nvfp4(71, f"w{N}x{K}", N, K)
+    a = synth.normal(71, f"a{M}x{K}", (M, K), 1.0).astype(np.float16)
+    bias = synth.normal(71, f"b{N}", (N,), 0.1)
+    packed = torch.empty(dit.nvfp4_packed_bytes(N, K), dtype=torch.uint8, device="cuda")
+    dit.pack_nvfp4(torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda(), packed)
+    odt = {0: torch.bfloat16, 1: torch.float32, 2: torch.float16}[out_kind]
+    out = torch.full((M, N), float("nan"), dtype=odt, device="cuda")
+    dit.gemm_nvfp4(torch.from_numpy(a).cuda(), packed, g, gu.dev_f32(bias), N, out, out_kind)
+    got = out.double().cpu().numpy()
+    oracle.set_threads(8)
+    ref = oracle.nvfp4_linear(a.astype(np.float64), q, s, g, bias)
+    # sum|a||w|: the same linear with |A| and the codes' sign bits cleared (the scales are positive)
+    sumabs = oracle.nvfp4_linear(np.abs(a.astype(np.float64)), (q & 0x77).astype(np.uint8), s, g)
+    oracle.set_threads(1)
+    rel = {0: 2.0 ** -8, 1: 0.0, 2: 2.0 ** -11}[out_kind]
+    bound = (K + 2) * 2.0 ** -23 * sumabs + rel * np.abs(ref) + 1e-30
+    assert np.isfinite(got).all()
+    assert np.all(np.abs(got - ref) <= bound), np.abs(got - ref).max()
+
+
+def test_gemm_nvfp4_rejects_bad_shapes():
+    dit = _dit()
+    lib = dit.lib()
+    a = torch.zeros((4, 64), dtype=torch.float16, device="cuda")
+    p = torch.zeros(dit.nvfp4_packed_bytes(256, 64), dtype=torch.uint8, device="cuda")
+    o = torch.zeros((4, 256), dtype=torch.float32, device="cuda")
+    assert lib.dit_op_gemm_nvfp4(a.data_ptr(), p.data_ptr(), 1.0, None, 4, 128, 64, o.data_ptr(), 1, None) != 0
+    assert lib.dit_op_gemm_nvfp4(a.data_ptr(), p.data_ptr(), 1.0, None, 4, 256, 48, o.data_ptr(), 1, None) != 0
+    assert lib.dit_op_gemm_nvfp4(a.data_ptr(), p.data_ptr(), 1.0, None, 4, 256, 64, o.data_ptr(), 3, None) != 0
+    assert dit.nvfp4_packed_bytes(100, 64) == 0

@@ -1243,6 +1243,31 @@ dit_status dit_op_gemm(const void* a, const void* b, const float* bias, int M, i
   return e == cudaSuccess ? DIT_OK : cuda_err(nullptr, e, "gemm");
 }
 
+size_t dit_nvfp4_packed_bytes(int N, int K) {
+  if (N <= 0 || K <= 0 || N % 256 || K % 64) return 0;
+  return (size_t)N * K * 9 / 16;
+}
+
+dit_status dit_op_pack_nvfp4(const uint8_t* q, const uint8_t* scales, int N, int K, void* packed, void* stream) {
+  if (!q || !scales || !packed || N <= 0 || K <= 0 || N % 256 || K % 64 || !aligned16(packed))
+    return set_err(nullptr, DIT_ERR_INVALID_ARG, "bad NVFP4 pack arguments (N %% 256, K %% 64, 16-byte aligned out)");
+  cudaError_t e = nvfp4_pack_launch(q, scales, N, K, static_cast<uint8_t*>(packed), static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DIT_OK : cuda_err(nullptr, e, "nvfp4 pack");
+}
+
+dit_status dit_op_gemm_nvfp4(const void* a_f16, const void* packed, float w_scale, const float* bias, int M, int N,
+                             int K, void* out, int out_kind, void* stream) {
+  if (!a_f16 || !packed || !out || M < 1 || N <= 0 || K <= 0 || N % 256 || K % 64 || !aligned16(a_f16) ||
+      !aligned16(packed) || out_kind < 0 || out_kind > 2)
+    return set_err(nullptr, DIT_ERR_INVALID_ARG, "bad NVFP4 GEMM arguments");
+  GemmArgs g{};
+  g.M = M; g.N = N; g.K = K; g.bias = bias; g.out = out; g.out_kind = out_kind;
+  g.b_packed = static_cast<const uint8_t*>(packed);
+  g.w_scale = w_scale;
+  cudaError_t e = gemm_nvfp4_launch(kEpiStore, a_f16, g, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DIT_OK : cuda_err(nullptr, e, "nvfp4 gemm");
+}
+
 dit_status dit_op_gemm_qkv_rope(const void* a, const void* b, const float* bias, int M, int d, int K, int n_heads,
                                 int head_dim, int rotary_dim, const float* cos_cache, const float* sin_cache, void* q,
                                 void* k, void* vt, int n_pad, void* stream) {

@@ -14,6 +14,20 @@
 //            one thread per output row
 //   the 512 TMEM columns hold two 128x256 fp32 accumulators, so the epilogue of tile i overlaps
 //   the main loop of tile i+1.
+//
+// NVFP4 weights ([H3] "What this push adds": U8 codes two per byte, an E4M3 scale per 16 along K,
+// an F32 global scale).  Every E2M1 x E4M3 product is exact in f16, and E2M1 -> f16 is one
+// conversion per pair, so this mode runs the same kind::f16 MMA with f16 operands:
+//   4 stages (3 with the residual epilogue's staging tile) of {A f16 tile (TMA), the dequantised
+//   B tile}, and a 2-slot ring of packed weight tiles (one 9 KB bulk copy each of a bind-time
+//   tile-contiguous repack), released by the converters once expanded
+//   warps 6-13 converters: wait for a packed tile, expand 256 rows x 64 codes with their scales
+//            into the stage's 128-byte-swizzled f16 B tile (the layout a TMA load would have
+//            written), fence the writes to the async proxy, release the packed slot and arrive on
+//            the stage's full barrier, which therefore completes when A has landed AND B is
+//            expanded: the MMA thread waits once per K-block, as in the bf16 mode (every wait in
+//            the issuing thread idles the pipe)
+//   the epilogues take acc * global scale in place of acc.
 #include "common.cuh"
 #include "kernels.h"
 #include "tmap.h"
@@ -30,6 +44,18 @@ constexpr int GEMM_THREADS = 192;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 constexpr int SMEM_BYTES_RESID = SMEM_BYTES + BM * 64 * 4;  // + the residual epilogue's staging tile
 constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+// NVFP4 mode
+constexpr int Q_STAGES = 4, Q_STAGES_RESID = 3;  // A + dequantised B stages
+constexpr int Q_RAW_SLOTS = 2;                   // packed weight tiles in flight
+constexpr int Q_RAW_BYTES = kNvfp4TileBytes;     // 256 rows x 32 bytes of codes, then 256 x 4 scales
+constexpr int Q_CODE_BYTES = BN * BK / 2;
+constexpr int Q_CONV_WARPS = 8;                  // one weight row per converter thread
+constexpr int Q_THREADS = GEMM_THREADS + 32 * Q_CONV_WARPS;
+constexpr int Q_SMEM_BYTES = Q_STAGES * STAGE_BYTES + Q_RAW_SLOTS * Q_RAW_BYTES + 1024 + 256;
+constexpr int Q_SMEM_BYTES_RESID = Q_STAGES_RESID * STAGE_BYTES + Q_RAW_SLOTS * Q_RAW_BYTES + 1024 + 256 + BM * 64 * 4;
+constexpr uint32_t IDESC_F16 = idesc_f16_f32(BM, BN);
+static_assert(Q_RAW_BYTES == BN * BK / 2 + BN * BK / 16, "packed tile size");
+static_assert(Q_SMEM_BYTES <= 227 * 1024 && Q_SMEM_BYTES_RESID <= 227 * 1024, "NVFP4 stages exceed shared memory");
 
 struct TileCoord {
   int mb, nb;
@@ -63,6 +89,11 @@ __device__ __forceinline__ void load_bias4(const float* b, int col, float (&o)[4
   }
 }
 
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 // ---------------------------------------------------------------------------------------------
 // epilogues: the calling thread owns tile row `row` (global), TMEM address `t` = its lane, the
 // accumulator's column 0.  n0 = first global output column of the tile.
@@ -80,7 +111,7 @@ __device__ __forceinline__ void epi_store(const GemmArgs& a, uint32_t t, int row
       float b[4];
       load_bias4(a.bias, n0 + c + i, b);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) v[i + j] = __uint_as_float(r[i + j]) + b[j];
+      for (int j = 0; j < 4; ++j) v[i + j] = __uint_as_float(r[i + j]) * a.w_scale + b[j];
     }
     if (a.out_kind == 0) {
       __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out) + (size_t)row * a.N + n0 + c;
@@ -88,12 +119,24 @@ __device__ __forceinline__ void epi_store(const GemmArgs& a, uint32_t t, int row
       for (int i = 0; i < 32; i += 8)
         st_global_v4(o + i, pack_bf16x2(v[i], v[i + 1]), pack_bf16x2(v[i + 2], v[i + 3]),
                      pack_bf16x2(v[i + 4], v[i + 5]), pack_bf16x2(v[i + 6], v[i + 7]));
+    } else if (a.out_kind == 2) {
+      __half* o = static_cast<__half*>(a.out) + (size_t)row * a.N + n0 + c;
+#pragma unroll
+      for (int i = 0; i < 32; i += 8)
+        st_global_v4(o + i, pack_f16x2(v[i], v[i + 1]), pack_f16x2(v[i + 2], v[i + 3]),
+                     pack_f16x2(v[i + 4], v[i + 5]), pack_f16x2(v[i + 6], v[i + 7]));
     } else {
       float* o = static_cast<float*>(a.out) + (size_t)row * a.N + n0 + c;
 #pragma unroll
       for (int i = 0; i < 32; i += 4) *reinterpret_cast<float4*>(o + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
     }
   }
+}
+
+__device__ __forceinline__ void store_f16x16(__half* o, const float (&v)[16]) {
+  st_global_v4(o, pack_f16x2(v[0], v[1]), pack_f16x2(v[2], v[3]), pack_f16x2(v[4], v[5]), pack_f16x2(v[6], v[7]));
+  st_global_v4(o + 8, pack_f16x2(v[8], v[9]), pack_f16x2(v[10], v[11]), pack_f16x2(v[12], v[13]),
+               pack_f16x2(v[14], v[15]));
 }
 
 __device__ __forceinline__ void store_bf16x16(__nv_bfloat16* o, const float (&v)[16]) {
@@ -128,7 +171,7 @@ __device__ __forceinline__ void epi_qkv(const GemmArgs& a, uint32_t t, int row, 
 #pragma unroll
         for (int j = 0; j < 4; ++j)
           vt[(size_t)(col0 + c + i + j) * a.n_pad + row] =
-              __float2bfloat16_rn(live ? __uint_as_float(r[i + j]) + b[j] : 0.f);
+              __float2bfloat16_rn(live ? __uint_as_float(r[i + j]) * a.w_scale + b[j] : 0.f);
       }
     }
     return;
@@ -158,8 +201,8 @@ __device__ __forceinline__ void epi_qkv(const GemmArgs& a, uint32_t t, int row, 
         float cc[4] = {cv.x, cv.y, cv.z, cv.w}, ss[4] = {sv.x, sv.y, sv.z, sv.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          float x1 = __uint_as_float(r1[i + j]) + b1[j];
-          float x2 = __uint_as_float(r2[i + j]) + b2[j];
+          float x1 = __uint_as_float(r1[i + j]) * a.w_scale + b1[j];
+          float x2 = __uint_as_float(r2[i + j]) * a.w_scale + b2[j];
           o1[i + j] = x1 * cc[j] - x2 * ss[j];
           o2[i + j] = x2 * cc[j] + x1 * ss[j];
         }
@@ -179,7 +222,7 @@ __device__ __forceinline__ void epi_qkv(const GemmArgs& a, uint32_t t, int row, 
         float b1[4];
         load_bias4(a.bias, n0 + hb + c + i, b1);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) o1[i + j] = __uint_as_float(r1[i + j]) + b1[j];
+        for (int j = 0; j < 4; ++j) o1[i + j] = __uint_as_float(r1[i + j]) * a.w_scale + b1[j];
       }
       store_bf16x16(dst + hb + c, o1);
     }
@@ -196,10 +239,12 @@ __device__ __forceinline__ void epi_qkv(const GemmArgs& a, uint32_t t, int row, 
 //   phase B  each warp walks 32 rows; per row its 32 lanes own 2 adjacent columns, so the loads and
 //            stores of x (and of the gate and bias) are 256 contiguous bytes per row.
 constexpr int RES_COLS = 64;
-constexpr int RES_BATCH = 32;  // rows whose loads a warp has in flight at once
+constexpr int RES_BATCH = 32;  // rows whose loads a warp has in flight at once (4 in the NVFP4 mode,
+                               // whose 448-thread launch leaves fewer registers per thread)
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
+template <int RB = RES_BATCH>
 __device__ __forceinline__ void epi_resid(const GemmArgs& a, uint32_t t, int tile_row0, int quarter, int ew, int n0,
                                           float* stage, uint64_t* tempty_bar) {
   const int lane = threadIdx.x & 31;
@@ -231,11 +276,11 @@ __device__ __forceinline__ void epi_resid(const GemmArgs& a, uint32_t t, int til
     if (a.bias) bb = *reinterpret_cast<const float2*>(a.bias + col);
     const int chunk = lane >> 1, half8 = (lane & 1) * 8;
 #pragma unroll 1
-    for (int rr0 = 0; rr0 < 32; rr0 += RES_BATCH) {
-      float2 acc[RES_BATCH], xv[RES_BATCH], gv[RES_BATCH];
-      int rows[RES_BATCH];
+    for (int rr0 = 0; rr0 < 32; rr0 += RB) {
+      float2 acc[RB], xv[RB], gv[RB];
+      int rows[RB];
 #pragma unroll
-      for (int u = 0; u < RES_BATCH; ++u) {
+      for (int u = 0; u < RB; ++u) {
         const int rt = ew * 32 + rr0 + u;
         rows[u] = tile_row0 + rt;
         const uint32_t sa = smem_u32(stage) + rt * (RES_COLS * 4) + ((chunk ^ (rt & 7)) << 4) + half8;
@@ -247,11 +292,11 @@ __device__ __forceinline__ void epi_resid(const GemmArgs& a, uint32_t t, int til
         }
       }
 #pragma unroll
-      for (int u = 0; u < RES_BATCH; ++u) {
+      for (int u = 0; u < RB; ++u) {
         if (rows[u] < a.M) {
           float2 o;
-          o.x = xv[u].x + gv[u].x * (acc[u].x + bb.x);
-          o.y = xv[u].y + gv[u].y * (acc[u].y + bb.y);
+          o.x = xv[u].x + gv[u].x * (acc[u].x * a.w_scale + bb.x);
+          o.y = xv[u].y + gv[u].y * (acc[u].y * a.w_scale + bb.y);
           *reinterpret_cast<float2*>(a.x + (size_t)rows[u] * a.N + col) = o;
         }
       }
@@ -267,6 +312,7 @@ __device__ __forceinline__ void epi_swiglu(const GemmArgs& a, uint32_t t, int ro
   const int F = a.N / 2;
   const int f0 = n0 / 2;
   __nv_bfloat16* hrow = static_cast<__nv_bfloat16*>(a.out) + (size_t)row * F + f0;
+  __half* hrow16 = static_cast<__half*>(a.out) + (size_t)row * F + f0;  // out_kind 2
 #pragma unroll 1
   for (int c = 0; c < BN / 2; c += 16) {
     uint32_t ru[16], rg[16];
@@ -283,29 +329,80 @@ __device__ __forceinline__ void epi_swiglu(const GemmArgs& a, uint32_t t, int ro
       load_bias4(a.bias, n0 + BN / 2 + c + i, bg);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        float u = __uint_as_float(ru[i + j]) + bu[j];
-        float g = __uint_as_float(rg[i + j]) + bg[j];
+        float u = __uint_as_float(ru[i + j]) * a.w_scale + bu[j];
+        float g = __uint_as_float(rg[i + j]) * a.w_scale + bg[j];
         h[i + j] = u * silu_f(g);
       }
     }
-    store_bf16x16(hrow + c, h);
+    if (a.out_kind == 2)
+      store_f16x16(hrow16 + c, h);
+    else
+      store_bf16x16(hrow + c, h);
   }
 }
 
-template <int EPI>
-__global__ void __launch_bounds__(GEMM_THREADS, 1)
+// NVFP4 converter: expand row r of a stage's packed weight tile (256 rows x 64
+// E2M1 codes, even k in the low nibble, and 4 E4M3 scales per row, one per 16 codes) into f16 in
+// the layout a 128-byte-swizzled TMA load of a [256 x 64] f16 box writes: row r at r * 128 bytes,
+// its 16-byte chunk c at position c ^ (r & 7).  code * scale is exact in f16.
+__device__ __forceinline__ void nvfp4_expand_row(uint32_t raw, uint32_t dst, int r) {
+  {
+    uint32_t w[8], sc;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(raw + r * 32));
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7]) : "r"(raw + r * 32 + 16));
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(sc) : "r"(raw + Q_CODE_BYTES + r * 4));
+    uint32_t s01, s23;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s01) : "h"(static_cast<uint16_t>(sc & 0xFFFFu)));
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s23) : "h"(static_cast<uint16_t>(sc >> 16)));
+    uint32_t sg[4];  // each group's scale in both halves
+    asm("prmt.b32 %0, %1, %1, 0x1010;" : "=r"(sg[0]) : "r"(s01));
+    asm("prmt.b32 %0, %1, %1, 0x3232;" : "=r"(sg[1]) : "r"(s01));
+    asm("prmt.b32 %0, %1, %1, 0x1010;" : "=r"(sg[2]) : "r"(s23));
+    asm("prmt.b32 %0, %1, %1, 0x3232;" : "=r"(sg[3]) : "r"(s23));
+    const uint32_t row = dst + r * 128;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      uint32_t h[8];
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+        asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+            "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+            "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+            "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+            "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+            "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+            : "=r"(h[4 * q]), "=r"(h[4 * q + 1]), "=r"(h[4 * q + 2]), "=r"(h[4 * q + 3])
+            : "r"(w[2 * g + q]));
+#pragma unroll
+      for (int j = 0; j < 8; ++j) asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(h[j]) : "r"(sg[g]));
+      st_shared_v4(row + (((2 * g) ^ (r & 7)) << 4), h[0], h[1], h[2], h[3]);
+      st_shared_v4(row + (((2 * g + 1) ^ (r & 7)) << 4), h[4], h[5], h[6], h[7]);
+    }
+  }
+}
+
+template <int EPI, bool BQ>
+__global__ void __launch_bounds__(BQ ? Q_THREADS : GEMM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
+  constexpr int NST = BQ ? (EPI == kEpiGatedResid ? Q_STAGES_RESID : Q_STAGES) : STAGES;
+  constexpr int RING_BYTES = NST * STAGE_BYTES + (BQ ? Q_RAW_SLOTS * Q_RAW_BYTES : 0);
+  constexpr uint32_t ID = BQ ? IDESC_F16 : IDESC;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = smem + STAGES * A_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  uint64_t* empty = full + STAGES;
-  uint64_t* tfull = empty + STAGES;
+  uint8_t* sB = smem + NST * A_BYTES;
+  uint8_t* sQ = sB + NST * B_BYTES;  // NVFP4 mode: the packed weight tiles (Q_RAW_SLOTS)
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + RING_BYTES);
+  uint64_t* empty = full + NST;
+  uint64_t* rawfull = empty + NST;                     // NVFP4: a packed tile has landed
+  uint64_t* rawempty = rawfull + (BQ ? Q_RAW_SLOTS : 0);  // NVFP4: the converters are done with a slot
+  uint64_t* tfull = rawempty + (BQ ? Q_RAW_SLOTS : 0);
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* res_stage = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES + 256);  // residual epilogue only
+  float* res_stage = reinterpret_cast<float*>(smem + RING_BYTES + 256);  // residual epilogue only
 
   if (args.status && (*reinterpret_cast<volatile int*>(args.status) & kDevLayout)) return;
 
@@ -315,10 +412,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const int gn = args.group_n > 0 ? args.group_n : n_n;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(&full[s], BQ ? 1 + Q_CONV_WARPS : 1);  // NVFP4: + one arrival per converter warp
       mbar_init(&empty[s], 1);
     }
+    if (BQ)
+      for (int q = 0; q < Q_RAW_SLOTS; ++q) {
+        mbar_init(&rawfull[q], 1);
+        mbar_init(&rawempty[q], Q_CONV_WARPS);
+      }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&tfull[s], 1);
       mbar_init(&tempty[s], 4);
@@ -328,7 +430,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
+    if (!BQ) tma_prefetch_desc(&tmB);
   }
   if (warp == 1) tmem_alloc(tmem_slot, 512);
   tc_fence_before();
@@ -338,16 +440,31 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
+      int stage = 0, rslot = 0;
+      uint32_t phase = 0, rphase = 0;
       for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
         TileCoord tc = tile_coord(tile, n_m, n_n, gn);
         for (int kb = 0; kb < k_blocks; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, args.status)) goto producer_done;
-          mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-          tma_load_2d(sA + stage * A_BYTES, &tmA, &full[stage], kb * BK, tc.mb * BM);
-          tma_load_2d(sB + stage * B_BYTES, &tmB, &full[stage], kb * BK, tc.nb * BN);
-          if (++stage == STAGES) {
+          if (BQ) {
+            // the packed slot is free once the converters expanded its previous tile; the stage's B
+            // tile is free because empty[stage] fired before this copy is issued
+            if (!mbar_wait(&rawempty[rslot], rphase ^ 1, abort_flag, args.status)) goto producer_done;
+            mbar_arrive_expect_tx(&rawfull[rslot], Q_RAW_BYTES);
+            bulk_load(sQ + rslot * Q_RAW_BYTES, args.b_packed + ((size_t)tc.nb * k_blocks + kb) * Q_RAW_BYTES,
+                      Q_RAW_BYTES, &rawfull[rslot]);
+            if (++rslot == Q_RAW_SLOTS) {
+              rslot = 0;
+              rphase ^= 1;
+            }
+            mbar_arrive_expect_tx(&full[stage], A_BYTES);
+            tma_load_2d(sA + stage * A_BYTES, &tmA, &full[stage], kb * BK, tc.mb * BM);
+          } else {
+            mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+            tma_load_2d(sA + stage * A_BYTES, &tmA, &full[stage], kb * BK, tc.mb * BM);
+            tma_load_2d(sB + stage * B_BYTES, &tmB, &full[stage], kb * BK, tc.nb * BN);
+          }
+          if (++stage == NST) {
             stage = 0;
             phase ^= 1;
           }
@@ -355,9 +472,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       }
       // Drain: wait until the MMAs consumed every stage we filled, so no TMA write into this
       // CTA's shared memory is still in flight when the CTA exits.
-      for (int s = 0; s < STAGES; ++s) {
+      for (int s = 0; s < NST; ++s) {
         if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, args.status)) break;
-        if (++stage == STAGES) {
+        if (++stage == NST) {
           stage = 0;
           phase ^= 1;
         }
@@ -385,9 +502,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           const uint32_t b0 = smem_u32(sB + stage * B_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            umma_bf16(d_tmem, sdesc_sw128(a0 + k * 32), sdesc_sw128(b0 + k * 32), IDESC, (kb | k) != 0);
+            umma_bf16(d_tmem, sdesc_sw128(a0 + k * 32), sdesc_sw128(b0 + k * 32), ID, (kb | k) != 0);
           umma_commit(&empty[stage]);
-          if (++stage == STAGES) {
+          if (++stage == NST) {
             stage = 0;
             phase ^= 1;
           }
@@ -398,6 +515,34 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         if (acc == 0) acc_phase ^= 1;
       }
     }
+  } else if (BQ && warp >= 6) {
+    // converters: one pass over the same (tile, k-block) sequence as the producer
+    // The stage's B tile is free: the packed tile of this fill was copied only after the MMA's
+    // commit for the previous fill of the stage (the producer waits on empty[stage] first).
+    const int ct = threadIdx.x - GEMM_THREADS;
+    int stage = 0, rslot = 0;
+    uint32_t phase = 0, rphase = 0;
+    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+      for (int kb = 0; kb < k_blocks; ++kb) {
+        if (!mbar_wait(&rawfull[rslot], rphase, abort_flag, args.status)) goto convert_done;
+        nvfp4_expand_row(smem_u32(sQ + rslot * Q_RAW_BYTES), smem_u32(sB + stage * B_BYTES), ct);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&rawempty[rslot]);
+          mbar_arrive(&full[stage]);
+        }
+        if (++rslot == Q_RAW_SLOTS) {
+          rslot = 0;
+          rphase ^= 1;
+        }
+        if (++stage == NST) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+  convert_done:;
   } else {
     const int quarter = warp & 3;  // TMEM lanes [32 * quarter, +32) belong to this warp
     int acc = 0;
@@ -410,7 +555,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const uint32_t t = tmem + acc * BN + (static_cast<uint32_t>(quarter * 32) << 16);
       const int n0 = tc.nb * BN;
       if (EPI == kEpiGatedResid) {
-        epi_resid(args, t, tc.mb * BM, quarter, warp - 2, n0, res_stage, &tempty[acc]);
+        epi_resid<BQ ? 4 : RES_BATCH>(args, t, tc.mb * BM, quarter, warp - 2, n0, res_stage, &tempty[acc]);
       } else {
         if (EPI == kEpiStore) epi_store(args, t, row, n0);
         if (EPI == kEpiQkvRope) epi_qkv(args, t, row, n0);
@@ -432,19 +577,45 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   }
 }
 
-template <int EPI>
+template <int EPI, bool BQ>
 cudaError_t launch_t(const void* A, const void* B, const GemmArgs& args, cudaStream_t stream) {
-  constexpr int smem = EPI == kEpiGatedResid ? SMEM_BYTES_RESID : SMEM_BYTES;
+  constexpr int smem = BQ ? (EPI == kEpiGatedResid ? Q_SMEM_BYTES_RESID : Q_SMEM_BYTES)
+                          : (EPI == kEpiGatedResid ? SMEM_BYTES_RESID : SMEM_BYTES);
   static unsigned long long smem_set = 0;
-  cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(gemm_kernel<EPI>), smem, &smem_set);
+  cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(gemm_kernel<EPI, BQ>), smem, &smem_set);
   if (e != cudaSuccess) return e;
+  // The NVFP4 mode's A is f16: the map only moves 2-byte elements, so the bf16 map serves it.
   CUtensorMap ta, tb;
   if (!make_tmap_bf16_2d(&ta, A, args.K, args.M, (uint64_t)args.K * 2, BK, BM)) return cudaErrorInvalidValue;
-  if (!make_tmap_bf16_2d(&tb, B, args.K, args.N, (uint64_t)args.K * 2, BK, BN)) return cudaErrorInvalidValue;
+  if (BQ)
+    tb = ta;  // unused
+  else if (!make_tmap_bf16_2d(&tb, B, args.K, args.N, (uint64_t)args.K * 2, BK, BN))
+    return cudaErrorInvalidValue;
   const int tiles = ((args.M + BM - 1) / BM) * (args.N / BN);
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  gemm_kernel<EPI><<<grid, GEMM_THREADS, smem, stream>>>(ta, tb, args);
+  gemm_kernel<EPI, BQ><<<grid, BQ ? Q_THREADS : GEMM_THREADS, smem, stream>>>(ta, tb, args);
   return cudaGetLastError();
+}
+
+__global__ void nvfp4_pack_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ sc, int N, int K,
+                                  uint8_t* __restrict__ packed) {
+  const int kbs = K / BK;
+  const size_t total = (size_t)(N / BN) * kbs * Q_RAW_BYTES;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+    const size_t t = i / Q_RAW_BYTES;
+    const int o = (int)(i - t * Q_RAW_BYTES);
+    const int nb = (int)(t / kbs), kb = (int)(t - (size_t)nb * kbs);
+    uint8_t v;
+    if (o < Q_CODE_BYTES) {
+      const int r = o / (BK / 2), j = o - r * (BK / 2);
+      v = q[(size_t)(nb * BN + r) * (K / 2) + kb * (BK / 2) + j];
+    } else {
+      const int o2 = o - Q_CODE_BYTES;
+      const int r = o2 / (BK / 16), j = o2 - r * (BK / 16);
+      v = sc[(size_t)(nb * BN + r) * (K / 16) + kb * (BK / 16) + j];
+    }
+    packed[i] = v;
+  }
 }
 
 }  // namespace
@@ -459,12 +630,40 @@ cudaError_t gemm_launch(int epilogue, const void* A, const void* B, const GemmAr
     args.group_n = g < 1 ? 1 : g;
   }
   switch (epilogue) {
-    case kEpiStore: return launch_t<kEpiStore>(A, B, args, stream);
-    case kEpiQkvRope: return launch_t<kEpiQkvRope>(A, B, args, stream);
-    case kEpiGatedResid: return launch_t<kEpiGatedResid>(A, B, args, stream);
-    case kEpiSwiglu: return launch_t<kEpiSwiglu>(A, B, args, stream);
+    case kEpiStore: return launch_t<kEpiStore, false>(A, B, args, stream);
+    case kEpiQkvRope: return launch_t<kEpiQkvRope, false>(A, B, args, stream);
+    case kEpiGatedResid: return launch_t<kEpiGatedResid, false>(A, B, args, stream);
+    case kEpiSwiglu: return launch_t<kEpiSwiglu, false>(A, B, args, stream);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t gemm_nvfp4_launch(int epilogue, const void* A, const GemmArgs& args_in, cudaStream_t stream) {
+  GemmArgs args = args_in;
+  if (args.M <= 0) return cudaSuccess;
+  if (!args.b_packed || (reinterpret_cast<uintptr_t>(args.b_packed) & 15) || args.N % BN || args.K % BK)
+    return cudaErrorInvalidValue;
+  if (args.group_n <= 0) {
+    long long per_nb = (long long)BN * args.K * 9 / 16;  // codes + scales of one N-block
+    int g = (int)((48ll << 20) / (per_nb > 0 ? per_nb : 1));
+    args.group_n = g < 1 ? 1 : g;
+  }
+  switch (epilogue) {
+    case kEpiStore: return launch_t<kEpiStore, true>(A, nullptr, args, stream);
+    case kEpiQkvRope: return launch_t<kEpiQkvRope, true>(A, nullptr, args, stream);
+    case kEpiGatedResid: return launch_t<kEpiGatedResid, true>(A, nullptr, args, stream);
+    case kEpiSwiglu: return launch_t<kEpiSwiglu, true>(A, nullptr, args, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t nvfp4_pack_launch(const uint8_t* q, const uint8_t* s, int N, int K, uint8_t* packed, cudaStream_t st) {
+  if (N % BN || K % BK || N <= 0 || K <= 0) return cudaErrorInvalidValue;
+  const size_t total = (size_t)(N / BN) * (K / BK) * Q_RAW_BYTES;
+  size_t g = (total + 255) / 256;
+  const size_t cap = (size_t)num_sms() * 16;
+  nvfp4_pack_kernel<<<(unsigned)(g < cap ? g : cap), 256, 0, st>>>(q, s, N, K, packed);
+  return cudaGetLastError();
 }
 
 }  // namespace dit

@@ -50,10 +50,20 @@ struct GemmArgs {
   // common
   int* status;             // device status word (may be null)
   int group_n;             // N-blocks per raster group (L2 reuse of B)
+  // NVFP4 weights (gemm_nvfp4_launch): B is the tile-contiguous repack of nvfp4_pack_launch, A f16;
+  // every epilogue takes acc * w_scale (the weight's global scale) in place of acc
+  const uint8_t* b_packed = nullptr;
+  float w_scale = 1.f;
 };
 
 // Launch D = A B^T with the given epilogue.  A bf16 [M, K], B bf16 [N, K].  Returns a CUDA error.
 cudaError_t gemm_launch(int epilogue, const void* A, const void* B, const GemmArgs& args, cudaStream_t stream);
+// The same with NVFP4 weights: A f16 [M, K]; B from args.b_packed (N % 256 == 0, K % 64 == 0).
+cudaError_t gemm_nvfp4_launch(int epilogue, const void* A, const GemmArgs& args, cudaStream_t stream);
+// NVFP4 weight repack: q [N][K/2] (two E2M1 per byte, even k low), s [N][K/16] (E4M3) ->
+// [N/256][K/64] tiles of 9216 bytes: 256 rows x 32 bytes of codes, then 256 rows x 4 scales.
+constexpr int kNvfp4TileBytes = 9216;
+cudaError_t nvfp4_pack_launch(const uint8_t* q, const uint8_t* s, int N, int K, uint8_t* packed, cudaStream_t st);
 
 // Attention: q, k bf16 [N, H*Dh], vt bf16 [H*Dh, n_pad], o bf16 [N, H*Dh].  `items` is the
 // device tile list built by attention_schedule_launch (int2 {doc, q_start}), `count` its length.

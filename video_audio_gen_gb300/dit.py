@@ -29,7 +29,8 @@ EXPORTS = ["dit_create", "dit_destroy", "dit_last_error", "dit_workspace_bytes",
            "dit_forward_latent", "dit_patchify", "dit_unpatchify", "dit_audio_pack", "dit_audio_unpack", "dit_get_stats", "dit_sync_status",
            "dit_set_dump", "dit_set_kernel_timing", "dit_get_kernel_times", "dit_op_norm_modulate",
            "dit_op_rope_cache", "dit_op_adaln", "dit_op_gemm", "dit_op_gemm_qkv_rope", "dit_op_gemm_gated_residual",
-           "dit_op_gemm_swiglu", "dit_gemm_f32_workspace_bytes", "dit_op_gemm_f32", "dit_op_pack_ffn_in", "dit_attention_workspace_bytes", "dit_op_attention",
+           "dit_op_gemm_swiglu", "dit_nvfp4_packed_bytes", "dit_op_pack_nvfp4", "dit_op_gemm_nvfp4",
+           "dit_gemm_f32_workspace_bytes", "dit_op_gemm_f32", "dit_op_pack_ffn_in", "dit_attention_workspace_bytes", "dit_op_attention",
            "dit_op_attention_noalloc", "dit_selftest_wait_timeout"]
 
 
@@ -129,6 +130,9 @@ def lib():
             "dit_op_pack_ffn_in": (i32, [vp, vp, i32, i32, vp, vp, vp]),
             "dit_attention_workspace_bytes": (sz, [i32, i32]),
             "dit_gemm_f32_workspace_bytes": (sz, [i32, i32, i32]),
+            "dit_nvfp4_packed_bytes": (sz, [i32, i32]),
+            "dit_op_pack_nvfp4": (i32, [vp, vp, i32, i32, vp, vp]),
+            "dit_op_gemm_nvfp4": (i32, [vp, vp, f32, vp, i32, i32, i32, vp, i32, vp]),
             "dit_op_gemm_f32": (i32, [vp, vp, vp, i32, i32, i32, vp, vp, vp]),
             "dit_op_attention": (i32, [vp, vp, vp, i32, vp, i32, i32, i32, i32, vp, vp, vp]),
             "dit_op_attention_noalloc": (i32, [vp, vp, vp, i32, vp, i32, i32, i32, i32, vp, vp]),
@@ -363,6 +367,24 @@ def gemm(a, b, bias, out, out_kind: int, stream=None):
     M, K = a.shape
     N = b.shape[0]
     _check(lib().dit_op_gemm(_ptr(a), _ptr(b), _ptr(bias), M, N, K, _ptr(out), out_kind, _stream(stream)))
+
+
+def nvfp4_packed_bytes(N: int, K: int) -> int:
+    return int(lib().dit_nvfp4_packed_bytes(N, K))
+
+
+def pack_nvfp4(q, scales, packed, stream=None):
+    """dit_op_pack_nvfp4: q u8 [N, K/2], scales u8 [N, K/16] (device) -> packed (device bytes)."""
+    N = q.shape[0]
+    K = scales.shape[1] * 16
+    _check(lib().dit_op_pack_nvfp4(_ptr(q), _ptr(scales), N, K, _ptr(packed), _stream(stream)))
+
+
+def gemm_nvfp4(a_f16, packed, w_scale: float, bias, N: int, out, out_kind: int, stream=None):
+    """dit_op_gemm_nvfp4: out = A W^T + bias, A f16 [M, K], W the packed NVFP4 weight [N, K]."""
+    M, K = a_f16.shape
+    _check(lib().dit_op_gemm_nvfp4(_ptr(a_f16), _ptr(packed), float(w_scale), _ptr(bias), M, N, K, _ptr(out),
+                                   out_kind, _stream(stream)))
 
 
 def gemm_f32_workspace_bytes(M: int, N: int, K: int) -> int:
