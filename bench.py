@@ -452,6 +452,123 @@ def run_gpu(args, w, dist, rank, world):
                 launches=launches, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, flops=fl["total"], docs=D, lay=lay)
 
 
+def run_nvfp4_gemm(args):
+    """The four linear maps of one block of the video+audio model at its full 17,408-token sequence,
+    with NVFP4 weights (E2M1 codes, an E4M3 scale per 16 along K, fp32 global scale; f16
+    activations) and, on the same shapes, with bf16 weights through the bf16 engine.  A step is one
+    pass over the four NVFP4 GEMMs; the bf16 GEMMs run in a second pass for the comparison."""
+    import torch
+
+    import synth
+    from video_audio_gen_gb300 import dit
+
+    dev = torch.cuda.current_device()
+    m = synth.WORKLOADS["video_audio_bf16"]["model"]
+    d, F = m["hidden"], m["ffn_hidden"]
+    M = synth.build_layout(synth.WORKLOADS["video_audio_bf16"]["docs"])["n_tokens"]
+    shapes = {"gemm_qkv": (3 * d, d), "gemm_out": (d, d), "gemm_ffn_up": (2 * F, d), "gemm_ffn_down": (d, F)}
+    ops = {}
+    for k, (N, K) in shapes.items():
+        q, sc, g = synth.make_nvfp4(5, f"bench.{k}", N, K)
+        packed = torch.empty(dit.nvfp4_packed_bytes(N, K), dtype=torch.uint8, device="cuda")
+        dit.pack_nvfp4(torch.from_numpy(q).cuda(), torch.from_numpy(sc).cuda(), packed)
+        a16 = torch.from_numpy(synth.normal(5, f"bench.a.{k}", (M, K), 1.0).astype(np.float16)).cuda()
+        wbf = torch.from_numpy(synth.normal(5, f"bench.w.{k}", (N, K), 0.02)).cuda().bfloat16()
+        out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        ops[k] = dict(N=N, K=K, packed=packed, g=g, a16=a16, abf=a16.bfloat16(), wbf=wbf, out=out)
+    stream = torch.cuda.current_stream()
+
+    def timed(fn_for):
+        ev = {k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for k in ops}
+        tot = {k: 0.0 for k in ops}
+        for _ in range(args.steps):
+            for k, o in ops.items():
+                ev[k][0].record(stream)
+                fn_for(o)
+                ev[k][1].record(stream)
+            torch.cuda.synchronize()
+            for k in ops:
+                tot[k] += ev[k][0].elapsed_time(ev[k][1])
+        return {k: v / args.steps for k, v in tot.items()}
+
+    nv = lambda o: dit.gemm_nvfp4(o["a16"], o["packed"], o["g"], None, o["N"], o["out"], 0)
+    bf = lambda o: dit.gemm(o["abf"], o["wbf"], None, o["out"], 0)
+    for _ in range(args.warmup):
+        for o in ops.values():
+            nv(o)
+            bf(o)
+    torch.cuda.synchronize()
+    with ClockSampler(dev) as clk:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            for o in ops.values():
+                nv(o)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        t_nv = timed(nv)
+        t_bf = timed(bf)
+    ms_step = e0.elapsed_time(e1) / args.steps
+    flops = {k: 2.0 * M * o["N"] * o["K"] for k, o in ops.items()}
+    peaks, peak_src = load_peaks()
+    peak = peaks["bf16_tflops_sustained"]  # f16 and bf16 share the tensor rate
+    kernels = {}
+    for k in ops:
+        tf_nv = flops[k] / (t_nv[k] * 1e-3) / 1e12
+        tf_bf = flops[k] / (t_bf[k] * 1e-3) / 1e12
+        kernels[k] = {"M": M, "N": ops[k]["N"], "K": ops[k]["K"], "nvfp4_ms": round(t_nv[k], 4),
+                      "nvfp4_tflops": round(tf_nv, 1), "frac": round(tf_nv / peak, 3),
+                      "bf16_ms": round(t_bf[k], 4), "bf16_tflops": round(tf_bf, 1),
+                      "weight_bytes_nvfp4": ops[k]["N"] * ops[k]["K"] * 9 // 16,
+                      "weight_bytes_bf16": ops[k]["N"] * ops[k]["K"] * 2}
+    top = max(kernels, key=lambda k: t_nv[k])
+    value = sum(flops.values()) / (ms_step * 1e-3) / 1e12
+    line = {"metric": "NVFP4-weight GEMM TFLOP/s on the four linear maps of one video+audio block (1 GB300)",
+            "value": round(value, 1), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f16 x nvfp4", "data": "synthetic (random valid NVFP4 codes, N(0, 1) f16 activations)",
+            "config": {"workload": f"nvfp4_gemm: M={M} tokens; QKV {3 * d}x{d}, out {d}x{d}, FFN up {2 * F}x{d}, "
+                                   f"FFN down {d}x{F}", "l2": "activations and outputs (>400 MB) larger than L2; "
+                                                            "weights L2-resident as in the forward"},
+            "roofline": {"bound": "tensor", "kernel": f"{top} (nvfp4)", "achieved": kernels[top]["nvfp4_tflops"],
+                         "peak": peak, "unit": "TFLOP/s", "frac": kernels[top]["frac"], "traffic": None,
+                         "peak_source": f"bf16_tflops_sustained of {peak_src} (f16 runs at the bf16 rate)",
+                         "algorithmic_flops_per_launch": flops[top]},
+            "kernels": kernels, "gpu_launches": args.steps * len(ops), "clocks": clk.summary()}
+    print(json.dumps(line))
+
+
+def run_nvfp4_reference(args):
+    """The oracle's NVFP4 linear (double precision) on a bounded sample of rows of the QKV shape,
+    scaled to TFLOP/s."""
+    import oracle
+    import synth
+    d = synth.WORKLOADS["video_audio_bf16"]["model"]["hidden"]
+    N, K = 3 * d, d
+    q, sc, g = synth.make_nvfp4(5, "bench.gemm_qkv", N, K)
+    threads = os.cpu_count() or 1
+    oracle.set_threads(threads)
+    vals = []
+    R = 4
+    for _ in range(args.steps):
+        a = synth.normal(5, "bench.a.sample", (R, K), 1.0).astype(np.float16).astype(np.float64)
+        t0 = time.perf_counter()
+        oracle.nvfp4_linear(a, q, sc, g)
+        dt = time.perf_counter() - t0
+        vals.append(2.0 * R * N * K / dt / 1e12)
+    oracle.set_threads(1)
+    v = statistics.median(vals)
+    line = {"impl": "reference", "metric": "NVFP4-weight GEMM TFLOP/s on the four linear maps of one video+audio "
+            "block (1 GB300)", "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"nvfp4_gemm: the oracle's NVFP4 linear on {R} rows of the {N}x{K} QKV shape"},
+            "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{R} rows x {N} outputs x {K} per step, dequantisation included"},
+            "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -504,7 +621,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="video_audio_bf16",
                     choices=["video_audio_bf16", "long_doc_bf16", "denoise_loop", "t2va_loop", "music_fp32",
-                             "video_audio_bf16_l1", "tiny", "ragged", "music_small"])
+                             "video_audio_bf16_l1", "tiny", "ragged", "music_small", "nvfp4_gemm"])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
@@ -512,6 +629,10 @@ def main():
     args.warmup = max(args.warmup, 3)
 
     import synth
+    if args.workload == "nvfp4_gemm":
+        if int(os.environ.get("RANK", "0")) == 0:
+            (run_nvfp4_reference if args.impl == "reference" else run_nvfp4_gemm)(args)
+        return
     w = synth.WORKLOADS[args.workload]
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
