@@ -27,11 +27,12 @@ class OrcConfig(ctypes.Structure):
                 ("head_dim", ctypes.c_int), ("ffn_hidden", ctypes.c_int), ("norm", ctypes.c_int),
                 ("norm_eps", ctypes.c_double), ("adaln", ctypes.c_int), ("n_mod", ctypes.c_int),
                 ("t_dim", ctypes.c_int), ("rope_axes", ctypes.c_int), ("rope_dims", ctypes.c_int * 3),
-                ("rotary_dim", ctypes.c_int), ("rope_base", ctypes.c_double), ("io_channels", ctypes.c_int)]
+                ("rotary_dim", ctypes.c_int), ("rope_base", ctypes.c_double), ("io_channels", ctypes.c_int),
+                ("qk_norm", ctypes.c_int), ("qkv_interleaved", ctypes.c_int), ("final_norm", ctypes.c_int)]
 
 
 _BLOCK_NAMES = ["w_qkv", "b_qkv", "w_o", "b_o", "w_in", "b_in", "w_down", "b_down", "w_ada", "b_ada",
-                "ln1_g", "ln1_b", "ln2_g", "ln2_b"]
+                "ln1_g", "ln1_b", "ln2_g", "ln2_b", "res1", "res2"]
 _GLOB_NAMES = ["w_ada_final", "b_ada_final", "lnf_g", "lnf_b", "w_pre", "b_pre", "w_post", "b_post"]
 
 
@@ -106,6 +107,9 @@ def config(m: dict) -> OrcConfig:
     for i in range(3):
         c.rope_dims[i] = m["rope_dims"][i]
     c.rotary_dim, c.rope_base, c.io_channels = m["rotary_dim"], m["rope_base"], m["io_channels"]
+    c.qk_norm = 1 if m.get("qk_norm") else 0
+    c.qkv_interleaved = 1 if m.get("qkv_interleaved") else 0
+    c.final_norm = {"same": 0, "rms": 1, "ln": 2}[m.get("final_norm", "same")]
     return c
 
 
@@ -172,6 +176,13 @@ def adaln(m: dict, weights: dict, t):
         assert tm.shape == (nm,)
         lib().orc_adaln_mod(ctypes.byref(c), ctypes.byref(w.w), _d(tm), _d(mod), _d(modf))
     return mod, modf
+
+
+def vit_positions(T: int, H: int, W: int) -> np.ndarray:
+    """RotaryEmbeddingND positions [T*H*W, 3] (fp64) of the video-VAE decoder's T x H x W grid."""
+    pos = np.empty((T * H * W, 3), dtype=np.float64)
+    lib().orc_vit_positions(ctypes.c_int(T), ctypes.c_int(H), ctypes.c_int(W), _d(pos))
+    return pos
 
 
 def time_shift(sigma: float, shift: float) -> float:

@@ -38,12 +38,17 @@ typedef struct {
   int rotary_dim;    // sum of rope_dims, <= head_dim
   double rope_base;
   int io_channels;   // > 0: 1x1 pre/post convolutions io_channels <-> hidden
+  // The video-VAE ViT3D decoder block ([H3] "Update: video-VAE decoder block ported"):
+  int qk_norm;          // 1: per-head RMS norm of q and k, no affine, before RoPE
+  int qkv_interleaved;  // 1: the fused qkv rows per head, [q_h | k_h | v_h] (else [q_all | k_all | v_all])
+  int final_norm;       // without AdaLN: 0 the blocks' norm, 1 RMSNorm, 2 LayerNorm
 } orc_config;
 
 typedef struct {
   const float *w_qkv, *b_qkv, *w_o, *b_o, *w_in, *b_in, *w_down, *b_down;
   const float *w_ada, *b_ada;
-  const float *ln1_g, *ln1_b, *ln2_g, *ln2_b;
+  const float *ln1_g, *ln1_b, *ln2_g, *ln2_b;  // norm gains / shifts (either norm; NULL = none)
+  const float *res1, *res2;                   // per-channel residual scales (NULL = 1)
 } orc_block;
 
 typedef struct {
@@ -258,6 +263,25 @@ void orc_layer_norm(const double* x, int n, int d, double eps, const float* g, c
   }
 }
 
+// The block norm: RMSNorm or LayerNorm of each row, then the per-channel gain and shift when
+// present ([H3] "Update: video-VAE ViT3D decoder complete": rms_norm affine).
+static void block_norm(int norm, const double* x, int n, int d, double eps, const float* g, const float* b,
+                       double* y) {
+  if (norm == 1) {
+    orc_layer_norm(x, n, d, eps, g, b, y);
+    return;
+  }
+  orc_rms_norm(x, n, d, eps, y);
+  if (g || b)
+    for (int r = 0; r < n; ++r)
+      for (int i = 0; i < d; ++i) {
+        double v = y[(size_t)r * d + i];
+        if (g) v *= (double)g[i];
+        if (b) v += (double)b[i];
+        y[(size_t)r * d + i] = v;
+      }
+}
+
 // Indexed AdaLN modulate: token r takes the row of its modality tag.
 //   y = n * (1 + scale[tag]) + shift[tag]
 // shift / scale point at [n_mod] rows of d values, ``stride`` doubles apart.
@@ -457,6 +481,26 @@ void orc_unpatchify(const float* tok, int C, int T, int H, int W, int pt, int ph
 }
 
 // ---------------------------------------------------------------------------------------------
+// RotaryEmbeddingND positions of the video-VAE decoder.  [H3] "Update: video-VAE ViT3D decoder
+// complete": each axis id i of n becomes (i + 0.5) / n mapped into [-1, 1), scaled by 2 pi; the
+// per-axis frequency blocks are concatenated and tiled twice (the NeoX rotate_half layout of
+// orc_rope_apply).  pos [T*H*W][3] for a T x H x W grid, w fastest, in double:
+//   pos_a(i) = (2 * ((i + 0.5) / n_a) - 1) * (2 pi)
+// READING: the frequencies are rope_theta^(-2k / dim_a) per axis, as for the DiT's axes.
+// ---------------------------------------------------------------------------------------------
+void orc_vit_positions(int T, int H, int W, double* pos) {
+  const double two_pi = 2.0 * 3.14159265358979323846;
+  const int n[3] = {T, H, W};
+  for (int t = 0; t < T; ++t)
+    for (int h = 0; h < H; ++h)
+      for (int w = 0; w < W; ++w) {
+        const int id[3] = {t, h, w};
+        double* p = pos + ((size_t)(t * H + h) * W + w) * 3;
+        for (int a = 0; a < 3; ++a) p[a] = (2.0 * ((id[a] + 0.5) / (double)n[a]) - 1.0) * two_pi;
+      }
+}
+
+// ---------------------------------------------------------------------------------------------
 // NVFP4 weights.  [H3] "What this push adds" (the NVFP4 checkpoint): each quantized projection
 // carries a U8 weight packing two FP4 values per byte (logical [N][K] stored [N][K/2]), an
 // F8_E4M3 scale per group of 16 along K ([N][K/16]) and an F32 global scale.
@@ -519,35 +563,46 @@ void orc_block_forward(const orc_config* c, const orc_block* w, const double* mo
   size_t md = (size_t)6 * d;
   std::vector<double> nrm((size_t)n * d), y((size_t)n * d), qkv((size_t)n * 3 * d);
   std::vector<double> q((size_t)n * d), k((size_t)n * d), v((size_t)n * d), o((size_t)n * d), t((size_t)n * d);
-  if (c->norm == 0) {
-    orc_rms_norm(x, n, d, c->norm_eps, nrm.data());
-  } else {
-    orc_layer_norm(x, n, d, c->norm_eps, w->ln1_g, w->ln1_b, nrm.data());
-  }
+  block_norm(c->norm, x, n, d, c->norm_eps, w->ln1_g, w->ln1_b, nrm.data());
   if (c->adaln)
     orc_modulate(nrm.data(), n, d, tags, mod + 0 * d, mod + 1 * d, md, y.data());
   else
     y = nrm;
   orc_linear(y.data(), n, d, w->w_qkv, w->b_qkv, 3 * d, qkv.data());
   for (int r = 0; r < n; ++r)
-    for (int i = 0; i < d; ++i) {
-      q[(size_t)r * d + i] = qkv[(size_t)r * 3 * d + i];
-      k[(size_t)r * d + i] = qkv[(size_t)r * 3 * d + d + i];
-      v[(size_t)r * d + i] = qkv[(size_t)r * 3 * d + 2 * d + i];
-    }
+    for (int h = 0; h < H; ++h)
+      for (int j = 0; j < Dh; ++j) {
+        const size_t o = (size_t)r * d + (size_t)h * Dh + j, row = (size_t)r * 3 * d;
+        if (c->qkv_interleaved) {  // the ViT's qkv.view(S, H, 3 Dh).chunk(3): [q_h | k_h | v_h] per head
+          q[o] = qkv[row + (size_t)h * 3 * Dh + j];
+          k[o] = qkv[row + (size_t)h * 3 * Dh + Dh + j];
+          v[o] = qkv[row + (size_t)h * 3 * Dh + 2 * Dh + j];
+        } else {
+          q[o] = qkv[row + (size_t)h * Dh + j];
+          k[o] = qkv[row + d + (size_t)h * Dh + j];
+          v[o] = qkv[row + 2 * d + (size_t)h * Dh + j];
+        }
+      }
+  if (c->qk_norm)  // per-head RMS norm of q and k over Dh, no affine ([H3] "Update: video-VAE decoder block ported")
+    for (std::vector<double>* m : {&q, &k})
+      for (int r = 0; r < n; ++r)
+        for (int h = 0; h < H; ++h) {
+          double* p = m->data() + (size_t)r * d + (size_t)h * Dh;
+          double ss = 0.0;
+          for (int j = 0; j < Dh; ++j) ss += p[j] * p[j];
+          const double inv = 1.0 / sqrt(ss / (double)Dh + c->norm_eps);
+          for (int j = 0; j < Dh; ++j) p[j] *= inv;
+        }
   orc_rope_apply(q.data(), n, H, Dh, c->rotary_dim, cs, sn);
   orc_rope_apply(k.data(), n, H, Dh, c->rotary_dim, cs, sn);
   orc_attention(q.data(), k.data(), v.data(), n, H, Dh, cu, n_docs, o.data());
   orc_linear(o.data(), n, d, w->w_o, w->b_o, d, t.data());
   for (int r = 0; r < n; ++r) {
     const double* g1 = c->adaln ? mod + (size_t)tags[r] * md + 2 * d : nullptr;
-    for (int i = 0; i < d; ++i) x[(size_t)r * d + i] += (g1 ? g1[i] : 1.0) * t[(size_t)r * d + i];
+    for (int i = 0; i < d; ++i)
+      x[(size_t)r * d + i] += (g1 ? g1[i] : (w->res1 ? (double)w->res1[i] : 1.0)) * t[(size_t)r * d + i];
   }
-  if (c->norm == 0) {
-    orc_rms_norm(x, n, d, c->norm_eps, nrm.data());
-  } else {
-    orc_layer_norm(x, n, d, c->norm_eps, w->ln2_g, w->ln2_b, nrm.data());
-  }
+  block_norm(c->norm, x, n, d, c->norm_eps, w->ln2_g, w->ln2_b, nrm.data());
   if (c->adaln)
     orc_modulate(nrm.data(), n, d, tags, mod + 3 * d, mod + 4 * d, md, y.data());
   else
@@ -558,7 +613,8 @@ void orc_block_forward(const orc_config* c, const orc_block* w, const double* mo
   orc_linear(hh.data(), n, F, w->w_down, w->b_down, d, t.data());
   for (int r = 0; r < n; ++r) {
     const double* g2 = c->adaln ? mod + (size_t)tags[r] * md + 5 * d : nullptr;
-    for (int i = 0; i < d; ++i) x[(size_t)r * d + i] += (g2 ? g2[i] : 1.0) * t[(size_t)r * d + i];
+    for (int i = 0; i < d; ++i)
+      x[(size_t)r * d + i] += (g2 ? g2[i] : (w->res2 ? (double)w->res2[i] : 1.0)) * t[(size_t)r * d + i];
   }
 }
 
@@ -622,7 +678,8 @@ static void forward_core(const orc_config* c, const orc_weights* w, std::vector<
     orc_rms_norm(x.data(), n, d, c->norm_eps, nrm.data());
     orc_modulate(nrm.data(), n, d, tags, modf.data(), modf.data() + d, (size_t)2 * d, out);
   } else {
-    orc_layer_norm(x.data(), n, d, c->norm_eps, w->lnf_g, w->lnf_b, nrm.data());
+    const int fnorm = c->final_norm == 0 ? c->norm : c->final_norm - 1;  // 0 RMS, 1 LN
+    block_norm(fnorm, x.data(), n, d, c->norm_eps, w->lnf_g, w->lnf_b, nrm.data());
     if (c->io_channels > 0) {
       int co = c->io_channels;
       for (int j = 0; j < n_docs; ++j) {

@@ -233,6 +233,12 @@ def weight_shapes(m: dict) -> dict:
     if m["norm"] == "ln":
         blk.update(ln1_g=(d,), ln1_b=(d,), ln2_g=(d,), ln2_b=(d,))
         glob.update(lnf_g=(d,), lnf_b=(d,))
+    if m.get("norm_affine"):  # RMSNorm with a per-channel gain
+        blk.update(ln1_g=(d,), ln2_g=(d,))
+    if m.get("final_norm") == "ln":
+        glob.update(lnf_g=(d,), lnf_b=(d,))
+    if m.get("res_scale"):  # per-channel residual scales
+        blk.update(res1=(d,), res2=(d,))
     if m["io_channels"]:
         c = m["io_channels"]
         glob.update(w_pre=(d, c), b_pre=(d,), w_post=(c, d), b_post=(c,))
@@ -253,11 +259,17 @@ def make_weights(w: dict, bf16: bool | None = None):
 
     def gen(name, shp):
         base = name.split(".")[-1]  # "block3.b_qkv" -> "b_qkv"
-        if base.startswith("ln") and base.endswith("_g"):
+        # gains, shifts and residual scales: fp32 vectors (no bf16 bits); 1 / 0 unless the workload
+        # asks for spread (affine_std) so that their paths are exercised
+        spread = w.get("affine_std", 0.0)
+        if (base.startswith("ln") and base.endswith("_g")) or base.startswith("res"):
             v = np.ones(shp, dtype=np.float32)
-            return v, (np.full(shp, 0x3F80, dtype=np.uint16) if bf16 else None)
+            if spread:
+                v = v + normal(seed, name, shp, spread)
+            return v, None
         if base.startswith("ln") and base.endswith("_b"):
-            return np.zeros(shp, dtype=np.float32), (np.zeros(shp, dtype=np.uint16) if bf16 else None)
+            v = normal(seed, name, shp, spread) if spread else np.zeros(shp, dtype=np.float32)
+            return v, None
         std = w["bias_std"] if base.startswith("b_") else w["w_std"]
         if std == 0.0:
             return np.zeros(shp, dtype=np.float32), (np.zeros(shp, dtype=np.uint16) if bf16 else None)

@@ -33,7 +33,8 @@ def upload_weights(W: dict, bf16: bool):
     def up(name, f, b):
         if f is None:
             return None
-        return dev_bf16(b) if bf16 else dev_f32(f)
+        # matrices and biases in the model dtype; gains, shifts and residual scales (no bf16 bits) fp32
+        return dev_bf16(b) if (bf16 and b is not None) else dev_f32(f)
     blocks = []
     for l, fb in enumerate(W["blocks"]):
         bb = W["bits"]["blocks"][l] if bf16 else {}

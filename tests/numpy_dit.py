@@ -54,9 +54,10 @@ def attention(q, k, v, cu, H, Dh):
     return np.einsum("hij,jhe->ihe", p, vh).reshape(N, H * Dh)
 
 
-def norm(x, m, g=None, b=None):
-    if m["norm"] == "rms":
-        return x / np.sqrt((x * x).mean(axis=1, keepdims=True) + m["norm_eps"])
+def norm(x, m, g=None, b=None, kind=None):
+    if (kind or m["norm"]) == "rms":
+        y = x / np.sqrt((x * x).mean(axis=1, keepdims=True) + m["norm_eps"])
+        return y * (1.0 if g is None else g) + (0.0 if b is None else b)
     mu = x.mean(axis=1, keepdims=True)
     var = ((x - mu) ** 2).mean(axis=1, keepdims=True)
     y = (x - mu) / np.sqrt(var + m["norm_eps"])
@@ -93,11 +94,20 @@ def forward(m, W, x_in, lay, t):
         else:
             y = norm(x, m, B.get("ln1_g"), B.get("ln1_b"))
         qkv = y @ B["w_qkv"].T + B["b_qkv"]
-        q, k, v = qkv[:, :d], qkv[:, d:2 * d], qkv[:, 2 * d:]
+        if m.get("qkv_interleaved"):
+            # per head [q_h | k_h | v_h]: view [N, H, 3 Dh] and split the last axis in three
+            qh, kh, vh = np.split(qkv.reshape(N, H, 3 * Dh), 3, axis=2)
+            q, k, v = qh.reshape(N, d), kh.reshape(N, d), vh.reshape(N, d)
+        else:
+            q, k, v = qkv[:, :d], qkv[:, d:2 * d], qkv[:, 2 * d:]
+        if m.get("qk_norm"):
+            rmsn = lambda a: (a.reshape(N, H, Dh) / np.sqrt((a.reshape(N, H, Dh) ** 2).mean(axis=2, keepdims=True)
+                                                          + m["norm_eps"])).reshape(N, d)
+            q, k = rmsn(q), rmsn(k)
         q, k = rope(q, ang, H, Dh, R), rope(k, ang, H, Dh, R)
         o = attention(q, k, v, cu, H, Dh)
         upd = o @ B["w_o"].T + B["b_o"]
-        x = x + (mod[:, 2] * upd if m["adaln"] else upd)
+        x = x + (mod[:, 2] * upd if m["adaln"] else upd * (1.0 if B.get("res1") is None else B["res1"]))
         if m["adaln"]:
             y2 = norm(x, m) * (1 + mod[:, 4]) + mod[:, 3]
         else:
@@ -105,7 +115,7 @@ def forward(m, W, x_in, lay, t):
         uv = y2 @ B["w_in"].T + B["b_in"]
         h = uv[:, :F] * silu(uv[:, F:])
         upd = h @ B["w_down"].T + B["b_down"]
-        x = x + (mod[:, 5] * upd if m["adaln"] else upd)
+        x = x + (mod[:, 5] * upd if m["adaln"] else upd * (1.0 if B.get("res2") is None else B["res2"]))
     if m["adaln"]:
         G = {k: f64(v) for k, v in W["glob"].items()}
         wf = G["w_ada_final"].reshape(nm, 2 * d, -1)
@@ -113,7 +123,7 @@ def forward(m, W, x_in, lay, t):
         mf = np.stack([wf[i] @ se[i] + bf[i] for i in range(nm)]).reshape(nm, 2, d)[tags]
         return norm(x, m) * (1 + mf[:, 1]) + mf[:, 0]
     G = {k: f64(v) for k, v in W["glob"].items()}
-    y = norm(x, m, G.get("lnf_g"), G.get("lnf_b"))
+    y = norm(x, m, G.get("lnf_g"), G.get("lnf_b"), kind={"same": None, "rms": "rms", "ln": "ln"}[m.get("final_norm", "same")])
     if m["io_channels"]:
         c = m["io_channels"]
         out = np.zeros(c * N)

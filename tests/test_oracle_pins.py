@@ -648,3 +648,70 @@ def test_synthetic_nvfp4_weights_have_the_intended_scale():
     assert np.bincount(codes, minlength=16).min() > 0.8 * codes.size / 16  # all 16 codes, near uniform
     rms = np.sqrt((vals[codes] ** 2).mean()) * np.sqrt((oracle.e4m3_decode(s) ** 2).mean()) * g
     assert 0.01 < rms < 0.04
+
+
+# ---------------------------------------------------------------------------------------------
+# the video-VAE ViT3D decoder block
+# ---------------------------------------------------------------------------------------------
+
+TINY_VIT = dict(n_blocks=2, hidden=32, n_heads=2, head_dim=16, ffn_hidden=24, norm="rms", norm_eps=1e-6,
+                adaln=False, n_mod=1, t_dim=16, rope_axes=3, rope_dims=(4, 4, 4), rotary_dim=12,
+                rope_base=100.0, io_channels=0, dtype="fp32", qk_norm=True, qkv_interleaved=True,
+                final_norm="ln", res_scale=True, norm_affine=True)
+
+
+def _vit_case(seed, m=TINY_VIT, grid=(2, 2, 2)):
+    docs = [dict(video=grid)]
+    w = dict(model=m, seed=seed, docs=docs, t=0.0, w_std=0.3, bias_std=0.2, x_std=1.0, affine_std=0.2)
+    lay = dict(synth.build_layout(docs))
+    lay["pos"] = oracle.vit_positions(*grid)
+    return w, lay, synth.make_weights(w, bf16=False), synth.make_tokens(w, lay)
+
+
+def test_vit_positions_closed_form():
+    """(i + 0.5) / n mapped into [-1, 1), times 2 pi: symmetric about 0, spacing 4 pi / n, w fastest."""
+    T, H, W = 3, 4, 5
+    pos = oracle.vit_positions(T, H, W).reshape(T, H, W, 3)
+    for a, n in enumerate((T, H, W)):
+        ax = np.moveaxis(pos[..., a], a, 0).reshape(n, -1)
+        assert (ax == ax[:, :1]).all()  # depends on its own axis id only
+        v = ax[:, 0]
+        assert np.allclose(v, 2 * np.pi * (np.arange(n) * 2 + 1 - n) / n, rtol=0, atol=1e-14)
+        assert np.allclose(v + v[::-1], 0.0, atol=1e-14) and np.all(np.abs(v) < 2 * np.pi)
+
+
+def test_forward_brute_force_vit_block():
+    """Interleaved qkv, per-head q/k RMS norm, RMS gains, per-channel residual scales, 3-axis RoPE
+    on the normalised grid (base 100, 12 of 16 dims) and a final LayerNorm: against the numpy forward."""
+    w, lay, W, x = _vit_case(37)
+    out, _ = oracle.forward(TINY_VIT, W, x, lay, 0.0)
+    ref = numpy_dit.forward(TINY_VIT, W, x, lay, 0.0)
+    assert np.abs(out - ref).max() <= 1e-12 * np.abs(ref).max()
+
+
+def test_vit_interleaved_qkv_is_a_row_permutation_of_the_dit_order():
+    """qkv.view(S, H, 3 Dh).chunk(3) == the [q_all | k_all | v_all] order with W's rows permuted."""
+    w, lay, W, x = _vit_case(38)
+    H, Dh = TINY_VIT["n_heads"], TINY_VIT["head_dim"]
+    perm = np.array([h * 3 * Dh + s * Dh + j for s in range(3) for h in range(H) for j in range(Dh)])
+    W2 = dict(blocks=[dict(b) for b in W["blocks"]], glob=W["glob"])
+    for b in W2["blocks"]:
+        b["w_qkv"] = b["w_qkv"][perm]
+        b["b_qkv"] = b["b_qkv"][perm]
+    a, _ = oracle.forward(TINY_VIT, W, x, lay, 0.0)
+    b, _ = oracle.forward(dict(TINY_VIT, qkv_interleaved=False), W2, x, lay, 0.0)
+    assert np.array_equal(a, b)
+    c, _ = oracle.forward(dict(TINY_VIT, qkv_interleaved=False), W, x, lay, 0.0)
+    assert np.abs(a - c).max() > 1e-3  # reading the interleaved weight the DiT way is wrong
+
+
+def test_vit_zero_residual_scales_make_the_blocks_the_identity():
+    w, lay, W, x = _vit_case(39)
+    for b in W["blocks"]:
+        b["res1"] = np.zeros_like(b["res1"])
+        b["res2"] = np.zeros_like(b["res2"])
+    out, dumps = oracle.forward(TINY_VIT, W, x, lay, 0.0, dumps=True)
+    for l in range(TINY_VIT["n_blocks"]):
+        assert np.array_equal(dumps[l], x.astype(np.float64))
+    G = W["glob"]
+    assert np.allclose(out, oracle.layer_norm(x, TINY_VIT["norm_eps"], G["lnf_g"], G["lnf_b"]), rtol=0, atol=1e-13)
