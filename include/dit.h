@@ -62,7 +62,7 @@ typedef struct {
   int n_heads;        /* H */
   int head_dim;       /* Dh, H * Dh == d */
   int ffn_hidden;     /* F: the FFN computes value * silu(gate) over an up projection 2F wide */
-  int norm;           /* DIT_RMSNORM (no affine) | DIT_LAYERNORM (gain + shift) */
+  int norm;           /* DIT_RMSNORM | DIT_LAYERNORM; either takes the per-channel gain / shift weights when given */
   float norm_eps;
   int adaln;          /* 1: modality-indexed AdaLN modulate + gated residuals; 0: plain residuals */
   int n_modalities;   /* tags index [0, n_modalities): 0 = video, 1 = audio */
@@ -75,9 +75,16 @@ typedef struct {
   int dtype;          /* DIT_BF16 (bf16 weights and GEMM operands, fp32 residual) | DIT_FP32 */
   int max_tokens;     /* capacity: largest n_tokens a forward may pass */
   int max_docs;       /* capacity: largest n_docs a forward may pass */
+  /* The video-VAE ViT3D decoder block ([H3] "Update: video-VAE decoder block ported"): */
+  int qk_norm;         /* 1: per-head RMS norm of q and k over head_dim, no affine, eps = norm_eps,
+                          before RoPE */
+  int qkv_interleaved; /* 1: w_qkv / b_qkv rows per head [q_h | k_h | v_h] (the ViT's
+                          qkv.view(S, H, 3 Dh).chunk(3)); repacked at bind.  0: [q_all | k_all | v_all] */
+  int final_norm;      /* without AdaLN, the final norm: 0 the blocks' norm, 1 RMSNorm, 2 LayerNorm */
 } dit_config;
 
-/* One block's weights (device pointers, dtype = cfg.dtype; biases may be NULL = zero).
+/* One block's weights (device pointers; matrices and biases in cfg.dtype, biases may be NULL = zero;
+ * gains, shifts and residual scales always fp32).
  *   w_qkv  [3d, d]   fused rows in the order [q_all | k_all | v_all], heads contiguous
  *                    ([H3] "Update: video-VAE decoder block ported": the DiT's fused qkv order)
  *   w_o    [d, d]
@@ -85,11 +92,15 @@ typedef struct {
  *   w_down [d, F]
  *   w_ada  [n_mod * 6d, t_embed_dim]  per modality six d-wide chunks:
  *          shift1, scale1, gate1, shift2, scale2, gate2           (adaln = 1 only)
- *   ln1_g/ln1_b/ln2_g/ln2_b [d]                                     (LayerNorm only) */
+ *   ln1_g/ln1_b/ln2_g/ln2_b [d]  the two norms' gains / shifts (LayerNorm; RMSNorm takes the gains,
+ *                                the ViT's rms_norm affine); NULL = none
+ *   res1/res2 [d]                per-channel residual scales without AdaLN: x += res1 * attention
+ *                                branch, x += res2 * FFN branch (NULL = 1) */
 typedef struct {
   const void *w_qkv, *b_qkv, *w_o, *b_o, *w_in, *b_in, *w_down, *b_down;
   const void *w_ada, *b_ada;
   const void *ln1_g, *ln1_b, *ln2_g, *ln2_b;
+  const void *res1, *res2;
 } dit_block_weights;
 
 /* All weights.  `blocks` is a HOST array of n_blocks entries (read during the call only).
@@ -121,10 +132,10 @@ typedef struct dit_handle dit_handle;
  * ------------------------------------------------------------------------------------------- */
 
 /* Validate `cfg` and create a handle.  No device memory is allocated here.
- * What the kernels tile: dtype DIT_BF16 with adaln = 1 and RMSNorm; hidden a multiple of 256 with
- * hidden / 128 in {1..6, 8, 10, 12, 16, 20, 24, 32, 40, 48, 64}; head_dim 64 or 128; ffn_hidden a
- * multiple of 128; rotary_dim / 2 and head_dim - rotary_dim multiples of 16; t_embed_dim a
- * multiple of 8 (of 256 above 256); io_channels 0.  Anything else returns DIT_ERR_CONFIG (not a
+ * What the kernels tile: dtype DIT_BF16 with RMSNorm blocks (with or without AdaLN); hidden a
+ * multiple of 256 with hidden / 128 in {1..6, 8, 10, 12, 16, 20, 24, 32, 40, 48, 64}; head_dim 64
+ * or 128; ffn_hidden a multiple of 128; rotary_dim / 2 a multiple of 8 and head_dim - rotary_dim a
+ * multiple of 16; t_embed_dim a multiple of 8 (of 256 above 256); io_channels 0.  Anything else returns DIT_ERR_CONFIG (not a
  * valid model) or DIT_ERR_UNSUPPORTED (valid, not tiled), dit_last_error(NULL) naming the field. */
 DIT_API dit_status dit_create(const dit_config* cfg, dit_handle** out);
 
@@ -251,6 +262,14 @@ DIT_API dit_status dit_unpatchify(const float* tokens, int C, int T, int H, int 
 DIT_API dit_status dit_audio_pack(const float* latent, int C, int T, float* tokens, void* stream);
 DIT_API dit_status dit_audio_unpack(const float* tokens, int C, int T, float* latent, void* stream);
 
+/* RotaryEmbeddingND positions of the video-VAE decoder, for a T x H x W token grid (w fastest):
+ * pos[(t*H + h)*W + w] = (p(t, T), p(h, H), p(w, W)), p(i, n) = (2 * ((i + 0.5) / n) - 1) * 2 pi,
+ * in double.  [H3] "Update: video-VAE ViT3D decoder complete": length-normalised ids mapped into
+ * [-1, 1), scaled by 2 pi.  With rope_axes 3, rope_base 100 (rope_theta) and rope_dims splitting
+ * rotary_dim = 0.75 * head_dim over the axes, dit_forward's cos/sin cache then holds that RoPE's
+ * angles.  Host only; pos HOST [T*H*W][3]. */
+DIT_API dit_status dit_vit_positions(int T, int H, int W, double* pos);
+
 /* The same forward from HOST buffers: copies the inputs in (cudaMemcpyAsync, one per array),
  * runs dit_forward and copies `out_host` back, all on `stream`, then synchronises the stream.
  * Use pinned host memory for full copy speed.  workspace must hold
@@ -321,8 +340,8 @@ DIT_API dit_status dit_get_kernel_times(dit_handle* h, double* ms_out, int64_t* 
 
 /* Norm + indexed AdaLN modulate ([H3] "The device-resident forward (W2b)"):
  *   y[r] = N(x[r]) * (1 + scale[tag[r]]) + shift[tag[r]]
- * N = RMSNorm x / sqrt(mean(x^2) + eps) (norm = DIT_RMSNORM) or LayerNorm with gain/shift ln_g,
- * ln_b (DIT_LAYERNORM).  x fp32 [n, d]; shift/scale fp32 rows of d values, row m at
+ * N = RMSNorm x / sqrt(mean(x^2) + eps) (norm = DIT_RMSNORM) or LayerNorm (DIT_LAYERNORM), either
+ * followed by the per-channel gain ln_g and shift ln_b when given (NULL = none).  x fp32 [n, d]; shift/scale fp32 rows of d values, row m at
  * shift + m * mod_stride (NULL shift and scale = no modulation); tags uint8 [n] (may be NULL
  * when shift is NULL).  Output bf16 bits [n, d] (out_kind 0) or fp32 [n, d] (out_kind 1).
  * Requires d % 128 == 0 and d <= 8192. */

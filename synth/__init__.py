@@ -144,6 +144,13 @@ def _model(**kw):
     return m
 
 
+# The video-VAE decoder's block: no AdaLN, RMS gains, per-head q/k RMS norm, interleaved qkv,
+# per-channel residual scales, final LayerNorm; READINGS: ffn_hidden 5632 (the usual 8/3 d rounded
+# to 256; the pages give none), norm eps 1e-6, 48 rotary dims split 16/16/16 over (t, h, w).
+VIT_MODEL = _model(n_blocks=36, hidden=2048, n_heads=32, head_dim=64, ffn_hidden=5632, adaln=False, n_mod=1,
+                   rope_dims=(16, 16, 16), rotary_dim=48, rope_base=100.0, qk_norm=True, qkv_interleaved=True,
+                   final_norm="ln", res_scale=True, norm_affine=True, vit_positions=True)
+
 C2_MODEL = _model(n_blocks=8, hidden=3072, n_heads=24, head_dim=128, ffn_hidden=8192,
                   rope_dims=(32, 48, 48), rotary_dim=128)
 
@@ -177,6 +184,15 @@ WORKLOADS = {
                       docs=[dict(video=(8, 32, 64), audio=1024), dict(video=(4, 32, 64), audio=1024)],
                       t="schedule", steps=50, latent=True, shifts=(12.0, 3.0), w_std=0.02, bias_std=0.0,
                       x_std=1.0),
+    # The video-VAE ViT3D decoder stack ([H3] "Update: video-VAE ViT3D decoder complete": 36 blocks,
+    # 32 x 64 heads, rms_norm affine, q/k rms_norm without affine, gated SiLU, rope_theta 100,
+    # rope_dim_ratio 0.75) on one 8 x 32 x 32 latent grid; positions are RotaryEmbeddingND's.
+    "vit3d_decoder": dict(model=VIT_MODEL, seed=6, docs=[dict(video=(8, 32, 32))], t=0.0, w_std=0.02,
+                          bias_std=0.02, x_std=1.0, affine_std=0.1),
+    # The same block at parity size: two grids (one ragged), 2 blocks of width 256.
+    "vit3d_small": dict(model=dict(VIT_MODEL, n_blocks=2, hidden=256, n_heads=4, ffn_hidden=768), seed=7,
+                        docs=[dict(video=(2, 8, 16)), dict(video=(1, 6, 10))], t=0.0, w_std=0.02,
+                        bias_std=0.02, x_std=1.0, affine_std=0.1),
     # One block of the video+audio model on its full 17,408-token sequence: every kernel launch has
     # exactly the full workload's shape, with a few GB on the device (profiling captures).
     "video_audio_bf16_l1": dict(model=dict(C2_MODEL, n_blocks=1), seed=2,

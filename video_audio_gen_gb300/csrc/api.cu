@@ -46,6 +46,8 @@ struct BlockDev {
   float* b_o = nullptr;
   float* b_in_packed = nullptr;
   float* b_down = nullptr;
+  float* res1 = nullptr;           // per-channel residual scales without AdaLN (NULL = 1)
+  float* res2 = nullptr;
 };
 
 // Workspace layout of one forward (offsets in bytes from the workspace base).
@@ -145,24 +147,30 @@ dit_status validate_config(const dit_config* c) {
   if (c->io_channels < 0) return set_err(nullptr, DIT_ERR_CONFIG, "io_channels must be >= 0");
   if (c->max_tokens < 1 || c->max_docs < 1) return set_err(nullptr, DIT_ERR_CONFIG, "max_tokens/max_docs must be >= 1");
   if (c->dtype != DIT_BF16 && c->dtype != DIT_FP32) return set_err(nullptr, DIT_ERR_CONFIG, "bad dtype");
+  if ((c->qk_norm != 0 && c->qk_norm != 1) || (c->qkv_interleaved != 0 && c->qkv_interleaved != 1))
+    return set_err(nullptr, DIT_ERR_CONFIG, "qk_norm and qkv_interleaved must be 0 or 1");
+  if (c->final_norm < 0 || c->final_norm > 2) return set_err(nullptr, DIT_ERR_CONFIG, "final_norm must be 0, 1 or 2");
+  if (c->adaln && c->final_norm)
+    return set_err(nullptr, DIT_ERR_CONFIG, "with AdaLN the final layer is RMSNorm + modulate (final_norm must be 0)");
   // What the sm_103a kernels tile.
   if (c->head_dim != 128 && c->head_dim != 64)
     return set_err(nullptr, DIT_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
   if (!norm_width_supported(c->hidden)) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "hidden width not tiled by the norm kernel");
   if (c->dtype == DIT_FP32) {
     if (c->adaln) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "the fp32 forward has no AdaLN (adaln must be 0)");
+    if (c->qk_norm || c->qkv_interleaved || c->final_norm)
+      return set_err(nullptr, DIT_ERR_UNSUPPORTED, "qk_norm / qkv_interleaved / final_norm need the bf16 forward");
     if (c->hidden % 128) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "fp32: hidden must be a multiple of 128");
     if (c->ffn_hidden % 64) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "fp32: ffn_hidden must be a multiple of 64");
     if (c->io_channels % 128) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "fp32: io_channels must be 0 or a multiple of 128");
     return DIT_OK;
   }
   if (c->hidden % 256) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "hidden must be a multiple of 256");
-  if ((c->rotary_dim / 2) % 16 || (c->head_dim - c->rotary_dim) % 16)
-    return set_err(nullptr, DIT_ERR_UNSUPPORTED, "rotary_dim/2 and head_dim-rotary_dim must be multiples of 16");
+  if ((c->rotary_dim / 2) % 8 || (c->head_dim - c->rotary_dim) % 16)
+    return set_err(nullptr, DIT_ERR_UNSUPPORTED, "rotary_dim/2 must be a multiple of 8 and head_dim-rotary_dim of 16");
   if (c->ffn_hidden % 128) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "ffn_hidden must be a multiple of 128");
   if (c->io_channels) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "pre/post convolutions need the fp32 forward");
   if (c->norm == DIT_LAYERNORM) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "LayerNorm blocks need the fp32 forward");
-  if (!c->adaln) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "the bf16 forward needs adaln = 1");
   return DIT_OK;
 }
 
@@ -557,13 +565,14 @@ dit_status dit_bind_weights(dit_handle* h, const dit_weights* w, void* stream) {
     const struct {
       const void* p;
       const char* name;
-    } req[] = {{b.w_qkv, "w_qkv"}, {b.w_o, "w_o"}, {b.w_in, "w_in"}, {b.w_down, "w_down"}, {b.w_ada, "w_ada"}};
+    } req[] = {{b.w_qkv, "w_qkv"}, {b.w_o, "w_o"}, {b.w_in, "w_in"}, {b.w_down, "w_down"},
+               {c.adaln ? b.w_ada : b.w_qkv, "w_ada"}};
     for (const auto& r : req) {
       if (!r.p) return set_err(h, DIT_ERR_MISSING_WEIGHT, "missing weight: blocks[%d].%s", l, r.name);
       if (!aligned16(r.p)) return set_err(h, DIT_ERR_INVALID_ARG, "blocks[%d].%s is not 16-byte aligned", l, r.name);
     }
   }
-  if (!w->w_ada_final) return set_err(h, DIT_ERR_MISSING_WEIGHT, "missing weight: w_ada_final");
+  if (c.adaln && !w->w_ada_final) return set_err(h, DIT_ERR_MISSING_WEIGHT, "missing weight: w_ada_final");
 
   // Free a previous binding.
   cudaStreamSynchronize(s);
@@ -584,6 +593,13 @@ dit_status dit_bind_weights(dit_handle* h, const dit_weights* w, void* stream) {
       e = cudaMemsetAsync(dst, 0, n * 4, s);
     return e == cudaSuccess ? dst : nullptr;
   };
+  // fp32 vectors (gains, shifts, residual scales): library-owned copies, NULL stays NULL
+  auto vec32 = [&](const void* src, long long n) -> float* {
+    if (!src) return nullptr;
+    float* dst = static_cast<float*>(dev_alloc(h, n * 4, &e));
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dst, src, n * 4, cudaMemcpyDeviceToDevice, s);
+    return dst;
+  };
   for (int l = 0; l < c.n_blocks; ++l) {
     const dit_block_weights& b = w->blocks[l];
     BlockDev& bd = h->blocks[l];
@@ -591,6 +607,24 @@ dit_status dit_bind_weights(dit_handle* h, const dit_weights* w, void* stream) {
     bd.w_o = b.w_o;
     bd.w_down = b.w_down;
     if (!(bd.b_qkv = bias_f32(b.b_qkv, 3ll * d))) return cuda_err(h, e, "bind b_qkv");
+    if (c.qkv_interleaved) {
+      // [q_h | k_h | v_h] per head -> the engine's [q_all | k_all | v_all]: a library-owned copy
+      void* wq = dev_alloc(h, (size_t)3 * d * d * 2, &e);
+      if (e != cudaSuccess) return cuda_err(h, e, "alloc w_qkv");
+      DIT_CK(h, qkv_deinterleave_launch(b.w_qkv, wq, c.n_heads, c.head_dim, d * 2, s), "deinterleave w_qkv");
+      float* bq = static_cast<float*>(dev_alloc(h, (size_t)3 * d * 4, &e));
+      if (e != cudaSuccess) return cuda_err(h, e, "alloc b_qkv");
+      DIT_CK(h, qkv_deinterleave_launch(bd.b_qkv, bq, c.n_heads, c.head_dim, 4, s), "deinterleave b_qkv");
+      bd.w_qkv = wq;
+      bd.b_qkv = bq;
+    }
+    bd.ln1_g = vec32(b.ln1_g, d);
+    bd.ln1_b = vec32(b.ln1_b, d);
+    bd.ln2_g = vec32(b.ln2_g, d);
+    bd.ln2_b = vec32(b.ln2_b, d);
+    bd.res1 = vec32(b.res1, d);
+    bd.res2 = vec32(b.res2, d);
+    if (e != cudaSuccess) return cuda_err(h, e, "bind gains / residual scales");
     if (!(bd.b_o = bias_f32(b.b_o, d))) return cuda_err(h, e, "bind b_o");
     if (!(bd.b_down = bias_f32(b.b_down, d))) return cuda_err(h, e, "bind b_down");
     float* b_in = nullptr;
@@ -600,6 +634,15 @@ dit_status dit_bind_weights(dit_handle* h, const dit_weights* w, void* stream) {
     bd.b_in_packed = static_cast<float*>(dev_alloc(h, (size_t)2 * F * 4, &e));
     if (e != cudaSuccess) return cuda_err(h, e, "alloc b_in");
     DIT_CK(h, pack_ffn_in_launch(b.w_in, b_in, F, d, bd.w_in_packed, bd.b_in_packed, s), "pack w_in");
+  }
+  h->lnf_g = vec32(w->lnf_g, d);
+  h->lnf_b = vec32(w->lnf_b, d);
+  if (e != cudaSuccess) return cuda_err(h, e, "bind final norm");
+  if (!c.adaln) {
+    h->ada_rows = 0;
+    DIT_CK(h, cudaStreamSynchronize(s), "bind sync");
+    h->bound = true;
+    return DIT_OK;
   }
   // AdaLN matrices of every block, then the final layer's, in one [rows, t_dim] matrix.
   const size_t blk_rows = (size_t)nm * 6 * d, fin_rows = (size_t)nm * 2 * d;
@@ -729,7 +772,7 @@ static dit_status forward_impl(dit_handle* h, const float* x_tokens, const int32
     DIT_CK(h, rope_cache_launch(pos_thw, N, c.rope_axes, c.rope_dims, c.rope_base, cosc, sinc, status, s), "rope cache");
     ln.done();
   }
-  {
+  if (c.adaln) {
     Launch ln(h, s, 6);
     AdaTimesteps ts{};
     ts.n_t = n_t;
@@ -767,8 +810,9 @@ static dit_status forward_impl(dit_handle* h, const float* x_tokens, const int32
     const float* ml = mod + (size_t)l * nm * 6 * d;
     {
       Launch ln(h, s, 5);
-      DIT_CK(h, norm_modulate_launch(resid, resid_lo, N, d, c.norm, c.norm_eps, nullptr, nullptr, modality_tags, ml + 0 * d,
-                                     ml + 1 * d, mstride, y, 0, status, s), "norm1");
+      DIT_CK(h, norm_modulate_launch(resid, resid_lo, N, d, c.norm, c.norm_eps, B.ln1_g, B.ln1_b, modality_tags,
+                                     c.adaln ? ml + 0 * d : nullptr, c.adaln ? ml + 1 * d : nullptr, mstride, y, 0,
+                                     status, s), "norm1");
       ln.done();
     }
     {
@@ -777,6 +821,7 @@ static dit_status forward_impl(dit_handle* h, const float* x_tokens, const int32
       g.M = N; g.N = 3 * d; g.K = d; g.bias = B.b_qkv;
       g.d = d; g.head_dim = c.head_dim; g.rot_half = c.rotary_dim / 2;
       g.cos_cache = cosc; g.sin_cache = sinc; g.q = q; g.k = k; g.vt = vt; g.n_pad = L.n_pad;
+      g.qk_norm = c.qk_norm; g.qk_eps = c.norm_eps;
       g.status = status;
       DIT_CK(h, gemm_launch(kEpiQkvRope, y, B.w_qkv, g, s), "gemm qkv");
       ln.done();
@@ -790,14 +835,16 @@ static dit_status forward_impl(dit_handle* h, const float* x_tokens, const int32
       Launch ln(h, s, 2);
       GemmArgs g{};
       g.M = N; g.N = d; g.K = d; g.bias = B.b_o;
-      g.x = resid; g.gate = ml + 2 * d; g.gate_stride = mstride; g.tags = modality_tags; g.status = status;
+      g.x = resid; g.gate = c.adaln ? ml + 2 * d : B.res1; g.gate_stride = c.adaln ? mstride : 0;
+      g.tags = modality_tags; g.status = status;
       DIT_CK(h, gemm_launch(kEpiGatedResid, o, B.w_o, g, s), "gemm out");
       ln.done();
     }
     {
       Launch ln(h, s, 5);
-      DIT_CK(h, norm_modulate_launch(resid, resid_lo, N, d, c.norm, c.norm_eps, nullptr, nullptr, modality_tags, ml + 3 * d,
-                                     ml + 4 * d, mstride, y, 0, status, s), "norm2");
+      DIT_CK(h, norm_modulate_launch(resid, resid_lo, N, d, c.norm, c.norm_eps, B.ln2_g, B.ln2_b, modality_tags,
+                                     c.adaln ? ml + 3 * d : nullptr, c.adaln ? ml + 4 * d : nullptr, mstride, y, 0,
+                                     status, s), "norm2");
       ln.done();
     }
     {
@@ -811,7 +858,8 @@ static dit_status forward_impl(dit_handle* h, const float* x_tokens, const int32
       Launch ln(h, s, 4);
       GemmArgs g{};
       g.M = N; g.N = d; g.K = F; g.bias = B.b_down;
-      g.x = resid; g.gate = ml + 5 * d; g.gate_stride = mstride; g.tags = modality_tags; g.status = status;
+      g.x = resid; g.gate = c.adaln ? ml + 5 * d : B.res2; g.gate_stride = c.adaln ? mstride : 0;
+      g.tags = modality_tags; g.status = status;
       DIT_CK(h, gemm_launch(kEpiGatedResid, hbuf, B.w_down, g, s), "gemm ffn down");
       ln.done();
     }
@@ -822,8 +870,13 @@ static dit_status forward_impl(dit_handle* h, const float* x_tokens, const int32
   {
     const float* mf = mod + (size_t)c.n_blocks * nm * 6 * d;
     Launch ln(h, s, 5);
-    DIT_CK(h, norm_modulate_launch(resid, resid_lo, N, d, c.norm, c.norm_eps, nullptr, nullptr, modality_tags, mf, mf + d,
-                                   2ll * d, out, 1, status, s), "final norm");
+    if (c.adaln)
+      DIT_CK(h, norm_modulate_launch(resid, resid_lo, N, d, c.norm, c.norm_eps, nullptr, nullptr, modality_tags, mf,
+                                     mf + d, 2ll * d, out, 1, status, s), "final norm");
+    else  // the final norm without modulation: the blocks' kind, or final_norm's
+      DIT_CK(h, norm_modulate_launch(resid, resid_lo, N, d, c.final_norm ? c.final_norm - 1 : c.norm, c.norm_eps,
+                                     h->lnf_g, h->lnf_b, nullptr, nullptr, nullptr, 0, out, 1, status, s),
+             "final norm");
     ln.done();
   }
   h->stats.forwards++;
@@ -1112,6 +1165,20 @@ dit_status dit_euler_step_modal(float* x, const float* v, int n_tokens, int d, c
   }
   cudaError_t e = euler_tagged_launch(x, v, n_tokens, d, tags, sg, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? DIT_OK : cuda_err(nullptr, e, "euler tagged");
+}
+
+dit_status dit_vit_positions(int T, int H, int W, double* pos) {
+  if (T < 1 || H < 1 || W < 1 || !pos) return set_err(nullptr, DIT_ERR_INVALID_ARG, "bad vit_positions arguments");
+  const double two_pi = 6.283185307179586476925;  // 2 pi
+  const int n[3] = {T, H, W};
+  for (int t = 0; t < T; ++t)
+    for (int hh = 0; hh < H; ++hh)
+      for (int w = 0; w < W; ++w) {
+        const int id[3] = {t, hh, w};
+        double* p = pos + ((size_t)(t * H + hh) * W + w) * 3;
+        for (int a = 0; a < 3; ++a) p[a] = (2.0 * ((id[a] + 0.5) / (double)n[a]) - 1.0) * two_pi;
+      }
+  return DIT_OK;
 }
 
 float dit_time_shift(float sigma, float shift) {

@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(256) norm_mod_kernel(const float* __restrict__
   for (int i = 0; i < NV; ++i) {
     const int c = (i * 32 + lane) * 4;
     float o[4] = {(v[i].x - mean) * inv, (v[i].y - mean) * inv, (v[i].z - mean) * inv, (v[i].w - mean) * inv};
-    if (norm == 1) {
+    {  // gain and shift of either norm (NULL = none)
       if (g) {
         const float4 gg = *reinterpret_cast<const float4*>(g + c);
         o[0] *= gg.x; o[1] *= gg.y; o[2] *= gg.z; o[3] *= gg.w;
@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(256) norm_mod_persistent_kernel(
       const int c = (i * 256 + threadIdx.x) * 4;
       float o[4] = {(cur[i].x - mean) * inv, (cur[i].y - mean) * inv, (cur[i].z - mean) * inv,
                     (cur[i].w - mean) * inv};
-      if (norm == 1) {
+      {  // gain and shift of either norm (NULL = none)
         if (g) {
           const float4 gg = *reinterpret_cast<const float4*>(g + c);
           o[0] *= gg.x; o[1] *= gg.y; o[2] *= gg.z; o[3] *= gg.w;
@@ -463,6 +463,25 @@ cudaError_t euler_tagged_launch(float* x, const float* v, int n_tokens, int d, c
   const long long n = (long long)n_tokens * d;
   if (n <= 0) return cudaSuccess;
   euler_tagged_kernel<<<grid_for(n, 256), 256, 0, s>>>(x, v, n_tokens, d, tags, sg);
+  return cudaGetLastError();
+}
+
+// Row r of the [q_all | k_all | v_all] order, r = s * H * Dh + h * Dh + j (s = 0 q, 1 k, 2 v), is
+// row h * 3 Dh + s * Dh + j of the per-head interleaved [q_h | k_h | v_h] order; rows of row_bytes.
+__global__ void qkv_deinterleave_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int H, int Dh,
+                                        int row_bytes) {
+  const int r = blockIdx.x;
+  const int HD = H * Dh;
+  const int sgm = r / HD, h = (r - sgm * HD) / Dh, j = r - sgm * HD - h * Dh;
+  const size_t from = ((size_t)h * 3 * Dh + (size_t)sgm * Dh + j) * row_bytes;
+  const size_t to = (size_t)r * row_bytes;
+  for (int b = threadIdx.x; b < row_bytes; b += blockDim.x) dst[to + b] = src[from + b];
+}
+
+cudaError_t qkv_deinterleave_launch(const void* src, void* dst, int H, int Dh, int row_bytes, cudaStream_t s) {
+  if (H < 1 || Dh < 1 || row_bytes < 1) return cudaErrorInvalidValue;
+  qkv_deinterleave_kernel<<<3 * H * Dh, 128, 0, s>>>(static_cast<const uint8_t*>(src), static_cast<uint8_t*>(dst), H, Dh,
+                                                     row_bytes);
   return cudaGetLastError();
 }
 

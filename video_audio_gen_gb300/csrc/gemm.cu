@@ -145,11 +145,57 @@ __device__ __forceinline__ void store_bf16x16(__nv_bfloat16* o, const float (&v)
                pack_bf16x2(v[14], v[15]));
 }
 
+// NeoX rotate_half on W-column chunks of one head: columns [c, c + W) and [c + half, ...), each value
+// x = (acc + bias) * rn; out_j = x_j cos_j - x_{j+half} sin_j, out_{j+half} = x_{j+half} cos_j + x_j sin_j.
+template <int W>
+__device__ __forceinline__ void rope_chunk(const GemmArgs& a, uint32_t t, int hb, int c, int half, float rn, bool live,
+                                           const float* cs, const float* sn, __nv_bfloat16* dst, int n0) {
+  uint32_t r1[W], r2[W];
+  if constexpr (W == 16) {
+    tmem_ld16(t + hb + c, *reinterpret_cast<uint32_t(*)[16]>(r1));
+    tmem_ld16(t + hb + half + c, *reinterpret_cast<uint32_t(*)[16]>(r2));
+    tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[16]>(r1));
+    tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[16]>(r2));
+  } else {
+    tmem_ld8(t + hb + c, *reinterpret_cast<uint32_t(*)[8]>(r1));
+    tmem_ld8(t + hb + half + c, *reinterpret_cast<uint32_t(*)[8]>(r2));
+    tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[8]>(r1));
+    tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[8]>(r2));
+  }
+  if (!live) return;
+  float o1[W], o2[W];
+#pragma unroll
+  for (int i = 0; i < W; i += 4) {
+    float b1[4], b2[4];
+    load_bias4(a.bias, n0 + hb + c + i, b1);
+    load_bias4(a.bias, n0 + hb + half + c + i, b2);
+    float4 cv = *reinterpret_cast<const float4*>(cs + c + i);
+    float4 sv = *reinterpret_cast<const float4*>(sn + c + i);
+    float cc[4] = {cv.x, cv.y, cv.z, cv.w}, ss[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float x1 = (__uint_as_float(r1[i + j]) * a.w_scale + b1[j]) * rn;
+      float x2 = (__uint_as_float(r2[i + j]) * a.w_scale + b2[j]) * rn;
+      o1[i + j] = x1 * cc[j] - x2 * ss[j];
+      o2[i + j] = x2 * cc[j] + x1 * ss[j];
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < W; i += 8) {
+    st_global_v4(dst + hb + c + i, pack_bf16x2(o1[i], o1[i + 1]), pack_bf16x2(o1[i + 2], o1[i + 3]),
+                 pack_bf16x2(o1[i + 4], o1[i + 5]), pack_bf16x2(o1[i + 6], o1[i + 7]));
+    st_global_v4(dst + hb + half + c + i, pack_bf16x2(o2[i], o2[i + 1]), pack_bf16x2(o2[i + 2], o2[i + 3]),
+                 pack_bf16x2(o2[i + 4], o2[i + 5]), pack_bf16x2(o2[i + 6], o2[i + 7]));
+  }
+}
+
 // Fused QKV epilogue.  Columns [0, d) are q, [d, 2d) k, [2d, 3d) v ([q_all | k_all | v_all]);
 // d % 256 == 0, so a tile never straddles two of them, and a tile holds 256 / Dh whole heads.
 // q and k get NeoX rotate_half on the first R = 2 * rot_half dims of each head: for j < R/2,
 //   out_j = a_j cos_j - a_{j+R/2} sin_j,   out_{j+R/2} = a_{j+R/2} cos_j + a_j sin_j,
-// with a = acc + bias and cos/sin the row's cache entries.
+// with a = acc + bias and cos/sin the row's cache entries.  With qk_norm, a is first divided by the
+// head's RMS, sqrt(mean(a^2) + eps) ([H3] "Update: video-VAE decoder block ported": per-head RMS
+// q/k norm without affine).
 __device__ __forceinline__ void epi_qkv(const GemmArgs& a, uint32_t t, int row, int n0) {
   const bool live = row < a.M;
   const int seg = n0 / a.d;
@@ -182,33 +228,34 @@ __device__ __forceinline__ void epi_qkv(const GemmArgs& a, uint32_t t, int row, 
   const float* sn = a.sin_cache + (size_t)row * half;
 #pragma unroll 1
   for (int hb = 0; hb < BN; hb += Dh) {
+    // qk_norm: x / sqrt(mean over the head of x^2 + eps), x = acc + bias, before the rotation
+    float rn = 1.f;
+    if (a.qk_norm) {
+      float ss = 0.f;
 #pragma unroll 1
-    for (int c = 0; c < half; c += 16) {
-      uint32_t r1[16], r2[16];
-      tmem_ld16(t + hb + c, r1);
-      tmem_ld16(t + hb + half + c, r2);
-      tmem_ld_wait_regs(r1);
-      tmem_ld_wait_regs(r2);
-      if (!live) continue;
-      float o1[16], o2[16];
+      for (int c = 0; c < Dh; c += 16) {
+        uint32_t r1[16];
+        tmem_ld16(t + hb + c, r1);
+        tmem_ld_wait_regs(r1);
 #pragma unroll
-      for (int i = 0; i < 16; i += 4) {
-        float b1[4], b2[4];
-        load_bias4(a.bias, n0 + hb + c + i, b1);
-        load_bias4(a.bias, n0 + hb + half + c + i, b2);
-        float4 cv = *reinterpret_cast<const float4*>(cs + c + i);
-        float4 sv = *reinterpret_cast<const float4*>(sn + c + i);
-        float cc[4] = {cv.x, cv.y, cv.z, cv.w}, ss[4] = {sv.x, sv.y, sv.z, sv.w};
+        for (int i = 0; i < 16; i += 4) {
+          float b1[4];
+          load_bias4(a.bias, n0 + hb + c + i, b1);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          float x1 = __uint_as_float(r1[i + j]) * a.w_scale + b1[j];
-          float x2 = __uint_as_float(r2[i + j]) * a.w_scale + b2[j];
-          o1[i + j] = x1 * cc[j] - x2 * ss[j];
-          o2[i + j] = x2 * cc[j] + x1 * ss[j];
+          for (int j = 0; j < 4; ++j) {
+            const float x = __uint_as_float(r1[i + j]) * a.w_scale + b1[j];
+            ss += x * x;
+          }
         }
       }
-      store_bf16x16(dst + hb + c, o1);
-      store_bf16x16(dst + hb + half + c, o2);
+      rn = 1.f / sqrtf(ss / (float)Dh + a.qk_eps);
+    }
+    if (half % 16 == 0) {
+#pragma unroll 1
+      for (int c = 0; c < half; c += 16) rope_chunk<16>(a, t, hb, c, half, rn, live, cs, sn, dst, n0);
+    } else {  // a rotary half of 8 (mod 16) columns, e.g. 24 of a 64-wide head
+#pragma unroll 1
+      for (int c = 0; c < half; c += 8) rope_chunk<8>(a, t, hb, c, half, rn, live, cs, sn, dst, n0);
     }
 #pragma unroll 1
     for (int c = 2 * half; c < Dh; c += 16) {  // partial rotary: dims >= R pass through
@@ -222,7 +269,7 @@ __device__ __forceinline__ void epi_qkv(const GemmArgs& a, uint32_t t, int row, 
         float b1[4];
         load_bias4(a.bias, n0 + hb + c + i, b1);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) o1[i + j] = __uint_as_float(r1[i + j]) * a.w_scale + b1[j];
+        for (int j = 0; j < 4; ++j) o1[i + j] = (__uint_as_float(r1[i + j]) * a.w_scale + b1[j]) * rn;
       }
       store_bf16x16(dst + hb + c, o1);
     }

@@ -36,6 +36,8 @@ struct GemmArgs {
   int out_kind;            // 0 bf16, 1 fp32
   // kEpiQkvRope
   int d, head_dim, rot_half;
+  int qk_norm;             // 1: per-head RMS norm of q and k (no affine) before the rotation
+  float qk_eps;
   const float* cos_cache;  // [M, rot_half]
   const float* sin_cache;
   void* q;
@@ -123,6 +125,8 @@ struct ModalRows {
 };
 cudaError_t row_map_launch(const uint8_t* tags, int n, const ModalRows& mr, int* rows, int* layout_code, int* status,
                            cudaStream_t s);
+// Rows of the per-head interleaved qkv order [q_h | k_h | v_h] into [q_all | k_all | v_all].
+cudaError_t qkv_deinterleave_launch(const void* src, void* dst, int H, int Dh, int row_bytes, cudaStream_t s);
 cudaError_t pack_ffn_in_launch(const void* w_in, const float* b_in, int F, int d, void* w_packed, float* b_packed,
                                cudaStream_t s);
 cudaError_t to_f32_launch(const void* src, int src_is_bf16, long long n, float* dst, cudaStream_t s);

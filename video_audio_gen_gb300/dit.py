@@ -25,7 +25,7 @@ MAX_LATENT_MODALITIES = 8
 
 EXPORTS = ["dit_create", "dit_destroy", "dit_last_error", "dit_workspace_bytes", "dit_bind_weights", "dit_forward",
            "dit_forward_modal", "dit_workspace_bytes_host", "dit_forward_host", "dit_euler_step",
-           "dit_euler_step_modal", "dit_time_shift", "dit_bind_latent_io", "dit_workspace_bytes_latent",
+           "dit_euler_step_modal", "dit_time_shift", "dit_vit_positions", "dit_bind_latent_io", "dit_workspace_bytes_latent",
            "dit_forward_latent", "dit_patchify", "dit_unpatchify", "dit_audio_pack", "dit_audio_unpack", "dit_get_stats", "dit_sync_status",
            "dit_set_dump", "dit_set_kernel_timing", "dit_get_kernel_times", "dit_op_norm_modulate",
            "dit_op_rope_cache", "dit_op_adaln", "dit_op_gemm", "dit_op_gemm_qkv_rope", "dit_op_gemm_gated_residual",
@@ -51,11 +51,12 @@ class DitConfig(ctypes.Structure):
                 ("norm_eps", ctypes.c_float), ("adaln", ctypes.c_int), ("n_modalities", ctypes.c_int),
                 ("t_embed_dim", ctypes.c_int), ("rope_axes", ctypes.c_int), ("rope_dims", ctypes.c_int * 3),
                 ("rotary_dim", ctypes.c_int), ("rope_base", ctypes.c_double), ("io_channels", ctypes.c_int),
-                ("dtype", ctypes.c_int), ("max_tokens", ctypes.c_int), ("max_docs", ctypes.c_int)]
+                ("dtype", ctypes.c_int), ("max_tokens", ctypes.c_int), ("max_docs", ctypes.c_int),
+                ("qk_norm", ctypes.c_int), ("qkv_interleaved", ctypes.c_int), ("final_norm", ctypes.c_int)]
 
 
 BLOCK_FIELDS = ["w_qkv", "b_qkv", "w_o", "b_o", "w_in", "b_in", "w_down", "b_down", "w_ada", "b_ada",
-                "ln1_g", "ln1_b", "ln2_g", "ln2_b"]
+                "ln1_g", "ln1_b", "ln2_g", "ln2_b", "res1", "res2"]
 GLOB_FIELDS = ["w_ada_final", "b_ada_final", "lnf_g", "lnf_b", "w_pre", "b_pre", "w_post", "b_post"]
 
 
@@ -106,6 +107,7 @@ def lib():
             "dit_euler_step_modal": (i32, [vp, vp, i32, i32, vp, ctypes.POINTER(ctypes.c_float),
                                            ctypes.POINTER(ctypes.c_float), i32, vp]),
             "dit_time_shift": (f32, [f32, f32]),
+            "dit_vit_positions": (i32, [i32, i32, i32, vp]),
             "dit_bind_latent_io": (i32, [vp, ctypes.POINTER(DitLatentIO), vp]),
             "dit_workspace_bytes_latent": (sz, [vp, i32, i32]),
             "dit_forward_latent": (i32, [vp, ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_int), vp, i32, vp,
@@ -177,6 +179,9 @@ def make_config(m: dict, max_tokens: int, max_docs: int) -> DitConfig:
     c.rotary_dim, c.rope_base, c.io_channels = m["rotary_dim"], m["rope_base"], m["io_channels"]
     c.dtype = DIT_BF16 if m["dtype"] == "bf16" else DIT_FP32
     c.max_tokens, c.max_docs = max_tokens, max_docs
+    c.qk_norm = 1 if m.get("qk_norm") else 0
+    c.qkv_interleaved = 1 if m.get("qkv_interleaved") else 0
+    c.final_norm = {"same": 0, "rms": 1, "ln": 2}[m.get("final_norm", "same")]
     return c
 
 
@@ -316,6 +321,14 @@ def euler_step_modal(x, v, tags, sigma, sigma_next, stream=None):
     st = (ctypes.c_float * len(sigma))(*[float(a) for a in sigma])
     sn = (ctypes.c_float * len(sigma_next))(*[float(a) for a in sigma_next])
     _check(lib().dit_euler_step_modal(_ptr(x), _ptr(v), n, d, _ptr(tags), st, sn, len(sigma), _stream(stream)))
+
+
+def vit_positions(T: int, H: int, W: int):
+    """dit_vit_positions: RotaryEmbeddingND positions [T*H*W, 3] (numpy fp64) of a T x H x W grid."""
+    import numpy as np
+    pos = np.empty((T * H * W, 3), dtype=np.float64)
+    _check(lib().dit_vit_positions(T, H, W, pos.ctypes.data))
+    return pos
 
 
 def time_shift(sigma: float, shift: float) -> float:
