@@ -198,7 +198,7 @@ def oracle_sample(w: dict, lay: dict, budget_rows: int | None = None, seconds: f
     d, F, H, Dh = m["hidden"], m["ffn_hidden"], m["n_heads"], m["head_dim"]
     threads = len(os.sched_getaffinity(0))
     oracle.set_threads(threads)
-    if not m["adaln"]:
+    if not m["adaln"] and not m.get("vit_positions"):
         # small token counts (the music DiT): whole blocks over every token, repeated until about
         # `seconds` of CPU work, scaled by L
         sub = dict(m, n_blocks=1)
@@ -272,6 +272,8 @@ def run_gpu(args, w, dist, rank, world):
     m = w["model"]
     docs = rank_documents(w["docs"], rank, world)
     lay = synth.build_layout(docs)
+    if m.get("vit_positions"):  # RotaryEmbeddingND's normalised grid, from the library
+        lay = dict(lay, pos=np.concatenate([dit.vit_positions(*dd["video"]) for dd in docs]))
     wr = dict(w, seed=rank_seed(w["seed"], rank))
     W = synth.make_weights(wr)
     h = gpu_util.make_handle(m, lay, W)
@@ -590,6 +592,9 @@ def workload_config(name, w, lay, extra=None):
     docs = ", ".join(f"{synth_doc(d)}" for d in w["docs"])
     cond = ("rmsnorm + modality AdaLN" if m["adaln"] else
             f"{m['norm']}norm, ungated residuals, 1x1 convs {m['io_channels']}->{m['hidden']}->{m['io_channels']}")
+    if m.get("vit_positions"):
+        cond = (f"RMSNorm gains, interleaved qkv, per-head q/k RMS norm, per-channel residual scales, "
+                f"RotaryEmbeddingND (base {m['rope_base']:g}, {m['rotary_dim']} of {m['head_dim']} dims), final LayerNorm")
     c = {"workload": f"{name}: {m['n_blocks']} blocks, d={m['hidden']}, {m['n_heads']}x{m['head_dim']} heads, "
                      f"FFN {m['ffn_hidden']} (value*silu(gate)), {cond}; "
                      f"{lay['n_tokens']} packed tokens in {lay['n_docs']} documents ({docs})",
@@ -621,7 +626,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="video_audio_bf16",
                     choices=["video_audio_bf16", "long_doc_bf16", "denoise_loop", "t2va_loop", "music_fp32",
-                             "video_audio_bf16_l1", "tiny", "ragged", "music_small", "nvfp4_gemm"])
+                             "video_audio_bf16_l1", "tiny", "ragged", "music_small", "nvfp4_gemm", "vit3d_decoder",
+                             "vit3d_small"])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
@@ -641,15 +647,20 @@ def main():
     if w.get("latent"):
         metric = ("DiT t2va denoise step ms/step (latent forward: patch projections, blocks, heads; Euler per "
                   "modality) and tokens/s on 1 GB300")
+    if w["model"].get("vit_positions"):
+        metric = "video-VAE ViT3D decoder forward tokens/s & ms/forward on 1 GB300; % of bf16 tensor-pipe peak"
 
     if args.impl == "reference":
         if rank != 0:
             return
         lay = synth.build_layout(w["docs"])
+        if w["model"].get("vit_positions"):
+            import oracle
+            lay = dict(lay, pos=np.concatenate([oracle.vit_positions(*dd["video"]) for dd in w["docs"]]))
         vals, secs = [], []
         # each step a bounded sample: the whole run stays within a couple of minutes
         per_step = max(1.0, min(SAMPLE_SECONDS, 120.0 / max(1, args.steps)))
-        rows = sample_rows(w, lay, per_step) if w["model"]["adaln"] else None
+        rows = sample_rows(w, lay, per_step) if (w["model"]["adaln"] or w["model"].get("vit_positions")) else None
         for _ in range(args.steps):
             tps, dt, R, threads = oracle_sample(w, lay, budget_rows=rows, seconds=per_step)
             vals.append(tps)
@@ -658,7 +669,7 @@ def main():
         ms_step = lay["n_tokens"] / tps * 1e3
         sample = (f"{R} query rows x 1 block of the workload per step ({args.steps} steps, median), "
                   f"scaled by N={lay['n_tokens']} rows x L={w['model']['n_blocks']} blocks")
-        if not w["model"]["adaln"]:
+        if not w["model"]["adaln"] and not w["model"].get("vit_positions"):
             sample = (f"whole blocks over {R} tokens per step ({args.steps} steps, median), "
                       f"scaled by L={w['model']['n_blocks']} blocks")
         line = {"impl": "reference", "metric": metric, "value": round(tps, 4), "unit": "tokens/s",
@@ -705,8 +716,13 @@ def main():
                          "d2h_bytes_per_step": int(r["d2h"])}),
                 "gpu_launches": int(r["launches"]), "clocks": r["clocks"]}
         if not args.no_cpu_baseline:
-            tps, dt, R, threads = oracle_sample(w, r["lay"])
-            what = (f"whole blocks over {R} tokens in all" if not w["model"]["adaln"] else f"{R} query rows x 1 block")
+            lay_cpu = r["lay"]
+            if w["model"].get("vit_positions"):  # the oracle's own positions
+                import oracle
+                lay_cpu = dict(lay_cpu, pos=np.concatenate([oracle.vit_positions(*dd["video"]) for dd in w["docs"]]))
+            tps, dt, R, threads = oracle_sample(w, lay_cpu)
+            whole = not w["model"]["adaln"] and not w["model"].get("vit_positions")
+            what = f"whole blocks over {R} tokens in all" if whole else f"{R} query rows x 1 block"
             line["cpu_baseline"] = {"value": round(tps, 4), "unit": "tokens/s", "cores": threads, "kind": "oracle",
                                     "sample": f"{what} ({dt:.1f} s on {threads} threads), "
                                               f"scaled by N={r['tokens']} rows x L={w['model']['n_blocks']} blocks"}
