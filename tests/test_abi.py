@@ -43,6 +43,14 @@ def _model(**kw):
     return m
 
 
+def test_create_accepts_the_vit_decoder_block():
+    import synth
+    dit = _lib()
+    h = dit.Dit(synth.WORKLOADS["vit3d_decoder"]["model"], 8192, 1)
+    assert h.workspace_bytes(8192, 1) > 8192 * 2048 * 4
+    h.h = None
+
+
 def test_create_validates_config():
     dit = _lib()
     h = dit.Dit(_model(), 17408, 2)  # a supported model: no device memory is touched
@@ -51,7 +59,10 @@ def test_create_validates_config():
     bad = [(dict(n_heads=23), dit.DIT_ERR_CONFIG), (dict(rope_dims=(32, 48, 40)), dit.DIT_ERR_CONFIG),
            (dict(hidden=3200, n_heads=25), dit.DIT_ERR_UNSUPPORTED), (dict(dtype="fp32"), dit.DIT_ERR_UNSUPPORTED),
            (dict(dtype="fp32", adaln=False, io_channels=96), dit.DIT_ERR_UNSUPPORTED),
-           (dict(head_dim=96, n_heads=32, rope_dims=(32, 32, 32), rotary_dim=96), dit.DIT_ERR_UNSUPPORTED), (dict(n_blocks=0), dit.DIT_ERR_CONFIG)]
+           (dict(head_dim=96, n_heads=32, rope_dims=(32, 32, 32), rotary_dim=96), dit.DIT_ERR_UNSUPPORTED), (dict(n_blocks=0), dit.DIT_ERR_CONFIG),
+           (dict(final_norm="ln"), dit.DIT_ERR_CONFIG),  # AdaLN's final layer is RMSNorm + modulate
+           (dict(dtype="fp32", adaln=False, qk_norm=True), dit.DIT_ERR_UNSUPPORTED),
+           (dict(rope_dims=(12, 16, 16), rotary_dim=44, n_heads=48, head_dim=64), dit.DIT_ERR_UNSUPPORTED)]
     for kw, st in bad:
         with pytest.raises(dit.DitError) as e:
             dit.Dit(_model(**kw), 100, 1)
