@@ -39,15 +39,15 @@ KINDS = ["gemm_qkv", "attention", "gemm_out", "gemm_ffn_up", "gemm_ffn_down", "n
 TRAFFIC = {
     ("attention", "video_audio_bf16"): {"bytes": 410346240, "src_sha": "cd92e0423d13c9de",
                                         "profile": "profiles/attention_video_audio_bf16.md"},
-    ("gemm_qkv", "video_audio_bf16"): {"bytes": 793978592, "src_sha": "41de12cade82e5ed",
+    ("gemm_qkv", "video_audio_bf16"): {"bytes": 821493760, "src_sha": "86f8bc031b1d4c6a",
                                        "profile": "profiles/gemm_video_audio_bf16.md"},
-    ("gemm_out", "video_audio_bf16"): {"bytes": 507667256, "src_sha": "41de12cade82e5ed",
+    ("gemm_out", "video_audio_bf16"): {"bytes": 504877312, "src_sha": "86f8bc031b1d4c6a",
                                        "profile": "profiles/gemm_video_audio_bf16.md"},
-    ("gemm_ffn_up", "video_audio_bf16"): {"bytes": 888858624, "src_sha": "41de12cade82e5ed",
+    ("gemm_ffn_up", "video_audio_bf16"): {"bytes": 832782848, "src_sha": "86f8bc031b1d4c6a",
                                           "profile": "profiles/gemm_video_audio_bf16.md"},
-    ("gemm_ffn_down", "video_audio_bf16"): {"bytes": 1242892616, "src_sha": "41de12cade82e5ed",
+    ("gemm_ffn_down", "video_audio_bf16"): {"bytes": 1241438208, "src_sha": "86f8bc031b1d4c6a",
                                             "profile": "profiles/gemm_video_audio_bf16.md"},
-    ("norm_modulate", "video_audio_bf16"): {"bytes": 289035776, "src_sha": "6ea3766d997bcd19",
+    ("norm_modulate", "video_audio_bf16"): {"bytes": 288634112, "src_sha": "139ad8f729b321b6",
                                             "profile": "profiles/norm_video_audio_bf16.md"},
 }
 
