@@ -162,3 +162,32 @@ def test_latent_rows_in_the_wrong_packed_places_fail_the_head_gate(base):
     mut_back[perm] = mut[0]  # undo the permutation on the output rows: only the packed places differ
     rms = np.sqrt((ref[0] ** 2).mean())
     assert np.abs(mut_back - ref[0]).max() > GATE * rms
+
+
+# ------------------------------------------------------------------------------------------------
+# NVFP4 format mistakes against the NVFP4 GEMM's gate (fp32 accumulation bound, see test_gpu_ops)
+# ------------------------------------------------------------------------------------------------
+
+def _nvfp4_case():
+    M, N, K = 16, 32, 128
+    q, s, g = synth.make_nvfp4(90, "w", N, K)
+    a = synth.normal(90, "a", (M, K), 1.0).astype(np.float16).astype(np.float64)
+    ref = oracle.nvfp4_linear(a, q, s, g)
+    bound = (K + 2) * 2.0 ** -23 * oracle.nvfp4_linear(np.abs(a), (q & 0x77).astype(np.uint8), s, g)
+    return a, q, s, g, ref, bound
+
+
+@pytest.mark.parametrize("mistake", ["nibbles_swapped", "scale_group_shifted", "global_divides", "scale_bias_6"])
+def test_planted_nvfp4_mistake_fails_the_gemm_gate(mistake):
+    a, q, s, g, ref, bound = _nvfp4_case()
+    if mistake == "nibbles_swapped":       # odd k in the low nibble
+        got = oracle.nvfp4_linear(a, ((q >> 4) | (q << 4)).astype(np.uint8), s, g)
+    elif mistake == "scale_group_shifted":  # group index off by one along K
+        got = oracle.nvfp4_linear(a, q, np.roll(s, 1, axis=1), g)
+    elif mistake == "global_divides":       # code * scale / global
+        got = oracle.nvfp4_linear(a, q, s, 1.0 / g)
+    else:                                   # E4M3 decoded with exponent bias 6 instead of 7: every scale x2
+        got = oracle.nvfp4_linear(a, q, s, g) * 2.0
+    assert np.any(np.abs(got - ref) > bound)
+    # the unmutated linear passes it under fp32-level noise
+    assert np.all(np.abs(ref * (1 + 2.0 ** -24) - ref) <= bound + 1e-30)
