@@ -232,3 +232,41 @@ def test_latent_denoise_loop_matches_oracle():
     for k in range(2):
         rms_v = np.sqrt((z0[k].astype(np.float64) ** 2).mean())
         assert np.abs(zg[k].astype(np.float64) - zo[k]).max() <= GATE * rms_v, k
+
+
+def test_forward_latent_with_an_empty_modality():
+    """Documents without audio: the audio modality has no rows, its z / v pointers are NULL, and the
+    video rows match the oracle."""
+    gu = _gu()
+    w = dict(synth.WORKLOADS["tiny"], docs=[dict(video=(2, 6, 8)), dict(video=(1, 4, 4))])
+    m = w["model"]
+    lay = synth.build_layout(w["docs"])
+    assert (lay["tags"] == 0).all()
+    W = synth.make_weights(w)
+    widths = synth.latent_widths()
+    io = synth.make_latent_io(52, m["hidden"], widths)
+    z = synth.make_latents(52, lay, widths)
+    assert z[1].shape[0] == 0
+    h = gu.make_handle(m, lay, W)
+    h.bind_latent_io({k: [None if a is None else gu.dev_f32(a) for a in v] for k, v in io.items()})
+    dl = gu.dev_layout(lay)
+    zd = [gu.dev_f32(z[0]), None]
+    vd = [torch.full((z[0].shape[0], widths[0]), float("nan"), dtype=torch.float32, device="cuda"), None]
+    ws = torch.empty(h.workspace_bytes_latent(lay["n_tokens"], lay["n_docs"]), dtype=torch.uint8, device="cuda")
+    ts = [float(np.float32(0.6)), float(np.float32(0.2))]
+    h.forward_latent(zd, dl["cu"], dl["ids"], dl["tags"], dl["pos"], ts, vd, ws)
+    assert h.sync_status(ws) == 0
+    ref, _ = oracle.forward_latent(m, W, io, z, lay, ts)
+    got = vd[0].double().cpu().numpy()
+    rms = np.sqrt((ref[0] ** 2).mean())
+    assert np.isfinite(got).all() and np.abs(got - ref[0]).max() <= GATE * rms
+
+
+def test_patchify_at_the_widest_token():
+    """C*pt*ph*pw = 12287, the widest token one CTA stages: one patch per run."""
+    dit, gu = _dit(), _gu()
+    C, T, H, W, pt, ph, pw = 12287, 1, 1, 3, 1, 1, 1
+    lat = synth.normal(42, "wide", (C, T * pt, H * ph, W * pw), 1.0)
+    tok = torch.empty((T * H * W, C), dtype=torch.float32, device="cuda")
+    dit.patchify(gu.dev_f32(lat), pt, ph, pw, tok)
+    assert np.array_equal(_bits(tok.cpu().numpy()), _bits(oracle.patchify(lat, pt, ph, pw)))

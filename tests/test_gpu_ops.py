@@ -498,3 +498,26 @@ def test_gemm_nvfp4_rejects_bad_shapes():
     assert lib.dit_op_gemm_nvfp4(a.data_ptr(), p.data_ptr(), 1.0, None, 4, 256, 48, o.data_ptr(), 1, None) != 0
     assert lib.dit_op_gemm_nvfp4(a.data_ptr(), p.data_ptr(), 1.0, None, 4, 256, 64, o.data_ptr(), 3, None) != 0
     assert dit.nvfp4_packed_bytes(100, 64) == 0
+
+
+def test_gemm_nvfp4_zero_codes_give_the_bias():
+    """Every code +0 or -0: the weight is zero whatever the scales, so out = bias exactly."""
+    dit, gu = _dit(), _gu()
+    M, N, K = 70, 256, 128
+    _, s, g = synth.make_nvfp4(73, "wz", N, K)
+    q = np.where(synth.uniform(73, "sign", N * K // 2).reshape(N, K // 2) < 0.5, 0x00, 0x88).astype(np.uint8)
+    a = synth.normal(73, "az", (M, K), 1.0).astype(np.float16)
+    bias = synth.normal(73, "bz", (N,), 0.5)
+    packed = torch.empty(dit.nvfp4_packed_bytes(N, K), dtype=torch.uint8, device="cuda")
+    dit.pack_nvfp4(torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda(), packed)
+    out = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    dit.gemm_nvfp4(torch.from_numpy(a).cuda(), packed, g, gu.dev_f32(bias), N, out, 1)
+    assert np.array_equal(out.cpu().numpy(), np.broadcast_to(bias, (M, N)))
+
+
+def test_euler_step_modal_with_no_tokens_is_a_no_op():
+    dit, gu = _dit(), _gu()
+    x = torch.zeros((0, 16), dtype=torch.float32, device="cuda")
+    t = torch.zeros((0,), dtype=torch.uint8, device="cuda")
+    dit.euler_step_modal(x, x, t, [0.5, 0.4], [0.4, 0.3])  # returns DIT_OK, launches nothing
+    torch.cuda.synchronize()
