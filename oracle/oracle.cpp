@@ -107,7 +107,8 @@ void orc_linspace(double start, double stop, int n, double* out) {
 // Timestep embedding.  READING (pages silent on the formula): the usual DiT sinusoid,
 // half = t_dim/2, f_k = exp(-ln(10000) * k / half), e = [cos(1000 t f_k) | sin(1000 t f_k)].
 // The ungated SiLU of [H3] "The device-resident forward (W2b)" is applied by the caller.
-// parity unpinned beyond the closed form at t = 0.
+// Pinned to that reading by closed forms and invariants: t = 0, the quarter and half turn of the
+// first pair at t = pi / 2000 and pi / 1000, the unit circle, and the geometric fall of the angles.
 // ---------------------------------------------------------------------------------------------
 void orc_timestep_embedding(double t, int t_dim, double* out) {
   int half = t_dim / 2;

@@ -106,6 +106,28 @@ def test_timestep_embedding_closed_form_at_zero():
     assert (e[:128] == 1.0).all() and (e[128:] == 0.0).all()
 
 
+def test_timestep_embedding_invariants_and_quarter_turn():
+    """Closed forms and invariants of the sinusoid [cos(1000 t f_k) | sin(1000 t f_k)] at t != 0:
+    each (cos, sin) pair lies on the unit circle; f_0 = 1 puts the first pair a quarter and a half
+    turn round at t = pi / 2000 and pi / 1000; the recovered angles fall geometrically by
+    10000^(-1 / half) from 1000 t (so a swapped cos/sin, a missing 1000 or an endpoint-style
+    exponent k / (half - 1) each fail)."""
+    half = 128
+    for t in (0.37, 0.9731, 1.0):
+        e = oracle.timestep_embedding(t, 2 * half)
+        assert np.allclose(e[:half] ** 2 + e[half:] ** 2, 1.0, rtol=0, atol=1e-15)
+    e = oracle.timestep_embedding(np.pi / 2000, 2 * half)
+    assert abs(e[0]) < 1e-15 and abs(e[half] - 1.0) < 1e-15
+    e = oracle.timestep_embedding(np.pi / 1000, 2 * half)
+    assert abs(e[0] + 1.0) < 1e-15 and abs(e[half]) < 1e-15
+    t = 1e-3  # every angle below pi: atan2 recovers it without wrapping
+    e = oracle.timestep_embedding(t, 2 * half)
+    ang = np.arctan2(e[half:], e[:half])
+    assert abs(ang[0] - 1000 * t) < 1e-14
+    ratio = ang[1:] / ang[:-1]
+    assert np.allclose(ratio, 10000.0 ** (-1.0 / half), rtol=1e-12, atol=0)
+
+
 def test_adaln_is_matvec_of_silu_embedding():
     w = _workload(TINY_RMS, 5, DOCS8)
     W = synth.make_weights(w)
