@@ -42,3 +42,10 @@ def test_vit3d_block_reading_matches_the_printed_manifest():
     assert m["rotary_dim"] == float(t["rope_dim_ratio"][0]) * m["head_dim"]
     total = m["n_blocks"] * len(shapes["block"]) + len(shapes["glob"]) + int(t["surround"][0])
     assert len(shapes["block"]) == 12 and total == int(t["tensors"][0])
+
+
+def test_audio_latent_width_matches_the_printed_width():
+    t = _table("audio_latent_width.txt")
+    c = int(t["audio_latent_channels"][0])
+    assert synth.AUDIO_LATENT["channels"] == c == int(t["dec_in_proj"][0])
+    assert synth.latent_widths()[1] == c  # audio pack: one token per latent frame, c features
