@@ -34,21 +34,15 @@ SAMPLE_SECONDS = 10.0   # target CPU work of the oracle baseline sample
 KINDS = ["gemm_qkv", "attention", "gemm_out", "gemm_ffn_up", "gemm_ffn_down", "norm_modulate", "other", "latent_io"]
 
 # DRAM traffic per launch from ncu captures (dram__bytes_read.sum + dram__bytes_write.sum), keyed by
-# kernel kind and workload, with the sha256 of the kernel source the capture was taken on; the
-# figure is reported only while the source is unchanged.  See profiles/.
+# kernel kind and workload, with the sha256 prefix of the kernel source the capture was taken on; the
+# figure is reported only while that source is unchanged.
 TRAFFIC = {
-    ("attention", "video_audio_bf16"): {"bytes": 410396416, "src_sha": "95e4b2ef60a3ac48",
-                                        "profile": "profiles/attention_video_audio_bf16.md"},
-    ("gemm_qkv", "video_audio_bf16"): {"bytes": 821493760, "src_sha": "86f8bc031b1d4c6a",
-                                       "profile": "profiles/gemm_video_audio_bf16.md"},
-    ("gemm_out", "video_audio_bf16"): {"bytes": 504877312, "src_sha": "86f8bc031b1d4c6a",
-                                       "profile": "profiles/gemm_video_audio_bf16.md"},
-    ("gemm_ffn_up", "video_audio_bf16"): {"bytes": 832782848, "src_sha": "86f8bc031b1d4c6a",
-                                          "profile": "profiles/gemm_video_audio_bf16.md"},
-    ("gemm_ffn_down", "video_audio_bf16"): {"bytes": 1241438208, "src_sha": "86f8bc031b1d4c6a",
-                                            "profile": "profiles/gemm_video_audio_bf16.md"},
-    ("norm_modulate", "video_audio_bf16"): {"bytes": 288634112, "src_sha": "139ad8f729b321b6",
-                                            "profile": "profiles/norm_video_audio_bf16.md"},
+    ("attention", "video_audio_bf16"): {"bytes": 410396416, "src_sha": "95e4b2ef60a3ac48"},
+    ("gemm_qkv", "video_audio_bf16"): {"bytes": 821493760, "src_sha": "86f8bc031b1d4c6a"},
+    ("gemm_out", "video_audio_bf16"): {"bytes": 504877312, "src_sha": "86f8bc031b1d4c6a"},
+    ("gemm_ffn_up", "video_audio_bf16"): {"bytes": 832782848, "src_sha": "86f8bc031b1d4c6a"},
+    ("gemm_ffn_down", "video_audio_bf16"): {"bytes": 1241438208, "src_sha": "86f8bc031b1d4c6a"},
+    ("norm_modulate", "video_audio_bf16"): {"bytes": 288634112, "src_sha": "139ad8f729b321b6"},
 }
 
 
@@ -454,6 +448,73 @@ def run_gpu(args, w, dist, rank, world):
                 launches=launches, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, flops=fl["total"], docs=D, lay=lay)
 
 
+def run_loop_figures(args, dist, rank, world):
+    """The 50-step denoise loop on the video+audio model (requests of 17,408 and 9,216 tokens packed in
+    one sequence), measured beside the default workload's forward: ms per step (forward + Euler step,
+    inputs resident) over one whole 50-step loop, and the loop end to end, from the initial noise in
+    pinned host memory to the final x read back (the copies inside the timed region)."""
+    import torch
+
+    import synth
+    from tests import gpu_util
+    from video_audio_gen_gb300 import dit
+
+    w = synth.WORKLOADS["denoise_loop"]
+    m = w["model"]
+    lay = synth.build_layout(rank_documents(w["docs"], rank, world))
+    wr = dict(w, seed=rank_seed(w["seed"], rank))
+    W = synth.make_weights(wr)
+    h = gpu_util.make_handle(m, lay, W)
+    del W
+    N, D = lay["n_tokens"], lay["n_docs"]
+    dl = gpu_util.dev_layout(lay)
+    x_host = synth.make_tokens(wr, lay)
+    x0 = gpu_util.dev_f32(x_host)
+    x = torch.empty_like(x0)
+    v = torch.empty_like(x0)
+    ws = gpu_util.workspace(h, N, D)
+    sig = [float(a) for a in synth.sigmas(w["steps"])]
+    steps = len(sig) - 1
+    stream = torch.cuda.current_stream()
+
+    def loop():
+        for i in range(steps):
+            h.forward(x, dl["cu"], dl["ids"], dl["tags"], dl["pos"], sig[i], v, ws)
+            dit.euler_step(x, v, sig[i], sig[i + 1])
+
+    x.copy_(x0)
+    for i in range(args.warmup):
+        h.forward(x, dl["cu"], dl["ids"], dl["tags"], dl["pos"], sig[i], v, ws)
+    x.copy_(x0)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    loop()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    loop_ms = reduce_max_ms(e0.elapsed_time(e1), dist)
+    assert h.sync_status(ws) == 0, "device status after the timed loop"
+    hx = torch.from_numpy(np.ascontiguousarray(x_host)).pin_memory()
+    hout = torch.empty(x_host.shape, dtype=torch.float32).pin_memory()
+    if dist is not None:
+        dist.barrier()
+    t0 = time.perf_counter()
+    x.copy_(hx, non_blocking=True)
+    loop()
+    hout.copy_(x, non_blocking=True)
+    stream.synchronize()
+    e2e_ms = reduce_max_ms((time.perf_counter() - t0) * 1e3, dist)
+    assert h.sync_status(ws) == 0, "device status after the end-to-end loop"
+    h.close()
+    return {"workload": f"denoise_loop: the {m['n_blocks']}-block video+audio model, {N} tokens in {D} requests "
+                        f"({', '.join(synth_doc(d) for d in w['docs'])}), {steps} Euler steps, sigmas 1 -> 0",
+            "steps": steps, "ms_per_step": round(loop_ms / steps, 3), "loop_ms": round(loop_ms, 1),
+            "tokens_per_s": round(N * world / (loop_ms / steps * 1e-3), 1),
+            "e2e_loop_ms": round(e2e_ms, 1), "h2d_bytes": int(hx.numel() * 4), "d2h_bytes": int(hout.numel() * 4)}
+
+
 def run_nvfp4_gemm(args):
     """The four linear maps of one block of the video+audio model at its full 17,408-token sequence,
     with NVFP4 weights (E2M1 codes, an E4M3 scale per 16 along K, fp32 global scale; f16
@@ -624,13 +685,15 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", default="video_audio_bf16",
+    ap.add_argument("--workload", default="long_doc_bf16",
                     choices=["video_audio_bf16", "long_doc_bf16", "denoise_loop", "t2va_loop", "music_fp32",
                              "video_audio_bf16_l1", "tiny", "ragged", "music_small", "nvfp4_gemm", "vit3d_decoder",
                              "vit3d_small"])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-loop", action="store_true",
+                    help="skip the denoise-loop figures that the default workload's line carries")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -726,6 +789,12 @@ def main():
             line["cpu_baseline"] = {"value": round(tps, 4), "unit": "tokens/s", "cores": threads, "kind": "oracle",
                                     "sample": f"{what} ({dt:.1f} s on {threads} threads), "
                                               f"scaled by N={r['tokens']} rows x L={w['model']['n_blocks']} blocks"}
+    loop = None
+    if args.workload == "long_doc_bf16" and not args.no_loop:
+        loop = run_loop_figures(args, dist, rank, world)
+    if rank == 0:
+        if loop is not None:
+            line["denoise_loop"] = loop
         print(json.dumps(line))
     if dist is not None:
         dist.barrier()

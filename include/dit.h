@@ -131,12 +131,18 @@ typedef struct dit_handle dit_handle;
  * Model-level calls
  * ------------------------------------------------------------------------------------------- */
 
-/* Validate `cfg` and create a handle.  No device memory is allocated here.
- * What the kernels tile: dtype DIT_BF16 with RMSNorm blocks (with or without AdaLN); hidden a
- * multiple of 256 with hidden / 128 in {1..6, 8, 10, 12, 16, 20, 24, 32, 40, 48, 64}; head_dim 64
- * or 128; ffn_hidden a multiple of 128; rotary_dim / 2 a multiple of 8 and head_dim - rotary_dim a
- * multiple of 16; t_embed_dim a multiple of 8 (of 256 above 256); io_channels 0.  Anything else returns DIT_ERR_CONFIG (not a
- * valid model) or DIT_ERR_UNSUPPORTED (valid, not tiled), dit_last_error(NULL) naming the field. */
+/* Validate `cfg` and create a handle.  No device memory is allocated here.  What the kernels tile:
+ *   DIT_BF16: RMSNorm blocks, with modality AdaLN or without it (the ViT3D decoder block: qk_norm,
+ *     qkv_interleaved, final_norm, RMS gains and residual scales); hidden a multiple of 256 with
+ *     hidden / 128 in {1..6, 8, 10, 12, 16, 20, 24, 32, 40, 48, 64}; head_dim 64 or 128;
+ *     ffn_hidden a multiple of 128; rotary_dim / 2 a multiple of 8 and head_dim - rotary_dim a
+ *     multiple of 16; t_embed_dim a multiple of 8 (of 256 above 256); io_channels 0.
+ *   DIT_FP32 (the music DiT, [M3] "What moved"): RMSNorm or LayerNorm blocks without AdaLN,
+ *     head_dim 64 or 128, any even rotary_dim <= head_dim (partial rotary), hidden a multiple of 128
+ *     (a width the norm kernel tiles), ffn_hidden a multiple of 64, and io_channels 0 or a multiple
+ *     of 128 (1x1 pre/post convolutions around the stack).
+ * Anything else returns DIT_ERR_CONFIG (not a valid model) or DIT_ERR_UNSUPPORTED (valid, not
+ * tiled), dit_last_error(NULL) naming the field. */
 DIT_API dit_status dit_create(const dit_config* cfg, dit_handle** out);
 
 /* Release the handle and its repacked weight copies (synchronises the device first). */
@@ -448,8 +454,12 @@ DIT_API dit_status dit_op_attention(const void* q, const void* k, const void* vt
  *   held by every GPU that loads the library until the process exits.  Nothing is allocated or freed.
  *   Capacity: ceil(n_tokens / 128) + n_docs <= DIT_ATTENTION_NOALLOC_MAX_TILES, else
  *   DIT_ERR_CAPACITY with dit_last_error(NULL) saying so, before any work is enqueued.
- *   Set-up: the first call on each device looks up the array's device address
- *   (cudaGetSymbolAddress) and caches it; make that first call before any stream capture.
+ *   Errors found on the device: cu_seqlens is checked on the device, as in dit_op_attention; a
+ *   rejected layout leaves `o` unwritten and the call still returns DIT_OK (the work is
+ *   asynchronous).  dit_op_attention_noalloc_status reads the outcome back.
+ *   Set-up: the first call in each CUDA context (per device; again after cudaDeviceReset) looks up
+ *   the array's device address (cudaGetSymbolAddress) and caches it for that context; make that
+ *   first call before any stream capture.
  *   Sharing: all calls use the same array, which keeps the last call's contents (the status words
  *   are cleared at the start of each call).  Calls whose device work overlaps (other streams, other
  *   host threads on the same device) race on it: serialise them. */
@@ -457,6 +467,14 @@ DIT_API dit_status dit_op_attention(const void* q, const void* k, const void* vt
 DIT_API dit_status dit_op_attention_noalloc(const void* q, const void* k, const void* vt, int n_pad,
                                             const int32_t* cu_seqlens, int n_docs, int n_tokens, int n_heads,
                                             int head_dim, void* o, void* stream);
+
+/* Outcome of the last dit_op_attention_noalloc call in the current context: synchronises `stream`,
+ * reads the fixed array's status words (no allocation) and returns DIT_OK, DIT_ERR_LAYOUT
+ * (cu_seqlens rejected; *layout_code, when layout_code is not NULL, gets the validator's code:
+ * 1 no documents, 2 cu[0] != 0, 3 not strictly increasing, 4 cu[n_docs] != n_tokens),
+ * DIT_ERR_DEVICE_TIMEOUT (a bounded wait ran out) or DIT_ERR_CUDA.  Shares the array, so it reads
+ * whichever call's device work finished last. */
+DIT_API dit_status dit_op_attention_noalloc_status(int* layout_code, void* stream);
 
 #ifdef __cplusplus
 }

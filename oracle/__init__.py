@@ -425,6 +425,66 @@ def block_forward(m: dict, weights: dict, l: int, mod_block, x, layout: dict, cs
     return x
 
 
+def block_rows(m: dict, weights: dict, l: int, mod_block, x, layout: dict, rows) -> np.ndarray:
+    """Block ``l`` of the modality-AdaLN DiT on a subset of query rows: the output rows ``rows`` of
+    orc_block_forward for the block input x [N, d], without computing the other rows' outputs.
+
+    The attention of a row reads every key and value of its own document, so those are computed for
+    every row of the documents the sampled rows fall in; everything after the attention is per row.
+    The steps are orc_block_forward's ([H3] "The device-resident forward (W2b)"):
+      y = RMS(x) (1 + scale1[tag]) + shift1[tag];   k, v = y W_{k,v}^T + b;   k <- RoPE(k)
+      q = RoPE(y W_q^T + b) on the sampled rows;    o = softmax(q k^T / sqrt(Dh)) v per document
+      x' = x + gate1[tag] (o W_o^T + b_o);          y2 = RMS(x') (1 + scale2) + shift2
+      out = x' + gate2[tag] ((u * silu(g)) W_down^T + b_down),  [u | g] = y2 W_in^T + b_in
+    every step in double.  The key/value projection of whole documents is the one step done with a
+    library primitive (numpy's float64 matmul) rather than the oracle's naive loop, so that documents
+    of tens of thousands of tokens finish in seconds; the other steps are the oracle's own functions.
+    mod_block: [n_mod, 6, d] (this block's AdaLN rows).  Returns [len(rows), d] float64."""
+    assert m["adaln"] and m["norm"] == "rms" and not m.get("qk_norm") and not m.get("qkv_interleaved")
+    d, H, Dh, R, eps = m["hidden"], m["n_heads"], m["head_dim"], m["rotary_dim"], m["norm_eps"]
+    bw = weights["blocks"][l]
+    x = np.asarray(x)
+    rows = np.asarray(rows, dtype=np.int64)
+    cu = np.asarray(layout["cu_seqlens"], dtype=np.int64)
+    tags = np.asarray(layout["tags"], dtype=np.uint8)
+    mod = _dbl(mod_block)
+    docs = np.unique(np.asarray(layout["doc_ids"])[rows])
+    keys = np.concatenate([np.arange(cu[j], cu[j + 1]) for j in docs])
+    lens = np.array([cu[j + 1] - cu[j] for j in docs], dtype=np.int64)
+    cu_loc = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    first = {int(j): int(cu_loc[i]) - int(cu[j]) for i, j in enumerate(docs)}
+    loc = np.array([r + first[int(layout["doc_ids"][r])] for r in rows], dtype=np.int64)
+
+    y = modulate(rms_norm(x[keys], eps), tags[keys], mod[:, 0], mod[:, 1])
+    w_qkv = np.asarray(bw["w_qkv"], dtype=np.float64)
+    b_qkv = bw.get("b_qkv")
+    b_qkv = None if b_qkv is None else np.asarray(b_qkv, dtype=np.float64)
+    k = y @ w_qkv[d:2 * d].T
+    v = y @ w_qkv[2 * d:].T
+    if b_qkv is not None:
+        k += b_qkv[d:2 * d]
+        v += b_qkv[2 * d:]
+    cs, sn = rope_cos_sin(m, np.asarray(layout["pos"])[keys])
+    k = rope_apply(k, H, Dh, R, cs, sn)
+    q = linear(y[loc], bw["w_qkv"][:d], None if b_qkv is None else bw["b_qkv"][:d])
+    q = rope_apply(q, H, Dh, R, cs[loc], sn[loc])
+    q_all = np.zeros_like(k)  # only the sampled rows' queries are read
+    q_all[loc] = q
+    o = attention_rows(q_all, k, v, cu_loc, H, Dh, loc)
+    tg = tags[rows]
+    xm = _dbl(x[rows]) + mod[tg, 2] * linear(o, bw["w_o"], bw.get("b_o"))
+    y2 = modulate(rms_norm(xm, eps), tg, mod[:, 3], mod[:, 4])
+    hh = swiglu(linear(y2, bw["w_in"], bw.get("b_in")))
+    return xm + mod[tg, 5] * linear(hh, bw["w_down"], bw.get("b_down"))
+
+
+def final_rows(m: dict, mod_final, x, tags) -> np.ndarray:
+    """The final layer of the AdaLN DiT on given rows: RMS(x) (1 + scale_f[tag]) + shift_f[tag]
+    (orc_forward's last step).  mod_final [n_mod, 2, d]; x [n, d]; tags [n]."""
+    mf = _dbl(mod_final)
+    return modulate(rms_norm(x, m["norm_eps"]), tags, mf[:, 0], mf[:, 1])
+
+
 def forward(m: dict, weights: dict, x_in, layout: dict, t, dumps: bool = False):
     """Whole forward.  Returns (out float64 shaped like x_in, block dumps [L, N, d] or None).
     t is one timestep, or one per modality."""

@@ -233,6 +233,17 @@ LOOP_SMALL = dict(model=dict(synth.WORKLOADS["ragged"]["model"], hidden=256, n_h
                   t="schedule", steps=50, w_std=0.02, bias_std=0.0, x_std=1.0)
 
 
+def _loop_gate(xg, xo, x0, what):
+    """The loop's gate, GATE x the RMS of the initial noise x0, printed beside the measured error and
+    beside the RMS of the oracle's final x (the gate's scale before it was tied to the noise)."""
+    err = float(np.abs(xg.astype(np.float64) - xo).max())
+    rms_x0 = float(np.sqrt((x0.astype(np.float64) ** 2).mean()))
+    rms_final = float(np.sqrt((xo ** 2).mean()))
+    print(f"loop ({what}): max|x_gpu - x_oracle| = {err:.3e}; gate GATE * RMS(x0) = {GATE * rms_x0:.3e}; "
+          f"GATE * RMS(final x) = {GATE * rms_final:.3e}; error / RMS(x0) = {err / rms_x0:.2e}")
+    assert err <= GATE * rms_x0
+
+
 def _gpu_loop(h, lay, x0, sig, start=0, stop=None, x_from=None):
     dit, gu = _dit(), _gu()
     dl = gu.dev_layout(lay)
@@ -266,10 +277,9 @@ def test_denoise_loop_matches_oracle_reduced():
         xo = oracle.euler_step(xo, v.astype(np.float32), sig[i], sig[i + 1])
     oracle.set_threads(1)
     # Each step moves x by (sigma_next - sigma) * v, and the steps' sigma decrements sum to 1, so the
-    # loop inherits the per-forward bound on v's scale (the initial noise's RMS); the final x itself
-    # nearly cancels (x0 - sum dsigma v) and is no scale to measure against.
-    rms_v = np.sqrt((x0.astype(np.float64) ** 2).mean())
-    assert np.abs(xg.astype(np.float64) - xo).max() <= GATE * rms_v
+    # loop inherits the per-forward bound on v's scale, which is the initial noise's RMS; the final x
+    # itself nearly cancels (x0 - sum dsigma v) and is no scale to measure against.
+    _loop_gate(xg, xo, x0, "single schedule")
 
 
 def _gpu_loop_modal(h, lay, x0, sig_v, sig_a):
@@ -309,8 +319,7 @@ def test_denoise_loop_shifted_modal_schedules_match_oracle():
         xo = oracle.euler_step_tagged(xo, v.astype(np.float32), lay["tags"], [sv[i], sa[i]], [sv[i + 1], sa[i + 1]])
     oracle.set_threads(1)
     # the same bound as the single-schedule loop: each modality's decrements still sum to 1
-    rms_v = np.sqrt((x0.astype(np.float64) ** 2).mean())
-    assert np.abs(xg.astype(np.float64) - xo).max() <= GATE * rms_v
+    _loop_gate(xg, xo, x0, "shifted schedules")
 
 
 def test_denoise_loop_resume_is_bit_identical():
@@ -331,11 +340,11 @@ def test_denoise_loop_resume_is_bit_identical():
 
 # ------------------------------------------------------------------------------------------------
 # the fp32 forward (music DiT shape)
-# Gate (the fp32 counterpart of the bf16 gate): every layer output within 1e-5 of its RMS, with a
-# 1e-6 absolute floor: max|g - r| <= max(1e-5 * RMS(r), 1e-6).  The stricter per-element reading
-# |g - r| <= 1e-5 |r| + 1e-6 holds on the small case; at the full 24-block, K = 8192 shape fp32
-# accumulation noise (~1e-6 absolute on O(1) values) exceeds it on near-zero elements, for any fp32
-# implementation, so there it is reported, not asserted.
+# Gates: every layer output within 1e-5 of its RMS with a 1e-6 absolute floor,
+# max|g - r| <= max(1e-5 * RMS(r), 1e-6), and the per-element form |g - r| <= 1e-5 |r| + 1e-6.
+# The per-element form is asserted on the small case.  On the full 24-block shape each layer's count
+# of elements outside it and its worst ratio |g - r| / (1e-5 |r| + 1e-6) are printed: there the
+# elements whose value is near zero carry the absolute rounding of K = 8192 fp32 sums.
 # ------------------------------------------------------------------------------------------------
 
 FP32_REL, FP32_ABS = 1e-5, 1e-6
@@ -347,10 +356,15 @@ def _fp32_check(w, run, ref_out, ref_dumps, per_element):
     for i, (g, o) in enumerate(layers):
         err = np.abs(g - o).max()
         rms = np.sqrt((o ** 2).mean())
+        ratio = np.abs(g - o) / (FP32_REL * np.abs(o) + FP32_ABS)
+        bad = ratio > 1.0
+        name = f"block {i}" if i < len(layers) - 1 else "output"
+        print(f"{w['model']['n_blocks']}-block fp32 {name}: max|g - r| / RMS = {err / rms:.3e}; per-element "
+              f"violations {int(bad.sum())} of {bad.size} ({bad.mean():.2e}), worst ratio {ratio.max():.3f}, at "
+              f"|r| = {np.abs(o).reshape(-1)[int(ratio.argmax())]:.3e}")
         assert err <= max(FP32_REL * rms, FP32_ABS), (i, float(err), float(rms))
         worst = max(worst, float(err / rms))
         if per_element:
-            bad = np.abs(g - o) > FP32_REL * np.abs(o) + FP32_ABS
             assert not bad.any(), (i, int(bad.sum()), float(err))
     return worst
 

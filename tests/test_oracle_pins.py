@@ -414,6 +414,53 @@ def test_forward_modality_swap_symmetry():
     assert np.array_equal(out, out2)
 
 
+def test_block_rows_equals_the_whole_block_on_its_rows():
+    """The teacher-forcing block (the keys and values of whole documents, everything else on the
+    sampled rows only) against the oracle's whole block: every sampled row agrees to rounding.
+    Rows: document ends, 128-row tile edges, a 1-token document, audio rows; non-zero biases."""
+    w = synth.WORKLOADS["ragged"]
+    m = dict(w["model"], n_blocks=1)
+    wl = dict(w, model=m)
+    lay = synth.build_layout(w["docs"])
+    W = synth.make_weights(wl)
+    x = synth.make_tokens(wl, lay).astype(np.float64) * 1.5
+    mod, _ = oracle.adaln(m, W, 0.37)
+    cs, sn = oracle.rope_cos_sin(m, lay["pos"])
+    oracle.set_threads(4)
+    full = oracle.block_forward(m, W, 0, mod[0], x, lay, cs, sn)
+    cu = lay["cu_seqlens"]
+    rows = np.unique([0, 1, int(cu[1]) - 1, int(cu[1]), 127, 128, 129, int(cu[2]), int(cu[3]) - 1,
+                      int(cu[3]), 300, lay["n_tokens"] - 1] + list(np.nonzero(lay["tags"] == 1)[0][::9]))
+    got = oracle.block_rows(m, W, 0, mod[0], x, lay, rows)
+    # rows of only some documents: the others' keys are not needed
+    one = oracle.block_rows(m, W, 0, mod[0], x, lay, [int(cu[3]) + 5])
+    oracle.set_threads(1)
+    scale = np.abs(full[rows]).max()
+    assert np.abs(got - full[rows]).max() <= 1e-12 * scale
+    assert np.abs(one[0] - full[int(cu[3]) + 5]).max() <= 1e-12 * scale
+    # and the block did move these rows (the comparison is not of the residual alone)
+    assert np.abs(full[rows] - x[rows]).max() > 1e-3
+
+
+def test_block_rows_reads_only_its_own_document():
+    """Changing another document's inputs leaves a sampled row's block output unchanged (bit for bit):
+    the keys and values it attends over are its own document's."""
+    w = synth.WORKLOADS["ragged"]
+    m = dict(w["model"], n_blocks=1)
+    wl = dict(w, model=m)
+    lay = synth.build_layout(w["docs"])
+    W = synth.make_weights(wl)
+    x = synth.make_tokens(wl, lay).astype(np.float64)
+    mod, _ = oracle.adaln(m, W, 0.37)
+    cu = lay["cu_seqlens"]
+    r = [int(cu[1]) + 3]
+    a = oracle.block_rows(m, W, 0, mod[0], x, lay, r)
+    x2 = x.copy()
+    x2[cu[3]:cu[4]] += 1.0
+    b = oracle.block_rows(m, W, 0, mod[0], x2, lay, r)
+    assert np.array_equal(a, b)
+
+
 def test_forward_thread_count_does_not_change_bits():
     w = synth.WORKLOADS["ragged"]
     w = dict(w, model=dict(w["model"], n_blocks=1))

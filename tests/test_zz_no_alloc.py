@@ -4,7 +4,7 @@ The no-allocation variant exists for callers that cannot call cudaMalloc (a plug
 framework's executor with no allocator handed to it, a latency-critical serving thread that cannot
 take cudaMalloc's implicit device synchronisation): its scratch lives in a fixed array inside the
 library.  Two calls in a row with different layouts check that the shared array is reset between
-calls.  This file is collected last so a failure here cannot hide any other test's result; it also
+calls: their results equal dit_op_attention's bit for bit.  This file is collected last so a failure here cannot hide any other test's result; it also
 passes on its own in a fresh process.
 """
 import numpy as np
@@ -45,10 +45,30 @@ def test_attention_noalloc_matches_workspace_entry_point():
         got = torch.full((n, H * Dh), float("nan"), dtype=torch.bfloat16, device="cuda")
         dit.attention_noalloc(q, k, vt, n_pad, cu, H, Dh, got)
         torch.cuda.synchronize()
-        r = ref.float().double().cpu().numpy()
+        # the same kernels on the same inputs: the results agree bit for bit (a stale entry left in
+        # the shared array by the previous call would show here)
+        assert torch.equal(got, ref)
+        assert dit.attention_noalloc_status() == (dit.DIT_OK, 0)
         g = got.float().double().cpu().numpy()
-        assert np.isfinite(g).all()
-        assert np.all(np.abs(g - r) <= BF16_REL * np.abs(r) + 2.0 ** -8 * np.abs(v).max())
+        assert np.isfinite(g).all() and np.abs(g).max() <= np.abs(v).max() * (1 + BF16_REL)
+
+
+def test_attention_noalloc_reports_a_rejected_layout():
+    """cu_seqlens that is not strictly increasing is rejected on the device: the output is left as it
+    was, the call itself returns DIT_OK (its work is asynchronous), and the status reader returns
+    DIT_ERR_LAYOUT with the validator's code 3; a valid call afterwards reads DIT_OK again."""
+    from video_audio_gen_gb300 import build, dit
+    build.build()
+    lay, n_pad, q, k, vt, cu, _ = _attention_inputs(synth.WORKLOADS["tiny"]["docs"], 4, 64, 203)
+    n = lay["n_tokens"]
+    bad = torch.tensor([0, 160, 96], dtype=torch.int32, device="cuda")  # same sizes, decreasing
+    o = torch.full((n, 4 * 64), 5.0, dtype=torch.bfloat16, device="cuda")
+    dit.attention_noalloc(q, k, vt, n_pad, bad, 4, 64, o)
+    assert dit.attention_noalloc_status() == (dit.DIT_ERR_LAYOUT, 3)
+    assert (o == 5.0).all()
+    dit.attention_noalloc(q, k, vt, n_pad, cu, 4, 64, o)
+    assert dit.attention_noalloc_status() == (dit.DIT_OK, 0)
+    assert torch.isfinite(o.float()).all() and not (o == 5.0).all()
 
 
 def test_attention_noalloc_rejects_sizes_beyond_its_scratch():

@@ -1476,31 +1476,74 @@ dit_status dit_op_attention(const void* q, const void* k, const void* vt, int n_
 // ------------------------------------------------------------------------------------------------
 namespace {
 
-constexpr int kNoAllocMaxItems = 8192;       // (document, 128-row q-tile) work items
-constexpr size_t kNoAllocStatusBytes = 256;  // StatusWords, padded to the array's alignment
-constexpr int kNoAllocMaxDevices = 64;
+constexpr int kNoAllocMaxItems = DIT_ATTENTION_NOALLOC_MAX_TILES;  // (document, 128-row q-tile) work items
+constexpr size_t kNoAllocStatusBytes = 256;                        // StatusWords, padded to the array's alignment
+constexpr int kNoAllocCacheSlots = 64;
+static_assert(sizeof(StatusWords) <= kNoAllocStatusBytes, "status words must fit their slot of the array");
+static_assert(kNoAllocStatusBytes % alignof(int2) == 0, "the tile list must stay aligned");
 
 static __device__ __align__(256) unsigned char g_attention_scratch[kNoAllocStatusBytes + kNoAllocMaxItems * 8];
 
-std::mutex g_noalloc_mutex;
-void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+// The array's device address is a property of the CUDA context that loaded the library's module:
+// a cudaDeviceReset (which ends the primary context) or a caller-made context gives another one.
+// Addresses are therefore cached per context, keyed by the driver's unique context id, which is never
+// reused within a process.  Without that id (an older driver) the address is looked up on every call.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
 
-// Device address of g_attention_scratch on the current device.  The host-side symbol is only a
-// stand-in for the array, so its device address is looked up once per device (the first call on
-// that device) and cached.
+struct NoAllocSlot {
+  unsigned long long ctx_id;
+  void* ptr;
+};
+
+std::mutex g_noalloc_mutex;
+NoAllocSlot g_noalloc_cache[kNoAllocCacheSlots] = {};
+int g_noalloc_next = 0;
+
+template <typename F>
+F driver_fn(const char* name) {
+  cudaDriverEntryPointQueryResult q;
+  void* p = nullptr;
+  if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    return reinterpret_cast<F>(p);
+  return nullptr;
+}
+
+// Unique id of the calling thread's current context, or 0 when there is none or the driver cannot
+// say.
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+  static CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+  if (!get_current || !get_id) return 0;
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&c) != CUDA_SUCCESS || !c) return 0;
+  if (get_id(c, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of g_attention_scratch in the current context.  The host-side symbol is only a
+// stand-in for the array, so its device address is looked up (cudaGetSymbolAddress, with the
+// context current) the first time a context uses it and cached for that context.
 cudaError_t noalloc_scratch(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kNoAllocMaxDevices) return cudaErrorInvalidDevice;
+  unsigned long long id = current_context_id();
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  if (!g_noalloc_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress((void**)&p, g_attention_scratch);
-    if (e != cudaSuccess) return e;
-    g_noalloc_ptr[dev] = p;
+  if (id)
+    for (const NoAllocSlot& sl : g_noalloc_cache)
+      if (sl.ctx_id == id) {
+        *out = sl.ptr;
+        return cudaSuccess;
+      }
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress((void**)&p, g_attention_scratch);
+  if (e != cudaSuccess) return e;
+  if (!id) id = current_context_id();  // the lookup above may have made the primary context current
+  if (id) {
+    g_noalloc_cache[g_noalloc_next] = NoAllocSlot{id, p};
+    g_noalloc_next = (g_noalloc_next + 1) % kNoAllocCacheSlots;
   }
-  *out = g_noalloc_ptr[dev];
+  *out = p;
   return cudaSuccess;
 }
 
@@ -1541,4 +1584,21 @@ extern "C" dit_status dit_op_attention_noalloc(const void* q, const void* k, con
   aa.status = &sw->bits;
   e = attention_launch(q, k, vt, o, aa, s);
   return e == cudaSuccess ? DIT_OK : cuda_err(nullptr, e, "attention");
+}
+
+extern "C" dit_status dit_op_attention_noalloc_status(int* layout_code, void* stream) {
+  void* scratch = nullptr;
+  cudaError_t e = noalloc_scratch(&scratch);
+  if (e != cudaSuccess) return cuda_err(nullptr, e, "cudaGetSymbolAddress(attention scratch)");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  StatusWords sw;
+  e = cudaMemcpyAsync(&sw, scratch, sizeof(sw), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_err(nullptr, e, "reading the attention scratch's status words");
+  if (layout_code) *layout_code = sw.layout_code;
+  if (sw.bits & kDevTimeout) return set_err(nullptr, DIT_ERR_DEVICE_TIMEOUT, "attention: a bounded wait ran out");
+  if (sw.bits & kDevLayout)
+    return set_err(nullptr, DIT_ERR_LAYOUT, "attention: cu_seqlens rejected (layout code %d)", sw.layout_code);
+  if (sw.bits & kDevCapacity) return set_err(nullptr, DIT_ERR_CAPACITY, "attention: tile list overflow");
+  return DIT_OK;
 }

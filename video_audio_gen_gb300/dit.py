@@ -31,7 +31,7 @@ EXPORTS = ["dit_create", "dit_destroy", "dit_last_error", "dit_workspace_bytes",
            "dit_op_rope_cache", "dit_op_adaln", "dit_op_gemm", "dit_op_gemm_qkv_rope", "dit_op_gemm_gated_residual",
            "dit_op_gemm_swiglu", "dit_nvfp4_packed_bytes", "dit_op_pack_nvfp4", "dit_op_gemm_nvfp4",
            "dit_gemm_f32_workspace_bytes", "dit_op_gemm_f32", "dit_op_pack_ffn_in", "dit_attention_workspace_bytes", "dit_op_attention",
-           "dit_op_attention_noalloc", "dit_selftest_wait_timeout"]
+           "dit_op_attention_noalloc", "dit_op_attention_noalloc_status", "dit_selftest_wait_timeout"]
 
 
 class DitLatentIO(ctypes.Structure):
@@ -138,6 +138,7 @@ def lib():
             "dit_op_gemm_f32": (i32, [vp, vp, vp, i32, i32, i32, vp, vp, vp]),
             "dit_op_attention": (i32, [vp, vp, vp, i32, vp, i32, i32, i32, i32, vp, vp, vp]),
             "dit_op_attention_noalloc": (i32, [vp, vp, vp, i32, vp, i32, i32, i32, i32, vp, vp]),
+            "dit_op_attention_noalloc_status": (i32, [vp, vp]),
             "dit_selftest_wait_timeout": (i32, [ctypes.c_uint64, vp, vp]),
         }
         for name, (res, args) in sig.items():
@@ -454,3 +455,11 @@ def attention_noalloc(q, k, vt, n_pad, cu_seqlens, n_heads, head_dim, o, stream=
     _check(lib().dit_op_attention_noalloc(_ptr(q), _ptr(k), _ptr(vt), n_pad, _ptr(cu_seqlens),
                                           cu_seqlens.numel() - 1, n_tokens, n_heads, head_dim, _ptr(o),
                                           _stream(stream)))
+
+
+def attention_noalloc_status(stream=None) -> tuple[int, int]:
+    """dit_op_attention_noalloc_status: (status, layout code) of the last no-allocation attention call
+    in this context; synchronises the stream."""
+    code = ctypes.c_int(0)
+    st = int(lib().dit_op_attention_noalloc_status(ctypes.byref(code), _stream(stream)))
+    return st, int(code.value)
