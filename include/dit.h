@@ -47,11 +47,14 @@ typedef enum {
   DIT_ERR_CAPACITY = 6,       /* n_tokens > max_tokens, n_docs > max_docs, workspace too small */
   DIT_ERR_CUDA = 7,           /* a CUDA runtime call failed; dit_last_error has its message */
   DIT_ERR_DEVICE_TIMEOUT = 8, /* a kernel's bounded wait ran out; the kernel exited cleanly */
-  DIT_ERR_UNSUPPORTED = 9     /* shape outside what the kernels tile (see dit_create) */
+  DIT_ERR_UNSUPPORTED = 9,    /* shape outside what the kernels tile (see dit_create) */
+  DIT_ERR_RANGE = 10          /* a weight or activation beyond the f16 operands' range (65504); see act_bf16 */
 } dit_status;
 
 enum { DIT_RMSNORM = 0, DIT_LAYERNORM = 1 };
 enum { DIT_BF16 = 0, DIT_FP32 = 1 };
+/* 16-bit operand type of the op-level tensor-core calls (A, B, and the 16-bit outputs they write). */
+enum { DIT_ELEM_BF16 = 0, DIT_ELEM_F16 = 1 };
 
 /* Model configuration.  [H3] "The device-resident forward (W2b)" for the modality-indexed AdaLN
  * DiT (adaln = 1, RMSNorm); [M3] "What moved" for the music DiT (adaln = 0, LayerNorm, partial
@@ -81,6 +84,16 @@ typedef struct {
   int qkv_interleaved; /* 1: w_qkv / b_qkv rows per head [q_h | k_h | v_h] (the ViT's
                           qkv.view(S, H, 3 Dh).chunk(3)); repacked at bind.  0: [q_all | k_all | v_all] */
   int final_norm;      /* without AdaLN, the final norm: 0 the blocks' norm, 1 RMSNorm, 2 LayerNorm */
+  /* Operand precision of a DIT_BF16 model.  The weights are bf16 values; the tensor cores take both
+   * operands in one 16-bit type.  act_bf16 = 0 (the default): f16 operands.  Each weight is copied to
+   * f16 at bind (exact for magnitudes 2^-17 .. 65504; a larger one makes bind return DIT_ERR_RANGE)
+   * and the norm outputs, q, k, v, the attention probabilities and output, and the FFN hidden state
+   * are rounded to f16: 2^-11 relative instead of bf16's 2^-8, at the same tensor-core rate.  With
+   * bf16 rounding the block outputs of the full-width models (d = 3072, F = 8192 and up) miss the
+   * bf16 stream's 3e-3 x RMS tolerance; with f16 they meet it.  A norm output or FFN hidden value
+   * beyond 65504 sets the status word to DIT_ERR_RANGE.  act_bf16 = 1: bf16 operands throughout
+   * (bf16's range, coarser rounding). */
+  int act_bf16;
 } dit_config;
 
 /* One block's weights (device pointers; matrices and biases in cfg.dtype, biases may be NULL = zero;
@@ -349,7 +362,7 @@ DIT_API dit_status dit_get_kernel_times(dit_handle* h, double* ms_out, int64_t* 
  * N = RMSNorm x / sqrt(mean(x^2) + eps) (norm = DIT_RMSNORM) or LayerNorm (DIT_LAYERNORM), either
  * followed by the per-channel gain ln_g and shift ln_b when given (NULL = none).  x fp32 [n, d]; shift/scale fp32 rows of d values, row m at
  * shift + m * mod_stride (NULL shift and scale = no modulation); tags uint8 [n] (may be NULL
- * when shift is NULL).  Output bf16 bits [n, d] (out_kind 0) or fp32 [n, d] (out_kind 1).
+ * when shift is NULL).  Output bf16 [n, d] (out_kind 0), fp32 [n, d] (1) or f16 [n, d] (2).
  * Requires d % 128 == 0 and d <= 8192. */
 DIT_API dit_status dit_op_norm_modulate(const float* x, int n, int d, int norm, float eps, const float* ln_g,
                                 const float* ln_b, const uint8_t* tags, const float* shift, const float* scale,
@@ -367,29 +380,30 @@ DIT_API dit_status dit_op_rope_cache(const double* pos, int n, int n_axes, const
  * mod fp32 [rows].  t_dim % 256 == 0 or t_dim in {64, 128}. */
 DIT_API dit_status dit_op_adaln(const void* w, const float* b, int rows, int t_dim, float t, float* mod, void* stream);
 
-/* GEMM D = A B^T on the tcgen05 tensor cores, bf16 operands, fp32 accumulation in TMEM.
- * A bf16 [M, K] row-major, B bf16 [N, K] row-major (the weight), bias fp32 [N] or NULL.
+/* GEMM D = A B^T on the tcgen05 tensor cores, 16-bit operands, fp32 accumulation in TMEM.
+ * A [M, K] row-major, B [N, K] row-major (the weight), both of the 16-bit type `elem`
+ * (DIT_ELEM_BF16 or DIT_ELEM_F16), bias fp32 [N] or NULL.
  * M >= 1 any; N % 256 == 0; K % 64 == 0; A, B 16-byte aligned.  Epilogues:
- *   dit_op_gemm            out = A B^T + bias, stored bf16 bits (out_kind 0) or fp32 (1), [M, N]
+ *   dit_op_gemm            out = A B^T + bias, stored bf16 (out_kind 0), fp32 (1) or f16 (2), [M, N]
  *   dit_op_gemm_qkv_rope   N = 3d: q, k get bias + NeoX rotate_half with cos/sin [M, R/2] on the
- *                          first R dims of each Dh-wide head and are stored bf16 [M, d]; v is
- *                          stored TRANSPOSED, vt bf16 [d, n_pad] (vt[c * n_pad + row]),
+ *                          first R dims of each Dh-wide head and are stored as `elem` [M, d]; v is
+ *                          stored TRANSPOSED, vt [d, n_pad] (vt[c * n_pad + row]) of type `elem`,
  *                          n_pad >= M, n_pad % 8 == 0; the padding columns [M, n_pad) are
  *                          written as zeros.
  *   dit_op_gemm_gated_residual  x[M, N] (fp32, in place) += gate[tag[r]] * (A B^T + bias);
  *                          gate rows at gate + m * gate_stride (NULL gate = plain residual add).
  *   dit_op_gemm_swiglu     B, bias in the interleaved layout of dit_op_pack_ffn_in (2F rows);
- *                          h bf16 [M, F] = (u + b_u) * silu(g + b_g). */
+ *                          h [M, F] of type `elem` = (u + b_u) * silu(g + b_g). */
 DIT_API dit_status dit_op_gemm(const void* a, const void* b, const float* bias, int M, int N, int K, void* out, int out_kind,
-                       void* stream);
+                       int elem, void* stream);
 DIT_API dit_status dit_op_gemm_qkv_rope(const void* a, const void* b, const float* bias, int M, int d, int K, int n_heads,
                                 int head_dim, int rotary_dim, const float* cos_cache, const float* sin_cache,
-                                void* q, void* k, void* vt, int n_pad, void* stream);
+                                void* q, void* k, void* vt, int n_pad, int elem, void* stream);
 DIT_API dit_status dit_op_gemm_gated_residual(const void* a, const void* b, const float* bias, int M, int N, int K,
                                       float* x, const float* gate, int64_t gate_stride, const uint8_t* tags,
-                                      void* stream);
+                                      int elem, void* stream);
 DIT_API dit_status dit_op_gemm_swiglu(const void* a, const void* b_packed, const float* bias_packed, int M, int F, int K,
-                              void* h, void* stream);
+                              void* h, int elem, void* stream);
 
 /* GEMM with NVFP4 weights.  [H3] "What this push adds": the NVFP4 checkpoint's projections carry
  * a U8 weight with two FP4 (E2M1) codes per byte ([N][K/2]), an F8_E4M3 scale per group of 16
@@ -430,19 +444,21 @@ DIT_API dit_status dit_op_pack_ffn_in(const void* w_in, const float* b_in, int F
 /* Varlen non-causal flash attention on the tcgen05 tensor cores ([H3] "Correctness gates":
  * DFlashBlockAttention(causal=false) over the packed sequence; [M3] "What moved": non-causal,
  * no bias).  Per document [cu[j], cu[j+1]) and head h:  o_i = softmax_j(q_i . k_j / sqrt(Dh)) v_j.
- *   q, k  bf16 [n_tokens, H * Dh];  vt bf16 [H * Dh, n_pad] (n_pad % 8 == 0, n_pad >= n_tokens;
- *         its padding columns must hold finite values, e.g. the zeros dit_op_gemm_qkv_rope writes)
- * Key/value tiles are 128 tokens wide and 128-aligned, so a document's boundary tiles also load
- * its neighbours' keys and values; their softmax weights are exactly 0, which keeps every document's
- * output bit-independent of the others' (finite) values.  A non-finite value in one document's V
- * can still reach a neighbour sharing a boundary tile (0 * NaN = NaN).
- *   o     bf16 [n_tokens, H * Dh]
+ * Every 16-bit array is of the type `elem` (DIT_ELEM_BF16 or DIT_ELEM_F16); the probabilities
+ * take the same type as the PV operand.
+ *   q, k  [n_tokens, H * Dh];  vt [H * Dh, n_pad] (n_pad % 8 == 0, n_pad >= n_tokens; its padding
+ *         columns are never read into a result)
+ * Key/value tiles are 128 tokens wide and 128-aligned, so a document's boundary tiles also load its
+ * neighbours' keys and values: their scores are replaced by -inf and their V^T columns by zeros
+ * before they are used, so every document's output is bit-independent of the other documents'
+ * values, non-finite ones included.
+ *   o     [n_tokens, H * Dh]
  * head_dim is 64 or 128.  The (document, 128-row q-tile) work list is built on the device from
  * cu_seqlens into `workspace` (dit_attention_workspace_bytes(n_docs, n_tokens) bytes). */
 DIT_API size_t dit_attention_workspace_bytes(int n_docs, int n_tokens);
 DIT_API dit_status dit_op_attention(const void* q, const void* k, const void* vt, int n_pad, const int32_t* cu_seqlens,
                             int n_docs, int n_tokens, int n_heads, int head_dim, void* o, void* workspace,
-                            void* stream);
+                            int elem, void* stream);
 
 /* The same attention with no caller-provided scratch, for callers that cannot allocate device
  * memory: e.g. a plugin running inside another framework's executor that is handed no allocator, or
@@ -466,7 +482,7 @@ DIT_API dit_status dit_op_attention(const void* q, const void* k, const void* vt
 #define DIT_ATTENTION_NOALLOC_MAX_TILES 8192
 DIT_API dit_status dit_op_attention_noalloc(const void* q, const void* k, const void* vt, int n_pad,
                                             const int32_t* cu_seqlens, int n_docs, int n_tokens, int n_heads,
-                                            int head_dim, void* o, void* stream);
+                                            int head_dim, void* o, int elem, void* stream);
 
 /* Outcome of the last dit_op_attention_noalloc call in the current context: synchronises `stream`,
  * reads the fixed array's status words (no allocation) and returns DIT_OK, DIT_ERR_LAYOUT

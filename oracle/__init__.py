@@ -64,6 +64,8 @@ def lib():
             _lib.orc_forward_mod.restype = ctypes.c_int
             _lib.orc_forward_latent.restype = ctypes.c_int
             _lib.orc_time_shift.restype = ctypes.c_double
+            _lib.orc_span_sum_sequential.restype = ctypes.c_double
+            _lib.orc_span_sum_pairwise.restype = ctypes.c_double
             _lib.orc_e2m1_decode.restype = ctypes.c_double
             _lib.orc_e4m3_decode.restype = ctypes.c_double
             _lib.orc_check_layout.restype = ctypes.c_int
@@ -148,6 +150,18 @@ def check_layout(cu, doc_ids, tags, n_tokens: int, n_mod: int) -> int:
     tags = np.ascontiguousarray(tags, dtype=np.uint8)
     return int(lib().orc_check_layout(_p(cu), len(cu) - 1, _p(doc_ids), _p(tags),
                                       int(n_tokens), int(n_mod)))
+
+
+def span_sum_sequential(x) -> float:
+    """Left-to-right sum of the spans, each add rounded ([H3] "Correctness gates")."""
+    x = _dbl(np.asarray(x).reshape(-1))
+    return float(lib().orc_span_sum_sequential(_d(x), ctypes.c_int(x.size)))
+
+
+def span_sum_pairwise(x) -> float:
+    """The spans summed in numpy's pairwise order ([H3] "Correctness gates")."""
+    x = _dbl(np.asarray(x).reshape(-1))
+    return float(lib().orc_span_sum_pairwise(_d(x), ctypes.c_int(x.size)))
 
 
 def count_q_tiles(cu, tile: int = 128) -> int:

@@ -104,6 +104,46 @@ void orc_linspace(double start, double stop, int n, double* out) {
 }
 
 // ---------------------------------------------------------------------------------------------
+// Span sums of the packed layouts.  [H3] "Correctness gates": the fp64 grid of the packed layouts
+// is gated bit-exact, and upstream keeps two span sums apart on purpose, a numpy-pairwise one and a
+// Python-sequential one, because the two differ in the last ulp from n = 16.  Both are written out
+// here in their own arithmetic order (the pages give the order, not the layout that uses them):
+//   sequential: s = 0; s = s + x[i] for i = 0, 1, ..., n - 1 (every add rounded in turn)
+//   pairwise:   numpy's summation of a contiguous float64 array: fewer than 8 terms are summed left
+//               to right from 0; up to 128 terms go into 8 running partial sums (term i into sum
+//               i mod 8, over the largest multiple of 8), which are combined as a balanced tree
+//               ((p0 + p1) + (p2 + p3)) + ((p4 + p5) + (p6 + p7)) before the leftover terms are
+//               added left to right; above 128 terms the array is cut after m terms, m = n / 2
+//               rounded down to a multiple of 8, and the two parts' sums are added.
+// ---------------------------------------------------------------------------------------------
+double orc_span_sum_sequential(const double* x, int n) {
+  double s = 0.0;
+  for (int i = 0; i < n; ++i) s = s + x[i];
+  return s;
+}
+
+double orc_span_sum_pairwise(const double* x, int n) {
+  if (n < 8) {
+    double s = 0.0;
+    for (int i = 0; i < n; ++i) s = s + x[i];
+    return s;
+  }
+  if (n <= 128) {
+    double p[8];
+    for (int j = 0; j < 8; ++j) p[j] = x[j];
+    const int full = n - n % 8;
+    for (int i = 8; i < full; i += 8)
+      for (int j = 0; j < 8; ++j) p[j] = p[j] + x[i + j];
+    double s = ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
+    for (int i = full; i < n; ++i) s = s + x[i];
+    return s;
+  }
+  int m = n / 2;
+  m -= m % 8;
+  return orc_span_sum_pairwise(x, m) + orc_span_sum_pairwise(x + m, n - m);
+}
+
+// ---------------------------------------------------------------------------------------------
 // Timestep embedding.  READING (pages silent on the formula): the usual DiT sinusoid,
 // half = t_dim/2, f_k = exp(-ln(10000) * k / half), e = [cos(1000 t f_k) | sin(1000 t f_k)].
 // The ungated SiLU of [H3] "The device-resident forward (W2b)" is applied by the caller.

@@ -85,8 +85,9 @@ def test_op_argument_checks_need_no_device():
     L = dit.lib()
     assert L.dit_euler_step(None, None, 5, 1.0, 0.5, None) == dit.DIT_ERR_INVALID_ARG
     assert L.dit_euler_step(None, None, 0, 0.0, 0.5, None) == dit.DIT_ERR_INVALID_ARG  # sigma must be > 0
-    assert L.dit_op_gemm(None, None, None, 10, 256, 64, None, 0, None) == dit.DIT_ERR_INVALID_ARG
+    assert L.dit_op_gemm(None, None, None, 10, 256, 64, None, 0, 0, None) == dit.DIT_ERR_INVALID_ARG
     p = ctypes.c_void_p(256)
-    assert L.dit_op_gemm(p, p, None, 10, 200, 64, p, 0, None) == dit.DIT_ERR_UNSUPPORTED
-    assert L.dit_op_attention(p, p, p, 16, p, 1, 10, 2, 96, p, p, None) == dit.DIT_ERR_UNSUPPORTED
+    assert L.dit_op_gemm(p, p, None, 10, 200, 64, p, 0, 0, None) == dit.DIT_ERR_UNSUPPORTED
+    assert L.dit_op_attention(p, p, p, 16, p, 1, 10, 2, 96, p, p, 0, None) == dit.DIT_ERR_UNSUPPORTED
+    assert L.dit_op_attention(p, p, p, 16, p, 1, 10, 2, 128, p, p, 2, None) == dit.DIT_ERR_INVALID_ARG
     assert dit.attention_workspace_bytes(2, 17408) > 0 and dit.attention_workspace_bytes(0, 5) == 0

@@ -139,6 +139,53 @@ def test_segmentation_bit_identity():
     assert not np.array_equal(r1["out"][~other], r2["out"][~other])
 
 
+def test_nonfinite_document_does_not_reach_the_others():
+    """NaN and Inf in one document's input tokens: every row of the other documents, including the
+    neighbours that share its 128-token attention tiles, is finite and bit-identical to the clean run
+    (the forward has no other cross-document step)."""
+    gu = _gu()
+    w = synth.WORKLOADS["many_docs"]
+    lay = synth.build_layout(w["docs"])
+    W = synth.make_weights(w)
+    x = synth.make_tokens(w, lay)
+    r1 = gu.run_forward(w, layout=lay, weights=W, x=x)
+    cu = lay["cu_seqlens"]
+    j = int(np.argmax([(cu[i] % 128 != 0) and (cu[i + 1] % 128 != 0) and cu[i + 1] - cu[i] > 100
+                       for i in range(lay["n_docs"] - 1)]))
+    a, b = int(cu[j]), int(cu[j + 1])
+    assert a % 128 and b % 128 and j + 1 < lay["n_docs"]
+    x2 = x.copy()
+    x2[a:b:5, 3] = np.nan
+    x2[a + 1:b:7, 11] = np.inf
+    x2[b - 1, :] = -np.inf
+    r2 = gu.run_forward(w, layout=lay, weights=W, x=x2, handle=r1["handle"])
+    other = np.ones(lay["n_tokens"], dtype=bool)
+    other[a:b] = False
+    assert np.isfinite(r2["out"][other]).all()
+    assert np.array_equal(r1["out"][other].view(np.uint64), r2["out"][other].view(np.uint64))
+    assert not np.isfinite(r2["out"][a:b]).all()
+
+
+def test_bf16_operand_forward_matches_oracle():
+    """The act_bf16 configuration (bf16 operands throughout instead of f16) on the ragged case: the
+    same gates at this width (its rounding only misses the tolerance on the full-width models)."""
+    gu = _gu()
+    w = synth.WORKLOADS["ragged"]
+    wb = dict(w, model=dict(w["model"], act_bf16=True))
+    run = gu.run_forward(wb, dumps=True)
+    assert run["status"] == 0
+    oracle.set_threads(8)
+    ref, dumps = oracle.forward(w["model"], run["weights"], run["x"], run["layout"], run["t"], dumps=True)
+    oracle.set_threads(1)
+    check_against_oracle(wb, run, ref, dumps)
+    # and the f16 operands are the more accurate of the two on the same inputs
+    r16 = gu.run_forward(w, dumps=True, layout=run["layout"], weights=run["weights"], x=run["x"], t=run["t"])
+    e16 = max(np.abs(r16["dumps"][l] - dumps[l]).max() for l in range(len(dumps)))
+    e_bf = max(np.abs(run["dumps"][l] - dumps[l]).max() for l in range(len(dumps)))
+    print(f"ragged: max block error f16 operands {e16:.3e}, bf16 operands {e_bf:.3e}")
+    assert e16 < e_bf
+
+
 def test_forward_host_equals_device_forward():
     gu = _gu()
     w = synth.WORKLOADS["tiny"]

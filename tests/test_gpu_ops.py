@@ -11,6 +11,9 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 BF16_REL = 2.0 ** -8   # one bf16 rounding (2^-9) with a factor 2 of headroom
+F16_REL = 2.0 ** -10   # one f16 rounding (2^-11) with a factor 2 of headroom
+REL = {"bf16": BF16_REL, "f16": F16_REL}
+ELEMS = ["bf16", "f16"]
 
 
 def _dit():
@@ -25,6 +28,20 @@ def _gu():
 
 def bf16_to_f64(t):
     return t.float().double().cpu().numpy()
+
+
+def dev16(vals, bits, elem):
+    """(device tensor, the float32 values it holds): the seeded bf16 values as a bf16 tensor (from
+    their bits), or rounded to f16 (exact except below 2^-17, where f16 is subnormal)."""
+    from tests import gpu_util
+    if elem == "bf16":
+        return gpu_util.dev_bf16(bits), np.asarray(vals, dtype=np.float32)
+    t = torch.from_numpy(np.ascontiguousarray(vals, dtype=np.float32)).cuda().half()
+    return t, t.float().cpu().numpy()
+
+
+def tdt(elem):
+    return torch.bfloat16 if elem == "bf16" else torch.float16
 
 
 def fp32_sum_bound(a, b):
@@ -56,6 +73,10 @@ def test_rms_norm_modulate_matches_oracle(n, d):
                       shift=gu.dev_f32(shift), scale=gu.dev_f32(scale), mod_stride=d)
     gotf = yf.double().cpu().numpy()
     assert np.abs(gotf - ref).max() <= 1e-5 * np.abs(ref).max()
+    yh = torch.empty((n, d), dtype=torch.float16, device="cuda")
+    dit.norm_modulate(xd, dit.DIT_RMSNORM, 1e-6, yh, 2, tags=torch.from_numpy(tags).cuda(),
+                      shift=gu.dev_f32(shift), scale=gu.dev_f32(scale), mod_stride=d)
+    assert np.all(np.abs(bf16_to_f64(yh) - ref) <= F16_REL * np.abs(ref) + 1e-5)
 
 
 def test_norm_without_modulation_is_bare_rms():
@@ -131,70 +152,76 @@ def _ab(M, N, K, seed, std_b=0.05):
     return a, abits, b, bbits, bias
 
 
+@pytest.mark.parametrize("elem", ELEMS)
 @pytest.mark.parametrize("M,N,K", [(1, 256, 64), (333, 512, 512), (128, 768, 256), (1000, 1024, 1536)])
-def test_gemm_store_matches_oracle(M, N, K):
+def test_gemm_store_matches_oracle(M, N, K, elem):
     dit, gu = _dit(), _gu()
     a, abits, b, bbits, bias = _ab(M, N, K, 40 + M)
+    (A, a), (B, b) = dev16(a, abits, elem), dev16(b, bbits, elem)
     ref = oracle.linear(a, b, bias)
     bound = fp32_sum_bound(a.astype(np.float64), b.astype(np.float64))
     out = torch.empty((M, N), dtype=torch.float32, device="cuda")
-    dit.gemm(gu.dev_bf16(abits), gu.dev_bf16(bbits), gu.dev_f32(bias), out, 1)
+    dit.gemm(A, B, gu.dev_f32(bias), out, 1)
     got = out.double().cpu().numpy()
     assert np.all(np.abs(got - ref) <= bound + 1e-6)
-    outb = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-    dit.gemm(gu.dev_bf16(abits), gu.dev_bf16(bbits), None, outb, 0)
+    outb = torch.empty((M, N), dtype=tdt(elem), device="cuda")
+    dit.gemm(A, B, None, outb, 0 if elem == "bf16" else 2)
     refb = oracle.linear(a, b, None)
-    assert np.all(np.abs(bf16_to_f64(outb) - refb) <= BF16_REL * np.abs(refb) + bound + 1e-6)
+    assert np.all(np.abs(bf16_to_f64(outb) - refb) <= REL[elem] * np.abs(refb) + bound + 1e-6)
 
 
+@pytest.mark.parametrize("elem", ELEMS)
 @pytest.mark.parametrize("name", ["tiny", "ragged"])
-def test_gemm_qkv_rope_matches_oracle(name):
+def test_gemm_qkv_rope_matches_oracle(name, elem):
     dit, gu = _dit(), _gu()
     w = synth.WORKLOADS[name]
     m = w["model"]
     lay = synth.build_layout(w["docs"])
     M, d, H, Dh, R = lay["n_tokens"], m["hidden"], m["n_heads"], m["head_dim"], m["rotary_dim"]
     a, abits, b, bbits, bias = _ab(M, 3 * d, d, 50)
+    (A, a), (B, b) = dev16(a, abits, elem), dev16(b, bbits, elem)
     cs, sn = oracle.rope_cos_sin(m, lay["pos"])
     qkv = oracle.linear(a, b, bias)
     qr = oracle.rope_apply(qkv[:, :d], H, Dh, R, cs, sn)
     kr = oracle.rope_apply(qkv[:, d:2 * d], H, Dh, R, cs, sn)
     vr = qkv[:, 2 * d:]
     n_pad = (M + 7) // 8 * 8
-    q = torch.empty((M, d), dtype=torch.bfloat16, device="cuda")
+    q = torch.empty((M, d), dtype=tdt(elem), device="cuda")
     k = torch.empty_like(q)
-    vt = torch.full((d, n_pad), float("nan"), dtype=torch.bfloat16, device="cuda")  # garbage on entry
+    vt = torch.full((d, n_pad), float("nan"), dtype=tdt(elem), device="cuda")  # garbage on entry
     gcs = torch.empty((M, R // 2), dtype=torch.float32, device="cuda")
     gsn = torch.empty_like(gcs)
     dit.rope_cache(gu.dev_layout(lay)["pos"], m["rope_axes"], m["rope_dims"], m["rope_base"], gcs, gsn)
-    dit.gemm_qkv_rope(gu.dev_bf16(abits), gu.dev_bf16(bbits), gu.dev_f32(bias), H, Dh, R, gcs, gsn, q, k, vt, n_pad)
+    dit.gemm_qkv_rope(A, B, gu.dev_f32(bias), H, Dh, R, gcs, gsn, q, k, vt, n_pad)
     bound = fp32_sum_bound(a.astype(np.float64), b.astype(np.float64))
-    # rotation mixes two accumulators: bound both, plus fp32 cos/sin (2^-24) and the bf16 store
+    # rotation mixes two accumulators: bound both, plus fp32 cos/sin (2^-24) and the 16-bit store
     bq = bound[:, :d] + np.roll(bound[:, :d], 1, axis=1)  # generous pair bound
     for got, ref, bb in ((bf16_to_f64(q), qr, bq), (bf16_to_f64(k), kr, bq)):
         err = np.abs(got - ref)
-        assert np.all(err <= BF16_REL * np.abs(ref) + 2 * bb.max() + 1e-5), err.max()
+        assert np.all(err <= REL[elem] * np.abs(ref) + 2 * bb.max() + 1e-5), err.max()
     gv = bf16_to_f64(vt)[:, :M].T
-    assert np.all(np.abs(gv - vr) <= BF16_REL * np.abs(vr) + bound[:, 2 * d:] + 1e-6)
+    assert np.all(np.abs(gv - vr) <= REL[elem] * np.abs(vr) + bound[:, 2 * d:] + 1e-6)
     assert (bf16_to_f64(vt)[:, M:] == 0).all()  # padding columns are written as zeros
 
 
-def test_gemm_gated_residual_matches_oracle():
+@pytest.mark.parametrize("elem", ELEMS)
+def test_gemm_gated_residual_matches_oracle(elem):
     dit, gu = _dit(), _gu()
     M, N, K = 555, 512, 1024
     a, abits, b, bbits, bias = _ab(M, N, K, 60)
+    (A, a), (B, b) = dev16(a, abits, elem), dev16(b, bbits, elem)
     x = synth.normal(60, "x", (M, N), 1.0)
     gate = synth.normal(60, "gate", (2, N), 0.3)
     tags = (synth.uniform(60, "tags", M) < 0.5).astype(np.uint8)
     ref = x.astype(np.float64) + gate[tags].astype(np.float64) * oracle.linear(a, b, bias)
     xd = gu.dev_f32(x)
-    dit.gemm_gated_residual(gu.dev_bf16(abits), gu.dev_bf16(bbits), gu.dev_f32(bias), xd, gate=gu.dev_f32(gate),
-                            gate_stride=N, tags=torch.from_numpy(tags).cuda())
+    dit.gemm_gated_residual(A, B, gu.dev_f32(bias), xd, gate=gu.dev_f32(gate), gate_stride=N,
+                            tags=torch.from_numpy(tags).cuda())
     bound = fp32_sum_bound(a.astype(np.float64), b.astype(np.float64)) * np.abs(gate[tags]) + 2 ** -23 * 4
     assert np.all(np.abs(xd.double().cpu().numpy() - ref) <= bound + 1e-6)
     # gate = NULL: plain residual add
     xd2 = gu.dev_f32(x)
-    dit.gemm_gated_residual(gu.dev_bf16(abits), gu.dev_bf16(bbits), None, xd2)
+    dit.gemm_gated_residual(A, B, None, xd2)
     ref2 = x.astype(np.float64) + oracle.linear(a, b, None)
     assert np.abs(xd2.double().cpu().numpy() - ref2).max() <= 1e-4
 
@@ -245,25 +272,27 @@ def test_gemm_f32_rejects_bad_shapes():
         dit.gemm_f32(x, w, None, y, ws)  # K = 48 is not a multiple of 32
 
 
-def test_gemm_swiglu_matches_oracle():
+@pytest.mark.parametrize("elem", ELEMS)
+def test_gemm_swiglu_matches_oracle(elem):
     dit, gu = _dit(), _gu()
     M, F, d = 300, 768, 512
     a, abits, _, _, _ = _ab(M, 256, d, 70)
     win, wbits = synth.normal(70, "win", (2 * F, d), 0.05, bf16=True)
+    (A, a), (Win, win) = dev16(a, abits, elem), dev16(win, wbits, elem)
     bin_ = synth.normal(70, "bin", (2 * F,), 0.1)
     ref = oracle.swiglu(oracle.linear(a, win, bin_))
-    wp = torch.empty((2 * F, d), dtype=torch.bfloat16, device="cuda")
+    wp = torch.empty((2 * F, d), dtype=tdt(elem), device="cuda")
     bp = torch.empty((2 * F,), dtype=torch.float32, device="cuda")
-    dit.pack_ffn_in(gu.dev_bf16(wbits), gu.dev_f32(bin_), wp, bp)
-    h = torch.empty((M, F), dtype=torch.bfloat16, device="cuda")
-    dit.gemm_swiglu(gu.dev_bf16(abits), wp, bp, h)
+    dit.pack_ffn_in(Win, gu.dev_f32(bin_), wp, bp)
+    h = torch.empty((M, F), dtype=tdt(elem), device="cuda")
+    dit.gemm_swiglu(A, wp, bp, h)
     got = bf16_to_f64(h)
     uv_bound = fp32_sum_bound(a.astype(np.float64), win.astype(np.float64))
     # |d(u silu g)| <= |silu g| du + |u| |silu'| dg with |silu'| <= 1.1
     uv = oracle.linear(a, win, bin_)
     u, g = uv[:, :F], uv[:, F:]
     prop = np.abs(g) * uv_bound[:, :F] + 1.1 * np.abs(u) * uv_bound[:, F:]
-    assert np.all(np.abs(got - ref) <= BF16_REL * np.abs(ref) + prop + 1e-5 * np.abs(u) + 1e-6)
+    assert np.all(np.abs(got - ref) <= REL[elem] * np.abs(ref) + prop + 1e-5 * np.abs(u) + 1e-6)
 
 
 # ------------------------------------------------------------------------------------------------
@@ -281,22 +310,27 @@ def _attn_inputs(lay, H, Dh, seed, same_keys=False):
     return q, qb, k, kb, v, vb
 
 
-def _run_attention(lay, H, Dh, qb, kb, vb):
+def _run_attention(lay, H, Dh, qb, kb, vb, elem="bf16"):
+    """qb, kb, vb: bf16 bits of the inputs; with elem "f16" the same values run as f16."""
     dit, gu = _dit(), _gu()
     n = lay["n_tokens"]
     n_pad = (n + 7) // 8 * 8
     vt = np.zeros((H * Dh, n_pad), dtype=np.uint16)
     vt[:, :n] = vb.T
-    o = torch.empty((n, H * Dh), dtype=torch.bfloat16, device="cuda")
+    def dev(bits):
+        t = gu.dev_bf16(bits)
+        return t if elem == "bf16" else t.half()  # bf16 values are exact in f16 at these magnitudes
+    o = torch.empty((n, H * Dh), dtype=tdt(elem), device="cuda")
     ws = torch.empty(dit.attention_workspace_bytes(lay["n_docs"], n), dtype=torch.uint8, device="cuda")
-    dit.attention(gu.dev_bf16(qb), gu.dev_bf16(kb), gu.dev_bf16(vt), n_pad, gu.dev_layout(lay)["cu"], H, Dh, o, ws)
+    dit.attention(dev(qb), dev(kb), dev(vt), n_pad, gu.dev_layout(lay)["cu"], H, Dh, o, ws)
     torch.cuda.synchronize()
     return bf16_to_f64(o)
 
 
-def attn_tol(ref, v):
-    """P is rounded to bf16 before P.V (relative 2^-9 per weight) and O is stored bf16."""
-    return BF16_REL * np.abs(ref) + 2.0 ** -8 * np.abs(v).max()
+def attn_tol(ref, v, elem="bf16"):
+    """P is rounded to the 16-bit type before P.V (relative 2^-9 or 2^-11 per weight) and O is stored
+    in it."""
+    return REL[elem] * np.abs(ref) + REL[elem] * np.abs(v).max()
 
 
 DOCSETS = {
@@ -307,15 +341,16 @@ DOCSETS = {
 }
 
 
+@pytest.mark.parametrize("elem", ELEMS)
 @pytest.mark.parametrize("docs", list(DOCSETS))
 @pytest.mark.parametrize("Dh", [64, 128])
-def test_attention_matches_oracle(docs, Dh):
+def test_attention_matches_oracle(docs, Dh, elem):
     lay = synth.build_layout(DOCSETS[docs])
     H = 2
     q, qb, k, kb, v, vb = _attn_inputs(lay, H, Dh, 80 + Dh)
     ref = oracle.attention(q, k, v, lay["cu_seqlens"], H, Dh)
-    got = _run_attention(lay, H, Dh, qb, kb, vb)
-    assert np.all(np.abs(got - ref) <= attn_tol(ref, v))
+    got = _run_attention(lay, H, Dh, qb, kb, vb, elem)
+    assert np.all(np.abs(got - ref) <= attn_tol(ref, v, elem))
 
 
 def test_attention_identical_keys_gives_mean_of_v():
@@ -347,6 +382,35 @@ def test_attention_one_token_doc_returns_v_and_docs_do_not_mix():
     mask[a:b] = False
     assert np.array_equal(got[mask], got2[mask])
     assert not np.array_equal(got[~mask], got2[~mask])
+
+
+@pytest.mark.parametrize("elem", ELEMS)
+@pytest.mark.parametrize("Dh", [64, 128])
+def test_attention_nonfinite_document_is_isolated(Dh, elem):
+    """NaN and +-Inf in one document's q, k and v: every other document's output rows stay
+    bit-identical to the clean run, including the neighbours that share its 128-token boundary
+    tiles (their keys are masked and their V^T columns zeroed before the P.V product)."""
+    lay = synth.build_layout(DOCSETS["edges"] + [dict(video=(1, 3, 70)), dict(video=(1, 1, 50))])
+    H = 2
+    q, qb, k, kb, v, vb = _attn_inputs(lay, H, Dh, 93)
+    clean = _run_attention(lay, H, Dh, qb, kb, vb, elem)
+    cu = lay["cu_seqlens"]
+    j = 6                                  # tokens [642, 852): both ends inside tiles shared with neighbours
+    a, b = int(cu[j]), int(cu[j + 1])
+    assert a % 128 and b % 128
+    NAN, PINF, NINF = np.uint16(0x7FC0), np.uint16(0x7F80), np.uint16(0xFF80)
+    qb2, kb2, vb2 = qb.copy(), kb.copy(), vb.copy()
+    qb2[a:b:3, 5] = NAN
+    kb2[a + 1:b:4, 7] = PINF
+    kb2[a + 2:b:5, 1] = NAN
+    vb2[a:b:2, 3] = NAN
+    vb2[a + 1:b:7, Dh + 9] = NINF
+    vb2[b - 1, :] = PINF
+    got = _run_attention(lay, H, Dh, qb2, kb2, vb2, elem)
+    mask = np.ones(lay["n_tokens"], dtype=bool)
+    mask[a:b] = False
+    assert np.isfinite(got[mask]).all()
+    assert np.array_equal(got[mask].view(np.uint64), clean[mask].view(np.uint64))
 
 
 @pytest.mark.slow

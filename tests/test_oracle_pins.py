@@ -63,6 +63,40 @@ def test_linspace_order_matters():
     assert miss > 0
 
 
+SPAN_SETS = {
+    "uniform": lambda n: synth.uniform(41, "spans", n, 0.0, 3.0),
+    "one third": lambda n: np.full(n, 1.0 / 3.0),
+    "steps of 1/17": lambda n: np.arange(n) / 17.0,
+    "normal x 1e3": lambda n: synth.normal(42, "spans", (n,), 1e3).astype(np.float64) / 7.0,
+}
+
+
+@pytest.mark.parametrize("name", list(SPAN_SETS))
+def test_span_sums_bit_exact_vs_numpy_and_python(name):
+    """The pairwise span sum equals numpy's sum of a float64 array bit for bit, and the sequential
+    one a Python left-to-right loop, from n = 0 through several recursion levels of the pairwise
+    split."""
+    for n in list(range(0, 300)) + [511, 512, 513, 1000, 1024, 1031, 4097]:
+        x = SPAN_SETS[name](n)
+        assert oracle.span_sum_pairwise(x) == float(np.sum(x)), n
+        seq = 0.0
+        for v in x:
+            seq = seq + float(v)
+        assert oracle.span_sum_sequential(x) == seq, n
+
+
+@pytest.mark.parametrize("span", [1.0 / 3.0, 2.0 / 3.0, 0.3])
+def test_span_sums_part_in_the_last_ulp_from_n_16(span):
+    """[H3] "Correctness gates": the numpy-pairwise and the Python-sequential span sums diverge in
+    the last ulp from n = 16.  For these spans they agree below 16 terms and part by one ulp at 16."""
+    for n in range(1, 16):
+        x = np.full(n, span)
+        assert oracle.span_sum_pairwise(x) == oracle.span_sum_sequential(x), n
+    x = np.full(16, span)
+    a, b = oracle.span_sum_pairwise(x), oracle.span_sum_sequential(x)
+    assert a != b and abs(a - b) == np.spacing(max(abs(a), abs(b)))
+
+
 def test_layout_sizes_and_grid():
     expect = {"tiny": [96, 160], "video_audio_bf16": [8704, 8704], "long_doc_bf16": [33792],
               "denoise_loop": [17408, 9216], "music_fp32": [86, 86]}

@@ -85,6 +85,6 @@ def test_attention_noalloc_rejects_sizes_beyond_its_scratch():
     o = torch.empty_like(q)
     cu = torch.arange(n + 1, dtype=torch.int32, device="cuda")
     st = dit.lib().dit_op_attention_noalloc(q.data_ptr(), k.data_ptr(), vt.data_ptr(), n_pad, cu.data_ptr(), n_docs,
-                                            n, 1, 128, o.data_ptr(), None)
+                                            n, 1, 128, o.data_ptr(), dit.DIT_ELEM_BF16, None)
     assert st == dit.DIT_ERR_CAPACITY
     assert b"fixed scratch" in dit.lib().dit_last_error(None)

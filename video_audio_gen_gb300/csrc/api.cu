@@ -150,6 +150,7 @@ dit_status validate_config(const dit_config* c) {
   if ((c->qk_norm != 0 && c->qk_norm != 1) || (c->qkv_interleaved != 0 && c->qkv_interleaved != 1))
     return set_err(nullptr, DIT_ERR_CONFIG, "qk_norm and qkv_interleaved must be 0 or 1");
   if (c->final_norm < 0 || c->final_norm > 2) return set_err(nullptr, DIT_ERR_CONFIG, "final_norm must be 0, 1 or 2");
+  if (c->act_bf16 != 0 && c->act_bf16 != 1) return set_err(nullptr, DIT_ERR_CONFIG, "act_bf16 must be 0 or 1");
   if (c->adaln && c->final_norm)
     return set_err(nullptr, DIT_ERR_CONFIG, "with AdaLN the final layer is RMSNorm + modulate (final_norm must be 0)");
   // What the sm_103a kernels tile.
@@ -635,6 +636,31 @@ dit_status dit_bind_weights(dit_handle* h, const dit_weights* w, void* stream) {
     if (e != cudaSuccess) return cuda_err(h, e, "alloc b_in");
     DIT_CK(h, pack_ffn_in_launch(b.w_in, b_in, F, d, bd.w_in_packed, bd.b_in_packed, s), "pack w_in");
   }
+  if (!c.act_bf16) {
+    // f16 GEMM operands: the four linear maps' weights as library-owned f16 copies.  bf16 -> f16 is
+    // exact for every value of magnitude 2^-17 .. 65504; a weight beyond 65504 is refused.
+    int* range = static_cast<int*>(dev_alloc(h, 16, &e));
+    if (e != cudaSuccess) return cuda_err(h, e, "alloc range flag");
+    DIT_CK(h, cudaMemsetAsync(range, 0, 16, s), "range flag");
+    auto to_f16 = [&](const void* src, long long n, bool in_place) -> const void* {
+      void* dst = in_place ? const_cast<void*>(src) : dev_alloc(h, (size_t)n * 2, &e);
+      if (e == cudaSuccess) e = bf16_to_f16_launch(src, dst, n, range, s);
+      return dst;
+    };
+    for (int l = 0; l < c.n_blocks; ++l) {
+      BlockDev& bd = h->blocks[l];
+      bd.w_qkv = to_f16(bd.w_qkv, 3ll * d * d, c.qkv_interleaved != 0);  // the de-interleaved copy is ours
+      if (e == cudaSuccess) bd.w_o = to_f16(bd.w_o, (long long)d * d, false);
+      if (e == cudaSuccess) bd.w_down = to_f16(bd.w_down, (long long)d * F, false);
+      if (e == cudaSuccess) to_f16(bd.w_in_packed, 2ll * F * d, true);
+      if (e != cudaSuccess) return cuda_err(h, e, "bind: f16 weight copies");
+    }
+    int flag = 0;
+    DIT_CK(h, cudaMemcpyAsync(&flag, range, sizeof flag, cudaMemcpyDeviceToHost, s), "read range flag");
+    DIT_CK(h, cudaStreamSynchronize(s), "bind sync");
+    if (flag & kDevRange)
+      return set_err(h, DIT_ERR_RANGE, "a weight exceeds f16's range (65504); bind with act_bf16 = 1");
+  }
   h->lnf_g = vec32(w->lnf_g, d);
   h->lnf_b = vec32(w->lnf_b, d);
   if (e != cudaSuccess) return cuda_err(h, e, "bind final norm");
@@ -745,6 +771,8 @@ static dit_status forward_impl(dit_handle* h, const float* x_tokens, const int32
                         s);
   const int d = c.hidden, F = c.ffn_hidden, H = c.n_heads, nm = c.n_modalities;
   const int N = n_tokens;
+  const int f16 = c.act_bf16 ? 0 : 1;     // 16-bit operand type: f16 unless the config asks for bf16
+  const int y_kind = f16 ? 2 : 0;
   StatusWords* sw = at<StatusWords>(workspace, L.status);
   int* status = &sw->bits;
   int2* items = at<int2>(workspace, L.items);
@@ -804,6 +832,7 @@ static dit_status forward_impl(dit_handle* h, const float* x_tokens, const int32
   aa.max_items = L.max_items;
   aa.scale_log2 = (float)(1.4426950408889634 / sqrt((double)c.head_dim));
   aa.status = status;
+  aa.f16 = f16;
 
   for (int l = 0; l < c.n_blocks; ++l) {
     const BlockDev& B = h->blocks[l];
@@ -811,8 +840,8 @@ static dit_status forward_impl(dit_handle* h, const float* x_tokens, const int32
     {
       Launch ln(h, s, 5);
       DIT_CK(h, norm_modulate_launch(resid, resid_lo, N, d, c.norm, c.norm_eps, B.ln1_g, B.ln1_b, modality_tags,
-                                     c.adaln ? ml + 0 * d : nullptr, c.adaln ? ml + 1 * d : nullptr, mstride, y, 0,
-                                     status, s), "norm1");
+                                     c.adaln ? ml + 0 * d : nullptr, c.adaln ? ml + 1 * d : nullptr, mstride, y,
+                                     y_kind, status, s), "norm1");
       ln.done();
     }
     {
@@ -822,7 +851,7 @@ static dit_status forward_impl(dit_handle* h, const float* x_tokens, const int32
       g.d = d; g.head_dim = c.head_dim; g.rot_half = c.rotary_dim / 2;
       g.cos_cache = cosc; g.sin_cache = sinc; g.q = q; g.k = k; g.vt = vt; g.n_pad = L.n_pad;
       g.qk_norm = c.qk_norm; g.qk_eps = c.norm_eps;
-      g.status = status;
+      g.status = status; g.f16 = f16;
       DIT_CK(h, gemm_launch(kEpiQkvRope, y, B.w_qkv, g, s), "gemm qkv");
       ln.done();
     }
@@ -836,21 +865,22 @@ static dit_status forward_impl(dit_handle* h, const float* x_tokens, const int32
       GemmArgs g{};
       g.M = N; g.N = d; g.K = d; g.bias = B.b_o;
       g.x = resid; g.gate = c.adaln ? ml + 2 * d : B.res1; g.gate_stride = c.adaln ? mstride : 0;
-      g.tags = modality_tags; g.status = status;
+      g.tags = modality_tags; g.status = status; g.f16 = f16;
       DIT_CK(h, gemm_launch(kEpiGatedResid, o, B.w_o, g, s), "gemm out");
       ln.done();
     }
     {
       Launch ln(h, s, 5);
       DIT_CK(h, norm_modulate_launch(resid, resid_lo, N, d, c.norm, c.norm_eps, B.ln2_g, B.ln2_b, modality_tags,
-                                     c.adaln ? ml + 3 * d : nullptr, c.adaln ? ml + 4 * d : nullptr, mstride, y, 0,
-                                     status, s), "norm2");
+                                     c.adaln ? ml + 3 * d : nullptr, c.adaln ? ml + 4 * d : nullptr, mstride, y,
+                                     y_kind, status, s), "norm2");
       ln.done();
     }
     {
       Launch ln(h, s, 3);
       GemmArgs g{};
       g.M = N; g.N = 2 * F; g.K = d; g.bias = B.b_in_packed; g.out = hbuf; g.status = status;
+      g.f16 = f16; g.out_kind = y_kind;
       DIT_CK(h, gemm_launch(kEpiSwiglu, y, B.w_in_packed, g, s), "gemm ffn up");
       ln.done();
     }
@@ -859,7 +889,7 @@ static dit_status forward_impl(dit_handle* h, const float* x_tokens, const int32
       GemmArgs g{};
       g.M = N; g.N = d; g.K = F; g.bias = B.b_down;
       g.x = resid; g.gate = c.adaln ? ml + 5 * d : B.res2; g.gate_stride = c.adaln ? mstride : 0;
-      g.tags = modality_tags; g.status = status;
+      g.tags = modality_tags; g.status = status; g.f16 = f16;
       DIT_CK(h, gemm_launch(kEpiGatedResid, hbuf, B.w_down, g, s), "gemm ffn down");
       ln.done();
     }
@@ -1204,6 +1234,8 @@ dit_status dit_sync_status(dit_handle* h, const void* workspace, void* stream) {
   if (sw.bits & kDevLayout) return set_err(h, DIT_ERR_LAYOUT, "device validator rejected the layout (code %d)", sw.layout_code);
   if (sw.bits & kDevTimeout) return set_err(h, DIT_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait ran out");
   if (sw.bits & kDevCapacity) return set_err(h, DIT_ERR_CAPACITY, "tile schedule overflow");
+  if (sw.bits & kDevRange)
+    return set_err(h, DIT_ERR_RANGE, "an f16 operand (norm output or FFN hidden) exceeded 65504; act_bf16 = 1 avoids it");
   return DIT_OK;
 }
 
@@ -1262,7 +1294,7 @@ dit_status dit_get_kernel_times(dit_handle* h, double* ms_out, int64_t* launches
 dit_status dit_op_norm_modulate(const float* x, int n, int d, int norm, float eps, const float* ln_g, const float* ln_b,
                                 const uint8_t* tags, const float* shift, const float* scale, int64_t mod_stride,
                                 void* y, int out_kind, void* stream) {
-  if (n < 0 || !x || !y || (shift && (!scale || !tags)) || (out_kind != 0 && out_kind != 1) ||
+  if (n < 0 || !x || !y || (shift && (!scale || !tags)) || out_kind < 0 || out_kind > 2 ||
       (norm != DIT_RMSNORM && norm != DIT_LAYERNORM))
     return set_err(nullptr, DIT_ERR_INVALID_ARG, "bad norm_modulate arguments");
   if (!norm_width_supported(d)) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "width %d not tiled by the norm kernel", d);
@@ -1292,20 +1324,22 @@ dit_status dit_op_adaln(const void* w, const float* b, int rows, int t_dim, floa
   return e == cudaSuccess ? DIT_OK : cuda_err(nullptr, e, "adaln");
 }
 
-static dit_status check_gemm(const void* a, const void* b, int M, int N, int K) {
+static dit_status check_gemm(const void* a, const void* b, int M, int N, int K, int elem) {
   if (!a || !b || M < 0 || N <= 0 || K <= 0) return set_err(nullptr, DIT_ERR_INVALID_ARG, "bad GEMM arguments");
+  if (elem != DIT_ELEM_BF16 && elem != DIT_ELEM_F16)
+    return set_err(nullptr, DIT_ERR_INVALID_ARG, "elem must be DIT_ELEM_BF16 or DIT_ELEM_F16");
   if (N % 256 || K % 64) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "GEMM needs N %% 256 == 0 and K %% 64 == 0");
   if (!aligned16(a) || !aligned16(b)) return set_err(nullptr, DIT_ERR_INVALID_ARG, "GEMM operands must be 16-byte aligned");
   return DIT_OK;
 }
 
 dit_status dit_op_gemm(const void* a, const void* b, const float* bias, int M, int N, int K, void* out, int out_kind,
-                       void* stream) {
-  dit_status st = check_gemm(a, b, M, N, K);
+                       int elem, void* stream) {
+  dit_status st = check_gemm(a, b, M, N, K, elem);
   if (st != DIT_OK) return st;
-  if (!out || (out_kind != 0 && out_kind != 1)) return set_err(nullptr, DIT_ERR_INVALID_ARG, "bad GEMM output");
+  if (!out || out_kind < 0 || out_kind > 2) return set_err(nullptr, DIT_ERR_INVALID_ARG, "bad GEMM output");
   GemmArgs g{};
-  g.M = M; g.N = N; g.K = K; g.bias = bias; g.out = out; g.out_kind = out_kind;
+  g.M = M; g.N = N; g.K = K; g.bias = bias; g.out = out; g.out_kind = out_kind; g.f16 = elem;
   cudaError_t e = gemm_launch(kEpiStore, a, b, g, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? DIT_OK : cuda_err(nullptr, e, "gemm");
 }
@@ -1337,8 +1371,8 @@ dit_status dit_op_gemm_nvfp4(const void* a_f16, const void* packed, float w_scal
 
 dit_status dit_op_gemm_qkv_rope(const void* a, const void* b, const float* bias, int M, int d, int K, int n_heads,
                                 int head_dim, int rotary_dim, const float* cos_cache, const float* sin_cache, void* q,
-                                void* k, void* vt, int n_pad, void* stream) {
-  dit_status st = check_gemm(a, b, M, 3 * d, K);
+                                void* k, void* vt, int n_pad, int elem, void* stream) {
+  dit_status st = check_gemm(a, b, M, 3 * d, K, elem);
   if (st != DIT_OK) return st;
   if (d % 256 || n_heads * head_dim != d || 256 % head_dim || rotary_dim > head_dim || (rotary_dim / 2) % 16 ||
       (head_dim - rotary_dim) % 16 || !q || !k || !vt || n_pad < M || n_pad % 8 ||
@@ -1346,30 +1380,32 @@ dit_status dit_op_gemm_qkv_rope(const void* a, const void* b, const float* bias,
     return set_err(nullptr, DIT_ERR_INVALID_ARG, "bad qkv_rope arguments");
   GemmArgs g{};
   g.M = M; g.N = 3 * d; g.K = K; g.bias = bias; g.d = d; g.head_dim = head_dim; g.rot_half = rotary_dim / 2;
-  g.cos_cache = cos_cache; g.sin_cache = sin_cache; g.q = q; g.k = k; g.vt = vt; g.n_pad = n_pad;
+  g.cos_cache = cos_cache; g.sin_cache = sin_cache; g.q = q; g.k = k; g.vt = vt; g.n_pad = n_pad; g.f16 = elem;
   cudaError_t e = gemm_launch(kEpiQkvRope, a, b, g, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? DIT_OK : cuda_err(nullptr, e, "gemm qkv");
 }
 
 dit_status dit_op_gemm_gated_residual(const void* a, const void* b, const float* bias, int M, int N, int K, float* x,
-                                      const float* gate, int64_t gate_stride, const uint8_t* tags, void* stream) {
-  dit_status st = check_gemm(a, b, M, N, K);
+                                      const float* gate, int64_t gate_stride, const uint8_t* tags, int elem,
+                                      void* stream) {
+  dit_status st = check_gemm(a, b, M, N, K, elem);
   if (st != DIT_OK) return st;
   if (!x || (gate && (!tags || gate_stride % 4 || !aligned16(gate))) || !aligned16(x))
     return set_err(nullptr, DIT_ERR_INVALID_ARG, "bad gated_residual arguments");
   GemmArgs g{};
   g.M = M; g.N = N; g.K = K; g.bias = bias; g.x = x; g.gate = gate; g.gate_stride = gate_stride; g.tags = tags;
+  g.f16 = elem;
   cudaError_t e = gemm_launch(kEpiGatedResid, a, b, g, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? DIT_OK : cuda_err(nullptr, e, "gemm gated residual");
 }
 
 dit_status dit_op_gemm_swiglu(const void* a, const void* b_packed, const float* bias_packed, int M, int F, int K,
-                              void* hout, void* stream) {
-  dit_status st = check_gemm(a, b_packed, M, 2 * F, K);
+                              void* hout, int elem, void* stream) {
+  dit_status st = check_gemm(a, b_packed, M, 2 * F, K, elem);
   if (st != DIT_OK) return st;
   if (!hout || F % 128) return set_err(nullptr, DIT_ERR_INVALID_ARG, "bad swiglu arguments");
   GemmArgs g{};
-  g.M = M; g.N = 2 * F; g.K = K; g.bias = bias_packed; g.out = hout;
+  g.M = M; g.N = 2 * F; g.K = K; g.bias = bias_packed; g.out = hout; g.f16 = elem; g.out_kind = elem ? 2 : 0;
   cudaError_t e = gemm_launch(kEpiSwiglu, a, b_packed, g, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? DIT_OK : cuda_err(nullptr, e, "gemm swiglu");
 }
@@ -1436,10 +1472,11 @@ size_t dit_attention_workspace_bytes(int n_docs, int n_tokens) {
 }
 
 dit_status dit_op_attention(const void* q, const void* k, const void* vt, int n_pad, const int32_t* cu_seqlens,
-                            int n_docs, int n_tokens, int n_heads, int head_dim, void* o, void* workspace,
+                            int n_docs, int n_tokens, int n_heads, int head_dim, void* o, void* workspace, int elem,
                             void* stream) {
   if (!q || !k || !vt || !o || !cu_seqlens || !workspace || n_docs < 1 || n_tokens < 1 || n_heads < 1 ||
-      n_pad < n_tokens || n_pad % 8 || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
+      n_pad < n_tokens || n_pad % 8 || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) ||
+      (elem != DIT_ELEM_BF16 && elem != DIT_ELEM_F16))
     return set_err(nullptr, DIT_ERR_INVALID_ARG, "bad attention arguments");
   if (head_dim != 128 && head_dim != 64) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "attention needs head_dim 64 or 128");
   if (!aligned16(q) || !aligned16(k) || !aligned16(vt) || !aligned16(o))
@@ -1458,6 +1495,7 @@ dit_status dit_op_attention(const void* q, const void* k, const void* vt, int n_
   aa.cu = cu_seqlens; aa.items = items; aa.count = &sw->count; aa.max_items = max_items;
   aa.scale_log2 = (float)(1.4426950408889634 / sqrt((double)head_dim));
   aa.status = &sw->bits;
+  aa.f16 = elem;
   e = attention_launch(q, k, vt, o, aa, s);
   return e == cudaSuccess ? DIT_OK : cuda_err(nullptr, e, "attention");
 }
@@ -1551,9 +1589,9 @@ cudaError_t noalloc_scratch(void** out) {
 
 extern "C" dit_status dit_op_attention_noalloc(const void* q, const void* k, const void* vt, int n_pad,
                                                const int32_t* cu_seqlens, int n_docs, int n_tokens, int n_heads,
-                                               int head_dim, void* o, void* stream) {
+                                               int head_dim, void* o, int elem, void* stream) {
   if (!q || !k || !vt || !o || !cu_seqlens || n_docs < 1 || n_tokens < 1 || n_heads < 1 || n_pad < n_tokens ||
-      n_pad % 8)
+      n_pad % 8 || (elem != DIT_ELEM_BF16 && elem != DIT_ELEM_F16))
     return set_err(nullptr, DIT_ERR_INVALID_ARG, "bad attention arguments");
   if (head_dim != 128 && head_dim != 64) return set_err(nullptr, DIT_ERR_UNSUPPORTED, "attention needs head_dim 64 or 128");
   if (!aligned16(q) || !aligned16(k) || !aligned16(vt) || !aligned16(o))
@@ -1582,6 +1620,7 @@ extern "C" dit_status dit_op_attention_noalloc(const void* q, const void* k, con
   aa.cu = cu_seqlens; aa.items = items; aa.count = &sw->count; aa.max_items = max_items;
   aa.scale_log2 = (float)(1.4426950408889634 / sqrt((double)head_dim));
   aa.status = &sw->bits;
+  aa.f16 = elem;
   e = attention_launch(q, k, vt, o, aa, s);
   return e == cudaSuccess ? DIT_OK : cuda_err(nullptr, e, "attention");
 }

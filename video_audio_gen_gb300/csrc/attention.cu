@@ -6,22 +6,29 @@
 //
 // One CTA = one (document, 128-row q-tile, head).  Key/value tiles are 128 tokens wide and start
 // at multiples of 128 in the packed sequence (so the TMA x coordinate of the transposed V is
-// 16-byte aligned); columns outside the document are masked to -inf.
-//   warp 0     TMA producer: Q once, then K and V^T tiles through two 2-stage rings
+// 16-byte aligned); columns outside the document are masked to -inf in S and zeroed in V^T.
+//   warp 0     TMA producer: Q once, then K and V^T tiles through two 2-stage rings, polling both
+//              rings so that a K load never queues behind a V load
 //   warp 1     TMEM allocator + S issuer: S(j) = Q K(j)^T into TMEM buffer j % 2, issued as soon as
 //              the softmax has loaded S(j - 2) from that buffer
-//   warp 10    PV issuer: O_h += P(j) V(j) once P(j) is in shared memory and V(j) has landed (one
-//              barrier counts both); key columns [0, 64) accumulate into O_0, [64, 128) into O_1
-//   warps 2-9  softmax, two warps per query row: warp half h owns key columns [64h, 64h + 64) of
-//              every tile and keeps its own running max m_h, sum l_h and accumulator O_h, exactly as
-//              two independent passes over disjoint key subsets would; the halves exchange nothing
-//              per tile and are merged once at the end:
+//   warp 10    PV issuer: O_{j%2} += P(j) V(j) once P(j) is in shared memory and V(j) has landed (one
+//              barrier counts both); on a document's boundary tiles the warp first zeroes the V^T
+//              columns outside the document, so that a non-finite value in a neighbouring document
+//              cannot reach this one through 0 * inf
+//   warps 2-9  softmax, two groups of four warps (one thread per query row) on alternating tiles:
+//              group g takes the tiles j with j % 2 == g, all 128 key columns of each, and keeps its
+//              own running max m_g, sum l_g and accumulator O_g, exactly as two independent passes
+//              over the even and the odd key tiles would; the groups exchange nothing per tile and
+//              are merged once at the end:
 //                  o = (2^(m_0-m) O_0 + 2^(m_1-m) O_1) / (2^(m_0-m) l_0 + 2^(m_1-m) l_1),  m = max(m_0, m_1)
+//              While one group computes the exponentials of its tile, the other loads its scores
+//              and stores its probabilities, so the exponential unit is busy through both.
 // Two issuing threads, because one thread's tcgen05.mma issue runs nearly in step with the tensor
 // pipe: whatever else that thread waits on leaves the pipe idle.  With S and PV on separate
-// threads, S(j + 2) runs while the softmax works on tile j, and PV(j) while it works on j + 1.
-// The softmax waits on one barrier per tile: "S(j) ready" completes only when S(j) is in TMEM and
-// O += P(j - 2) V(j - 2) is done, so it also says that P buffer j % 2 is free.
+// threads, S(j + 2) runs while group j % 2 works on tile j, and PV(j) while it works on j + 2.
+// The softmax waits for S(j) on "S(j) ready", and for its own previous P(j - 2) V(j - 2) only where it
+// needs it: before it rescales O_{j%2} (rare) or rewrites P buffer j % 2, so that PV runs while the
+// next tile's scores are loaded and reduced.
 // TMEM: S double buffer (2 x 128 columns) + O_0, O_1 (2 x HD columns) <= 512.  P(j) (bf16) goes to
 // shared memory buffer j % 2 in the swizzled K-major layout the PV MMA reads.
 #include "common.cuh"
@@ -38,6 +45,7 @@ constexpr int P_BYTES = 2 * ATOM;          // P tile: 128 q rows x 128 kv column
 constexpr int KV_STAGES = 2;
 constexpr int ATT_THREADS = 352;           // producer, S issuer, 8 softmax warps, PV issuer
 constexpr int SOFTMAX_THREADS = 256;
+constexpr int GROUP_WARPS = 4;             // softmax warps per tile group
 constexpr int PV_WARP = 10;
 static_assert(KV_STAGES == 2, "V(j) lands on the barrier of P buffer j % 2");
 
@@ -65,10 +73,34 @@ __device__ __forceinline__ bool wait_noabort(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// Zero the columns of a landed V^T tile (two 64-column atoms of HD rows, 128-byte swizzled) whose
+// key index lies outside [lo, hi): one 16-byte chunk (8 keys of one row) per step, by the 32 lanes of
+// one warp.  Chunks wholly inside the document are left alone.
+template <int HD>
+__device__ __forceinline__ void zero_v_outside(uint8_t* sv_tile, int lo, int hi, int lane) {
+  const uint32_t base = smem_u32(sv_tile);
+  for (int idx = lane; idx < HD * 16; idx += 32) {
+    const int row = idx >> 4, chunk = idx & 15;  // chunk: keys [8 chunk, 8 chunk + 8)
+    const int k0 = chunk * 8;
+    if (k0 >= lo && k0 + 8 <= hi) continue;
+    const uint32_t addr = base + (chunk >> 3) * (HD * 128) + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
+    uint4 v = ld_shared_v4(addr);
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int k = k0 + 2 * e;
+      const uint32_t keep_lo = (k >= lo && k < hi) ? 0x0000FFFFu : 0u;
+      const uint32_t keep_hi = (k + 1 >= lo && k + 1 < hi) ? 0xFFFF0000u : 0u;
+      w[e] &= keep_lo | keep_hi;
+    }
+    st_shared_v4(addr, w[0], w[1], w[2], w[3]);
+  }
+}
+
 template <int HD>
 __global__ void __launch_bounds__(ATT_THREADS, 1)
     attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O, const AttnArgs args) {
+                     const __grid_constant__ CUtensorMap tmV, uint16_t* __restrict__ O, const AttnArgs args) {
   if (args.status && (*reinterpret_cast<volatile int*>(args.status) & kDevLayout)) return;
   const int count = *args.count;
   const int head = blockIdx.x / args.max_items;
@@ -92,10 +124,10 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   uint64_t* k_full = bars + 1;                         // [stage]  K tile landed
   uint64_t* k_empty = k_full + KV_STAGES;              // [stage]  S MMA done with the K tile
   uint64_t* v_empty = k_empty + KV_STAGES;             // [stage]  PV MMA done with the V^T tile
-  uint64_t* s_full = v_empty + KV_STAGES;              // [2]  S(j) in TMEM and P(j - 2) V(j - 2) done
+  uint64_t* s_full = v_empty + KV_STAGES;              // [2]  S(j) in TMEM
   uint64_t* s_free = s_full + 2;                       // [2]  softmax has loaded S(j) from its buffer
   uint64_t* p_full = s_free + 2;                       // [2]  P(j) in shared memory and V(j) landed
-  uint64_t* o_done = p_full + 2;                       // [2]  O += P(j) V(j) complete
+  uint64_t* o_done = p_full + 2;                       // [2]  O_{j%2} += P(j) V(j) complete
   uint64_t* s_drain = o_done + 2;                      // every S MMA complete
   uint64_t* o_drain = s_drain + 1;                     // every PV MMA complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_drain + 1);
@@ -110,9 +142,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       mbar_init(&v_empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&s_full[s], 2);                          // S commit + PV commit of tile j - 2
-      mbar_init(&s_free[s], SOFTMAX_THREADS / 32);
-      mbar_init(&p_full[s], SOFTMAX_THREADS / 32 + 1);   // softmax warps + the V^T load
+      mbar_init(&s_full[s], 1);                          // the S commit
+      mbar_init(&s_free[s], GROUP_WARPS);
+      mbar_init(&p_full[s], GROUP_WARPS + 1);            // the group's warps + the V^T load
       mbar_init(&o_done[s], 1);
     }
     mbar_init(s_drain, 1);
@@ -134,38 +166,46 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       mbar_arrive_expect_tx(q_full, Plan::Q_BYTES);
 #pragma unroll
       for (int a = 0; a < HD / 64; ++a) tma_load_2d(sQ + a * ATOM, &tmQ, q_full, hx + 64 * a, q0);
-      // K tiles run two ahead of the V tiles: K(j) waits for S(j - KV_STAGES), V(j) for
-      // P(j - KV_STAGES) V(j - KV_STAGES).
-      auto load_k = [&](int j) -> bool {
-        const int st = j % KV_STAGES;
-        if (!mbar_wait(&k_empty[st], ((j / KV_STAGES) & 1) ^ 1, abort_flag, args.status)) return false;
-        const int kv0 = kv_base + j * TK;
-        mbar_arrive_expect_tx(&k_full[st], Plan::K_BYTES);
-#pragma unroll
-        for (int a = 0; a < HD / 64; ++a)
-          tma_load_2d(sK + st * Plan::K_BYTES + a * ATOM, &tmK, &k_full[st], hx + 64 * a, kv0);
-        return true;
-      };
-      auto load_v = [&](int j) -> bool {
-        const int st = j % KV_STAGES;
-        if (!mbar_wait(&v_empty[st], ((j / KV_STAGES) & 1) ^ 1, abort_flag, args.status)) return false;
-        const int kv0 = kv_base + j * TK;
-        // V(j) completes on the barrier that also counts the softmax warps' P(j) (stage = j % 2)
-        mbar_arrive_expect_tx(&p_full[st], Plan::V_BYTES);
-        tma_load_2d(sV + st * Plan::V_BYTES, &tmV, &p_full[st], kv0, hx);
-        tma_load_2d(sV + st * Plan::V_BYTES + Plan::V_ATOM, &tmV, &p_full[st], kv0 + 64, hx);
-        return true;
-      };
+      // K(j) needs its stage back from S(j - 2), V(j) from P(j - 2) V(j - 2).  Both rings are polled,
+      // so each load is issued as soon as its own stage is free.  Each wait is bounded on its own.
       int nk = 0, nv = 0;
       bool ok = true;
-      for (; ok && nk < n_kv && nk < 2; ++nk) ok = load_k(nk);
-      while (ok && nv < n_kv) {
-        ok = load_v(nv);
-        if (!ok) break;
-        ++nv;
-        if (nk < n_kv) {
-          ok = load_k(nk);
-          if (ok) ++nk;
+      uint64_t t0 = globaltimer_ns();
+      for (uint32_t spins = 0; nk < n_kv || nv < n_kv;) {
+        bool moved = false;
+        if (nk < n_kv && mbar_test_wait(&k_empty[nk % KV_STAGES], ((nk / KV_STAGES) & 1) ^ 1)) {
+          const int st = nk % KV_STAGES, kv0 = kv_base + nk * TK;
+          mbar_arrive_expect_tx(&k_full[st], Plan::K_BYTES);
+#pragma unroll
+          for (int a = 0; a < HD / 64; ++a)
+            tma_load_2d(sK + st * Plan::K_BYTES + a * ATOM, &tmK, &k_full[st], hx + 64 * a, kv0);
+          ++nk;
+          moved = true;
+        }
+        if (nv < nk && mbar_test_wait(&v_empty[nv % KV_STAGES], ((nv / KV_STAGES) & 1) ^ 1)) {
+          const int st = nv % KV_STAGES, kv0 = kv_base + nv * TK;
+          // V(j) completes on the barrier that also counts the softmax group's P(j) (stage = j % 2)
+          mbar_arrive_expect_tx(&p_full[st], Plan::V_BYTES);
+          tma_load_2d(sV + st * Plan::V_BYTES, &tmV, &p_full[st], kv0, hx);
+          tma_load_2d(sV + st * Plan::V_BYTES + Plan::V_ATOM, &tmV, &p_full[st], kv0 + 64, hx);
+          ++nv;
+          moved = true;
+        }
+        if (moved) {
+          t0 = globaltimer_ns();
+          spins = 0;
+          continue;
+        }
+        __nanosleep(32);  // a short yield: this thread shares its scheduler with softmax warps
+        if ((++spins & 255u) == 0) {
+          if (*abort_flag) {
+            ok = false;
+          } else if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            if (args.status) atomicOr(args.status, kDevTimeout);
+            ok = false;
+          }
+          if (!ok) break;
         }
       }
       // Every copy this CTA issued must land before the CTA may exit.
@@ -181,6 +221,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       bool ok = mbar_wait(q_full, 0, abort_flag, args.status);
       tc_fence_after();
       const uint32_t q_addr = smem_u32(sQ);
+      const uint32_t id_s = args.f16 ? idesc_f16_f32(128, TK) : Plan::IDESC_S;
       for (int j = 0; ok && j < n_kv; ++j) {
         const int st = j % KV_STAGES, sb = j & 1;
         if (j >= 2 && !mbar_wait(&s_free[sb], ((j - 2) >> 1) & 1, abort_flag, args.status)) break;
@@ -190,7 +231,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
 #pragma unroll
         for (int ks = 0; ks < HD / 16; ++ks) {
           const uint32_t off = (ks >> 2) * ATOM + (ks & 3) * 32;
-          umma_bf16(t_s + sb * TK, sdesc_sw128(q_addr + off), sdesc_sw128(k_addr + off), Plan::IDESC_S, ks != 0);
+          umma_bf16(t_s + sb * TK, sdesc_sw128(q_addr + off), sdesc_sw128(k_addr + off), id_s, ks != 0);
         }
         umma_commit(&s_full[sb]);
         umma_commit(&k_empty[st]);
@@ -200,166 +241,196 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       wait_noabort(s_drain, 0);
     }
   } else if (warp == PV_WARP) {
-    if (lane == 0) {
-      // tiles 0 and 1 have no PV two tiles back: their "S ready" phases get that arrival now
-      mbar_arrive(&s_full[0]);
-      mbar_arrive(&s_full[1]);
-      for (int j = 0; j < n_kv; ++j) {
-        const int pb = j & 1, st = j % KV_STAGES;
-        if (!mbar_wait(&p_full[pb], (j >> 1) & 1, abort_flag, args.status)) break;
+    for (int j = 0; j < n_kv; ++j) {
+      const int pb = j & 1, st = j % KV_STAGES;
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(&p_full[pb], (j >> 1) & 1, abort_flag, args.status);
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+      const int c0 = kv_base + j * TK;
+      const int lo = ds > c0 ? ds - c0 : 0;
+      const int hi = de - c0 < TK ? de - c0 : TK;
+      if (lo > 0 || hi < TK) {
+        // a boundary tile: every lane sees the landed V^T tile through the barrier (its phase cannot
+        // move on before this tile's PV is committed), zeroes its share of the outside columns and
+        // makes the stores visible to the tensor core's operand reads
+        wait_noabort(&p_full[pb], (j >> 1) & 1);
+        zero_v_outside<HD>(sV + st * Plan::V_BYTES, lo, hi, lane);
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+      if (lane == 0) {
         tc_fence_after();
+        const uint32_t id_o = args.f16 ? idesc_f16_f32(128, HD) : Plan::IDESC_O;
         const uint32_t p_addr = smem_u32(sP + pb * P_BYTES);
         const uint32_t v_addr = smem_u32(sV + st * Plan::V_BYTES);
 #pragma unroll
         for (int ks = 0; ks < TK / 16; ++ks) {
-          // key columns [0, 64) (P atom 0, V^T atom 0) -> O_0; [64, 128) (atom 1) -> O_1
+          // key columns [0, 64) in P atom 0 / V^T atom 0, [64, 128) in atom 1; all into O_{j%2}
           const uint32_t p_off = (ks >> 2) * ATOM + (ks & 3) * 32;
           const uint32_t v_off = (ks >> 2) * Plan::V_ATOM + (ks & 3) * 32;
-          umma_bf16(t_o + (ks >> 2) * HD, sdesc_sw128(p_addr + p_off), sdesc_sw128(v_addr + v_off), Plan::IDESC_O,
-                    (j | (ks & 3)) != 0);
+          umma_bf16(t_o + pb * HD, sdesc_sw128(p_addr + p_off), sdesc_sw128(v_addr + v_off), id_o,
+                    (j >= 2 || ks != 0) ? 1u : 0u);
         }
         umma_commit(&o_done[pb]);
         umma_commit(&v_empty[st]);
-        umma_commit(&s_full[pb]);                          // the second arrival of "S(j + 2) ready"
       }
+      __syncwarp();
+    }
+    if (lane == 0) {
       umma_commit(o_drain);
       wait_noabort(o_drain, 0);
     }
   } else {
     // ---------------- softmax warps ----------------
-    // Two warps per row: TMEM lane quarter = warp % 4 (the rows a warp may access), key-column half
-    // = (warp - 2) / 4.  O_h accumulates in TMEM through the MMA; the running max m_h is only raised
-    // (and O_h, l_h rescaled by exp2(m_old - m_new)) when the half-row max grows by more than 2^8,
-    // so most tiles never touch O_h.  Between raises p = exp2(s * scale - m_h) stays below 2^8.
-    constexpr int HC = TK / 2;                   // key columns per half
+    // Group g = (warp - 2) / 4 takes tiles j = g, g + 2, ...; TMEM lane quarter = warp % 4 (the rows a
+    // warp may access), one thread per query row and all 128 key columns of the tile.  O_g accumulates
+    // in TMEM through the MMA; the running max m_g is only raised (and O_g, l_g rescaled by
+    // exp2(m_old - m_new)) when the row max grows by more than 2^8, so most tiles never touch O_g.
+    // Between raises p = exp2(s * scale - m_g) stays below 2^8.  Every key tile holds at least one
+    // key of the document, so m_g is finite after the group's first tile.
     const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int grp = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;           // tile row owned by this thread
     const int row = q0 + r;                      // packed-sequence row
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t t_oh = t_o + half * HD + lane_off;
+    const uint32_t t_og = t_o + grp * HD + lane_off;
+    const uint32_t ts = t_s + grp * TK + lane_off;
     const float sc = args.scale_log2;
+    const bool f16 = args.f16;                   // P and o as f16 (else bf16)
     constexpr float kRescaleThreshold = 8.0f;    // log2 units
     float m = -INFINITY, l = 0.f;
     bool ok = true;
+    int last = -1;
 
-    for (int j = 0; j < n_kv; ++j) {
-      const int sb = j & 1;
-      if (!mbar_wait(&s_full[sb], (j >> 1) & 1, abort_flag, args.status)) {
+    for (int j = grp; j < n_kv; j += 2) {
+      if (!mbar_wait(&s_full[grp], (j >> 1) & 1, abort_flag, args.status)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const int c0 = kv_base + j * TK + half * HC;
+      const int c0 = kv_base + j * TK;
       const int lo = ds > c0 ? ds - c0 : 0;
-      const int hi = de - c0 < HC ? de - c0 : HC;
-      const bool interior = (lo == 0) && (hi == HC);
-      const uint32_t ts = t_s + sb * TK + half * HC + lane_off;
-      uint32_t sv[HC];
+      const int hi = de - c0 < TK ? de - c0 : TK;
+      uint32_t sv[TK];
 #pragma unroll
-      for (int c = 0; c < HC; c += 32) tmem_ld32(ts + c, *reinterpret_cast<uint32_t(*)[32]>(&sv[c]));
+      for (int c = 0; c < TK; c += 32) tmem_ld32(ts + c, *reinterpret_cast<uint32_t(*)[32]>(&sv[c]));
 #pragma unroll
-      for (int c = 0; c < HC; c += 32) tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&sv[c]));
+      for (int c = 0; c < TK; c += 32) tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&sv[c]));
       // the scores are in registers: the S issuer may overwrite this buffer with S(j + 2)
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[sb]);
-      if (!interior) {
+      if (lane == 0) mbar_arrive(&s_free[grp]);
+      if (lo > 0 || hi < TK) {
 #pragma unroll
-        for (int i = 0; i < HC; ++i)
+        for (int i = 0; i < TK; ++i)
           if (i < lo || i >= hi) sv[i] = __float_as_uint(-INFINITY);
       }
-      // half-row max: four independent chains of three-input max
+      // row max: four independent chains of three-input max
       float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < HC; i += 8) {
+      for (int i = 0; i < TK; i += 8) {
         mx0 = fmax3(mx0, __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]));
         mx1 = fmax3(mx1, __uint_as_float(sv[i + 2]), __uint_as_float(sv[i + 3]));
         mx2 = fmax3(mx2, __uint_as_float(sv[i + 4]), __uint_as_float(sv[i + 5]));
         mx3 = fmax3(mx3, __uint_as_float(sv[i + 6]), __uint_as_float(sv[i + 7]));
       }
       const float m_cand = fmaxf(fmax3(mx0, mx1, mx2), mx3) * sc;
-      // true on the first tile with a key of the document in this half (m = -inf until then)
+      // true on the group's first tile (m = -inf until then)
       const bool raise = m_cand > m + kRescaleThreshold;
+      // The group's previous tile, P(j - 2) V(j - 2), must be done before O_g is rescaled or P
+      // buffer j % 2 is rewritten; it runs while this tile's scores are loaded and reduced, and is
+      // waited for only at the first of those two points.
+      bool pv_prev = j < 2;
+      auto wait_pv_prev = [&]() -> bool {
+        if (pv_prev) return true;
+        pv_prev = true;
+        const bool w = mbar_wait(&o_done[grp], ((j - 2) >> 1) & 1, abort_flag, args.status);
+        tc_fence_after();
+        return w;
+      };
       if (__any_sync(0xffffffffu, raise)) {
         const float m_new = raise ? m_cand : m;
-        const float alpha = raise ? fast_exp2(m - m_new) : 1.f;  // exp2(-inf) = 0 before the first key
-        if (j > 0) {
-          // O_h holds this half's sum over tiles < j relative to m: wait for the last PV, rescale
-          if (!mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, args.status)) {
+        const float alpha = raise ? fast_exp2(m - m_new) : 1.f;  // exp2(-inf) = 0 before the first tile
+        if (j >= 2) {
+          // O_g holds the group's sum over its earlier tiles relative to m
+          if (!wait_pv_prev()) {
             ok = false;
             break;
           }
-          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < HD; c += 16) {  // 16 columns at a time: the row's scores stay in registers
+            uint32_t ov[16];
+            tmem_ld16(t_og + c, ov);
+            tmem_ld_wait_regs(ov);
 #pragma unroll
-          for (int c = 0; c < HD; c += 32) {
-            uint32_t ov[32];
-            tmem_ld32_sync(t_oh + c, ov);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-            tmem_st32(t_oh + c, ov);
-            tmem_st_wait();
+            for (int i = 0; i < 16; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+            tmem_st16(t_og + c, ov);
           }
+          tmem_st_wait();
         }
         l *= alpha;
         m = m_new;
       }
-      // A half that has seen no key of the document yet has m = -inf and only masked scores:
-      // p = exp2(-inf - 0) = 0 keeps O_h and l_h at zero.
-      const float mu = m == -INFINITY ? 0.f : m;
-      // p = exp2(s * scale - m) -> bf16 pairs; this half's 64 columns are exactly P atom `half` of
-      // shared-memory buffer j % 2, one 128-byte swizzled row per query row
-      uint32_t pk[HC / 2];
-      // paired fp32 arithmetic (one f32x2 FMA / add per two scores); four partial row sums
-      const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-mu, -mu);
-      float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      // p = exp2(s * scale - m) -> 16-bit pairs, one 128-byte swizzled row per query row in each of
+      // the two 64-column atoms of P buffer j % 2; paired fp32 arithmetic, two partial row sums
+      const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-m, -m);
+      float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      const uint32_t p_row = smem_u32(sP + grp * P_BYTES) + r * 128;
 #pragma unroll
-      for (int c = 0; c < HC; c += 8) {
+      for (int c = 0; c < 16; ++c) {  // 16-byte chunk c of the row: keys [8c, 8c + 8), atom c / 8
+        if (c == 0 && !wait_pv_prev()) {  // P buffer j % 2 is read by P(j - 2) V(j - 2) until it is done
+          ok = false;
+          break;
+        }
+        uint32_t pk[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const float2 x = ffma2(make_float2(__uint_as_float(sv[c + 2 * u]), __uint_as_float(sv[c + 2 * u + 1])), sc2, nm2);
+          const int i = c * 8 + 2 * u;
+          const float2 x = ffma2(make_float2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), sc2, nm2);
           const float2 e = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-          rs[u] = fadd2(rs[u], e);
-          pk[c / 2 + u] = pack_bf16x2(e.x, e.y);
+          rs[u & 1] = fadd2(rs[u & 1], e);
+          pk[u] = pack16(f16, e.x, e.y);
         }
+        st_shared_v4(p_row + (c >> 3) * ATOM + (((c & 7) ^ (r & 7)) << 4), pk[0], pk[1], pk[2], pk[3]);
       }
-      l += (rs[0].x + rs[0].y + rs[1].x + rs[1].y) + (rs[2].x + rs[2].y + rs[3].x + rs[3].y);
-      // P buffer j % 2 is free: "S(j) ready" included O += P(j - 2) V(j - 2) being done
-      const uint32_t p_row = smem_u32(sP + sb * P_BYTES + half * ATOM) + r * 128;
-#pragma unroll
-      for (int c = 0; c < HC / 8; ++c)
-        st_shared_v4(p_row + ((c ^ (r & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      if (!ok) break;
+      l += (rs[0].x + rs[0].y) + (rs[1].x + rs[1].y);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[sb]);
+      if (lane == 0) mbar_arrive(&p_full[grp]);
+      last = j;
     }
-    if (ok && n_kv > 0) {
-      const int jl = n_kv - 1;
-      ok = mbar_wait(&o_done[jl & 1], (jl >> 1) & 1, abort_flag, args.status);
+    if (ok && last >= 0) {
+      ok = mbar_wait(&o_done[grp], (last >> 1) & 1, abort_flag, args.status);
       tc_fence_after();
     }
-    // Merge the halves.  Once the last PV is done no MMA reads shared memory and every K tile has
-    // landed, so K stage 0 holds the exchange of (m_h, l_h).  Every softmax warp reaches the barrier
+    // Merge the groups.  Once the group's last PV is done no MMA reads its P buffer again, so that
+    // buffer holds the group's (m_g, l_g) for the exchange.  Every softmax warp reaches the barrier
     // (all waits above are bounded).
-    float* xch = reinterpret_cast<float*>(sK);   // [2 halves][m | l][128 rows]
-    xch[half * 256 + r] = m;
-    xch[half * 256 + 128 + r] = l;
+    float* xg = reinterpret_cast<float*>(sP + grp * P_BYTES);   // [m | l][128 rows]
+    xg[r] = m;
+    xg[128 + r] = l;
+    tc_fence_before();
     asm volatile("bar.sync 1, %0;" ::"n"(SOFTMAX_THREADS) : "memory");
+    tc_fence_after();
     if (ok) {
-      const float m0 = xch[r], l0 = xch[128 + r], m1 = xch[256 + r], l1 = xch[384 + r];
+      const float* x0 = reinterpret_cast<const float*>(sP);
+      const float* x1 = reinterpret_cast<const float*>(sP + P_BYTES);
+      const float m0 = x0[r], l0 = x0[128 + r], m1 = x1[r], l1 = x1[128 + r];
       const float mm = fmaxf(m0, m1);
-      const float a0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - mm);
-      const float a1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - mm);
+      const bool has1 = n_kv > 1;                // group 1 saw a tile (O_1 was written)
+      const float a0 = fast_exp2(m0 - mm);
+      const float a1 = has1 ? fast_exp2(m1 - mm) : 0.f;
       const float inv = 1.f / (a0 * l0 + a1 * l1);
       const float w0 = a0 * inv, w1 = a1 * inv;
-      // this warp writes output columns [half * HD / 2, half * HD / 2 + HD / 2)
-      __nv_bfloat16* orow = O + (size_t)row * (args.n_heads * HD) + head * HD + half * (HD / 2);
+      // group g writes output columns [g * HD / 2, g * HD / 2 + HD / 2)
+      uint16_t* orow = O + (size_t)row * (args.n_heads * HD) + head * HD + grp * (HD / 2);
 #pragma unroll
       for (int c = 0; c < HD / 2; c += 32) {
         uint32_t o0[32], o1[32];
-        tmem_ld32(t_o + lane_off + half * (HD / 2) + c, o0);
-        tmem_ld32(t_o + HD + lane_off + half * (HD / 2) + c, o1);
+        tmem_ld32(t_o + lane_off + grp * (HD / 2) + c, o0);
+        tmem_ld32(t_o + HD + lane_off + grp * (HD / 2) + c, o1);
         tmem_ld_wait_regs(o0);
         tmem_ld_wait_regs(o1);
         if (row < de) {
@@ -367,9 +438,11 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
           for (int i = 0; i < 32; i += 8) {
             float v[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = __uint_as_float(o0[i + u]) * w0 + __uint_as_float(o1[i + u]) * w1;
-            st_global_v4(orow + c + i, pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
-                         pack_bf16x2(v[6], v[7]));
+            for (int u = 0; u < 8; ++u)
+              v[u] = has1 ? __uint_as_float(o0[i + u]) * w0 + __uint_as_float(o1[i + u]) * w1
+                          : __uint_as_float(o0[i + u]) * w0;
+            st_global_v4(orow + c + i, pack16(f16, v[0], v[1]), pack16(f16, v[2], v[3]), pack16(f16, v[4], v[5]),
+                         pack16(f16, v[6], v[7]));
           }
         }
       }
@@ -483,8 +556,7 @@ cudaError_t attention_launch_t(const void* q, const void* k, const void* vt, voi
   if (!make_tmap_bf16_2d(&tv, vt, args.n_pad, d, (uint64_t)args.n_pad * 2, 64, HD)) return cudaErrorInvalidValue;
   const int grid = args.max_items * args.n_heads;
   if (grid <= 0) return cudaSuccess;
-  attention_kernel<HD><<<grid, ATT_THREADS, AttPlan<HD>::SMEM, stream>>>(tq, tk, tv, static_cast<__nv_bfloat16*>(o),
-                                                                          args);
+  attention_kernel<HD><<<grid, ATT_THREADS, AttPlan<HD>::SMEM, stream>>>(tq, tk, tv, static_cast<uint16_t*>(o), args);
   return cudaGetLastError();
 }
 

@@ -15,7 +15,11 @@ enum : int {
   kDevTimeout = 1 << 0,     // a bounded mbarrier wait ran out; the kernel exited cleanly
   kDevLayout = 1 << 1,      // the packed-layout validator rejected the input
   kDevCapacity = 1 << 2,    // a schedule did not fit its buffer
+  kDevRange = 1 << 3,       // a value stored as an f16 operand was beyond f16's finite range
 };
+
+// Largest finite f16 magnitude: operands stored as f16 beyond it would become inf.
+constexpr float kF16Max = 65504.f;
 
 // Upper bound for one mbarrier wait.  Ordinary waits last microseconds; a wait that reaches this
 // bound means a producer never arrived, so the kernel records kDevTimeout and unwinds.
@@ -61,6 +65,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
       : "r"(addr), "r"(parity)
       : "memory");
   return ok != 0;
+}
+
+// Non-blocking probe: true when the phase of `bar` with the given parity has completed.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+               : "memory");
+  return v;
 }
 
 // Wait for the phase of `bar` with the given parity to complete.  Returns false (after setting
@@ -288,6 +312,15 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ------------------------------------------------------------------------------------------
@@ -296,6 +329,20 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Two values as the 16-bit operand type of the tensor cores: f16 (f16 = true) or bf16.
+__device__ __forceinline__ uint32_t pack16(bool f16, float lo, float hi) {
+  return f16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
+}
+
+__device__ __forceinline__ uint16_t to16(bool f16, float v) {
+  return f16 ? __half_as_ushort(__float2half_rn(v)) : __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {

@@ -30,7 +30,7 @@ __global__ void __launch_bounds__(256) norm_mod_kernel(const float* __restrict__
                                                        const uint8_t* __restrict__ tags,
                                                        const float* __restrict__ shift,
                                                        const float* __restrict__ scale, long long stride, void* y,
-                                                       int out_kind, const int* status) {
+                                                       int out_kind, int* status) {
   if (status && (*reinterpret_cast<const volatile int*>(status) & kDevLayout)) return;
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -89,9 +89,12 @@ __global__ void __launch_bounds__(256) norm_mod_kernel(const float* __restrict__
       o[2] = o[2] * (1.f + m.z) + a.z;
       o[3] = o[3] * (1.f + m.w) + a.w;
     }
-    if (out_kind == 0) {
-      uint2 pk = make_uint2(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]));
-      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(y) + (size_t)row * d + c) = pk;
+    if (out_kind == 0 || out_kind == 2) {
+      const bool f = out_kind == 2;
+      if (f && status && fmaxf(fmaxf(fabsf(o[0]), fabsf(o[1])), fmaxf(fabsf(o[2]), fabsf(o[3]))) > kF16Max)
+        atomicOr(status, kDevRange);
+      uint2 pk = make_uint2(pack16(f, o[0], o[1]), pack16(f, o[2], o[3]));
+      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(y) + (size_t)row * d + c) = pk;
     } else {
       *reinterpret_cast<float4*>(static_cast<float*>(y) + (size_t)row * d + c) = make_float4(o[0], o[1], o[2], o[3]);
     }
@@ -106,7 +109,7 @@ template <int VPT, bool LO>
 __global__ void __launch_bounds__(256) norm_mod_persistent_kernel(
     const float* __restrict__ x, const float* __restrict__ x_lo, int n, int d, int norm, float eps, const float* __restrict__ g,
     const float* __restrict__ b, const uint8_t* __restrict__ tags, const float* __restrict__ shift,
-    const float* __restrict__ scale, long long stride, void* y, int out_kind, const int* status) {
+    const float* __restrict__ scale, long long stride, void* y, int out_kind, int* status) {
   if (status && (*reinterpret_cast<const volatile int*>(status) & kDevLayout)) return;
   __shared__ float red[2][8];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -177,9 +180,12 @@ __global__ void __launch_bounds__(256) norm_mod_persistent_kernel(
         o[2] = o[2] * (1.f + m.z) + a.z;
         o[3] = o[3] * (1.f + m.w) + a.w;
       }
-      if (out_kind == 0) {
-        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(y) + (size_t)row * d + c) =
-            make_uint2(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]));
+      if (out_kind == 0 || out_kind == 2) {
+        const bool f = out_kind == 2;
+        if (f && status && fmaxf(fmaxf(fabsf(o[0]), fabsf(o[1])), fmaxf(fabsf(o[2]), fabsf(o[3]))) > kF16Max)
+          atomicOr(status, kDevRange);
+        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(y) + (size_t)row * d + c) =
+            make_uint2(pack16(f, o[0], o[1]), pack16(f, o[2], o[3]));
       } else {
         *reinterpret_cast<float4*>(static_cast<float*>(y) + (size_t)row * d + c) = make_float4(o[0], o[1], o[2], o[3]);
       }
@@ -323,6 +329,17 @@ __global__ void pack_ffn_in_kernel(const __nv_bfloat16* __restrict__ src, const 
   if (threadIdx.x == 0) b_dst[p] = b_src ? b_src[s] : 0.f;
 }
 
+// bf16 -> f16 in place or into another buffer; a value beyond f16's finite range sets kDevRange.
+__global__ void bf16_to_f16_kernel(const uint16_t* src, uint16_t* dst, long long n, int* flag) {
+  bool over = false;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const float v = __bfloat162float(__ushort_as_bfloat16(src[i]));
+    over |= fabsf(v) > kF16Max;
+    dst[i] = __half_as_ushort(__float2half_rn(v));
+  }
+  if (over) atomicOr(flag, kDevRange);
+}
+
 __global__ void to_f32_kernel(const void* __restrict__ src, int is_bf16, long long n, float* __restrict__ dst) {
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
     dst[i] = is_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(src)[i]) : static_cast<const float*>(src)[i];
@@ -345,7 +362,7 @@ template <int NV>
 cudaError_t norm_launch_t(const float* x, const float* x_lo, int n, int d, int norm, float eps, const float* g,
                           const float* b,
                           const uint8_t* tags, const float* shift, const float* scale, long long stride, void* y,
-                          int out_kind, const int* status, cudaStream_t s) {
+                          int out_kind, int* status, cudaStream_t s) {
   const int rows_per_block = 8;
   norm_mod_kernel<NV><<<(n + rows_per_block - 1) / rows_per_block, 32 * rows_per_block, 0, s>>>(
       x, x_lo, n, d, norm, eps, g, b, tags, shift, scale, stride, y, out_kind, status);
@@ -374,7 +391,7 @@ int num_sms() {
 
 cudaError_t norm_modulate_launch(const float* x, const float* x_lo, int n, int d, int norm, float eps, const float* ln_g,
                                  const float* ln_b, const uint8_t* tags, const float* shift, const float* scale,
-                                 long long mod_stride, void* y, int out_kind, const int* status, cudaStream_t s) {
+                                 long long mod_stride, void* y, int out_kind, int* status, cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
   if (d % 1024 == 0 && d <= 8192) {
     switch (d / 1024) {
@@ -495,6 +512,13 @@ cudaError_t pack_ffn_in_launch(const void* w_in, const float* b_in, int F, int d
 cudaError_t to_f32_launch(const void* src, int src_is_bf16, long long n, float* dst, cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
   to_f32_kernel<<<grid_for(n, 256), 256, 0, s>>>(src, src_is_bf16, n, dst);
+  return cudaGetLastError();
+}
+
+cudaError_t bf16_to_f16_launch(const void* src, void* dst, long long n, int* flag, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  bf16_to_f16_kernel<<<grid_for(n, 256), 256, 0, s>>>(static_cast<const uint16_t*>(src), static_cast<uint16_t*>(dst),
+                                                      n, flag);
   return cudaGetLastError();
 }
 

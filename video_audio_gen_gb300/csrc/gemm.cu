@@ -89,11 +89,6 @@ __device__ __forceinline__ void load_bias4(const float* b, int col, float (&o)[4
   }
 }
 
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-  const __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
-
 // ---------------------------------------------------------------------------------------------
 // epilogues: the calling thread owns tile row `row` (global), TMEM address `t` = its lane, the
 // accumulator's column 0.  n0 = first global output column of the tile.
@@ -149,7 +144,7 @@ __device__ __forceinline__ void store_bf16x16(__nv_bfloat16* o, const float (&v)
 // x = (acc + bias) * rn; out_j = x_j cos_j - x_{j+half} sin_j, out_{j+half} = x_{j+half} cos_j + x_j sin_j.
 template <int W>
 __device__ __forceinline__ void rope_chunk(const GemmArgs& a, uint32_t t, int hb, int c, int half, float rn, bool live,
-                                           const float* cs, const float* sn, __nv_bfloat16* dst, int n0) {
+                                           const float* cs, const float* sn, uint16_t* dst, int n0) {
   uint32_t r1[W], r2[W];
   if constexpr (W == 16) {
     tmem_ld16(t + hb + c, *reinterpret_cast<uint32_t(*)[16]>(r1));
@@ -180,12 +175,13 @@ __device__ __forceinline__ void rope_chunk(const GemmArgs& a, uint32_t t, int hb
       o2[i + j] = x2 * cc[j] + x1 * ss[j];
     }
   }
+  const bool f = a.f16;
 #pragma unroll
   for (int i = 0; i < W; i += 8) {
-    st_global_v4(dst + hb + c + i, pack_bf16x2(o1[i], o1[i + 1]), pack_bf16x2(o1[i + 2], o1[i + 3]),
-                 pack_bf16x2(o1[i + 4], o1[i + 5]), pack_bf16x2(o1[i + 6], o1[i + 7]));
-    st_global_v4(dst + hb + half + c + i, pack_bf16x2(o2[i], o2[i + 1]), pack_bf16x2(o2[i + 2], o2[i + 3]),
-                 pack_bf16x2(o2[i + 4], o2[i + 5]), pack_bf16x2(o2[i + 6], o2[i + 7]));
+    st_global_v4(dst + hb + c + i, pack16(f, o1[i], o1[i + 1]), pack16(f, o1[i + 2], o1[i + 3]),
+                 pack16(f, o1[i + 4], o1[i + 5]), pack16(f, o1[i + 6], o1[i + 7]));
+    st_global_v4(dst + hb + half + c + i, pack16(f, o2[i], o2[i + 1]), pack16(f, o2[i + 2], o2[i + 3]),
+                 pack16(f, o2[i + 4], o2[i + 5]), pack16(f, o2[i + 6], o2[i + 7]));
   }
 }
 
@@ -203,8 +199,9 @@ __device__ __forceinline__ void epi_qkv(const GemmArgs& a, uint32_t t, int row, 
   if (seg == 2) {
     // v is stored transposed; its padding columns [M, n_pad) are written as zeros so that the
     // attention's masked key/value tiles never multiply uninitialised memory (0 * NaN = NaN).
-    __nv_bfloat16* vt = static_cast<__nv_bfloat16*>(a.vt);
+    uint16_t* vt = static_cast<uint16_t*>(a.vt);
     const bool pad = !live && row < a.n_pad;
+    const bool f = a.f16;
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
       uint32_t r[32];
@@ -217,12 +214,12 @@ __device__ __forceinline__ void epi_qkv(const GemmArgs& a, uint32_t t, int row, 
 #pragma unroll
         for (int j = 0; j < 4; ++j)
           vt[(size_t)(col0 + c + i + j) * a.n_pad + row] =
-              __float2bfloat16_rn(live ? __uint_as_float(r[i + j]) * a.w_scale + b[j] : 0.f);
+              to16(f, live ? __uint_as_float(r[i + j]) * a.w_scale + b[j] : 0.f);
       }
     }
     return;
   }
-  __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(seg == 0 ? a.q : a.k) + (size_t)row * a.d + col0;
+  uint16_t* dst = static_cast<uint16_t*>(seg == 0 ? a.q : a.k) + (size_t)row * a.d + col0;
   const int Dh = a.head_dim, half = a.rot_half;
   const float* cs = a.cos_cache + (size_t)row * half;
   const float* sn = a.sin_cache + (size_t)row * half;
@@ -271,7 +268,10 @@ __device__ __forceinline__ void epi_qkv(const GemmArgs& a, uint32_t t, int row, 
 #pragma unroll
         for (int j = 0; j < 4; ++j) o1[i + j] = (__uint_as_float(r1[i + j]) * a.w_scale + b1[j]) * rn;
       }
-      store_bf16x16(dst + hb + c, o1);
+      if (a.f16)
+        store_f16x16(reinterpret_cast<__half*>(dst + hb + c), o1);
+      else
+        store_bf16x16(reinterpret_cast<__nv_bfloat16*>(dst + hb + c), o1);
     }
   }
 }
@@ -360,6 +360,7 @@ __device__ __forceinline__ void epi_swiglu(const GemmArgs& a, uint32_t t, int ro
   const int f0 = n0 / 2;
   __nv_bfloat16* hrow = static_cast<__nv_bfloat16*>(a.out) + (size_t)row * F + f0;
   __half* hrow16 = static_cast<__half*>(a.out) + (size_t)row * F + f0;  // out_kind 2
+  bool over = false;  // an f16 value beyond the finite range
 #pragma unroll 1
   for (int c = 0; c < BN / 2; c += 16) {
     uint32_t ru[16], rg[16];
@@ -381,11 +382,15 @@ __device__ __forceinline__ void epi_swiglu(const GemmArgs& a, uint32_t t, int ro
         h[i + j] = u * silu_f(g);
       }
     }
-    if (a.out_kind == 2)
+    if (a.out_kind == 2) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) over |= fabsf(h[i]) > kF16Max;
       store_f16x16(hrow16 + c, h);
-    else
+    } else {
       store_bf16x16(hrow + c, h);
+    }
   }
+  if (over && a.status) atomicOr(a.status, kDevRange);
 }
 
 // NVFP4 converter: expand row r of a stage's packed weight tile (256 rows x 64
@@ -435,7 +440,7 @@ __global__ void __launch_bounds__(BQ ? Q_THREADS : GEMM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
   constexpr int NST = BQ ? (EPI == kEpiGatedResid ? Q_STAGES_RESID : Q_STAGES) : STAGES;
   constexpr int RING_BYTES = NST * STAGE_BYTES + (BQ ? Q_RAW_SLOTS * Q_RAW_BYTES : 0);
-  constexpr uint32_t ID = BQ ? IDESC_F16 : IDESC;
+  const uint32_t ID = (BQ || args.f16) ? IDESC_F16 : IDESC;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;

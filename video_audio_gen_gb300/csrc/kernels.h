@@ -30,10 +30,11 @@ enum GemmEpilogue : int {
 
 struct GemmArgs {
   int M, N, K;
+  int f16 = 0;             // A, B and the 16-bit outputs of kEpiQkvRope / kEpiSwiglu are f16 (1) or bf16 (0)
   const float* bias;       // [N] or nullptr
   // kEpiStore
   void* out;
-  int out_kind;            // 0 bf16, 1 fp32
+  int out_kind;            // 0 bf16, 1 fp32, 2 f16
   // kEpiQkvRope
   int d, head_dim, rot_half;
   int qk_norm;             // 1: per-head RMS norm of q and k (no affine) before the rotation
@@ -77,6 +78,7 @@ struct AttnArgs {
   int max_items;
   float scale_log2;   // log2(e) / sqrt(Dh)
   int* status;
+  int f16 = 0;        // q, k, vt, P and o are f16 (1) or bf16 (0)
 };
 cudaError_t attention_launch(const void* q, const void* k, const void* vt, void* o, const AttnArgs& args,
                              cudaStream_t stream);
@@ -89,9 +91,10 @@ cudaError_t attention_schedule_launch(const int32_t* cu, int n_docs, int n_token
 int attention_max_items(int n_docs, int n_tokens);
 
 // Elementwise / reduction kernels.
+// out_kind: 0 bf16, 1 fp32, 2 f16 (values beyond f16's finite range set kDevRange in *status).
 cudaError_t norm_modulate_launch(const float* x, const float* x_lo, int n, int d, int norm, float eps, const float* ln_g,
                                  const float* ln_b, const uint8_t* tags, const float* shift, const float* scale,
-                                 long long mod_stride, void* y, int out_kind, const int* status, cudaStream_t s);
+                                 long long mod_stride, void* y, int out_kind, int* status, cudaStream_t s);
 cudaError_t rope_cache_launch(const double* pos, int n, int n_axes, const int* dims, double base, float* cos_out,
                               float* sin_out, const int* status, cudaStream_t s);
 // Timesteps of the AdaLN conditioning: one for every row (n_t = 1), or one per modality (n_t =
@@ -130,6 +133,9 @@ cudaError_t qkv_deinterleave_launch(const void* src, void* dst, int H, int Dh, i
 cudaError_t pack_ffn_in_launch(const void* w_in, const float* b_in, int F, int d, void* w_packed, float* b_packed,
                                cudaStream_t s);
 cudaError_t to_f32_launch(const void* src, int src_is_bf16, long long n, float* dst, cudaStream_t s);
+// bf16 -> f16 (round to nearest even; exact for |v| >= 2^-17 and <= 65504); *flag |= kDevRange when a
+// value is beyond f16's finite range.  src and dst may be the same buffer.
+cudaError_t bf16_to_f16_launch(const void* src, void* dst, long long n, int* flag, cudaStream_t s);
 
 int num_sms();
 bool norm_width_supported(int d);

@@ -13,12 +13,13 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libdit.so")
 
 DIT_OK, DIT_ERR_INVALID_ARG, DIT_ERR_CONFIG, DIT_ERR_UNBOUND, DIT_ERR_MISSING_WEIGHT, DIT_ERR_LAYOUT, \
-    DIT_ERR_CAPACITY, DIT_ERR_CUDA, DIT_ERR_DEVICE_TIMEOUT, DIT_ERR_UNSUPPORTED = range(10)
+    DIT_ERR_CAPACITY, DIT_ERR_CUDA, DIT_ERR_DEVICE_TIMEOUT, DIT_ERR_UNSUPPORTED, DIT_ERR_RANGE = range(11)
 STATUS_NAMES = {0: "DIT_OK", 1: "DIT_ERR_INVALID_ARG", 2: "DIT_ERR_CONFIG", 3: "DIT_ERR_UNBOUND",
                 4: "DIT_ERR_MISSING_WEIGHT", 5: "DIT_ERR_LAYOUT", 6: "DIT_ERR_CAPACITY", 7: "DIT_ERR_CUDA",
-                8: "DIT_ERR_DEVICE_TIMEOUT", 9: "DIT_ERR_UNSUPPORTED"}
+                8: "DIT_ERR_DEVICE_TIMEOUT", 9: "DIT_ERR_UNSUPPORTED", 10: "DIT_ERR_RANGE"}
 DIT_RMSNORM, DIT_LAYERNORM = 0, 1
 DIT_BF16, DIT_FP32 = 0, 1
+DIT_ELEM_BF16, DIT_ELEM_F16 = 0, 1
 KERNEL_KINDS = ["gemm_qkv", "attention", "gemm_out", "gemm_ffn_up", "gemm_ffn_down", "norm_modulate", "other",
                 "latent_io"]
 MAX_LATENT_MODALITIES = 8
@@ -52,7 +53,8 @@ class DitConfig(ctypes.Structure):
                 ("t_embed_dim", ctypes.c_int), ("rope_axes", ctypes.c_int), ("rope_dims", ctypes.c_int * 3),
                 ("rotary_dim", ctypes.c_int), ("rope_base", ctypes.c_double), ("io_channels", ctypes.c_int),
                 ("dtype", ctypes.c_int), ("max_tokens", ctypes.c_int), ("max_docs", ctypes.c_int),
-                ("qk_norm", ctypes.c_int), ("qkv_interleaved", ctypes.c_int), ("final_norm", ctypes.c_int)]
+                ("qk_norm", ctypes.c_int), ("qkv_interleaved", ctypes.c_int), ("final_norm", ctypes.c_int),
+                ("act_bf16", ctypes.c_int)]
 
 
 BLOCK_FIELDS = ["w_qkv", "b_qkv", "w_o", "b_o", "w_in", "b_in", "w_down", "b_down", "w_ada", "b_ada",
@@ -125,10 +127,11 @@ def lib():
             "dit_op_norm_modulate": (i32, [vp, i32, i32, i32, f32, vp, vp, vp, vp, vp, i64, vp, i32, vp]),
             "dit_op_rope_cache": (i32, [vp, i32, i32, ctypes.POINTER(ctypes.c_int), f64, vp, vp, vp]),
             "dit_op_adaln": (i32, [vp, vp, i32, i32, f32, vp, vp]),
-            "dit_op_gemm": (i32, [vp, vp, vp, i32, i32, i32, vp, i32, vp]),
-            "dit_op_gemm_qkv_rope": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, i32, vp]),
-            "dit_op_gemm_gated_residual": (i32, [vp, vp, vp, i32, i32, i32, vp, vp, i64, vp, vp]),
-            "dit_op_gemm_swiglu": (i32, [vp, vp, vp, i32, i32, i32, vp, vp]),
+            "dit_op_gemm": (i32, [vp, vp, vp, i32, i32, i32, vp, i32, i32, vp]),
+            "dit_op_gemm_qkv_rope": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, i32, i32,
+                                           vp]),
+            "dit_op_gemm_gated_residual": (i32, [vp, vp, vp, i32, i32, i32, vp, vp, i64, vp, i32, vp]),
+            "dit_op_gemm_swiglu": (i32, [vp, vp, vp, i32, i32, i32, vp, i32, vp]),
             "dit_op_pack_ffn_in": (i32, [vp, vp, i32, i32, vp, vp, vp]),
             "dit_attention_workspace_bytes": (sz, [i32, i32]),
             "dit_gemm_f32_workspace_bytes": (sz, [i32, i32, i32]),
@@ -136,8 +139,8 @@ def lib():
             "dit_op_pack_nvfp4": (i32, [vp, vp, i32, i32, vp, vp]),
             "dit_op_gemm_nvfp4": (i32, [vp, vp, f32, vp, i32, i32, i32, vp, i32, vp]),
             "dit_op_gemm_f32": (i32, [vp, vp, vp, i32, i32, i32, vp, vp, vp]),
-            "dit_op_attention": (i32, [vp, vp, vp, i32, vp, i32, i32, i32, i32, vp, vp, vp]),
-            "dit_op_attention_noalloc": (i32, [vp, vp, vp, i32, vp, i32, i32, i32, i32, vp, vp]),
+            "dit_op_attention": (i32, [vp, vp, vp, i32, vp, i32, i32, i32, i32, vp, vp, i32, vp]),
+            "dit_op_attention_noalloc": (i32, [vp, vp, vp, i32, vp, i32, i32, i32, i32, vp, i32, vp]),
             "dit_op_attention_noalloc_status": (i32, [vp, vp]),
             "dit_selftest_wait_timeout": (i32, [ctypes.c_uint64, vp, vp]),
         }
@@ -183,6 +186,7 @@ def make_config(m: dict, max_tokens: int, max_docs: int) -> DitConfig:
     c.qk_norm = 1 if m.get("qk_norm") else 0
     c.qkv_interleaved = 1 if m.get("qkv_interleaved") else 0
     c.final_norm = {"same": 0, "rms": 1, "ln": 2}[m.get("final_norm", "same")]
+    c.act_bf16 = 1 if m.get("act_bf16") else 0
     return c
 
 
@@ -377,10 +381,20 @@ def adaln(w, b, t: float, mod, stream=None):
     _check(lib().dit_op_adaln(_ptr(w), _ptr(b), rows, t_dim, float(t), _ptr(mod), _stream(stream)))
 
 
+def elem_of(t) -> int:
+    """DIT_ELEM_F16 for a torch.float16 tensor, DIT_ELEM_BF16 for a torch.bfloat16 one."""
+    import torch
+    if t.dtype == torch.float16:
+        return DIT_ELEM_F16
+    if t.dtype == torch.bfloat16:
+        return DIT_ELEM_BF16
+    raise TypeError(f"16-bit operand expected, got {t.dtype}")
+
+
 def gemm(a, b, bias, out, out_kind: int, stream=None):
     M, K = a.shape
     N = b.shape[0]
-    _check(lib().dit_op_gemm(_ptr(a), _ptr(b), _ptr(bias), M, N, K, _ptr(out), out_kind, _stream(stream)))
+    _check(lib().dit_op_gemm(_ptr(a), _ptr(b), _ptr(bias), M, N, K, _ptr(out), out_kind, elem_of(a), _stream(stream)))
 
 
 def nvfp4_packed_bytes(N: int, K: int) -> int:
@@ -416,20 +430,22 @@ def gemm_qkv_rope(a, b, bias, n_heads, head_dim, rotary_dim, cos_c, sin_c, q, k,
     M, K = a.shape
     d = b.shape[0] // 3
     _check(lib().dit_op_gemm_qkv_rope(_ptr(a), _ptr(b), _ptr(bias), M, d, K, n_heads, head_dim, rotary_dim,
-                                      _ptr(cos_c), _ptr(sin_c), _ptr(q), _ptr(k), _ptr(vt), n_pad, _stream(stream)))
+                                      _ptr(cos_c), _ptr(sin_c), _ptr(q), _ptr(k), _ptr(vt), n_pad, elem_of(a),
+                                      _stream(stream)))
 
 
 def gemm_gated_residual(a, b, bias, x, gate=None, gate_stride=0, tags=None, stream=None):
     M, K = a.shape
     N = b.shape[0]
     _check(lib().dit_op_gemm_gated_residual(_ptr(a), _ptr(b), _ptr(bias), M, N, K, _ptr(x), _ptr(gate),
-                                            int(gate_stride), _ptr(tags), _stream(stream)))
+                                            int(gate_stride), _ptr(tags), elem_of(a), _stream(stream)))
 
 
 def gemm_swiglu(a, b_packed, bias_packed, h, stream=None):
     M, K = a.shape
     F = b_packed.shape[0] // 2
-    _check(lib().dit_op_gemm_swiglu(_ptr(a), _ptr(b_packed), _ptr(bias_packed), M, F, K, _ptr(h), _stream(stream)))
+    _check(lib().dit_op_gemm_swiglu(_ptr(a), _ptr(b_packed), _ptr(bias_packed), M, F, K, _ptr(h), elem_of(a),
+                                    _stream(stream)))
 
 
 def pack_ffn_in(w_in, b_in, w_packed, b_packed, stream=None):
@@ -445,7 +461,7 @@ def attention_workspace_bytes(n_docs: int, n_tokens: int) -> int:
 def attention(q, k, vt, n_pad, cu_seqlens, n_heads, head_dim, o, workspace, stream=None):
     n_tokens = q.shape[0]
     _check(lib().dit_op_attention(_ptr(q), _ptr(k), _ptr(vt), n_pad, _ptr(cu_seqlens), cu_seqlens.numel() - 1,
-                                  n_tokens, n_heads, head_dim, _ptr(o), _ptr(workspace), _stream(stream)))
+                                  n_tokens, n_heads, head_dim, _ptr(o), _ptr(workspace), elem_of(q), _stream(stream)))
 
 
 def attention_noalloc(q, k, vt, n_pad, cu_seqlens, n_heads, head_dim, o, stream=None):
@@ -453,7 +469,7 @@ def attention_noalloc(q, k, vt, n_pad, cu_seqlens, n_heads, head_dim, o, stream=
     (for callers that cannot allocate); calls whose device work overlaps must be serialised."""
     n_tokens = q.shape[0]
     _check(lib().dit_op_attention_noalloc(_ptr(q), _ptr(k), _ptr(vt), n_pad, _ptr(cu_seqlens),
-                                          cu_seqlens.numel() - 1, n_tokens, n_heads, head_dim, _ptr(o),
+                                          cu_seqlens.numel() - 1, n_tokens, n_heads, head_dim, _ptr(o), elem_of(q),
                                           _stream(stream)))
 
 
