@@ -7,30 +7,28 @@
 // One CTA = one (document, 128-row q-tile, head).  Key/value tiles are 128 tokens wide and start
 // at multiples of 128 in the packed sequence (so the TMA x coordinate of the transposed V is
 // 16-byte aligned); columns outside the document are masked to -inf in S and zeroed in V^T.
-//   warp 0     TMA producer: Q once, then K and V^T tiles through two 2-stage rings, polling both
-//              rings so that a K load never queues behind a V load
-//   warp 1     TMEM allocator + S issuer: S(j) = Q K(j)^T into TMEM buffer j % 2, issued as soon as
-//              the softmax has loaded S(j - 2) from that buffer
-//   warp 10    PV issuer: O_{j%2} += P(j) V(j) once P(j) is in shared memory and V(j) has landed (one
-//              barrier counts both); on a document's boundary tiles the warp first zeroes the V^T
-//              columns outside the document, so that a non-finite value in a neighbouring document
-//              cannot reach this one through 0 * inf
+//   warp 0     TMA producer: Q once, then K tiles through a 3-stage ring and V^T tiles through a
+//              2-stage ring, polling both so that a K load never queues behind a V load
+//   warp 1     TMEM allocator + S issuer: S(j) = Q K(j)^T into TMEM buffer j % 2, once K(j) has
+//              landed and O_{j%2} += P(j - 2) V(j - 2) has read the previous contents of the buffer
+//   warp 10    PV issuer: O_{j%2} += P(j) V(j), P read from TMEM (it overwrites S(j) in place), once
+//              the softmax has written P(j) and V(j) has landed (one barrier counts both); on a
+//              document's boundary tiles the warp first zeroes the V^T columns outside the
+//              document, so that a non-finite value in a neighbouring document cannot reach this
+//              one through 0 * inf
 //   warps 2-9  softmax, two groups of four warps (one thread per query row) on alternating tiles:
 //              group g takes the tiles j with j % 2 == g, all 128 key columns of each, and keeps its
 //              own running max m_g, sum l_g and accumulator O_g, exactly as two independent passes
 //              over the even and the odd key tiles would; the groups exchange nothing per tile and
 //              are merged once at the end:
 //                  o = (2^(m_0-m) O_0 + 2^(m_1-m) O_1) / (2^(m_0-m) l_0 + 2^(m_1-m) l_1),  m = max(m_0, m_1)
-//              While one group computes the exponentials of its tile, the other loads its scores
-//              and stores its probabilities, so the exponential unit is busy through both.
+//              While one group loads and exponentiates its scores, the tensor core runs the other
+//              group's P V and next S.
 // Two issuing threads, because one thread's tcgen05.mma issue runs nearly in step with the tensor
-// pipe: whatever else that thread waits on leaves the pipe idle.  With S and PV on separate
-// threads, S(j + 2) runs while group j % 2 works on tile j, and PV(j) while it works on j + 2.
-// The softmax waits for S(j) on "S(j) ready", and for its own previous P(j - 2) V(j - 2) only where it
-// needs it: before it rescales O_{j%2} (rare) or rewrites P buffer j % 2, so that PV runs while the
-// next tile's scores are loaded and reduced.
-// TMEM: S double buffer (2 x 128 columns) + O_0, O_1 (2 x HD columns) <= 512.  P(j) (bf16) goes to
-// shared memory buffer j % 2 in the swizzled K-major layout the PV MMA reads.
+// pipe: whatever else that thread waits on leaves the pipe idle.
+// TMEM: S double buffer (2 x 128 columns; P(j) as 16-bit pairs in the first 64 columns of S(j)'s
+// buffer) + O_0, O_1 (2 x HD columns) <= 512.  With P in TMEM, shared memory holds Q, three K
+// stages and two V^T stages: the third K stage lets K(j + 2) load while S(j) is still being read.
 #include "common.cuh"
 #include "kernels.h"
 #include "tmap.h"
@@ -40,28 +38,29 @@ namespace dit {
 namespace {
 
 constexpr int TQ = 128, TK = 128;
-constexpr int ATOM = 128 * 64 * 2;         // 128 rows x 64 bf16 columns, 128-byte swizzled (16 KB)
-constexpr int P_BYTES = 2 * ATOM;          // P tile: 128 q rows x 128 kv columns
-constexpr int KV_STAGES = 2;
+constexpr int ATOM = 128 * 64 * 2;         // 128 rows x 64 16-bit columns, 128-byte swizzled (16 KB)
+constexpr int K_STAGES = 3;
+constexpr int V_STAGES = 2;
 constexpr int ATT_THREADS = 352;           // producer, S issuer, 8 softmax warps, PV issuer
 constexpr int SOFTMAX_THREADS = 256;
 constexpr int GROUP_WARPS = 4;             // softmax warps per tile group
 constexpr int PV_WARP = 10;
-static_assert(KV_STAGES == 2, "V(j) lands on the barrier of P buffer j % 2");
+static_assert(V_STAGES == 2, "V(j) lands on the barrier of P buffer j % 2");
 
 // Shared-memory plan for head dim HD (64 or 128):
-//   Q  [128 q, HD]   HD/64 atoms of 16 KB          K  [128 kv, HD]  HD/64 atoms of 16 KB
-//   Vt [HD, 128 kv]  2 atoms (kv halves) of HD * 128 bytes each
-//   P  [128 q, 128 kv] x 2 buffers
+//   Q  [128 q, HD]   HD/64 atoms of 16 KB          K  [128 kv, HD]  HD/64 atoms of 16 KB, K_STAGES
+//   Vt [HD, 128 kv]  2 atoms (kv halves) of HD * 128 bytes each, V_STAGES
 template <int HD>
 struct AttPlan {
   static constexpr int Q_BYTES = 128 * HD * 2;
   static constexpr int K_BYTES = 128 * HD * 2;
   static constexpr int V_ATOM = HD * 128;
   static constexpr int V_BYTES = 2 * V_ATOM;
-  static constexpr int SMEM = Q_BYTES + KV_STAGES * (K_BYTES + V_BYTES) + 2 * P_BYTES + 1024 + 256;
+  static constexpr int SMEM = Q_BYTES + K_STAGES * K_BYTES + V_STAGES * V_BYTES + 1024 + 256;
   static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, TK);
   static constexpr uint32_t IDESC_O = idesc_bf16_f32(128, HD);
+  static_assert(SMEM <= 227 * 1024, "attention shared-memory plan");
+  static_assert(Q_BYTES >= 2 * 2 * 128 * 4, "Q's buffer holds the groups' (m, l) exchange");
 };
 
 __device__ __forceinline__ bool wait_noabort(uint64_t* bar, uint32_t parity) {
@@ -116,17 +115,15 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   using Plan = AttPlan<HD>;
   uint8_t* sQ = smem;
-  uint8_t* sK = sQ + Plan::Q_BYTES;                    // [stage]
-  uint8_t* sV = sK + KV_STAGES * Plan::K_BYTES;        // [stage]
-  uint8_t* sP = sV + KV_STAGES * Plan::V_BYTES;        // [2]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * P_BYTES);
+  uint8_t* sK = sQ + Plan::Q_BYTES;                    // [K_STAGES]
+  uint8_t* sV = sK + K_STAGES * Plan::K_BYTES;         // [V_STAGES]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + V_STAGES * Plan::V_BYTES);
   uint64_t* q_full = bars;
-  uint64_t* k_full = bars + 1;                         // [stage]  K tile landed
-  uint64_t* k_empty = k_full + KV_STAGES;              // [stage]  S MMA done with the K tile
-  uint64_t* v_empty = k_empty + KV_STAGES;             // [stage]  PV MMA done with the V^T tile
-  uint64_t* s_full = v_empty + KV_STAGES;              // [2]  S(j) in TMEM
-  uint64_t* s_free = s_full + 2;                       // [2]  softmax has loaded S(j) from its buffer
-  uint64_t* p_full = s_free + 2;                       // [2]  P(j) in shared memory and V(j) landed
+  uint64_t* k_full = bars + 1;                         // [K_STAGES]  K tile landed
+  uint64_t* k_empty = k_full + K_STAGES;               // [K_STAGES]  S MMA done with the K tile
+  uint64_t* v_empty = k_empty + K_STAGES;              // [V_STAGES]  PV MMA done with the V^T tile
+  uint64_t* s_full = v_empty + V_STAGES;               // [2]  S(j) in TMEM
+  uint64_t* p_full = s_full + 2;                       // [2]  P(j) in TMEM and V(j) landed
   uint64_t* o_done = p_full + 2;                       // [2]  O_{j%2} += P(j) V(j) complete
   uint64_t* s_drain = o_done + 2;                      // every S MMA complete
   uint64_t* o_drain = s_drain + 1;                     // every PV MMA complete
@@ -136,14 +133,13 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < KV_STAGES; ++s) {
+    for (int s = 0; s < K_STAGES; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
-      mbar_init(&v_empty[s], 1);
     }
+    for (int s = 0; s < V_STAGES; ++s) mbar_init(&v_empty[s], 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&s_full[s], 1);                          // the S commit
-      mbar_init(&s_free[s], GROUP_WARPS);
       mbar_init(&p_full[s], GROUP_WARPS + 1);            // the group's warps + the V^T load
       mbar_init(&o_done[s], 1);
     }
@@ -157,7 +153,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t t_s = tmem;            // S buffers at columns 0, 128
+  const uint32_t t_s = tmem;            // S buffers at columns 0, 128 (P in the first 64 of each)
   const uint32_t t_o = tmem + 256;      // O_0 at columns [256, 256 + HD), O_1 at [256 + HD, 256 + 2 HD)
 
   if (warp == 0) {
@@ -166,15 +162,15 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       mbar_arrive_expect_tx(q_full, Plan::Q_BYTES);
 #pragma unroll
       for (int a = 0; a < HD / 64; ++a) tma_load_2d(sQ + a * ATOM, &tmQ, q_full, hx + 64 * a, q0);
-      // K(j) needs its stage back from S(j - 2), V(j) from P(j - 2) V(j - 2).  Both rings are polled,
+      // K(j) needs its stage back from S(j - 3), V(j) from P(j - 2) V(j - 2).  Both rings are polled,
       // so each load is issued as soon as its own stage is free.  Each wait is bounded on its own.
       int nk = 0, nv = 0;
       bool ok = true;
       uint64_t t0 = globaltimer_ns();
       for (uint32_t spins = 0; nk < n_kv || nv < n_kv;) {
         bool moved = false;
-        if (nk < n_kv && mbar_test_wait(&k_empty[nk % KV_STAGES], ((nk / KV_STAGES) & 1) ^ 1)) {
-          const int st = nk % KV_STAGES, kv0 = kv_base + nk * TK;
+        if (nk < n_kv && mbar_test_wait(&k_empty[nk % K_STAGES], ((nk / K_STAGES) & 1) ^ 1)) {
+          const int st = nk % K_STAGES, kv0 = kv_base + nk * TK;
           mbar_arrive_expect_tx(&k_full[st], Plan::K_BYTES);
 #pragma unroll
           for (int a = 0; a < HD / 64; ++a)
@@ -182,12 +178,14 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
           ++nk;
           moved = true;
         }
-        if (nv < nk && mbar_test_wait(&v_empty[nv % KV_STAGES], ((nv / KV_STAGES) & 1) ^ 1)) {
-          const int st = nv % KV_STAGES, kv0 = kv_base + nv * TK;
-          // V(j) completes on the barrier that also counts the softmax group's P(j) (stage = j % 2)
-          mbar_arrive_expect_tx(&p_full[st], Plan::V_BYTES);
-          tma_load_2d(sV + st * Plan::V_BYTES, &tmV, &p_full[st], kv0, hx);
-          tma_load_2d(sV + st * Plan::V_BYTES + Plan::V_ATOM, &tmV, &p_full[st], kv0 + 64, hx);
+        if (nv < nk && mbar_test_wait(&v_empty[nv % V_STAGES], ((nv / V_STAGES) & 1) ^ 1)) {
+          // V(j) completes on the barrier that also counts the softmax group's P(j): with two V^T
+          // stages, V(j) is only issued once P(j - 2) V(j - 2) is done, so that barrier's previous
+          // phase (tile j - 2) is complete
+          const int st = nv % V_STAGES, kv0 = kv_base + nv * TK;
+          mbar_arrive_expect_tx(&p_full[nv & 1], Plan::V_BYTES);
+          tma_load_2d(sV + st * Plan::V_BYTES, &tmV, &p_full[nv & 1], kv0, hx);
+          tma_load_2d(sV + st * Plan::V_BYTES + Plan::V_ATOM, &tmV, &p_full[nv & 1], kv0 + 64, hx);
           ++nv;
           moved = true;
         }
@@ -210,22 +208,22 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       }
       // Every copy this CTA issued must land before the CTA may exit.
       wait_noabort(q_full, 0);
-      for (int j = nk - KV_STAGES < 0 ? 0 : nk - KV_STAGES; j < nk; ++j)
-        wait_noabort(&k_full[j % KV_STAGES], (j / KV_STAGES) & 1);
-      for (int j = nv - KV_STAGES < 0 ? 0 : nv - KV_STAGES; j < nv; ++j)
-        wait_noabort(&p_full[j % KV_STAGES], (j / KV_STAGES) & 1);
+      for (int j = nk - K_STAGES < 0 ? 0 : nk - K_STAGES; j < nk; ++j)
+        wait_noabort(&k_full[j % K_STAGES], (j / K_STAGES) & 1);
+      for (int j = nv - V_STAGES < 0 ? 0 : nv - V_STAGES; j < nv; ++j)
+        wait_noabort(&p_full[j & 1], (j >> 1) & 1);
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // S(j) into buffer j % 2 once K(j) has landed and the softmax has loaded S(j - 2) from it.
+      // S(j) into buffer j % 2 once K(j) has landed and P(j - 2) V(j - 2) has read P(j - 2) from it.
       bool ok = mbar_wait(q_full, 0, abort_flag, args.status);
       tc_fence_after();
       const uint32_t q_addr = smem_u32(sQ);
       const uint32_t id_s = args.f16 ? idesc_f16_f32(128, TK) : Plan::IDESC_S;
       for (int j = 0; ok && j < n_kv; ++j) {
-        const int st = j % KV_STAGES, sb = j & 1;
-        if (j >= 2 && !mbar_wait(&s_free[sb], ((j - 2) >> 1) & 1, abort_flag, args.status)) break;
-        if (!mbar_wait(&k_full[st], (j / KV_STAGES) & 1, abort_flag, args.status)) break;
+        const int st = j % K_STAGES, sb = j & 1;
+        if (j >= 2 && !mbar_wait(&o_done[sb], ((j - 2) >> 1) & 1, abort_flag, args.status)) break;
+        if (!mbar_wait(&k_full[st], (j / K_STAGES) & 1, abort_flag, args.status)) break;
         tc_fence_after();
         const uint32_t k_addr = smem_u32(sK + st * Plan::K_BYTES);
 #pragma unroll
@@ -236,13 +234,14 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         umma_commit(&s_full[sb]);
         umma_commit(&k_empty[st]);
       }
-      // No MMA may still read shared memory or write TMEM when the CTA tears down.
+      // No MMA may still read shared memory or write TMEM when the CTA tears down; the softmax
+      // warps also wait for this before they reuse Q's shared memory.
       umma_commit(s_drain);
       wait_noabort(s_drain, 0);
     }
   } else if (warp == PV_WARP) {
     for (int j = 0; j < n_kv; ++j) {
-      const int pb = j & 1, st = j % KV_STAGES;
+      const int pb = j & 1, st = j % V_STAGES;
       bool ok = true;
       if (lane == 0) ok = mbar_wait(&p_full[pb], (j >> 1) & 1, abort_flag, args.status);
       if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
@@ -261,15 +260,14 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       if (lane == 0) {
         tc_fence_after();
         const uint32_t id_o = args.f16 ? idesc_f16_f32(128, HD) : Plan::IDESC_O;
-        const uint32_t p_addr = smem_u32(sP + pb * P_BYTES);
         const uint32_t v_addr = smem_u32(sV + st * Plan::V_BYTES);
 #pragma unroll
         for (int ks = 0; ks < TK / 16; ++ks) {
-          // key columns [0, 64) in P atom 0 / V^T atom 0, [64, 128) in atom 1; all into O_{j%2}
-          const uint32_t p_off = (ks >> 2) * ATOM + (ks & 3) * 32;
+          // P(j): 16 keys per step = 8 TMEM columns of 16-bit pairs; V^T: keys [0, 64) in atom 0,
+          // [64, 128) in atom 1
           const uint32_t v_off = (ks >> 2) * Plan::V_ATOM + (ks & 3) * 32;
-          umma_bf16(t_o + pb * HD, sdesc_sw128(p_addr + p_off), sdesc_sw128(v_addr + v_off), id_o,
-                    (j >= 2 || ks != 0) ? 1u : 0u);
+          umma_bf16_ts(t_o + pb * HD, t_s + pb * TK + ks * 8, sdesc_sw128(v_addr + v_off), id_o,
+                       (j >= 2 || ks != 0) ? 1u : 0u);
         }
         umma_commit(&o_done[pb]);
         umma_commit(&v_empty[st]);
@@ -316,10 +314,6 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       for (int c = 0; c < TK; c += 32) tmem_ld32(ts + c, *reinterpret_cast<uint32_t(*)[32]>(&sv[c]));
 #pragma unroll
       for (int c = 0; c < TK; c += 32) tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&sv[c]));
-      // the scores are in registers: the S issuer may overwrite this buffer with S(j + 2)
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[grp]);
       if (lo > 0 || hi < TK) {
 #pragma unroll
         for (int i = 0; i < TK; ++i)
@@ -337,26 +331,12 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       const float m_cand = fmaxf(fmax3(mx0, mx1, mx2), mx3) * sc;
       // true on the group's first tile (m = -inf until then)
       const bool raise = m_cand > m + kRescaleThreshold;
-      // The group's previous tile, P(j - 2) V(j - 2), must be done before O_g is rescaled or P
-      // buffer j % 2 is rewritten; it runs while this tile's scores are loaded and reduced, and is
-      // waited for only at the first of those two points.
-      bool pv_prev = j < 2;
-      auto wait_pv_prev = [&]() -> bool {
-        if (pv_prev) return true;
-        pv_prev = true;
-        const bool w = mbar_wait(&o_done[grp], ((j - 2) >> 1) & 1, abort_flag, args.status);
-        tc_fence_after();
-        return w;
-      };
       if (__any_sync(0xffffffffu, raise)) {
         const float m_new = raise ? m_cand : m;
         const float alpha = raise ? fast_exp2(m - m_new) : 1.f;  // exp2(-inf) = 0 before the first tile
         if (j >= 2) {
-          // O_g holds the group's sum over its earlier tiles relative to m
-          if (!wait_pv_prev()) {
-            ok = false;
-            break;
-          }
+          // O_g holds the group's sum over its earlier tiles relative to m.  Their last PV,
+          // P(j - 2) V(j - 2), is done: S(j) was issued only after it.
 #pragma unroll 1
           for (int c = 0; c < HD; c += 16) {  // 16 columns at a time: the row's scores stay in registers
             uint32_t ov[16];
@@ -366,36 +346,29 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             for (int i = 0; i < 16; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
             tmem_st16(t_og + c, ov);
           }
-          tmem_st_wait();
         }
         l *= alpha;
         m = m_new;
       }
-      // p = exp2(s * scale - m) -> 16-bit pairs, one 128-byte swizzled row per query row in each of
-      // the two 64-column atoms of P buffer j % 2; paired fp32 arithmetic, two partial row sums
+      // p = exp2(s * scale - m) -> 16-bit pairs written over the first 64 columns of S(j)'s buffer
+      // (the PV MMA's A operand), 32 keys (16 columns) at a time; two partial row sums
       const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-m, -m);
       float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      const uint32_t p_row = smem_u32(sP + grp * P_BYTES) + r * 128;
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {  // 16-byte chunk c of the row: keys [8c, 8c + 8), atom c / 8
-        if (c == 0 && !wait_pv_prev()) {  // P buffer j % 2 is read by P(j - 2) V(j - 2) until it is done
-          ok = false;
-          break;
-        }
-        uint32_t pk[4];
+      for (int c = 0; c < TK / 32; ++c) {
+        uint32_t pk[16];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int i = c * 8 + 2 * u;
+        for (int u = 0; u < 16; ++u) {
+          const int i = c * 32 + 2 * u;
           const float2 x = ffma2(make_float2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), sc2, nm2);
           const float2 e = make_float2(fast_exp2(x.x), fast_exp2(x.y));
           rs[u & 1] = fadd2(rs[u & 1], e);
           pk[u] = pack16(f16, e.x, e.y);
         }
-        st_shared_v4(p_row + (c >> 3) * ATOM + (((c & 7) ^ (r & 7)) << 4), pk[0], pk[1], pk[2], pk[3]);
+        tmem_st16(ts + c * 16, pk);
       }
-      if (!ok) break;
       l += (rs[0].x + rs[0].y) + (rs[1].x + rs[1].y);
-      fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[grp]);
@@ -405,19 +378,17 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       ok = mbar_wait(&o_done[grp], (last >> 1) & 1, abort_flag, args.status);
       tc_fence_after();
     }
-    // Merge the groups.  Once the group's last PV is done no MMA reads its P buffer again, so that
-    // buffer holds the group's (m_g, l_g) for the exchange.  Every softmax warp reaches the barrier
-    // (all waits above are bounded).
-    float* xg = reinterpret_cast<float*>(sP + grp * P_BYTES);   // [m | l][128 rows]
-    xg[r] = m;
-    xg[128 + r] = l;
+    // Merge the groups.  Q's shared memory holds the exchange of (m_g, l_g) once every S MMA is done
+    // (the S issuer's drain).  Every softmax warp reaches the barrier (all waits are bounded).
+    wait_noabort(s_drain, 0);
+    float* xch = reinterpret_cast<float*>(sQ);   // [2 groups][m | l][128 rows]
+    xch[grp * 256 + r] = m;
+    xch[grp * 256 + 128 + r] = l;
     tc_fence_before();
     asm volatile("bar.sync 1, %0;" ::"n"(SOFTMAX_THREADS) : "memory");
     tc_fence_after();
     if (ok) {
-      const float* x0 = reinterpret_cast<const float*>(sP);
-      const float* x1 = reinterpret_cast<const float*>(sP + P_BYTES);
-      const float m0 = x0[r], l0 = x0[128 + r], m1 = x1[r], l1 = x1[128 + r];
+      const float m0 = xch[r], l0 = xch[128 + r], m1 = xch[256 + r], l1 = xch[384 + r];
       const float mm = fmaxf(m0, m1);
       const bool has1 = n_kv > 1;                // group 1 saw a tile (O_1 was written)
       const float a0 = fast_exp2(m0 - mm);
