@@ -7,28 +7,27 @@
 // One CTA = one (document, 128-row q-tile, head).  Key/value tiles are 128 tokens wide and start
 // at multiples of 128 in the packed sequence (so the TMA x coordinate of the transposed V is
 // 16-byte aligned); columns outside the document are masked to -inf in S and zeroed in V^T.
-//   warp 0     TMA producer: Q once, then K tiles through a 3-stage ring and V^T tiles through a
-//              2-stage ring, polling both so that a K load never queues behind a V load
-//   warp 1     TMEM allocator + S issuer: S(j) = Q K(j)^T into TMEM buffer j % 2, once K(j) has
-//              landed and O_{j%2} += P(j - 2) V(j - 2) has read the previous contents of the buffer
-//   warp 10    PV issuer: O_{j%2} += P(j) V(j), P read from TMEM (it overwrites S(j) in place), once
-//              the softmax has written P(j) and V(j) has landed (one barrier counts both); on a
-//              document's boundary tiles the warp first zeroes the V^T columns outside the
+//   warp 0     TMA producer: Q once, then K and V^T tiles through two 2-stage rings
+//   warp 1     TMEM allocator + S issuer: S(j) = Q K(j)^T into TMEM buffer j % 2, issued as soon as
+//              the softmax has loaded S(j - 2) from that buffer
+//   warp 10    PV issuer: O_h += P(j) V(j) once P(j) is in shared memory and V(j) has landed (one
+//              barrier counts both); key columns [0, 64) accumulate into O_0, [64, 128) into O_1.
+//              On a document's boundary tiles the warp first zeroes the V^T columns outside the
 //              document, so that a non-finite value in a neighbouring document cannot reach this
-//              one through 0 * inf
-//   warps 2-9  softmax, two groups of four warps (one thread per query row) on alternating tiles:
-//              group g takes the tiles j with j % 2 == g, all 128 key columns of each, and keeps its
-//              own running max m_g, sum l_g and accumulator O_g, exactly as two independent passes
-//              over the even and the odd key tiles would; the groups exchange nothing per tile and
-//              are merged once at the end:
+//              one through 0 * inf (their softmax weights are exactly 0 already)
+//   warps 2-9  softmax, two warps per query row: warp half h owns key columns [64h, 64h + 64) of
+//              every tile and keeps its own running max m_h, sum l_h and accumulator O_h, exactly as
+//              two independent passes over disjoint key subsets would; the halves exchange nothing
+//              per tile and are merged once at the end:
 //                  o = (2^(m_0-m) O_0 + 2^(m_1-m) O_1) / (2^(m_0-m) l_0 + 2^(m_1-m) l_1),  m = max(m_0, m_1)
-//              While one group loads and exponentiates its scores, the tensor core runs the other
-//              group's P V and next S.
 // Two issuing threads, because one thread's tcgen05.mma issue runs nearly in step with the tensor
-// pipe: whatever else that thread waits on leaves the pipe idle.
-// TMEM: S double buffer (2 x 128 columns; P(j) as 16-bit pairs in the first 64 columns of S(j)'s
-// buffer) + O_0, O_1 (2 x HD columns) <= 512.  With P in TMEM, shared memory holds Q, three K
-// stages and two V^T stages: the third K stage lets K(j + 2) load while S(j) is still being read.
+// pipe: whatever else that thread waits on leaves the pipe idle.  With S and PV on separate
+// threads, S(j + 2) runs while the softmax works on tile j, and PV(j) while it works on j + 1.
+// The softmax waits on one barrier per tile: "S(j) ready" completes only when S(j) is in TMEM and
+// O += P(j - 2) V(j - 2) is done, so it also says that P buffer j % 2 is free.
+// TMEM: S double buffer (2 x 128 columns) + O_0, O_1 (2 x HD columns) <= 512.  P(j) (16-bit, the
+// type of the PV operands) goes to shared memory buffer j % 2 in the swizzled K-major layout the PV
+// MMA reads.
 #include "common.cuh"
 #include "kernels.h"
 #include "tmap.h"
@@ -39,28 +38,26 @@ namespace {
 
 constexpr int TQ = 128, TK = 128;
 constexpr int ATOM = 128 * 64 * 2;         // 128 rows x 64 16-bit columns, 128-byte swizzled (16 KB)
-constexpr int K_STAGES = 3;
-constexpr int V_STAGES = 2;
+constexpr int P_BYTES = 2 * ATOM;          // P tile: 128 q rows x 128 kv columns
+constexpr int KV_STAGES = 2;
 constexpr int ATT_THREADS = 352;           // producer, S issuer, 8 softmax warps, PV issuer
 constexpr int SOFTMAX_THREADS = 256;
-constexpr int GROUP_WARPS = 4;             // softmax warps per tile group
 constexpr int PV_WARP = 10;
-static_assert(V_STAGES == 2, "V(j) lands on the barrier of P buffer j % 2");
+static_assert(KV_STAGES == 2, "V(j) lands on the barrier of P buffer j % 2");
 
 // Shared-memory plan for head dim HD (64 or 128):
-//   Q  [128 q, HD]   HD/64 atoms of 16 KB          K  [128 kv, HD]  HD/64 atoms of 16 KB, K_STAGES
-//   Vt [HD, 128 kv]  2 atoms (kv halves) of HD * 128 bytes each, V_STAGES
+//   Q  [128 q, HD]   HD/64 atoms of 16 KB          K  [128 kv, HD]  HD/64 atoms of 16 KB
+//   Vt [HD, 128 kv]  2 atoms (kv halves) of HD * 128 bytes each
+//   P  [128 q, 128 kv] x 2 buffers
 template <int HD>
 struct AttPlan {
   static constexpr int Q_BYTES = 128 * HD * 2;
   static constexpr int K_BYTES = 128 * HD * 2;
   static constexpr int V_ATOM = HD * 128;
   static constexpr int V_BYTES = 2 * V_ATOM;
-  static constexpr int SMEM = Q_BYTES + K_STAGES * K_BYTES + V_STAGES * V_BYTES + 1024 + 256;
+  static constexpr int SMEM = Q_BYTES + KV_STAGES * (K_BYTES + V_BYTES) + 2 * P_BYTES + 1024 + 256;
   static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, TK);
   static constexpr uint32_t IDESC_O = idesc_bf16_f32(128, HD);
-  static_assert(SMEM <= 227 * 1024, "attention shared-memory plan");
-  static_assert(Q_BYTES >= 2 * 2 * 128 * 4, "Q's buffer holds the groups' (m, l) exchange");
 };
 
 __device__ __forceinline__ bool wait_noabort(uint64_t* bar, uint32_t parity) {
@@ -115,16 +112,18 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   using Plan = AttPlan<HD>;
   uint8_t* sQ = smem;
-  uint8_t* sK = sQ + Plan::Q_BYTES;                    // [K_STAGES]
-  uint8_t* sV = sK + K_STAGES * Plan::K_BYTES;         // [V_STAGES]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + V_STAGES * Plan::V_BYTES);
+  uint8_t* sK = sQ + Plan::Q_BYTES;                    // [stage]
+  uint8_t* sV = sK + KV_STAGES * Plan::K_BYTES;        // [stage]
+  uint8_t* sP = sV + KV_STAGES * Plan::V_BYTES;        // [2]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * P_BYTES);
   uint64_t* q_full = bars;
-  uint64_t* k_full = bars + 1;                         // [K_STAGES]  K tile landed
-  uint64_t* k_empty = k_full + K_STAGES;               // [K_STAGES]  S MMA done with the K tile
-  uint64_t* v_empty = k_empty + K_STAGES;              // [V_STAGES]  PV MMA done with the V^T tile
-  uint64_t* s_full = v_empty + V_STAGES;               // [2]  S(j) in TMEM
-  uint64_t* p_full = s_full + 2;                       // [2]  P(j) in TMEM and V(j) landed
-  uint64_t* o_done = p_full + 2;                       // [2]  O_{j%2} += P(j) V(j) complete
+  uint64_t* k_full = bars + 1;                         // [stage]  K tile landed
+  uint64_t* k_empty = k_full + KV_STAGES;              // [stage]  S MMA done with the K tile
+  uint64_t* v_empty = k_empty + KV_STAGES;             // [stage]  PV MMA done with the V^T tile
+  uint64_t* s_full = v_empty + KV_STAGES;              // [2]  S(j) in TMEM and P(j - 2) V(j - 2) done
+  uint64_t* s_free = s_full + 2;                       // [2]  softmax has loaded S(j) from its buffer
+  uint64_t* p_full = s_free + 2;                       // [2]  P(j) in shared memory and V(j) landed
+  uint64_t* o_done = p_full + 2;                       // [2]  O += P(j) V(j) complete
   uint64_t* s_drain = o_done + 2;                      // every S MMA complete
   uint64_t* o_drain = s_drain + 1;                     // every PV MMA complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_drain + 1);
@@ -133,14 +132,15 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < K_STAGES; ++s) {
+    for (int s = 0; s < KV_STAGES; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
-    for (int s = 0; s < V_STAGES; ++s) mbar_init(&v_empty[s], 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&s_full[s], 1);                          // the S commit
-      mbar_init(&p_full[s], GROUP_WARPS + 1);            // the group's warps + the V^T load
+      mbar_init(&s_full[s], 2);                          // S commit + PV commit of tile j - 2
+      mbar_init(&s_free[s], SOFTMAX_THREADS / 32);
+      mbar_init(&p_full[s], SOFTMAX_THREADS / 32 + 1);   // softmax warps + the V^T load
       mbar_init(&o_done[s], 1);
     }
     mbar_init(s_drain, 1);
@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t t_s = tmem;            // S buffers at columns 0, 128 (P in the first 64 of each)
+  const uint32_t t_s = tmem;            // S buffers at columns 0, 128
   const uint32_t t_o = tmem + 256;      // O_0 at columns [256, 256 + HD), O_1 at [256 + HD, 256 + 2 HD)
 
   if (warp == 0) {
@@ -162,68 +162,58 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       mbar_arrive_expect_tx(q_full, Plan::Q_BYTES);
 #pragma unroll
       for (int a = 0; a < HD / 64; ++a) tma_load_2d(sQ + a * ATOM, &tmQ, q_full, hx + 64 * a, q0);
-      // K(j) needs its stage back from S(j - 3), V(j) from P(j - 2) V(j - 2).  Both rings are polled,
-      // so each load is issued as soon as its own stage is free.  Each wait is bounded on its own.
+      // K tiles run two ahead of the V tiles: K(j) waits for S(j - KV_STAGES), V(j) for
+      // P(j - KV_STAGES) V(j - KV_STAGES).
+      auto load_k = [&](int j) -> bool {
+        const int st = j % KV_STAGES;
+        if (!mbar_wait(&k_empty[st], ((j / KV_STAGES) & 1) ^ 1, abort_flag, args.status)) return false;
+        const int kv0 = kv_base + j * TK;
+        mbar_arrive_expect_tx(&k_full[st], Plan::K_BYTES);
+#pragma unroll
+        for (int a = 0; a < HD / 64; ++a)
+          tma_load_2d(sK + st * Plan::K_BYTES + a * ATOM, &tmK, &k_full[st], hx + 64 * a, kv0);
+        return true;
+      };
+      auto load_v = [&](int j) -> bool {
+        const int st = j % KV_STAGES;
+        if (!mbar_wait(&v_empty[st], ((j / KV_STAGES) & 1) ^ 1, abort_flag, args.status)) return false;
+        const int kv0 = kv_base + j * TK;
+        // V(j) completes on the barrier that also counts the softmax warps' P(j) (stage = j % 2)
+        mbar_arrive_expect_tx(&p_full[st], Plan::V_BYTES);
+        tma_load_2d(sV + st * Plan::V_BYTES, &tmV, &p_full[st], kv0, hx);
+        tma_load_2d(sV + st * Plan::V_BYTES + Plan::V_ATOM, &tmV, &p_full[st], kv0 + 64, hx);
+        return true;
+      };
       int nk = 0, nv = 0;
       bool ok = true;
-      uint64_t t0 = globaltimer_ns();
-      for (uint32_t spins = 0; nk < n_kv || nv < n_kv;) {
-        bool moved = false;
-        if (nk < n_kv && mbar_test_wait(&k_empty[nk % K_STAGES], ((nk / K_STAGES) & 1) ^ 1)) {
-          const int st = nk % K_STAGES, kv0 = kv_base + nk * TK;
-          mbar_arrive_expect_tx(&k_full[st], Plan::K_BYTES);
-#pragma unroll
-          for (int a = 0; a < HD / 64; ++a)
-            tma_load_2d(sK + st * Plan::K_BYTES + a * ATOM, &tmK, &k_full[st], hx + 64 * a, kv0);
-          ++nk;
-          moved = true;
-        }
-        if (nv < nk && mbar_test_wait(&v_empty[nv % V_STAGES], ((nv / V_STAGES) & 1) ^ 1)) {
-          // V(j) completes on the barrier that also counts the softmax group's P(j): with two V^T
-          // stages, V(j) is only issued once P(j - 2) V(j - 2) is done, so that barrier's previous
-          // phase (tile j - 2) is complete
-          const int st = nv % V_STAGES, kv0 = kv_base + nv * TK;
-          mbar_arrive_expect_tx(&p_full[nv & 1], Plan::V_BYTES);
-          tma_load_2d(sV + st * Plan::V_BYTES, &tmV, &p_full[nv & 1], kv0, hx);
-          tma_load_2d(sV + st * Plan::V_BYTES + Plan::V_ATOM, &tmV, &p_full[nv & 1], kv0 + 64, hx);
-          ++nv;
-          moved = true;
-        }
-        if (moved) {
-          t0 = globaltimer_ns();
-          spins = 0;
-          continue;
-        }
-        __nanosleep(32);  // a short yield: this thread shares its scheduler with softmax warps
-        if ((++spins & 255u) == 0) {
-          if (*abort_flag) {
-            ok = false;
-          } else if (globaltimer_ns() - t0 > kWaitLimitNs) {
-            *abort_flag = 1;
-            if (args.status) atomicOr(args.status, kDevTimeout);
-            ok = false;
-          }
-          if (!ok) break;
+      for (; ok && nk < n_kv && nk < 2; ++nk) ok = load_k(nk);
+      while (ok && nv < n_kv) {
+        ok = load_v(nv);
+        if (!ok) break;
+        ++nv;
+        if (nk < n_kv) {
+          ok = load_k(nk);
+          if (ok) ++nk;
         }
       }
       // Every copy this CTA issued must land before the CTA may exit.
       wait_noabort(q_full, 0);
-      for (int j = nk - K_STAGES < 0 ? 0 : nk - K_STAGES; j < nk; ++j)
-        wait_noabort(&k_full[j % K_STAGES], (j / K_STAGES) & 1);
-      for (int j = nv - V_STAGES < 0 ? 0 : nv - V_STAGES; j < nv; ++j)
-        wait_noabort(&p_full[j & 1], (j >> 1) & 1);
+      for (int j = nk - KV_STAGES < 0 ? 0 : nk - KV_STAGES; j < nk; ++j)
+        wait_noabort(&k_full[j % KV_STAGES], (j / KV_STAGES) & 1);
+      for (int j = nv - KV_STAGES < 0 ? 0 : nv - KV_STAGES; j < nv; ++j)
+        wait_noabort(&p_full[j % KV_STAGES], (j / KV_STAGES) & 1);
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // S(j) into buffer j % 2 once K(j) has landed and P(j - 2) V(j - 2) has read P(j - 2) from it.
+      // S(j) into buffer j % 2 once K(j) has landed and the softmax has loaded S(j - 2) from it.
       bool ok = mbar_wait(q_full, 0, abort_flag, args.status);
       tc_fence_after();
       const uint32_t q_addr = smem_u32(sQ);
       const uint32_t id_s = args.f16 ? idesc_f16_f32(128, TK) : Plan::IDESC_S;
       for (int j = 0; ok && j < n_kv; ++j) {
-        const int st = j % K_STAGES, sb = j & 1;
-        if (j >= 2 && !mbar_wait(&o_done[sb], ((j - 2) >> 1) & 1, abort_flag, args.status)) break;
-        if (!mbar_wait(&k_full[st], (j / K_STAGES) & 1, abort_flag, args.status)) break;
+        const int st = j % KV_STAGES, sb = j & 1;
+        if (j >= 2 && !mbar_wait(&s_free[sb], ((j - 2) >> 1) & 1, abort_flag, args.status)) break;
+        if (!mbar_wait(&k_full[st], (j / KV_STAGES) & 1, abort_flag, args.status)) break;
         tc_fence_after();
         const uint32_t k_addr = smem_u32(sK + st * Plan::K_BYTES);
 #pragma unroll
@@ -234,14 +224,18 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         umma_commit(&s_full[sb]);
         umma_commit(&k_empty[st]);
       }
-      // No MMA may still read shared memory or write TMEM when the CTA tears down; the softmax
-      // warps also wait for this before they reuse Q's shared memory.
+      // No MMA may still read shared memory or write TMEM when the CTA tears down.
       umma_commit(s_drain);
       wait_noabort(s_drain, 0);
     }
   } else if (warp == PV_WARP) {
+    // tiles 0 and 1 have no PV two tiles back: their "S ready" phases get that arrival now
+    if (lane == 0) {
+      mbar_arrive(&s_full[0]);
+      mbar_arrive(&s_full[1]);
+    }
     for (int j = 0; j < n_kv; ++j) {
-      const int pb = j & 1, st = j % V_STAGES;
+      const int pb = j & 1, st = j % KV_STAGES;
       bool ok = true;
       if (lane == 0) ok = mbar_wait(&p_full[pb], (j >> 1) & 1, abort_flag, args.status);
       if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
@@ -260,17 +254,19 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       if (lane == 0) {
         tc_fence_after();
         const uint32_t id_o = args.f16 ? idesc_f16_f32(128, HD) : Plan::IDESC_O;
+        const uint32_t p_addr = smem_u32(sP + pb * P_BYTES);
         const uint32_t v_addr = smem_u32(sV + st * Plan::V_BYTES);
 #pragma unroll
         for (int ks = 0; ks < TK / 16; ++ks) {
-          // P(j): 16 keys per step = 8 TMEM columns of 16-bit pairs; V^T: keys [0, 64) in atom 0,
-          // [64, 128) in atom 1
+          // key columns [0, 64) (P atom 0, V^T atom 0) -> O_0; [64, 128) (atom 1) -> O_1
+          const uint32_t p_off = (ks >> 2) * ATOM + (ks & 3) * 32;
           const uint32_t v_off = (ks >> 2) * Plan::V_ATOM + (ks & 3) * 32;
-          umma_bf16_ts(t_o + pb * HD, t_s + pb * TK + ks * 8, sdesc_sw128(v_addr + v_off), id_o,
-                       (j >= 2 || ks != 0) ? 1u : 0u);
+          umma_bf16(t_o + (ks >> 2) * HD, sdesc_sw128(p_addr + p_off), sdesc_sw128(v_addr + v_off), id_o,
+                    (j | (ks & 3)) != 0);
         }
         umma_commit(&o_done[pb]);
         umma_commit(&v_empty[st]);
+        umma_commit(&s_full[pb]);                          // the second arrival of "S(j + 2) ready"
       }
       __syncwarp();
     }
@@ -280,128 +276,140 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     }
   } else {
     // ---------------- softmax warps ----------------
-    // Group g = (warp - 2) / 4 takes tiles j = g, g + 2, ...; TMEM lane quarter = warp % 4 (the rows a
-    // warp may access), one thread per query row and all 128 key columns of the tile.  O_g accumulates
-    // in TMEM through the MMA; the running max m_g is only raised (and O_g, l_g rescaled by
-    // exp2(m_old - m_new)) when the row max grows by more than 2^8, so most tiles never touch O_g.
-    // Between raises p = exp2(s * scale - m_g) stays below 2^8.  Every key tile holds at least one
-    // key of the document, so m_g is finite after the group's first tile.
+    // Two warps per row: TMEM lane quarter = warp % 4 (the rows a warp may access), key-column half
+    // = (warp - 2) / 4.  O_h accumulates in TMEM through the MMA; the running max m_h is only raised
+    // (and O_h, l_h rescaled by exp2(m_old - m_new)) when the half-row max grows by more than 2^8,
+    // so most tiles never touch O_h.  Between raises p = exp2(s * scale - m_h) stays below 2^8.
+    constexpr int HC = TK / 2;                   // key columns per half
     const int quarter = warp & 3;
-    const int grp = (warp - 2) >> 2;
+    const int half = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;           // tile row owned by this thread
     const int row = q0 + r;                      // packed-sequence row
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t t_og = t_o + grp * HD + lane_off;
-    const uint32_t ts = t_s + grp * TK + lane_off;
+    const uint32_t t_oh = t_o + half * HD + lane_off;
     const float sc = args.scale_log2;
     const bool f16 = args.f16;                   // P and o as f16 (else bf16)
     constexpr float kRescaleThreshold = 8.0f;    // log2 units
     float m = -INFINITY, l = 0.f;
     bool ok = true;
-    int last = -1;
 
-    for (int j = grp; j < n_kv; j += 2) {
-      if (!mbar_wait(&s_full[grp], (j >> 1) & 1, abort_flag, args.status)) {
+    for (int j = 0; j < n_kv; ++j) {
+      const int sb = j & 1;
+      if (!mbar_wait(&s_full[sb], (j >> 1) & 1, abort_flag, args.status)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const int c0 = kv_base + j * TK;
+      const int c0 = kv_base + j * TK + half * HC;
       const int lo = ds > c0 ? ds - c0 : 0;
-      const int hi = de - c0 < TK ? de - c0 : TK;
-      uint32_t sv[TK];
+      const int hi = de - c0 < HC ? de - c0 : HC;
+      const bool interior = (lo == 0) && (hi == HC);
+      const uint32_t ts = t_s + sb * TK + half * HC + lane_off;
+      uint32_t sv[HC];
 #pragma unroll
-      for (int c = 0; c < TK; c += 32) tmem_ld32(ts + c, *reinterpret_cast<uint32_t(*)[32]>(&sv[c]));
+      for (int c = 0; c < HC; c += 32) tmem_ld32(ts + c, *reinterpret_cast<uint32_t(*)[32]>(&sv[c]));
 #pragma unroll
-      for (int c = 0; c < TK; c += 32) tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&sv[c]));
-      if (lo > 0 || hi < TK) {
+      for (int c = 0; c < HC; c += 32) tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&sv[c]));
+      // the scores are in registers: the S issuer may overwrite this buffer with S(j + 2)
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[sb]);
+      if (!interior) {
 #pragma unroll
-        for (int i = 0; i < TK; ++i)
+        for (int i = 0; i < HC; ++i)
           if (i < lo || i >= hi) sv[i] = __float_as_uint(-INFINITY);
       }
-      // row max: four independent chains of three-input max
+      // half-row max: four independent chains of three-input max
       float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < TK; i += 8) {
+      for (int i = 0; i < HC; i += 8) {
         mx0 = fmax3(mx0, __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]));
         mx1 = fmax3(mx1, __uint_as_float(sv[i + 2]), __uint_as_float(sv[i + 3]));
         mx2 = fmax3(mx2, __uint_as_float(sv[i + 4]), __uint_as_float(sv[i + 5]));
         mx3 = fmax3(mx3, __uint_as_float(sv[i + 6]), __uint_as_float(sv[i + 7]));
       }
       const float m_cand = fmaxf(fmax3(mx0, mx1, mx2), mx3) * sc;
-      // true on the group's first tile (m = -inf until then)
+      // true on the first tile with a key of the document in this half (m = -inf until then)
       const bool raise = m_cand > m + kRescaleThreshold;
       if (__any_sync(0xffffffffu, raise)) {
         const float m_new = raise ? m_cand : m;
-        const float alpha = raise ? fast_exp2(m - m_new) : 1.f;  // exp2(-inf) = 0 before the first tile
-        if (j >= 2) {
-          // O_g holds the group's sum over its earlier tiles relative to m.  Their last PV,
-          // P(j - 2) V(j - 2), is done: S(j) was issued only after it.
-#pragma unroll 1
-          for (int c = 0; c < HD; c += 16) {  // 16 columns at a time: the row's scores stay in registers
-            uint32_t ov[16];
-            tmem_ld16(t_og + c, ov);
-            tmem_ld_wait_regs(ov);
+        const float alpha = raise ? fast_exp2(m - m_new) : 1.f;  // exp2(-inf) = 0 before the first key
+        if (j > 0) {
+          // O_h holds this half's sum over tiles < j relative to m: wait for the last PV, rescale
+          if (!mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, args.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-            tmem_st16(t_og + c, ov);
+          for (int c = 0; c < HD; c += 32) {
+            uint32_t ov[32];
+            tmem_ld32_sync(t_oh + c, ov);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+            tmem_st32(t_oh + c, ov);
+            tmem_st_wait();
           }
         }
         l *= alpha;
         m = m_new;
       }
-      // p = exp2(s * scale - m) -> 16-bit pairs written over the first 64 columns of S(j)'s buffer
-      // (the PV MMA's A operand), 32 keys (16 columns) at a time; two partial row sums
-      const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-m, -m);
-      float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      // A half that has seen no key of the document yet has m = -inf and only masked scores:
+      // p = exp2(-inf - 0) = 0 keeps O_h and l_h at zero.
+      const float mu = m == -INFINITY ? 0.f : m;
+      // p = exp2(s * scale - m) -> 16-bit pairs; this half's 64 columns are exactly P atom `half` of
+      // shared-memory buffer j % 2, one 128-byte swizzled row per query row
+      uint32_t pk[HC / 2];
+      // paired fp32 arithmetic (one f32x2 FMA / add per two scores); four partial row sums
+      const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-mu, -mu);
+      float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-      for (int c = 0; c < TK / 32; ++c) {
-        uint32_t pk[16];
+      for (int c = 0; c < HC; c += 8) {
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const int i = c * 32 + 2 * u;
-          const float2 x = ffma2(make_float2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), sc2, nm2);
+        for (int u = 0; u < 4; ++u) {
+          const float2 x = ffma2(make_float2(__uint_as_float(sv[c + 2 * u]), __uint_as_float(sv[c + 2 * u + 1])), sc2, nm2);
           const float2 e = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-          rs[u & 1] = fadd2(rs[u & 1], e);
-          pk[u] = pack16(f16, e.x, e.y);
+          rs[u] = fadd2(rs[u], e);
+          pk[c / 2 + u] = pack16(f16, e.x, e.y);
         }
-        tmem_st16(ts + c * 16, pk);
       }
-      l += (rs[0].x + rs[0].y) + (rs[1].x + rs[1].y);
-      tmem_st_wait();
+      l += (rs[0].x + rs[0].y + rs[1].x + rs[1].y) + (rs[2].x + rs[2].y + rs[3].x + rs[3].y);
+      // P buffer j % 2 is free: "S(j) ready" included O += P(j - 2) V(j - 2) being done
+      const uint32_t p_row = smem_u32(sP + sb * P_BYTES + half * ATOM) + r * 128;
+#pragma unroll
+      for (int c = 0; c < HC / 8; ++c)
+        st_shared_v4(p_row + ((c ^ (r & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[grp]);
-      last = j;
+      if (lane == 0) mbar_arrive(&p_full[sb]);
     }
-    if (ok && last >= 0) {
-      ok = mbar_wait(&o_done[grp], (last >> 1) & 1, abort_flag, args.status);
+    if (ok && n_kv > 0) {
+      const int jl = n_kv - 1;
+      ok = mbar_wait(&o_done[jl & 1], (jl >> 1) & 1, abort_flag, args.status);
       tc_fence_after();
     }
-    // Merge the groups.  Q's shared memory holds the exchange of (m_g, l_g) once every S MMA is done
-    // (the S issuer's drain).  Every softmax warp reaches the barrier (all waits are bounded).
-    wait_noabort(s_drain, 0);
-    float* xch = reinterpret_cast<float*>(sQ);   // [2 groups][m | l][128 rows]
-    xch[grp * 256 + r] = m;
-    xch[grp * 256 + 128 + r] = l;
-    tc_fence_before();
+    // Merge the halves.  Once the last PV is done no MMA reads shared memory and every K tile has
+    // landed, so K stage 0 holds the exchange of (m_h, l_h).  Every softmax warp reaches the barrier
+    // (all waits above are bounded).
+    float* xch = reinterpret_cast<float*>(sK);   // [2 halves][m | l][128 rows]
+    xch[half * 256 + r] = m;
+    xch[half * 256 + 128 + r] = l;
     asm volatile("bar.sync 1, %0;" ::"n"(SOFTMAX_THREADS) : "memory");
-    tc_fence_after();
     if (ok) {
       const float m0 = xch[r], l0 = xch[128 + r], m1 = xch[256 + r], l1 = xch[384 + r];
       const float mm = fmaxf(m0, m1);
-      const bool has1 = n_kv > 1;                // group 1 saw a tile (O_1 was written)
-      const float a0 = fast_exp2(m0 - mm);
-      const float a1 = has1 ? fast_exp2(m1 - mm) : 0.f;
+      const float a0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - mm);
+      const float a1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - mm);
       const float inv = 1.f / (a0 * l0 + a1 * l1);
       const float w0 = a0 * inv, w1 = a1 * inv;
-      // group g writes output columns [g * HD / 2, g * HD / 2 + HD / 2)
-      uint16_t* orow = O + (size_t)row * (args.n_heads * HD) + head * HD + grp * (HD / 2);
+      // this warp writes output columns [half * HD / 2, half * HD / 2 + HD / 2)
+      uint16_t* orow = O + (size_t)row * (args.n_heads * HD) + head * HD + half * (HD / 2);
 #pragma unroll
       for (int c = 0; c < HD / 2; c += 32) {
         uint32_t o0[32], o1[32];
-        tmem_ld32(t_o + lane_off + grp * (HD / 2) + c, o0);
-        tmem_ld32(t_o + HD + lane_off + grp * (HD / 2) + c, o1);
+        tmem_ld32(t_o + lane_off + half * (HD / 2) + c, o0);
+        tmem_ld32(t_o + HD + lane_off + half * (HD / 2) + c, o1);
         tmem_ld_wait_regs(o0);
         tmem_ld_wait_regs(o1);
         if (row < de) {
@@ -409,9 +417,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
           for (int i = 0; i < 32; i += 8) {
             float v[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-              v[u] = has1 ? __uint_as_float(o0[i + u]) * w0 + __uint_as_float(o1[i + u]) * w1
-                          : __uint_as_float(o0[i + u]) * w0;
+            for (int u = 0; u < 8; ++u) v[u] = __uint_as_float(o0[i + u]) * w0 + __uint_as_float(o1[i + u]) * w1;
             st_global_v4(orow + c + i, pack16(f16, v[0], v[1]), pack16(f16, v[2], v[3]), pack16(f16, v[4], v[5]),
                          pack16(f16, v[6], v[7]));
           }
