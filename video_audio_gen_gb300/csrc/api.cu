@@ -31,8 +31,15 @@ struct SplitW {
   float* lo = nullptr;
 };
 
+// An fp32 weight as the 3xF16 GEMM reads it: f16 (hi, lo) parts of W 2^e and the exponent e (device).
+struct SplitW16 {
+  uint16_t* hi = nullptr;
+  uint16_t* lo = nullptr;
+  int* e = nullptr;
+};
+
 struct BlockDev {
-  SplitW s_qkv, s_o, s_in, s_down;  // fp32 path
+  SplitW16 s_qkv, s_o, s_in, s_down;  // fp32 path
   const void* w_qkv = nullptr;
   const void* w_o = nullptr;
   const void* w_down = nullptr;
@@ -76,7 +83,7 @@ struct dit_handle {
   // fp32 path: final LayerNorm and the 1x1 pre/post convolutions
   float *lnf_g = nullptr, *lnf_b = nullptr, *b_pre = nullptr, *b_post = nullptr;
   const float *w_pre = nullptr, *w_post = nullptr;
-  SplitW s_pre, s_post;  // fp32 path: the 1x1 convolutions' weights split for the 3xTF32 GEMM
+  SplitW16 s_pre, s_post;  // fp32 path: the 1x1 convolutions' weights split for the 3xF16 GEMM
   // latent I/O (dit_bind_latent_io): per modality the patch projection [d][kp] and the output head
   // [np][d] split for the 3xTF32 GEMM, zero-padded to the GEMM's K chunk and N tile
   int lat_n = 0;
@@ -342,20 +349,26 @@ dit_status bind_fp32(dit_handle* h, const dit_weights* w, cudaStream_t s) {
     e = src ? to_f32_launch(src, 0, n, dst, s) : cudaMemsetAsync(dst, 0, n * 4, s);
     return e == cudaSuccess ? dst : nullptr;
   };
-  // tf32 (hi, lo) copies of every fp32 linear weight, read by the 3xTF32 GEMM
-  auto split = [&](const void* src, long long n, SplitW* out) -> bool {
-    out->hi = static_cast<float*>(dev_alloc(h, n * 4, &e));
-    if (e != cudaSuccess) return false;
-    out->lo = static_cast<float*>(dev_alloc(h, n * 4, &e));
-    if (e != cudaSuccess) return false;
-    e = tf32_split_launch(static_cast<const float*>(src), (size_t)n, out->hi, out->lo, s);
+  // f16 (hi, lo) copies of every fp32 linear weight [rows, K] scaled by its own power of two, read by
+  // the 3xF16 GEMM: 4 bytes per weight, as the fp32 weight itself
+  unsigned int* maxbuf = static_cast<unsigned int*>(dev_alloc(h, 16, &e));
+  if (e != cudaSuccess) return cuda_err(h, e, "bind: alloc");
+  auto split = [&](const void* src, long long rows, int K, SplitW16* out) -> bool {
+    const size_t n = (size_t)rows * K;
+    out->hi = static_cast<uint16_t*>(dev_alloc(h, n * 2, &e));
+    if (e == cudaSuccess) out->lo = static_cast<uint16_t*>(dev_alloc(h, n * 2, &e));
+    if (e == cudaSuccess) out->e = static_cast<int*>(dev_alloc(h, 16, &e));
+    if (e == cudaSuccess) e = absmax_launch(static_cast<const float*>(src), n, maxbuf, s);
+    if (e == cudaSuccess)
+      e = f16_split_launch(static_cast<const float*>(src), K, K, (int)rows, K, maxbuf, 0, out->e, out->hi, out->lo,
+                           nullptr, s);
     return e == cudaSuccess;
   };
   for (int l = 0; l < c.n_blocks; ++l) {
     const dit_block_weights& b = w->blocks[l];
     BlockDev& bd = h->blocks[l];
-    if (!split(b.w_qkv, 3ll * d * d, &bd.s_qkv) || !split(b.w_o, (long long)d * d, &bd.s_o) ||
-        !split(b.w_in, 2ll * F * d, &bd.s_in) || !split(b.w_down, (long long)d * F, &bd.s_down))
+    if (!split(b.w_qkv, 3ll * d, d, &bd.s_qkv) || !split(b.w_o, d, d, &bd.s_o) ||
+        !split(b.w_in, 2ll * F, d, &bd.s_in) || !split(b.w_down, d, F, &bd.s_down))
       return cuda_err(h, e, "bind: split fp32 weights");
     bd.w_qkv = b.w_qkv;
     bd.w_o = b.w_o;
@@ -376,7 +389,7 @@ dit_status bind_fp32(dit_handle* h, const dit_weights* w, cudaStream_t s) {
   if (io) {
     h->w_pre = static_cast<const float*>(w->w_pre);
     h->w_post = static_cast<const float*>(w->w_post);
-    if (!split(w->w_pre, (long long)d * io, &h->s_pre) || !split(w->w_post, (long long)io * d, &h->s_post))
+    if (!split(w->w_pre, d, io, &h->s_pre) || !split(w->w_post, io, d, &h->s_post))
       return cuda_err(h, e, "bind: split conv weights");
     h->b_pre = vec(w->b_pre, d, true);
     h->b_post = vec(w->b_post, io, true);
@@ -387,22 +400,22 @@ dit_status bind_fp32(dit_handle* h, const dit_weights* w, cudaStream_t s) {
   return DIT_OK;
 }
 
-// One fp32 GEMM of the forward: the input split into tf32 (hi, lo), the 3xTF32 partial sums, then
-// (by the caller) the fixed-order reduction that applies the epilogue.
+// One fp32 GEMM of the forward: the input split into f16 (hi, lo) parts of x 2^4, the 3xF16 partial
+// sums, then (by the caller) the fixed-order reduction that applies the epilogue.
 struct Sgemm {
   dit_handle* h;
   cudaStream_t s;
   float* part;
-  float* x_hi;
-  float* x_lo;
-  const int* status;
+  uint16_t* x_hi;
+  uint16_t* x_lo;
+  int* status;
   int S;  // effective splits of the last partial launch
-  cudaError_t run(const float* X, const SplitW& W, int M, int N, int K) {
-    cudaError_t e = tf32_split_launch(X, (size_t)M * K, x_hi, x_lo, s);
+  cudaError_t run(const float* X, const SplitW16& W, int M, int N, int K) {
+    cudaError_t e = f16_split_launch(X, K, K, M, K, nullptr, kF16x3ActExp, nullptr, x_hi, x_lo, status, s);
     if (e != cudaSuccess) return e;
-    const int want = tf32x3_splits(M, N, K);
-    S = tf32x3_effective_splits(K, want);
-    return tf32x3_partial_launch(x_hi, x_lo, W.hi, W.lo, M, N, K, want, part, status, s);
+    const int want = f16x3_splits(M, N, K);
+    S = f16x3_effective_splits(K, want);
+    return f16x3_partial_launch(x_hi, x_lo, W.hi, W.lo, W.e, kF16x3ActExp, M, N, K, want, part, status, s);
   }
 };
 
@@ -425,7 +438,8 @@ dit_status forward_fp32(dit_handle* h, const float* x_tokens, const int32_t* cu_
   float* o = at<float>(workspace, L.o);
   float* hb = at<float>(workspace, L.h);
   float* xt = at<float>(workspace, L.mod);
-  Sgemm g{h, s, at<float>(workspace, L.part), at<float>(workspace, L.xs_hi), at<float>(workspace, L.xs_lo), status, 1};
+  Sgemm g{h, s, at<float>(workspace, L.part), at<uint16_t>(workspace, L.xs_hi), at<uint16_t>(workspace, L.xs_lo),
+          status, 1};
   {
     Launch ln(h, s, 6);
     DIT_CK(h, cudaMemsetAsync(sw, 0, sizeof(StatusWords), s), "status reset");
@@ -1420,21 +1434,25 @@ dit_status dit_op_pack_ffn_in(const void* w_in, const float* b_in, int F, int d,
 
 namespace {
 struct GemmF32Ws {
-  size_t x_hi, x_lo, w_hi, w_lo, part, total;
+  size_t x_hi, x_lo, w_hi, w_lo, part, maxbits, w_exp, total;
+  int Kp;
 };
 GemmF32Ws gemm_f32_ws(int M, int N, int K) {
   GemmF32Ws w{};
+  w.Kp = (K + kF16x3K - 1) / kF16x3K * kF16x3K;  // zero-padded to the GEMM's K step
   size_t off = 0;
   auto take = [&](size_t bytes) {
     size_t o = off;
     off = align_up(off + bytes);
     return o;
   };
-  w.x_hi = take((size_t)M * K * 4);
-  w.x_lo = take((size_t)M * K * 4);
-  w.w_hi = take((size_t)N * K * 4);
-  w.w_lo = take((size_t)N * K * 4);
+  w.x_hi = take((size_t)M * w.Kp * 2);
+  w.x_lo = take((size_t)M * w.Kp * 2);
+  w.w_hi = take((size_t)N * w.Kp * 2);
+  w.w_lo = take((size_t)N * w.Kp * 2);
   w.part = take((size_t)kSgemmMaxSplits * M * N * 4);
+  w.maxbits = take(16);
+  w.w_exp = take(16);
   w.total = off;
   return w;
 }
@@ -1452,17 +1470,22 @@ dit_status dit_op_gemm_f32(const float* x, const float* w, const float* bias, in
     return set_err(nullptr, DIT_ERR_INVALID_ARG, "fp32 GEMM needs M >= 1, N %% 128 == 0, K %% 32 == 0, aligned pointers");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const GemmF32Ws L = gemm_f32_ws(M, N, K);
-  float* x_hi = at<float>(workspace, L.x_hi);
-  float* x_lo = at<float>(workspace, L.x_lo);
-  float* w_hi = at<float>(workspace, L.w_hi);
-  float* w_lo = at<float>(workspace, L.w_lo);
+  const int Kp = L.Kp;
+  uint16_t* x_hi = at<uint16_t>(workspace, L.x_hi);
+  uint16_t* x_lo = at<uint16_t>(workspace, L.x_lo);
+  uint16_t* w_hi = at<uint16_t>(workspace, L.w_hi);
+  uint16_t* w_lo = at<uint16_t>(workspace, L.w_lo);
   float* part = at<float>(workspace, L.part);
-  cudaError_t e = tf32_split_launch(x, (size_t)M * K, x_hi, x_lo, s);
-  if (e == cudaSuccess) e = tf32_split_launch(w, (size_t)N * K, w_hi, w_lo, s);
-  const int want = tf32x3_splits(M, N, K);
-  if (e == cudaSuccess) e = tf32x3_partial_launch(x_hi, x_lo, w_hi, w_lo, M, N, K, want, part, nullptr, s);
+  unsigned int* maxbits = at<unsigned int>(workspace, L.maxbits);
+  int* w_exp = at<int>(workspace, L.w_exp);
+  cudaError_t e = f16_split_launch(x, K, K, M, Kp, nullptr, kF16x3ActExp, nullptr, x_hi, x_lo, nullptr, s);
+  if (e == cudaSuccess) e = absmax_launch(w, (size_t)N * K, maxbits, s);
+  if (e == cudaSuccess) e = f16_split_launch(w, K, K, N, Kp, maxbits, 0, w_exp, w_hi, w_lo, nullptr, s);
+  const int want = f16x3_splits(M, N, Kp);
   if (e == cudaSuccess)
-    e = sgemm_reduce_store_launch(part, tf32x3_effective_splits(K, want), M, N, bias, y, 0, nullptr, nullptr, s);
+    e = f16x3_partial_launch(x_hi, x_lo, w_hi, w_lo, w_exp, kF16x3ActExp, M, N, Kp, want, part, nullptr, s);
+  if (e == cudaSuccess)
+    e = sgemm_reduce_store_launch(part, f16x3_effective_splits(Kp, want), M, N, bias, y, 0, nullptr, nullptr, s);
   return e == cudaSuccess ? DIT_OK : cuda_err(nullptr, e, "fp32 gemm");
 }
 

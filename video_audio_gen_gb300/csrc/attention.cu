@@ -93,7 +93,9 @@ __device__ __forceinline__ void zero_v_outside(uint8_t* sv_tile, int lo, int hi,
   }
 }
 
-template <int HD>
+// F16: the 16-bit operand type (q, k, V^T, P and o) is f16, else bf16.  A template parameter, so that
+// the softmax's conversions are one instruction per pair with no select.
+template <int HD, bool F16>
 __global__ void __launch_bounds__(ATT_THREADS, 1)
     attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, uint16_t* __restrict__ O, const AttnArgs args) {
@@ -209,7 +211,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       bool ok = mbar_wait(q_full, 0, abort_flag, args.status);
       tc_fence_after();
       const uint32_t q_addr = smem_u32(sQ);
-      const uint32_t id_s = args.f16 ? idesc_f16_f32(128, TK) : Plan::IDESC_S;
+      constexpr uint32_t id_s = F16 ? idesc_f16_f32(128, TK) : Plan::IDESC_S;
       for (int j = 0; ok && j < n_kv; ++j) {
         const int st = j % KV_STAGES, sb = j & 1;
         if (j >= 2 && !mbar_wait(&s_free[sb], ((j - 2) >> 1) & 1, abort_flag, args.status)) break;
@@ -253,7 +255,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       __syncwarp();
       if (lane == 0) {
         tc_fence_after();
-        const uint32_t id_o = args.f16 ? idesc_f16_f32(128, HD) : Plan::IDESC_O;
+        constexpr uint32_t id_o = F16 ? idesc_f16_f32(128, HD) : Plan::IDESC_O;
         const uint32_t p_addr = smem_u32(sP + pb * P_BYTES);
         const uint32_t v_addr = smem_u32(sV + st * Plan::V_BYTES);
 #pragma unroll
@@ -288,7 +290,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t t_oh = t_o + half * HD + lane_off;
     const float sc = args.scale_log2;
-    const bool f16 = args.f16;                   // P and o as f16 (else bf16)
+    constexpr bool f16 = F16;                    // P and o as f16 (else bf16)
     constexpr float kRescaleThreshold = 8.0f;    // log2 units
     float m = -INFINITY, l = 0.f;
     bool ok = true;
@@ -502,7 +504,7 @@ __global__ void schedule_kernel(const int32_t* cu, int n_docs, int n_tokens, con
 
 int attention_max_items_impl(int n_docs, int n_tokens) { return (n_tokens + ITEM_ROWS - 1) / ITEM_ROWS + n_docs; }
 
-template <int HD>
+template <int HD, bool F16>
 cudaError_t attention_launch_t(const void* q, const void* k, const void* vt, void* o, const AttnArgs& args,
                                cudaStream_t stream);
 
@@ -520,11 +522,12 @@ cudaError_t attention_schedule_launch(const int32_t* cu, int n_docs, int n_token
 
 namespace {
 
-template <int HD>
+template <int HD, bool F16>
 cudaError_t attention_launch_t(const void* q, const void* k, const void* vt, void* o, const AttnArgs& args,
                                cudaStream_t stream) {
   static unsigned long long smem_set = 0;
-  cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(attention_kernel<HD>), AttPlan<HD>::SMEM, &smem_set);
+  cudaError_t e =
+      opt_in_smem(reinterpret_cast<const void*>(attention_kernel<HD, F16>), AttPlan<HD>::SMEM, &smem_set);
   if (e != cudaSuccess) return e;
   const int d = args.n_heads * HD;
   CUtensorMap tq, tk, tv;
@@ -533,7 +536,8 @@ cudaError_t attention_launch_t(const void* q, const void* k, const void* vt, voi
   if (!make_tmap_bf16_2d(&tv, vt, args.n_pad, d, (uint64_t)args.n_pad * 2, 64, HD)) return cudaErrorInvalidValue;
   const int grid = args.max_items * args.n_heads;
   if (grid <= 0) return cudaSuccess;
-  attention_kernel<HD><<<grid, ATT_THREADS, AttPlan<HD>::SMEM, stream>>>(tq, tk, tv, static_cast<uint16_t*>(o), args);
+  attention_kernel<HD, F16><<<grid, ATT_THREADS, AttPlan<HD>::SMEM, stream>>>(tq, tk, tv, static_cast<uint16_t*>(o),
+                                                                               args);
   return cudaGetLastError();
 }
 
@@ -541,8 +545,12 @@ cudaError_t attention_launch_t(const void* q, const void* k, const void* vt, voi
 
 cudaError_t attention_launch(const void* q, const void* k, const void* vt, void* o, const AttnArgs& args,
                              cudaStream_t stream) {
-  if (args.head_dim == 128) return attention_launch_t<128>(q, k, vt, o, args, stream);
-  if (args.head_dim == 64) return attention_launch_t<64>(q, k, vt, o, args, stream);
+  if (args.head_dim == 128)
+    return args.f16 ? attention_launch_t<128, true>(q, k, vt, o, args, stream)
+                    : attention_launch_t<128, false>(q, k, vt, o, args, stream);
+  if (args.head_dim == 64)
+    return args.f16 ? attention_launch_t<64, true>(q, k, vt, o, args, stream)
+                    : attention_launch_t<64, false>(q, k, vt, o, args, stream);
   return cudaErrorInvalidValue;
 }
 

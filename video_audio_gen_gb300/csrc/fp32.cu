@@ -3,9 +3,12 @@
 // value * silu(gate), 1x1 pre/post convolutions as MatmulBT on the frame-major activation).
 // A single TF32 product would round operands to 10 mantissa bits, far above the 1e-5 tolerance;
 // three of them on split operands (3xTF32) keep fp32-level accuracy on the tensor cores:
-//   tf32_split_kernel       x -> tf32(x), tf32(x - tf32(x)) (weights once at bind, activations per GEMM)
-//   tf32x3_partial_kernel   tcgen05 kind::tf32, 32-deep accumulation chunks summed in fp32; split-K,
-//                           each split writes its partial sums to a [S][M][N] buffer
+//   tf32_split_kernel       x -> tf32(x), tf32(x - tf32(x)) (the latent islands' operands)
+//   f16_split_kernel        x -> f16 hi and lo parts of x * 2^e (the forward's operands: weights once
+//                           at bind with a per-tensor e, activations per GEMM with a fixed e)
+//   x3_partial_kernel       three products per fp32 product on the tcgen05 tensor cores, kind::tf32
+//                           or kind::f16, 12-MMA accumulation chunks summed in fp32; split-K, each
+//                           split writes its partial sums to a [S][M][N] buffer
 //   sgemm_reduce_*          sums the S partials in a fixed order and applies the epilogue (bias,
 //                           residual add, NeoX RoPE + q/k/v split, value * silu(gate))
 //   attention_f32_kernel    one warp per (query row, head), exact fp32 online softmax with expf
@@ -159,45 +162,58 @@ __global__ void io_transpose_kernel(const float* __restrict__ src, float* __rest
 }
 
 // ------------------------------------------------------------------------------------------
-// 3xTF32 partial GEMM on the tcgen05 tensor cores.  Every fp32 operand x is split once into
-// x_hi = tf32(x) and x_lo = tf32(x - x_hi) (round to nearest), and
+// Three-product partial GEMM on the tcgen05 tensor cores.  Every fp32 operand x is split into a high
+// and a low part of a narrower type T, x ~ x_hi + x_lo, and
 //     a . b  ~=  a_hi b_hi + a_hi b_lo + a_lo b_hi
-// drops only a_lo b_lo and the tf32 rounding of the low parts, about 2^-21 of |a b| per product.
+// drops only a_lo b_lo and the rounding of the low parts, about 2^-21 of |a b| per product when T
+// has an 11-bit significand.  Two types serve:
+//   tf32 (kind::tf32, 32 K per 128-byte row): x_hi = tf32(x), x_lo = tf32(x - x_hi)
+//   f16  (kind::f16,  64 K per 128-byte row): x_hi = f16(x 2^e), x_lo = f16(x 2^e - x_hi), with e
+//        chosen so that both parts stay in f16's normal range (per weight tensor from its largest
+//        magnitude; a fixed e for activations); the sums are scaled back by 2^-(e_w + e_x), exactly.
+//        kind::f16 runs at twice the tf32 rate and its two parts take 4 bytes per weight, so the
+//        weight stream is half of tf32's.
 // The tensor core's fp32 accumulation of these products is biased (measured on GB300: the error
 // of a TMEM accumulation grows linearly with its depth, about 2e-5 relative at K = 2048), so the
-// MMAs accumulate only 32-deep chunks, alternately into two TMEM accumulators, and the epilogue
-// adds each chunk into fp32 running sums in registers (round to nearest), much as the FFMA path's
-// 64-deep chunks did.  The roles are transposed so that the small token count sits on the MMA's
-// N side: one CTA owns 128 output features (M = 128 rows of W) x NT tokens (N = NT <= 256, all
-// the tokens of a music forward in one tile) x one K split, and writes part[split][token][feature]
-// for the same fixed-order reductions as before.
-//   warp 0     TMA producer: W_hi, W_lo [128 x 32] and X_hi, X_lo [NT x 32] per 32-deep stage
+// MMAs accumulate only one stage (12 MMAs: 4 K-steps x 3 products), alternately into two TMEM
+// accumulators, and the epilogue adds each chunk into fp32 running sums in registers (round to
+// nearest).  The roles are transposed so that the small token count sits on the MMA's N side: one
+// CTA owns 128 output features (M = 128 rows of W) x NT tokens (N = NT <= 256, all the tokens of a
+// music forward in one tile) x one K split, and writes part[split][token][feature] for the same
+// fixed-order reductions as before.
+//   warp 0     TMA producer: W_hi, W_lo [128 x 128 B] and X_hi, X_lo [NT x 128 B] per stage
 //   warp 1     TMEM allocator + MMA issuer: 4 K-steps x 3 products per stage, one stage per chunk
 //   warps 2-9  epilogue: TMEM lane = feature, column = token; two warps per lane quarter split the
 //              token columns; running sums in registers, coalesced stores along features
-constexpr int T3_BK = kTf32x3K;           // K per stage: one 128-byte swizzled row of fp32
-constexpr int T3_ROWS = kTf32x3N;         // output features per CTA (MMA M)
+constexpr int T3_ROW_BYTES = 128;                 // one 128-byte swizzled row of K per stage
+constexpr int T3_ROWS = kTf32x3N;                 // output features per CTA (MMA M)
 constexpr int T3_STAGES = 2;
-constexpr int T3_CHUNK = 1;               // stages per accumulation chunk (32-deep)
-constexpr int T3_W_BYTES = T3_ROWS * T3_BK * 4;  // 16 KB
+constexpr int T3_CHUNK = 1;                       // stages per accumulation chunk
+constexpr int T3_W_BYTES = T3_ROWS * T3_ROW_BYTES;  // 16 KB
 constexpr int T3_THREADS = 320;
-constexpr int T3_MAX_UNITS = 8;           // 16-column units per epilogue warp (NT <= 256)
+constexpr int T3_MAX_UNITS = 8;                   // 16-column units per epilogue warp (NT <= 256)
+constexpr int X3_F16_BK = 64;                     // K per stage, f16
+constexpr int X3_TF32_BK = kTf32x3K;              // K per stage, tf32 (32)
 
 struct T3Args {
   int M, N, K, k_split, nt;
   float* part;
   int* status;
+  const int* w_exp;  // f16: the weight's scale exponent (device); the sums are scaled by 2^-(w_exp + x_exp)
+  int x_exp;
 };
 
+template <bool F16>
 __global__ void __launch_bounds__(T3_THREADS, 1)
-    tf32x3_partial_kernel(const __grid_constant__ CUtensorMap tmWhi, const __grid_constant__ CUtensorMap tmWlo,
-                          const __grid_constant__ CUtensorMap tmXhi, const __grid_constant__ CUtensorMap tmXlo,
-                          const T3Args a) {
+    x3_partial_kernel(const __grid_constant__ CUtensorMap tmWhi, const __grid_constant__ CUtensorMap tmWlo,
+                      const __grid_constant__ CUtensorMap tmXhi, const __grid_constant__ CUtensorMap tmXlo,
+                      const T3Args a) {
+  constexpr int T3_BK = F16 ? X3_F16_BK : X3_TF32_BK;  // K elements per stage
   if (a.status && (*reinterpret_cast<const volatile int*>(a.status) & kDevLayout)) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int nt = a.nt;
-  const int x_bytes = nt * T3_BK * 4;
+  const int x_bytes = nt * T3_ROW_BYTES;
   const int stage_bytes = 2 * T3_W_BYTES + 2 * x_bytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + T3_STAGES * stage_bytes);
   uint64_t* empty = full + T3_STAGES;
@@ -251,7 +267,7 @@ __global__ void __launch_bounds__(T3_THREADS, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t idesc = idesc_tf32_f32(T3_ROWS, nt);
+      const uint32_t idesc = F16 ? idesc_f16_f32(T3_ROWS, nt) : idesc_tf32_f32(T3_ROWS, nt);
       for (int i = 0; i < n_kb; ++i) {
         const int st = i % T3_STAGES;
         const int c = i / T3_CHUNK, cb = c & 1;
@@ -267,16 +283,23 @@ __global__ void __launch_bounds__(T3_THREADS, 1)
         const uint32_t xlo = xhi + x_bytes;
         // The small cross terms go first, while the accumulator is still about 2^-11 of its final
         // size (their rounding is then negligible); the four hi x hi products come last.
+        // 32 bytes per instruction: K = 8 tf32 or 16 f16
+        auto mma = [&](uint32_t w, uint32_t x, uint32_t accumulate) {
+          if (F16)
+            umma_bf16(acc, sdesc_sw128(w), sdesc_sw128(x), idesc, accumulate);
+          else
+            umma_tf32(acc, sdesc_sw128(w), sdesc_sw128(x), idesc, accumulate);
+        };
 #pragma unroll
-        for (int ks = 0; ks < T3_BK / 8; ++ks) {
-          const uint32_t off = ks * 32;  // K = 8 fp32 per instruction
-          umma_tf32(acc, sdesc_sw128(whi + off), sdesc_sw128(xlo + off), idesc, !(chunk_start && ks == 0));
-          umma_tf32(acc, sdesc_sw128(wlo + off), sdesc_sw128(xhi + off), idesc, 1);
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint32_t off = ks * 32;
+          mma(whi + off, xlo + off, !(chunk_start && ks == 0));
+          mma(wlo + off, xhi + off, 1);
         }
 #pragma unroll
-        for (int ks = 0; ks < T3_BK / 8; ++ks) {
+        for (int ks = 0; ks < 4; ++ks) {
           const uint32_t off = ks * 32;
-          umma_tf32(acc, sdesc_sw128(whi + off), sdesc_sw128(xhi + off), idesc, 1);
+          mma(whi + off, xhi + off, 1);
         }
         umma_commit(&empty[st]);
         if (chunk_end) umma_commit(&chunk_full[cb]);
@@ -315,6 +338,8 @@ __global__ void __launch_bounds__(T3_THREADS, 1)
       if (lane == 0) mbar_arrive(&chunk_empty[cb]);
     }
     if (ok) {
+      // f16: undo the operands' power-of-two scales (exact)
+      const float osc = (F16 && a.w_exp) ? ldexpf(1.f, -(*a.w_exp + a.x_exp)) : 1.f;
       float* dst = a.part + (size_t)split * a.M * a.N + n0 + quarter * 32 + lane;
 #pragma unroll
       for (int u = 0; u < T3_MAX_UNITS; ++u) {
@@ -322,7 +347,7 @@ __global__ void __launch_bounds__(T3_THREADS, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int m = m0 + (u0 + u) * 16 + j;
-            if (m < a.M) dst[(size_t)m * a.N] = run[u * 16 + j];
+            if (m < a.M) dst[(size_t)m * a.N] = run[u * 16 + j] * osc;
           }
         }
       }
@@ -369,6 +394,50 @@ __global__ void tf32_split_rows_kernel(const float* __restrict__ x, long long ld
   }
 }
 
+// Largest magnitude of x, as the bits of a non-negative float (they order like the values).
+__global__ void absmax_kernel(const float* __restrict__ x, size_t n, unsigned int* __restrict__ out) {
+  unsigned int m = 0;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+    m = max(m, __float_as_uint(fabsf(x[i])));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
+  if ((threadIdx.x & 31) == 0) atomicMax(out, m);
+}
+
+// The scale exponent e of a weight tensor from its largest magnitude: max * 2^e in [2^14, 2^15), so
+// the high parts stay below f16's largest finite value (65504) and the low parts of all but the
+// smallest weights stay normal.  e = 0 for an all-zero tensor.
+__device__ __forceinline__ int weight_exp(unsigned int max_bits) {
+  if (max_bits == 0 || max_bits >= 0x7F800000u) return 0;
+  const int ex = (int)(max_bits >> 23) - 127;  // floor(log2(max)) for a normal max
+  const int e = 14 - ex;
+  return e < -100 ? -100 : (e > 100 ? 100 : e);
+}
+
+// x [M][K] (row stride ldx) -> hi, lo [M][Kp] f16 bits of x * 2^e, zero-padded for k >= K:
+//   hi = f16(x 2^e), lo = f16(x 2^e - hi)     (round to nearest even)
+// e is the weight exponent of *max_bits when given (and then written to *e_out by block 0), else
+// e_fixed.  A magnitude of x 2^e beyond 65504 sets kDevRange in *status.
+__global__ void f16_split_kernel(const float* __restrict__ x, long long ldx, int K, int M, int Kp,
+                                 const unsigned int* __restrict__ max_bits, int e_fixed, int* __restrict__ e_out,
+                                 uint16_t* __restrict__ hi, uint16_t* __restrict__ lo, int* status) {
+  if (status && (*reinterpret_cast<const volatile int*>(status) & kDevLayout)) return;
+  const int e = max_bits ? weight_exp(*max_bits) : e_fixed;
+  if (e_out && blockIdx.x == 0 && threadIdx.x == 0) *e_out = e;
+  const size_t n = (size_t)M * Kp;
+  bool over = false;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const int r = (int)(i / Kp), k = (int)(i - (size_t)r * Kp);
+    const float v = k < K ? ldexpf(x[(size_t)r * ldx + k], e) : 0.f;
+    over |= fabsf(v) > kF16Max;
+    const __half h = __float2half_rn(v);
+    const __half l = __float2half_rn(__fsub_rn(v, __half2float(h)));
+    hi[i] = __half_as_ushort(h);
+    lo[i] = __half_as_ushort(l);
+  }
+  if (over && status) atomicOr(status, kDevRange);
+}
+
 // out[(rows ? rows[r] : r) * ld_out + n] = sum over S partials [S][M][Np] + bias[n], n < n_out:
 // the row-scattered, column-trimmed store of a GEMM whose N was padded to Np.
 __global__ void sgemm_reduce_rows_kernel(const float* __restrict__ part, int S, int M, int Np, int n_out,
@@ -397,43 +466,85 @@ int tf32x3_token_tile(int M) {
   return m16 < 256 ? (m16 < 32 ? 32 : m16) : 256;
 }
 
-int tf32x3_splits(int M, int N, int K) {
+static int x3_splits(int M, int N, int K, int bk) {
   const int tiles = (N / T3_ROWS) * ((M + tf32x3_token_tile(M) - 1) / tf32x3_token_tile(M));
   int S = (2 * num_sms() + tiles - 1) / tiles;  // about two waves of one CTA per SM
-  const int max_s = K / T3_BK > 0 ? K / T3_BK : 1;
+  const int max_s = K / bk > 0 ? K / bk : 1;
   if (S > max_s) S = max_s;
   if (S > kSgemmMaxSplits) S = kSgemmMaxSplits;
   return S < 1 ? 1 : S;
 }
 
-int tf32x3_effective_splits(int K, int S) {
+static int x3_effective_splits(int K, int S, int bk) {
   int ks = (K + S - 1) / S;
-  ks = (ks + T3_BK - 1) / T3_BK * T3_BK;
+  ks = (ks + bk - 1) / bk * bk;
   return (K + ks - 1) / ks;
+}
+
+int tf32x3_splits(int M, int N, int K) { return x3_splits(M, N, K, X3_TF32_BK); }
+int tf32x3_effective_splits(int K, int S) { return x3_effective_splits(K, S, X3_TF32_BK); }
+int f16x3_splits(int M, int N, int K) { return x3_splits(M, N, K, X3_F16_BK); }
+int f16x3_effective_splits(int K, int S) { return x3_effective_splits(K, S, X3_F16_BK); }
+
+template <bool F16>
+static cudaError_t x3_partial_launch(const void* x_hi, const void* x_lo, const void* w_hi, const void* w_lo,
+                                     const int* w_exp, int x_exp, int M, int N, int K, int S, float* part,
+                                     const int* status, cudaStream_t s) {
+  constexpr int BK = F16 ? X3_F16_BK : X3_TF32_BK;
+  if (M <= 0) return cudaSuccess;
+  if (N % T3_ROWS || K % BK) return cudaErrorInvalidValue;
+  const int nt = tf32x3_token_tile(M);
+  int ks = (K + S - 1) / S;
+  ks = (ks + BK - 1) / BK * BK;
+  const int S_eff = (K + ks - 1) / ks;
+  CUtensorMap whi, wlo, xhi, xlo;
+  bool ok;
+  if (F16)
+    ok = make_tmap_bf16_2d(&whi, w_hi, K, N, (uint64_t)K * 2, BK, T3_ROWS) &&
+         make_tmap_bf16_2d(&wlo, w_lo, K, N, (uint64_t)K * 2, BK, T3_ROWS) &&
+         make_tmap_bf16_2d(&xhi, x_hi, K, M, (uint64_t)K * 2, BK, nt) &&
+         make_tmap_bf16_2d(&xlo, x_lo, K, M, (uint64_t)K * 2, BK, nt);
+  else
+    ok = make_tmap_f32_2d(&whi, w_hi, K, N, (uint64_t)K * 4, T3_ROWS) &&
+         make_tmap_f32_2d(&wlo, w_lo, K, N, (uint64_t)K * 4, T3_ROWS) &&
+         make_tmap_f32_2d(&xhi, x_hi, K, M, (uint64_t)K * 4, nt) &&
+         make_tmap_f32_2d(&xlo, x_lo, K, M, (uint64_t)K * 4, nt);
+  if (!ok) return cudaErrorInvalidValue;
+  const int smem = T3_STAGES * (2 * T3_W_BYTES + 2 * nt * T3_ROW_BYTES) + 1024 + 256;
+  static unsigned long long smem_set = 0;  // opted in to the largest plan (NT = 256) once per device
+  cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(x3_partial_kernel<F16>),
+                              T3_STAGES * (2 * T3_W_BYTES + 2 * 256 * T3_ROW_BYTES) + 1024 + 256, &smem_set);
+  if (e != cudaSuccess) return e;
+  T3Args a{M, N, K, ks, nt, part, const_cast<int*>(status), w_exp, x_exp};
+  dim3 grid(N / T3_ROWS, (M + nt - 1) / nt, S_eff);
+  x3_partial_kernel<F16><<<grid, T3_THREADS, smem, s>>>(whi, wlo, xhi, xlo, a);
+  return cudaGetLastError();
 }
 
 cudaError_t tf32x3_partial_launch(const float* x_hi, const float* x_lo, const float* w_hi, const float* w_lo, int M,
                                   int N, int K, int S, float* part, const int* status, cudaStream_t s) {
+  return x3_partial_launch<false>(x_hi, x_lo, w_hi, w_lo, nullptr, 0, M, N, K, S, part, status, s);
+}
+
+cudaError_t f16x3_partial_launch(const uint16_t* x_hi, const uint16_t* x_lo, const uint16_t* w_hi,
+                                 const uint16_t* w_lo, const int* w_exp, int x_exp, int M, int N, int K, int S,
+                                 float* part, const int* status, cudaStream_t s) {
+  return x3_partial_launch<true>(x_hi, x_lo, w_hi, w_lo, w_exp, x_exp, M, N, K, S, part, status, s);
+}
+
+cudaError_t absmax_launch(const float* x, size_t n, unsigned int* out, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(out, 0, sizeof(unsigned int), s);
+  if (e != cudaSuccess || n == 0) return e;
+  absmax_kernel<<<ew_grid(n), 256, 0, s>>>(x, n, out);
+  return cudaGetLastError();
+}
+
+cudaError_t f16_split_launch(const float* x, long long ldx, int K, int M, int Kp, const unsigned int* max_bits,
+                             int e_fixed, int* e_out, uint16_t* hi, uint16_t* lo, int* status, cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
-  if (N % T3_ROWS || K % T3_BK) return cudaErrorInvalidValue;
-  const int nt = tf32x3_token_tile(M);
-  int ks = (K + S - 1) / S;
-  ks = (ks + T3_BK - 1) / T3_BK * T3_BK;
-  const int S_eff = (K + ks - 1) / ks;
-  CUtensorMap whi, wlo, xhi, xlo;
-  if (!make_tmap_f32_2d(&whi, w_hi, K, N, (uint64_t)K * 4, T3_ROWS) ||
-      !make_tmap_f32_2d(&wlo, w_lo, K, N, (uint64_t)K * 4, T3_ROWS) ||
-      !make_tmap_f32_2d(&xhi, x_hi, K, M, (uint64_t)K * 4, nt) ||
-      !make_tmap_f32_2d(&xlo, x_lo, K, M, (uint64_t)K * 4, nt))
-    return cudaErrorInvalidValue;
-  const int smem = T3_STAGES * (2 * T3_W_BYTES + 2 * nt * T3_BK * 4) + 1024 + 256;
-  static unsigned long long smem_set = 0;  // opted in to the largest plan (NT = 256) once per device
-  cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(tf32x3_partial_kernel),
-                              2 * (2 * T3_W_BYTES + 2 * 256 * T3_BK * 4) + 1024 + 256, &smem_set);
-  if (e != cudaSuccess) return e;
-  T3Args a{M, N, K, ks, nt, part, const_cast<int*>(status)};
-  dim3 grid(N / T3_ROWS, (M + nt - 1) / nt, S_eff);
-  tf32x3_partial_kernel<<<grid, T3_THREADS, smem, s>>>(whi, wlo, xhi, xlo, a);
+  if (K < 1 || Kp < K || ldx < K) return cudaErrorInvalidValue;
+  f16_split_kernel<<<ew_grid((size_t)M * Kp), 256, 0, s>>>(x, ldx, K, M, Kp, max_bits, e_fixed, e_out, hi, lo,
+                                                             status);
   return cudaGetLastError();
 }
 
