@@ -198,6 +198,12 @@ WORKLOADS = {
     "video_audio_bf16_l1": dict(model=dict(C2_MODEL, n_blocks=1), seed=2,
                                 docs=[dict(video=(8, 32, 32), audio=512), dict(video=(8, 32, 32), audio=512)],
                                 t="uniform", w_std=0.02, bias_std=0.0, x_std=1.0),
+    # One block of the long-document model on its full 33,792-token sequence (profiling captures of
+    # the same launch shapes with a few GB on the device).
+    "long_doc_bf16_l1": dict(model=_model(n_blocks=1, hidden=5120, n_heads=40, head_dim=128, ffn_hidden=13824,
+                                          rope_dims=(32, 48, 48), rotary_dim=128),
+                             seed=3, docs=[dict(video=(16, 32, 64), audio=1024)], t="uniform", w_std=0.02,
+                             bias_std=0.0, x_std=1.0),
     # Parity cases that span several 128-row tiles with ragged document ends, a 1-token document and
     # non-zero biases (the oracle finishes them in seconds).
     "ragged": dict(model=_model(n_blocks=2, hidden=512, n_heads=4, head_dim=128, ffn_hidden=1536,
