@@ -43,6 +43,7 @@ TRAFFIC = {
     ("gemm_ffn_up", "video_audio_bf16"): {"bytes": 832782848, "src_sha": "86f8bc031b1d4c6a"},
     ("gemm_ffn_down", "video_audio_bf16"): {"bytes": 1241438208, "src_sha": "86f8bc031b1d4c6a"},
     ("norm_modulate", "video_audio_bf16"): {"bytes": 288634112, "src_sha": "139ad8f729b321b6"},
+    ("attention", "long_doc_bf16"): {"bytes": 1366486272, "src_sha": "b30c215725fdbf8d"},
 }
 
 
@@ -270,8 +271,15 @@ def run_gpu(args, w, dist, rank, world):
         lay = dict(lay, pos=np.concatenate([dit.vit_positions(*dd["video"]) for dd in docs]))
     wr = dict(w, seed=rank_seed(w["seed"], rank))
     W = synth.make_weights(wr)
+    if m.get("nvfp4"):  # the four linear maps come as NVFP4 weights; their bf16 matrices are not bound
+        for b, bb in zip(W["blocks"], W["bits"]["blocks"]):
+            for n in ("w_qkv", "w_o", "w_in", "w_down"):
+                b[n] = bb[n] = None
     h = gpu_util.make_handle(m, lay, W)
     del W
+    if m.get("nvfp4"):
+        h.bind_nvfp4([{n: (torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda(), g) for n, (q, s, g) in b.items()}
+                      for b in synth.make_nvfp4_linears(wr)])
     N, D = lay["n_tokens"], lay["n_docs"]
     dl = gpu_util.dev_layout(lay)
     x_host = synth.make_tokens(wr, lay)
@@ -464,8 +472,15 @@ def run_loop_figures(args, dist, rank, world):
     lay = synth.build_layout(rank_documents(w["docs"], rank, world))
     wr = dict(w, seed=rank_seed(w["seed"], rank))
     W = synth.make_weights(wr)
+    if m.get("nvfp4"):  # the four linear maps come as NVFP4 weights; their bf16 matrices are not bound
+        for b, bb in zip(W["blocks"], W["bits"]["blocks"]):
+            for n in ("w_qkv", "w_o", "w_in", "w_down"):
+                b[n] = bb[n] = None
     h = gpu_util.make_handle(m, lay, W)
     del W
+    if m.get("nvfp4"):
+        h.bind_nvfp4([{n: (torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda(), g) for n, (q, s, g) in b.items()}
+                      for b in synth.make_nvfp4_linears(wr)])
     N, D = lay["n_tokens"], lay["n_docs"]
     dl = gpu_util.dev_layout(lay)
     x_host = synth.make_tokens(wr, lay)
@@ -687,7 +702,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="long_doc_bf16",
                     choices=["video_audio_bf16", "long_doc_bf16", "denoise_loop", "t2va_loop", "music_fp32",
-                             "video_audio_bf16_l1", "long_doc_bf16_l1", "tiny", "ragged", "music_small", "nvfp4_gemm", "vit3d_decoder",
+                             "video_audio_bf16_l1", "long_doc_bf16_l1", "video_audio_nvfp4", "tiny", "ragged", "music_small", "nvfp4_gemm", "vit3d_decoder",
                              "vit3d_small"])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")

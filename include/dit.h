@@ -94,6 +94,11 @@ typedef struct {
    * beyond 65504 sets the status word to DIT_ERR_RANGE.  act_bf16 = 1: bf16 operands throughout
    * (bf16's range, coarser rounding). */
   int act_bf16;
+  /* 1: the four linear maps of every block (qkv, out, FFN up, FFN down) have NVFP4 weights, bound
+   * with dit_bind_nvfp4 ([H3] "What this push adds": the NVFP4 checkpoint's projections); the
+   * weights' matrices in dit_bind_weights are then ignored (may be NULL), their biases used.  Needs
+   * DIT_BF16 with act_bf16 = 0 (the GEMMs take f16 activations) and qkv_interleaved = 0. */
+  int nvfp4;
 } dit_config;
 
 /* One block's weights (device pointers; matrices and biases in cfg.dtype, biases may be NULL = zero;
@@ -157,6 +162,31 @@ typedef struct dit_handle dit_handle;
  * Anything else returns DIT_ERR_CONFIG (not a valid model) or DIT_ERR_UNSUPPORTED (valid, not
  * tiled), dit_last_error(NULL) naming the field. */
 DIT_API dit_status dit_create(const dit_config* cfg, dit_handle** out);
+
+/* NVFP4 weights of one linear map [N, K] ([H3] "What this push adds"): q [N][K/2] E2M1 codes two
+ * per byte (even k in the low nibble), s [N][K/16] E4M3 scales (one per 16 along K), g the fp32
+ * global scale; the weight is code * scale * g.  Device pointers. */
+typedef struct {
+  const uint8_t* q;
+  const uint8_t* s;
+  float g;
+} dit_nvfp4_linear;
+typedef struct {
+  dit_nvfp4_linear qkv;   /* [3d, d] in the order [q_all | k_all | v_all] */
+  dit_nvfp4_linear o;     /* [d, d] */
+  dit_nvfp4_linear in;    /* [2F, d]: value rows, then gate rows */
+  dit_nvfp4_linear down;  /* [d, F] */
+} dit_nvfp4_block;
+
+/* Bind the NVFP4 linear maps of a handle created with nvfp4 = 1 (blocks: HOST array of n_blocks
+ * entries; the device arrays are read during the call only).  Each weight is repacked once into
+ * the library's tile-contiguous layout (N * K * 9 / 16 bytes, library-owned; the FFN up rows
+ * interleaved for the SiLU-gate epilogue), and the forward's four GEMMs of every block read it,
+ * expanding codes * scales to f16 in shared memory for the tensor cores.  Call after
+ * dit_bind_weights (which binds the biases, AdaLN and norms); a forward before both returns
+ * DIT_ERR_UNBOUND.  A NULL code or scale pointer returns DIT_ERR_MISSING_WEIGHT naming it.
+ * Synchronises `stream`. */
+DIT_API dit_status dit_bind_nvfp4(dit_handle* h, const dit_nvfp4_block* blocks, void* stream);
 
 /* Release the handle and its repacked weight copies (synchronises the device first). */
 DIT_API dit_status dit_destroy(dit_handle* h);

@@ -346,6 +346,25 @@ def nvfp4_linear(x, q, scales, g: float, b=None) -> np.ndarray:
     return y
 
 
+def nvfp4_dequant(q, scales, g: float) -> np.ndarray:
+    """The logical weight [N, K] of NVFP4 codes: e2m1(code) * e4m3(scale) * g, from the oracle's
+    decoders, in double; returned as float32, which holds it exactly when g is a power of two (an E2M1
+    value times an E4M3 scale has at most 6 significant bits)."""
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    sc = np.ascontiguousarray(scales, dtype=np.uint8)
+    N = q.shape[0]
+    K = q.shape[1] * 2
+    codes = np.empty((N, K), dtype=np.uint8)
+    codes[:, 0::2] = q & 15
+    codes[:, 1::2] = q >> 4
+    t2 = e2m1_decode(np.arange(16))
+    t4 = e4m3_decode(np.arange(256))
+    w = t2[codes] * np.repeat(t4[sc], 16, axis=1) * float(g)
+    w32 = w.astype(np.float32)
+    assert np.array_equal(w32.astype(np.float64), w), "not exact in fp32 (global scale not a power of two?)"
+    return w32
+
+
 def patchify(lat, pt: int, ph: int, pw: int) -> np.ndarray:
     """Latent [C, T*pt, H*ph, W*pw] -> tokens [T*H*W, C*pt*ph*pw] (exact)."""
     lat = np.ascontiguousarray(lat, dtype=np.float32)

@@ -198,6 +198,11 @@ WORKLOADS = {
     "video_audio_bf16_l1": dict(model=dict(C2_MODEL, n_blocks=1), seed=2,
                                 docs=[dict(video=(8, 32, 32), audio=512), dict(video=(8, 32, 32), audio=512)],
                                 t="uniform", w_std=0.02, bias_std=0.0, x_std=1.0),
+    # The video+audio model with NVFP4 weights in its four linear maps per block ([H3] "What this
+    # push adds": the NVFP4 checkpoint), everything else as in video_audio_bf16.
+    "video_audio_nvfp4": dict(model=dict(C2_MODEL, nvfp4=True), seed=2,
+                              docs=[dict(video=(8, 32, 32), audio=512), dict(video=(8, 32, 32), audio=512)],
+                              t="uniform", w_std=0.02, bias_std=0.0, x_std=1.0),
     # One block of the long-document model on its full 33,792-token sequence (profiling captures of
     # the same launch shapes with a few GB on the device).
     "long_doc_bf16_l1": dict(model=_model(n_blocks=1, hidden=5120, n_heads=40, head_dim=128, ffn_hidden=13824,
@@ -354,10 +359,24 @@ def make_latents(seed: int, layout: dict, widths, name: str = "z") -> list:
 # ---------------------------------------------------------------------------------------------
 # NVFP4 weights: random valid codes, no quantisation arithmetic.  Two FP4 (E2M1) codes per byte,
 # uniform over all 16; one E4M3 scale per 16 along K with exponent field 4..6 (2^-3 .. 2^-1) and a
-# random mantissa; the fp32 global scale 0.015, so the dequantised weight has RMS near 0.02.
+# random mantissa; the fp32 global scale 2^-6, so the dequantised weight has RMS near 0.02 (and,
+# the global scale being a power of two, code * scale * global is exact in fp32).
 # ---------------------------------------------------------------------------------------------
 
-NVFP4_GLOBAL = 0.015
+NVFP4_GLOBAL = 2.0 ** -6
+
+
+def nvfp4_shapes(m: dict) -> dict:
+    """[N, K] of the four linear maps of a block (the logical weight shapes)."""
+    d, F = m["hidden"], m["ffn_hidden"]
+    return {"qkv": (3 * d, d), "o": (d, d), "in": (2 * F, d), "down": (d, F)}
+
+
+def make_nvfp4_linears(w: dict) -> list:
+    """Per block {name: (q, s, g)} NVFP4 weights of the four linear maps of workload w."""
+    shapes = nvfp4_shapes(w["model"])
+    return [{n: make_nvfp4(w["seed"], f"block{l}.nvfp4.{n}", N, K) for n, (N, K) in shapes.items()}
+            for l in range(w["model"]["n_blocks"])]
 
 
 def make_nvfp4(seed: int, name: str, N: int, K: int):

@@ -62,7 +62,9 @@ def test_create_validates_config():
            (dict(head_dim=96, n_heads=32, rope_dims=(32, 32, 32), rotary_dim=96), dit.DIT_ERR_UNSUPPORTED), (dict(n_blocks=0), dit.DIT_ERR_CONFIG),
            (dict(final_norm="ln"), dit.DIT_ERR_CONFIG),  # AdaLN's final layer is RMSNorm + modulate
            (dict(dtype="fp32", adaln=False, qk_norm=True), dit.DIT_ERR_UNSUPPORTED),
-           (dict(rope_dims=(12, 16, 16), rotary_dim=44, n_heads=48, head_dim=64), dit.DIT_ERR_UNSUPPORTED)]
+           (dict(rope_dims=(12, 16, 16), rotary_dim=44, n_heads=48, head_dim=64), dit.DIT_ERR_UNSUPPORTED),
+           (dict(nvfp4=True, act_bf16=True), dit.DIT_ERR_UNSUPPORTED),  # NVFP4 GEMMs take f16 activations
+           (dict(nvfp4=True, qkv_interleaved=True), dit.DIT_ERR_UNSUPPORTED)]
     for kw, st in bad:
         with pytest.raises(dit.DitError) as e:
             dit.Dit(_model(**kw), 100, 1)

@@ -742,6 +742,20 @@ def test_nvfp4_even_k_sits_in_the_low_nibble():
     assert np.array_equal(y[:, 0], x[:, 1].astype(np.float64))
 
 
+def test_nvfp4_dequant_is_the_linear_maps_weight():
+    """The dequantised weight fed to the oracle's forward is the weight of the oracle's NVFP4 linear:
+    x W^T with W = nvfp4_dequant(q, s, g) equals nvfp4_linear(x, q, s, g), and with a power-of-two
+    global scale W is exact in fp32."""
+    q, s, g = synth.make_nvfp4(63, "w", 256, 192)
+    assert g == 2.0 ** -6
+    x = synth.normal(63, "x", (5, 192), 1.0).astype(np.float64)
+    W = oracle.nvfp4_dequant(q, s, g)
+    ref = oracle.nvfp4_linear(x, q, s, g)
+    assert np.abs(x @ W.astype(np.float64).T - ref).max() <= 1e-12 * np.abs(ref).max()
+    with pytest.raises(AssertionError):
+        oracle.nvfp4_dequant(q, s, 0.015)  # not a power of two: not exact in fp32
+
+
 def test_synthetic_nvfp4_weights_have_the_intended_scale():
     q, s, g = synth.make_nvfp4(62, "w", 256, 1024)
     e = (s >> 3) & 15

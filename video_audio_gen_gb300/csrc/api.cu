@@ -53,6 +53,9 @@ struct BlockDev {
   float* b_o = nullptr;
   float* b_in_packed = nullptr;
   float* b_down = nullptr;
+  // NVFP4 linear maps (nvfp4 = 1): tile-contiguous repacks and global scales
+  uint8_t *nv_qkv = nullptr, *nv_o = nullptr, *nv_in = nullptr, *nv_down = nullptr;
+  float g_qkv = 1.f, g_o = 1.f, g_in = 1.f, g_down = 1.f;
   float* res1 = nullptr;           // per-channel residual scales without AdaLN (NULL = 1)
   float* res2 = nullptr;
 };
@@ -74,6 +77,7 @@ struct TimedLaunch {
 struct dit_handle {
   dit_config cfg;
   bool bound = false;
+  bool nvfp4_bound = false;
   std::string err;
   std::vector<void*> allocs;
   std::vector<BlockDev> blocks;
@@ -158,6 +162,9 @@ dit_status validate_config(const dit_config* c) {
     return set_err(nullptr, DIT_ERR_CONFIG, "qk_norm and qkv_interleaved must be 0 or 1");
   if (c->final_norm < 0 || c->final_norm > 2) return set_err(nullptr, DIT_ERR_CONFIG, "final_norm must be 0, 1 or 2");
   if (c->act_bf16 != 0 && c->act_bf16 != 1) return set_err(nullptr, DIT_ERR_CONFIG, "act_bf16 must be 0 or 1");
+  if (c->nvfp4 != 0 && c->nvfp4 != 1) return set_err(nullptr, DIT_ERR_CONFIG, "nvfp4 must be 0 or 1");
+  if (c->nvfp4 && (c->dtype != DIT_BF16 || c->act_bf16 || c->qkv_interleaved))
+    return set_err(nullptr, DIT_ERR_UNSUPPORTED, "nvfp4 needs dtype DIT_BF16, act_bf16 = 0 and qkv_interleaved = 0");
   if (c->adaln && c->final_norm)
     return set_err(nullptr, DIT_ERR_CONFIG, "with AdaLN the final layer is RMSNorm + modulate (final_norm must be 0)");
   // What the sm_103a kernels tile.
@@ -577,12 +584,16 @@ dit_status dit_bind_weights(dit_handle* h, const dit_weights* w, void* stream) {
   // Missing tensors are reported by name before anything is allocated.
   for (int l = 0; l < c.n_blocks; ++l) {
     const dit_block_weights& b = w->blocks[l];
+    // with NVFP4 linear maps the four matrices come from dit_bind_nvfp4
+    const bool lin = !c.nvfp4;
     const struct {
       const void* p;
       const char* name;
-    } req[] = {{b.w_qkv, "w_qkv"}, {b.w_o, "w_o"}, {b.w_in, "w_in"}, {b.w_down, "w_down"},
-               {c.adaln ? b.w_ada : b.w_qkv, "w_ada"}};
+      bool need;
+    } req[] = {{b.w_qkv, "w_qkv", lin}, {b.w_o, "w_o", lin}, {b.w_in, "w_in", lin}, {b.w_down, "w_down", lin},
+               {b.w_ada, "w_ada", c.adaln != 0}};
     for (const auto& r : req) {
+      if (!r.need) continue;
       if (!r.p) return set_err(h, DIT_ERR_MISSING_WEIGHT, "missing weight: blocks[%d].%s", l, r.name);
       if (!aligned16(r.p)) return set_err(h, DIT_ERR_INVALID_ARG, "blocks[%d].%s is not 16-byte aligned", l, r.name);
     }
@@ -596,6 +607,7 @@ dit_status dit_bind_weights(dit_handle* h, const dit_weights* w, void* stream) {
   h->blocks.assign(c.n_blocks, BlockDev());
   h->stats.bound_bytes = 0;
   h->bound = false;
+  h->nvfp4_bound = false;
 
   cudaError_t e;
   const int is_bf16 = c.dtype == DIT_BF16;
@@ -644,13 +656,14 @@ dit_status dit_bind_weights(dit_handle* h, const dit_weights* w, void* stream) {
     if (!(bd.b_down = bias_f32(b.b_down, d))) return cuda_err(h, e, "bind b_down");
     float* b_in = nullptr;
     if (b.b_in && !(b_in = bias_f32(b.b_in, 2ll * F))) return cuda_err(h, e, "bind b_in");
-    bd.w_in_packed = dev_alloc(h, (size_t)2 * F * d * 2, &e);
+    bd.w_in_packed = c.nvfp4 ? nullptr : dev_alloc(h, (size_t)2 * F * d * 2, &e);
     if (e != cudaSuccess) return cuda_err(h, e, "alloc w_in");
     bd.b_in_packed = static_cast<float*>(dev_alloc(h, (size_t)2 * F * 4, &e));
     if (e != cudaSuccess) return cuda_err(h, e, "alloc b_in");
-    DIT_CK(h, pack_ffn_in_launch(b.w_in, b_in, F, d, bd.w_in_packed, bd.b_in_packed, s), "pack w_in");
+    DIT_CK(h, pack_ffn_in_launch(c.nvfp4 ? nullptr : b.w_in, b_in, F, d, bd.w_in_packed, bd.b_in_packed, s),
+           "pack w_in");
   }
-  if (!c.act_bf16) {
+  if (!c.act_bf16 && !c.nvfp4) {
     // f16 GEMM operands: the four linear maps' weights as library-owned f16 copies.  bf16 -> f16 is
     // exact for every value of magnitude 2^-17 .. 65504; a weight beyond 65504 is refused.
     int* range = static_cast<int*>(dev_alloc(h, 16, &e));
@@ -711,6 +724,46 @@ dit_status dit_bind_weights(dit_handle* h, const dit_weights* w, void* stream) {
   return DIT_OK;
 }
 
+dit_status dit_bind_nvfp4(dit_handle* h, const dit_nvfp4_block* blocks, void* stream) {
+  if (!h) return DIT_ERR_INVALID_ARG;
+  const dit_config& c = h->cfg;
+  if (!c.nvfp4) return set_err(h, DIT_ERR_CONFIG, "dit_bind_nvfp4 needs a handle created with nvfp4 = 1");
+  if (!h->bound) return set_err(h, DIT_ERR_UNBOUND, "dit_bind_nvfp4 before dit_bind_weights");
+  if (!blocks) return set_err(h, DIT_ERR_INVALID_ARG, "blocks is NULL");
+  const int d = c.hidden, F = c.ffn_hidden;
+  for (int l = 0; l < c.n_blocks; ++l) {
+    const dit_nvfp4_block& b = blocks[l];
+    const struct {
+      const dit_nvfp4_linear* w;
+      const char* name;
+    } lin[] = {{&b.qkv, "qkv"}, {&b.o, "o"}, {&b.in, "in"}, {&b.down, "down"}};
+    for (const auto& x : lin) {
+      if (!x.w->q) return set_err(h, DIT_ERR_MISSING_WEIGHT, "missing weight: blocks[%d].%s.q", l, x.name);
+      if (!x.w->s) return set_err(h, DIT_ERR_MISSING_WEIGHT, "missing weight: blocks[%d].%s.s", l, x.name);
+      if (!(x.w->g > 0.f) || !isfinite(x.w->g))
+        return set_err(h, DIT_ERR_INVALID_ARG, "blocks[%d].%s.g must be a finite positive scale", l, x.name);
+    }
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  auto pack = [&](const dit_nvfp4_linear& w, int N, int K, int ffn_F, uint8_t** out, float* g) -> bool {
+    *out = static_cast<uint8_t*>(dev_alloc(h, (size_t)N * K * 9 / 16, &e));
+    if (e == cudaSuccess) e = nvfp4_pack_launch(w.q, w.s, N, K, *out, s, ffn_F);
+    *g = w.g;
+    return e == cudaSuccess;
+  };
+  for (int l = 0; l < c.n_blocks; ++l) {
+    const dit_nvfp4_block& b = blocks[l];
+    BlockDev& bd = h->blocks[l];
+    if (!pack(b.qkv, 3 * d, d, 0, &bd.nv_qkv, &bd.g_qkv) || !pack(b.o, d, d, 0, &bd.nv_o, &bd.g_o) ||
+        !pack(b.in, 2 * F, d, F, &bd.nv_in, &bd.g_in) || !pack(b.down, d, F, 0, &bd.nv_down, &bd.g_down))
+      return cuda_err(h, e, "bind NVFP4 linear maps");
+  }
+  DIT_CK(h, cudaStreamSynchronize(s), "bind nvfp4 sync");
+  h->nvfp4_bound = true;
+  return DIT_OK;
+}
+
 // The latent forward's inputs and scratch, resolved on the host.
 struct LatentArgs {
   const float* const* z;  // host array of device pointers, z[m] [count[m]][width[m]]
@@ -754,6 +807,16 @@ static dit_status latent_embed(dit_handle* h, const LatentArgs& a, const uint8_t
   return DIT_OK;
 }
 
+// One of the forward's GEMMs: the 16-bit weight B, or its NVFP4 repack (then A is f16 and the global
+// scale multiplies the accumulator in the epilogue).
+static cudaError_t gemm_any(int epi, const void* A, const void* B, const uint8_t* nv, float g_scale, GemmArgs g,
+                            cudaStream_t s) {
+  if (!nv) return gemm_launch(epi, A, B, g, s);
+  g.b_packed = nv;
+  g.w_scale = g_scale;
+  return gemm_nvfp4_launch(epi, A, g, s);
+}
+
 // The forward with its AdaLN timesteps: n_t = 1 (every modality at t[0]) or n_t = n_modalities.
 // With `lat` the residual is filled by the patch projections instead of copied from x_tokens.
 static dit_status forward_impl(dit_handle* h, const float* x_tokens, const int32_t* cu_seqlens, int n_docs,
@@ -763,6 +826,7 @@ static dit_status forward_impl(dit_handle* h, const float* x_tokens, const int32
   if (!h) return DIT_ERR_INVALID_ARG;
   if (!h->bound) return set_err(h, DIT_ERR_UNBOUND, "dit_forward before dit_bind_weights");
   const dit_config& c = h->cfg;
+  if (c.nvfp4 && !h->nvfp4_bound) return set_err(h, DIT_ERR_UNBOUND, "nvfp4 = 1: dit_forward before dit_bind_nvfp4");
   if ((!x_tokens && !lat) || !cu_seqlens || !doc_ids || !modality_tags || !pos_thw || !out || !workspace)
     return set_err(h, DIT_ERR_INVALID_ARG, "a required pointer is NULL");
   if (n_tokens < 1 || n_docs < 1) return set_err(h, DIT_ERR_LAYOUT, "n_tokens and n_docs must be >= 1");
@@ -866,7 +930,7 @@ static dit_status forward_impl(dit_handle* h, const float* x_tokens, const int32
       g.cos_cache = cosc; g.sin_cache = sinc; g.q = q; g.k = k; g.vt = vt; g.n_pad = L.n_pad;
       g.qk_norm = c.qk_norm; g.qk_eps = c.norm_eps;
       g.status = status; g.f16 = f16;
-      DIT_CK(h, gemm_launch(kEpiQkvRope, y, B.w_qkv, g, s), "gemm qkv");
+      DIT_CK(h, gemm_any(kEpiQkvRope, y, B.w_qkv, B.nv_qkv, B.g_qkv, g, s), "gemm qkv");
       ln.done();
     }
     {
@@ -880,7 +944,7 @@ static dit_status forward_impl(dit_handle* h, const float* x_tokens, const int32
       g.M = N; g.N = d; g.K = d; g.bias = B.b_o;
       g.x = resid; g.gate = c.adaln ? ml + 2 * d : B.res1; g.gate_stride = c.adaln ? mstride : 0;
       g.tags = modality_tags; g.status = status; g.f16 = f16;
-      DIT_CK(h, gemm_launch(kEpiGatedResid, o, B.w_o, g, s), "gemm out");
+      DIT_CK(h, gemm_any(kEpiGatedResid, o, B.w_o, B.nv_o, B.g_o, g, s), "gemm out");
       ln.done();
     }
     {
@@ -895,7 +959,7 @@ static dit_status forward_impl(dit_handle* h, const float* x_tokens, const int32
       GemmArgs g{};
       g.M = N; g.N = 2 * F; g.K = d; g.bias = B.b_in_packed; g.out = hbuf; g.status = status;
       g.f16 = f16; g.out_kind = y_kind;
-      DIT_CK(h, gemm_launch(kEpiSwiglu, y, B.w_in_packed, g, s), "gemm ffn up");
+      DIT_CK(h, gemm_any(kEpiSwiglu, y, B.w_in_packed, B.nv_in, B.g_in, g, s), "gemm ffn up");
       ln.done();
     }
     {
@@ -904,7 +968,7 @@ static dit_status forward_impl(dit_handle* h, const float* x_tokens, const int32
       g.M = N; g.N = d; g.K = F; g.bias = B.b_down;
       g.x = resid; g.gate = c.adaln ? ml + 5 * d : B.res2; g.gate_stride = c.adaln ? mstride : 0;
       g.tags = modality_tags; g.status = status; g.f16 = f16;
-      DIT_CK(h, gemm_launch(kEpiGatedResid, hbuf, B.w_down, g, s), "gemm ffn down");
+      DIT_CK(h, gemm_any(kEpiGatedResid, hbuf, B.w_down, B.nv_down, B.g_down, g, s), "gemm ffn down");
       ln.done();
     }
     if (h->dump)

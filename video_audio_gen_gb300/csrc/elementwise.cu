@@ -323,9 +323,11 @@ __global__ void pack_ffn_in_kernel(const __nv_bfloat16* __restrict__ src, const 
   const int p = blockIdx.x;
   const int g = p >> 8, w = p & 255;
   const int s = w < 128 ? 128 * g + w : F + 128 * g + (w - 128);
-  const uint4* in = reinterpret_cast<const uint4*>(src + (size_t)s * d);
-  uint4* out = reinterpret_cast<uint4*>(dst + (size_t)p * d);
-  for (int i = threadIdx.x; i < d / 8; i += blockDim.x) out[i] = in[i];
+  if (src) {  // NULL: the biases alone (the weight is bound in another form)
+    const uint4* in = reinterpret_cast<const uint4*>(src + (size_t)s * d);
+    uint4* out = reinterpret_cast<uint4*>(dst + (size_t)p * d);
+    for (int i = threadIdx.x; i < d / 8; i += blockDim.x) out[i] = in[i];
+  }
   if (threadIdx.x == 0) b_dst[p] = b_src ? b_src[s] : 0.f;
 }
 

@@ -649,8 +649,12 @@ cudaError_t launch_t(const void* A, const void* B, const GemmArgs& args, cudaStr
   return cudaGetLastError();
 }
 
+// ffn_F > 0: the weight is an FFN up projection [2F, K] whose rows are interleaved in 128-feature
+// groups as they are packed (packed row p of group p / 256 takes value row 128 (p / 256) + p % 256 for
+// p % 256 < 128, else gate row F + 128 (p / 256) + p % 256 - 128), the layout the SiLU-gate epilogue
+// reads.
 __global__ void nvfp4_pack_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ sc, int N, int K,
-                                  uint8_t* __restrict__ packed) {
+                                  int ffn_F, uint8_t* __restrict__ packed) {
   const int kbs = K / BK;
   const size_t total = (size_t)(N / BN) * kbs * Q_RAW_BYTES;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
@@ -658,13 +662,18 @@ __global__ void nvfp4_pack_kernel(const uint8_t* __restrict__ q, const uint8_t* 
     const int o = (int)(i - t * Q_RAW_BYTES);
     const int nb = (int)(t / kbs), kb = (int)(t - (size_t)nb * kbs);
     uint8_t v;
+    auto src_row = [&](int p) {
+      if (!ffn_F) return p;
+      const int g = p >> 8, w = p & 255;
+      return w < 128 ? 128 * g + w : ffn_F + 128 * g + (w - 128);
+    };
     if (o < Q_CODE_BYTES) {
       const int r = o / (BK / 2), j = o - r * (BK / 2);
-      v = q[(size_t)(nb * BN + r) * (K / 2) + kb * (BK / 2) + j];
+      v = q[(size_t)src_row(nb * BN + r) * (K / 2) + kb * (BK / 2) + j];
     } else {
       const int o2 = o - Q_CODE_BYTES;
       const int r = o2 / (BK / 16), j = o2 - r * (BK / 16);
-      v = sc[(size_t)(nb * BN + r) * (K / 16) + kb * (BK / 16) + j];
+      v = sc[(size_t)src_row(nb * BN + r) * (K / 16) + kb * (BK / 16) + j];
     }
     packed[i] = v;
   }
@@ -709,12 +718,13 @@ cudaError_t gemm_nvfp4_launch(int epilogue, const void* A, const GemmArgs& args_
   }
 }
 
-cudaError_t nvfp4_pack_launch(const uint8_t* q, const uint8_t* s, int N, int K, uint8_t* packed, cudaStream_t st) {
-  if (N % BN || K % BK || N <= 0 || K <= 0) return cudaErrorInvalidValue;
+cudaError_t nvfp4_pack_launch(const uint8_t* q, const uint8_t* s, int N, int K, uint8_t* packed, cudaStream_t st,
+                              int ffn_F) {
+  if (N % BN || K % BK || N <= 0 || K <= 0 || (ffn_F && (N != 2 * ffn_F || ffn_F % 128))) return cudaErrorInvalidValue;
   const size_t total = (size_t)(N / BN) * (K / BK) * Q_RAW_BYTES;
   size_t g = (total + 255) / 256;
   const size_t cap = (size_t)num_sms() * 16;
-  nvfp4_pack_kernel<<<(unsigned)(g < cap ? g : cap), 256, 0, st>>>(q, s, N, K, packed);
+  nvfp4_pack_kernel<<<(unsigned)(g < cap ? g : cap), 256, 0, st>>>(q, s, N, K, ffn_F, packed);
   return cudaGetLastError();
 }
 

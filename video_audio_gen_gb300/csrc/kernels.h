@@ -66,7 +66,9 @@ cudaError_t gemm_nvfp4_launch(int epilogue, const void* A, const GemmArgs& args,
 // NVFP4 weight repack: q [N][K/2] (two E2M1 per byte, even k low), s [N][K/16] (E4M3) ->
 // [N/256][K/64] tiles of 9216 bytes: 256 rows x 32 bytes of codes, then 256 rows x 4 scales.
 constexpr int kNvfp4TileBytes = 9216;
-cudaError_t nvfp4_pack_launch(const uint8_t* q, const uint8_t* s, int N, int K, uint8_t* packed, cudaStream_t st);
+// ffn_F > 0 interleaves the rows of an FFN up projection [2F, K] into 128-feature value/gate groups.
+cudaError_t nvfp4_pack_launch(const uint8_t* q, const uint8_t* s, int N, int K, uint8_t* packed, cudaStream_t st,
+                              int ffn_F = 0);
 
 // Attention: q, k bf16 [N, H*Dh], vt bf16 [H*Dh, n_pad], o bf16 [N, H*Dh].  `items` is the
 // device tile list built by attention_schedule_launch (int2 {doc, q_start}), `count` its length.

@@ -24,7 +24,8 @@ KERNEL_KINDS = ["gemm_qkv", "attention", "gemm_out", "gemm_ffn_up", "gemm_ffn_do
                 "latent_io"]
 MAX_LATENT_MODALITIES = 8
 
-EXPORTS = ["dit_create", "dit_destroy", "dit_last_error", "dit_workspace_bytes", "dit_bind_weights", "dit_forward",
+EXPORTS = ["dit_create", "dit_destroy", "dit_last_error", "dit_workspace_bytes", "dit_bind_weights", "dit_bind_nvfp4",
+           "dit_forward",
            "dit_forward_modal", "dit_workspace_bytes_host", "dit_forward_host", "dit_euler_step",
            "dit_euler_step_modal", "dit_time_shift", "dit_vit_positions", "dit_bind_latent_io", "dit_workspace_bytes_latent",
            "dit_forward_latent", "dit_patchify", "dit_unpatchify", "dit_audio_pack", "dit_audio_unpack", "dit_get_stats", "dit_sync_status",
@@ -54,7 +55,18 @@ class DitConfig(ctypes.Structure):
                 ("rotary_dim", ctypes.c_int), ("rope_base", ctypes.c_double), ("io_channels", ctypes.c_int),
                 ("dtype", ctypes.c_int), ("max_tokens", ctypes.c_int), ("max_docs", ctypes.c_int),
                 ("qk_norm", ctypes.c_int), ("qkv_interleaved", ctypes.c_int), ("final_norm", ctypes.c_int),
-                ("act_bf16", ctypes.c_int)]
+                ("act_bf16", ctypes.c_int), ("nvfp4", ctypes.c_int)]
+
+
+class DitNvfp4Linear(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("s", ctypes.c_void_p), ("g", ctypes.c_float)]
+
+
+NVFP4_LINEARS = ["qkv", "o", "in", "down"]
+
+
+class DitNvfp4Block(ctypes.Structure):
+    _fields_ = [(n, DitNvfp4Linear) for n in NVFP4_LINEARS]
 
 
 BLOCK_FIELDS = ["w_qkv", "b_qkv", "w_o", "b_o", "w_in", "b_in", "w_down", "b_down", "w_ada", "b_ada",
@@ -101,6 +113,7 @@ def lib():
             "dit_workspace_bytes": (sz, [ctypes.POINTER(DitConfig), i32, i32]),
             "dit_workspace_bytes_host": (sz, [ctypes.POINTER(DitConfig), i32, i32]),
             "dit_bind_weights": (i32, [vp, ctypes.POINTER(DitWeights), vp]),
+            "dit_bind_nvfp4": (i32, [vp, ctypes.POINTER(DitNvfp4Block), vp]),
             "dit_forward": (i32, [vp, vp, vp, i32, vp, vp, vp, i32, f32, vp, vp, sz, vp]),
             "dit_forward_host": (i32, [vp, vp, vp, i32, vp, vp, vp, i32, f32, vp, vp, sz, vp]),
             "dit_forward_modal": (i32, [vp, vp, vp, i32, vp, vp, vp, i32, ctypes.POINTER(ctypes.c_float), vp, vp,
@@ -187,6 +200,7 @@ def make_config(m: dict, max_tokens: int, max_docs: int) -> DitConfig:
     c.qkv_interleaved = 1 if m.get("qkv_interleaved") else 0
     c.final_norm = {"same": 0, "rms": 1, "ln": 2}[m.get("final_norm", "same")]
     c.act_bf16 = 1 if m.get("act_bf16") else 0
+    c.nvfp4 = 1 if m.get("nvfp4") else 0
     return c
 
 
@@ -231,6 +245,18 @@ class Dit:
             setattr(w, n, t.data_ptr() if t is not None else None)
         self._keep = (blocks, glob)
         _check(lib().dit_bind_weights(self.h, ctypes.byref(w), _stream(stream)), self.h)
+
+    def bind_nvfp4(self, blocks: list[dict], stream=None):
+        """dit_bind_nvfp4: per block a dict {name: (q, s, g)} for name in qkv, o, in, down, with q, s
+        device uint8 tensors (E2M1 codes two per byte, E4M3 scales) and g the fp32 global scale."""
+        arr = (DitNvfp4Block * len(blocks))()
+        for l, b in enumerate(blocks):
+            for n in NVFP4_LINEARS:
+                q, s, g = b[n]
+                lin = getattr(arr[l], n)
+                lin.q, lin.s, lin.g = _ptr(q), _ptr(s), float(g)
+        self._keep_nvfp4 = blocks
+        _check(lib().dit_bind_nvfp4(self.h, arr, _stream(stream)), self.h)
 
     def forward(self, x, cu_seqlens, doc_ids, tags, pos, t: float, out, workspace, stream=None):
         n_docs = cu_seqlens.numel() - 1
