@@ -93,13 +93,11 @@ def fp32_alu_peak_tflops(peaks: dict, n_sms: int) -> float:
     return n_sms * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
 
 
-TF32_PER_BF16 = 1.1 / 2.25   # nominal dense tf32 / bf16 tensor rates
-
-
-def fp32_3xtf32_peak_tflops(peaks: dict) -> float:
-    """fp32-equivalent peak of the 3xTF32 GEMM: the tf32 rate (measured sustained bf16 figure x the
-    nominal tf32/bf16 ratio) over the three tf32 products it spends per fp32 product."""
-    return peaks["bf16_tflops_sustained"] * TF32_PER_BF16 / 3.0
+def fp32_3xf16_peak_tflops(peaks: dict) -> float:
+    """fp32-equivalent peak of the 3xF16 GEMM: the f16 tensor rate (the measured sustained bf16
+    figure; kind::f16 runs f16 and bf16 at one rate) over the three f16 products it spends per fp32
+    product."""
+    return peaks["bf16_tflops_sustained"] / 3.0
 
 
 def load_peaks():
@@ -352,7 +350,7 @@ def run_gpu(args, w, dist, rank, world):
     fl = step_flops(m, lay["cu_seqlens"])
     peaks, peak_src = load_peaks()
     alu_peak = fp32_alu_peak_tflops(peaks, torch.cuda.get_device_properties(dev).multi_processor_count)
-    tf32x3_peak = fp32_3xtf32_peak_tflops(peaks)
+    f16x3_peak = fp32_3xf16_peak_tflops(peaks)
     kernels = {}
     for k in KINDS:
         ms, n = kt[k]
@@ -365,7 +363,7 @@ def run_gpu(args, w, dist, rank, world):
             if m["dtype"] == "fp32" and k == "attention":
                 entry.update(bound="alu", achieved_tflops=round(tf, 1), frac=round(tf / alu_peak, 3))
             elif m["dtype"] == "fp32":
-                entry.update(bound="tensor", achieved_tflops=round(tf, 1), frac=round(tf / tf32x3_peak, 3))
+                entry.update(bound="tensor", achieved_tflops=round(tf, 1), frac=round(tf / f16x3_peak, 3))
             else:
                 entry.update(bound="tensor", achieved_tflops=round(tf, 1),
                              frac=round(tf / peaks["bf16_tflops_sustained"], 3))
@@ -391,9 +389,9 @@ def run_gpu(args, w, dist, rank, world):
                     "algorithmic_flops_per_launch": fl["per_launch"][top]}
     elif m["dtype"] == "fp32":
         roofline = {"bound": "tensor", "kernel": top, "achieved": kernels[top]["achieved_tflops"],
-                    "peak": round(tf32x3_peak, 1), "unit": "TFLOP/s", "frac": kernels[top]["frac"], "traffic": traffic,
-                    "peak_source": f"3xTF32: bf16_tflops_sustained of {peak_src} x nominal tf32/bf16 (1.1/2.25) / 3 "
-                                   "tf32 products per fp32 product",
+                    "peak": round(f16x3_peak, 1), "unit": "TFLOP/s", "frac": kernels[top]["frac"], "traffic": traffic,
+                    "peak_source": f"3xF16: bf16_tflops_sustained of {peak_src} (the f16 rate) / 3 f16 products "
+                                   "per fp32 product",
                     "algorithmic_flops_per_launch": fl["per_launch"][top]}
     else:
         roofline = {"bound": "tensor", "kernel": top, "achieved": kernels[top]["achieved_tflops"],

@@ -128,15 +128,19 @@ __device__ __forceinline__ void epi_store(const GemmArgs& a, uint32_t t, int row
   }
 }
 
+// The epilogues' 16-bit outputs (q, k, h) are read by the next kernel, not by this GEMM: they are
+// stored evict-first so that they do not push the weight panels out of L2.
 __device__ __forceinline__ void store_f16x16(__half* o, const float (&v)[16]) {
-  st_global_v4(o, pack_f16x2(v[0], v[1]), pack_f16x2(v[2], v[3]), pack_f16x2(v[4], v[5]), pack_f16x2(v[6], v[7]));
-  st_global_v4(o + 8, pack_f16x2(v[8], v[9]), pack_f16x2(v[10], v[11]), pack_f16x2(v[12], v[13]),
+  st_global_v4_stream(o, pack_f16x2(v[0], v[1]), pack_f16x2(v[2], v[3]), pack_f16x2(v[4], v[5]),
+                      pack_f16x2(v[6], v[7]));
+  st_global_v4_stream(o + 8, pack_f16x2(v[8], v[9]), pack_f16x2(v[10], v[11]), pack_f16x2(v[12], v[13]),
                pack_f16x2(v[14], v[15]));
 }
 
 __device__ __forceinline__ void store_bf16x16(__nv_bfloat16* o, const float (&v)[16]) {
-  st_global_v4(o, pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
-  st_global_v4(o + 8, pack_bf16x2(v[8], v[9]), pack_bf16x2(v[10], v[11]), pack_bf16x2(v[12], v[13]),
+  st_global_v4_stream(o, pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                      pack_bf16x2(v[6], v[7]));
+  st_global_v4_stream(o + 8, pack_bf16x2(v[8], v[9]), pack_bf16x2(v[10], v[11]), pack_bf16x2(v[12], v[13]),
                pack_bf16x2(v[14], v[15]));
 }
 
@@ -178,9 +182,9 @@ __device__ __forceinline__ void rope_chunk(const GemmArgs& a, uint32_t t, int hb
   const bool f = a.f16;
 #pragma unroll
   for (int i = 0; i < W; i += 8) {
-    st_global_v4(dst + hb + c + i, pack16(f, o1[i], o1[i + 1]), pack16(f, o1[i + 2], o1[i + 3]),
+    st_global_v4_stream(dst + hb + c + i, pack16(f, o1[i], o1[i + 1]), pack16(f, o1[i + 2], o1[i + 3]),
                  pack16(f, o1[i + 4], o1[i + 5]), pack16(f, o1[i + 6], o1[i + 7]));
-    st_global_v4(dst + hb + half + c + i, pack16(f, o2[i], o2[i + 1]), pack16(f, o2[i + 2], o2[i + 3]),
+    st_global_v4_stream(dst + hb + half + c + i, pack16(f, o2[i], o2[i + 1]), pack16(f, o2[i + 2], o2[i + 3]),
                  pack16(f, o2[i + 4], o2[i + 5]), pack16(f, o2[i + 6], o2[i + 7]));
   }
 }
@@ -492,6 +496,7 @@ __global__ void __launch_bounds__(BQ ? Q_THREADS : GEMM_THREADS, 1)
 
   if (warp == 0) {
     if (lane == 0) {
+      const uint64_t b_policy = l2_policy_evict_last();
       int stage = 0, rslot = 0;
       uint32_t phase = 0, rphase = 0;
       for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
@@ -514,7 +519,8 @@ __global__ void __launch_bounds__(BQ ? Q_THREADS : GEMM_THREADS, 1)
           } else {
             mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
             tma_load_2d(sA + stage * A_BYTES, &tmA, &full[stage], kb * BK, tc.mb * BM);
-            tma_load_2d(sB + stage * B_BYTES, &tmB, &full[stage], kb * BK, tc.nb * BN);
+            // a raster group's weight panels are read by every M-block of the group: keep them in L2
+            tma_load_2d_hint(sB + stage * B_BYTES, &tmB, &full[stage], kb * BK, tc.nb * BN, b_policy);
           }
           if (++stage == NST) {
             stage = 0;
