@@ -407,22 +407,26 @@ dit_status bind_fp32(dit_handle* h, const dit_weights* w, cudaStream_t s) {
   return DIT_OK;
 }
 
-// One fp32 GEMM of the forward: the input split into f16 (hi, lo) parts of x 2^4, the 3xF16 partial
-// sums, then (by the caller) the fixed-order reduction that applies the epilogue.
+// One fp32 GEMM of the forward: the 3xF16 partial sums of the activation operand in `xs` (f16 hi
+// [M][K] then lo [M][K] of x 2^kF16x3ActExp), then (by the caller) the fixed-order reduction that
+// applies the epilogue.  The operand is written by the kernel that produces x (the norms, the
+// attention, the SiLU-gate reduction); `run` splits an fp32 x first (the 1x1 convolutions' inputs).
 struct Sgemm {
   dit_handle* h;
   cudaStream_t s;
   float* part;
-  uint16_t* x_hi;
-  uint16_t* x_lo;
+  uint16_t* xs;
   int* status;
   int S;  // effective splits of the last partial launch
-  cudaError_t run(const float* X, const SplitW16& W, int M, int N, int K) {
-    cudaError_t e = f16_split_launch(X, K, K, M, K, nullptr, kF16x3ActExp, nullptr, x_hi, x_lo, status, s);
-    if (e != cudaSuccess) return e;
+  cudaError_t run_split(const SplitW16& W, int M, int N, int K) {
     const int want = f16x3_splits(M, N, K);
     S = f16x3_effective_splits(K, want);
-    return f16x3_partial_launch(x_hi, x_lo, W.hi, W.lo, W.e, kF16x3ActExp, M, N, K, want, part, status, s);
+    return f16x3_partial_launch(xs, xs + (size_t)M * K, W.hi, W.lo, W.e, kF16x3ActExp, M, N, K, want, part, status,
+                                s);
+  }
+  cudaError_t run(const float* X, const SplitW16& W, int M, int N, int K) {
+    cudaError_t e = f16_split_launch(X, K, K, M, K, nullptr, kF16x3ActExp, nullptr, xs, xs + (size_t)M * K, status, s);
+    return e == cudaSuccess ? run_split(W, M, N, K) : e;
   }
 };
 
@@ -442,11 +446,8 @@ dit_status forward_fp32(dit_handle* h, const float* x_tokens, const int32_t* cu_
   float* q = at<float>(workspace, L.q);
   float* k = at<float>(workspace, L.k);
   float* v = at<float>(workspace, L.vt);
-  float* o = at<float>(workspace, L.o);
-  float* hb = at<float>(workspace, L.h);
   float* xt = at<float>(workspace, L.mod);
-  Sgemm g{h, s, at<float>(workspace, L.part), at<uint16_t>(workspace, L.xs_hi), at<uint16_t>(workspace, L.xs_lo),
-          status, 1};
+  Sgemm g{h, s, at<float>(workspace, L.part), at<uint16_t>(workspace, L.xs_hi), status, 1};
   {
     Launch ln(h, s, 6);
     DIT_CK(h, cudaMemsetAsync(sw, 0, sizeof(StatusWords), s), "status reset");
@@ -475,43 +476,45 @@ dit_status forward_fp32(dit_handle* h, const float* x_tokens, const int32_t* cu_
     const BlockDev& B = h->blocks[l];
     {
       Launch ln(h, s, 5);
-      DIT_CK(h, norm_modulate_launch(resid, resid_lo, N, d, c.norm, c.norm_eps, B.ln1_g, B.ln1_b, nullptr, nullptr, nullptr, 0, y,
-                                     1, status, s), "norm1");
+      DIT_CK(h, norm_modulate_launch(resid, resid_lo, N, d, c.norm, c.norm_eps, B.ln1_g, B.ln1_b, nullptr, nullptr,
+                                     nullptr, 0, g.xs, 3, status, s), "norm1");
       ln.done();
     }
     {
       Launch ln(h, s, 0);
-      DIT_CK(h, g.run(y, B.s_qkv, N, 3 * d, d), "qkv");
+      DIT_CK(h, g.run_split(B.s_qkv, N, 3 * d, d), "qkv");
       DIT_CK(h, sgemm_reduce_qkv_launch(g.part, g.S, N, d, c.head_dim, L.half, B.b_qkv, cosc, sinc, q, k, v, status, s),
              "qkv reduce");
       ln.done();
     }
     {
       Launch ln(h, s, 1);
-      DIT_CK(h, attention_f32_launch(q, k, v, cu_seqlens, doc_ids, N, H, c.head_dim, o, status, s), "attention");
+      DIT_CK(h, attention_f32_launch(q, k, v, cu_seqlens, items, &sw->count, L.max_items, N, H, c.head_dim, nullptr,
+                                     g.xs, status, s), "attention");
       ln.done();
     }
     {
       Launch ln(h, s, 2);
-      DIT_CK(h, g.run(o, B.s_o, N, d, d), "out-proj");
+      DIT_CK(h, g.run_split(B.s_o, N, d, d), "out-proj");
       DIT_CK(h, sgemm_reduce_store_launch(g.part, g.S, N, d, B.b_o, resid, 1, resid_lo, status, s), "out-proj reduce");
       ln.done();
     }
     {
       Launch ln(h, s, 5);
-      DIT_CK(h, norm_modulate_launch(resid, resid_lo, N, d, c.norm, c.norm_eps, B.ln2_g, B.ln2_b, nullptr, nullptr, nullptr, 0, y,
-                                     1, status, s), "norm2");
+      DIT_CK(h, norm_modulate_launch(resid, resid_lo, N, d, c.norm, c.norm_eps, B.ln2_g, B.ln2_b, nullptr, nullptr,
+                                     nullptr, 0, g.xs, 3, status, s), "norm2");
       ln.done();
     }
     {
       Launch ln(h, s, 3);
-      DIT_CK(h, g.run(y, B.s_in, N, 2 * F, d), "ffn up");
-      DIT_CK(h, sgemm_reduce_swiglu_launch(g.part, g.S, N, F, B.b_in_packed, hb, status, s), "ffn up reduce");
+      DIT_CK(h, g.run_split(B.s_in, N, 2 * F, d), "ffn up");
+      DIT_CK(h, sgemm_reduce_swiglu_launch(g.part, g.S, N, F, B.b_in_packed, nullptr, g.xs, status, s),
+             "ffn up reduce");
       ln.done();
     }
     {
       Launch ln(h, s, 4);
-      DIT_CK(h, g.run(hb, B.s_down, N, d, F), "ffn down");
+      DIT_CK(h, g.run_split(B.s_down, N, d, F), "ffn down");
       DIT_CK(h, sgemm_reduce_store_launch(g.part, g.S, N, d, B.b_down, resid, 1, resid_lo, status, s),
              "ffn down reduce");
       ln.done();

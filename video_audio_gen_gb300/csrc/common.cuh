@@ -367,6 +367,25 @@ __device__ __forceinline__ uint16_t to16(bool f16, float v) {
   return f16 ? __half_as_ushort(__float2half_rn(v)) : __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 
+// Four values v * 2^e as f16 (hi, lo) pairs for the 3xF16 GEMM: hi = f16(v 2^e), lo = f16(v 2^e - hi);
+// stored at hi_dst / lo_dst (4 consecutive 16-bit elements each, 8-byte aligned).  Returns true when a
+// scaled value is beyond f16's finite range.
+__device__ __forceinline__ bool store_f16_split4(const float (&v)[4], int e, uint16_t* hi_dst, uint16_t* lo_dst) {
+  uint16_t h[4], l[4];
+  bool over = false;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float x = ldexpf(v[i], e);
+    over |= fabsf(x) > 65504.f;
+    const __half hh = __float2half_rn(x);
+    h[i] = __half_as_ushort(hh);
+    l[i] = __half_as_ushort(__float2half_rn(__fsub_rn(x, __half2float(hh))));
+  }
+  *reinterpret_cast<uint2*>(hi_dst) = make_uint2(h[0] | (uint32_t)h[1] << 16, h[2] | (uint32_t)h[3] << 16);
+  *reinterpret_cast<uint2*>(lo_dst) = make_uint2(l[0] | (uint32_t)l[1] << 16, l[2] | (uint32_t)l[3] << 16);
+  return over;
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -11,7 +11,7 @@
 //                           split writes its partial sums to a [S][M][N] buffer
 //   sgemm_reduce_*          sums the S partials in a fixed order and applies the epilogue (bias,
 //                           residual add, NeoX RoPE + q/k/v split, value * silu(gate))
-//   attention_f32_kernel    one warp per (query row, head), exact fp32 online softmax with expf
+//   attention_f32_kernel    exact fp32 online softmax with expf; keys and values staged in shared memory
 //   io_transpose_kernel     channel-major [io, len] per document <-> frame-major [N, io]
 #include "common.cuh"
 #include "kernels.h"
@@ -85,61 +85,153 @@ __global__ void sgemm_reduce_qkv_kernel(const float* __restrict__ part, int S, i
   }
 }
 
-// h[r, f] = (u + b_u) * silu(g + b_g): value columns [0, F), gate columns [F, 2F)
+// h[r, f] = (u + b_u) * silu(g + b_g): value columns [0, F), gate columns [F, 2F).  With h_split the
+// result goes out as the 3xF16 GEMM's f16 (hi, lo) operand, four features per thread (F % 4 == 0).
 __global__ void sgemm_reduce_swiglu_kernel(const float* __restrict__ part, int S, int M, int F,
-                                           const float* __restrict__ bias, float* __restrict__ h, const int* status) {
+                                           const float* __restrict__ bias, float* __restrict__ h,
+                                           uint16_t* __restrict__ h_split, int* status) {
   if (status && (*reinterpret_cast<const volatile int*>(status) & kDevLayout)) return;
   const size_t MN = (size_t)M * 2 * F;
-  const size_t total = (size_t)M * F;
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
-    const int r = (int)(i / F), f = (int)(i - (size_t)r * F);
-    const float u = sum_parts(part, S, MN, (size_t)r * 2 * F + f) + (bias ? bias[f] : 0.f);
-    const float g = sum_parts(part, S, MN, (size_t)r * 2 * F + F + f) + (bias ? bias[F + f] : 0.f);
-    h[i] = u * (g / (1.0f + expf(-g)));
+  const size_t total = (size_t)M * F / 4;
+  bool over = false;
+  for (size_t i4 = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i4 < total; i4 += (size_t)gridDim.x * blockDim.x) {
+    const size_t i = i4 * 4;
+    const int r = (int)(i / F), f0 = (int)(i - (size_t)r * F);
+    float hv[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int f = f0 + e;
+      const float u = sum_parts(part, S, MN, (size_t)r * 2 * F + f) + (bias ? bias[f] : 0.f);
+      const float g = sum_parts(part, S, MN, (size_t)r * 2 * F + F + f) + (bias ? bias[F + f] : 0.f);
+      hv[e] = u * (g / (1.0f + expf(-g)));
+    }
+    if (h_split)
+      over |= store_f16_split4(hv, kF16x3ActExp, h_split + i, h_split + (size_t)M * F + i);
+    else
+      *reinterpret_cast<float4*>(h + i) = make_float4(hv[0], hv[1], hv[2], hv[3]);
   }
+  if (over && status) atomicOr(status, kDevRange);
 }
 
-// Exact fp32 softmax attention over the document of each row.  One warp per (row, head); lanes
-// hold DH/32 dims of q, o; running max / sum (online softmax) in registers.
+// Exact fp32 softmax attention over the document of each row.  One CTA per (document, 128-row
+// q-tile, head, 32-row quarter), 4 warps of 8 query rows each.  The document's keys and values pass
+// through shared memory 32 at a time (lane j scores key j of the chunk); every row keeps an exact fp32
+// online softmax (running max m, sum l, accumulator o, each chunk rescaled by exp(m_old - m_new)):
+//     o_i = sum_j exp(s_ij - m_i) v_j / sum_j exp(s_ij - m_i),   s_ij = q_i . k_j / sqrt(Dh)
+// Lane l accumulates output dims [l * DH / 32, (l + 1) * DH / 32).
+constexpr int AF_KC = 32;      // keys per chunk
+constexpr int AF_ROWS = 8;     // query rows per warp
+constexpr int AF_WARPS = 4;
+
 template <int DH>
-__global__ void __launch_bounds__(256) attention_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
-                                                            const float* __restrict__ v, const int32_t* __restrict__ cu,
-                                                            const int32_t* __restrict__ doc_ids, int n, int H,
-                                                            float scale, float* __restrict__ o, const int* status) {
+constexpr int af_smem_bytes() {
+  return (AF_KC * (DH + 1) + AF_KC * DH + AF_WARPS * AF_ROWS * DH) * 4;
+}
+
+template <int DH>
+__global__ void __launch_bounds__(AF_WARPS * 32) attention_f32_kernel(
+    const float* __restrict__ q, const float* __restrict__ k, const float* __restrict__ v, const int32_t* __restrict__ cu,
+    const int2* __restrict__ items, const int* __restrict__ count, int n_tokens, int H, float scale,
+    float* __restrict__ o, uint16_t* __restrict__ o_split, int* status) {
   if (status && (*reinterpret_cast<const volatile int*>(status) & kDevLayout)) return;
   constexpr int PL = DH / 32;
-  const int lane = threadIdx.x & 31;
-  const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (w >= n * H) return;
-  const int i = w / H, h = w - i * H;
+  extern __shared__ float af_smem[];
+  float* sk = af_smem;                           // [KC][DH + 1] (padded: lane j reads row j)
+  float* sv = sk + AF_KC * (DH + 1);             // [KC][DH]
+  float* sq = sv + AF_KC * DH;                   // [warps][rows][DH]
+  const int quarter = blockIdx.x & 3, item_idx = blockIdx.x >> 2, h = blockIdx.y;
+  if (item_idx >= *count) return;
+  const int2 it = items[item_idx];
+  const int a = cu[it.x], b = cu[it.x + 1];
   const int d = H * DH;
-  const int doc = doc_ids[i];
-  const int a = cu[doc], b = cu[doc + 1];
-  float qv[PL], ov[PL];
-#pragma unroll
-  for (int e = 0; e < PL; ++e) {
-    qv[e] = q[(size_t)i * d + h * DH + lane * PL + e];
-    ov[e] = 0.f;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r0 = it.y + quarter * 32 + warp * AF_ROWS;  // this warp's first row
+  if (it.y + quarter * 32 >= b) return;                  // the whole CTA is past the document's end
+  float* myq = sq + warp * AF_ROWS * DH;
+  for (int i = 0; i < AF_ROWS; ++i) {
+    const int r = r0 + i;
+    for (int e = lane; e < DH; e += 32) myq[i * DH + e] = r < b ? q[(size_t)r * d + h * DH + e] : 0.f;
   }
-  float m = -INFINITY, l = 0.f;
-  for (int j = a; j < b; ++j) {
-    float s = 0.f;
+  float m[AF_ROWS], l[AF_ROWS], acc[AF_ROWS][PL];
 #pragma unroll
-    for (int e = 0; e < PL; ++e) s = fmaf(qv[e], k[(size_t)j * d + h * DH + lane * PL + e], s);
+  for (int i = 0; i < AF_ROWS; ++i) {
+    m[i] = -INFINITY;
+    l[i] = 0.f;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    s *= scale;
-    const float mn = fmaxf(m, s);
-    const float corr = expf(m - mn);  // 0 for the first key
-    const float p = expf(s - mn);
-    l = l * corr + p;
-#pragma unroll
-    for (int e = 0; e < PL; ++e) ov[e] = fmaf(p, v[(size_t)j * d + h * DH + lane * PL + e], ov[e] * corr);
-    m = mn;
+    for (int e = 0; e < PL; ++e) acc[i][e] = 0.f;
   }
-  const float inv = 1.0f / l;
+  for (int c0 = a; c0 < b; c0 += AF_KC) {
+    const int nk = b - c0 < AF_KC ? b - c0 : AF_KC;
+    __syncthreads();  // the previous chunk is no longer read
+    for (int idx = threadIdx.x; idx < AF_KC * DH; idx += blockDim.x) {
+      const int j = idx / DH, e = idx - j * DH;
+      const bool in = j < nk;
+      sk[j * (DH + 1) + e] = in ? k[(size_t)(c0 + j) * d + h * DH + e] : 0.f;
+      sv[j * DH + e] = in ? v[(size_t)(c0 + j) * d + h * DH + e] : 0.f;
+    }
+    __syncthreads();
 #pragma unroll
-  for (int e = 0; e < PL; ++e) o[(size_t)i * d + h * DH + lane * PL + e] = ov[e] * inv;
+    for (int i = 0; i < AF_ROWS; ++i) {
+      if (r0 + i >= b) continue;  // warp-uniform
+      const float* qi = myq + i * DH;
+      const float* kj = sk + lane * (DH + 1);
+      float s = 0.f;
+#pragma unroll 8
+      for (int e = 0; e < DH; ++e) s = fmaf(qi[e], kj[e], s);
+      s = lane < nk ? s * scale : -INFINITY;
+      float cm = s;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
+      const float mn = fmaxf(m[i], cm);
+      const float alpha = expf(m[i] - mn);  // 0 on the first chunk (m = -inf)
+      const float p = lane < nk ? expf(s - mn) : 0.f;
+      float ps = p;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+      l[i] = l[i] * alpha + ps;
+#pragma unroll
+      for (int e = 0; e < PL; ++e) acc[i][e] *= alpha;
+      for (int j = 0; j < nk; ++j) {
+        const float pj = __shfl_sync(0xffffffffu, p, j);
+#pragma unroll
+        for (int e = 0; e < PL; ++e) acc[i][e] = fmaf(pj, sv[j * DH + lane * PL + e], acc[i][e]);
+      }
+      m[i] = mn;
+    }
+  }
+  bool over = false;
+#pragma unroll
+  for (int i = 0; i < AF_ROWS; ++i) {
+    const int r = r0 + i;
+    if (r >= b) continue;
+    const float inv = 1.0f / l[i];
+    float ov[PL];
+#pragma unroll
+    for (int e = 0; e < PL; ++e) ov[e] = acc[i][e] * inv;
+    const size_t at = (size_t)r * d + h * DH + lane * PL;
+    if (o_split) {
+      if constexpr (PL % 4 == 0) {
+#pragma unroll
+        for (int e = 0; e < PL; e += 4) {
+          const float v4[4] = {ov[e], ov[e + 1], ov[e + 2], ov[e + 3]};
+          over |= store_f16_split4(v4, kF16x3ActExp, o_split + at + e, o_split + (size_t)n_tokens * d + at + e);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < PL; ++e) {
+          const float x = ldexpf(ov[e], kF16x3ActExp);
+          over |= fabsf(x) > kF16Max;
+          const __half hh = __float2half_rn(x);
+          o_split[at + e] = __half_as_ushort(hh);
+          o_split[(size_t)n_tokens * d + at + e] = __half_as_ushort(__float2half_rn(__fsub_rn(x, __half2float(hh))));
+        }
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < PL; ++e) o[at + e] = ov[e];
+    }
+  }
+  if (over && status) atomicOr(status, kDevRange);
 }
 
 // to_frames = 1: channel-major per document (document j is [io, len_j] at offset io * cu[j]) ->
@@ -587,23 +679,33 @@ cudaError_t sgemm_reduce_qkv_launch(const float* part, int S, int M, int d, int 
 }
 
 cudaError_t sgemm_reduce_swiglu_launch(const float* part, int S, int M, int F, const float* bias, float* h,
-                                       const int* status, cudaStream_t s) {
-  sgemm_reduce_swiglu_kernel<<<ew_grid((size_t)M * F), 256, 0, s>>>(part, S, M, F, bias, h, status);
+                                       uint16_t* h_split, int* status, cudaStream_t s) {
+  if (F % 4) return cudaErrorInvalidValue;
+  sgemm_reduce_swiglu_kernel<<<ew_grid((size_t)M * F / 4), 256, 0, s>>>(part, S, M, F, bias, h, h_split, status);
   return cudaGetLastError();
 }
 
-cudaError_t attention_f32_launch(const float* q, const float* k, const float* v, const int32_t* cu,
-                                 const int32_t* doc_ids, int n, int H, int Dh, float* o, const int* status,
-                                 cudaStream_t s) {
-  const long long warps = (long long)n * H;
-  const int blocks = (int)((warps * 32 + 255) / 256);
+cudaError_t attention_f32_launch(const float* q, const float* k, const float* v, const int32_t* cu, const int2* items,
+                                 const int* count, int max_items, int n_tokens, int H, int Dh, float* o,
+                                 uint16_t* o_split, int* status, cudaStream_t s) {
+  if (max_items <= 0) return cudaSuccess;
+  const dim3 grid(max_items * 4, H);
   const float scale = (float)(1.0 / sqrt((double)Dh));
-  if (Dh == 128)
-    attention_f32_kernel<128><<<blocks, 256, 0, s>>>(q, k, v, cu, doc_ids, n, H, scale, o, status);
-  else if (Dh == 64)
-    attention_f32_kernel<64><<<blocks, 256, 0, s>>>(q, k, v, cu, doc_ids, n, H, scale, o, status);
-  else
+  if (Dh == 128) {
+    static unsigned long long set = 0;
+    cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(attention_f32_kernel<128>), af_smem_bytes<128>(), &set);
+    if (e != cudaSuccess) return e;
+    attention_f32_kernel<128><<<grid, AF_WARPS * 32, af_smem_bytes<128>(), s>>>(q, k, v, cu, items, count, n_tokens,
+                                                                              H, scale, o, o_split, status);
+  } else if (Dh == 64) {
+    static unsigned long long set = 0;
+    cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(attention_f32_kernel<64>), af_smem_bytes<64>(), &set);
+    if (e != cudaSuccess) return e;
+    attention_f32_kernel<64><<<grid, AF_WARPS * 32, af_smem_bytes<64>(), s>>>(q, k, v, cu, items, count, n_tokens, H,
+                                                                            scale, o, o_split, status);
+  } else {
     return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 

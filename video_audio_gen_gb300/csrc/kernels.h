@@ -93,7 +93,8 @@ cudaError_t attention_schedule_launch(const int32_t* cu, int n_docs, int n_token
 int attention_max_items(int n_docs, int n_tokens);
 
 // Elementwise / reduction kernels.
-// out_kind: 0 bf16, 1 fp32, 2 f16 (values beyond f16's finite range set kDevRange in *status).
+// out_kind: 0 bf16, 1 fp32, 2 f16 (values beyond f16's finite range set kDevRange in *status),
+// 3 the 3xF16 GEMM's operand: f16 hi [n][d] at y and lo [n][d] right after it, of y * 2^kF16x3ActExp.
 cudaError_t norm_modulate_launch(const float* x, const float* x_lo, int n, int d, int norm, float eps, const float* ln_g,
                                  const float* ln_b, const uint8_t* tags, const float* shift, const float* scale,
                                  long long mod_stride, void* y, int out_kind, int* status, cudaStream_t s);
@@ -182,11 +183,16 @@ cudaError_t sgemm_reduce_store_launch(const float* part, int S, int M, int N, co
 cudaError_t sgemm_reduce_qkv_launch(const float* part, int S, int M, int d, int Dh, int half, const float* bias,
                                     const float* cs, const float* sn, float* q, float* k, float* v, const int* status,
                                     cudaStream_t s);
+// h_split: when given, h is written as the 3xF16 GEMM's operand (f16 hi [M][F] then lo [M][F] of
+// h * 2^kF16x3ActExp) instead of fp32 into h.
 cudaError_t sgemm_reduce_swiglu_launch(const float* part, int S, int M, int F, const float* bias, float* h,
-                                       const int* status, cudaStream_t s);
-cudaError_t attention_f32_launch(const float* q, const float* k, const float* v, const int32_t* cu,
-                                 const int32_t* doc_ids, int n, int H, int Dh, float* o, const int* status,
-                                 cudaStream_t s);
+                                       uint16_t* h_split, int* status, cudaStream_t s);
+// Exact fp32 attention over the (document, 128-row q-tile) list of attention_schedule_launch.
+// o_split: when given, o is written as the 3xF16 GEMM's operand (f16 hi [n][d] then lo [n][d] of
+// o * 2^kF16x3ActExp, n_tokens rows) instead of fp32 into o.
+cudaError_t attention_f32_launch(const float* q, const float* k, const float* v, const int32_t* cu, const int2* items,
+                                 const int* count, int max_items, int n_tokens, int H, int Dh, float* o,
+                                 uint16_t* o_split, int* status, cudaStream_t s);
 cudaError_t io_transpose_launch(const float* src, float* dst, const int32_t* cu, const int32_t* doc_ids, int n, int io,
                                 int to_frames, const int* status, cudaStream_t s);
 
