@@ -700,7 +700,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="long_doc_bf16",
                     choices=["video_audio_bf16", "long_doc_bf16", "denoise_loop", "t2va_loop", "music_fp32",
-                             "video_audio_bf16_l1", "long_doc_bf16_l1", "video_audio_nvfp4", "tiny", "ragged", "music_small", "nvfp4_gemm", "vit3d_decoder",
+                             "video_audio_bf16_l1", "long_doc_bf16_l1", "video_audio_nvfp4", "tiny", "ragged", "music_small", "music_fp32_l2", "nvfp4_gemm", "vit3d_decoder",
                              "vit3d_small"])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -226,6 +226,13 @@ WORKLOADS = {
                             dict(video=(1, 1, 1), audio=5), dict(video=(5, 5, 5), audio=3),
                             dict(video=(1, 3, 3)), dict(video=(2, 16, 8), audio=1)],
                       t=0.61, w_std=0.02, bias_std=0.02, x_std=1.0),
+    # Two blocks of the music model on its full 172-frame batch: every launch has the full workload's
+    # shape, with about 0.6 GB on the device (profiling captures).
+    "music_fp32_l2": dict(model=_model(n_blocks=2, hidden=2048, n_heads=16, head_dim=128, ffn_hidden=8192,
+                                       norm="ln", norm_eps=1e-5, adaln=False, n_mod=1, rope_axes=1,
+                                       rope_dims=(64, 0, 0), rotary_dim=64, io_channels=128, dtype="fp32"),
+                          seed=1, docs=[dict(frames=86), dict(frames=86)], t=0.0, w_std=0.02, bias_std=0.02,
+                          x_std=1.0),
     "music_small": dict(model=_model(n_blocks=2, hidden=256, n_heads=2, head_dim=128, ffn_hidden=1024,
                                      norm="ln", norm_eps=1e-5, adaln=False, n_mod=1, rope_axes=1,
                                      rope_dims=(64, 0, 0), rotary_dim=64, io_channels=128, dtype="fp32"),

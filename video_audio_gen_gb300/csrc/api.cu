@@ -368,7 +368,7 @@ dit_status bind_fp32(dit_handle* h, const dit_weights* w, cudaStream_t s) {
     if (e == cudaSuccess) e = absmax_launch(static_cast<const float*>(src), n, maxbuf, s);
     if (e == cudaSuccess)
       e = f16_split_launch(static_cast<const float*>(src), K, K, (int)rows, K, maxbuf, 0, out->e, out->hi, out->lo,
-                           nullptr, s);
+                           nullptr, s, 1);
     return e == cudaSuccess;
   };
   for (int l = 0; l < c.n_blocks; ++l) {
@@ -422,7 +422,7 @@ struct Sgemm {
     const int want = f16x3_splits(M, N, K);
     S = f16x3_effective_splits(K, want);
     return f16x3_partial_launch(xs, xs + (size_t)M * K, W.hi, W.lo, W.e, kF16x3ActExp, M, N, K, want, part, status,
-                                s);
+                                s, 1);
   }
   cudaError_t run(const float* X, const SplitW16& W, int M, int N, int K) {
     cudaError_t e = f16_split_launch(X, K, K, M, K, nullptr, kF16x3ActExp, nullptr, xs, xs + (size_t)M * K, status, s);

@@ -257,6 +257,19 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
   return d;
 }
 
+// The same for a K-major tile in rows of 64 bytes (what a TMA load with CU_TENSOR_MAP_SWIZZLE_64B
+// writes for a box whose inner extent is 32 16-bit elements): 8-row groups are 512 bytes apart;
+// layout 4 = SWIZZLE_64B.  The tile must start on a 512-byte boundary.
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(1u) << 16;
+  d |= static_cast<uint64_t>(512u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(4u) << 61;
+  return d;
+}
+
 // 32 lanes x 32 consecutive 32-bit TMEM columns: thread i of the warp gets lane (base + i),
 // columns [col, col + 32).  Must be followed by tmem_ld_wait() before the registers are read.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {

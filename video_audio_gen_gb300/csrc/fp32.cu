@@ -29,6 +29,21 @@ __device__ __forceinline__ float sum_parts(const float* __restrict__ part, int S
   return v;
 }
 
+// Sum of the S partials of the four consecutive elements at idx (a multiple of 4), in split order.
+__device__ __forceinline__ float4 sum_parts4(const float* __restrict__ part, int S, size_t MN, size_t idx) {
+  float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = 0; s < S; ++s) {
+    const float4 p = __ldcs(reinterpret_cast<const float4*>(part + (size_t)s * MN + idx));
+    v.x += p.x;
+    v.y += p.y;
+    v.z += p.z;
+    v.w += p.w;
+  }
+  return v;
+}
+
+// The reductions run on a 2-D grid: x = 4-column groups of a row (256 threads, 1024 columns per
+// block), y = rows (grid-stride), so no index needs a 64-bit division.  N is a multiple of 4.
 // out = sum + bias (add = 0: store into out [M, N]; add = 1: out[M, N] += sum + bias).  With `lo`
 // the residual is a compensated pair (out = high part, lo = low part): the add is an exact TwoSum
 // whose rounding error goes into lo, so the residual stream keeps about twice fp32's precision.
@@ -37,26 +52,41 @@ __global__ void sgemm_reduce_store_kernel(const float* __restrict__ part, int S,
                                           float* __restrict__ lo, const int* status) {
   if (status && (*reinterpret_cast<const volatile int*>(status) & kDevLayout)) return;
   const size_t MN = (size_t)M * N;
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < MN; i += (size_t)gridDim.x * blockDim.x) {
-    const float v = sum_parts(part, S, MN, i) + (bias ? bias[i % N] : 0.f);
+  const int c = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (c >= N) return;
+  const float4 b4 = bias ? *reinterpret_cast<const float4*>(bias + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int r = blockIdx.y; r < M; r += gridDim.y) {
+    const size_t i = (size_t)r * N + c;
+    const float4 p = sum_parts4(part, S, MN, i);
+    const float v[4] = {p.x + b4.x, p.y + b4.y, p.z + b4.z, p.w + b4.w};
+    float4* o4 = reinterpret_cast<float4*>(out + i);
     if (!add) {
-      out[i] = v;
-      if (lo) lo[i] = 0.f;
+      *o4 = make_float4(v[0], v[1], v[2], v[3]);
+      if (lo) *reinterpret_cast<float4*>(lo + i) = make_float4(0.f, 0.f, 0.f, 0.f);
     } else if (lo) {
-      const float a = out[i];
-      const float s = __fadd_rn(a, v);
-      const float bb = __fsub_rn(s, a);
-      const float err = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(v, bb));
-      out[i] = s;
-      lo[i] = __fadd_rn(lo[i], err);
+      const float4 a4 = *o4, l4 = *reinterpret_cast<const float4*>(lo + i);
+      const float a[4] = {a4.x, a4.y, a4.z, a4.w}, l[4] = {l4.x, l4.y, l4.z, l4.w};
+      float so[4], lo_[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float s = __fadd_rn(a[e], v[e]);
+        const float bb = __fsub_rn(s, a[e]);
+        const float err = __fadd_rn(__fsub_rn(a[e], __fsub_rn(s, bb)), __fsub_rn(v[e], bb));
+        so[e] = s;
+        lo_[e] = __fadd_rn(l[e], err);
+      }
+      *o4 = make_float4(so[0], so[1], so[2], so[3]);
+      *reinterpret_cast<float4*>(lo + i) = make_float4(lo_[0], lo_[1], lo_[2], lo_[3]);
     } else {
-      out[i] = out[i] + v;
+      const float4 a4 = *o4;
+      *o4 = make_float4(a4.x + v[0], a4.y + v[1], a4.z + v[2], a4.w + v[3]);
     }
   }
 }
 
-// [q | k | v] = sum + bias, NeoX rotate_half over the first R dims of each q/k head, stored fp32
-// [M, d] each.
+// [q | k | v] = sum + bias, NeoX rotate_half over the first R = 2 half dims of each q/k head, stored
+// fp32 [M, d] each.  A 4-column group never straddles a head, a segment or the rotary boundary
+// (d, Dh and half are multiples of 4).
 __global__ void sgemm_reduce_qkv_kernel(const float* __restrict__ part, int S, int M, int d, int Dh, int half,
                                         const float* __restrict__ bias, const float* __restrict__ cs,
                                         const float* __restrict__ sn, float* __restrict__ q, float* __restrict__ k,
@@ -64,24 +94,33 @@ __global__ void sgemm_reduce_qkv_kernel(const float* __restrict__ part, int S, i
   if (status && (*reinterpret_cast<const volatile int*>(status) & kDevLayout)) return;
   const int N = 3 * d;
   const size_t MN = (size_t)M * N;
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < MN; i += (size_t)gridDim.x * blockDim.x) {
-    const int r = (int)(i / N), c = (int)(i - (size_t)r * N);
-    const int seg = c / d, cc = c - seg * d;
-    const float x = sum_parts(part, S, MN, i) + (bias ? bias[c] : 0.f);
-    if (seg == 2) {
-      v[(size_t)r * d + cc] = x;
-      continue;
+  const int c0 = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (c0 >= N) return;
+  const int seg = c0 / d, cc = c0 - seg * d;
+  const int jd = cc % Dh;  // dim within the head
+  const bool rot = seg < 2 && jd < 2 * half;
+  const int j = jd < half ? jd : jd - half;
+  const int pc = jd < half ? c0 + half : c0 - half;  // partner columns
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float4 b4 = bias ? *reinterpret_cast<const float4*>(bias + c0) : zero;
+  const float4 pb4 = bias && rot ? *reinterpret_cast<const float4*>(bias + pc) : zero;
+  float* dst = seg == 0 ? q : (seg == 1 ? k : v);
+  for (int r = blockIdx.y; r < M; r += gridDim.y) {
+    float4 x = sum_parts4(part, S, MN, (size_t)r * N + c0);
+    x = make_float4(x.x + b4.x, x.y + b4.y, x.z + b4.z, x.w + b4.w);
+    if (rot) {
+      float4 y = sum_parts4(part, S, MN, (size_t)r * N + pc);
+      y = make_float4(y.x + pb4.x, y.y + pb4.y, y.z + pb4.z, y.w + pb4.w);
+      const float4 co = *reinterpret_cast<const float4*>(cs + (size_t)r * half + j);
+      const float4 si = *reinterpret_cast<const float4*>(sn + (size_t)r * half + j);
+      if (jd < half)
+        x = make_float4(x.x * co.x - y.x * si.x, x.y * co.y - y.y * si.y, x.z * co.z - y.z * si.z,
+                        x.w * co.w - y.w * si.w);
+      else
+        x = make_float4(x.x * co.x + y.x * si.x, x.y * co.y + y.y * si.y, x.z * co.z + y.z * si.z,
+                        x.w * co.w + y.w * si.w);
     }
-    const int jd = cc % Dh;  // dim within the head
-    float o = x;
-    if (jd < 2 * half) {
-      const int j = jd < half ? jd : jd - half;
-      const int pc = jd < half ? c + half : c - half;  // partner column
-      const float y = sum_parts(part, S, MN, (size_t)r * N + pc) + (bias ? bias[pc] : 0.f);
-      const float co = cs[(size_t)r * half + j], si = sn[(size_t)r * half + j];
-      o = jd < half ? x * co - y * si : x * co + y * si;
-    }
-    (seg == 0 ? q : k)[(size_t)r * d + cc] = o;
+    *reinterpret_cast<float4*>(dst + (size_t)r * d + cc) = x;
   }
 }
 
@@ -92,19 +131,21 @@ __global__ void sgemm_reduce_swiglu_kernel(const float* __restrict__ part, int S
                                            uint16_t* __restrict__ h_split, int* status) {
   if (status && (*reinterpret_cast<const volatile int*>(status) & kDevLayout)) return;
   const size_t MN = (size_t)M * 2 * F;
-  const size_t total = (size_t)M * F / 4;
+  const int f0 = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (f0 >= F) return;
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float4 bu = bias ? *reinterpret_cast<const float4*>(bias + f0) : zero;
+  const float4 bg = bias ? *reinterpret_cast<const float4*>(bias + F + f0) : zero;
   bool over = false;
-  for (size_t i4 = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i4 < total; i4 += (size_t)gridDim.x * blockDim.x) {
-    const size_t i = i4 * 4;
-    const int r = (int)(i / F), f0 = (int)(i - (size_t)r * F);
+  for (int r = blockIdx.y; r < M; r += gridDim.y) {
+    const float4 u4 = sum_parts4(part, S, MN, (size_t)r * 2 * F + f0);
+    const float4 g4 = sum_parts4(part, S, MN, (size_t)r * 2 * F + F + f0);
+    const float u[4] = {u4.x + bu.x, u4.y + bu.y, u4.z + bu.z, u4.w + bu.w};
+    const float g[4] = {g4.x + bg.x, g4.y + bg.y, g4.z + bg.z, g4.w + bg.w};
     float hv[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int f = f0 + e;
-      const float u = sum_parts(part, S, MN, (size_t)r * 2 * F + f) + (bias ? bias[f] : 0.f);
-      const float g = sum_parts(part, S, MN, (size_t)r * 2 * F + F + f) + (bias ? bias[F + f] : 0.f);
-      hv[e] = u * (g / (1.0f + expf(-g)));
-    }
+    for (int e = 0; e < 4; ++e) hv[e] = u[e] * (g[e] / (1.0f + expf(-g[e])));
+    const size_t i = (size_t)r * F + f0;
     if (h_split)
       over |= store_f16_split4(hv, kF16x3ActExp, h_split + i, h_split + (size_t)M * F + i);
     else
@@ -115,17 +156,24 @@ __global__ void sgemm_reduce_swiglu_kernel(const float* __restrict__ part, int S
 
 // Exact fp32 softmax attention over the document of each row.  One CTA per (document, 128-row
 // q-tile, head, 32-row quarter), 4 warps of 8 query rows each.  The document's keys and values pass
-// through shared memory 32 at a time (lane j scores key j of the chunk); every row keeps an exact fp32
-// online softmax (running max m, sum l, accumulator o, each chunk rescaled by exp(m_old - m_new)):
+// through shared memory 32 at a time (lane j scores key j of the chunk for all 8 rows of its warp);
+// every row keeps an exact fp32 online softmax (running max m, sum l, accumulator o, each chunk
+// rescaled by exp(m_old - m_new)):
 //     o_i = sum_j exp(s_ij - m_i) v_j / sum_j exp(s_ij - m_i),   s_ij = q_i . k_j / sqrt(Dh)
-// Lane l accumulates output dims [l * DH / 32, (l + 1) * DH / 32).
+// Lane l accumulates output dims [l * DH / 32, (l + 1) * DH / 32).  The next chunk's keys and values
+// are loaded into registers while the current one is scored.
 constexpr int AF_KC = 32;      // keys per chunk
 constexpr int AF_ROWS = 8;     // query rows per warp
 constexpr int AF_WARPS = 4;
 
 template <int DH>
+__host__ __device__ constexpr int af_kstride() {
+  return DH + 4;  // float4 rows; lanes 8 apart fall in one 128-byte phase, conflict-free
+}
+
+template <int DH>
 constexpr int af_smem_bytes() {
-  return (AF_KC * (DH + 1) + AF_KC * DH + AF_WARPS * AF_ROWS * DH) * 4;
+  return (AF_KC * af_kstride<DH>() + AF_KC * DH + AF_WARPS * AF_ROWS * DH) * 4;
 }
 
 template <int DH>
@@ -135,10 +183,14 @@ __global__ void __launch_bounds__(AF_WARPS * 32) attention_f32_kernel(
     float* __restrict__ o, uint16_t* __restrict__ o_split, int* status) {
   if (status && (*reinterpret_cast<const volatile int*>(status) & kDevLayout)) return;
   constexpr int PL = DH / 32;
-  extern __shared__ float af_smem[];
-  float* sk = af_smem;                           // [KC][DH + 1] (padded: lane j reads row j)
-  float* sv = sk + AF_KC * (DH + 1);             // [KC][DH]
-  float* sq = sv + AF_KC * DH;                   // [warps][rows][DH]
+  constexpr int KS = af_kstride<DH>();
+  constexpr int D4 = DH / 4;
+  constexpr int LD = AF_KC * D4 / (AF_WARPS * 32);  // float4 of K (and of V) per thread per chunk
+  static_assert(AF_KC * D4 % (AF_WARPS * 32) == 0, "chunk load must divide evenly");
+  extern __shared__ float4 af_smem4[];
+  float* sk = reinterpret_cast<float*>(af_smem4);  // [KC][KS]
+  float* sv = sk + AF_KC * KS;                     // [KC][DH]
+  float* sq = sv + AF_KC * DH;                     // [warps][rows][DH]
   const int quarter = blockIdx.x & 3, item_idx = blockIdx.x >> 2, h = blockIdx.y;
   if (item_idx >= *count) return;
   const int2 it = items[item_idx];
@@ -148,10 +200,28 @@ __global__ void __launch_bounds__(AF_WARPS * 32) attention_f32_kernel(
   const int r0 = it.y + quarter * 32 + warp * AF_ROWS;  // this warp's first row
   if (it.y + quarter * 32 >= b) return;                  // the whole CTA is past the document's end
   float* myq = sq + warp * AF_ROWS * DH;
-  for (int i = 0; i < AF_ROWS; ++i) {
+#pragma unroll
+  for (int t = lane; t < AF_ROWS * D4; t += 32) {
+    const int i = t / D4, e4 = t - i * D4;
     const int r = r0 + i;
-    for (int e = lane; e < DH; e += 32) myq[i * DH + e] = r < b ? q[(size_t)r * d + h * DH + e] : 0.f;
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (r < b) x = *reinterpret_cast<const float4*>(q + (size_t)r * d + h * DH + e4 * 4);
+    *reinterpret_cast<float4*>(myq + i * DH + e4 * 4) = x;
   }
+  float4 nk4[LD], nv4[LD];
+  auto fetch = [&](int c0) {
+#pragma unroll
+    for (int u = 0; u < LD; ++u) {
+      const int t = threadIdx.x + u * AF_WARPS * 32;
+      const int j = t / D4, e4 = t - j * D4;
+      nk4[u] = nv4[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (c0 + j < b) {
+        const size_t at = (size_t)(c0 + j) * d + h * DH + e4 * 4;
+        nk4[u] = *reinterpret_cast<const float4*>(k + at);
+        nv4[u] = *reinterpret_cast<const float4*>(v + at);
+      }
+    }
+  };
   float m[AF_ROWS], l[AF_ROWS], acc[AF_ROWS][PL];
 #pragma unroll
   for (int i = 0; i < AF_ROWS; ++i) {
@@ -160,43 +230,68 @@ __global__ void __launch_bounds__(AF_WARPS * 32) attention_f32_kernel(
 #pragma unroll
     for (int e = 0; e < PL; ++e) acc[i][e] = 0.f;
   }
+  fetch(a);
   for (int c0 = a; c0 < b; c0 += AF_KC) {
     const int nk = b - c0 < AF_KC ? b - c0 : AF_KC;
     __syncthreads();  // the previous chunk is no longer read
-    for (int idx = threadIdx.x; idx < AF_KC * DH; idx += blockDim.x) {
-      const int j = idx / DH, e = idx - j * DH;
-      const bool in = j < nk;
-      sk[j * (DH + 1) + e] = in ? k[(size_t)(c0 + j) * d + h * DH + e] : 0.f;
-      sv[j * DH + e] = in ? v[(size_t)(c0 + j) * d + h * DH + e] : 0.f;
+#pragma unroll
+    for (int u = 0; u < LD; ++u) {
+      const int t = threadIdx.x + u * AF_WARPS * 32;
+      const int j = t / D4, e4 = t - j * D4;
+      *reinterpret_cast<float4*>(sk + j * KS + e4 * 4) = nk4[u];
+      *reinterpret_cast<float4*>(sv + j * DH + e4 * 4) = nv4[u];
     }
     __syncthreads();
+    if (c0 + AF_KC < b) fetch(c0 + AF_KC);
+    float s[AF_ROWS];
+#pragma unroll
+    for (int i = 0; i < AF_ROWS; ++i) s[i] = 0.f;
+    const float4* kj = reinterpret_cast<const float4*>(sk + lane * KS);
+#pragma unroll 4
+    for (int e4 = 0; e4 < D4; ++e4) {
+      const float4 kv = kj[e4];
+#pragma unroll
+      for (int i = 0; i < AF_ROWS; ++i) {
+        const float4 qv = reinterpret_cast<const float4*>(myq + i * DH)[e4];
+        s[i] = fmaf(qv.x, kv.x, s[i]);
+        s[i] = fmaf(qv.y, kv.y, s[i]);
+        s[i] = fmaf(qv.z, kv.z, s[i]);
+        s[i] = fmaf(qv.w, kv.w, s[i]);
+      }
+    }
+    float p[AF_ROWS];
 #pragma unroll
     for (int i = 0; i < AF_ROWS; ++i) {
-      if (r0 + i >= b) continue;  // warp-uniform
-      const float* qi = myq + i * DH;
-      const float* kj = sk + lane * (DH + 1);
-      float s = 0.f;
-#pragma unroll 8
-      for (int e = 0; e < DH; ++e) s = fmaf(qi[e], kj[e], s);
-      s = lane < nk ? s * scale : -INFINITY;
-      float cm = s;
+      const float si = lane < nk ? s[i] * scale : -INFINITY;
+      float cm = si;
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
       const float mn = fmaxf(m[i], cm);
       const float alpha = expf(m[i] - mn);  // 0 on the first chunk (m = -inf)
-      const float p = lane < nk ? expf(s - mn) : 0.f;
-      float ps = p;
+      p[i] = lane < nk ? expf(si - mn) : 0.f;
+      float ps = p[i];
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
       l[i] = l[i] * alpha + ps;
 #pragma unroll
       for (int e = 0; e < PL; ++e) acc[i][e] *= alpha;
-      for (int j = 0; j < nk; ++j) {
-        const float pj = __shfl_sync(0xffffffffu, p, j);
-#pragma unroll
-        for (int e = 0; e < PL; ++e) acc[i][e] = fmaf(pj, sv[j * DH + lane * PL + e], acc[i][e]);
-      }
       m[i] = mn;
+    }
+    for (int j = 0; j < nk; ++j) {
+      float vv[PL];
+      if constexpr (PL == 4) {
+        const float4 x = reinterpret_cast<const float4*>(sv + j * DH)[lane];
+        vv[0] = x.x; vv[1] = x.y; vv[2] = x.z; vv[3] = x.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < PL; ++e) vv[e] = sv[j * DH + lane * PL + e];
+      }
+#pragma unroll
+      for (int i = 0; i < AF_ROWS; ++i) {
+        const float pj = __shfl_sync(0xffffffffu, p[i], j);
+#pragma unroll
+        for (int e = 0; e < PL; ++e) acc[i][e] = fmaf(pj, vv[e], acc[i][e]);
+      }
     }
   }
   bool over = false;
@@ -260,35 +355,48 @@ __global__ void io_transpose_kernel(const float* __restrict__ src, float* __rest
 // drops only a_lo b_lo and the rounding of the low parts, about 2^-21 of |a b| per product when T
 // has an 11-bit significand.  Two types serve:
 //   tf32 (kind::tf32, 32 K per 128-byte row): x_hi = tf32(x), x_lo = tf32(x - x_hi)
-//   f16  (kind::f16,  64 K per 128-byte row): x_hi = f16(x 2^e), x_lo = f16(x 2^e - x_hi), with e
+//   f16  (kind::f16,  32 K per 64-byte row):  x_hi = f16(x 2^e), x_lo = f16(x 2^e - x_hi), with e
 //        chosen so that both parts stay in f16's normal range (per weight tensor from its largest
 //        magnitude; a fixed e for activations); the sums are scaled back by 2^-(e_w + e_x), exactly.
 //        kind::f16 runs at twice the tf32 rate and its two parts take 4 bytes per weight, so the
 //        weight stream is half of tf32's.
 // The tensor core's fp32 accumulation of these products is biased (measured on GB300: the error
 // of a TMEM accumulation grows linearly with its depth, about 2e-5 relative at K = 2048), so the
-// MMAs accumulate only one stage (12 MMAs: 4 K-steps x 3 products), alternately into two TMEM
-// accumulators, and the epilogue adds each chunk into fp32 running sums in registers (round to
-// nearest).  The roles are transposed so that the small token count sits on the MMA's N side: one
+// MMAs accumulate only one chunk (64 K for f16: two stages of 2 K-steps x 3 products; 32 K for tf32:
+// one stage of 4), alternately into two TMEM accumulators, and the epilogue adds each chunk into
+// fp32 running sums in registers (round to nearest).  The roles are transposed so that the small token count sits on the MMA's N side: one
 // CTA owns 128 output features (M = 128 rows of W) x NT tokens (N = NT <= 256, all the tokens of a
 // music forward in one tile) x one K split, and writes part[split][token][feature] for the same
-// fixed-order reductions as before.
-//   warp 0     TMA producer: W_hi, W_lo [128 x 128 B] and X_hi, X_lo [NT x 128 B] per stage
-//   warp 1     TMEM allocator + MMA issuer: 4 K-steps x 3 products per stage, one stage per chunk
+// fixed-order reductions as before.  At these token counts the weights stream from HBM at about
+// one byte per two tensor-core FLOPs, so the loads need depth: the stage ring is as deep as shared
+// memory allows (f16: five 38 KB stages of 64-byte rows at NT = 176; tf32: two of 128-byte rows).
+//   warp 0     TMA producer: W_hi, W_lo [128 x R] and X_hi, X_lo [NT x R] per stage (R row bytes)
+//   warp 1     TMEM allocator + MMA issuer: the chunk's cross products, then its hi x hi products
 //   warps 2-9  epilogue: TMEM lane = feature, column = token; two warps per lane quarter split the
 //              token columns; running sums in registers, coalesced stores along features
-constexpr int T3_ROW_BYTES = 128;                 // one 128-byte swizzled row of K per stage
 constexpr int T3_ROWS = kTf32x3N;                 // output features per CTA (MMA M)
-constexpr int T3_STAGES = 2;
-constexpr int T3_CHUNK = 1;                       // stages per accumulation chunk
-constexpr int T3_W_BYTES = T3_ROWS * T3_ROW_BYTES;  // 16 KB
+constexpr int T3_MAX_STAGES = 8;
 constexpr int T3_THREADS = 320;
 constexpr int T3_MAX_UNITS = 8;                   // 16-column units per epilogue warp (NT <= 256)
-constexpr int X3_F16_BK = 64;                     // K per stage, f16
+constexpr int T3_SMEM_MAX = 232448;               // opt-in dynamic shared memory per CTA
+constexpr int X3_F16_BK = 32;                     // K per stage, f16
 constexpr int X3_TF32_BK = kTf32x3K;              // K per stage, tf32 (32)
 
+// Stage geometry per operand type: one swizzled row of K per operand row and stage.
+template <bool F16>
+struct X3Geom {
+  static constexpr int ROW_BYTES = F16 ? 64 : 128;  // SWIZZLE_64B rows of 32 f16, SWIZZLE_128B of 32 tf32
+  static constexpr int BK = F16 ? X3_F16_BK : X3_TF32_BK;
+  static constexpr int KSTEPS = ROW_BYTES / 32;     // 32 bytes of K per MMA: 16 f16 or 8 tf32
+  static constexpr int W_BYTES = T3_ROWS * ROW_BYTES;
+  static constexpr int CHUNK = 1;                    // stages per TMEM accumulation chunk
+};
+
 struct T3Args {
-  int M, N, K, k_split, nt;
+  int M, N, K, k_split, nt, stages;
+  int w_tiled;  // f16: W in pre-swizzled [N / 128][K / 32][128][32] tiles, one 8 KB bulk copy per stage
+  const uint16_t* w_hi;
+  const uint16_t* w_lo;
   float* part;
   int* status;
   const int* w_exp;  // f16: the weight's scale exponent (device); the sums are scaled by 2^-(w_exp + x_exp)
@@ -300,16 +408,20 @@ __global__ void __launch_bounds__(T3_THREADS, 1)
     x3_partial_kernel(const __grid_constant__ CUtensorMap tmWhi, const __grid_constant__ CUtensorMap tmWlo,
                       const __grid_constant__ CUtensorMap tmXhi, const __grid_constant__ CUtensorMap tmXlo,
                       const T3Args a) {
-  constexpr int T3_BK = F16 ? X3_F16_BK : X3_TF32_BK;  // K elements per stage
+  using G = X3Geom<F16>;
+  constexpr int T3_BK = G::BK;  // K elements per stage
+  constexpr int T3_CHUNK = G::CHUNK;
+  constexpr int T3_W_BYTES = G::W_BYTES;
   if (a.status && (*reinterpret_cast<const volatile int*>(a.status) & kDevLayout)) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int nt = a.nt;
-  const int x_bytes = nt * T3_ROW_BYTES;
+  const int T3_STAGES = a.stages;
+  const int x_bytes = nt * G::ROW_BYTES;
   const int stage_bytes = 2 * T3_W_BYTES + 2 * x_bytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + T3_STAGES * stage_bytes);
-  uint64_t* empty = full + T3_STAGES;
-  uint64_t* chunk_full = empty + T3_STAGES;   // [2] an accumulator holds a finished chunk
+  uint64_t* empty = full + T3_MAX_STAGES;
+  uint64_t* chunk_full = empty + T3_MAX_STAGES;   // [2] an accumulator holds a finished chunk
   uint64_t* chunk_empty = chunk_full + 2;     // [2] the epilogue has added it to its running sums
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(chunk_empty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -341,15 +453,25 @@ __global__ void __launch_bounds__(T3_THREADS, 1)
 
   if (warp == 0) {
     if (lane == 0) {
+      // CTAs side by side start at different K blocks of their range, so that they do not all ask
+      // L2 for the same activation rows at the same time (the chunk sums are independent of order)
+      const int rot = n_kb > 0 ? (int)((long long)blockIdx.x * n_kb / gridDim.x) : 0;
       int i = 0;
       for (; i < n_kb; ++i) {
         const int st = i % T3_STAGES;
         if (!mbar_wait(&empty[st], ((i / T3_STAGES) & 1) ^ 1, abort_flag, a.status)) break;
         uint8_t* base = smem + st * stage_bytes;
-        const int k0 = kb + i * T3_BK;
+        const int j = i + rot < n_kb ? i + rot : i + rot - n_kb;
+        const int k0 = kb + j * T3_BK;
         mbar_arrive_expect_tx(&full[st], stage_bytes);
-        tma_load_2d(base, &tmWhi, &full[st], k0, n0);
-        tma_load_2d(base + T3_W_BYTES, &tmWlo, &full[st], k0, n0);
+        if (a.w_tiled) {
+          const size_t t = ((size_t)blockIdx.x * (a.K / T3_BK) + k0 / T3_BK) * (T3_ROWS * T3_BK);
+          bulk_load(base, a.w_hi + t, T3_W_BYTES, &full[st]);
+          bulk_load(base + T3_W_BYTES, a.w_lo + t, T3_W_BYTES, &full[st]);
+        } else {
+          tma_load_2d(base, &tmWhi, &full[st], k0, n0);
+          tma_load_2d(base + T3_W_BYTES, &tmWlo, &full[st], k0, n0);
+        }
         tma_load_2d(base + 2 * T3_W_BYTES, &tmXhi, &full[st], k0, m0);
         tma_load_2d(base + 2 * T3_W_BYTES + x_bytes, &tmXlo, &full[st], k0, m0);
       }
@@ -360,41 +482,47 @@ __global__ void __launch_bounds__(T3_THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       const uint32_t idesc = F16 ? idesc_f16_f32(T3_ROWS, nt) : idesc_tf32_f32(T3_ROWS, nt);
-      for (int i = 0; i < n_kb; ++i) {
-        const int st = i % T3_STAGES;
-        const int c = i / T3_CHUNK, cb = c & 1;
-        const bool chunk_start = (i % T3_CHUNK) == 0;
-        const bool chunk_end = (i % T3_CHUNK) == T3_CHUNK - 1 || i == n_kb - 1;
-        if (chunk_start && !mbar_wait(&chunk_empty[cb], ((c >> 1) & 1) ^ 1, abort_flag, a.status)) break;
-        if (!mbar_wait(&full[st], (i / T3_STAGES) & 1, abort_flag, a.status)) break;
+      // 32 bytes per instruction: K = 8 tf32 or 16 f16
+      auto mma = [&](uint32_t acc, uint32_t w, uint32_t x, uint32_t accumulate) {
+        if (F16)
+          umma_bf16(acc, sdesc_sw64(w), sdesc_sw64(x), idesc, accumulate);
+        else
+          umma_tf32(acc, sdesc_sw128(w), sdesc_sw128(x), idesc, accumulate);
+      };
+      bool ok = true;
+      for (int c = 0; c < n_chunks && ok; ++c) {
+        const int cb = c & 1;
+        const int i0 = c * T3_CHUNK, i1 = min(n_kb, i0 + T3_CHUNK);
+        if (!mbar_wait(&chunk_empty[cb], ((c >> 1) & 1) ^ 1, abort_flag, a.status)) break;
+        for (int i = i0; i < i1 && ok; ++i) ok = mbar_wait(&full[i % T3_STAGES], (i / T3_STAGES) & 1, abort_flag, a.status);
+        if (!ok) break;
         tc_fence_after();
         const uint32_t acc = tmem + cb * nt;
-        const uint32_t whi = smem_u32(smem + st * stage_bytes);
-        const uint32_t wlo = whi + T3_W_BYTES;
-        const uint32_t xhi = whi + 2 * T3_W_BYTES;
-        const uint32_t xlo = xhi + x_bytes;
-        // The small cross terms go first, while the accumulator is still about 2^-11 of its final
-        // size (their rounding is then negligible); the four hi x hi products come last.
-        // 32 bytes per instruction: K = 8 tf32 or 16 f16
-        auto mma = [&](uint32_t w, uint32_t x, uint32_t accumulate) {
-          if (F16)
-            umma_bf16(acc, sdesc_sw128(w), sdesc_sw128(x), idesc, accumulate);
-          else
-            umma_tf32(acc, sdesc_sw128(w), sdesc_sw128(x), idesc, accumulate);
-        };
+        // The small cross terms of every stage of the chunk go first, while the accumulator is still
+        // about 2^-11 of its final size (their rounding is then negligible); the hi x hi products last.
+        bool first = true;
+        for (int i = i0; i < i1; ++i) {
+          const uint32_t whi = smem_u32(smem + (i % T3_STAGES) * stage_bytes);
+          const uint32_t xhi = whi + 2 * T3_W_BYTES;
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint32_t off = ks * 32;
-          mma(whi + off, xlo + off, !(chunk_start && ks == 0));
-          mma(wlo + off, xhi + off, 1);
+          for (int ks = 0; ks < G::KSTEPS; ++ks) {
+            const uint32_t off = ks * 32;
+            mma(acc, whi + off, xhi + x_bytes + off, first ? 0u : 1u);
+            mma(acc, whi + T3_W_BYTES + off, xhi + off, 1);
+            first = false;
+          }
         }
+        for (int i = i0; i < i1; ++i) {
+          const uint32_t whi = smem_u32(smem + (i % T3_STAGES) * stage_bytes);
+          const uint32_t xhi = whi + 2 * T3_W_BYTES;
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint32_t off = ks * 32;
-          mma(whi + off, xhi + off, 1);
+          for (int ks = 0; ks < G::KSTEPS; ++ks) {
+            const uint32_t off = ks * 32;
+            mma(acc, whi + off, xhi + off, 1);
+          }
         }
-        umma_commit(&empty[st]);
-        if (chunk_end) umma_commit(&chunk_full[cb]);
+        for (int i = i0; i < i1; ++i) umma_commit(&empty[i % T3_STAGES]);
+        umma_commit(&chunk_full[cb]);
       }
     }
   } else {
@@ -508,11 +636,15 @@ __device__ __forceinline__ int weight_exp(unsigned int max_bits) {
 
 // x [M][K] (row stride ldx) -> hi, lo [M][Kp] f16 bits of x * 2^e, zero-padded for k >= K:
 //   hi = f16(x 2^e), lo = f16(x 2^e - hi)     (round to nearest even)
+// With `tiled` the outputs are laid out as the 3xF16 GEMM's weight tiles, [M / 128][Kp / 32][128][32],
+// each tile already in the shared-memory image of the 64-byte swizzle (16-byte chunk c of row r at
+// c ^ ((r >> 1) & 3)): every stage of the GEMM then reads one contiguous 8 KB block per part with a
+// plain bulk copy (M % 128 == 0, Kp % 32 == 0).
 // e is the weight exponent of *max_bits when given (and then written to *e_out by block 0), else
 // e_fixed.  A magnitude of x 2^e beyond 65504 sets kDevRange in *status.
 __global__ void f16_split_kernel(const float* __restrict__ x, long long ldx, int K, int M, int Kp,
                                  const unsigned int* __restrict__ max_bits, int e_fixed, int* __restrict__ e_out,
-                                 uint16_t* __restrict__ hi, uint16_t* __restrict__ lo, int* status) {
+                                 uint16_t* __restrict__ hi, uint16_t* __restrict__ lo, int tiled, int* status) {
   if (status && (*reinterpret_cast<const volatile int*>(status) & kDevLayout)) return;
   const int e = max_bits ? weight_exp(*max_bits) : e_fixed;
   if (e_out && blockIdx.x == 0 && threadIdx.x == 0) *e_out = e;
@@ -524,8 +656,12 @@ __global__ void f16_split_kernel(const float* __restrict__ x, long long ldx, int
     over |= fabsf(v) > kF16Max;
     const __half h = __float2half_rn(v);
     const __half l = __float2half_rn(__fsub_rn(v, __half2float(h)));
-    hi[i] = __half_as_ushort(h);
-    lo[i] = __half_as_ushort(l);
+    const int rr = r % T3_ROWS, kk = k % X3_F16_BK;
+    const size_t o = tiled ? ((size_t)(r / T3_ROWS) * (Kp / X3_F16_BK) + k / X3_F16_BK) * (T3_ROWS * X3_F16_BK) +
+                                 rr * X3_F16_BK + ((((kk >> 3) ^ (rr >> 1)) & 3) << 3) + (kk & 7)
+                           : i;
+    hi[o] = __half_as_ushort(h);
+    lo[o] = __half_as_ushort(l);
   }
   if (over && status) atomicOr(status, kDevRange);
 }
@@ -558,19 +694,22 @@ int tf32x3_token_tile(int M) {
   return m16 < 256 ? (m16 < 32 ? 32 : m16) : 256;
 }
 
-static int x3_splits(int M, int N, int K, int bk) {
-  const int tiles = (N / T3_ROWS) * ((M + tf32x3_token_tile(M) - 1) / tf32x3_token_tile(M));
-  int S = (2 * num_sms() + tiles - 1) / tiles;  // about two waves of one CTA per SM
-  const int max_s = K / bk > 0 ? K / bk : 1;
-  if (S > max_s) S = max_s;
-  if (S > kSgemmMaxSplits) S = kSgemmMaxSplits;
-  return S < 1 ? 1 : S;
-}
-
 static int x3_effective_splits(int K, int S, int bk) {
   int ks = (K + S - 1) / S;
   ks = (ks + bk - 1) / bk * bk;
   return (K + ks - 1) / ks;
+}
+
+// The K split count: the most CTAs (one per SM, each with a deep stage ring) that still run as one
+// wave; 1 when the output tiles alone fill the SMs.
+static int x3_splits(int M, int N, int K, int bk) {
+  const int tiles = (N / T3_ROWS) * ((M + tf32x3_token_tile(M) - 1) / tf32x3_token_tile(M));
+  int max_s = K / bk > 0 ? K / bk : 1;
+  if (max_s > kSgemmMaxSplits) max_s = kSgemmMaxSplits;
+  int best = 1;
+  for (int S = 2; S <= max_s; ++S)
+    if (tiles * x3_effective_splits(K, S, bk) <= num_sms()) best = S;
+  return best;
 }
 
 int tf32x3_splits(int M, int N, int K) { return x3_splits(M, N, K, X3_TF32_BK); }
@@ -581,7 +720,7 @@ int f16x3_effective_splits(int K, int S) { return x3_effective_splits(K, S, X3_F
 template <bool F16>
 static cudaError_t x3_partial_launch(const void* x_hi, const void* x_lo, const void* w_hi, const void* w_lo,
                                      const int* w_exp, int x_exp, int M, int N, int K, int S, float* part,
-                                     const int* status, cudaStream_t s) {
+                                     const int* status, cudaStream_t s, int w_tiled) {
   constexpr int BK = F16 ? X3_F16_BK : X3_TF32_BK;
   if (M <= 0) return cudaSuccess;
   if (N % T3_ROWS || K % BK) return cudaErrorInvalidValue;
@@ -592,22 +731,27 @@ static cudaError_t x3_partial_launch(const void* x_hi, const void* x_lo, const v
   CUtensorMap whi, wlo, xhi, xlo;
   bool ok;
   if (F16)
-    ok = make_tmap_bf16_2d(&whi, w_hi, K, N, (uint64_t)K * 2, BK, T3_ROWS) &&
-         make_tmap_bf16_2d(&wlo, w_lo, K, N, (uint64_t)K * 2, BK, T3_ROWS) &&
-         make_tmap_bf16_2d(&xhi, x_hi, K, M, (uint64_t)K * 2, BK, nt) &&
-         make_tmap_bf16_2d(&xlo, x_lo, K, M, (uint64_t)K * 2, BK, nt);
+    ok = make_tmap_bf16_2d(&whi, w_hi, K, N, (uint64_t)K * 2, BK, T3_ROWS, CU_TENSOR_MAP_SWIZZLE_64B) &&
+         make_tmap_bf16_2d(&wlo, w_lo, K, N, (uint64_t)K * 2, BK, T3_ROWS, CU_TENSOR_MAP_SWIZZLE_64B) &&
+         make_tmap_bf16_2d(&xhi, x_hi, K, M, (uint64_t)K * 2, BK, nt, CU_TENSOR_MAP_SWIZZLE_64B) &&
+         make_tmap_bf16_2d(&xlo, x_lo, K, M, (uint64_t)K * 2, BK, nt, CU_TENSOR_MAP_SWIZZLE_64B);
   else
     ok = make_tmap_f32_2d(&whi, w_hi, K, N, (uint64_t)K * 4, T3_ROWS) &&
          make_tmap_f32_2d(&wlo, w_lo, K, N, (uint64_t)K * 4, T3_ROWS) &&
          make_tmap_f32_2d(&xhi, x_hi, K, M, (uint64_t)K * 4, nt) &&
          make_tmap_f32_2d(&xlo, x_lo, K, M, (uint64_t)K * 4, nt);
   if (!ok) return cudaErrorInvalidValue;
-  const int smem = T3_STAGES * (2 * T3_W_BYTES + 2 * nt * T3_ROW_BYTES) + 1024 + 256;
-  static unsigned long long smem_set = 0;  // opted in to the largest plan (NT = 256) once per device
-  cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(x3_partial_kernel<F16>),
-                              T3_STAGES * (2 * T3_W_BYTES + 2 * 256 * T3_ROW_BYTES) + 1024 + 256, &smem_set);
+  // as many stages as fit: 1024 bytes of alignment slack and 256 of barriers besides the ring
+  const int stage_bytes = 2 * X3Geom<F16>::W_BYTES + 2 * nt * X3Geom<F16>::ROW_BYTES;
+  int stages = (T3_SMEM_MAX - 1024 - 256) / stage_bytes;
+  if (stages > T3_MAX_STAGES) stages = T3_MAX_STAGES;
+  if (stages < 2) return cudaErrorInvalidValue;
+  const int smem = stages * stage_bytes + 1024 + 256;
+  static unsigned long long smem_set = 0;  // opted in to the largest size once per device
+  cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(x3_partial_kernel<F16>), T3_SMEM_MAX, &smem_set);
   if (e != cudaSuccess) return e;
-  T3Args a{M, N, K, ks, nt, part, const_cast<int*>(status), w_exp, x_exp};
+  T3Args a{M, N, K, ks, nt, stages, F16 && w_tiled, static_cast<const uint16_t*>(w_hi),
+           static_cast<const uint16_t*>(w_lo), part, const_cast<int*>(status), w_exp, x_exp};
   dim3 grid(N / T3_ROWS, (M + nt - 1) / nt, S_eff);
   x3_partial_kernel<F16><<<grid, T3_THREADS, smem, s>>>(whi, wlo, xhi, xlo, a);
   return cudaGetLastError();
@@ -615,13 +759,13 @@ static cudaError_t x3_partial_launch(const void* x_hi, const void* x_lo, const v
 
 cudaError_t tf32x3_partial_launch(const float* x_hi, const float* x_lo, const float* w_hi, const float* w_lo, int M,
                                   int N, int K, int S, float* part, const int* status, cudaStream_t s) {
-  return x3_partial_launch<false>(x_hi, x_lo, w_hi, w_lo, nullptr, 0, M, N, K, S, part, status, s);
+  return x3_partial_launch<false>(x_hi, x_lo, w_hi, w_lo, nullptr, 0, M, N, K, S, part, status, s, 0);
 }
 
 cudaError_t f16x3_partial_launch(const uint16_t* x_hi, const uint16_t* x_lo, const uint16_t* w_hi,
                                  const uint16_t* w_lo, const int* w_exp, int x_exp, int M, int N, int K, int S,
-                                 float* part, const int* status, cudaStream_t s) {
-  return x3_partial_launch<true>(x_hi, x_lo, w_hi, w_lo, w_exp, x_exp, M, N, K, S, part, status, s);
+                                 float* part, const int* status, cudaStream_t s, int w_tiled) {
+  return x3_partial_launch<true>(x_hi, x_lo, w_hi, w_lo, w_exp, x_exp, M, N, K, S, part, status, s, w_tiled);
 }
 
 cudaError_t absmax_launch(const float* x, size_t n, unsigned int* out, cudaStream_t s) {
@@ -632,10 +776,12 @@ cudaError_t absmax_launch(const float* x, size_t n, unsigned int* out, cudaStrea
 }
 
 cudaError_t f16_split_launch(const float* x, long long ldx, int K, int M, int Kp, const unsigned int* max_bits,
-                             int e_fixed, int* e_out, uint16_t* hi, uint16_t* lo, int* status, cudaStream_t s) {
+                             int e_fixed, int* e_out, uint16_t* hi, uint16_t* lo, int* status, cudaStream_t s,
+                             int tiled) {
   if (M <= 0) return cudaSuccess;
   if (K < 1 || Kp < K || ldx < K) return cudaErrorInvalidValue;
-  f16_split_kernel<<<ew_grid((size_t)M * Kp), 256, 0, s>>>(x, ldx, K, M, Kp, max_bits, e_fixed, e_out, hi, lo,
+  if (tiled && (M % T3_ROWS || Kp % X3_F16_BK)) return cudaErrorInvalidValue;
+  f16_split_kernel<<<ew_grid((size_t)M * Kp), 256, 0, s>>>(x, ldx, K, M, Kp, max_bits, e_fixed, e_out, hi, lo, tiled,
                                                              status);
   return cudaGetLastError();
 }
@@ -664,24 +810,32 @@ cudaError_t sgemm_reduce_rows_launch(const float* part, int S, int M, int Np, in
   return cudaGetLastError();
 }
 
+// 2-D grid of the reductions: 1024 columns per 256-thread block, rows up to 65535 per launch row
+static dim3 reduce_grid(int M, int cols) { return dim3((cols + 1023) / 1024, M < 65535 ? M : 65535); }
+
 cudaError_t sgemm_reduce_store_launch(const float* part, int S, int M, int N, const float* bias, float* out, int add,
                                       float* lo, const int* status, cudaStream_t s) {
-  sgemm_reduce_store_kernel<<<ew_grid((size_t)M * N), 256, 0, s>>>(part, S, M, N, bias, out, add, lo, status);
+  if (M <= 0) return cudaSuccess;
+  if (N % 4) return cudaErrorInvalidValue;
+  sgemm_reduce_store_kernel<<<reduce_grid(M, N), 256, 0, s>>>(part, S, M, N, bias, out, add, lo, status);
   return cudaGetLastError();
 }
 
 cudaError_t sgemm_reduce_qkv_launch(const float* part, int S, int M, int d, int Dh, int half, const float* bias,
                                     const float* cs, const float* sn, float* q, float* k, float* v, const int* status,
                                     cudaStream_t s) {
-  sgemm_reduce_qkv_kernel<<<ew_grid((size_t)M * 3 * d), 256, 0, s>>>(part, S, M, d, Dh, half, bias, cs, sn, q, k, v,
-                                                                      status);
+  if (M <= 0) return cudaSuccess;
+  if (d % 4 || Dh % 4 || half % 4) return cudaErrorInvalidValue;
+  sgemm_reduce_qkv_kernel<<<reduce_grid(M, 3 * d), 256, 0, s>>>(part, S, M, d, Dh, half, bias, cs, sn, q, k, v,
+                                                                 status);
   return cudaGetLastError();
 }
 
 cudaError_t sgemm_reduce_swiglu_launch(const float* part, int S, int M, int F, const float* bias, float* h,
                                        uint16_t* h_split, int* status, cudaStream_t s) {
+  if (M <= 0) return cudaSuccess;
   if (F % 4) return cudaErrorInvalidValue;
-  sgemm_reduce_swiglu_kernel<<<ew_grid((size_t)M * F / 4), 256, 0, s>>>(part, S, M, F, bias, h, h_split, status);
+  sgemm_reduce_swiglu_kernel<<<reduce_grid(M, F), 256, 0, s>>>(part, S, M, F, bias, h, h_split, status);
   return cudaGetLastError();
 }
 

@@ -161,13 +161,15 @@ int f16x3_splits(int M, int N, int K);
 int f16x3_effective_splits(int K, int S);
 cudaError_t f16x3_partial_launch(const uint16_t* x_hi, const uint16_t* x_lo, const uint16_t* w_hi,
                                  const uint16_t* w_lo, const int* w_exp, int x_exp, int M, int N, int K, int S,
-                                 float* part, const int* status, cudaStream_t s);
+                                 float* part, const int* status, cudaStream_t s, int w_tiled = 0);
 // Largest |x| (as float bits) into *out (cleared first).
 cudaError_t absmax_launch(const float* x, size_t n, unsigned int* out, cudaStream_t s);
 // x [M][K] (stride ldx) -> f16 hi, lo [M][Kp] of x 2^e, zero-padded: e from *max_bits (a weight's scale,
-// also written to *e_out) when max_bits is given, else e_fixed; kDevRange in *status past 65504.
+// also written to *e_out) when max_bits is given, else e_fixed; kDevRange in *status past 65504.  With
+// `tiled` (weights) the parts are laid out [M / 128][Kp / 32][128][32] for f16x3_partial_launch's w_tiled.
 cudaError_t f16_split_launch(const float* x, long long ldx, int K, int M, int Kp, const unsigned int* max_bits,
-                             int e_fixed, int* e_out, uint16_t* hi, uint16_t* lo, int* status, cudaStream_t s);
+                             int e_fixed, int* e_out, uint16_t* hi, uint16_t* lo, int* status, cudaStream_t s,
+                             int tiled = 0);
 // The 3xTF32 GEMM's tiling: K a multiple of kTf32x3K, N (output features) a multiple of kTf32x3N.
 constexpr int kTf32x3K = 32;
 constexpr int kTf32x3N = 128;

@@ -25,10 +25,12 @@ inline EncodeTiledFn encode_tiled_fn() {
   return fn;
 }
 
-// 2-D bf16 tensor [outer, inner] with row pitch `row_bytes`, box [box_outer, box_inner],
-// 128-byte swizzle (box_inner * 2 must be 128), out-of-bounds elements read as zero.
+// 2-D 16-bit tensor [outer, inner] with row pitch `row_bytes`, box [box_outer, box_inner], out-of-bounds
+// elements read as zero.  The swizzle span must equal the box row: box_inner * 2 = 128 bytes for
+// SWIZZLE_128B (the default), 64 for SWIZZLE_64B.
 inline bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
-                              uint32_t box_inner, uint32_t box_outer) {
+                              uint32_t box_inner, uint32_t box_outer,
+                              CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn fn = encode_tiled_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {inner, outer};
@@ -36,7 +38,7 @@ inline bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
