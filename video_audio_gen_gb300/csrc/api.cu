@@ -256,7 +256,10 @@ WsLayout ws_layout_fp32(const dit_config* c, int n, int n_docs) {
   size_t widest_in = (size_t)d;  // the GEMM inputs: io (pre-conv), d, F (FFN down)
   if ((size_t)F > widest_in) widest_in = (size_t)F;
   if ((size_t)io > widest_in) widest_in = (size_t)io;
-  w.xs_hi = take((size_t)n * widest_in * 4);
+  // the 3xF16 operand: rows padded to whole token tiles, hi and lo parts
+  const int x_nt = x3_token_tile(n > 0 ? n : 1);
+  const size_t n_pad = (size_t)((n + x_nt - 1) / x_nt) * x_nt;
+  w.xs_hi = take(n_pad * widest_in * 4);
   w.xs_lo = take((size_t)n * widest_in * 4);
   w.total = off;
   return w;
@@ -360,15 +363,16 @@ dit_status bind_fp32(dit_handle* h, const dit_weights* w, cudaStream_t s) {
   // the 3xF16 GEMM: 4 bytes per weight, as the fp32 weight itself
   unsigned int* maxbuf = static_cast<unsigned int*>(dev_alloc(h, 16, &e));
   if (e != cudaSuccess) return cuda_err(h, e, "bind: alloc");
+  // (128 x 32 tiles, each tile's hi part followed by its lo part, in the GEMM's shared-memory image)
   auto split = [&](const void* src, long long rows, int K, SplitW16* out) -> bool {
     const size_t n = (size_t)rows * K;
-    out->hi = static_cast<uint16_t*>(dev_alloc(h, n * 2, &e));
-    if (e == cudaSuccess) out->lo = static_cast<uint16_t*>(dev_alloc(h, n * 2, &e));
+    out->hi = static_cast<uint16_t*>(dev_alloc(h, n * 4, &e));
+    if (e == cudaSuccess) out->lo = out->hi + (size_t)kTf32x3N * kTf32x3K;
     if (e == cudaSuccess) out->e = static_cast<int*>(dev_alloc(h, 16, &e));
     if (e == cudaSuccess) e = absmax_launch(static_cast<const float*>(src), n, maxbuf, s);
     if (e == cudaSuccess)
       e = f16_split_launch(static_cast<const float*>(src), K, K, (int)rows, K, maxbuf, 0, out->e, out->hi, out->lo,
-                           nullptr, s, 1);
+                           nullptr, s, kSplitWeightTiles);
     return e == cudaSuccess;
   };
   for (int l = 0; l < c.n_blocks; ++l) {
@@ -407,9 +411,9 @@ dit_status bind_fp32(dit_handle* h, const dit_weights* w, cudaStream_t s) {
   return DIT_OK;
 }
 
-// One fp32 GEMM of the forward: the 3xF16 partial sums of the activation operand in `xs` (f16 hi
-// [M][K] then lo [M][K] of x 2^kF16x3ActExp), then (by the caller) the fixed-order reduction that
-// applies the epilogue.  The operand is written by the kernel that produces x (the norms, the
+// One fp32 GEMM of the forward: the 3xF16 partial sums of the activation operand in `xs` (f16 hi and
+// lo parts of x 2^kF16x3ActExp in the token-tiled layout), then (by the caller) the fixed-order
+// reduction that applies the epilogue.  The operand is written by the kernel that produces x (the norms, the
 // attention, the SiLU-gate reduction); `run` splits an fp32 x first (the 1x1 convolutions' inputs).
 struct Sgemm {
   dit_handle* h;
@@ -421,11 +425,12 @@ struct Sgemm {
   cudaError_t run_split(const SplitW16& W, int M, int N, int K) {
     const int want = f16x3_splits(M, N, K);
     S = f16x3_effective_splits(K, want);
-    return f16x3_partial_launch(xs, xs + (size_t)M * K, W.hi, W.lo, W.e, kF16x3ActExp, M, N, K, want, part, status,
-                                s, 1);
+    return f16x3_partial_launch(xs, nullptr, W.hi, nullptr, W.e, kF16x3ActExp, M, N, K, want, part, status, s, 1,
+                                1);
   }
   cudaError_t run(const float* X, const SplitW16& W, int M, int N, int K) {
-    cudaError_t e = f16_split_launch(X, K, K, M, K, nullptr, kF16x3ActExp, nullptr, xs, xs + (size_t)M * K, status, s);
+    cudaError_t e =
+        f16_split_launch(X, K, K, M, K, nullptr, kF16x3ActExp, nullptr, xs, nullptr, status, s, kSplitTokenTiles);
     return e == cudaSuccess ? run_split(W, M, N, K) : e;
   }
 };

@@ -383,6 +383,26 @@ __device__ __forceinline__ uint16_t to16(bool f16, float v) {
 // Four values v * 2^e as f16 (hi, lo) pairs for the 3xF16 GEMM: hi = f16(v 2^e), lo = f16(v 2^e - hi);
 // stored at hi_dst / lo_dst (4 consecutive 16-bit elements each, 8-byte aligned).  Returns true when a
 // scaled value is beyond f16's finite range.
+// Token tile of the 3xF16 GEMM (its MMA's N): M split into the fewest tiles of at most 192 tokens
+// (so that an epilogue warp's running sums fit its registers), rounded up to 16, at least 32.
+__host__ __device__ __forceinline__ int x3_token_tile(int M) {
+  const int tiles = (M + 191) / 192;
+  const int per = (M + tiles - 1) / (tiles > 0 ? tiles : 1);
+  const int m16 = (per + 15) / 16 * 16;
+  return m16 < 32 ? 32 : m16;
+}
+
+// The 3xF16 GEMM's activation operand in its token-tiled layout: K in blocks of 32, tokens in tiles of
+// nt; per (K block, token tile) the hi part [nt][32] and then the lo part [nt][32], each already the
+// shared-memory image of the 64-byte swizzle (16-byte chunk c of row r at c ^ ((r >> 1) & 3)), so
+// that one plain bulk copy loads a GEMM stage.  Index of element (r, k) of the hi part; its lo part is
+// nt * 32 elements further.  Four consecutive k from a multiple of 4 stay contiguous.
+__device__ __forceinline__ size_t x3_xs_index(int r, int k, int nt, int mtiles) {
+  const int t = r / nt, rr = r - t * nt, kk = k & 31;
+  return ((size_t)(k >> 5) * mtiles + t) * (size_t)(2 * nt * 32) + rr * 32 + ((((kk >> 3) ^ (rr >> 1)) & 3) << 3) +
+         (kk & 7);
+}
+
 __device__ __forceinline__ bool store_f16_split4(const float (&v)[4], int e, uint16_t* hi_dst, uint16_t* lo_dst) {
   uint16_t h[4], l[4];
   bool over = false;

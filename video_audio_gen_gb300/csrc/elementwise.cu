@@ -96,8 +96,10 @@ __global__ void __launch_bounds__(256) norm_mod_kernel(const float* __restrict__
       uint2 pk = make_uint2(pack16(f, o[0], o[1]), pack16(f, o[2], o[3]));
       *reinterpret_cast<uint2*>(static_cast<uint16_t*>(y) + (size_t)row * d + c) = pk;
     } else if (out_kind == 3) {
-      uint16_t* hi = static_cast<uint16_t*>(y) + (size_t)row * d + c;
-      if (store_f16_split4(o, kF16x3ActExp, hi, hi + (size_t)n * d) && status) atomicOr(status, kDevRange);
+      const int nt = x3_token_tile(n);
+      const size_t xi = x3_xs_index(row, c, nt, (n + nt - 1) / nt);
+      uint16_t* xs = static_cast<uint16_t*>(y);
+      if (store_f16_split4(o, kF16x3ActExp, xs + xi, xs + xi + (size_t)nt * 32) && status) atomicOr(status, kDevRange);
     } else {
       *reinterpret_cast<float4*>(static_cast<float*>(y) + (size_t)row * d + c) = make_float4(o[0], o[1], o[2], o[3]);
     }
@@ -190,8 +192,11 @@ __global__ void __launch_bounds__(256) norm_mod_persistent_kernel(
         *reinterpret_cast<uint2*>(static_cast<uint16_t*>(y) + (size_t)row * d + c) =
             make_uint2(pack16(f, o[0], o[1]), pack16(f, o[2], o[3]));
       } else if (out_kind == 3) {
-        uint16_t* hi = static_cast<uint16_t*>(y) + (size_t)row * d + c;
-        if (store_f16_split4(o, kF16x3ActExp, hi, hi + (size_t)n * d) && status) atomicOr(status, kDevRange);
+        const int nt = x3_token_tile(n);
+        const size_t xi = x3_xs_index(row, c, nt, (n + nt - 1) / nt);
+        uint16_t* xs = static_cast<uint16_t*>(y);
+        if (store_f16_split4(o, kF16x3ActExp, xs + xi, xs + xi + (size_t)nt * 32) && status)
+          atomicOr(status, kDevRange);
       } else {
         *reinterpret_cast<float4*>(static_cast<float*>(y) + (size_t)row * d + c) = make_float4(o[0], o[1], o[2], o[3]);
       }

@@ -137,6 +137,7 @@ __global__ void sgemm_reduce_swiglu_kernel(const float* __restrict__ part, int S
   const float4 bu = bias ? *reinterpret_cast<const float4*>(bias + f0) : zero;
   const float4 bg = bias ? *reinterpret_cast<const float4*>(bias + F + f0) : zero;
   bool over = false;
+  const int nt = x3_token_tile(M), mt = (M + nt - 1) / nt;
   for (int r = blockIdx.y; r < M; r += gridDim.y) {
     const float4 u4 = sum_parts4(part, S, MN, (size_t)r * 2 * F + f0);
     const float4 g4 = sum_parts4(part, S, MN, (size_t)r * 2 * F + F + f0);
@@ -145,26 +146,29 @@ __global__ void sgemm_reduce_swiglu_kernel(const float* __restrict__ part, int S
     float hv[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) hv[e] = u[e] * (g[e] / (1.0f + expf(-g[e])));
-    const size_t i = (size_t)r * F + f0;
-    if (h_split)
-      over |= store_f16_split4(hv, kF16x3ActExp, h_split + i, h_split + (size_t)M * F + i);
-    else
-      *reinterpret_cast<float4*>(h + i) = make_float4(hv[0], hv[1], hv[2], hv[3]);
+    if (h_split) {
+      const size_t xi = x3_xs_index(r, f0, nt, mt);
+      over |= store_f16_split4(hv, kF16x3ActExp, h_split + xi, h_split + xi + (size_t)nt * 32);
+    } else {
+      *reinterpret_cast<float4*>(h + (size_t)r * F + f0) = make_float4(hv[0], hv[1], hv[2], hv[3]);
+    }
   }
   if (over && status) atomicOr(status, kDevRange);
 }
 
 // Exact fp32 softmax attention over the document of each row.  One CTA per (document, 128-row
-// q-tile, head, 32-row quarter), 4 warps of 8 query rows each.  The document's keys and values pass
-// through shared memory 32 at a time (lane j scores key j of the chunk for all 8 rows of its warp);
+// q-tile, head, 16-row block), 4 warps of 4 query rows each.  The document's keys and values pass
+// through shared memory 32 at a time (lane j scores key j of the chunk for all 4 rows of its warp);
 // every row keeps an exact fp32 online softmax (running max m, sum l, accumulator o, each chunk
 // rescaled by exp(m_old - m_new)):
 //     o_i = sum_j exp(s_ij - m_i) v_j / sum_j exp(s_ij - m_i),   s_ij = q_i . k_j / sqrt(Dh)
 // Lane l accumulates output dims [l * DH / 32, (l + 1) * DH / 32).  The next chunk's keys and values
 // are loaded into registers while the current one is scored.
 constexpr int AF_KC = 32;      // keys per chunk
-constexpr int AF_ROWS = 8;     // query rows per warp
+constexpr int AF_ROWS = 4;     // query rows per warp
 constexpr int AF_WARPS = 4;
+constexpr int AF_CTA_ROWS = AF_ROWS * AF_WARPS;  // 16
+constexpr int AF_BLOCKS = 128 / AF_CTA_ROWS;     // CTAs per 128-row item of the schedule
 
 template <int DH>
 __host__ __device__ constexpr int af_kstride() {
@@ -191,14 +195,14 @@ __global__ void __launch_bounds__(AF_WARPS * 32) attention_f32_kernel(
   float* sk = reinterpret_cast<float*>(af_smem4);  // [KC][KS]
   float* sv = sk + AF_KC * KS;                     // [KC][DH]
   float* sq = sv + AF_KC * DH;                     // [warps][rows][DH]
-  const int quarter = blockIdx.x & 3, item_idx = blockIdx.x >> 2, h = blockIdx.y;
+  const int blk = blockIdx.x % AF_BLOCKS, item_idx = blockIdx.x / AF_BLOCKS, h = blockIdx.y;
   if (item_idx >= *count) return;
   const int2 it = items[item_idx];
   const int a = cu[it.x], b = cu[it.x + 1];
   const int d = H * DH;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r0 = it.y + quarter * 32 + warp * AF_ROWS;  // this warp's first row
-  if (it.y + quarter * 32 >= b) return;                  // the whole CTA is past the document's end
+  const int r0 = it.y + blk * AF_CTA_ROWS + warp * AF_ROWS;  // this warp's first row
+  if (it.y + blk * AF_CTA_ROWS >= b) return;                  // the whole CTA is past the document's end
   float* myq = sq + warp * AF_ROWS * DH;
 #pragma unroll
   for (int t = lane; t < AF_ROWS * D4; t += 32) {
@@ -295,6 +299,7 @@ __global__ void __launch_bounds__(AF_WARPS * 32) attention_f32_kernel(
     }
   }
   bool over = false;
+  const int xnt = x3_token_tile(n_tokens), xmt = (n_tokens + xnt - 1) / xnt;
 #pragma unroll
   for (int i = 0; i < AF_ROWS; ++i) {
     const int r = r0 + i;
@@ -309,7 +314,8 @@ __global__ void __launch_bounds__(AF_WARPS * 32) attention_f32_kernel(
 #pragma unroll
         for (int e = 0; e < PL; e += 4) {
           const float v4[4] = {ov[e], ov[e + 1], ov[e + 2], ov[e + 3]};
-          over |= store_f16_split4(v4, kF16x3ActExp, o_split + at + e, o_split + (size_t)n_tokens * d + at + e);
+          const size_t xi = x3_xs_index(r, h * DH + lane * PL + e, xnt, xmt);
+          over |= store_f16_split4(v4, kF16x3ActExp, o_split + xi, o_split + xi + (size_t)xnt * 32);
         }
       } else {
 #pragma unroll
@@ -317,8 +323,9 @@ __global__ void __launch_bounds__(AF_WARPS * 32) attention_f32_kernel(
           const float x = ldexpf(ov[e], kF16x3ActExp);
           over |= fabsf(x) > kF16Max;
           const __half hh = __float2half_rn(x);
-          o_split[at + e] = __half_as_ushort(hh);
-          o_split[(size_t)n_tokens * d + at + e] = __half_as_ushort(__float2half_rn(__fsub_rn(x, __half2float(hh))));
+          const size_t xi = x3_xs_index(r, h * DH + lane * PL + e, xnt, xmt);
+          o_split[xi] = __half_as_ushort(hh);
+          o_split[xi + (size_t)xnt * 32] = __half_as_ushort(__float2half_rn(__fsub_rn(x, __half2float(hh))));
         }
       }
     } else {
@@ -362,22 +369,26 @@ __global__ void io_transpose_kernel(const float* __restrict__ src, float* __rest
 //        weight stream is half of tf32's.
 // The tensor core's fp32 accumulation of these products is biased (measured on GB300: the error
 // of a TMEM accumulation grows linearly with its depth, about 2e-5 relative at K = 2048), so the
-// MMAs accumulate only one chunk (64 K for f16: two stages of 2 K-steps x 3 products; 32 K for tf32:
-// one stage of 4), alternately into two TMEM accumulators, and the epilogue adds each chunk into
-// fp32 running sums in registers (round to nearest).  The roles are transposed so that the small token count sits on the MMA's N side: one
-// CTA owns 128 output features (M = 128 rows of W) x NT tokens (N = NT <= 256, all the tokens of a
-// music forward in one tile) x one K split, and writes part[split][token][feature] for the same
-// fixed-order reductions as before.  At these token counts the weights stream from HBM at about
+// MMAs accumulate only one stage (32 K: 2 f16 or 4 tf32 K-steps x 3 products), in turn into as many
+// TMEM accumulators as fit (2 to 4), and the epilogue adds each
+// chunk into fp32 running sums in registers (round to nearest).  The roles are transposed so that the
+// small token count sits on the MMA's N side: one CTA owns 128 output features (M = 128 rows of W) x
+// NT tokens (N = NT <= 192, all the tokens of a music forward in one tile) x one K split, and writes
+// part[split][token][feature] for the fixed-order reductions.  At these token counts the weights stream from HBM at about
 // one byte per two tensor-core FLOPs, so the loads need depth: the stage ring is as deep as shared
 // memory allows (f16: five 38 KB stages of 64-byte rows at NT = 176; tf32: two of 128-byte rows).
-//   warp 0     TMA producer: W_hi, W_lo [128 x R] and X_hi, X_lo [NT x R] per stage (R row bytes)
-//   warp 1     TMEM allocator + MMA issuer: the chunk's cross products, then its hi x hi products
+//   warp 0     producer: W_hi, W_lo [128 x R] and X_hi, X_lo [NT x R] per stage (R row bytes)
+//   warp 1     TMEM allocator + MMA issuer of the even chunks: the chunk's cross products, then its
+//              hi x hi products
+//   warp 10    MMA issuer of the odd chunks (one thread alone left the tensor core idle while it
+//              waited on its barriers)
 //   warps 2-9  epilogue: TMEM lane = feature, column = token; two warps per lane quarter split the
 //              token columns; running sums in registers, coalesced stores along features
 constexpr int T3_ROWS = kTf32x3N;                 // output features per CTA (MMA M)
 constexpr int T3_MAX_STAGES = 8;
-constexpr int T3_THREADS = 320;
-constexpr int T3_MAX_UNITS = 8;                   // 16-column units per epilogue warp (NT <= 256)
+constexpr int T3_MAX_ACC = 4;                     // TMEM accumulator buffers at most
+constexpr int T3_THREADS = 352;                   // producer, MMA, 8 epilogue warps, second MMA issuer
+constexpr int T3_MAX_UNITS = 6;                   // 16-column units per epilogue warp (NT <= 192)
 constexpr int T3_SMEM_MAX = 232448;               // opt-in dynamic shared memory per CTA
 constexpr int X3_F16_BK = 32;                     // K per stage, f16
 constexpr int X3_TF32_BK = kTf32x3K;              // K per stage, tf32 (32)
@@ -394,9 +405,10 @@ struct X3Geom {
 
 struct T3Args {
   int M, N, K, k_split, nt, stages;
-  int w_tiled;  // f16: W in pre-swizzled [N / 128][K / 32][128][32] tiles, one 8 KB bulk copy per stage
+  int w_tiled;  // f16: W in pre-swizzled 128 x 32 tiles (hi then lo), one 16 KB bulk copy per stage
+  int x_tiled;  // f16: X in the token-tiled layout (hi then lo per tile), one bulk copy per stage
   const uint16_t* w_hi;
-  const uint16_t* w_lo;
+  const uint16_t* x_hi;
   float* part;
   int* status;
   const int* w_exp;  // f16: the weight's scale exponent (device); the sums are scaled by 2^-(w_exp + x_exp)
@@ -416,14 +428,18 @@ __global__ void __launch_bounds__(T3_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int nt = a.nt;
+  const int acc_cols = (nt + 31) & ~31;  // TMEM columns per accumulator buffer
+  // as many accumulator buffers as the 512 TMEM columns hold (2 at NT = 176, 4 at NT <= 128): the
+  // MMAs of a chunk wait only for the drain of the chunk n_acc before it
+  const int n_acc = 512 / acc_cols < T3_MAX_ACC ? 512 / acc_cols : T3_MAX_ACC;
   const int T3_STAGES = a.stages;
   const int x_bytes = nt * G::ROW_BYTES;
   const int stage_bytes = 2 * T3_W_BYTES + 2 * x_bytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + T3_STAGES * stage_bytes);
   uint64_t* empty = full + T3_MAX_STAGES;
-  uint64_t* chunk_full = empty + T3_MAX_STAGES;   // [2] an accumulator holds a finished chunk
-  uint64_t* chunk_empty = chunk_full + 2;     // [2] the epilogue has added it to its running sums
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(chunk_empty + 2);
+  uint64_t* chunk_full = empty + T3_MAX_STAGES;       // [NB] an accumulator holds a finished chunk
+  uint64_t* chunk_empty = chunk_full + T3_MAX_ACC;    // [NB] the epilogue has added it to its sums
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(chunk_empty + T3_MAX_ACC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -438,7 +454,7 @@ __global__ void __launch_bounds__(T3_THREADS, 1)
       mbar_init(&full[st], 1);
       mbar_init(&empty[st], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < T3_MAX_ACC; ++b) {
       mbar_init(&chunk_full[b], 1);
       mbar_init(&chunk_empty[b], 8);
     }
@@ -451,35 +467,43 @@ __global__ void __launch_bounds__(T3_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    if (lane == 0) {
-      // CTAs side by side start at different K blocks of their range, so that they do not all ask
-      // L2 for the same activation rows at the same time (the chunk sums are independent of order)
-      const int rot = n_kb > 0 ? (int)((long long)blockIdx.x * n_kb / gridDim.x) : 0;
-      int i = 0;
-      for (; i < n_kb; ++i) {
-        const int st = i % T3_STAGES;
-        if (!mbar_wait(&empty[st], ((i / T3_STAGES) & 1) ^ 1, abort_flag, a.status)) break;
-        uint8_t* base = smem + st * stage_bytes;
-        const int j = i + rot < n_kb ? i + rot : i + rot - n_kb;
-        const int k0 = kb + j * T3_BK;
-        mbar_arrive_expect_tx(&full[st], stage_bytes);
-        if (a.w_tiled) {
-          const size_t t = ((size_t)blockIdx.x * (a.K / T3_BK) + k0 / T3_BK) * (T3_ROWS * T3_BK);
-          bulk_load(base, a.w_hi + t, T3_W_BYTES, &full[st]);
-          bulk_load(base + T3_W_BYTES, a.w_lo + t, T3_W_BYTES, &full[st]);
-        } else {
-          tma_load_2d(base, &tmWhi, &full[st], k0, n0);
-          tma_load_2d(base + T3_W_BYTES, &tmWlo, &full[st], k0, n0);
-        }
+  auto produce = [&]() {
+    // CTAs side by side start at different K blocks of their range, so that they do not all ask L2
+    // for the same activation rows at the same time (the chunk sums are independent of order)
+    const int rot = n_kb > 0 ? (int)((long long)blockIdx.x * n_kb / gridDim.x) : 0;
+    int i = 0;
+    for (; i < n_kb; ++i) {
+      const int st = i % T3_STAGES;
+      if (!mbar_wait(&empty[st], ((i / T3_STAGES) & 1) ^ 1, abort_flag, a.status)) break;
+      uint8_t* base = smem + st * stage_bytes;
+      const int j = i + rot < n_kb ? i + rot : i + rot - n_kb;
+      const int k0 = kb + j * T3_BK;
+      mbar_arrive_expect_tx(&full[st], stage_bytes);
+      if (a.w_tiled) {
+        const size_t t = ((size_t)blockIdx.x * (a.K / T3_BK) + k0 / T3_BK) * (2 * T3_ROWS * T3_BK);
+        bulk_load(base, a.w_hi + t, 2 * T3_W_BYTES, &full[st]);
+      } else {
+        tma_load_2d(base, &tmWhi, &full[st], k0, n0);
+        tma_load_2d(base + T3_W_BYTES, &tmWlo, &full[st], k0, n0);
+      }
+      if (a.x_tiled) {
+        const size_t t = ((size_t)(k0 / T3_BK) * gridDim.y + blockIdx.y) * (size_t)(2 * nt * T3_BK);
+        bulk_load(base + 2 * T3_W_BYTES, a.x_hi + t, 2 * x_bytes, &full[st]);
+      } else {
         tma_load_2d(base + 2 * T3_W_BYTES, &tmXhi, &full[st], k0, m0);
         tma_load_2d(base + 2 * T3_W_BYTES + x_bytes, &tmXlo, &full[st], k0, m0);
       }
-      // Every copy issued must land before the CTA exits: wait for the stages still in flight.
-      for (int j = i - T3_STAGES < 0 ? 0 : i - T3_STAGES; j < i; ++j)
-        mbar_wait(&full[j % T3_STAGES], (j / T3_STAGES) & 1, abort_flag, nullptr);
     }
-  } else if (warp == 1) {
+    // Every copy issued must land before the CTA exits: wait for the stages still in flight.
+    for (int j = i - T3_STAGES < 0 ? 0 : i - T3_STAGES; j < i; ++j)
+      mbar_wait(&full[j % T3_STAGES], (j / T3_STAGES) & 1, abort_flag, nullptr);
+  };
+  if (warp == 0) {
+    if (lane == 0) produce();
+  } else if (warp == 1 || warp == T3_THREADS / 32 - 1) {
+    // Two MMA issuers take alternate chunks (each into its own accumulator buffers), so that one
+    // issues while the other waits on its barriers: a single issuing thread left the tensor core
+    // idle for most of each chunk.
     if (lane == 0) {
       const uint32_t idesc = F16 ? idesc_f16_f32(T3_ROWS, nt) : idesc_tf32_f32(T3_ROWS, nt);
       // 32 bytes per instruction: K = 8 tf32 or 16 f16
@@ -490,14 +514,14 @@ __global__ void __launch_bounds__(T3_THREADS, 1)
           umma_tf32(acc, sdesc_sw128(w), sdesc_sw128(x), idesc, accumulate);
       };
       bool ok = true;
-      for (int c = 0; c < n_chunks && ok; ++c) {
-        const int cb = c & 1;
+      for (int c = warp == 1 ? 0 : 1; c < n_chunks && ok; c += 2) {
+        const int cb = c % n_acc;
         const int i0 = c * T3_CHUNK, i1 = min(n_kb, i0 + T3_CHUNK);
-        if (!mbar_wait(&chunk_empty[cb], ((c >> 1) & 1) ^ 1, abort_flag, a.status)) break;
+        if (!mbar_wait(&chunk_empty[cb], ((c / n_acc) & 1) ^ 1, abort_flag, a.status)) break;
         for (int i = i0; i < i1 && ok; ++i) ok = mbar_wait(&full[i % T3_STAGES], (i / T3_STAGES) & 1, abort_flag, a.status);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t acc = tmem + cb * nt;
+        const uint32_t acc = tmem + cb * acc_cols;
         // The small cross terms of every stage of the chunk go first, while the accumulator is still
         // about 2^-11 of its final size (their rounding is then negligible); the hi x hi products last.
         bool first = true;
@@ -526,36 +550,56 @@ __global__ void __launch_bounds__(T3_THREADS, 1)
       }
     }
   } else {
-    // epilogue: lane quarter = warp % 4 (TMEM access rule), column half = (warp - 2) / 4
+    // epilogue: lane quarter = warp % 4 (TMEM access rule), column half = (warp - 2) / 4 (split at an
+    // even unit so that every 32-column load starts on a multiple of 32 columns)
     const int quarter = warp & 3;
     const int units = nt / 16;
-    const int u0 = (warp - 2) >> 2 ? (units + 1) / 2 : 0;
-    const int u1 = (warp - 2) >> 2 ? units : (units + 1) / 2;
+    const int half_u = ((units + 1) / 2 + 1) & ~1;
+    const int u0 = (warp - 2) >> 2 ? half_u : 0;
+    const int u1 = (warp - 2) >> 2 ? units : (half_u < units ? half_u : units);
+    const int nu = u1 > u0 ? u1 - u0 : 0;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     float run[T3_MAX_UNITS * 16];
 #pragma unroll
     for (int i = 0; i < T3_MAX_UNITS * 16; ++i) run[i] = 0.f;
     bool ok = true;
     for (int c = 0; c < n_chunks; ++c) {
-      const int cb = c & 1;
-      if (!mbar_wait(&chunk_full[cb], (c >> 1) & 1, abort_flag, a.status)) {
+      const int cb = c % n_acc;
+      if (!mbar_wait(&chunk_full[cb], (c / n_acc) & 1, abort_flag, a.status)) {
         ok = false;
         break;
       }
       tc_fence_after();
+      // 32 columns per load; the accumulator is handed back as soon as the warp's last load has
+      // landed, before the adds of that batch
+#define T3_RELEASE()                                 \
+  do {                                               \
+    tc_fence_before();                               \
+    __syncwarp();                                    \
+    if (lane == 0) mbar_arrive(&chunk_empty[cb]);   \
+  } while (0)
+      if (nu == 0) T3_RELEASE();
+      const uint32_t col0 = tmem + lane_off + cb * acc_cols + u0 * 16;
 #pragma unroll
-      for (int u = 0; u < T3_MAX_UNITS; ++u) {
-        if (u0 + u < u1) {
-          uint32_t v[16];
-          tmem_ld16(tmem + lane_off + cb * nt + (u0 + u) * 16, v);
+      for (int p = 0; p < T3_MAX_UNITS / 2; ++p) {
+        const int u = 2 * p;
+        if (u + 1 < nu) {
+          uint32_t v[32];
+          tmem_ld32(col0 + u * 16, v);
           tmem_ld_wait_regs(v);
+          if (u + 2 >= nu) T3_RELEASE();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) run[u * 16 + j] = __fadd_rn(run[u * 16 + j], __uint_as_float(v[j]));
+        } else if (u < nu) {
+          uint32_t v[16];
+          tmem_ld16(col0 + u * 16, v);
+          tmem_ld_wait_regs(v);
+          T3_RELEASE();
 #pragma unroll
           for (int j = 0; j < 16; ++j) run[u * 16 + j] = __fadd_rn(run[u * 16 + j], __uint_as_float(v[j]));
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&chunk_empty[cb]);
+#undef T3_RELEASE
     }
     if (ok) {
       // f16: undo the operands' power-of-two scales (exact)
@@ -644,10 +688,11 @@ __device__ __forceinline__ int weight_exp(unsigned int max_bits) {
 // e_fixed.  A magnitude of x 2^e beyond 65504 sets kDevRange in *status.
 __global__ void f16_split_kernel(const float* __restrict__ x, long long ldx, int K, int M, int Kp,
                                  const unsigned int* __restrict__ max_bits, int e_fixed, int* __restrict__ e_out,
-                                 uint16_t* __restrict__ hi, uint16_t* __restrict__ lo, int tiled, int* status) {
+                                 uint16_t* __restrict__ hi, uint16_t* __restrict__ lo, int layout, int* status) {
   if (status && (*reinterpret_cast<const volatile int*>(status) & kDevLayout)) return;
   const int e = max_bits ? weight_exp(*max_bits) : e_fixed;
   if (e_out && blockIdx.x == 0 && threadIdx.x == 0) *e_out = e;
+  const int tok_nt = x3_token_tile(M), tok_mt = (M + tok_nt - 1) / tok_nt;
   const size_t n = (size_t)M * Kp;
   bool over = false;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
@@ -656,12 +701,19 @@ __global__ void f16_split_kernel(const float* __restrict__ x, long long ldx, int
     over |= fabsf(v) > kF16Max;
     const __half h = __float2half_rn(v);
     const __half l = __float2half_rn(__fsub_rn(v, __half2float(h)));
-    const int rr = r % T3_ROWS, kk = k % X3_F16_BK;
-    const size_t o = tiled ? ((size_t)(r / T3_ROWS) * (Kp / X3_F16_BK) + k / X3_F16_BK) * (T3_ROWS * X3_F16_BK) +
-                                 rr * X3_F16_BK + ((((kk >> 3) ^ (rr >> 1)) & 3) << 3) + (kk & 7)
-                           : i;
+    size_t o = i;
+    if (layout == kSplitWeightTiles) {
+      const int rr = r % T3_ROWS, kk = k % X3_F16_BK;
+      o = ((size_t)(r / T3_ROWS) * (Kp / X3_F16_BK) + k / X3_F16_BK) * (2 * T3_ROWS * X3_F16_BK) + rr * X3_F16_BK +
+          ((((kk >> 3) ^ (rr >> 1)) & 3) << 3) + (kk & 7);
+    } else if (layout == kSplitTokenTiles) {
+      o = x3_xs_index(r, k, tok_nt, tok_mt);
+    }
     hi[o] = __half_as_ushort(h);
-    lo[o] = __half_as_ushort(l);
+    if (layout == kSplitTokenTiles)
+      hi[o + (size_t)tok_nt * 32] = __half_as_ushort(l);
+    else
+      lo[o] = __half_as_ushort(l);
   }
   if (over && status) atomicOr(status, kDevRange);
 }
@@ -689,10 +741,8 @@ int ew_grid(size_t work) {
 
 }  // namespace
 
-int tf32x3_token_tile(int M) {
-  const int m16 = (M + 15) / 16 * 16;
-  return m16 < 256 ? (m16 < 32 ? 32 : m16) : 256;
-}
+// Tokens per CTA (the MMA's N).
+int tf32x3_token_tile(int M) { return x3_token_tile(M); }
 
 static int x3_effective_splits(int K, int S, int bk) {
   int ks = (K + S - 1) / S;
@@ -720,7 +770,7 @@ int f16x3_effective_splits(int K, int S) { return x3_effective_splits(K, S, X3_F
 template <bool F16>
 static cudaError_t x3_partial_launch(const void* x_hi, const void* x_lo, const void* w_hi, const void* w_lo,
                                      const int* w_exp, int x_exp, int M, int N, int K, int S, float* part,
-                                     const int* status, cudaStream_t s, int w_tiled) {
+                                     const int* status, cudaStream_t s, int w_tiled, int x_tiled) {
   constexpr int BK = F16 ? X3_F16_BK : X3_TF32_BK;
   if (M <= 0) return cudaSuccess;
   if (N % T3_ROWS || K % BK) return cudaErrorInvalidValue;
@@ -730,6 +780,8 @@ static cudaError_t x3_partial_launch(const void* x_hi, const void* x_lo, const v
   const int S_eff = (K + ks - 1) / ks;
   CUtensorMap whi, wlo, xhi, xlo;
   bool ok;
+  if (w_tiled) w_lo = w_hi;  // the tiled layouts hold both parts (the maps are then unused)
+  if (x_tiled) x_lo = x_hi;
   if (F16)
     ok = make_tmap_bf16_2d(&whi, w_hi, K, N, (uint64_t)K * 2, BK, T3_ROWS, CU_TENSOR_MAP_SWIZZLE_64B) &&
          make_tmap_bf16_2d(&wlo, w_lo, K, N, (uint64_t)K * 2, BK, T3_ROWS, CU_TENSOR_MAP_SWIZZLE_64B) &&
@@ -750,8 +802,8 @@ static cudaError_t x3_partial_launch(const void* x_hi, const void* x_lo, const v
   static unsigned long long smem_set = 0;  // opted in to the largest size once per device
   cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(x3_partial_kernel<F16>), T3_SMEM_MAX, &smem_set);
   if (e != cudaSuccess) return e;
-  T3Args a{M, N, K, ks, nt, stages, F16 && w_tiled, static_cast<const uint16_t*>(w_hi),
-           static_cast<const uint16_t*>(w_lo), part, const_cast<int*>(status), w_exp, x_exp};
+  T3Args a{M, N, K, ks, nt, stages, F16 && w_tiled, F16 && x_tiled, static_cast<const uint16_t*>(w_hi),
+           static_cast<const uint16_t*>(x_hi), part, const_cast<int*>(status), w_exp, x_exp};
   dim3 grid(N / T3_ROWS, (M + nt - 1) / nt, S_eff);
   x3_partial_kernel<F16><<<grid, T3_THREADS, smem, s>>>(whi, wlo, xhi, xlo, a);
   return cudaGetLastError();
@@ -759,13 +811,14 @@ static cudaError_t x3_partial_launch(const void* x_hi, const void* x_lo, const v
 
 cudaError_t tf32x3_partial_launch(const float* x_hi, const float* x_lo, const float* w_hi, const float* w_lo, int M,
                                   int N, int K, int S, float* part, const int* status, cudaStream_t s) {
-  return x3_partial_launch<false>(x_hi, x_lo, w_hi, w_lo, nullptr, 0, M, N, K, S, part, status, s, 0);
+  return x3_partial_launch<false>(x_hi, x_lo, w_hi, w_lo, nullptr, 0, M, N, K, S, part, status, s, 0, 0);
 }
 
 cudaError_t f16x3_partial_launch(const uint16_t* x_hi, const uint16_t* x_lo, const uint16_t* w_hi,
                                  const uint16_t* w_lo, const int* w_exp, int x_exp, int M, int N, int K, int S,
-                                 float* part, const int* status, cudaStream_t s, int w_tiled) {
-  return x3_partial_launch<true>(x_hi, x_lo, w_hi, w_lo, w_exp, x_exp, M, N, K, S, part, status, s, w_tiled);
+                                 float* part, const int* status, cudaStream_t s, int w_tiled, int x_tiled) {
+  return x3_partial_launch<true>(x_hi, x_lo, w_hi, w_lo, w_exp, x_exp, M, N, K, S, part, status, s, w_tiled,
+                                 x_tiled);
 }
 
 cudaError_t absmax_launch(const float* x, size_t n, unsigned int* out, cudaStream_t s) {
@@ -777,11 +830,12 @@ cudaError_t absmax_launch(const float* x, size_t n, unsigned int* out, cudaStrea
 
 cudaError_t f16_split_launch(const float* x, long long ldx, int K, int M, int Kp, const unsigned int* max_bits,
                              int e_fixed, int* e_out, uint16_t* hi, uint16_t* lo, int* status, cudaStream_t s,
-                             int tiled) {
+                             int layout) {
   if (M <= 0) return cudaSuccess;
   if (K < 1 || Kp < K || ldx < K) return cudaErrorInvalidValue;
-  if (tiled && (M % T3_ROWS || Kp % X3_F16_BK)) return cudaErrorInvalidValue;
-  f16_split_kernel<<<ew_grid((size_t)M * Kp), 256, 0, s>>>(x, ldx, K, M, Kp, max_bits, e_fixed, e_out, hi, lo, tiled,
+  if (layout == kSplitWeightTiles && (M % T3_ROWS || Kp % X3_F16_BK)) return cudaErrorInvalidValue;
+  if (layout == kSplitTokenTiles && Kp % X3_F16_BK) return cudaErrorInvalidValue;
+  f16_split_kernel<<<ew_grid((size_t)M * Kp), 256, 0, s>>>(x, ldx, K, M, Kp, max_bits, e_fixed, e_out, hi, lo, layout,
                                                              status);
   return cudaGetLastError();
 }
@@ -843,7 +897,7 @@ cudaError_t attention_f32_launch(const float* q, const float* k, const float* v,
                                  const int* count, int max_items, int n_tokens, int H, int Dh, float* o,
                                  uint16_t* o_split, int* status, cudaStream_t s) {
   if (max_items <= 0) return cudaSuccess;
-  const dim3 grid(max_items * 4, H);
+  const dim3 grid(max_items * AF_BLOCKS, H);
   const float scale = (float)(1.0 / sqrt((double)Dh));
   if (Dh == 128) {
     static unsigned long long set = 0;

@@ -94,7 +94,8 @@ int attention_max_items(int n_docs, int n_tokens);
 
 // Elementwise / reduction kernels.
 // out_kind: 0 bf16, 1 fp32, 2 f16 (values beyond f16's finite range set kDevRange in *status),
-// 3 the 3xF16 GEMM's operand: f16 hi [n][d] at y and lo [n][d] right after it, of y * 2^kF16x3ActExp.
+// 3 the 3xF16 GEMM's operand: f16 hi and lo parts of y * 2^kF16x3ActExp in the token-tiled layout of
+// x3_xs_index (token tile x3_token_tile(n)).
 cudaError_t norm_modulate_launch(const float* x, const float* x_lo, int n, int d, int norm, float eps, const float* ln_g,
                                  const float* ln_b, const uint8_t* tags, const float* shift, const float* scale,
                                  long long mod_stride, void* y, int out_kind, int* status, cudaStream_t s);
@@ -159,17 +160,23 @@ constexpr int kF16x3K = 64;
 constexpr int kF16x3ActExp = 4;  // the activations' fixed scale exponent
 int f16x3_splits(int M, int N, int K);
 int f16x3_effective_splits(int K, int S);
+// With w_tiled, W is the bind-time weight-tile layout of f16_split_launch (kSplitWeightTiles; w_lo is
+// unused); with x_tiled, x_hi is the token-tiled operand of x3_xs_index (x_lo unused).  Otherwise both
+// are row-major [rows][K] hi and lo arrays.
 cudaError_t f16x3_partial_launch(const uint16_t* x_hi, const uint16_t* x_lo, const uint16_t* w_hi,
                                  const uint16_t* w_lo, const int* w_exp, int x_exp, int M, int N, int K, int S,
-                                 float* part, const int* status, cudaStream_t s, int w_tiled = 0);
+                                 float* part, const int* status, cudaStream_t s, int w_tiled = 0, int x_tiled = 0);
 // Largest |x| (as float bits) into *out (cleared first).
 cudaError_t absmax_launch(const float* x, size_t n, unsigned int* out, cudaStream_t s);
-// x [M][K] (stride ldx) -> f16 hi, lo [M][Kp] of x 2^e, zero-padded: e from *max_bits (a weight's scale,
-// also written to *e_out) when max_bits is given, else e_fixed; kDevRange in *status past 65504.  With
-// `tiled` (weights) the parts are laid out [M / 128][Kp / 32][128][32] for f16x3_partial_launch's w_tiled.
+// x [M][K] (stride ldx) -> f16 hi, lo parts of x 2^e, zero-padded to Kp columns: e from *max_bits (a
+// weight's scale, also written to *e_out) when max_bits is given, else e_fixed; kDevRange in *status
+// past 65504.  Layouts: kSplitRows, hi and lo [M][Kp]; kSplitWeightTiles, 128 x 32 tiles [M / 128][Kp /
+// 32], each tile's hi part (4096 elements) followed by its lo part, pre-swizzled for the 64-byte
+// swizzle (pass lo = hi + 4096); kSplitTokenTiles, the layout of x3_xs_index (lo unused).
+enum F16SplitLayout : int { kSplitRows = 0, kSplitWeightTiles = 1, kSplitTokenTiles = 2 };
 cudaError_t f16_split_launch(const float* x, long long ldx, int K, int M, int Kp, const unsigned int* max_bits,
                              int e_fixed, int* e_out, uint16_t* hi, uint16_t* lo, int* status, cudaStream_t s,
-                             int tiled = 0);
+                             int layout = kSplitRows);
 // The 3xTF32 GEMM's tiling: K a multiple of kTf32x3K, N (output features) a multiple of kTf32x3N.
 constexpr int kTf32x3K = 32;
 constexpr int kTf32x3N = 128;
@@ -185,13 +192,13 @@ cudaError_t sgemm_reduce_store_launch(const float* part, int S, int M, int N, co
 cudaError_t sgemm_reduce_qkv_launch(const float* part, int S, int M, int d, int Dh, int half, const float* bias,
                                     const float* cs, const float* sn, float* q, float* k, float* v, const int* status,
                                     cudaStream_t s);
-// h_split: when given, h is written as the 3xF16 GEMM's operand (f16 hi [M][F] then lo [M][F] of
-// h * 2^kF16x3ActExp) instead of fp32 into h.
+// h_split: when given, h is written as the 3xF16 GEMM's token-tiled operand (x3_xs_index) of
+// h * 2^kF16x3ActExp instead of fp32 into h.
 cudaError_t sgemm_reduce_swiglu_launch(const float* part, int S, int M, int F, const float* bias, float* h,
                                        uint16_t* h_split, int* status, cudaStream_t s);
 // Exact fp32 attention over the (document, 128-row q-tile) list of attention_schedule_launch.
-// o_split: when given, o is written as the 3xF16 GEMM's operand (f16 hi [n][d] then lo [n][d] of
-// o * 2^kF16x3ActExp, n_tokens rows) instead of fp32 into o.
+// o_split: when given, o is written as the 3xF16 GEMM's token-tiled operand (x3_xs_index, n_tokens
+// rows) of o * 2^kF16x3ActExp instead of fp32 into o.
 cudaError_t attention_f32_launch(const float* q, const float* k, const float* v, const int32_t* cu, const int2* items,
                                  const int* count, int max_items, int n_tokens, int H, int Dh, float* o,
                                  uint16_t* o_split, int* status, cudaStream_t s);
