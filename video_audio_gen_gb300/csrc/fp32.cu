@@ -247,22 +247,30 @@ __global__ void __launch_bounds__(AF_WARPS * 32) attention_f32_kernel(
     }
     __syncthreads();
     if (c0 + AF_KC < b) fetch(c0 + AF_KC);
-    float s[AF_ROWS];
+    // four partial sums per row (4-dim groups e4 mod 4) quarter the dependent FMA chains
+    float s[AF_ROWS], sp[4][AF_ROWS];
 #pragma unroll
-    for (int i = 0; i < AF_ROWS; ++i) s[i] = 0.f;
+    for (int i = 0; i < AF_ROWS; ++i) sp[0][i] = sp[1][i] = sp[2][i] = sp[3][i] = 0.f;
     const float4* kj = reinterpret_cast<const float4*>(sk + lane * KS);
-#pragma unroll 4
-    for (int e4 = 0; e4 < D4; ++e4) {
-      const float4 kv = kj[e4];
+#pragma unroll 2
+    for (int e4 = 0; e4 < D4; e4 += 4) {
+      float4 kv[4];
+#pragma unroll
+      for (int g = 0; g < 4; ++g) kv[g] = kj[e4 + g];
 #pragma unroll
       for (int i = 0; i < AF_ROWS; ++i) {
-        const float4 qv = reinterpret_cast<const float4*>(myq + i * DH)[e4];
-        s[i] = fmaf(qv.x, kv.x, s[i]);
-        s[i] = fmaf(qv.y, kv.y, s[i]);
-        s[i] = fmaf(qv.z, kv.z, s[i]);
-        s[i] = fmaf(qv.w, kv.w, s[i]);
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const float4 qv = reinterpret_cast<const float4*>(myq + i * DH)[e4 + g];
+          sp[g][i] = fmaf(qv.x, kv[g].x, sp[g][i]);
+          sp[g][i] = fmaf(qv.y, kv[g].y, sp[g][i]);
+          sp[g][i] = fmaf(qv.z, kv[g].z, sp[g][i]);
+          sp[g][i] = fmaf(qv.w, kv[g].w, sp[g][i]);
+        }
       }
     }
+#pragma unroll
+    for (int i = 0; i < AF_ROWS; ++i) s[i] = (sp[0][i] + sp[1][i]) + (sp[2][i] + sp[3][i]);
     float p[AF_ROWS];
 #pragma unroll
     for (int i = 0; i < AF_ROWS; ++i) {
@@ -281,6 +289,7 @@ __global__ void __launch_bounds__(AF_WARPS * 32) attention_f32_kernel(
       for (int e = 0; e < PL; ++e) acc[i][e] *= alpha;
       m[i] = mn;
     }
+#pragma unroll 4
     for (int j = 0; j < nk; ++j) {
       float vv[PL];
       if constexpr (PL == 4) {
