@@ -477,6 +477,9 @@ __global__ void __launch_bounds__(T3_THREADS, 1)
   const uint32_t tmem = *tmem_slot;
 
   auto produce = [&]() {
+    // the weights are read once per forward: evict them first, so that the activations and the
+    // split partials (read by the next kernel) stay in L2
+    const uint64_t w_policy = l2_policy_evict_first();
     // CTAs side by side start at different K blocks of their range, so that they do not all ask L2
     // for the same activation rows at the same time (the chunk sums are independent of order)
     const int rot = n_kb > 0 ? (int)((long long)blockIdx.x * n_kb / gridDim.x) : 0;
@@ -490,7 +493,7 @@ __global__ void __launch_bounds__(T3_THREADS, 1)
       mbar_arrive_expect_tx(&full[st], stage_bytes);
       if (a.w_tiled) {
         const size_t t = ((size_t)blockIdx.x * (a.K / T3_BK) + k0 / T3_BK) * (2 * T3_ROWS * T3_BK);
-        bulk_load(base, a.w_hi + t, 2 * T3_W_BYTES, &full[st]);
+        bulk_load_hint(base, a.w_hi + t, 2 * T3_W_BYTES, &full[st], w_policy);
       } else {
         tma_load_2d(base, &tmWhi, &full[st], k0, n0);
         tma_load_2d(base + T3_W_BYTES, &tmWlo, &full[st], k0, n0);
@@ -787,16 +790,18 @@ static cudaError_t x3_partial_launch(const void* x_hi, const void* x_lo, const v
   int ks = (K + S - 1) / S;
   ks = (ks + BK - 1) / BK * BK;
   const int S_eff = (K + ks - 1) / ks;
-  CUtensorMap whi, wlo, xhi, xlo;
-  bool ok;
-  if (w_tiled) w_lo = w_hi;  // the tiled layouts hold both parts (the maps are then unused)
-  if (x_tiled) x_lo = x_hi;
-  if (F16)
-    ok = make_tmap_bf16_2d(&whi, w_hi, K, N, (uint64_t)K * 2, BK, T3_ROWS, CU_TENSOR_MAP_SWIZZLE_64B) &&
-         make_tmap_bf16_2d(&wlo, w_lo, K, N, (uint64_t)K * 2, BK, T3_ROWS, CU_TENSOR_MAP_SWIZZLE_64B) &&
-         make_tmap_bf16_2d(&xhi, x_hi, K, M, (uint64_t)K * 2, BK, nt, CU_TENSOR_MAP_SWIZZLE_64B) &&
-         make_tmap_bf16_2d(&xlo, x_lo, K, M, (uint64_t)K * 2, BK, nt, CU_TENSOR_MAP_SWIZZLE_64B);
-  else
+  // the tiled layouts are loaded with plain bulk copies: their tensor maps are never read, so they
+  // are left zeroed instead of encoded (the encoding is most of this launch's host time)
+  CUtensorMap whi = {}, wlo = {}, xhi = {}, xlo = {};
+  bool ok = true;
+  if (F16) {
+    if (!w_tiled)
+      ok = make_tmap_bf16_2d(&whi, w_hi, K, N, (uint64_t)K * 2, BK, T3_ROWS, CU_TENSOR_MAP_SWIZZLE_64B) &&
+           make_tmap_bf16_2d(&wlo, w_lo, K, N, (uint64_t)K * 2, BK, T3_ROWS, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (ok && !x_tiled)
+      ok = make_tmap_bf16_2d(&xhi, x_hi, K, M, (uint64_t)K * 2, BK, nt, CU_TENSOR_MAP_SWIZZLE_64B) &&
+           make_tmap_bf16_2d(&xlo, x_lo, K, M, (uint64_t)K * 2, BK, nt, CU_TENSOR_MAP_SWIZZLE_64B);
+  } else
     ok = make_tmap_f32_2d(&whi, w_hi, K, N, (uint64_t)K * 4, T3_ROWS) &&
          make_tmap_f32_2d(&wlo, w_lo, K, N, (uint64_t)K * 4, T3_ROWS) &&
          make_tmap_f32_2d(&xhi, x_hi, K, M, (uint64_t)K * 4, nt) &&
