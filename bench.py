@@ -93,6 +93,13 @@ def fp32_alu_peak_tflops(peaks: dict, n_sms: int) -> float:
     return n_sms * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
 
 
+def fp32_weight_bytes(m: dict) -> dict:
+    """Bytes of weights one launch of each fp32 GEMM kind streams: f16 hi and lo parts, 4 per weight."""
+    d, F = m["hidden"], m["ffn_hidden"]
+    return {"gemm_qkv": 3 * d * d * 4, "gemm_out": d * d * 4, "gemm_ffn_up": 2 * F * d * 4,
+            "gemm_ffn_down": d * F * 4}
+
+
 def fp32_3xf16_peak_tflops(peaks: dict) -> float:
     """fp32-equivalent peak of the 3xF16 GEMM: the f16 tensor rate (the measured sustained bf16
     figure; kind::f16 runs f16 and bf16 at one rate) over the three f16 products it spends per fp32
@@ -364,6 +371,12 @@ def run_gpu(args, w, dist, rank, world):
                 entry.update(bound="alu", achieved_tflops=round(tf, 1), frac=round(tf / alu_peak, 3))
             elif m["dtype"] == "fp32":
                 entry.update(bound="tensor", achieved_tflops=round(tf, 1), frac=round(tf / f16x3_peak, 3))
+                # the other bound of these small-M GEMMs: the weight stream, 4 bytes per weight
+                # (the f16 hi and lo parts), read once per launch
+                wb = fp32_weight_bytes(m).get(k)
+                if wb:
+                    gbs = wb / (avg * 1e-3) / 1e9
+                    entry.update(weight_gbs=round(gbs, 1), hbm_frac=round(gbs / peaks["hbm_gbs"], 3))
             else:
                 entry.update(bound="tensor", achieved_tflops=round(tf, 1),
                              frac=round(tf / peaks["bf16_tflops_sustained"], 3))
@@ -389,6 +402,9 @@ def run_gpu(args, w, dist, rank, world):
                     "algorithmic_flops_per_launch": fl["per_launch"][top]}
     elif m["dtype"] == "fp32":
         roofline = {"bound": "tensor", "kernel": top, "achieved": kernels[top]["achieved_tflops"],
+                    "hbm": {"achieved_gbs": kernels[top].get("weight_gbs"), "peak_gbs": peaks["hbm_gbs"],
+                            "frac": kernels[top].get("hbm_frac"),
+                            "bytes_per_launch": fp32_weight_bytes(m).get(top)},
                     "peak": round(f16x3_peak, 1), "unit": "TFLOP/s", "frac": kernels[top]["frac"], "traffic": traffic,
                     "peak_source": f"3xF16: bf16_tflops_sustained of {peak_src} (the f16 rate) / 3 f16 products "
                                    "per fp32 product",
