@@ -44,7 +44,20 @@ TRAFFIC = {
     ("gemm_ffn_down", "video_audio_bf16"): {"bytes": 1241438208, "src_sha": "86f8bc031b1d4c6a"},
     ("norm_modulate", "video_audio_bf16"): {"bytes": 288634112, "src_sha": "139ad8f729b321b6"},
     ("attention", "long_doc_bf16"): {"bytes": 1366486272, "src_sha": "b30c215725fdbf8d"},
+    # fp32 path, captured on the two-block slice music_fp32_l2 (the same launch shapes)
+    ("gemm_qkv", "music_fp32"): {"bytes": 52133888, "src_sha": "39e99c7e78d4646a"},
+    ("gemm_out", "music_fp32"): {"bytes": 18275072, "src_sha": "39e99c7e78d4646a"},
+    ("gemm_ffn_up", "music_fp32"): {"bytes": 139017728, "src_sha": "39e99c7e78d4646a"},
+    ("gemm_ffn_down", "music_fp32"): {"bytes": 74777856, "src_sha": "39e99c7e78d4646a"},
+    ("attention", "music_fp32"): {"bytes": 4258816, "src_sha": "39e99c7e78d4646a"},
 }
+
+
+def traffic_src(kind: str, m: dict) -> str:
+    """The source file of the kernels behind a kind (a TRAFFIC entry holds while its hash matches)."""
+    if m["dtype"] == "fp32":
+        return "fp32.cu"
+    return "attention.cu" if kind == "attention" else ("gemm.cu" if kind.startswith("gemm") else "elementwise.cu")
 
 
 # ------------------------------------------------------------------------------------------------
@@ -385,16 +398,14 @@ def run_gpu(args, w, dist, rank, world):
             entry.update(bound="hbm", achieved_gbs=round(gbs, 1), frac=round(gbs / peaks["hbm_gbs"], 3))
         tr = TRAFFIC.get((k, args.workload))
         if tr:
-            src = "attention.cu" if k == "attention" else ("gemm.cu" if k.startswith("gemm") else "elementwise.cu")
-            entry["traffic"] = tr["bytes"] if tr["src_sha"] == source_hash(src) else None
+            entry["traffic"] = tr["bytes"] if tr["src_sha"] == source_hash(traffic_src(k, m)) else None
         kernels[k] = entry
     tot = sum(kt[k][0] for k in KINDS)
     for k in kernels:
         kernels[k]["share"] = round(kt[k][0] / tot, 3) if tot else None
     top = max((k for k in kernels if k in fl["per_launch"]), key=lambda k: kt[k][0])
-    src = "attention.cu" if top == "attention" else "gemm.cu"
     tr = TRAFFIC.get((top, args.workload))
-    traffic = tr["bytes"] if tr and tr["src_sha"] == source_hash(src) else None
+    traffic = tr["bytes"] if tr and tr["src_sha"] == source_hash(traffic_src(top, m)) else None
     if m["dtype"] == "fp32" and top == "attention":
         roofline = {"bound": "alu", "kernel": top, "achieved": kernels[top]["achieved_tflops"],
                     "peak": round(alu_peak, 1), "unit": "TFLOP/s", "frac": kernels[top]["frac"], "traffic": traffic,
