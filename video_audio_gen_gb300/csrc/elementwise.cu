@@ -31,6 +31,8 @@ __global__ void __launch_bounds__(256) norm_mod_kernel(const float* __restrict__
                                                        const float* __restrict__ shift,
                                                        const float* __restrict__ scale, long long stride, void* y,
                                                        int out_kind, int* status) {
+  pdl_wait();
+  pdl_trigger();
   if (status && (*reinterpret_cast<const volatile int*>(status) & kDevLayout)) return;
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -115,6 +117,8 @@ __global__ void __launch_bounds__(256) norm_mod_persistent_kernel(
     const float* __restrict__ x, const float* __restrict__ x_lo, int n, int d, int norm, float eps, const float* __restrict__ g,
     const float* __restrict__ b, const uint8_t* __restrict__ tags, const float* __restrict__ shift,
     const float* __restrict__ scale, long long stride, void* y, int out_kind, int* status) {
+  pdl_wait();
+  pdl_trigger();
   if (status && (*reinterpret_cast<const volatile int*>(status) & kDevLayout)) return;
   __shared__ float red[2][8];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -377,9 +381,10 @@ cudaError_t norm_launch_t(const float* x, const float* x_lo, int n, int d, int n
                           const uint8_t* tags, const float* shift, const float* scale, long long stride, void* y,
                           int out_kind, int* status, cudaStream_t s) {
   const int rows_per_block = 8;
-  norm_mod_kernel<NV><<<(n + rows_per_block - 1) / rows_per_block, 32 * rows_per_block, 0, s>>>(
-      x, x_lo, n, d, norm, eps, g, b, tags, shift, scale, stride, y, out_kind, status);
-  return cudaGetLastError();
+  cudaError_t e = launch_pdl(norm_mod_kernel<NV>, dim3((n + rows_per_block - 1) / rows_per_block),
+                             dim3(32 * rows_per_block), 0, s, x, x_lo, n, d, norm, eps, g, b, tags, shift, scale,
+                             stride, y, out_kind, status);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 int grid_for(long long work, int threads) {
@@ -417,13 +422,12 @@ cudaError_t norm_modulate_launch(const float* x, const float* x_lo, int n, int d
       per_sm = 4;                                                                                               \
     int blocks = num_sms() * (per_sm > 0 ? per_sm : 1);                                                         \
     if (blocks > n) blocks = n;                                                                                 \
-    if (x_lo)                                                                                                   \
-      norm_mod_persistent_kernel<k, true><<<blocks, 256, 0, s>>>(x, x_lo, n, d, norm, eps, ln_g, ln_b, tags,     \
-                                                                 shift, scale, mod_stride, y, out_kind, status); \
-    else                                                                                                        \
-      norm_mod_persistent_kernel<k, false><<<blocks, 256, 0, s>>>(x, x_lo, n, d, norm, eps, ln_g, ln_b, tags,    \
-                                                                  shift, scale, mod_stride, y, out_kind, status); \
-    return cudaGetLastError();                                                                                  \
+    cudaError_t e = x_lo ? launch_pdl(norm_mod_persistent_kernel<k, true>, dim3(blocks), dim3(256), 0, s, x, x_lo, n, \
+                                      d, norm, eps, ln_g, ln_b, tags, shift, scale, mod_stride, y, out_kind, status) \
+                         : launch_pdl(norm_mod_persistent_kernel<k, false>, dim3(blocks), dim3(256), 0, s, x, x_lo,  \
+                                      n, d, norm, eps, ln_g, ln_b, tags, shift, scale, mod_stride, y, out_kind,     \
+                                      status);                                                                   \
+    return e != cudaSuccess ? e : cudaGetLastError();                                                           \
   }
       DIT_VPT(1) DIT_VPT(2) DIT_VPT(3) DIT_VPT(4) DIT_VPT(5) DIT_VPT(6) DIT_VPT(7) DIT_VPT(8)
 #undef DIT_VPT

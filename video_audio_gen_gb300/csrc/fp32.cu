@@ -50,6 +50,8 @@ __device__ __forceinline__ float4 sum_parts4(const float* __restrict__ part, int
 __global__ void sgemm_reduce_store_kernel(const float* __restrict__ part, int S, int M, int N,
                                           const float* __restrict__ bias, float* __restrict__ out, int add,
                                           float* __restrict__ lo, const int* status) {
+  pdl_wait();
+  pdl_trigger();
   if (status && (*reinterpret_cast<const volatile int*>(status) & kDevLayout)) return;
   const size_t MN = (size_t)M * N;
   const int c = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
@@ -91,6 +93,8 @@ __global__ void sgemm_reduce_qkv_kernel(const float* __restrict__ part, int S, i
                                         const float* __restrict__ bias, const float* __restrict__ cs,
                                         const float* __restrict__ sn, float* __restrict__ q, float* __restrict__ k,
                                         float* __restrict__ v, const int* status) {
+  pdl_wait();
+  pdl_trigger();
   if (status && (*reinterpret_cast<const volatile int*>(status) & kDevLayout)) return;
   const int N = 3 * d;
   const size_t MN = (size_t)M * N;
@@ -129,6 +133,8 @@ __global__ void sgemm_reduce_qkv_kernel(const float* __restrict__ part, int S, i
 __global__ void sgemm_reduce_swiglu_kernel(const float* __restrict__ part, int S, int M, int F,
                                            const float* __restrict__ bias, float* __restrict__ h,
                                            uint16_t* __restrict__ h_split, int* status) {
+  pdl_wait();
+  pdl_trigger();
   if (status && (*reinterpret_cast<const volatile int*>(status) & kDevLayout)) return;
   const size_t MN = (size_t)M * 2 * F;
   const int f0 = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
@@ -185,6 +191,8 @@ __global__ void __launch_bounds__(AF_WARPS * 32) attention_f32_kernel(
     const float* __restrict__ q, const float* __restrict__ k, const float* __restrict__ v, const int32_t* __restrict__ cu,
     const int2* __restrict__ items, const int* __restrict__ count, int n_tokens, int H, float scale,
     float* __restrict__ o, uint16_t* __restrict__ o_split, int* status) {
+  pdl_wait();
+  pdl_trigger();
   if (status && (*reinterpret_cast<const volatile int*>(status) & kDevLayout)) return;
   constexpr int PL = DH / 32;
   constexpr int KS = af_kstride<DH>();
@@ -429,6 +437,8 @@ __global__ void __launch_bounds__(T3_THREADS, 1)
     x3_partial_kernel(const __grid_constant__ CUtensorMap tmWhi, const __grid_constant__ CUtensorMap tmWlo,
                       const __grid_constant__ CUtensorMap tmXhi, const __grid_constant__ CUtensorMap tmXlo,
                       const T3Args a) {
+  pdl_wait();
+  pdl_trigger();
   using G = X3Geom<F16>;
   constexpr int T3_BK = G::BK;  // K elements per stage
   constexpr int T3_CHUNK = G::CHUNK;
@@ -819,8 +829,8 @@ static cudaError_t x3_partial_launch(const void* x_hi, const void* x_lo, const v
   T3Args a{M, N, K, ks, nt, stages, F16 && w_tiled, F16 && x_tiled, static_cast<const uint16_t*>(w_hi),
            static_cast<const uint16_t*>(x_hi), part, const_cast<int*>(status), w_exp, x_exp};
   dim3 grid(N / T3_ROWS, (M + nt - 1) / nt, S_eff);
-  x3_partial_kernel<F16><<<grid, T3_THREADS, smem, s>>>(whi, wlo, xhi, xlo, a);
-  return cudaGetLastError();
+  e = launch_pdl(x3_partial_kernel<F16>, grid, dim3(T3_THREADS), smem, s, whi, wlo, xhi, xlo, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t tf32x3_partial_launch(const float* x_hi, const float* x_lo, const float* w_hi, const float* w_lo, int M,
@@ -885,8 +895,9 @@ cudaError_t sgemm_reduce_store_launch(const float* part, int S, int M, int N, co
                                       float* lo, const int* status, cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
   if (N % 4) return cudaErrorInvalidValue;
-  sgemm_reduce_store_kernel<<<reduce_grid(M, N), 256, 0, s>>>(part, S, M, N, bias, out, add, lo, status);
-  return cudaGetLastError();
+  cudaError_t e = launch_pdl(sgemm_reduce_store_kernel, reduce_grid(M, N), dim3(256), 0, s, part, S, M, N, bias, out,
+                             add, lo, status);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t sgemm_reduce_qkv_launch(const float* part, int S, int M, int d, int Dh, int half, const float* bias,
@@ -894,17 +905,18 @@ cudaError_t sgemm_reduce_qkv_launch(const float* part, int S, int M, int d, int 
                                     cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
   if (d % 4 || Dh % 4 || half % 4) return cudaErrorInvalidValue;
-  sgemm_reduce_qkv_kernel<<<reduce_grid(M, 3 * d), 256, 0, s>>>(part, S, M, d, Dh, half, bias, cs, sn, q, k, v,
-                                                                 status);
-  return cudaGetLastError();
+  cudaError_t e = launch_pdl(sgemm_reduce_qkv_kernel, reduce_grid(M, 3 * d), dim3(256), 0, s, part, S, M, d, Dh, half,
+                             bias, cs, sn, q, k, v, status);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t sgemm_reduce_swiglu_launch(const float* part, int S, int M, int F, const float* bias, float* h,
                                        uint16_t* h_split, int* status, cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
   if (F % 4) return cudaErrorInvalidValue;
-  sgemm_reduce_swiglu_kernel<<<reduce_grid(M, F), 256, 0, s>>>(part, S, M, F, bias, h, h_split, status);
-  return cudaGetLastError();
+  cudaError_t e = launch_pdl(sgemm_reduce_swiglu_kernel, reduce_grid(M, F), dim3(256), 0, s, part, S, M, F, bias, h,
+                             h_split, status);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t attention_f32_launch(const float* q, const float* k, const float* v, const int32_t* cu, const int2* items,
@@ -917,14 +929,16 @@ cudaError_t attention_f32_launch(const float* q, const float* k, const float* v,
     static unsigned long long set = 0;
     cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(attention_f32_kernel<128>), af_smem_bytes<128>(), &set);
     if (e != cudaSuccess) return e;
-    attention_f32_kernel<128><<<grid, AF_WARPS * 32, af_smem_bytes<128>(), s>>>(q, k, v, cu, items, count, n_tokens,
-                                                                              H, scale, o, o_split, status);
+    e = launch_pdl(attention_f32_kernel<128>, grid, dim3(AF_WARPS * 32), af_smem_bytes<128>(), s, q, k, v, cu, items,
+                   count, n_tokens, H, scale, o, o_split, status);
+    if (e != cudaSuccess) return e;
   } else if (Dh == 64) {
     static unsigned long long set = 0;
     cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(attention_f32_kernel<64>), af_smem_bytes<64>(), &set);
     if (e != cudaSuccess) return e;
-    attention_f32_kernel<64><<<grid, AF_WARPS * 32, af_smem_bytes<64>(), s>>>(q, k, v, cu, items, count, n_tokens, H,
-                                                                            scale, o, o_split, status);
+    e = launch_pdl(attention_f32_kernel<64>, grid, dim3(AF_WARPS * 32), af_smem_bytes<64>(), s, q, k, v, cu, items,
+                   count, n_tokens, H, scale, o, o_split, status);
+    if (e != cudaSuccess) return e;
   } else {
     return cudaErrorInvalidValue;
   }
