@@ -306,7 +306,8 @@ struct Launch {
       if (a) cudaEventRecord(a, s);
     }
   }
-  void done() {
+  // n: the kernels launched in this group (the stats count kernels)
+  void done(int n = 1) {
     if (h && h->timing && a) {
       cudaEvent_t b = next_event(h);
       if (b) {
@@ -315,11 +316,11 @@ struct Launch {
       }
     }
     if (h) {
-      h->stats.kernels_launched++;
-      if (kind == 0 || kind == 2 || kind == 3 || kind == 4) h->stats.gemm_launches++;
-      else if (kind == 1) h->stats.attention_launches++;
-      else if (kind == 5) h->stats.norm_launches++;
-      else h->stats.other_launches++;
+      h->stats.kernels_launched += n;
+      if (kind == 0 || kind == 2 || kind == 3 || kind == 4) h->stats.gemm_launches += n;
+      else if (kind == 1) h->stats.attention_launches += n;
+      else if (kind == 5) h->stats.norm_launches += n;
+      else h->stats.other_launches += n;
     }
   }
 };
@@ -465,21 +466,33 @@ dit_status forward_fp32(dit_handle* h, const float* x_tokens, const int32_t* cu_
     DIT_CK(h, rope_cache_launch(pos_thw, N, c.rope_axes, c.rope_dims, c.rope_base, cosc, sinc, status, s), "rope cache");
     ln.done();
   }
+  // The reductions that add into the residual stream are fused with the norm that reads it next
+  // (one kernel instead of two) when the width allows it.
+  const bool fuse = reduce_norm_fusable(d) && c.n_blocks > 0;
+  bool norm1_done = false;  // block l's norm1 was written by the previous fused reduction
   if (io) {
     // 1x1 pre-convolution as MatmulBT on the frame-major activation ([M3] "What moved")
     Launch ln(h, s, 6);
     DIT_CK(h, io_transpose_launch(x_tokens, xt, cu_seqlens, doc_ids, N, io, 1, status, s), "to frames");
     DIT_CK(h, g.run(xt, h->s_pre, N, d, io), "pre-conv");
-    DIT_CK(h, sgemm_reduce_store_launch(g.part, g.S, N, d, h->b_pre, resid, 0, resid_lo, status, s),
-           "pre-conv reduce");
-    ln.done();
+    if (fuse) {
+      DIT_CK(h, sgemm_reduce_resid_norm_launch(g.part, g.S, N, d, h->b_pre, resid, resid_lo, 0, c.norm, c.norm_eps,
+                                               h->blocks[0].ln1_g, h->blocks[0].ln1_b, g.xs, 3, status, s),
+             "pre-conv reduce + norm1");
+      norm1_done = true;
+    } else {
+      DIT_CK(h, sgemm_reduce_store_launch(g.part, g.S, N, d, h->b_pre, resid, 0, resid_lo, status, s),
+             "pre-conv reduce");
+    }
+    ln.done(4);
   } else {
     DIT_CK(h, cudaMemcpyAsync(resid, x_tokens, (size_t)N * d * 4, cudaMemcpyDeviceToDevice, s), "copy x");
     DIT_CK(h, cudaMemsetAsync(resid_lo, 0, (size_t)N * d * 4, s), "clear residual low part");
   }
   for (int l = 0; l < c.n_blocks; ++l) {
     const BlockDev& B = h->blocks[l];
-    {
+    const bool last = l + 1 == c.n_blocks;
+    if (!norm1_done) {
       Launch ln(h, s, 5);
       DIT_CK(h, norm_modulate_launch(resid, resid_lo, N, d, c.norm, c.norm_eps, B.ln1_g, B.ln1_b, nullptr, nullptr,
                                      nullptr, 0, g.xs, 3, status, s), "norm1");
@@ -490,7 +503,7 @@ dit_status forward_fp32(dit_handle* h, const float* x_tokens, const int32_t* cu_
       DIT_CK(h, g.run_split(B.s_qkv, N, 3 * d, d), "qkv");
       DIT_CK(h, sgemm_reduce_qkv_launch(g.part, g.S, N, d, c.head_dim, L.half, B.b_qkv, cosc, sinc, q, k, v, status, s),
              "qkv reduce");
-      ln.done();
+      ln.done(2);
     }
     {
       Launch ln(h, s, 1);
@@ -501,10 +514,16 @@ dit_status forward_fp32(dit_handle* h, const float* x_tokens, const int32_t* cu_
     {
       Launch ln(h, s, 2);
       DIT_CK(h, g.run_split(B.s_o, N, d, d), "out-proj");
-      DIT_CK(h, sgemm_reduce_store_launch(g.part, g.S, N, d, B.b_o, resid, 1, resid_lo, status, s), "out-proj reduce");
-      ln.done();
+      if (fuse)
+        DIT_CK(h, sgemm_reduce_resid_norm_launch(g.part, g.S, N, d, B.b_o, resid, resid_lo, 1, c.norm, c.norm_eps,
+                                                 B.ln2_g, B.ln2_b, g.xs, 3, status, s),
+               "out-proj reduce + norm2");
+      else
+        DIT_CK(h, sgemm_reduce_store_launch(g.part, g.S, N, d, B.b_o, resid, 1, resid_lo, status, s),
+               "out-proj reduce");
+      ln.done(2);
     }
-    {
+    if (!fuse) {
       Launch ln(h, s, 5);
       DIT_CK(h, norm_modulate_launch(resid, resid_lo, N, d, c.norm, c.norm_eps, B.ln2_g, B.ln2_b, nullptr, nullptr,
                                      nullptr, 0, g.xs, 3, status, s), "norm2");
@@ -515,20 +534,31 @@ dit_status forward_fp32(dit_handle* h, const float* x_tokens, const int32_t* cu_
       DIT_CK(h, g.run_split(B.s_in, N, 2 * F, d), "ffn up");
       DIT_CK(h, sgemm_reduce_swiglu_launch(g.part, g.S, N, F, B.b_in_packed, nullptr, g.xs, status, s),
              "ffn up reduce");
-      ln.done();
+      ln.done(2);
     }
     {
       Launch ln(h, s, 4);
       DIT_CK(h, g.run_split(B.s_down, N, d, F), "ffn down");
-      DIT_CK(h, sgemm_reduce_store_launch(g.part, g.S, N, d, B.b_down, resid, 1, resid_lo, status, s),
-             "ffn down reduce");
-      ln.done();
+      if (fuse) {
+        // the next block's norm1, or after the last block the final norm
+        const float* ng = last ? h->lnf_g : h->blocks[l + 1].ln1_g;
+        const float* nb = last ? h->lnf_b : h->blocks[l + 1].ln1_b;
+        DIT_CK(h, sgemm_reduce_resid_norm_launch(g.part, g.S, N, d, B.b_down, resid, resid_lo, 1, c.norm, c.norm_eps,
+                                                 ng, nb, last ? (io ? static_cast<void*>(y) : out) : g.xs,
+                                                 last ? 1 : 3, status, s),
+               "ffn down reduce + norm");
+        norm1_done = true;
+      } else {
+        DIT_CK(h, sgemm_reduce_store_launch(g.part, g.S, N, d, B.b_down, resid, 1, resid_lo, status, s),
+               "ffn down reduce");
+      }
+      ln.done(2);
     }
     if (h->dump)
       DIT_CK(h, cudaMemcpyAsync(h->dump + (size_t)l * N * d, resid, (size_t)N * d * 4, cudaMemcpyDeviceToDevice, s),
              "dump");
   }
-  {
+  if (!fuse) {
     Launch ln(h, s, 5);
     DIT_CK(h, norm_modulate_launch(resid, resid_lo, N, d, c.norm, c.norm_eps, h->lnf_g, h->lnf_b, nullptr, nullptr, nullptr, 0,
                                    io ? y : out, 1, status, s), "final norm");
@@ -539,7 +569,7 @@ dit_status forward_fp32(dit_handle* h, const float* x_tokens, const int32_t* cu_
     DIT_CK(h, g.run(y, h->s_post, N, io, d), "post-conv");
     DIT_CK(h, sgemm_reduce_store_launch(g.part, g.S, N, io, h->b_post, xt, 0, nullptr, status, s), "post-conv reduce");
     DIT_CK(h, io_transpose_launch(xt, out, cu_seqlens, doc_ids, N, io, 0, status, s), "to channels");
-    ln.done();
+    ln.done(4);
   }
   h->stats.forwards++;
   return DIT_OK;
@@ -810,7 +840,7 @@ static dit_status latent_embed(dit_handle* h, const LatentArgs& a, const uint8_t
                                     status, s), "patch projection");
     DIT_CK(h, sgemm_reduce_rows_launch(a.part, tf32x3_effective_splits(Kp, want), M, d, d, h->lat_b_patch[m],
                                        a.rows + a.mr.off[m], resid, d, status, s), "patch projection store");
-    ln.done();
+    ln.done(3);
   }
   return DIT_OK;
 }
@@ -1179,7 +1209,7 @@ dit_status dit_forward_latent(dit_handle* h, const float* const* z, const int* n
     DIT_CK(h, sgemm_reduce_rows_launch(a.part, tf32x3_effective_splits(d, want), M, Np, h->lat_width[m],
                                        h->lat_b_head[m], nullptr, v[m], h->lat_width[m], status, s),
            "output head store");
-    ln.done();
+    ln.done(3);
   }
   return DIT_OK;
 }

@@ -86,6 +86,111 @@ __global__ void sgemm_reduce_store_kernel(const float* __restrict__ part, int S,
   }
 }
 
+// The split reduction of an fp32 GEMM whose output is added into the residual stream, fused with the
+// LayerNorm (or RMSNorm) that reads that stream next: one CTA per row (grid-stride), 256 threads of
+// VPT float4 each (d = 1024 * VPT).
+//   resid (+)= sum of the S partials + bias       (add = 0: resid = ..., resid_lo = 0; add = 1: the
+//                                                  compensated TwoSum add of sgemm_reduce_store_kernel)
+//   y = norm(resid + resid_lo) * g + b             (out_kind 1: fp32 [M][d]; 3: the next 3xF16
+//                                                  GEMM's token-tiled split operand)
+// The norm is the one of norm_mod_persistent_kernel on the compensated input, without modulation.
+template <int VPT>
+__global__ void __launch_bounds__(256) sgemm_reduce_resid_norm_kernel(
+    const float* __restrict__ part, int S, int M, int d, const float* __restrict__ bias, float* __restrict__ resid,
+    float* __restrict__ resid_lo, int add, int norm, float eps, const float* __restrict__ g,
+    const float* __restrict__ b, void* y, int out_kind, int* status) {
+  pdl_wait();
+  pdl_trigger();
+  if (status && (*reinterpret_cast<const volatile int*>(status) & kDevLayout)) return;
+  __shared__ float red[2][8];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const size_t MN = (size_t)M * d;
+  int parity = 0;
+  auto block_sum = [&](float s) -> float {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane == 0) red[parity][warp] = s;
+    __syncthreads();
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) t += red[parity][w];
+    parity ^= 1;
+    return t;
+  };
+  const int nt = x3_token_tile(M), mt = (M + nt - 1) / nt;
+  bool over = false;
+  for (int row = blockIdx.x; row < M; row += gridDim.x) {
+    float4 cur[VPT];
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int c = (i * 256 + threadIdx.x) * 4;
+      const size_t at = (size_t)row * d + c;
+      const float4 p = sum_parts4(part, S, MN, at);
+      const float4 b4 = bias ? *reinterpret_cast<const float4*>(bias + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float v[4] = {p.x + b4.x, p.y + b4.y, p.z + b4.z, p.w + b4.w};
+      float hi[4], lo[4];
+      if (!add) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          hi[e] = v[e];
+          lo[e] = 0.f;
+        }
+      } else {
+        const float4 a4 = *reinterpret_cast<const float4*>(resid + at);
+        const float4 l4 = *reinterpret_cast<const float4*>(resid_lo + at);
+        const float av[4] = {a4.x, a4.y, a4.z, a4.w}, lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float s = __fadd_rn(av[e], v[e]);
+          const float bb = __fsub_rn(s, av[e]);
+          const float err = __fadd_rn(__fsub_rn(av[e], __fsub_rn(s, bb)), __fsub_rn(v[e], bb));
+          hi[e] = s;
+          lo[e] = __fadd_rn(lv[e], err);
+        }
+      }
+      *reinterpret_cast<float4*>(resid + at) = make_float4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<float4*>(resid_lo + at) = make_float4(lo[0], lo[1], lo[2], lo[3]);
+      cur[i] = make_float4(hi[0] + lo[0], hi[1] + lo[1], hi[2] + lo[2], hi[3] + lo[3]);
+    }
+    float mean = 0.f;
+    if (norm == 1) {
+      float s = 0.f;
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) s += (cur[i].x + cur[i].y) + (cur[i].z + cur[i].w);
+      mean = block_sum(s) / (float)d;
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const float a0 = cur[i].x - mean, a1 = cur[i].y - mean, a2 = cur[i].z - mean, a3 = cur[i].w - mean;
+      ss += a0 * a0 + a1 * a1 + a2 * a2 + a3 * a3;
+    }
+    const float inv = 1.0f / sqrtf(block_sum(ss) / (float)d + eps);
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int c = (i * 256 + threadIdx.x) * 4;
+      float o[4] = {(cur[i].x - mean) * inv, (cur[i].y - mean) * inv, (cur[i].z - mean) * inv,
+                    (cur[i].w - mean) * inv};
+      if (g) {
+        const float4 gg = *reinterpret_cast<const float4*>(g + c);
+        o[0] *= gg.x; o[1] *= gg.y; o[2] *= gg.z; o[3] *= gg.w;
+      }
+      if (b) {
+        const float4 bb = *reinterpret_cast<const float4*>(b + c);
+        o[0] += bb.x; o[1] += bb.y; o[2] += bb.z; o[3] += bb.w;
+      }
+      if (out_kind == 3) {
+        const size_t xi = x3_xs_index(row, c, nt, mt);
+        uint16_t* xs = static_cast<uint16_t*>(y);
+        over |= store_f16_split4(o, kF16x3ActExp, xs + xi, xs + xi + (size_t)nt * 32);
+      } else {
+        *reinterpret_cast<float4*>(static_cast<float*>(y) + (size_t)row * d + c) = make_float4(o[0], o[1], o[2], o[3]);
+      }
+    }
+  }
+  if (over && status) atomicOr(status, kDevRange);
+}
+
 // [q | k | v] = sum + bias, NeoX rotate_half over the first R = 2 half dims of each q/k head, stored
 // fp32 [M, d] each.  A 4-column group never straddles a head, a segment or the rotary boundary
 // (d, Dh and half are multiples of 4).
@@ -899,6 +1004,28 @@ cudaError_t sgemm_reduce_store_launch(const float* part, int S, int M, int N, co
                              add, lo, status);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
+
+cudaError_t sgemm_reduce_resid_norm_launch(const float* part, int S, int M, int d, const float* bias, float* resid,
+                                           float* resid_lo, int add, int norm, float eps, const float* g,
+                                           const float* b, void* y, int out_kind, int* status, cudaStream_t s) {
+  if (M <= 0) return cudaSuccess;
+  if (!reduce_norm_fusable(d) || (out_kind != 1 && out_kind != 3) || !resid_lo) return cudaErrorInvalidValue;
+  const int blocks = M < num_sms() * 8 ? M : num_sms() * 8;
+  cudaError_t e = cudaErrorInvalidValue;
+  switch (d / 1024) {
+#define DIT_RN(k)                                                                                                   \
+  case k:                                                                                                           \
+    e = launch_pdl(sgemm_reduce_resid_norm_kernel<k>, dim3(blocks), dim3(256), 0, s, part, S, M, d, bias, resid,   \
+                   resid_lo, add, norm, eps, g, b, y, out_kind, status);                                            \
+    break;
+    DIT_RN(1) DIT_RN(2) DIT_RN(3) DIT_RN(4) DIT_RN(5) DIT_RN(6) DIT_RN(7) DIT_RN(8)
+#undef DIT_RN
+    default: break;
+  }
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+bool reduce_norm_fusable(int d) { return d > 0 && d % 1024 == 0 && d <= 8192; }
 
 cudaError_t sgemm_reduce_qkv_launch(const float* part, int S, int M, int d, int Dh, int half, const float* bias,
                                     const float* cs, const float* sn, float* q, float* k, float* v, const int* status,

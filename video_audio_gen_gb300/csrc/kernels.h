@@ -189,6 +189,13 @@ cudaError_t sgemm_reduce_rows_launch(const float* part, int S, int M, int Np, in
                                      cudaStream_t s);
 cudaError_t sgemm_reduce_store_launch(const float* part, int S, int M, int N, const float* bias, float* out, int add,
                                       float* lo, const int* status, cudaStream_t s);
+// The residual-stream reduction fused with the norm that reads the stream next (d % 1024 == 0,
+// d <= 8192): resid (+)= sum of the S partials + bias (compensated with resid_lo; add = 0 stores),
+// then y = norm(resid + resid_lo) * g + b as out_kind 1 (fp32) or 3 (the 3xF16 operand).
+bool reduce_norm_fusable(int d);
+cudaError_t sgemm_reduce_resid_norm_launch(const float* part, int S, int M, int d, const float* bias, float* resid,
+                                           float* resid_lo, int add, int norm, float eps, const float* g,
+                                           const float* b, void* y, int out_kind, int* status, cudaStream_t s);
 cudaError_t sgemm_reduce_qkv_launch(const float* part, int S, int M, int d, int Dh, int half, const float* bias,
                                     const float* cs, const float* sn, float* q, float* k, float* v, const int* status,
                                     cudaStream_t s);
