@@ -37,12 +37,13 @@ KINDS = ["gemm_qkv", "attention", "gemm_out", "gemm_ffn_up", "gemm_ffn_down", "n
 # kernel kind and workload, with the sha256 prefix of the kernel source the capture was taken on; the
 # figure is reported only while that source is unchanged.
 TRAFFIC = {
-    ("attention", "video_audio_bf16"): {"bytes": 410396416, "src_sha": "95e4b2ef60a3ac48"},
-    ("gemm_qkv", "video_audio_bf16"): {"bytes": 821493760, "src_sha": "86f8bc031b1d4c6a"},
-    ("gemm_out", "video_audio_bf16"): {"bytes": 504877312, "src_sha": "86f8bc031b1d4c6a"},
-    ("gemm_ffn_up", "video_audio_bf16"): {"bytes": 832782848, "src_sha": "86f8bc031b1d4c6a"},
-    ("gemm_ffn_down", "video_audio_bf16"): {"bytes": 1241438208, "src_sha": "86f8bc031b1d4c6a"},
-    ("norm_modulate", "video_audio_bf16"): {"bytes": 288634112, "src_sha": "139ad8f729b321b6"},
+    # C2 block kernels, captured on the one-block slice video_audio_bf16_l1 (the same launch shapes)
+    ("attention", "video_audio_bf16"): {"bytes": 409959000, "src_sha": "b30c215725fdbf8d"},
+    ("gemm_qkv", "video_audio_bf16"): {"bytes": 844992648, "src_sha": "9f8187b08155a351"},
+    ("gemm_out", "video_audio_bf16"): {"bytes": 507626576, "src_sha": "9f8187b08155a351"},
+    ("gemm_ffn_up", "video_audio_bf16"): {"bytes": 847073256, "src_sha": "9f8187b08155a351"},
+    ("gemm_ffn_down", "video_audio_bf16"): {"bytes": 1231706880, "src_sha": "9f8187b08155a351"},
+    ("norm_modulate", "video_audio_bf16"): {"bytes": 288434480, "src_sha": "a930da117ae01e0d"},
     ("attention", "long_doc_bf16"): {"bytes": 1366486272, "src_sha": "b30c215725fdbf8d"},
     # fp32 path, captured on the two-block slice music_fp32_l2 (the same launch shapes)
     ("gemm_qkv", "music_fp32"): {"bytes": 52133888, "src_sha": "39e99c7e78d4646a"},
