@@ -27,7 +27,8 @@
 // O += P(j - 2) V(j - 2) is done, so it also says that P buffer j % 2 is free.
 // TMEM: S double buffer (2 x 128 columns) + O_0, O_1 (2 x HD columns) <= 512.  P(j) (16-bit, the
 // type of the PV operands) goes to shared memory buffer j % 2 in the swizzled K-major layout the PV
-// MMA reads.
+// MMA reads; at head_dim 64 it goes to TMEM instead (the two 64-column buffers left after O), and
+// the PV MMA takes it as its TMEM operand.
 #include "common.cuh"
 #include "kernels.h"
 #include "tmap.h"
@@ -157,6 +158,11 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   const uint32_t tmem = *tmem_slot;
   const uint32_t t_s = tmem;            // S buffers at columns 0, 128
   const uint32_t t_o = tmem + 256;      // O_0 at columns [256, 256 + HD), O_1 at [256 + HD, 256 + 2 HD)
+  // At head_dim 64, P(j) goes to TMEM (two 64-column buffers after the O accumulators, 16-bit pairs)
+  // and the P.V MMA reads it from there: the tile's shared-memory traffic (operand reads, P stores,
+  // TMA fills) otherwise bounds it.
+  constexpr bool P_TMEM = HD == 64;
+  const uint32_t t_p = tmem + 256 + 2 * HD;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -263,8 +269,12 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
           // key columns [0, 64) (P atom 0, V^T atom 0) -> O_0; [64, 128) (atom 1) -> O_1
           const uint32_t p_off = (ks >> 2) * ATOM + (ks & 3) * 32;
           const uint32_t v_off = (ks >> 2) * Plan::V_ATOM + (ks & 3) * 32;
-          umma_bf16(t_o + (ks >> 2) * HD, sdesc_sw128(p_addr + p_off), sdesc_sw128(v_addr + v_off), id_o,
-                    (j | (ks & 3)) != 0);
+          if constexpr (P_TMEM)  // 16 keys = 8 columns of 16-bit pairs
+            umma_bf16_ts(t_o + (ks >> 2) * HD, t_p + pb * 64 + ks * 8, sdesc_sw128(v_addr + v_off), id_o,
+                         (j | (ks & 3)) != 0);
+          else
+            umma_bf16(t_o + (ks >> 2) * HD, sdesc_sw128(p_addr + p_off), sdesc_sw128(v_addr + v_off), id_o,
+                      (j | (ks & 3)) != 0);
         }
         umma_commit(&o_done[pb]);
         umma_commit(&v_empty[st]);
@@ -377,11 +387,17 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       }
       l += (rs[0].x + rs[0].y + rs[1].x + rs[1].y) + (rs[2].x + rs[2].y + rs[3].x + rs[3].y);
       // P buffer j % 2 is free: "S(j) ready" included O += P(j - 2) V(j - 2) being done
-      const uint32_t p_row = smem_u32(sP + sb * P_BYTES + half * ATOM) + r * 128;
+      if constexpr (P_TMEM) {
+        // this half's 64 keys are columns [32 half, 32 half + 32) of TMEM P buffer j % 2
+        tmem_st32(t_p + sb * 64 + lane_off + 32 * half, pk);
+        tmem_st_wait();
+      } else {
+        const uint32_t p_row = smem_u32(sP + sb * P_BYTES + half * ATOM) + r * 128;
 #pragma unroll
-      for (int c = 0; c < HC / 8; ++c)
-        st_shared_v4(p_row + ((c ^ (r & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-      fence_proxy_async_smem();
+        for (int c = 0; c < HC / 8; ++c)
+          st_shared_v4(p_row + ((c ^ (r & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        fence_proxy_async_smem();
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[sb]);
