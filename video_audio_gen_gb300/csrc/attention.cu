@@ -10,8 +10,9 @@
 //   warp 0     TMA producer: Q once, then K and V^T tiles through two 2-stage rings
 //   warp 1     TMEM allocator + S issuer: S(j) = Q K(j)^T into TMEM buffer j % 2, issued as soon as
 //              the softmax has loaded S(j - 2) from that buffer
-//   warp 10    PV issuer: O_h += P(j) V(j) once P(j) is in shared memory and V(j) has landed (one
-//              barrier counts both); key columns [0, 64) accumulate into O_0, [64, 128) into O_1.
+//   warps 10, 11  PV issuers, one per O half: O_h += P(j) V(j) once P(j) is in shared memory and
+//              V(j) has landed (one barrier counts both); key columns [0, 64) accumulate into O_0
+//              (warp 10), [64, 128) into O_1 (warp 11).
 //              On a document's boundary tiles the warp first zeroes the V^T columns outside the
 //              document, so that a non-finite value in a neighbouring document cannot reach this
 //              one through 0 * inf (their softmax weights are exactly 0 already)
@@ -20,9 +21,10 @@
 //              two independent passes over disjoint key subsets would; the halves exchange nothing
 //              per tile and are merged once at the end:
 //                  o = (2^(m_0-m) O_0 + 2^(m_1-m) O_1) / (2^(m_0-m) l_0 + 2^(m_1-m) l_1),  m = max(m_0, m_1)
-// Two issuing threads, because one thread's tcgen05.mma issue runs nearly in step with the tensor
-// pipe: whatever else that thread waits on leaves the pipe idle.  With S and PV on separate
-// threads, S(j + 2) runs while the softmax works on tile j, and PV(j) while it works on j + 1.
+// Three issuing threads, because one thread's tcgen05.mma issue is no faster than the tensor pipe
+// (slower for these 128-row, 16-deep instructions): whatever else that thread waits on leaves the
+// pipe idle.  With S and PV on separate threads, S(j + 2) runs while the softmax works on tile j,
+// and PV(j) while it works on j + 1.
 // The softmax waits on one barrier per tile: "S(j) ready" completes only when S(j) is in TMEM and
 // O += P(j - 2) V(j - 2) is done, so it also says that P buffer j % 2 is free.
 // TMEM: S double buffer (2 x 128 columns) + O_0, O_1 (2 x HD columns) <= 512.  P(j) (16-bit, the
@@ -41,9 +43,9 @@ constexpr int TQ = 128, TK = 128;
 constexpr int ATOM = 128 * 64 * 2;         // 128 rows x 64 16-bit columns, 128-byte swizzled (16 KB)
 constexpr int P_BYTES = 2 * ATOM;          // P tile: 128 q rows x 128 kv columns
 constexpr int KV_STAGES = 2;
-constexpr int ATT_THREADS = 352;           // producer, S issuer, 8 softmax warps, PV issuer
+constexpr int ATT_THREADS = 384;           // producer, S issuer, 8 softmax warps, two PV issuers
 constexpr int SOFTMAX_THREADS = 256;
-constexpr int PV_WARP = 10;
+constexpr int PV_WARP = 10;                // PV issuers: warp 10 for O_0, warp 11 for O_1
 static_assert(KV_STAGES == 2, "V(j) lands on the barrier of P buffer j % 2");
 
 // Shared-memory plan for head dim HD (64 or 128):
@@ -74,10 +76,10 @@ __device__ __forceinline__ bool wait_noabort(uint64_t* bar, uint32_t parity) {
 // key index lies outside [lo, hi): one 16-byte chunk (8 keys of one row) per step, by the 32 lanes of
 // one warp.  Chunks wholly inside the document are left alone.
 template <int HD>
-__device__ __forceinline__ void zero_v_outside(uint8_t* sv_tile, int lo, int hi, int lane) {
+__device__ __forceinline__ void zero_v_outside(uint8_t* sv_tile, int lo, int hi, int lane, int atom) {
   const uint32_t base = smem_u32(sv_tile);
-  for (int idx = lane; idx < HD * 16; idx += 32) {
-    const int row = idx >> 4, chunk = idx & 15;  // chunk: keys [8 chunk, 8 chunk + 8)
+  for (int idx = lane; idx < HD * 8; idx += 32) {
+    const int row = idx >> 3, chunk = atom * 8 + (idx & 7);  // chunk: keys [8 chunk, 8 chunk + 8)
     const int k0 = chunk * 8;
     if (k0 >= lo && k0 + 8 <= hi) continue;
     const uint32_t addr = base + (chunk >> 3) * (HD * 128) + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
@@ -138,16 +140,16 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     for (int s = 0; s < KV_STAGES; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
-      mbar_init(&v_empty[s], 1);
+      mbar_init(&v_empty[s], 2);                         // both PV issuers
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&s_full[s], 2);                          // S commit + PV commit of tile j - 2
+      mbar_init(&s_full[s], 3);                          // S commit + both PV commits of tile j - 2
       mbar_init(&s_free[s], SOFTMAX_THREADS / 32);
       mbar_init(&p_full[s], SOFTMAX_THREADS / 32 + 1);   // softmax warps + the V^T load
-      mbar_init(&o_done[s], 1);
+      mbar_init(&o_done[s], 2);
     }
     mbar_init(s_drain, 1);
-    mbar_init(o_drain, 1);
+    mbar_init(o_drain, 2);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -236,8 +238,12 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       umma_commit(s_drain);
       wait_noabort(s_drain, 0);
     }
-  } else if (warp == PV_WARP) {
-    // tiles 0 and 1 have no PV two tiles back: their "S ready" phases get that arrival now
+  } else if (warp == PV_WARP || warp == PV_WARP + 1) {
+    // Two PV issuers, one per O half (key columns [64 hv, 64 hv + 64) -> O_hv): one thread's MMA
+    // issue is slower than the tensor core's work on a 128-row, 16-deep instruction, so two threads
+    // issue side by side.
+    const int hv = warp - PV_WARP;
+    // tiles 0 and 1 have no PV two tiles back: their "S ready" phases get these arrivals now
     if (lane == 0) {
       mbar_arrive(&s_full[0]);
       mbar_arrive(&s_full[1]);
@@ -252,10 +258,10 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       const int hi = de - c0 < TK ? de - c0 : TK;
       if (lo > 0 || hi < TK) {
         // a boundary tile: every lane sees the landed V^T tile through the barrier (its phase cannot
-        // move on before this tile's PV is committed), zeroes its share of the outside columns and
-        // makes the stores visible to the tensor core's operand reads
+        // move on before this tile's PV is committed), zeroes its share of the outside columns of
+        // this issuer's V^T half and makes the stores visible to the tensor core's operand reads
         wait_noabort(&p_full[pb], (j >> 1) & 1);
-        zero_v_outside<HD>(sV + st * Plan::V_BYTES, lo, hi, lane);
+        zero_v_outside<HD>(sV + st * Plan::V_BYTES, lo, hi, lane, hv);
         fence_proxy_async_smem();
       }
       __syncwarp();
@@ -265,20 +271,18 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         const uint32_t p_addr = smem_u32(sP + pb * P_BYTES);
         const uint32_t v_addr = smem_u32(sV + st * Plan::V_BYTES);
 #pragma unroll
-        for (int ks = 0; ks < TK / 16; ++ks) {
-          // key columns [0, 64) (P atom 0, V^T atom 0) -> O_0; [64, 128) (atom 1) -> O_1
-          const uint32_t p_off = (ks >> 2) * ATOM + (ks & 3) * 32;
-          const uint32_t v_off = (ks >> 2) * Plan::V_ATOM + (ks & 3) * 32;
+        for (int kq = 0; kq < 4; ++kq) {
+          const int ks = hv * 4 + kq;  // P atom hv and V^T atom hv
+          const uint32_t p_off = hv * ATOM + kq * 32;
+          const uint32_t v_off = hv * Plan::V_ATOM + kq * 32;
           if constexpr (P_TMEM)  // 16 keys = 8 columns of 16-bit pairs
-            umma_bf16_ts(t_o + (ks >> 2) * HD, t_p + pb * 64 + ks * 8, sdesc_sw128(v_addr + v_off), id_o,
-                         (j | (ks & 3)) != 0);
+            umma_bf16_ts(t_o + hv * HD, t_p + pb * 64 + ks * 8, sdesc_sw128(v_addr + v_off), id_o, (j | kq) != 0);
           else
-            umma_bf16(t_o + (ks >> 2) * HD, sdesc_sw128(p_addr + p_off), sdesc_sw128(v_addr + v_off), id_o,
-                      (j | (ks & 3)) != 0);
+            umma_bf16(t_o + hv * HD, sdesc_sw128(p_addr + p_off), sdesc_sw128(v_addr + v_off), id_o, (j | kq) != 0);
         }
         umma_commit(&o_done[pb]);
         umma_commit(&v_empty[st]);
-        umma_commit(&s_full[pb]);                          // the second arrival of "S(j + 2) ready"
+        umma_commit(&s_full[pb]);                          // an arrival of "S(j + 2) ready"
       }
       __syncwarp();
     }
