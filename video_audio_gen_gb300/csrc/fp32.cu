@@ -645,34 +645,30 @@ __global__ void __launch_bounds__(T3_THREADS, 1)
         const int cb = c % n_acc;
         const int i0 = c * T3_CHUNK, i1 = min(n_kb, i0 + T3_CHUNK);
         if (!mbar_wait(&chunk_empty[cb], ((c / n_acc) & 1) ^ 1, abort_flag, a.status)) break;
-        for (int i = i0; i < i1 && ok; ++i) ok = mbar_wait(&full[i % T3_STAGES], (i / T3_STAGES) & 1, abort_flag, a.status);
-        if (!ok) break;
-        tc_fence_after();
         const uint32_t acc = tmem + cb * acc_cols;
-        // The small cross terms of every stage of the chunk go first, while the accumulator is still
-        // about 2^-11 of its final size (their rounding is then negligible); the hi x hi products last.
-        bool first = true;
-        for (int i = i0; i < i1; ++i) {
+        // Stage by stage: its small cross terms, then its hi x hi products, then the stage goes back
+        // to the producer as soon as its MMAs complete (a chunk never holds more than the stage it is
+        // working on).
+        for (int i = i0; i < i1 && ok; ++i) {
+          ok = mbar_wait(&full[i % T3_STAGES], (i / T3_STAGES) & 1, abort_flag, a.status);
+          if (!ok) break;
+          tc_fence_after();
           const uint32_t whi = smem_u32(smem + (i % T3_STAGES) * stage_bytes);
           const uint32_t xhi = whi + 2 * T3_W_BYTES;
 #pragma unroll
           for (int ks = 0; ks < G::KSTEPS; ++ks) {
             const uint32_t off = ks * 32;
-            mma(acc, whi + off, xhi + x_bytes + off, first ? 0u : 1u);
+            mma(acc, whi + off, xhi + x_bytes + off, (i == i0 && ks == 0) ? 0u : 1u);
             mma(acc, whi + T3_W_BYTES + off, xhi + off, 1);
-            first = false;
           }
-        }
-        for (int i = i0; i < i1; ++i) {
-          const uint32_t whi = smem_u32(smem + (i % T3_STAGES) * stage_bytes);
-          const uint32_t xhi = whi + 2 * T3_W_BYTES;
 #pragma unroll
           for (int ks = 0; ks < G::KSTEPS; ++ks) {
             const uint32_t off = ks * 32;
             mma(acc, whi + off, xhi + off, 1);
           }
+          umma_commit(&empty[i % T3_STAGES]);
         }
-        for (int i = i0; i < i1; ++i) umma_commit(&empty[i % T3_STAGES]);
+        if (!ok) break;
         umma_commit(&chunk_full[cb]);
       }
     }
