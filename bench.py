@@ -819,6 +819,14 @@ def main():
                          "ms_per_step": round(r["e2e_ms"], 3), "h2d_bytes_per_step": int(r["h2d"]),
                          "d2h_bytes_per_step": int(r["d2h"])}),
                 "gpu_launches": int(r["launches"]), "clocks": r["clocks"]}
+        if m_dtype == "f32":
+            # the fp32 path's own reference point: the FP32 FFMA rate of the device (the forward runs
+            # its contractions as three f16 tensor-core products per fp32 product instead)
+            import torch
+            ffma = fp32_alu_peak_tflops(peaks, torch.cuda.get_device_properties(torch.cuda.current_device())
+                                        .multi_processor_count)
+            line["config"]["step_frac_of_fp32_ffma_peak"] = round(tflops / ffma, 3)
+            line["config"]["fp32_ffma_peak_tflops"] = round(ffma, 1)
         if not args.no_cpu_baseline:
             lay_cpu = r["lay"]
             if w["model"].get("vit_positions"):  # the oracle's own positions
