@@ -10,8 +10,10 @@
 //   tile 128 x 256, K step 64, 4-stage TMA -> shared-memory ring (128-byte swizzle)
 //   warp 0   TMA producer (one elected lane)
 //   warp 1   TMEM allocator + UMMA issuer (one lane): tcgen05.mma M=128 N=256 K=16
-//   warps 2-5 epilogue: each warp reads its 32 TMEM lanes (= 32 tile rows) with tcgen05.ld,
-//            one thread per output row
+//   warps 2-9 epilogue: each warp reads its 32 TMEM lanes (= 32 tile rows) with tcgen05.ld,
+//            one thread per output row; warps 2-5 take the tile's columns [0, 128) and warps 6-9
+//            [128, 256), so two warps share each lane quarter (a warp may only read the quarter
+//            warp % 4) and a tile's epilogue runs in half the time of one warp per quarter
 //   the 512 TMEM columns hold two 128x256 fp32 accumulators, so the epilogue of tile i overlaps
 //   the main loop of tile i+1.
 //
@@ -40,7 +42,8 @@ constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;   // 16 KB
 constexpr int B_BYTES = BN * BK * 2;   // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int GEMM_THREADS = 192;
+constexpr int EPI_WARPS = 8;  // two per TMEM lane quarter, each on half of the tile's columns
+constexpr int GEMM_THREADS = 64 + 32 * EPI_WARPS;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 constexpr int SMEM_BYTES_RESID = SMEM_BYTES + BM * 64 * 4;  // + the residual epilogue's staging tile
 constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
@@ -50,7 +53,9 @@ constexpr int Q_RAW_SLOTS = 2;                   // packed weight tiles in fligh
 constexpr int Q_RAW_BYTES = kNvfp4TileBytes;     // 256 rows x 32 bytes of codes, then 256 x 4 scales
 constexpr int Q_CODE_BYTES = BN * BK / 2;
 constexpr int Q_CONV_WARPS = 8;                  // one weight row per converter thread
-constexpr int Q_THREADS = GEMM_THREADS + 32 * Q_CONV_WARPS;
+constexpr int Q_EPI_WARPS = 4;                   // one per lane quarter, all 256 columns
+constexpr int Q_BASE_THREADS = 64 + 32 * Q_EPI_WARPS;
+constexpr int Q_THREADS = Q_BASE_THREADS + 32 * Q_CONV_WARPS;
 constexpr int Q_SMEM_BYTES = Q_STAGES * STAGE_BYTES + Q_RAW_SLOTS * Q_RAW_BYTES + 1024 + 256;
 constexpr int Q_SMEM_BYTES_RESID = Q_STAGES_RESID * STAGE_BYTES + Q_RAW_SLOTS * Q_RAW_BYTES + 1024 + 256 + BM * 64 * 4;
 constexpr uint32_t IDESC_F16 = idesc_f16_f32(BM, BN);
@@ -91,12 +96,15 @@ __device__ __forceinline__ void load_bias4(const float* b, int col, float (&o)[4
 
 // ---------------------------------------------------------------------------------------------
 // epilogues: the calling thread owns tile row `row` (global), TMEM address `t` = its lane, the
-// accumulator's column 0.  n0 = first global output column of the tile.
+// accumulator's column 0.  n0 = first global output column of the tile.  The tile's columns are
+// split into NG groups (NG warps per lane quarter); the caller's warp handles group `grp`.
 // ---------------------------------------------------------------------------------------------
-__device__ __forceinline__ void epi_store(const GemmArgs& a, uint32_t t, int row, int n0) {
+template <int NG>
+__device__ __forceinline__ void epi_store(const GemmArgs& a, uint32_t t, int row, int n0, int grp) {
   const bool live = row < a.M;
+  constexpr int GC = BN / NG;
 #pragma unroll 1
-  for (int c = 0; c < BN; c += 32) {
+  for (int c = grp * GC; c < (grp + 1) * GC; c += 32) {
     uint32_t r[32];
     tmem_ld32_sync(t + c, r);
     if (!live) continue;
@@ -196,10 +204,13 @@ __device__ __forceinline__ void rope_chunk(const GemmArgs& a, uint32_t t, int hb
 // with a = acc + bias and cos/sin the row's cache entries.  With qk_norm, a is first divided by the
 // head's RMS, sqrt(mean(a^2) + eps) ([H3] "Update: video-VAE decoder block ported": per-head RMS
 // q/k norm without affine).
-__device__ __forceinline__ void epi_qkv(const GemmArgs& a, uint32_t t, int row, int n0) {
+// A head is never split between column groups: with Dh wider than a group, group 0 takes them all.
+template <int NG>
+__device__ __forceinline__ void epi_qkv(const GemmArgs& a, uint32_t t, int row, int n0, int grp) {
   const bool live = row < a.M;
   const int seg = n0 / a.d;
   const int col0 = n0 - seg * a.d;
+  constexpr int GC = BN / NG;
   if (seg == 2) {
     // v is stored transposed; its padding columns [M, n_pad) are written as zeros so that the
     // attention's masked key/value tiles never multiply uninitialised memory (0 * NaN = NaN).
@@ -207,7 +218,7 @@ __device__ __forceinline__ void epi_qkv(const GemmArgs& a, uint32_t t, int row, 
     const bool pad = !live && row < a.n_pad;
     const bool f = a.f16;
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
+    for (int c = grp * GC; c < (grp + 1) * GC; c += 32) {
       uint32_t r[32];
       tmem_ld32_sync(t + c, r);
       if (!live && !pad) continue;
@@ -227,8 +238,10 @@ __device__ __forceinline__ void epi_qkv(const GemmArgs& a, uint32_t t, int row, 
   const int Dh = a.head_dim, half = a.rot_half;
   const float* cs = a.cos_cache + (size_t)row * half;
   const float* sn = a.sin_cache + (size_t)row * half;
+  const int h_lo = Dh <= GC ? grp * GC : (grp == 0 ? 0 : BN);
+  const int h_hi = Dh <= GC ? h_lo + GC : BN;
 #pragma unroll 1
-  for (int hb = 0; hb < BN; hb += Dh) {
+  for (int hb = h_lo; hb < h_hi; hb += Dh) {
     // qk_norm: x / sqrt(mean over the head of x^2 + eps), x = acc + bias, before the rotation
     float rn = 1.f;
     if (a.qk_norm) {
@@ -284,57 +297,68 @@ __device__ __forceinline__ void epi_qkv(const GemmArgs& a, uint32_t t, int row, 
 //
 // The residual stream is fp32 in HBM, so this epilogue is a read-modify-write of a 128 x 256 fp32
 // tile.  TMEM hands each thread one row, which would make every global access a 32-row scatter;
-// instead the tile goes through shared memory 64 columns at a time:
-//   phase A  each thread moves its row's 64 accumulator columns TMEM -> registers -> shared memory
+// instead each column group's part of the tile goes through shared memory RC = 64 / NG columns at
+// a time (the staging area is 128 x 64 floats whichever NG):
+//   phase A  each thread moves its row's RC accumulator columns TMEM -> registers -> shared memory
 //            (16-byte chunks XOR-swizzled by row so a warp's stores spread over all banks)
-//   phase B  each warp walks 32 rows; per row its 32 lanes own 2 adjacent columns, so the loads and
-//            stores of x (and of the gate and bias) are 256 contiguous bytes per row.
-constexpr int RES_COLS = 64;
+//   phase B  each warp walks 32 rows; RC / 2 lanes share a row, two adjacent columns each, so the
+//            loads and stores of x (and of the gate and bias) are RC * 4 contiguous bytes per row.
+// The NG groups run on their own named barriers (ids 1 .. NG), so they overlap one another.
+constexpr int RES_STAGE_FLOATS = BM * 64;
 constexpr int RES_BATCH = 32;  // rows whose loads a warp has in flight at once (4 in the NVFP4 mode,
                                // whose 448-thread launch leaves fewer registers per thread)
 
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void epi_bar(int grp) { asm volatile("bar.sync %0, 128;" ::"r"(1 + grp) : "memory"); }
 
-template <int RB = RES_BATCH>
-__device__ __forceinline__ void epi_resid(const GemmArgs& a, uint32_t t, int tile_row0, int quarter, int ew, int n0,
-                                          float* stage, uint64_t* tempty_bar) {
+template <int RB, int NG>
+__device__ __forceinline__ void epi_resid(const GemmArgs& a, uint32_t t, int tile_row0, int quarter, int ew, int grp,
+                                          int n0, float* stage_all, uint64_t* tempty_bar) {
+  constexpr int RC = 64 / NG;          // columns per pass
+  constexpr int GC = BN / NG;          // columns of this group
+  constexpr int LPR = RC / 2;          // lanes per row in phase B
+  constexpr int RPI = 32 / LPR;        // rows per warp-wide access
+  static_assert(RB % RPI == 0 && 32 % RB == 0, "row batch");
   const int lane = threadIdx.x & 31;
+  float* stage = stage_all + grp * (RES_STAGE_FLOATS / NG);
   const int r_own = quarter * 32 + lane;  // the tile row whose TMEM lane this thread reads
-  const uint32_t st_row = smem_u32(stage) + r_own * (RES_COLS * 4);
+  const uint32_t st_row = smem_u32(stage) + r_own * (RC * 4);
+  const int sub = lane / LPR, lc = lane % LPR;
+  const int chunk = lc >> 1, half8 = (lc & 1) * 8;
 #pragma unroll 1
-  for (int c0 = 0; c0 < BN; c0 += RES_COLS) {
+  for (int c0 = grp * GC; c0 < (grp + 1) * GC; c0 += RC) {
     // phase A: TMEM -> shared memory (swizzled)
 #pragma unroll
-    for (int h = 0; h < RES_COLS; h += 32) {
+    for (int h = 0; h < RC; h += 32) {
       uint32_t r[32];
       tmem_ld32_sync(t + c0 + h, r);
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        const int chunk = (h >> 2) + q;  // 16-byte chunk index within the 256-byte row
-        st_shared_v4(st_row + ((chunk ^ (r_own & 7)) << 4), r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
+        const int ch = (h >> 2) + q;  // 16-byte chunk index within the row
+        st_shared_v4(st_row + ((ch ^ (r_own & 7)) << 4), r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
       }
     }
-    if (c0 + RES_COLS == BN) {
-      // every accumulator column of this tile is out of TMEM: hand the buffer back to the MMA warp
+    if (c0 + RC == (grp + 1) * GC) {
+      // every accumulator column of this group is out of TMEM: this warp's part of the buffer is
+      // handed back to the MMA warp
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar);
     }
-    epi_bar();
-    // phase B: coalesced read-modify-write of 32 rows x 64 columns per warp
-    const int col = n0 + c0 + 2 * lane;
+    epi_bar(grp);
+    // phase B: coalesced read-modify-write of 32 rows x RC columns per warp
+    const int col = n0 + c0 + 2 * lc;
     float2 bb = make_float2(0.f, 0.f);
     if (a.bias) bb = *reinterpret_cast<const float2*>(a.bias + col);
-    const int chunk = lane >> 1, half8 = (lane & 1) * 8;
 #pragma unroll 1
     for (int rr0 = 0; rr0 < 32; rr0 += RB) {
-      float2 acc[RB], xv[RB], gv[RB];
-      int rows[RB];
+      constexpr int U = RB / RPI;
+      float2 acc[U], xv[U], gv[U];
+      int rows[U];
 #pragma unroll
-      for (int u = 0; u < RB; ++u) {
-        const int rt = ew * 32 + rr0 + u;
+      for (int u = 0; u < U; ++u) {
+        const int rt = ew * 32 + rr0 + u * RPI + sub;
         rows[u] = tile_row0 + rt;
-        const uint32_t sa = smem_u32(stage) + rt * (RES_COLS * 4) + ((chunk ^ (rt & 7)) << 4) + half8;
+        const uint32_t sa = smem_u32(stage) + rt * (RC * 4) + ((chunk ^ (rt & 7)) << 4) + half8;
         asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(acc[u].x), "=f"(acc[u].y) : "r"(sa));
         if (rows[u] < a.M) {
           xv[u] = *reinterpret_cast<const float2*>(a.x + (size_t)rows[u] * a.N + col);
@@ -343,7 +367,7 @@ __device__ __forceinline__ void epi_resid(const GemmArgs& a, uint32_t t, int til
         }
       }
 #pragma unroll
-      for (int u = 0; u < RB; ++u) {
+      for (int u = 0; u < U; ++u) {
         if (rows[u] < a.M) {
           float2 o;
           o.x = xv[u].x + gv[u].x * (acc[u].x * a.w_scale + bb.x);
@@ -352,21 +376,23 @@ __device__ __forceinline__ void epi_resid(const GemmArgs& a, uint32_t t, int til
         }
       }
     }
-    epi_bar();  // the staging buffer is reused by the next column block
+    epi_bar(grp);  // the staging buffer is reused by the next column block
   }
 }
 
 // Tile columns [0, 128) hold value features f0 .. f0+127 and [128, 256) their gates
 // (the interleaved packing of the FFN up projection); h[row, f0 + j] = u_j * silu(g_j).
-__device__ __forceinline__ void epi_swiglu(const GemmArgs& a, uint32_t t, int row, int n0) {
+template <int NG>
+__device__ __forceinline__ void epi_swiglu(const GemmArgs& a, uint32_t t, int row, int n0, int grp) {
   const bool live = row < a.M;
   const int F = a.N / 2;
   const int f0 = n0 / 2;
   __nv_bfloat16* hrow = static_cast<__nv_bfloat16*>(a.out) + (size_t)row * F + f0;
   __half* hrow16 = static_cast<__half*>(a.out) + (size_t)row * F + f0;  // out_kind 2
   bool over = false;  // an f16 value beyond the finite range
+  constexpr int GF = BN / 2 / NG;  // value/gate pairs per group
 #pragma unroll 1
-  for (int c = 0; c < BN / 2; c += 16) {
+  for (int c = grp * GF; c < (grp + 1) * GF; c += 16) {
     uint32_t ru[16], rg[16];
     tmem_ld16(t + c, ru);
     tmem_ld16(t + BN / 2 + c, rg);
@@ -479,7 +505,7 @@ __global__ void __launch_bounds__(BQ ? Q_THREADS : GEMM_THREADS, 1)
       }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&tfull[s], 1);
-      mbar_init(&tempty[s], 4);
+      mbar_init(&tempty[s], BQ ? Q_EPI_WARPS : EPI_WARPS);
     }
     *abort_flag = 0;
     mbar_fence_init();
@@ -577,7 +603,7 @@ __global__ void __launch_bounds__(BQ ? Q_THREADS : GEMM_THREADS, 1)
     // converters: one pass over the same (tile, k-block) sequence as the producer
     // The stage's B tile is free: the packed tile of this fill was copied only after the MMA's
     // commit for the previous fill of the stage (the producer waits on empty[stage] first).
-    const int ct = threadIdx.x - GEMM_THREADS;
+    const int ct = threadIdx.x - Q_BASE_THREADS;
     int stage = 0, rslot = 0;
     uint32_t phase = 0, rphase = 0;
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
@@ -603,6 +629,8 @@ __global__ void __launch_bounds__(BQ ? Q_THREADS : GEMM_THREADS, 1)
   convert_done:;
   } else {
     const int quarter = warp & 3;  // TMEM lanes [32 * quarter, +32) belong to this warp
+    constexpr int NG = (BQ ? Q_EPI_WARPS : EPI_WARPS) / 4;
+    const int grp = (warp - 2) >> 2, ew = (warp - 2) & 3;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
@@ -613,11 +641,11 @@ __global__ void __launch_bounds__(BQ ? Q_THREADS : GEMM_THREADS, 1)
       const uint32_t t = tmem + acc * BN + (static_cast<uint32_t>(quarter * 32) << 16);
       const int n0 = tc.nb * BN;
       if (EPI == kEpiGatedResid) {
-        epi_resid<BQ ? 4 : RES_BATCH>(args, t, tc.mb * BM, quarter, warp - 2, n0, res_stage, &tempty[acc]);
+        epi_resid<BQ ? 4 : RES_BATCH, NG>(args, t, tc.mb * BM, quarter, ew, grp, n0, res_stage, &tempty[acc]);
       } else {
-        if (EPI == kEpiStore) epi_store(args, t, row, n0);
-        if (EPI == kEpiQkvRope) epi_qkv(args, t, row, n0);
-        if (EPI == kEpiSwiglu) epi_swiglu(args, t, row, n0);
+        if (EPI == kEpiStore) epi_store<NG>(args, t, row, n0, grp);
+        if (EPI == kEpiQkvRope) epi_qkv<NG>(args, t, row, n0, grp);
+        if (EPI == kEpiSwiglu) epi_swiglu<NG>(args, t, row, n0, grp);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[acc]);
