@@ -106,7 +106,7 @@ def test_forward_counters_and_tiles():
     L = w["model"]["n_blocks"]
     assert st["forwards"] == 1
     assert st["gemm_launches"] == 4 * L and st["attention_launches"] == L and st["norm_launches"] == 2 * L + 1
-    assert st["attention_tiles"] == oracle.count_q_tiles(run["layout"]["cu_seqlens"], 128) * w["model"]["n_heads"]
+    assert st["attention_tiles"] == oracle.count_q_tiles(run["layout"]["cu_seqlens"], _dit().attention_block_rows()) * w["model"]["n_heads"]
     assert st["device_status"] == 0 and st["last_layout_error"] == 0
 
 

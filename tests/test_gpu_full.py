@@ -199,5 +199,5 @@ def test_full_forward_is_deterministic_and_counts_tiles():
     r1 = gu.run_forward(w)
     r2 = gu.run_forward(w, layout=r1["layout"], weights=r1["weights"], x=r1["x"], handle=r1["handle"])
     assert np.array_equal(r1["out"], r2["out"])
-    assert r2["stats"]["attention_tiles"] == oracle.count_q_tiles(r1["layout"]["cu_seqlens"], 128) * w["model"]["n_heads"]
+    assert r2["stats"]["attention_tiles"] == oracle.count_q_tiles(r1["layout"]["cu_seqlens"], _dit().attention_block_rows()) * w["model"]["n_heads"]
     r1["handle"].close()

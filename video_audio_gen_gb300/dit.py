@@ -33,6 +33,7 @@ EXPORTS = ["dit_create", "dit_destroy", "dit_last_error", "dit_workspace_bytes",
            "dit_op_rope_cache", "dit_op_adaln", "dit_op_gemm", "dit_op_gemm_qkv_rope", "dit_op_gemm_gated_residual",
            "dit_op_gemm_swiglu", "dit_nvfp4_packed_bytes", "dit_op_pack_nvfp4", "dit_op_gemm_nvfp4",
            "dit_gemm_f32_workspace_bytes", "dit_op_gemm_f32", "dit_op_pack_ffn_in", "dit_attention_workspace_bytes", "dit_op_attention",
+           "dit_attention_block_rows",
            "dit_op_attention_noalloc", "dit_op_attention_noalloc_status", "dit_selftest_wait_timeout"]
 
 
@@ -147,6 +148,7 @@ def lib():
             "dit_op_gemm_swiglu": (i32, [vp, vp, vp, i32, i32, i32, vp, i32, vp]),
             "dit_op_pack_ffn_in": (i32, [vp, vp, i32, i32, vp, vp, vp]),
             "dit_attention_workspace_bytes": (sz, [i32, i32]),
+            "dit_attention_block_rows": (i32, []),
             "dit_gemm_f32_workspace_bytes": (sz, [i32, i32, i32]),
             "dit_nvfp4_packed_bytes": (sz, [i32, i32]),
             "dit_op_pack_nvfp4": (i32, [vp, vp, i32, i32, vp, vp]),
@@ -482,6 +484,10 @@ def pack_ffn_in(w_in, b_in, w_packed, b_packed, stream=None):
 
 def attention_workspace_bytes(n_docs: int, n_tokens: int) -> int:
     return int(lib().dit_attention_workspace_bytes(n_docs, n_tokens))
+
+
+def attention_block_rows() -> int:
+    return int(lib().dit_attention_block_rows())
 
 
 def attention(q, k, vt, n_pad, cu_seqlens, n_heads, head_dim, o, workspace, stream=None):
