@@ -8,11 +8,11 @@
 // at multiples of 128 in the packed sequence (so the TMA x coordinate of the transposed V is
 // 16-byte aligned); columns outside the document are masked to -inf in S and zeroed in V^T.
 //   warp 0     TMA producer: Q once, then K and V^T tiles through two 2-stage rings
-//   warp 1     TMEM allocator + S issuer: S(j) = Q K(j)^T into TMEM buffer j % 2, issued as soon as
-//              the softmax has loaded S(j - 2) from that buffer
-//   warps 10, 11  PV issuers, one per O half: O_h += P(j) V(j) once P(j) is in shared memory and
-//              V(j) has landed (one barrier counts both); key columns [0, 64) accumulate into O_0
-//              (warp 10), [64, 128) into O_1 (warp 11).
+//   warp 1     TMEM allocator + S issuer: S(j) = Q K(j)^T into S buffer j % S_BUFS, issued as soon
+//              as K(j) has landed and the softmax has read that buffer's previous scores
+//   warps 10, 11  PV issuers, one per O half: O_h += P(j) V(j) once P(j) is in TMEM and V(j) has
+//              landed (one barrier counts both); key columns [0, 64) accumulate into O_0 (warp 10),
+//              [64, 128) into O_1 (warp 11).
 //              On a document's boundary tiles the warp first zeroes the V^T columns outside the
 //              document, so that a non-finite value in a neighbouring document cannot reach this
 //              one through 0 * inf (their softmax weights are exactly 0 already)
@@ -21,16 +21,13 @@
 //              two independent passes over disjoint key subsets would; the halves exchange nothing
 //              per tile and are merged once at the end:
 //                  o = (2^(m_0-m) O_0 + 2^(m_1-m) O_1) / (2^(m_0-m) l_0 + 2^(m_1-m) l_1),  m = max(m_0, m_1)
-// Three issuing threads, because one thread's tcgen05.mma issue is no faster than the tensor pipe
-// (slower for these 128-row, 16-deep instructions): whatever else that thread waits on leaves the
-// pipe idle.  With S and PV on separate threads, S(j + 2) runs while the softmax works on tile j,
-// and PV(j) while it works on j + 1.
-// The softmax waits on one barrier per tile: "S(j) ready" completes only when S(j) is in TMEM and
-// O += P(j - 2) V(j - 2) is done, so it also says that P buffer j % 2 is free.
-// TMEM: S double buffer (2 x 128 columns) + O_0, O_1 (2 x HD columns) <= 512.  P(j) (16-bit, the
-// type of the PV operands) goes to shared memory buffer j % 2 in the swizzled K-major layout the PV
-// MMA reads; at head_dim 64 it goes to TMEM instead (the two 64-column buffers left after O), and
-// the PV MMA takes it as its TMEM operand.
+// Three issuing warps, each running converged and issuing through elect.sync: with S and PV on
+// separate threads, S(j + 1) runs while the softmax works on tile j, and PV(j) while it works on
+// j + 1.
+// TMEM: S_BUFS S buffers of 128 columns (two at head_dim 64, one at 128), O_0 and O_1 (Dh columns
+// each), and two P buffers of 64 columns: P(j) (16-bit pairs, the type of the PV operands) goes to
+// buffer j % 2 and the PV MMA reads it as its TMEM operand.  A P buffer is rewritten only after the
+// PV of two tiles back is complete.
 #include "common.cuh"
 #include "kernels.h"
 #include "tmap.h"
@@ -41,7 +38,6 @@ namespace {
 
 constexpr int TQ = 128, TK = 128;
 constexpr int ATOM = 128 * 64 * 2;         // 128 rows x 64 16-bit columns, 128-byte swizzled (16 KB)
-constexpr int P_BYTES = 2 * ATOM;          // P tile: 128 q rows x 128 kv columns
 constexpr int KV_STAGES = 2;
 constexpr int ATT_THREADS = 384;           // producer, S issuer, 8 softmax warps, two PV issuers
 constexpr int SOFTMAX_THREADS = 256;
@@ -51,16 +47,19 @@ static_assert(KV_STAGES == 2, "V(j) lands on the barrier of P buffer j % 2");
 // Shared-memory plan for head dim HD (64 or 128):
 //   Q  [128 q, HD]   HD/64 atoms of 16 KB          K  [128 kv, HD]  HD/64 atoms of 16 KB
 //   Vt [HD, 128 kv]  2 atoms (kv halves) of HD * 128 bytes each
-//   P  [128 q, 128 kv] x 2 buffers
 template <int HD>
 struct AttPlan {
   static constexpr int Q_BYTES = 128 * HD * 2;
   static constexpr int K_BYTES = 128 * HD * 2;
   static constexpr int V_ATOM = HD * 128;
   static constexpr int V_BYTES = 2 * V_ATOM;
-  static constexpr int SMEM = Q_BYTES + KV_STAGES * (K_BYTES + V_BYTES) + 2 * P_BYTES + 1024 + 256;
+  static constexpr int SMEM = Q_BYTES + KV_STAGES * (K_BYTES + V_BYTES) + 1024 + 256;
   static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, TK);
   static constexpr uint32_t IDESC_O = idesc_bf16_f32(128, HD);
+  // S buffers in TMEM: two where they fit beside O_0, O_1 and the two P buffers (head_dim 64), else
+  // one (S(j + 1) then waits for the softmax to have read S(j), and runs under its exponentials)
+  static constexpr int S_BUFS = HD == 64 ? 2 : 1;
+  static_assert(S_BUFS * TK + 2 * HD + 2 * 64 <= 512, "TMEM plan");
 };
 
 __device__ __forceinline__ bool wait_noabort(uint64_t* bar, uint32_t parity) {
@@ -141,15 +140,15 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   uint8_t* sQ = smem;
   uint8_t* sK = sQ + Plan::Q_BYTES;                    // [stage]
   uint8_t* sV = sK + KV_STAGES * Plan::K_BYTES;        // [stage]
-  uint8_t* sP = sV + KV_STAGES * Plan::V_BYTES;        // [2]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * P_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + KV_STAGES * Plan::V_BYTES);
   uint64_t* q_full = bars;
   uint64_t* k_full = bars + 1;                         // [stage]  K tile landed
   uint64_t* k_empty = k_full + KV_STAGES;              // [stage]  S MMA done with the K tile
   uint64_t* v_empty = k_empty + KV_STAGES;             // [stage]  PV MMA done with the V^T tile
-  uint64_t* s_full = v_empty + KV_STAGES;              // [2]  S(j) in TMEM and P(j - 2) V(j - 2) done
-  uint64_t* s_free = s_full + 2;                       // [2]  softmax has loaded S(j) from its buffer
-  uint64_t* p_full = s_free + 2;                       // [2]  P(j) in shared memory and V(j) landed
+  uint64_t* s_full = v_empty + KV_STAGES;              // [S_BUFS] S(j) in TMEM buffer j % S_BUFS (two
+                                                       //   buffers: and P(j - 2) V(j - 2) done)
+  uint64_t* s_free = s_full + Plan::S_BUFS;            // [S_BUFS] the softmax has loaded S(j)
+  uint64_t* p_full = s_free + Plan::S_BUFS;            // [2]  P(j) in TMEM buffer j % 2 and V(j) landed
   uint64_t* o_done = p_full + 2;                       // [2]  O += P(j) V(j) complete
   uint64_t* s_drain = o_done + 2;                      // every S MMA complete
   uint64_t* o_drain = s_drain + 1;                     // every PV MMA complete
@@ -164,11 +163,13 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       mbar_init(&k_empty[s], 1);
       mbar_init(&v_empty[s], 2);                         // both PV issuers
     }
+    for (int b = 0; b < Plan::S_BUFS; ++b) {
+      mbar_init(&s_full[b], Plan::S_BUFS == 2 ? 3 : 1);  // two buffers: + both PV commits of tile j - 2
+      mbar_init(&s_free[b], SOFTMAX_THREADS / 32);
+    }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&s_full[s], 3);                          // S commit + both PV commits of tile j - 2
-      mbar_init(&s_free[s], SOFTMAX_THREADS / 32);
       mbar_init(&p_full[s], SOFTMAX_THREADS / 32 + 1);   // softmax warps + the V^T load
-      mbar_init(&o_done[s], 2);
+      mbar_init(&o_done[s], 2);                          // both PV issuers
     }
     mbar_init(s_drain, 1);
     mbar_init(o_drain, 2);
@@ -180,13 +181,12 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t t_s = tmem;            // S buffers at columns 0, 128
-  const uint32_t t_o = tmem + 256;      // O_0 at columns [256, 256 + HD), O_1 at [256 + HD, 256 + 2 HD)
-  // At head_dim 64, P(j) goes to TMEM (two 64-column buffers after the O accumulators, 16-bit pairs)
-  // and the P.V MMA reads it from there: the tile's shared-memory traffic (operand reads, P stores,
-  // TMA fills) otherwise bounds it.
-  constexpr bool P_TMEM = HD == 64;
-  const uint32_t t_p = tmem + 256 + 2 * HD;
+  // TMEM: S_BUFS S buffers of 128 columns, O_0 and O_1 (HD each), then P buffers 0 and 1 of 64
+  // columns each (16-bit pairs), which the P.V MMA reads as its TMEM operand.
+  constexpr int SB = Plan::S_BUFS;
+  const uint32_t t_s = tmem;
+  const uint32_t t_o = tmem + SB * TK;
+  const uint32_t t_p = t_o + 2 * HD;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -236,15 +236,15 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         wait_noabort(&p_full[j % KV_STAGES], (j / KV_STAGES) & 1);
     }
   } else if (warp == 1) {
-    // S(j) into buffer j % 2 once K(j) has landed and the softmax has loaded S(j - 2) from it.  The
+    // S(j) into buffer j % SB once K(j) has landed and the softmax has read S(j - SB) from it.  The
     // warp runs converged and elect.sync picks the issuing lane.
     bool ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0, abort_flag, args.status));
     tc_fence_after();
     const uint64_t q_desc = sdesc_sw128(smem_u32(sQ));
     constexpr uint32_t id_s = F16 ? idesc_f16_f32(128, TK) : Plan::IDESC_S;
     for (int j = 0; ok && j < n_kv; ++j) {
-      const int st = j % KV_STAGES, sb = j & 1;
-      if (j >= 2) ok = __all_sync(0xffffffffu, mbar_wait(&s_free[sb], ((j - 2) >> 1) & 1, abort_flag, args.status));
+      const int st = j % KV_STAGES, sb = j % SB;
+      if (j >= SB) ok = __all_sync(0xffffffffu, mbar_wait(&s_free[sb], (j / SB - 1) & 1, abort_flag, args.status));
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&k_full[st], (j / KV_STAGES) & 1, abort_flag, args.status));
       if (!ok) break;
       tc_fence_after();
@@ -261,12 +261,12 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     umma_commit_elect(s_drain);
     wait_noabort(s_drain, 0);
   } else if (warp == PV_WARP || warp == PV_WARP + 1) {
-    // Two PV issuers, one per O half (key columns [64 hv, 64 hv + 64) -> O_hv): one thread's MMA
-    // issue is slower than the tensor core's work on a 128-row, 16-deep instruction, so two threads
-    // issue side by side.
+    // Two PV issuers, one per O half (key columns [64 hv, 64 hv + 64) -> O_hv), issuing side by
+    // side.
     const int hv = warp - PV_WARP;
-    // tiles 0 and 1 have no PV two tiles back: their "S ready" phases get these arrivals now
-    if (lane == 0) {
+    // With two S buffers, "S(j) ready" also counts both PV commits of tile j - 2 (so one wait tells
+    // the softmax that P buffer j % 2 is free); tiles 0 and 1 get those arrivals now.
+    if (SB == 2 && lane == 0) {
       mbar_arrive(&s_full[0]);
       mbar_arrive(&s_full[1]);
     }
@@ -289,21 +289,16 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       {
         // the whole warp computes the descriptors; elect.sync picks the issuing lane
         constexpr uint32_t id_o = F16 ? idesc_f16_f32(128, HD) : Plan::IDESC_O;
-        const uint64_t p_desc = sdesc_sw128(smem_u32(sP + pb * P_BYTES));
         const uint64_t v_desc = sdesc_sw128(smem_u32(sV + st * Plan::V_BYTES));
 #pragma unroll
         for (int kq = 0; kq < 4; ++kq) {
-          const int ks = hv * 4 + kq;  // P atom hv and V^T atom hv (TMEM P: 8 columns per step)
-          const uint64_t p_off = (uint64_t)((hv * ATOM + kq * 32) >> 4);
+          const int ks = hv * 4 + kq;  // keys [16 ks, 16 ks + 16): 8 TMEM columns of P, V^T atom hv
           const uint64_t v_off = (uint64_t)((hv * Plan::V_ATOM + kq * 32) >> 4);
-          if constexpr (P_TMEM)  // 16 keys = 8 columns of 16-bit pairs
-            umma_bf16_ts_elect(t_o + hv * HD, t_p + pb * 64 + ks * 8, v_desc + v_off, id_o, (j | kq) != 0);
-          else
-            umma_bf16_elect(t_o + hv * HD, p_desc + p_off, v_desc + v_off, id_o, (j | kq) != 0);
+          umma_bf16_ts_elect(t_o + hv * HD, t_p + pb * 64 + ks * 8, v_desc + v_off, id_o, (j | kq) != 0);
         }
         umma_commit_elect(&o_done[pb]);
         umma_commit_elect(&v_empty[st]);
-        umma_commit_elect(&s_full[pb]);                    // an arrival of "S(j + 2) ready"
+        if (SB == 2) umma_commit_elect(&s_full[pb]);  // an arrival of "S(j + 2) ready"
       }
       __syncwarp();
     }
@@ -329,8 +324,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     bool ok = true;
 
     for (int j = 0; j < n_kv; ++j) {
-      const int sb = j & 1;
-      if (!mbar_wait(&s_full[sb], (j >> 1) & 1, abort_flag, args.status)) {
+      const int sb = j & 1;  // P buffer
+      if (!mbar_wait(&s_full[j % SB], (j / SB) & 1, abort_flag, args.status)) {
         ok = false;
         break;
       }
@@ -339,16 +334,19 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       const int lo = ds > c0 ? ds - c0 : 0;
       const int hi = de - c0 < HC ? de - c0 : HC;
       const bool interior = (lo == 0) && (hi == HC);
-      const uint32_t ts = t_s + sb * TK + half * HC + lane_off;
+      const uint32_t ts = t_s + (j % SB) * TK + half * HC + lane_off;
       uint32_t sv[HC];
 #pragma unroll
       for (int c = 0; c < HC; c += 32) tmem_ld32(ts + c, *reinterpret_cast<uint32_t(*)[32]>(&sv[c]));
 #pragma unroll
       for (int c = 0; c < HC; c += 32) tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&sv[c]));
-      // the scores are in registers: the S issuer may overwrite this buffer with S(j + 2)
+      // the scores are in registers: the S issuer may overwrite this buffer with S(j + SB)
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[sb]);
+      if (lane == 0) mbar_arrive(&s_free[j % SB]);
+      // one buffer: probe now whether P(j - 2) V(j - 2) is complete (it nearly always is), so that
+      // the probe's latency hides under the exponentials
+      const bool p_buf_free = SB == 2 || j < 2 || mbar_test_wait(&o_done[sb], ((j - 2) >> 1) & 1);
       if (!interior) {
 #pragma unroll
         for (int i = 0; i < HC; ++i)
@@ -409,18 +407,16 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         }
       }
       l += (rs[0].x + rs[0].y + rs[1].x + rs[1].y) + (rs[2].x + rs[2].y + rs[3].x + rs[3].y);
-      // P buffer j % 2 is free: "S(j) ready" included O += P(j - 2) V(j - 2) being done
-      if constexpr (P_TMEM) {
-        // this half's 64 keys are columns [32 half, 32 half + 32) of TMEM P buffer j % 2
-        tmem_st32(t_p + sb * 64 + lane_off + 32 * half, pk);
-        tmem_st_wait();
-      } else {
-        const uint32_t p_row = smem_u32(sP + sb * P_BYTES + half * ATOM) + r * 128;
-#pragma unroll
-        for (int c = 0; c < HC / 8; ++c)
-          st_shared_v4(p_row + ((c ^ (r & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-        fence_proxy_async_smem();
+      // P buffer j % 2 is free once O += P(j - 2) V(j - 2) is complete (with two S buffers "S(j)
+      // ready" said so already; with one, the S barrier cannot count it: a PV commit of the next
+      // tile could then complete it before S(j) lands)
+      if (!p_buf_free && !mbar_wait(&o_done[sb], ((j - 2) >> 1) & 1, abort_flag, args.status)) {
+        ok = false;
+        break;
       }
+      // this half's 64 keys are columns [32 half, 32 half + 32) of TMEM P buffer j % 2
+      tmem_st32(t_p + sb * 64 + lane_off + 32 * half, pk);
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[sb]);
