@@ -7,7 +7,7 @@
 // One CTA = one (document, 128-row q-tile, head).  Key/value tiles are 128 tokens wide and start
 // at multiples of 128 in the packed sequence (so the TMA x coordinate of the transposed V is
 // 16-byte aligned); columns outside the document are masked to -inf in S and zeroed in V^T.
-//   warp 0     TMA producer: Q once, then K and V^T tiles through two 2-stage rings
+//   warp 0     TMA producer: Q once, then K and V^T tiles through a 3-stage and a 2-stage ring
 //   warp 1     TMEM allocator + S issuer: S(j) = Q K(j)^T into S buffer j % S_BUFS, issued as soon
 //              as K(j) has landed and the softmax has read that buffer's previous scores
 //   warps 10, 11  PV issuers, one per O half: O_h += P(j) V(j) once P(j) is in TMEM and V(j) has
@@ -38,7 +38,8 @@ namespace {
 
 constexpr int TQ = 128, TK = 128;
 constexpr int ATOM = 128 * 64 * 2;         // 128 rows x 64 16-bit columns, 128-byte swizzled (16 KB)
-constexpr int KV_STAGES = 2;
+constexpr int KV_STAGES = 2;               // V^T ring
+constexpr int K_STAGES = 3;                // K ring: K(j + 1) is wanted a tile before V(j + 1)
 constexpr int ATT_THREADS = 384;           // producer, S issuer, 8 softmax warps, two PV issuers
 constexpr int SOFTMAX_THREADS = 256;
 constexpr int PV_WARP = 10;                // PV issuers: warp 10 for O_0, warp 11 for O_1
@@ -53,7 +54,7 @@ struct AttPlan {
   static constexpr int K_BYTES = 128 * HD * 2;
   static constexpr int V_ATOM = HD * 128;
   static constexpr int V_BYTES = 2 * V_ATOM;
-  static constexpr int SMEM = Q_BYTES + KV_STAGES * (K_BYTES + V_BYTES) + 1024 + 256;
+  static constexpr int SMEM = Q_BYTES + K_STAGES * K_BYTES + KV_STAGES * V_BYTES + 1024 + 256;
   static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, TK);
   static constexpr uint32_t IDESC_O = idesc_bf16_f32(128, HD);
   // S buffers in TMEM: two where they fit beside O_0, O_1 and the two P buffers (head_dim 64), else
@@ -139,12 +140,12 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   using Plan = AttPlan<HD>;
   uint8_t* sQ = smem;
   uint8_t* sK = sQ + Plan::Q_BYTES;                    // [stage]
-  uint8_t* sV = sK + KV_STAGES * Plan::K_BYTES;        // [stage]
+  uint8_t* sV = sK + K_STAGES * Plan::K_BYTES;         // [stage]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sV + KV_STAGES * Plan::V_BYTES);
   uint64_t* q_full = bars;
   uint64_t* k_full = bars + 1;                         // [stage]  K tile landed
-  uint64_t* k_empty = k_full + KV_STAGES;              // [stage]  S MMA done with the K tile
-  uint64_t* v_empty = k_empty + KV_STAGES;             // [stage]  PV MMA done with the V^T tile
+  uint64_t* k_empty = k_full + K_STAGES;               // [stage]  S MMA done with the K tile
+  uint64_t* v_empty = k_empty + K_STAGES;              // [stage]  PV MMA done with the V^T tile
   uint64_t* s_full = v_empty + KV_STAGES;              // [S_BUFS] S(j) in TMEM buffer j % S_BUFS (two
                                                        //   buffers: and P(j - 2) V(j - 2) done)
   uint64_t* s_free = s_full + Plan::S_BUFS;            // [S_BUFS] the softmax has loaded S(j)
@@ -158,9 +159,11 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < KV_STAGES; ++s) {
+    for (int s = 0; s < K_STAGES; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < KV_STAGES; ++s) {
       mbar_init(&v_empty[s], 2);                         // both PV issuers
     }
     for (int b = 0; b < Plan::S_BUFS; ++b) {
@@ -194,44 +197,53 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       mbar_arrive_expect_tx(q_full, Plan::Q_BYTES);
 #pragma unroll
       for (int a = 0; a < HD / 64; ++a) tma_load_2d(sQ + a * ATOM, &tmQ, q_full, hx + 64 * a, q0);
-      // K tiles run two ahead of the V tiles: K(j) waits for S(j - KV_STAGES), V(j) for
-      // P(j - KV_STAGES) V(j - KV_STAGES).
-      auto load_k = [&](int j) -> bool {
-        const int st = j % KV_STAGES;
-        if (!mbar_wait(&k_empty[st], ((j / KV_STAGES) & 1) ^ 1, abort_flag, args.status)) return false;
-        const int kv0 = kv_base + j * TK;
+      // K(j) waits for S(j - K_STAGES), V(j) for P(j - KV_STAGES) V(j - KV_STAGES).  The two rings
+      // are polled side by side, so that a K stage still in use never holds back a free V stage or
+      // the other way round.
+      auto load_k = [&](int j) {
+        const int st = j % K_STAGES;
         mbar_arrive_expect_tx(&k_full[st], Plan::K_BYTES);
 #pragma unroll
         for (int a = 0; a < HD / 64; ++a)
-          tma_load_2d(sK + st * Plan::K_BYTES + a * ATOM, &tmK, &k_full[st], hx + 64 * a, kv0);
-        return true;
+          tma_load_2d(sK + st * Plan::K_BYTES + a * ATOM, &tmK, &k_full[st], hx + 64 * a, kv_base + j * TK);
       };
-      auto load_v = [&](int j) -> bool {
+      auto load_v = [&](int j) {
         const int st = j % KV_STAGES;
-        if (!mbar_wait(&v_empty[st], ((j / KV_STAGES) & 1) ^ 1, abort_flag, args.status)) return false;
         const int kv0 = kv_base + j * TK;
         // V(j) completes on the barrier that also counts the softmax warps' P(j) (stage = j % 2)
         mbar_arrive_expect_tx(&p_full[st], Plan::V_BYTES);
         tma_load_2d(sV + st * Plan::V_BYTES, &tmV, &p_full[st], kv0, hx);
         tma_load_2d(sV + st * Plan::V_BYTES + Plan::V_ATOM, &tmV, &p_full[st], kv0 + 64, hx);
-        return true;
       };
       int nk = 0, nv = 0;
-      bool ok = true;
-      for (; ok && nk < n_kv && nk < 2; ++nk) ok = load_k(nk);
-      while (ok && nv < n_kv) {
-        ok = load_v(nv);
-        if (!ok) break;
-        ++nv;
-        if (nk < n_kv) {
-          ok = load_k(nk);
-          if (ok) ++nk;
+      uint64_t t_last = globaltimer_ns();
+      for (uint32_t spin = 0; nk < n_kv || nv < n_kv; ++spin) {
+        bool moved = false;
+        if (nk < n_kv && mbar_test_wait(&k_empty[nk % K_STAGES], ((nk / K_STAGES) & 1) ^ 1)) {
+          load_k(nk++);
+          moved = true;
+        }
+        if (nv < n_kv && mbar_test_wait(&v_empty[nv % KV_STAGES], ((nv / KV_STAGES) & 1) ^ 1)) {
+          load_v(nv++);
+          moved = true;
+        }
+        if (moved) {
+          spin = 0;
+        } else if ((spin & 255u) == 255u) {
+          if (*abort_flag) break;
+          const uint64_t now = globaltimer_ns();
+          if (spin == 255u) t_last = now;  // the first idle check after progress starts the clock
+          if (now - t_last > kWaitLimitNs) {
+            *abort_flag = 1;
+            if (args.status) atomicOr(args.status, kDevTimeout);
+            break;
+          }
         }
       }
       // Every copy this CTA issued must land before the CTA may exit.
       wait_noabort(q_full, 0);
-      for (int j = nk - KV_STAGES < 0 ? 0 : nk - KV_STAGES; j < nk; ++j)
-        wait_noabort(&k_full[j % KV_STAGES], (j / KV_STAGES) & 1);
+      for (int j = nk - K_STAGES < 0 ? 0 : nk - K_STAGES; j < nk; ++j)
+        wait_noabort(&k_full[j % K_STAGES], (j / K_STAGES) & 1);
       for (int j = nv - KV_STAGES < 0 ? 0 : nv - KV_STAGES; j < nv; ++j)
         wait_noabort(&p_full[j % KV_STAGES], (j / KV_STAGES) & 1);
     }
@@ -243,9 +255,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     const uint64_t q_desc = sdesc_sw128(smem_u32(sQ));
     constexpr uint32_t id_s = F16 ? idesc_f16_f32(128, TK) : Plan::IDESC_S;
     for (int j = 0; ok && j < n_kv; ++j) {
-      const int st = j % KV_STAGES, sb = j % SB;
+      const int st = j % K_STAGES, sb = j % SB;
       if (j >= SB) ok = __all_sync(0xffffffffu, mbar_wait(&s_free[sb], (j / SB - 1) & 1, abort_flag, args.status));
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&k_full[st], (j / KV_STAGES) & 1, abort_flag, args.status));
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&k_full[st], (j / K_STAGES) & 1, abort_flag, args.status));
       if (!ok) break;
       tc_fence_after();
       const uint64_t k_desc = sdesc_sw128(smem_u32(sK + st * Plan::K_BYTES));
