@@ -137,8 +137,8 @@ typedef struct {
   int64_t forwards;             /* dit_forward calls that launched work */
   int64_t kernels_launched;     /* every kernel this handle launched */
   int64_t gemm_launches, attention_launches, norm_launches, other_launches;
-  int64_t attention_tiles;      /* (query block, head) work items of the last forward (device count): blocks of
-                                   dit_attention_block_rows() rows in the bf16/f16 forward, 128 in the fp32 one */
+  int64_t attention_tiles;      /* (query tile, head) work items of the last forward (device count), tiles of
+                                   dit_attention_block_rows() rows */
   int64_t bound_bytes;          /* bytes of library-owned repacked weight copies */
   int32_t device_status;        /* last status word read back (0 = ok) */
   int32_t last_layout_error;    /* device validator's code for the last forward (0 = ok) */
@@ -484,11 +484,11 @@ DIT_API dit_status dit_op_pack_ffn_in(const void* w_in, const float* b_in, int F
  * before they are used, so every document's output is bit-independent of the other documents'
  * values, non-finite ones included.
  *   o     [n_tokens, H * Dh]
- * head_dim is 64 or 128.  The (document, query block) work list is built on the device from
+ * head_dim is 64 or 128.  The (document, query tile) work list is built on the device from
  * cu_seqlens into `workspace` (dit_attention_workspace_bytes(n_docs, n_tokens) bytes). */
 DIT_API size_t dit_attention_workspace_bytes(int n_docs, int n_tokens);
-/* Query rows per (document, query block) work item of the bf16/f16 attention: the unit of
- * dit_stats.attention_tiles for the 16-bit forward (the fp32 forward's blocks are 128 rows). */
+/* Query rows per (document, query tile) work item of the attention: the unit of
+ * dit_stats.attention_tiles. */
 DIT_API int dit_attention_block_rows(void);
 DIT_API dit_status dit_op_attention(const void* q, const void* k, const void* vt, int n_pad, const int32_t* cu_seqlens,
                             int n_docs, int n_tokens, int n_heads, int head_dim, void* o, void* workspace,
@@ -500,7 +500,7 @@ DIT_API dit_status dit_op_attention(const void* q, const void* k, const void* vt
  * The pages have no counterpart of this call; it exists for such callers only.
  *   Arguments, layouts and results are those of dit_op_attention, without `workspace`.
  *   Scratch: a fixed array inside libdit.so's device memory (256 bytes of status words plus
- *   DIT_ATTENTION_NOALLOC_MAX_TILES (document, query block) entries of 8 bytes, about 64 KB),
+ *   DIT_ATTENTION_NOALLOC_MAX_TILES (document, 128-row q-tile) entries of 8 bytes, about 64 KB),
  *   held by every GPU that loads the library until the process exits.  Nothing is allocated or freed.
  *   Capacity: ceil(n_tokens / 128) + n_docs <= DIT_ATTENTION_NOALLOC_MAX_TILES, else
  *   DIT_ERR_CAPACITY with dit_last_error(NULL) saying so, before any work is enqueued.

@@ -458,7 +458,7 @@ dit_status forward_fp32(dit_handle* h, const float* x_tokens, const int32_t* cu_
     Launch ln(h, s, 6);
     DIT_CK(h, cudaMemsetAsync(sw, 0, sizeof(StatusWords), s), "status reset");
     DIT_CK(h, attention_schedule_launch(cu_seqlens, n_docs, N, doc_ids, modality_tags, 1, items, &sw->count,
-                                        L.max_items, &sw->layout_code, status, 128, s), "layout check");
+                                        L.max_items, &sw->layout_code, status, s), "layout check");
     ln.done();
   }
   if (L.half > 0) {
@@ -908,7 +908,7 @@ static dit_status forward_impl(dit_handle* h, const float* x_tokens, const int32
     Launch ln(h, s, 6);
     DIT_CK(h, cudaMemsetAsync(sw, 0, sizeof(StatusWords), s), "status reset");
     DIT_CK(h, attention_schedule_launch(cu_seqlens, n_docs, N, doc_ids, modality_tags, nm, items, &sw->count,
-                                        L.max_items, &sw->layout_code, status, attention_item_rows(), s), "schedule");
+                                        L.max_items, &sw->layout_code, status, s), "schedule");
     ln.done();
   }
   {
@@ -1615,7 +1615,7 @@ dit_status dit_op_attention(const void* q, const void* k, const void* vt, int n_
   cudaError_t e = cudaMemsetAsync(sw, 0, sizeof(StatusWords), s);
   if (e == cudaSuccess)
     e = attention_schedule_launch(cu_seqlens, n_docs, n_tokens, nullptr, nullptr, 0, items, &sw->count, max_items,
-                                  &sw->layout_code, &sw->bits, attention_item_rows(), s);
+                                  &sw->layout_code, &sw->bits, s);
   if (e != cudaSuccess) return cuda_err(nullptr, e, "attention schedule");
   AttnArgs aa;
   aa.n_tokens = n_tokens; aa.n_heads = n_heads; aa.head_dim = head_dim; aa.n_pad = n_pad; aa.n_docs = n_docs;
@@ -1740,7 +1740,7 @@ extern "C" dit_status dit_op_attention_noalloc(const void* q, const void* k, con
   e = cudaMemsetAsync(sw, 0, sizeof(StatusWords), s);
   if (e == cudaSuccess)
     e = attention_schedule_launch(cu_seqlens, n_docs, n_tokens, nullptr, nullptr, 0, items, &sw->count, max_items,
-                                  &sw->layout_code, &sw->bits, attention_item_rows(), s);
+                                  &sw->layout_code, &sw->bits, s);
   if (e != cudaSuccess) return cuda_err(nullptr, e, "attention schedule");
   AttnArgs aa;
   aa.n_tokens = n_tokens; aa.n_heads = n_heads; aa.head_dim = head_dim; aa.n_pad = n_pad; aa.n_docs = n_docs;

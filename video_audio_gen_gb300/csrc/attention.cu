@@ -96,28 +96,6 @@ __device__ __forceinline__ void zero_v_outside(uint8_t* sv_tile, int lo, int hi,
   }
 }
 
-// The same over both atoms of the tile by NT threads (t in [0, NT)).
-template <int HD, int NT>
-__device__ __forceinline__ void zero_v_outside_n(uint8_t* sv_tile, int lo, int hi, int t) {
-  const uint32_t base = smem_u32(sv_tile);
-  for (int idx = t; idx < HD * 16; idx += NT) {
-    const int row = idx >> 4, chunk = idx & 15;  // chunk: keys [8 chunk, 8 chunk + 8)
-    const int k0 = chunk * 8;
-    if (k0 >= lo && k0 + 8 <= hi) continue;
-    const uint32_t addr = base + (chunk >> 3) * (HD * 128) + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
-    uint4 v = ld_shared_v4(addr);
-    uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int k = k0 + 2 * e;
-      const uint32_t keep_lo = (k >= lo && k < hi) ? 0x0000FFFFu : 0u;
-      const uint32_t keep_hi = (k + 1 >= lo && k + 1 < hi) ? 0xFFFF0000u : 0u;
-      w[e] &= keep_lo | keep_hi;
-    }
-    st_shared_v4(addr, w[0], w[1], w[2], w[3]);
-  }
-}
-
 // F16: the 16-bit operand type (q, k, V^T, P and o) is f16, else bf16.  A template parameter, so that
 // the softmax's conversions are one instruction per pair with no select.
 template <int HD, bool F16>
@@ -483,403 +461,14 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   }
 }
 
-// ---------------------------------------------------------------------------------------------
-// Two query tiles per CTA.  One CTA = one (document, 256-row query block, head): query tiles Q_0
-// (rows q0 .. q0 + 127) and Q_1 (the next 128) share every K and V^T tile, and each has its own
-// softmax group of four warps, one thread per query row over all 128 keys of a tile.  The MMA
-// thread alternates between the groups:
-//     PV_0(j), S_0(j + 1), PV_1(j), S_1(j + 1), PV_0(j + 1), ...
-// so while group 0 turns S_0(j + 1) into P_0(j + 1), the tensor pipe runs group 1's PV and S, and
-// the other way round: the softmax of one group hides under the other group's MMAs instead of all
-// eight warps waiting for the same tile.
-//   warp 0     TMA producer: Q_0, Q_1 once, then K and V^T tiles through their rings
-//   warp 1     TMEM allocator + MMA issuer (one thread); on a document's boundary tiles the whole
-//              warp zeroes the V^T columns outside the document before the tile's first PV
-//   warps 2-5  softmax of Q_0, warps 6-9 softmax of Q_1 (TMEM lane quarter = warp % 4)
-// TMEM: S_0, S_1 (128 columns each) then O_0, O_1 (Dh each).  P_g(j) (16-bit pairs) is written over
-// the first 64 columns of S_g once the scores are in registers, and the PV MMA reads it from there
-// as its TMEM operand.  S_g(j + 1) overwrites those columns: it is issued after PV_g(j) by the same
-// thread, and one thread's MMAs execute in issue order.
-// Every "S_g(j) ready" commit follows PV_g(j - 1) in that order, so seeing it also says that the
-// previous PV of the group is complete: the softmax may rescale O_g and overwrite P_g.
-// A document's query blocks are 256 rows; when a block's second tile lies wholly past the document
-// end, group 1 and its MMAs are skipped.
-constexpr int QB_ROWS = 2 * TQ;   // query rows per work item of this kernel
-// attention_launch runs this kernel (true) or the one-tile kernel above (false)
-constexpr bool kTwoTileAttention = false;
-constexpr int A2_THREADS = 320;   // producer, MMA warp, two softmax groups of four warps
+constexpr int ITEM_ROWS = TQ;  // query rows per scheduled work item
 
-template <int HD>
-struct Att2Plan {
-  static constexpr int KS = 3;                   // K ring stages
-  static constexpr int VS = HD == 128 ? 2 : 3;   // V^T ring stages
-  static constexpr int Q_BYTES = 128 * HD * 2;   // one query tile
-  static constexpr int K_BYTES = 128 * HD * 2;
-  static constexpr int V_ATOM = HD * 128;
-  static constexpr int V_BYTES = 2 * V_ATOM;
-  static constexpr int SMEM = 2 * Q_BYTES + KS * K_BYTES + VS * V_BYTES + 1024 + 256;
-};
-static_assert(Att2Plan<128>::SMEM <= 227 * 1024, "head_dim 128 plan exceeds shared memory");
-
-template <int HD, bool F16>
-__global__ void __launch_bounds__(A2_THREADS, 1)
-    attention2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                      const __grid_constant__ CUtensorMap tmV, uint16_t* __restrict__ O, const AttnArgs args,
-                      int max_blocks) {
-  using Plan = Att2Plan<HD>;
-  constexpr int KS = Plan::KS, VS = Plan::VS;
-  if (args.status && (*reinterpret_cast<volatile int*>(args.status) & kDevLayout)) return;
-  const int count = *args.count;
-  const int head = blockIdx.x / max_blocks;
-  const int item_idx = blockIdx.x - head * max_blocks;
-  if (item_idx >= count || head >= args.n_heads) return;
-  const int2 item = args.items[item_idx];
-  const int doc = item.x, q0 = item.y;
-  const int ds = args.cu[doc], de = args.cu[doc + 1];
-  const int kv_base = (ds / TK) * TK;
-  const int n_kv = (de - kv_base + TK - 1) / TK;
-  const int ng = q0 + TQ < de ? 2 : 1;  // query tiles holding rows of the document
-
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem;                                  // [2] query tiles
-  uint8_t* sK = sQ + 2 * Plan::Q_BYTES;                // [KS]
-  uint8_t* sV = sK + KS * Plan::K_BYTES;               // [VS]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + VS * Plan::V_BYTES);
-  uint64_t* q_full = bars;
-  uint64_t* k_full = q_full + 1;                       // [KS] K tile landed
-  uint64_t* k_empty = k_full + KS;                     // [KS] the S MMAs are done with it
-  uint64_t* v_full = k_empty + KS;                     // [VS] V^T tile landed
-  uint64_t* v_empty = v_full + VS;                     // [VS] the PV MMAs are done with it
-  uint64_t* s_full = v_empty + VS;                     // [2] S_g(j) in TMEM (and PV_g(j - 1) done)
-  uint64_t* p_full = s_full + 2;                       // [2] P_g(j) in TMEM (O_g rescaled if needed)
-  uint64_t* o_last = p_full + 2;                       // [2] the group's last PV complete
-  uint64_t* drain = o_last + 2;                        // every MMA complete
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    for (int s = 0; s < KS; ++s) {
-      mbar_init(&k_full[s], 1);
-      mbar_init(&k_empty[s], 1);
-    }
-    for (int s = 0; s < VS; ++s) {
-      mbar_init(&v_full[s], 1);
-      mbar_init(&v_empty[s], 1);
-    }
-    for (int g = 0; g < 2; ++g) {
-      mbar_init(&s_full[g], 1);
-      mbar_init(&p_full[g], 4);  // the group's four softmax warps
-      mbar_init(&o_last[g], 1);
-    }
-    mbar_init(drain, 1);
-    *abort_flag = 0;
-    mbar_fence_init();
-  }
-  if (warp == 1) tmem_alloc(tmem_slot, 512);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      const int hx = head * HD;
-      mbar_arrive_expect_tx(q_full, ng * Plan::Q_BYTES);
-      for (int g = 0; g < ng; ++g)
-#pragma unroll
-        for (int a = 0; a < HD / 64; ++a) tma_load_2d(sQ + g * Plan::Q_BYTES + a * ATOM, &tmQ, q_full, hx + 64 * a, q0 + g * TQ);
-      // K(j) waits for the S MMAs of K(j - KS), V(j) for the PV MMAs of V(j - VS).  The two rings
-      // are polled side by side, so that a K stage still in use never holds back a free V stage
-      // (V(j + 1) is wanted one tile after K(j + 1), and a blocking wait on K would tie its load to
-      // the S MMAs of the tile before).
-      auto load_k = [&](int j) {
-        const int st = j % KS;
-        mbar_arrive_expect_tx(&k_full[st], Plan::K_BYTES);
-#pragma unroll
-        for (int a = 0; a < HD / 64; ++a)
-          tma_load_2d(sK + st * Plan::K_BYTES + a * ATOM, &tmK, &k_full[st], hx + 64 * a, kv_base + j * TK);
-      };
-      auto load_v = [&](int j) {
-        const int st = j % VS;
-        const int kv0 = kv_base + j * TK;
-        mbar_arrive_expect_tx(&v_full[st], Plan::V_BYTES);
-        tma_load_2d(sV + st * Plan::V_BYTES, &tmV, &v_full[st], kv0, hx);
-        tma_load_2d(sV + st * Plan::V_BYTES + Plan::V_ATOM, &tmV, &v_full[st], kv0 + 64, hx);
-      };
-      int nk = 0, nv = 0;
-      uint64_t t_last = globaltimer_ns();
-      for (uint32_t spin = 0; nk < n_kv || nv < n_kv; ++spin) {
-        bool moved = false;
-        if (nk < n_kv && mbar_test_wait(&k_empty[nk % KS], ((nk / KS) & 1) ^ 1)) {
-          load_k(nk++);
-          moved = true;
-        }
-        if (nv < n_kv && mbar_test_wait(&v_empty[nv % VS], ((nv / VS) & 1) ^ 1)) {
-          load_v(nv++);
-          moved = true;
-        }
-        if (moved) {
-          spin = 0;
-        } else if ((spin & 255u) == 255u) {
-          if (*abort_flag) break;
-          const uint64_t now = globaltimer_ns();
-          if (spin == 255u) t_last = now;  // the first idle check after progress starts the clock
-          if (now - t_last > kWaitLimitNs) {
-            *abort_flag = 1;
-            if (args.status) atomicOr(args.status, kDevTimeout);
-            break;
-          }
-        }
-      }
-      // Every copy this CTA issued must land before the CTA may exit.
-      wait_noabort(q_full, 0);
-      for (int j = nk - KS < 0 ? 0 : nk - KS; j < nk; ++j) wait_noabort(&k_full[j % KS], (j / KS) & 1);
-      for (int j = nv - VS < 0 ? 0 : nv - VS; j < nv; ++j) wait_noabort(&v_full[j % VS], (j / VS) & 1);
-    }
-  } else if (warp == 1) {
-    // The MMA warp runs converged: every lane waits and computes the descriptors, elect.sync picks
-    // the lane that issues (a branch taken by one lane issues markedly slower).
-    constexpr uint32_t id_s = F16 ? idesc_f16_f32(128, TK) : idesc_bf16_f32(128, TK);
-    constexpr uint32_t id_o = F16 ? idesc_f16_f32(128, HD) : idesc_bf16_f32(128, HD);
-    const uint64_t q_desc = sdesc_sw128(smem_u32(sQ));
-    // S_g(j) = Q_g K(j)^T into S_g.  A descriptor's start field is the address / 16, so an offset
-    // within the tile is added to the descriptor itself.
-    auto issue_s = [&](int g, int j) {
-      const uint64_t qd = q_desc + (uint64_t)((g * Plan::Q_BYTES) >> 4);
-      const uint64_t kd = sdesc_sw128(smem_u32(sK + (j % KS) * Plan::K_BYTES));
-#pragma unroll
-      for (int ks = 0; ks < HD / 16; ++ks) {
-        const uint64_t off = (uint64_t)((((ks >> 2) * ATOM) + (ks & 3) * 32) >> 4);
-        umma_bf16_elect(tmem + g * TK, qd + off, kd + off, id_s, ks != 0);
-      }
-    };
-    // O_g += P_g(j) V(j): P from TMEM (16 keys = 8 columns of 16-bit pairs per step), V^T from shared
-    auto issue_pv = [&](int g, int j) {
-      const uint64_t vd = sdesc_sw128(smem_u32(sV + (j % VS) * Plan::V_BYTES));
-#pragma unroll
-      for (int ks = 0; ks < TK / 16; ++ks) {
-        const uint64_t off = (uint64_t)((((ks >> 2) * Plan::V_ATOM) + (ks & 3) * 32) >> 4);
-        umma_bf16_ts_elect(tmem + 2 * TK + g * HD, tmem + g * TK + ks * 8, vd + off, id_o, (j | ks) != 0);
-      }
-    };
-    bool ok = mbar_wait(q_full, 0, abort_flag, args.status) && mbar_wait(&k_full[0], 0, abort_flag, args.status);
-    ok = __all_sync(0xffffffffu, ok);
-    if (ok) {
-      tc_fence_after();
-      for (int g = 0; g < ng; ++g) {
-        issue_s(g, 0);
-        umma_commit_elect(&s_full[g]);
-      }
-      umma_commit_elect(&k_empty[0]);
-    }
-    for (int j = 0; ok && j < n_kv; ++j) {
-      const int vs = j % VS;
-      const bool more = j + 1 < n_kv;
-      const int kn = (j + 1) % KS;
-      // P_0(j) ready also says that V(j) has landed and, on a boundary tile, that its columns
-      // outside the document are zeroed (softmax group 0 does it)
-      for (int g = 0; g < ng; ++g) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&p_full[g], j & 1, abort_flag, args.status));
-        if (!ok) break;
-        tc_fence_after();
-        issue_pv(g, j);
-        if (g == ng - 1) umma_commit_elect(&v_empty[vs]);
-        if (!more) {
-          umma_commit_elect(&o_last[g]);
-          continue;
-        }
-        if (g == 0) {
-          ok = __all_sync(0xffffffffu, mbar_wait(&k_full[kn], ((j + 1) / KS) & 1, abort_flag, args.status));
-          if (!ok) break;
-          tc_fence_after();
-        }
-        issue_s(g, j + 1);
-        umma_commit_elect(&s_full[g]);
-        if (g == ng - 1) umma_commit_elect(&k_empty[kn]);
-      }
-    }
-    // No MMA may still read shared memory or write TMEM when the CTA tears down.
-    umma_commit_elect(drain);
-    wait_noabort(drain, 0);
-  } else {
-    // ---------------- softmax: group g = query tile g, one thread per query row ----------------
-    // The running max m is raised (and O_g, l rescaled by exp2(m_old - m_new)) only when the row max
-    // grows by more than 2^8, so most tiles never touch O_g; between raises p = exp2(s * scale - m)
-    // stays below 2^8.
-    const int g = (warp - 2) >> 2;
-    const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;            // tile row owned by this thread
-    const int row = q0 + g * TQ + r;              // packed-sequence row
-    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t t_sg = tmem + g * TK + lane_off;       // S_g; P_g in its first 64 columns
-    const uint32_t t_og = tmem + 2 * TK + g * HD + lane_off;
-    const float sc = args.scale_log2;
-    constexpr bool f16 = F16;
-    constexpr float kRescaleThreshold = 8.0f;     // log2 units
-    float m = -INFINITY, l = 0.f;
-    bool ok = g < ng;
-    for (int j = 0; ok && j < n_kv; ++j) {
-      if (!mbar_wait(&s_full[g], j & 1, abort_flag, args.status)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const int c0 = kv_base + j * TK;
-      const int lo = ds > c0 ? ds - c0 : 0;
-      const int hi = de - c0 < TK ? de - c0 : TK;
-      const bool interior = lo == 0 && hi == TK;
-      // One pass against the current reference max m: each 32-column chunk of scores is loaded from
-      // TMEM while the previous one becomes exponentials, and the row max comes out of the same
-      // pass.  P stays in registers until the pass is over, so the scores in TMEM survive for the
-      // rare tile whose max exceeds m by more than 2^8 (and the first tile, m = -inf), which takes
-      // a second pass with the raised m.
-      uint32_t pk[TK / 2];
-      float2 rs[4];
-      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-      const float2 sc2 = make_float2(sc, sc);
-      auto exps32 = [&](const uint32_t (&v)[32], int c, float2 nm2) {
-#pragma unroll
-        for (int i = 0; i < 32; i += 8) {
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float2 x = ffma2(make_float2(__uint_as_float(v[i + 2 * u]), __uint_as_float(v[i + 2 * u + 1])), sc2, nm2);
-            const float2 e = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-            rs[u] = fadd2(rs[u], e);
-            pk[c / 2 + i / 2 + u] = pack16(f16, e.x, e.y);
-          }
-        }
-      };
-      auto mask32 = [&](uint32_t (&v)[32], int c) {
-        if (!interior) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (c + i < lo || c + i >= hi) v[i] = __float_as_uint(-INFINITY);
-        }
-      };
-#pragma unroll
-      for (int u = 0; u < 4; ++u) rs[u] = make_float2(0.f, 0.f);
-      {
-        const bool have_ref = j > 0;  // m is finite after the first tile
-        const float2 nm2 = make_float2(-m, -m);
-        uint32_t buf[2][32];
-        tmem_ld32(t_sg, buf[0]);
-        tmem_ld_wait_regs(buf[0]);
-#pragma unroll
-        for (int c = 0; c < TK; c += 32) {
-          uint32_t(&cur)[32] = buf[(c / 32) & 1];
-          if (c + 32 < TK) tmem_ld32(t_sg + c + 32, buf[(c / 32 + 1) & 1]);
-          mask32(cur, c);
-#pragma unroll
-          for (int i = 0; i < 32; i += 8) {
-            mx0 = fmax3(mx0, __uint_as_float(cur[i]), __uint_as_float(cur[i + 1]));
-            mx1 = fmax3(mx1, __uint_as_float(cur[i + 2]), __uint_as_float(cur[i + 3]));
-            mx2 = fmax3(mx2, __uint_as_float(cur[i + 4]), __uint_as_float(cur[i + 5]));
-            mx3 = fmax3(mx3, __uint_as_float(cur[i + 6]), __uint_as_float(cur[i + 7]));
-          }
-          if (have_ref) exps32(cur, c, nm2);
-          if (c + 32 < TK) tmem_ld_wait_regs(buf[(c / 32 + 1) & 1]);
-        }
-      }
-      const float m_cand = fmaxf(fmax3(mx0, mx1, mx2), mx3) * sc;
-      // true on the first tile (m = -inf); every tile holds at least one key of the document
-      const bool raise = m_cand > m + kRescaleThreshold;
-      if (__any_sync(0xffffffffu, raise)) {
-        const float m_new = raise ? m_cand : m;
-        const float alpha = raise ? fast_exp2(m - m_new) : 1.f;  // exp2(-inf) = 0 on the first tile
-        if (j > 0) {
-          // "S_g(j) ready" came after PV_g(j - 1): O_g holds the sum over tiles < j relative to m
-#pragma unroll
-          for (int c = 0; c < HD; c += 32) {
-            uint32_t ov[32];
-            tmem_ld32_sync(t_og + c, ov);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-            tmem_st32(t_og + c, ov);
-          }
-          tmem_st_wait();
-        }
-        l *= alpha;
-        m = m_new;
-        // the second pass, against the raised m (rows that kept theirs recompute the same values)
-        const float2 nm2 = make_float2(-m, -m);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) rs[u] = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int c = 0; c < TK; c += 32) {
-          uint32_t v[32];
-          tmem_ld32_sync(t_sg + c, v);
-          mask32(v, c);
-          exps32(v, c, nm2);
-        }
-      }
-      // P over the first 64 columns of S_g (the scores are no longer needed)
-#pragma unroll
-      for (int c = 0; c < TK / 2; c += 16) tmem_st16(t_sg + c, *reinterpret_cast<uint32_t(*)[16]>(&pk[c]));
-      l += (rs[0].x + rs[0].y + rs[1].x + rs[1].y) + (rs[2].x + rs[2].y + rs[3].x + rs[3].y);
-      if (g == 0) {
-        // P_0(j) ready must also mean V(j) ready for the MMA warp: group 0 waits for the tile and,
-        // on a document's boundary tile, zeroes its columns outside the document (one 16-byte chunk
-        // per thread per step) and makes the stores visible to the MMA's operand reads
-        const int vs = j % VS;
-        if (!mbar_wait(&v_full[vs], (j / VS) & 1, abort_flag, args.status)) {
-          ok = false;
-          break;
-        }
-        if (!interior) {
-          zero_v_outside_n<HD, 128>(sV + vs * Plan::V_BYTES, lo, hi, threadIdx.x - 64);
-          fence_proxy_async_smem();
-        }
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[g]);
-    }
-    if (ok && n_kv > 0) {
-      ok = mbar_wait(&o_last[g], 0, abort_flag, args.status);
-      tc_fence_after();
-    }
-    if (ok) {
-      const float inv = 1.f / l;
-      uint16_t* orow = O + (size_t)row * (args.n_heads * HD) + head * HD;
-#pragma unroll
-      for (int c = 0; c < HD; c += 32) {
-        uint32_t ov[32];
-        tmem_ld32_sync(t_og + c, ov);
-        if (row < de) {
-#pragma unroll
-          for (int i = 0; i < 32; i += 8) {
-            float v[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = __uint_as_float(ov[i + u]) * inv;
-            st_global_v4(orow + c + i, pack16(f16, v[0], v[1]), pack16(f16, v[2], v[3]), pack16(f16, v[4], v[5]),
-                         pack16(f16, v[6], v[7]));
-          }
-        }
-      }
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
-}
-
-constexpr int ITEM_ROWS = TQ;  // query rows per work item of the fp32 attention (the bound below)
-
-// Validate the packed layout and emit the (document, q_start) list of `item_rows`-row query blocks,
-// longest documents first.
+// Validate the packed layout and emit the (document, q-tile) list, longest documents first.
 // Codes follow the layout contract: 1 no documents, 2 cu[0] != 0, 3 not strictly increasing,
 // 4 cu[D] != N, 5 a doc id disagrees with cu_seqlens, 6 a tag >= n_mod, 7 list overflow.
 __global__ void schedule_kernel(const int32_t* cu, int n_docs, int n_tokens, const int32_t* doc_ids,
                                 const uint8_t* tags, int n_mod, int2* items, int* count, int max_items,
-                                int* layout_code, int* status, int item_rows) {
+                                int* layout_code, int* status) {
   __shared__ int code;
   if (threadIdx.x == 0) {
     code = 0;
@@ -921,7 +510,7 @@ __global__ void schedule_kernel(const int32_t* cu, int n_docs, int n_tokens, con
       }
       prev_len = best_len;
       prev_idx = best;
-      for (int q = cu[best]; q < cu[best + 1]; q += item_rows) {
+      for (int q = cu[best]; q < cu[best + 1]; q += ITEM_ROWS) {
         if (n >= max_items) {
           code = 7;
           break;
@@ -948,14 +537,13 @@ cudaError_t attention_launch_t(const void* q, const void* k, const void* vt, voi
 
 int attention_max_items(int n_docs, int n_tokens) { return attention_max_items_impl(n_docs, n_tokens); }
 
-int attention_item_rows() { return kTwoTileAttention ? QB_ROWS : TQ; }
+int attention_item_rows() { return ITEM_ROWS; }
 
 cudaError_t attention_schedule_launch(const int32_t* cu, int n_docs, int n_tokens, const int32_t* doc_ids,
                                       const uint8_t* tags, int n_mod, int2* items, int* count, int max_items,
-                                      int* layout_code, int* status, int item_rows, cudaStream_t stream) {
-  if (item_rows != TQ && item_rows != QB_ROWS) return cudaErrorInvalidValue;
+                                      int* layout_code, int* status, cudaStream_t stream) {
   schedule_kernel<<<1, 256, 0, stream>>>(cu, n_docs, n_tokens, doc_ids, tags, n_mod, items, count, max_items,
-                                         layout_code, status, item_rows);
+                                         layout_code, status);
   return cudaGetLastError();
 }
 
@@ -965,27 +553,18 @@ template <int HD, bool F16>
 cudaError_t attention_launch_t(const void* q, const void* k, const void* vt, void* o, const AttnArgs& args,
                                cudaStream_t stream) {
   static unsigned long long smem_set = 0;
-  const void* kernel = kTwoTileAttention ? reinterpret_cast<const void*>(attention2_kernel<HD, F16>)
-                                         : reinterpret_cast<const void*>(attention_kernel<HD, F16>);
-  cudaError_t e = opt_in_smem(kernel, kTwoTileAttention ? Att2Plan<HD>::SMEM : AttPlan<HD>::SMEM, &smem_set);
+  cudaError_t e =
+      opt_in_smem(reinterpret_cast<const void*>(attention_kernel<HD, F16>), AttPlan<HD>::SMEM, &smem_set);
   if (e != cudaSuccess) return e;
   const int d = args.n_heads * HD;
   CUtensorMap tq, tk, tv;
   if (!make_tmap_bf16_2d(&tq, q, d, args.n_tokens, (uint64_t)d * 2, 64, TQ)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16_2d(&tk, k, d, args.n_tokens, (uint64_t)d * 2, 64, TK)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16_2d(&tv, vt, args.n_pad, d, (uint64_t)args.n_pad * 2, 64, HD)) return cudaErrorInvalidValue;
-  uint16_t* out = static_cast<uint16_t*>(o);
-  if (kTwoTileAttention) {
-    // a bound on the (document, 256-row block) items: sum over documents of ceil(len / 256)
-    const int max_blocks = (args.n_tokens + QB_ROWS - 1) / QB_ROWS + args.n_docs;
-    const int grid = max_blocks * args.n_heads;
-    if (grid <= 0) return cudaSuccess;
-    attention2_kernel<HD, F16><<<grid, A2_THREADS, Att2Plan<HD>::SMEM, stream>>>(tq, tk, tv, out, args, max_blocks);
-  } else {
-    const int grid = args.max_items * args.n_heads;
-    if (grid <= 0) return cudaSuccess;
-    attention_kernel<HD, F16><<<grid, ATT_THREADS, AttPlan<HD>::SMEM, stream>>>(tq, tk, tv, out, args);
-  }
+  const int grid = args.max_items * args.n_heads;
+  if (grid <= 0) return cudaSuccess;
+  attention_kernel<HD, F16><<<grid, ATT_THREADS, AttPlan<HD>::SMEM, stream>>>(tq, tk, tv, static_cast<uint16_t*>(o),
+                                                                               args);
   return cudaGetLastError();
 }
 

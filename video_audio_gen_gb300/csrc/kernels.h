@@ -86,13 +86,12 @@ cudaError_t attention_launch(const void* q, const void* k, const void* vt, void*
                              cudaStream_t stream);
 
 // Validates cu_seqlens (and doc_ids / tags when given) and writes the (doc, q_start) list of
-// item_rows-row query blocks, longest documents first: item_rows = attention_item_rows() for
-// attention_launch, 128 for attention_f32_launch.  On a bad layout sets kDevLayout in *status and
-// writes count = 0.
+// attention_item_rows()-row query tiles, longest documents first.  On a bad layout sets kDevLayout
+// in *status and writes count = 0.
 cudaError_t attention_schedule_launch(const int32_t* cu, int n_docs, int n_tokens, const int32_t* doc_ids,
                                       const uint8_t* tags, int n_mod, int2* items, int* count, int max_items,
-                                      int* layout_code, int* status, int item_rows, cudaStream_t stream);
-// A bound on the list length for either block size: ceil(n_tokens / 128) + n_docs.
+                                      int* layout_code, int* status, cudaStream_t stream);
+// A bound on the list length: ceil(n_tokens / 128) + n_docs.
 int attention_max_items(int n_docs, int n_tokens);
 int attention_item_rows();
 
