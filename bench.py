@@ -38,19 +38,25 @@ KINDS = ["gemm_qkv", "attention", "gemm_out", "gemm_ffn_up", "gemm_ffn_down", "n
 # figure is reported only while that source is unchanged.
 TRAFFIC = {
     # C2 block kernels, captured on the one-block slice video_audio_bf16_l1 (the same launch shapes)
-    ("attention", "video_audio_bf16"): {"bytes": 408393728, "src_sha": "36cf96257d9fb7f4"},
-    ("gemm_qkv", "video_audio_bf16"): {"bytes": 844992648, "src_sha": "9f8187b08155a351"},
-    ("gemm_out", "video_audio_bf16"): {"bytes": 507626576, "src_sha": "9f8187b08155a351"},
-    ("gemm_ffn_up", "video_audio_bf16"): {"bytes": 847073256, "src_sha": "9f8187b08155a351"},
-    ("gemm_ffn_down", "video_audio_bf16"): {"bytes": 1231706880, "src_sha": "9f8187b08155a351"},
+    ("attention", "video_audio_bf16"): {"bytes": 407028480, "src_sha": "c1ac0a8214956547"},
+    ("gemm_qkv", "video_audio_bf16"): {"bytes": 874441728, "src_sha": "d85e916c026666df"},
+    ("gemm_out", "video_audio_bf16"): {"bytes": 506077184, "src_sha": "d85e916c026666df"},
+    ("gemm_ffn_up", "video_audio_bf16"): {"bytes": 800780544, "src_sha": "d85e916c026666df"},
+    ("gemm_ffn_down", "video_audio_bf16"): {"bytes": 1229975296, "src_sha": "d85e916c026666df"},
     ("norm_modulate", "video_audio_bf16"): {"bytes": 288434480, "src_sha": "a930da117ae01e0d"},
-    ("attention", "long_doc_bf16"): {"bytes": 1369980416, "src_sha": "36cf96257d9fb7f4"},
+    # C3 block kernels, captured on the one-block slice long_doc_bf16_l1
+    ("attention", "long_doc_bf16"): {"bytes": 1369134080, "src_sha": "c1ac0a8214956547"},
+    ("gemm_qkv", "long_doc_bf16"): {"bytes": 5533086720, "src_sha": "d85e916c026666df"},
+    ("gemm_out", "long_doc_bf16"): {"bytes": 3316553472, "src_sha": "d85e916c026666df"},
+    ("gemm_ffn_up", "long_doc_bf16"): {"bytes": 9850829056, "src_sha": "d85e916c026666df"},
+    ("gemm_ffn_down", "long_doc_bf16"): {"bytes": 6008213504, "src_sha": "d85e916c026666df"},
+    ("norm_modulate", "long_doc_bf16"): {"bytes": 1004406016, "src_sha": "a930da117ae01e0d"},
     # fp32 path, captured on the two-block slice music_fp32_l2 (the same launch shapes)
-    ("gemm_qkv", "music_fp32"): {"bytes": 52133888, "src_sha": "39e99c7e78d4646a"},
-    ("gemm_out", "music_fp32"): {"bytes": 18275072, "src_sha": "39e99c7e78d4646a"},
-    ("gemm_ffn_up", "music_fp32"): {"bytes": 139017728, "src_sha": "39e99c7e78d4646a"},
-    ("gemm_ffn_down", "music_fp32"): {"bytes": 74777856, "src_sha": "39e99c7e78d4646a"},
-    ("attention", "music_fp32"): {"bytes": 4258816, "src_sha": "39e99c7e78d4646a"},
+    ("gemm_qkv", "music_fp32"): {"bytes": 51839488, "src_sha": "dc490443327af73d"},
+    ("gemm_out", "music_fp32"): {"bytes": 18276352, "src_sha": "dc490443327af73d"},
+    ("gemm_ffn_up", "music_fp32"): {"bytes": 135834112, "src_sha": "dc490443327af73d"},
+    ("gemm_ffn_down", "music_fp32"): {"bytes": 73186560, "src_sha": "dc490443327af73d"},
+    ("attention", "music_fp32"): {"bytes": 4259584, "src_sha": "dc490443327af73d"},
 }
 
 
