@@ -312,10 +312,11 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     constexpr float kRescaleThreshold = 8.0f;    // log2 units
     float m = -INFINITY, l = 0.f;
     bool ok = true;
+    bool s_seen = false;  // "S(j) ready" already observed by the probe at the end of tile j - 1
 
     for (int j = 0; j < n_kv; ++j) {
       const int sb = j & 1;  // P buffer
-      if (!mbar_wait(&s_full[j % SB], (j / SB) & 1, abort_flag, args.status)) {
+      if (!s_seen && !mbar_wait(&s_full[j % SB], (j / SB) & 1, abort_flag, args.status)) {
         ok = false;
         break;
       }
@@ -364,7 +365,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             break;
           }
           tc_fence_after();
-#pragma unroll
+#pragma unroll 1  // a rare path: kept out of line so the tile loop stays small
           for (int c = 0; c < HD; c += 32) {
             uint32_t ov[32];
             tmem_ld32_sync(t_oh + c, ov);
@@ -406,6 +407,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       }
       // this half's 64 keys are columns [32 half, 32 half + 32) of TMEM P buffer j % 2
       tmem_st32(t_p + sb * 64 + lane_off + 32 * half, pk);
+      // probe "S(j + 1) ready" now, so that the probe's latency overlaps the P store
+      s_seen = j + 1 < n_kv && mbar_test_wait(&s_full[(j + 1) % SB], ((j + 1) / SB) & 1);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
