@@ -381,8 +381,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       // A half that has seen no key of the document yet has m = -inf and only masked scores:
       // p = exp2(-inf - 0) = 0 keeps O_h and l_h at zero.
       const float mu = m == -INFINITY ? 0.f : m;
-      // p = exp2(s * scale - m) -> 16-bit pairs; this half's 64 columns are exactly P atom `half` of
-      // shared-memory buffer j % 2, one 128-byte swizzled row per query row
+      // p = exp2(s * scale - m) -> 16-bit pairs, this half's 32 columns of TMEM P buffer j % 2
       uint32_t pk[HC / 2];
       // paired fp32 arithmetic (one f32x2 FMA / add per two scores); four partial row sums
       const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-mu, -mu);
