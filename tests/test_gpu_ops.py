@@ -204,6 +204,40 @@ def test_gemm_qkv_rope_matches_oracle(name, elem):
     assert (bf16_to_f64(vt)[:, M:] == 0).all()  # padding columns are written as zeros
 
 
+@pytest.mark.parametrize("Dh,R", [(32, 32), (128, 128), (128, 96), (256, 256), (256, 128)])
+def test_gemm_qkv_rope_head_dims(Dh, R):
+    """The QKV epilogue at other head dims than the models': the tile's 256 columns are split between
+    two epilogue warps per TMEM lane quarter, a head never between them (at head_dim 256 the first
+    warp takes the whole head).  d = 512, a ragged M of three row tiles, random cos/sin caches."""
+    dit, gu = _dit(), _gu()
+    d, M, K = 512, 300, 256
+    H = d // Dh
+    a, abits, b, bbits, bias = _ab(M, 3 * d, K, 70 + Dh + R)
+    (A, a), (B, b) = dev16(a, abits, "bf16"), dev16(b, bbits, "bf16")
+    ang = synth.uniform(71 + Dh + R, "angles", M * (R // 2)).reshape(M, R // 2) * 6.283185307179586
+    cs = np.cos(ang).astype(np.float32).astype(np.float64)
+    sn = np.sin(ang).astype(np.float32).astype(np.float64)
+    qkv = oracle.linear(a, b, bias)
+    qr = oracle.rope_apply(qkv[:, :d], H, Dh, R, cs, sn)
+    kr = oracle.rope_apply(qkv[:, d:2 * d], H, Dh, R, cs, sn)
+    vr = qkv[:, 2 * d:]
+    n_pad = (M + 7) // 8 * 8
+    q = torch.empty((M, d), dtype=torch.bfloat16, device="cuda")
+    k = torch.empty_like(q)
+    vt = torch.full((d, n_pad), float("nan"), dtype=torch.bfloat16, device="cuda")
+    gcs = gu.dev_f32(cs.astype(np.float32))
+    gsn = gu.dev_f32(sn.astype(np.float32))
+    dit.gemm_qkv_rope(A, B, gu.dev_f32(bias), H, Dh, R, gcs, gsn, q, k, vt, n_pad)
+    bound = fp32_sum_bound(a.astype(np.float64), b.astype(np.float64))
+    bq = bound[:, :d] + np.roll(bound[:, :d], 1, axis=1)
+    for got, ref in ((bf16_to_f64(q), qr), (bf16_to_f64(k), kr)):
+        err = np.abs(got - ref)
+        assert np.all(err <= REL["bf16"] * np.abs(ref) + 2 * bq.max() + 1e-5), err.max()
+    gv = bf16_to_f64(vt)[:, :M].T
+    assert np.all(np.abs(gv - vr) <= REL["bf16"] * np.abs(vr) + bound[:, 2 * d:] + 1e-6)
+    assert (bf16_to_f64(vt)[:, M:] == 0).all()
+
+
 @pytest.mark.parametrize("elem", ELEMS)
 def test_gemm_gated_residual_matches_oracle(elem):
     dit, gu = _dit(), _gu()
