@@ -566,38 +566,39 @@ __global__ void __launch_bounds__(BQ ? Q_THREADS : GEMM_THREADS, 1)
     producer_done:;
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      int acc = 0;
-      uint32_t acc_phase = 0;
-      for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
-        if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, args.status)) break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem + acc * BN;
-        bool ok = true;
-        for (int kb = 0; kb < k_blocks; ++kb) {
-          if (!mbar_wait(&full[stage], phase, abort_flag, args.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a0 = smem_u32(sA + stage * A_BYTES);
-          const uint32_t b0 = smem_u32(sB + stage * B_BYTES);
-#pragma unroll
-          for (int k = 0; k < BK / 16; ++k)
-            umma_bf16(d_tmem, sdesc_sw128(a0 + k * 32), sdesc_sw128(b0 + k * 32), ID, (kb | k) != 0);
-          umma_commit(&empty[stage]);
-          if (++stage == NST) {
-            stage = 0;
-            phase ^= 1;
-          }
+    // The MMA warp runs converged: every lane waits and computes the descriptors, elect.sync picks
+    // the issuing lane (a branch taken by one lane issues markedly slower).
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    const uint64_t a_desc0 = sdesc_sw128(smem_u32(sA)), b_desc0 = sdesc_sw128(smem_u32(sB));
+    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, args.status))) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem + acc * BN;
+      bool ok = true;
+      for (int kb = 0; kb < k_blocks; ++kb) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase, abort_flag, args.status))) {
+          ok = false;
+          break;
         }
-        if (!ok) break;
-        umma_commit(&tfull[acc]);
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1;
+        tc_fence_after();
+        // a descriptor's start field is the address / 16: offsets are added to it
+        const uint64_t ad = a_desc0 + (uint64_t)((stage * A_BYTES) >> 4);
+        const uint64_t bd = b_desc0 + (uint64_t)((stage * B_BYTES) >> 4);
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k) umma_bf16_elect(d_tmem, ad + 2 * k, bd + 2 * k, ID, (kb | k) != 0);
+        umma_commit_elect(&empty[stage]);
+        if (++stage == NST) {
+          stage = 0;
+          phase ^= 1;
+        }
       }
+      if (!ok) break;
+      umma_commit_elect(&tfull[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
     }
   } else if (BQ && warp >= 6) {
     // converters: one pass over the same (tile, k-block) sequence as the producer
