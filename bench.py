@@ -40,17 +40,17 @@ KINDS = ["gemm_qkv", "attention", "gemm_out", "gemm_ffn_up", "gemm_ffn_down", "n
 TRAFFIC = {
     # C2 block kernels, captured on the one-block slice video_audio_bf16_l1 (the same launch shapes)
     ("attention", "video_audio_bf16"): {"bytes": 409211648, "src_sha": "092678d55769e8ae"},
-    ("gemm_qkv", "video_audio_bf16"): {"bytes": 874441728, "src_sha": "26f29d6937350fb1"},
-    ("gemm_out", "video_audio_bf16"): {"bytes": 506077184, "src_sha": "26f29d6937350fb1"},
-    ("gemm_ffn_up", "video_audio_bf16"): {"bytes": 800780544, "src_sha": "26f29d6937350fb1"},
-    ("gemm_ffn_down", "video_audio_bf16"): {"bytes": 1229975296, "src_sha": "26f29d6937350fb1"},
+    ("gemm_qkv", "video_audio_bf16"): {"bytes": 870852352, "src_sha": "32f8a72205099025"},
+    ("gemm_out", "video_audio_bf16"): {"bytes": 506040320, "src_sha": "32f8a72205099025"},
+    ("gemm_ffn_up", "video_audio_bf16"): {"bytes": 897203456, "src_sha": "32f8a72205099025"},
+    ("gemm_ffn_down", "video_audio_bf16"): {"bytes": 1229849088, "src_sha": "32f8a72205099025"},
     ("norm_modulate", "video_audio_bf16"): {"bytes": 288434480, "src_sha": "ffcb4dee053268dc"},
     # C3 block kernels, captured on the one-block slice long_doc_bf16_l1
     ("attention", "long_doc_bf16"): {"bytes": 1369731840, "src_sha": "092678d55769e8ae"},
-    ("gemm_qkv", "long_doc_bf16"): {"bytes": 5533086720, "src_sha": "26f29d6937350fb1"},
-    ("gemm_out", "long_doc_bf16"): {"bytes": 3316553472, "src_sha": "26f29d6937350fb1"},
-    ("gemm_ffn_up", "long_doc_bf16"): {"bytes": 9850829056, "src_sha": "26f29d6937350fb1"},
-    ("gemm_ffn_down", "long_doc_bf16"): {"bytes": 6008213504, "src_sha": "26f29d6937350fb1"},
+    ("gemm_qkv", "long_doc_bf16"): {"bytes": 5589673472, "src_sha": "32f8a72205099025"},
+    ("gemm_out", "long_doc_bf16"): {"bytes": 3312640000, "src_sha": "32f8a72205099025"},
+    ("gemm_ffn_up", "long_doc_bf16"): {"bytes": 10139410432, "src_sha": "32f8a72205099025"},
+    ("gemm_ffn_down", "long_doc_bf16"): {"bytes": 6010215424, "src_sha": "32f8a72205099025"},
     ("norm_modulate", "long_doc_bf16"): {"bytes": 1004406016, "src_sha": "ffcb4dee053268dc"},
     # fp32 path, captured on the two-block slice music_fp32_l2 (the same launch shapes)
     ("gemm_qkv", "music_fp32"): {"bytes": 51839488, "src_sha": "8f478e2ee86c66d3"},
