@@ -239,14 +239,17 @@ def test_gemm_qkv_rope_head_dims(Dh, R):
 
 
 @pytest.mark.parametrize("elem", ELEMS)
-def test_gemm_gated_residual_matches_oracle(elem):
+@pytest.mark.parametrize("M", [1, 129, 555])
+def test_gemm_gated_residual_matches_oracle(M, elem):
+    """One row, one row past a tile, and several ragged tiles: the residual epilogue stages each
+    column group through shared memory and writes only the rows below M."""
     dit, gu = _dit(), _gu()
-    M, N, K = 555, 512, 1024
-    a, abits, b, bbits, bias = _ab(M, N, K, 60)
+    N, K = 512, 1024
+    a, abits, b, bbits, bias = _ab(M, N, K, 60 + M)
     (A, a), (B, b) = dev16(a, abits, elem), dev16(b, bbits, elem)
-    x = synth.normal(60, "x", (M, N), 1.0)
-    gate = synth.normal(60, "gate", (2, N), 0.3)
-    tags = (synth.uniform(60, "tags", M) < 0.5).astype(np.uint8)
+    x = synth.normal(60 + M, "x", (M, N), 1.0)
+    gate = synth.normal(60 + M, "gate", (2, N), 0.3)
+    tags = (synth.uniform(60 + M, "tags", M) < 0.5).astype(np.uint8)
     ref = x.astype(np.float64) + gate[tags].astype(np.float64) * oracle.linear(a, b, bias)
     xd = gu.dev_f32(x)
     dit.gemm_gated_residual(A, B, gu.dev_f32(bias), xd, gate=gu.dev_f32(gate), gate_stride=N,
