@@ -6,16 +6,20 @@
 // add; [H3] "The device-resident forward (W2b)": QkvSplit, RopeFromCache, SiluAndMul and the
 // indexed AdaLN gated add, here folded into the GEMM epilogue instead of separate passes.
 //
-// Design (one CTA per SM, persistent over output tiles):
-//   tile 128 x 256, K step 64, 4-stage TMA -> shared-memory ring (128-byte swizzle)
-//   warp 0   TMA producer (one elected lane)
-//   warp 1   TMEM allocator + UMMA issuer (one lane): tcgen05.mma M=128 N=256 K=16
+// Design for bf16 / f16 weights (gemm_pair_kernel: CTA pairs, one CTA per SM, persistent over
+// 256 x 256 output tiles):
+//   K step 64, a 6-stage TMA -> shared-memory ring (128-byte swizzle) per CTA holding its own 128
+//   rows of A and its half (128 rows) of the B tile
+//   warp 0   TMA producer (one lane per CTA)
+//   warp 1   TMEM allocator (both CTAs) + UMMA issuer (the first CTA, elect.sync): tcgen05.mma
+//            cta_group::2 M=256 N=256 K=16, each CTA's TMEM taking its own 128 rows
 //   warps 2-9 epilogue: each warp reads its 32 TMEM lanes (= 32 tile rows) with tcgen05.ld,
 //            one thread per output row; warps 2-5 take the tile's columns [0, 128) and warps 6-9
 //            [128, 256), so two warps share each lane quarter (a warp may only read the quarter
 //            warp % 4) and a tile's epilogue runs in half the time of one warp per quarter
 //   the 512 TMEM columns hold two 128x256 fp32 accumulators, so the epilogue of tile i overlaps
 //   the main loop of tile i+1.
+// gemm_kernel (one CTA of 128 x 256 tiles, 4 stages of 48 KB) runs the NVFP4 mode below.
 //
 // NVFP4 weights ([H3] "What this push adds": U8 codes two per byte, an E4M3 scale per 16 along K,
 // an F32 global scale).  Every E2M1 x E4M3 product is exact in f16, and E2M1 -> f16 is one
@@ -310,9 +314,22 @@ constexpr int RES_BATCH = 32;  // rows whose loads a warp has in flight at once 
 
 __device__ __forceinline__ void epi_bar(int grp) { asm volatile("bar.sync %0, 128;" ::"r"(1 + grp) : "memory"); }
 
+// Where an epilogue warp hands an accumulator buffer back: a local mbarrier, or (CTA pairs) the
+// pair's first CTA's barrier at a shared::cluster address.
+struct TRelease {
+  uint64_t* local;
+  uint32_t cluster;  // non-zero: arrive at this shared::cluster address instead
+  __device__ __forceinline__ void arrive() const {
+    if (cluster)
+      mbar_arrive_cluster(cluster);
+    else
+      mbar_arrive(local);
+  }
+};
+
 template <int RB, int NG>
 __device__ __forceinline__ void epi_resid(const GemmArgs& a, uint32_t t, int tile_row0, int quarter, int ew, int grp,
-                                          int n0, float* stage_all, uint64_t* tempty_bar) {
+                                          int n0, float* stage_all, TRelease rel) {
   constexpr int RC = 64 / NG;          // columns per pass
   constexpr int GC = BN / NG;          // columns of this group
   constexpr int LPR = RC / 2;          // lanes per row in phase B
@@ -342,7 +359,7 @@ __device__ __forceinline__ void epi_resid(const GemmArgs& a, uint32_t t, int til
       // handed back to the MMA warp
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar);
+      if (lane == 0) rel.arrive();
     }
     epi_bar(grp);
     // phase B: coalesced read-modify-write of 32 rows x RC columns per warp
@@ -642,7 +659,8 @@ __global__ void __launch_bounds__(BQ ? Q_THREADS : GEMM_THREADS, 1)
       const uint32_t t = tmem + acc * BN + (static_cast<uint32_t>(quarter * 32) << 16);
       const int n0 = tc.nb * BN;
       if (EPI == kEpiGatedResid) {
-        epi_resid<BQ ? 4 : RES_BATCH, NG>(args, t, tc.mb * BM, quarter, ew, grp, n0, res_stage, &tempty[acc]);
+        epi_resid<BQ ? 4 : RES_BATCH, NG>(args, t, tc.mb * BM, quarter, ew, grp, n0, res_stage,
+                                          TRelease{&tempty[acc], 0u});
       } else {
         if (EPI == kEpiStore) epi_store<NG>(args, t, row, n0, grp);
         if (EPI == kEpiQkvRope) epi_qkv<NG>(args, t, row, n0, grp);
@@ -664,24 +682,237 @@ __global__ void __launch_bounds__(BQ ? Q_THREADS : GEMM_THREADS, 1)
   }
 }
 
+
+// ---------------------------------------------------------------------------------------------
+// CTA pairs (clusters of 2) on tcgen05 cta_group::2: one MMA instruction covers a 256 x 256 x 16
+// block, each CTA holding 128 rows of A and 128 rows (one half) of B, and each CTA's TMEM the
+// accumulator of its own 128 rows.  A CTA's stage is then 32 KB instead of 48 for the same MMA work
+// per SM, so six stages fit where four did, and the loads run 1.5x further ahead of the MMAs: a
+// per-stage clock trace of the single-CTA kernel showed about 40 % of its K-blocks waiting beyond
+// the 512 cycles of MMA work for their stage.  Each CTA also fetches half the B bytes per tile.
+//   warp 0     TMA producer (both CTAs): this CTA's A tile and B half into its own stage; the bytes
+//              of both CTAs complete on the first CTA's barrier
+//   warp 1     TMEM allocator (both CTAs).  First CTA: MMA issuer, waits for the pair's stage,
+//              issues the pair MMAs, commits to both CTAs' barriers
+//   warps 2-9  epilogue (both CTAs), each on its own TMEM; the buffers are released to the first
+//              CTA's MMA warp (16 arrivals: 8 warps in each CTA)
+constexpr int P_STAGES = 6;
+constexpr int PB_BYTES = (BN / 2) * BK * 2;   // one CTA's half of the B tile
+constexpr int P_STAGE_BYTES = A_BYTES + PB_BYTES;
+constexpr int P_SMEM_BYTES = P_STAGES * P_STAGE_BYTES + 1024 + 256;
+constexpr int P_SMEM_BYTES_RESID = P_SMEM_BYTES + BM * 64 * 4;
+static_assert(P_SMEM_BYTES_RESID <= 227 * 1024, "pair stages exceed shared memory");
+
+template <int EPI>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const GemmArgs args) {
+  constexpr int NST = P_STAGES;
+  const uint32_t ID = args.f16 ? idesc_f16_f32(2 * BM, BN) : idesc_bf16_f32(2 * BM, BN);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + NST * A_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NST * P_STAGE_BYTES);  // [NST] first CTA: both stages landed
+  uint64_t* empty = full + NST;       // [NST] the pair MMAs are done with the stage (both CTAs)
+  uint64_t* tfull = empty + NST;      // [2] accumulator ready (both CTAs)
+  uint64_t* tempty = tfull + 2;       // [2] first CTA: both CTAs' epilogues are done with it
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* res_stage = reinterpret_cast<float*>(smem + NST * P_STAGE_BYTES + 256);  // residual epilogue only
+
+  if (args.status && (*reinterpret_cast<volatile int*>(args.status) & kDevLayout)) return;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int n_m = (args.M + BM - 1) / BM, n_n = args.N / BN, k_blocks = args.K / BK;
+  const int n_mp = (n_m + 1) / 2;  // row-block pairs; rank r takes row block 2 p + r
+  const int tiles = n_mp * n_n;
+  const int gn = args.group_n > 0 ? args.group_n : n_n;
+  const int t0 = (int)(blockIdx.x >> 1), tstep = (int)(gridDim.x >> 1);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&tfull[s], 1);
+      mbar_init(&tempty[s], 2 * EPI_WARPS);
+    }
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) tmem_alloc_pair(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers initialised and TMEM allocated before any remote arrival
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t b_policy = l2_policy_evict_last();
+      const uint32_t leader_full = mapa_shared(smem_u32(full), 0);
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int tile = t0; tile < tiles; tile += tstep) {
+        const TileCoord tc = tile_coord(tile, n_mp, n_n, gn);
+        const int mb = 2 * tc.mb + (int)rank;
+        for (int kb = 0; kb < k_blocks; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, args.status)) goto producer_done;
+          // both CTAs' bytes complete on the first CTA's barrier, which expects them all; its
+          // pending arrival keeps the phase open however the two CTAs' copies interleave
+          if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * P_STAGE_BYTES);
+          const uint32_t bar = leader_full + (uint32_t)stage * 8u;
+          tma_load_2d_pair(sA + stage * A_BYTES, &tmA, bar, kb * BK, mb * BM);
+          tma_load_2d_pair_hint(sB + stage * PB_BYTES, &tmB, bar, kb * BK, tc.nb * BN + (int)rank * (BN / 2),
+                                b_policy);
+          if (++stage == NST) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // Drain: every stage this CTA filled has been consumed, so no copy is in flight at exit.
+      for (int s = 0; s < NST; ++s) {
+        if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, args.status)) break;
+        if (++stage == NST) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    producer_done:;
+    }
+  } else if (warp == 1) {
+    if (rank == 0) {
+      // the first CTA: the pair's MMA warp, converged, elect.sync picks the issuing lane
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      const uint64_t a_desc0 = sdesc_sw128(smem_u32(sA)), b_desc0 = sdesc_sw128(smem_u32(sB));
+      for (int tile = t0; tile < tiles; tile += tstep) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, args.status))) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + acc * BN;
+        bool ok = true;
+        for (int kb = 0; kb < k_blocks; ++kb) {
+          if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase, abort_flag, args.status))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = a_desc0 + (uint64_t)((stage * A_BYTES) >> 4);
+          const uint64_t bd = b_desc0 + (uint64_t)((stage * PB_BYTES) >> 4);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) umma_pair_elect(d_tmem, ad + 2 * k, bd + 2 * k, ID, (kb | k) != 0);
+          umma_commit_pair_elect(&empty[stage]);  // the stage is free in both CTAs
+          if (++stage == NST) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        umma_commit_pair_elect(&tfull[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+    }
+  } else {
+    const int quarter = warp & 3;  // TMEM lanes [32 * quarter, +32) belong to this warp
+    constexpr int NG = EPI_WARPS / 4;
+    const int grp = (warp - 2) >> 2, ew = (warp - 2) & 3;
+    const uint32_t leader_tempty = mapa_shared(smem_u32(tempty), 0);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = t0; tile < tiles; tile += tstep) {
+      const TileCoord tc = tile_coord(tile, n_mp, n_n, gn);
+      const int mb = 2 * tc.mb + (int)rank;
+      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, args.status)) break;
+      tc_fence_after();
+      const int row = mb * BM + quarter * 32 + lane;
+      const uint32_t t = tmem + acc * BN + (static_cast<uint32_t>(quarter * 32) << 16);
+      const int n0 = tc.nb * BN;
+      const TRelease rel{&tempty[acc], leader_tempty + (uint32_t)acc * 8u};
+      if (EPI == kEpiGatedResid) {
+        epi_resid<RES_BATCH, NG>(args, t, mb * BM, quarter, ew, grp, n0, res_stage, rel);
+      } else {
+        if (EPI == kEpiStore) epi_store<NG>(args, t, row, n0, grp);
+        if (EPI == kEpiQkvRope) epi_qkv<NG>(args, t, row, n0, grp);
+        if (EPI == kEpiSwiglu) epi_swiglu<NG>(args, t, row, n0, grp);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) rel.arrive();
+      }
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no CTA frees TMEM or leaves while the pair's MMAs or arrivals may still reach it
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, 512);
+  }
+}
+
+// The bf16 / f16 modes run on CTA pairs, the NVFP4 mode on single CTAs.
 template <int EPI, bool BQ>
 cudaError_t launch_t(const void* A, const void* B, const GemmArgs& args, cudaStream_t stream) {
-  constexpr int smem = BQ ? (EPI == kEpiGatedResid ? Q_SMEM_BYTES_RESID : Q_SMEM_BYTES)
-                          : (EPI == kEpiGatedResid ? SMEM_BYTES_RESID : SMEM_BYTES);
-  static unsigned long long smem_set = 0;
-  cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(gemm_kernel<EPI, BQ>), smem, &smem_set);
-  if (e != cudaSuccess) return e;
-  // The NVFP4 mode's A is f16: the map only moves 2-byte elements, so the bf16 map serves it.
   CUtensorMap ta, tb;
+  // The NVFP4 mode's A is f16: the map only moves 2-byte elements, so the bf16 map serves it.
   if (!make_tmap_bf16_2d(&ta, A, args.K, args.M, (uint64_t)args.K * 2, BK, BM)) return cudaErrorInvalidValue;
-  if (BQ)
+  const int n_m = (args.M + BM - 1) / BM, n_n = args.N / BN;
+  if constexpr (BQ) {
+    constexpr int smem = EPI == kEpiGatedResid ? Q_SMEM_BYTES_RESID : Q_SMEM_BYTES;
+    static unsigned long long smem_set = 0;
+    cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(gemm_kernel<EPI, BQ>), smem, &smem_set);
+    if (e != cudaSuccess) return e;
     tb = ta;  // unused
-  else if (!make_tmap_bf16_2d(&tb, B, args.K, args.N, (uint64_t)args.K * 2, BK, BN))
-    return cudaErrorInvalidValue;
-  const int tiles = ((args.M + BM - 1) / BM) * (args.N / BN);
-  const int grid = tiles < num_sms() ? tiles : num_sms();
-  gemm_kernel<EPI, BQ><<<grid, BQ ? Q_THREADS : GEMM_THREADS, smem, stream>>>(ta, tb, args);
-  return cudaGetLastError();
+    const int tiles = n_m * n_n;
+    const int grid = tiles < num_sms() ? tiles : num_sms();
+    gemm_kernel<EPI, BQ><<<grid, Q_THREADS, smem, stream>>>(ta, tb, args);
+    return cudaGetLastError();
+  } else {
+    constexpr int smem = EPI == kEpiGatedResid ? P_SMEM_BYTES_RESID : P_SMEM_BYTES;
+    static unsigned long long smem_set = 0;
+    cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(gemm_pair_kernel<EPI>), smem, &smem_set);
+    if (e != cudaSuccess) return e;
+    // each CTA of a pair loads one half (128 rows) of the B tile
+    if (!make_tmap_bf16_2d(&tb, B, args.K, args.N, (uint64_t)args.K * 2, BK, BN / 2)) return cudaErrorInvalidValue;
+    const int pair_tiles = ((n_m + 1) / 2) * n_n;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(GEMM_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // The persistent grid holds only the pairs that can be resident at once: an SM whose partner
+    // SM is not available takes no pair, and a second wave would double the launch.
+    static int resident = 0;
+    if (resident == 0) {
+      cfg.gridDim = dim3(num_sms());
+      e = cudaOccupancyMaxActiveClusters(&resident, gemm_pair_kernel<EPI>, &cfg);
+      if (e != cudaSuccess) return e;
+      if (resident < 1) return cudaErrorLaunchOutOfResources;
+    }
+    const int pairs = pair_tiles < resident ? pair_tiles : resident;
+    cfg.gridDim = dim3(2 * pairs);
+    e = cudaLaunchKernelEx(&cfg, gemm_pair_kernel<EPI>, ta, tb, args);
+    return e != cudaSuccess ? e : cudaGetLastError();
+  }
 }
 
 // ffn_F > 0: the weight is an FFN up projection [2F, K] whose rows are interleaved in 128-feature
