@@ -899,8 +899,8 @@ cudaError_t launch_t(const void* A, const void* B, const GemmArgs& args, cudaStr
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    // The persistent grid holds only the pairs that can be resident at once: an SM whose partner
-    // SM is not available takes no pair, and a second wave would double the launch.
+    // The persistent grid holds only the pairs that can be resident at once (a second wave would
+    // double the launch): all 76 on a 152-SM part, fewer if another kernel holds SMs.
     static int resident = 0;
     if (resident == 0) {
       cfg.gridDim = dim3(num_sms());
