@@ -108,6 +108,27 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// The unwind path's waits, after a role has aborted: a copy or MMA already issued completes in
+// microseconds, so these ignore the abort flag and give up after kLandedLimitNs (a barrier whose
+// other arrivals will never come, e.g. from a role that aborted first, then costs that long).
+constexpr uint64_t kLandedLimitNs = 10000000ull;  // 10 ms
+
+__device__ __forceinline__ bool mbar_wait_landed(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait(a, parity)) return true;
+    if ((i & 255u) == 255u && globaltimer_ns() - t0 > kLandedLimitNs) return false;
+  }
+}
+
+// For copies that complete on another CTA's barrier: wait out the same bound.
+__device__ __forceinline__ void landed_grace() {
+  const uint64_t t0 = globaltimer_ns();
+  while (globaltimer_ns() - t0 < kLandedLimitNs) {
+  }
+}
+
 // ------------------------------------------------------------------------------------------
 // Programmatic dependent launch.  A kernel launched with launch_pdl may be scheduled while the
 // previous kernel of its stream is still running; it calls pdl_wait() before it touches memory
@@ -354,14 +375,15 @@ __device__ __forceinline__ void umma_pair_elect(uint32_t d_tmem, uint64_t a_desc
       : "memory");
 }
 
-// Arrive once on the mbarrier at bar's offset in both CTAs of the pair when the pair MMAs issued so
-// far (by the elected lane of this warp) have completed.
-__device__ __forceinline__ void umma_commit_pair_elect(uint64_t* bar) {
+// Arrive once on the mbarrier at bar's offset in each CTA of the pair that `cta_mask` names (bit r:
+// rank r; both by default) when the pair MMAs issued so far (by the elected lane of this warp) have
+// completed.
+__device__ __forceinline__ void umma_commit_pair_elect(uint64_t* bar, uint16_t cta_mask = 3) {
   asm volatile(
       "{\n\t.reg .pred e;\n\t"
       "elect.sync _|e, 0xffffffff;\n\t"
       "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}"
-      ::"r"(smem_u32(bar)), "h"((uint16_t)3)
+      ::"r"(smem_u32(bar)), "h"(cta_mask)
       : "memory");
 }
 

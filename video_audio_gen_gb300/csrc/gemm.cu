@@ -499,7 +499,8 @@ __global__ void __launch_bounds__(BQ ? Q_THREADS : GEMM_THREADS, 1)
   uint64_t* rawempty = rawfull + (BQ ? Q_RAW_SLOTS : 0);  // NVFP4: the converters are done with a slot
   uint64_t* tfull = rawempty + (BQ ? Q_RAW_SLOTS : 0);
   uint64_t* tempty = tfull + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* mma_done = tempty + 2;  // unwind: the MMAs issued before an abort have completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* res_stage = reinterpret_cast<float*>(smem + RING_BYTES + 256);  // residual epilogue only
 
@@ -524,6 +525,7 @@ __global__ void __launch_bounds__(BQ ? Q_THREADS : GEMM_THREADS, 1)
       mbar_init(&tfull[s], 1);
       mbar_init(&tempty[s], BQ ? Q_EPI_WARPS : EPI_WARPS);
     }
+    mbar_init(mma_done, 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -540,7 +542,7 @@ __global__ void __launch_bounds__(BQ ? Q_THREADS : GEMM_THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       const uint64_t b_policy = l2_policy_evict_last();
-      int stage = 0, rslot = 0;
+      int stage = 0, rslot = 0, issued = 0, raw_issued = 0;
       uint32_t phase = 0, rphase = 0;
       for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
         TileCoord tc = tile_coord(tile, n_m, n_n, gn);
@@ -553,6 +555,7 @@ __global__ void __launch_bounds__(BQ ? Q_THREADS : GEMM_THREADS, 1)
             mbar_arrive_expect_tx(&rawfull[rslot], Q_RAW_BYTES);
             bulk_load(sQ + rslot * Q_RAW_BYTES, args.b_packed + ((size_t)tc.nb * k_blocks + kb) * Q_RAW_BYTES,
                       Q_RAW_BYTES, &rawfull[rslot]);
+            ++raw_issued;
             if (++rslot == Q_RAW_SLOTS) {
               rslot = 0;
               rphase ^= 1;
@@ -565,6 +568,7 @@ __global__ void __launch_bounds__(BQ ? Q_THREADS : GEMM_THREADS, 1)
             // a raster group's weight panels are read by every M-block of the group: keep them in L2
             tma_load_2d_hint(sB + stage * B_BYTES, &tmB, &full[stage], kb * BK, tc.nb * BN, b_policy);
           }
+          ++issued;
           if (++stage == NST) {
             stage = 0;
             phase ^= 1;
@@ -574,13 +578,23 @@ __global__ void __launch_bounds__(BQ ? Q_THREADS : GEMM_THREADS, 1)
       // Drain: wait until the MMAs consumed every stage we filled, so no TMA write into this
       // CTA's shared memory is still in flight when the CTA exits.
       for (int s = 0; s < NST; ++s) {
-        if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, args.status)) break;
+        if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, args.status)) goto producer_done;
         if (++stage == NST) {
           stage = 0;
           phase ^= 1;
         }
       }
-    producer_done:;
+      goto producer_exit;
+    producer_done:
+      // Unwind: the copies of the last fills of each stage (and packed slot) may still be in
+      // flight; each is the latest phase of its barrier, so its landing completes that phase.
+      // (In the NVFP4 mode full[] also waits for the converters and may run out its bound.)
+      for (int j = issued - NST < 0 ? 0 : issued - NST; j < issued; ++j)
+        mbar_wait_landed(&full[j % NST], (uint32_t)(j / NST) & 1u);
+      if (BQ)
+        for (int j = raw_issued - Q_RAW_SLOTS < 0 ? 0 : raw_issued - Q_RAW_SLOTS; j < raw_issued; ++j)
+          mbar_wait_landed(&rawfull[j % Q_RAW_SLOTS], (uint32_t)(j / Q_RAW_SLOTS) & 1u);
+    producer_exit:;
     }
   } else if (warp == 1) {
     // The MMA warp runs converged: every lane waits and computes the descriptors, elect.sync picks
@@ -590,8 +604,12 @@ __global__ void __launch_bounds__(BQ ? Q_THREADS : GEMM_THREADS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     const uint64_t a_desc0 = sdesc_sw128(smem_u32(sA)), b_desc0 = sdesc_sw128(smem_u32(sB));
+    bool unwound = false;
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, args.status))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, args.status))) {
+        unwound = true;
+        break;
+      }
       tc_fence_after();
       const uint32_t d_tmem = tmem + acc * BN;
       bool ok = true;
@@ -612,10 +630,19 @@ __global__ void __launch_bounds__(BQ ? Q_THREADS : GEMM_THREADS, 1)
           phase ^= 1;
         }
       }
-      if (!ok) break;
+      if (!ok) {
+        unwound = true;
+        break;
+      }
       umma_commit_elect(&tfull[acc]);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
+    }
+    if (unwound) {
+      // the MMAs already issued still write TMEM and read shared memory: let them finish before
+      // the CTA frees either
+      umma_commit_elect(mma_done);
+      mbar_wait_landed(mma_done, 0);
     }
   } else if (BQ && warp >= 6) {
     // converters: one pass over the same (tile, k-block) sequence as the producer
@@ -717,7 +744,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   uint64_t* empty = full + NST;       // [NST] the pair MMAs are done with the stage (both CTAs)
   uint64_t* tfull = empty + NST;      // [2] accumulator ready (both CTAs)
   uint64_t* tempty = tfull + 2;       // [2] first CTA: both CTAs' epilogues are done with it
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* mma_done = tempty + 2;    // first CTA, unwind: the pair MMAs issued before an abort are done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* res_stage = reinterpret_cast<float*>(smem + NST * P_STAGE_BYTES + 256);  // residual epilogue only
 
@@ -740,6 +768,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       mbar_init(&tfull[s], 1);
       mbar_init(&tempty[s], 2 * EPI_WARPS);
     }
+    mbar_init(mma_done, 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -758,7 +787,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     if (lane == 0) {
       const uint64_t b_policy = l2_policy_evict_last();
       const uint32_t leader_full = mapa_shared(smem_u32(full), 0);
-      int stage = 0;
+      int stage = 0, issued = 0;
       uint32_t phase = 0;
       for (int tile = t0; tile < tiles; tile += tstep) {
         const TileCoord tc = tile_coord(tile, n_mp, n_n, gn);
@@ -772,6 +801,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           tma_load_2d_pair(sA + stage * A_BYTES, &tmA, bar, kb * BK, mb * BM);
           tma_load_2d_pair_hint(sB + stage * PB_BYTES, &tmB, bar, kb * BK, tc.nb * BN + (int)rank * (BN / 2),
                                 b_policy);
+          ++issued;
           if (++stage == NST) {
             stage = 0;
             phase ^= 1;
@@ -780,13 +810,24 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       }
       // Drain: every stage this CTA filled has been consumed, so no copy is in flight at exit.
       for (int s = 0; s < NST; ++s) {
-        if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, args.status)) break;
+        if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, args.status)) goto producer_done;
         if (++stage == NST) {
           stage = 0;
           phase ^= 1;
         }
       }
-    producer_done:;
+      goto producer_exit;
+    producer_done:
+      // Unwind: the last fill of each stage may still be in flight.  Its bytes complete on the
+      // first CTA's barrier, where the first CTA can wait for them; the second CTA cannot, and
+      // waits out the same bound instead.
+      if (rank == 0) {
+        for (int j = issued - NST < 0 ? 0 : issued - NST; j < issued; ++j)
+          mbar_wait_landed(&full[j % NST], (uint32_t)(j / NST) & 1u);
+      } else if (issued > 0) {
+        landed_grace();
+      }
+    producer_exit:;
     }
   } else if (warp == 1) {
     if (rank == 0) {
@@ -796,8 +837,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       const uint64_t a_desc0 = sdesc_sw128(smem_u32(sA)), b_desc0 = sdesc_sw128(smem_u32(sB));
+      bool unwound = false;
       for (int tile = t0; tile < tiles; tile += tstep) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, args.status))) break;
+        if (!__all_sync(0xffffffffu, mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, args.status))) {
+          unwound = true;
+          break;
+        }
         tc_fence_after();
         const uint32_t d_tmem = tmem + acc * BN;
         bool ok = true;
@@ -817,10 +862,19 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             phase ^= 1;
           }
         }
-        if (!ok) break;
+        if (!ok) {
+          unwound = true;
+          break;
+        }
         umma_commit_pair_elect(&tfull[acc]);
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1;
+      }
+      if (unwound) {
+        // the pair MMAs already issued still write both CTAs' TMEM: let them finish before either
+        // CTA frees it (the final cluster barrier holds the second CTA until this returns)
+        umma_commit_pair_elect(mma_done, 1);
+        mbar_wait_landed(mma_done, 0);
       }
     }
   } else {
