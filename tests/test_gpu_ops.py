@@ -153,8 +153,13 @@ def _ab(M, N, K, seed, std_b=0.05):
 
 
 @pytest.mark.parametrize("elem", ELEMS)
-@pytest.mark.parametrize("M,N,K", [(1, 256, 64), (333, 512, 512), (128, 768, 256), (1000, 1024, 1536)])
+@pytest.mark.parametrize("M,N,K", [(1, 256, 64), (333, 512, 512), (128, 768, 256), (1000, 1024, 1536),
+                                   (257, 256, 4096), (4224, 2560, 128)])
 def test_gemm_store_matches_oracle(M, N, K, elem):
+    """Row tiles run in pairs of 128-row blocks: one row (the second block of the pair past M), an
+    odd number of row blocks (the last pair's second block wholly past M), one K-block and one
+    N-tile, a K of 64 blocks (the stage ring wraps ten times), and 170 pair tiles (every pair of
+    the persistent grid takes two or three, so both accumulator buffers and their phases turn)."""
     dit, gu = _dit(), _gu()
     a, abits, b, bbits, bias = _ab(M, N, K, 40 + M)
     (A, a), (B, b) = dev16(a, abits, elem), dev16(b, bbits, elem)
