@@ -563,9 +563,6 @@ __device__ __forceinline__ uint16_t to16(bool f16, float v) {
   return f16 ? __half_as_ushort(__float2half_rn(v)) : __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 
-// Four values v * 2^e as f16 (hi, lo) pairs for the 3xF16 GEMM: hi = f16(v 2^e), lo = f16(v 2^e - hi);
-// stored at hi_dst / lo_dst (4 consecutive 16-bit elements each, 8-byte aligned).  Returns true when a
-// scaled value is beyond f16's finite range.
 // Token tile of the 3xF16 GEMM (its MMA's N): M split into the fewest tiles of at most 192 tokens
 // (so that an epilogue warp's running sums fit its registers), rounded up to 16, at least 32.
 __host__ __device__ __forceinline__ int x3_token_tile(int M) {
@@ -586,6 +583,9 @@ __device__ __forceinline__ size_t x3_xs_index(int r, int k, int nt, int mtiles) 
          (kk & 7);
 }
 
+// Four values v * 2^e as f16 (hi, lo) pairs for the 3xF16 GEMM: hi = f16(v 2^e), lo = f16(v 2^e - hi);
+// stored at hi_dst / lo_dst (4 consecutive 16-bit elements each, 8-byte aligned).  Returns true when a
+// scaled value is beyond f16's finite range.
 __device__ __forceinline__ bool store_f16_split4(const float (&v)[4], int e, uint16_t* hi_dst, uint16_t* lo_dst) {
   uint16_t h[4], l[4];
   bool over = false;
