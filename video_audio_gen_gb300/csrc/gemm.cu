@@ -42,15 +42,12 @@ namespace dit {
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int BM = 128, BN = 256, BK = 64;
 constexpr int A_BYTES = BM * BK * 2;   // 16 KB
 constexpr int B_BYTES = BN * BK * 2;   // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int EPI_WARPS = 8;  // two per TMEM lane quarter, each on half of the tile's columns
 constexpr int GEMM_THREADS = 64 + 32 * EPI_WARPS;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
-constexpr int SMEM_BYTES_RESID = SMEM_BYTES + BM * 64 * 4;  // + the residual epilogue's staging tile
-constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
 // NVFP4 mode
 constexpr int Q_STAGES = 4, Q_STAGES_RESID = 3;  // A + dequantised B stages
 constexpr int Q_RAW_SLOTS = 2;                   // packed weight tiles in flight
@@ -482,22 +479,22 @@ __device__ __forceinline__ void nvfp4_expand_row(uint32_t raw, uint32_t dst, int
   }
 }
 
-template <int EPI, bool BQ>
-__global__ void __launch_bounds__(BQ ? Q_THREADS : GEMM_THREADS, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
-  constexpr int NST = BQ ? (EPI == kEpiGatedResid ? Q_STAGES_RESID : Q_STAGES) : STAGES;
-  constexpr int RING_BYTES = NST * STAGE_BYTES + (BQ ? Q_RAW_SLOTS * Q_RAW_BYTES : 0);
-  const uint32_t ID = (BQ || args.f16) ? IDESC_F16 : IDESC;
+template <int EPI>
+__global__ void __launch_bounds__(Q_THREADS, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const GemmArgs args) {
+  constexpr int NST = EPI == kEpiGatedResid ? Q_STAGES_RESID : Q_STAGES;
+  constexpr int RING_BYTES = NST * STAGE_BYTES + Q_RAW_SLOTS * Q_RAW_BYTES;
+  const uint32_t ID = IDESC_F16;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + NST * A_BYTES;
-  uint8_t* sQ = sB + NST * B_BYTES;  // NVFP4 mode: the packed weight tiles (Q_RAW_SLOTS)
+  uint8_t* sQ = sB + NST * B_BYTES;  // the packed weight tiles (Q_RAW_SLOTS)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + RING_BYTES);
   uint64_t* empty = full + NST;
-  uint64_t* rawfull = empty + NST;                     // NVFP4: a packed tile has landed
-  uint64_t* rawempty = rawfull + (BQ ? Q_RAW_SLOTS : 0);  // NVFP4: the converters are done with a slot
-  uint64_t* tfull = rawempty + (BQ ? Q_RAW_SLOTS : 0);
+  uint64_t* rawfull = empty + NST;             // a packed tile has landed
+  uint64_t* rawempty = rawfull + Q_RAW_SLOTS;  // the converters are done with a slot
+  uint64_t* tfull = rawempty + Q_RAW_SLOTS;
   uint64_t* tempty = tfull + 2;
   uint64_t* mma_done = tempty + 2;  // unwind: the MMAs issued before an abort have completed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
@@ -513,26 +510,22 @@ __global__ void __launch_bounds__(BQ ? Q_THREADS : GEMM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NST; ++s) {
-      mbar_init(&full[s], BQ ? 1 + Q_CONV_WARPS : 1);  // NVFP4: + one arrival per converter warp
+      mbar_init(&full[s], 1 + Q_CONV_WARPS);  // the producer, and one arrival per converter warp
       mbar_init(&empty[s], 1);
     }
-    if (BQ)
-      for (int q = 0; q < Q_RAW_SLOTS; ++q) {
-        mbar_init(&rawfull[q], 1);
-        mbar_init(&rawempty[q], Q_CONV_WARPS);
-      }
+    for (int q = 0; q < Q_RAW_SLOTS; ++q) {
+      mbar_init(&rawfull[q], 1);
+      mbar_init(&rawempty[q], Q_CONV_WARPS);
+    }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&tfull[s], 1);
-      mbar_init(&tempty[s], BQ ? Q_EPI_WARPS : EPI_WARPS);
+      mbar_init(&tempty[s], Q_EPI_WARPS);
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmA);
-    if (!BQ) tma_prefetch_desc(&tmB);
-  }
+  if (warp == 0 && lane == 0) tma_prefetch_desc(&tmA);
   if (warp == 1) tmem_alloc(tmem_slot, 512);
   tc_fence_before();
   __syncthreads();
@@ -541,33 +534,25 @@ __global__ void __launch_bounds__(BQ ? Q_THREADS : GEMM_THREADS, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      const uint64_t b_policy = l2_policy_evict_last();
       int stage = 0, rslot = 0, issued = 0, raw_issued = 0;
       uint32_t phase = 0, rphase = 0;
       for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
         TileCoord tc = tile_coord(tile, n_m, n_n, gn);
         for (int kb = 0; kb < k_blocks; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, args.status)) goto producer_done;
-          if (BQ) {
-            // the packed slot is free once the converters expanded its previous tile; the stage's B
-            // tile is free because empty[stage] fired before this copy is issued
-            if (!mbar_wait(&rawempty[rslot], rphase ^ 1, abort_flag, args.status)) goto producer_done;
-            mbar_arrive_expect_tx(&rawfull[rslot], Q_RAW_BYTES);
-            bulk_load(sQ + rslot * Q_RAW_BYTES, args.b_packed + ((size_t)tc.nb * k_blocks + kb) * Q_RAW_BYTES,
-                      Q_RAW_BYTES, &rawfull[rslot]);
-            ++raw_issued;
-            if (++rslot == Q_RAW_SLOTS) {
-              rslot = 0;
-              rphase ^= 1;
-            }
-            mbar_arrive_expect_tx(&full[stage], A_BYTES);
-            tma_load_2d(sA + stage * A_BYTES, &tmA, &full[stage], kb * BK, tc.mb * BM);
-          } else {
-            mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-            tma_load_2d(sA + stage * A_BYTES, &tmA, &full[stage], kb * BK, tc.mb * BM);
-            // a raster group's weight panels are read by every M-block of the group: keep them in L2
-            tma_load_2d_hint(sB + stage * B_BYTES, &tmB, &full[stage], kb * BK, tc.nb * BN, b_policy);
+          // the packed slot is free once the converters expanded its previous tile; the stage's B
+          // tile is free because empty[stage] fired before this copy is issued
+          if (!mbar_wait(&rawempty[rslot], rphase ^ 1, abort_flag, args.status)) goto producer_done;
+          mbar_arrive_expect_tx(&rawfull[rslot], Q_RAW_BYTES);
+          bulk_load(sQ + rslot * Q_RAW_BYTES, args.b_packed + ((size_t)tc.nb * k_blocks + kb) * Q_RAW_BYTES,
+                    Q_RAW_BYTES, &rawfull[rslot]);
+          ++raw_issued;
+          if (++rslot == Q_RAW_SLOTS) {
+            rslot = 0;
+            rphase ^= 1;
           }
+          mbar_arrive_expect_tx(&full[stage], A_BYTES);
+          tma_load_2d(sA + stage * A_BYTES, &tmA, &full[stage], kb * BK, tc.mb * BM);
           ++issued;
           if (++stage == NST) {
             stage = 0;
@@ -588,12 +573,11 @@ __global__ void __launch_bounds__(BQ ? Q_THREADS : GEMM_THREADS, 1)
     producer_done:
       // Unwind: the copies of the last fills of each stage (and packed slot) may still be in
       // flight; each is the latest phase of its barrier, so its landing completes that phase.
-      // (In the NVFP4 mode full[] also waits for the converters and may run out its bound.)
+      // (full[] also waits for the converters, and may run out its bound when they aborted.)
       for (int j = issued - NST < 0 ? 0 : issued - NST; j < issued; ++j)
         mbar_wait_landed(&full[j % NST], (uint32_t)(j / NST) & 1u);
-      if (BQ)
-        for (int j = raw_issued - Q_RAW_SLOTS < 0 ? 0 : raw_issued - Q_RAW_SLOTS; j < raw_issued; ++j)
-          mbar_wait_landed(&rawfull[j % Q_RAW_SLOTS], (uint32_t)(j / Q_RAW_SLOTS) & 1u);
+      for (int j = raw_issued - Q_RAW_SLOTS < 0 ? 0 : raw_issued - Q_RAW_SLOTS; j < raw_issued; ++j)
+        mbar_wait_landed(&rawfull[j % Q_RAW_SLOTS], (uint32_t)(j / Q_RAW_SLOTS) & 1u);
     producer_exit:;
     }
   } else if (warp == 1) {
@@ -644,7 +628,7 @@ __global__ void __launch_bounds__(BQ ? Q_THREADS : GEMM_THREADS, 1)
       umma_commit_elect(mma_done);
       mbar_wait_landed(mma_done, 0);
     }
-  } else if (BQ && warp >= 6) {
+  } else if (warp >= 6) {
     // converters: one pass over the same (tile, k-block) sequence as the producer
     // The stage's B tile is free: the packed tile of this fill was copied only after the MMA's
     // commit for the previous fill of the stage (the producer waits on empty[stage] first).
@@ -674,7 +658,7 @@ __global__ void __launch_bounds__(BQ ? Q_THREADS : GEMM_THREADS, 1)
   convert_done:;
   } else {
     const int quarter = warp & 3;  // TMEM lanes [32 * quarter, +32) belong to this warp
-    constexpr int NG = (BQ ? Q_EPI_WARPS : EPI_WARPS) / 4;
+    constexpr int NG = Q_EPI_WARPS / 4;
     const int grp = (warp - 2) >> 2, ew = (warp - 2) & 3;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -686,8 +670,7 @@ __global__ void __launch_bounds__(BQ ? Q_THREADS : GEMM_THREADS, 1)
       const uint32_t t = tmem + acc * BN + (static_cast<uint32_t>(quarter * 32) << 16);
       const int n0 = tc.nb * BN;
       if (EPI == kEpiGatedResid) {
-        epi_resid<BQ ? 4 : RES_BATCH, NG>(args, t, tc.mb * BM, quarter, ew, grp, n0, res_stage,
-                                          TRelease{&tempty[acc], 0u});
+        epi_resid<4, NG>(args, t, tc.mb * BM, quarter, ew, grp, n0, res_stage, TRelease{&tempty[acc], 0u});
       } else {
         if (EPI == kEpiStore) epi_store<NG>(args, t, row, n0, grp);
         if (EPI == kEpiQkvRope) epi_qkv<NG>(args, t, row, n0, grp);
@@ -927,12 +910,11 @@ cudaError_t launch_t(const void* A, const void* B, const GemmArgs& args, cudaStr
   if constexpr (BQ) {
     constexpr int smem = EPI == kEpiGatedResid ? Q_SMEM_BYTES_RESID : Q_SMEM_BYTES;
     static unsigned long long smem_set = 0;
-    cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(gemm_kernel<EPI, BQ>), smem, &smem_set);
+    cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(gemm_kernel<EPI>), smem, &smem_set);
     if (e != cudaSuccess) return e;
-    tb = ta;  // unused
     const int tiles = n_m * n_n;
     const int grid = tiles < num_sms() ? tiles : num_sms();
-    gemm_kernel<EPI, BQ><<<grid, Q_THREADS, smem, stream>>>(ta, tb, args);
+    gemm_kernel<EPI><<<grid, Q_THREADS, smem, stream>>>(ta, args);
     return cudaGetLastError();
   } else {
     constexpr int smem = EPI == kEpiGatedResid ? P_SMEM_BYTES_RESID : P_SMEM_BYTES;
