@@ -40,17 +40,17 @@ KINDS = ["gemm_qkv", "attention", "gemm_out", "gemm_ffn_up", "gemm_ffn_down", "n
 TRAFFIC = {
     # C2 block kernels, captured on the one-block slice video_audio_bf16_l1 (the same launch shapes)
     ("attention", "video_audio_bf16"): {"bytes": 409211648, "src_sha": "092678d55769e8ae"},
-    ("gemm_qkv", "video_audio_bf16"): {"bytes": 917596160, "src_sha": "a917aa754a6af980"},
-    ("gemm_out", "video_audio_bf16"): {"bytes": 508300032, "src_sha": "a917aa754a6af980"},
-    ("gemm_ffn_up", "video_audio_bf16"): {"bytes": 964452864, "src_sha": "a917aa754a6af980"},
-    ("gemm_ffn_down", "video_audio_bf16"): {"bytes": 1242742016, "src_sha": "a917aa754a6af980"},
+    ("gemm_qkv", "video_audio_bf16"): {"bytes": 884737024, "src_sha": "0bff13141c90176c"},
+    ("gemm_out", "video_audio_bf16"): {"bytes": 508703488, "src_sha": "0bff13141c90176c"},
+    ("gemm_ffn_up", "video_audio_bf16"): {"bytes": 939630848, "src_sha": "0bff13141c90176c"},
+    ("gemm_ffn_down", "video_audio_bf16"): {"bytes": 1246642688, "src_sha": "0bff13141c90176c"},
     ("norm_modulate", "video_audio_bf16"): {"bytes": 288434480, "src_sha": "ffcb4dee053268dc"},
     # C3 block kernels, captured on the one-block slice long_doc_bf16_l1
     ("attention", "long_doc_bf16"): {"bytes": 1369731840, "src_sha": "092678d55769e8ae"},
-    ("gemm_qkv", "long_doc_bf16"): {"bytes": 6903734272, "src_sha": "a917aa754a6af980"},
-    ("gemm_out", "long_doc_bf16"): {"bytes": 3229878528, "src_sha": "a917aa754a6af980"},
-    ("gemm_ffn_up", "long_doc_bf16"): {"bytes": 11488970496, "src_sha": "a917aa754a6af980"},
-    ("gemm_ffn_down", "long_doc_bf16"): {"bytes": 9347943680, "src_sha": "a917aa754a6af980"},
+    ("gemm_qkv", "long_doc_bf16"): {"bytes": 6321965312, "src_sha": "0bff13141c90176c"},
+    ("gemm_out", "long_doc_bf16"): {"bytes": 3178683392, "src_sha": "0bff13141c90176c"},
+    ("gemm_ffn_up", "long_doc_bf16"): {"bytes": 10245911040, "src_sha": "0bff13141c90176c"},
+    ("gemm_ffn_down", "long_doc_bf16"): {"bytes": 8454970624, "src_sha": "0bff13141c90176c"},
     ("norm_modulate", "long_doc_bf16"): {"bytes": 1004406016, "src_sha": "ffcb4dee053268dc"},
     # fp32 path, captured on the two-block slice music_fp32_l2 (the same launch shapes)
     ("gemm_qkv", "music_fp32"): {"bytes": 51839488, "src_sha": "8f478e2ee86c66d3"},
