@@ -701,7 +701,9 @@ __global__ void __launch_bounds__(Q_THREADS, 1)
 // per-stage clock trace of the single-CTA kernel showed about 40 % of its K-blocks waiting beyond
 // the 512 cycles of MMA work for their stage.  Each CTA also fetches half the B bytes per tile.
 //   warp 0     TMA producer (both CTAs): this CTA's A tile and B half into its own stage; the bytes
-//              of both CTAs complete on the first CTA's barrier
+//              of both CTAs complete on the first CTA's barrier (a forward of "stage landed" from
+//              the second CTA by a remote mbarrier arrive, in series with every K-block, measured
+//              2.5x slower)
 //   warp 1     TMEM allocator (both CTAs).  First CTA: MMA issuer, waits for the pair's stage,
 //              issues the pair MMAs, commits to both CTAs' barriers
 //   warps 2-9  epilogue (both CTAs), each on its own TMEM; the buffers are released to the first
